@@ -1,0 +1,202 @@
+"""fp64 CPU oracle for paged KV attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never imports, links
+or calls it, and it never imports the CUDA library: the two share no code.
+The only thing both sides consume is the seeded input generator
+(``paged_kv_attention_14_gb300.workloads``), which holds none of the
+method's arithmetic.
+
+The arithmetic lives in ``pa_oracle.c`` (plain loops, fp64); this module
+compiles it with gcc on first use and wraps it for numpy arrays.  What each
+function computes and which passage of the source pages it follows is stated
+in ``pa_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB = os.path.join(_HERE, "libpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pa_oracle.c`` into ``libpa_oracle.so`` (gcc, -O2, no fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fno-fast-math", "-ffp-contract=off", "-shared", "-fPIC",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        F = ctypes.c_float
+        lib.pa_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.pa_oracle_e4m3_decode.restype = ctypes.c_double
+        lib.pa_oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.pa_oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.pa_oracle_cache_write.argtypes = [I, I, I, I, P, P, P, I, F, F, P, P]
+        lib.pa_oracle_cache_write.restype = None
+        lib.pa_oracle_attend_range.argtypes = [I, I, I, I, P, P, P, P, I, I, I, F, F, F, P, P]
+        lib.pa_oracle_attend_range.restype = None
+        lib.pa_oracle_decode.argtypes = [I, I, I, I, I, P, P, P, P, I, P, I, F, F, F, P, I, P, P]
+        lib.pa_oracle_decode.restype = None
+        lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, P, I, P, P]
+        lib.pa_oracle_prefill.restype = None
+        lib.pa_oracle_merge.argtypes = [P, P, I, I, P, P]
+        lib.pa_oracle_merge.restype = None
+        _lib = lib
+        return lib
+
+
+def _np(a, dtype):
+    """Contiguous numpy array of ``dtype`` from a numpy array or CPU torch tensor.
+    16-bit float tensors (bf16) are passed as their bit patterns."""
+    if hasattr(a, "detach"):
+        import torch
+        t = a.detach().cpu().contiguous()
+        if t.dtype in (torch.bfloat16, torch.float16):
+            t = t.view(torch.int16)
+        elif t.dtype == torch.float8_e4m3fn:
+            t = t.view(torch.uint8)
+        a = t.numpy()
+    a = np.ascontiguousarray(a)
+    want = np.dtype(dtype)
+    if a.dtype != want:
+        if a.dtype.kind in "iu" and want.kind in "iu" and a.dtype.itemsize == want.itemsize:
+            a = a.view(want)
+        else:
+            a = a.astype(want)
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _cache_np(cache, kv_dtype):
+    return _np(cache, np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+
+
+def e4m3_decode(byte: int) -> float:
+    return _load().pa_oracle_e4m3_decode(int(byte) & 0xFF)
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().pa_oracle_e4m3_encode(float(x)))
+
+
+def cache_write(kv_dtype, block_size, num_kv_heads, head_dim, k, v, slot_mapping,
+                k_cache, v_cache, k_scale=1.0, v_scale=1.0):
+    """Scatter new K/V rows into copies of the caches; returns (k_cache, v_cache)."""
+    lib = _load()
+    k = _np(k, np.uint16)
+    v = _np(v, np.uint16)
+    sm = _np(slot_mapping, np.int64)
+    kc = _cache_np(k_cache, kv_dtype).copy()
+    vc = _cache_np(v_cache, kv_dtype).copy()
+    lib.pa_oracle_cache_write(kv_dtype, block_size, num_kv_heads, head_dim, _ptr(k), _ptr(v),
+                              _ptr(sm), int(sm.shape[0]), float(k_scale), float(v_scale),
+                              _ptr(kc), _ptr(vc))
+    return kc, vc
+
+
+def attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
+                 table_row, kv_head, t_begin, t_end, scale, k_scale=1.0, v_scale=1.0):
+    """Attention of one bf16 query over logical keys [t_begin, t_end); returns (out, lse)."""
+    lib = _load()
+    qv = _np(q_vec, np.uint16)
+    kc = _cache_np(k_cache, kv_dtype)
+    vc = _cache_np(v_cache, kv_dtype)
+    tr = _np(table_row, np.int32)
+    out = np.zeros(head_dim, np.float64)
+    lse = np.zeros(1, np.float64)
+    lib.pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, _ptr(qv), _ptr(kc),
+                               _ptr(vc), _ptr(tr), int(kv_head), int(t_begin), int(t_end),
+                               float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse))
+    return out, float(lse[0])
+
+
+def decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, k_cache, v_cache,
+           block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None):
+    """Decode attention.  Returns (out [n, D], lse [n]) in fp64 for the (s, h)
+    pairs given (default: all, row-major over (s, h))."""
+    lib = _load()
+    qn = _np(q, np.uint16)
+    kc = _cache_np(k_cache, kv_dtype)
+    vc = _cache_np(v_cache, kv_dtype)
+    bt = _np(block_tables, np.int32)
+    cl = _np(context_lens, np.int32)
+    S = int(cl.shape[0])
+    if pairs is None:
+        n, pp = S * num_q_heads, None
+    else:
+        pp = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+        n = int(pp.shape[0])
+    out = np.zeros((n, head_dim), np.float64)
+    lse = np.zeros(n, np.float64)
+    lib.pa_oracle_decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
+                         _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
+                         float(scale), float(k_scale), float(v_scale),
+                         None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_start_loc,
+            k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0,
+            pairs=None):
+    """Causal chunked-prefill attention.  Returns (out [n, D], lse [n]) in fp64
+    for the (token row, head) pairs given (default: all rows x heads)."""
+    lib = _load()
+    qn = _np(q, np.uint16)
+    qsl = _np(query_start_loc, np.int32)
+    kc = _cache_np(k_cache, kv_dtype)
+    vc = _cache_np(v_cache, kv_dtype)
+    bt = _np(block_tables, np.int32)
+    cl = _np(context_lens, np.int32)
+    S = int(cl.shape[0])
+    if pairs is None:
+        n, pp = int(qsl[S]) * num_q_heads, None
+    else:
+        pp = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+        n = int(pp.shape[0])
+    out = np.zeros((n, head_dim), np.float64)
+    lse = np.zeros(n, np.float64)
+    lib.pa_oracle_prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
+                          _ptr(qsl), _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
+                          float(scale), float(k_scale), float(v_scale),
+                          None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def merge(part_o, part_lse):
+    """Log-sum-exp merge of partial results: part_o [P, D], part_lse [P] -> (out [D], lse)."""
+    lib = _load()
+    po = np.ascontiguousarray(np.asarray(part_o, np.float64))
+    pl = np.ascontiguousarray(np.asarray(part_lse, np.float64))
+    D = int(po.shape[1])
+    out = np.zeros(D, np.float64)
+    lse = np.zeros(1, np.float64)
+    lib.pa_oracle_merge(_ptr(po), _ptr(pl), int(po.shape[0]), D, _ptr(out), _ptr(lse))
+    return out, float(lse[0])

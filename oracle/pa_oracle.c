@@ -1,0 +1,318 @@
+/*
+ * pa_oracle.c -- plain, slow, fp64 CPU oracle for paged KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the tests, the smoke check and the bench's CPU-baseline
+ * leg use it.  It shares no code, header, table or helper with the CUDA
+ * library; it reads the same documented memory layout and nothing else.
+ *
+ * What it computes is the plain definition of attention over a block-paged
+ * KV cache:
+ *   - "Block-Paged KV Cache (FP8/FP16)" -- figure "vllm.cpp ARCHITECTURE
+ *     OVERVIEW" of "Building and Deploying vllm.cpp ..." (the sigmablogger
+ *     build/deploy walkthrough); block size 16 from its "Step 4: Serving Qwen"
+ *     launch commands (--block-size 16).
+ *   - "paged attention (block-paged KV cache)" and "chunked prefill" -- section
+ *     "What's implemented (CPU, behaviorally tested)" of the "vllm.cpp"
+ *     repository listing (Engine core and Model forward bullets).
+ *   - fp8 pages of one byte per element, E4M3 -- table in "2. CLI Configuration
+ *     Parameters" (--kv-cache-dtype) and the table in "Step 6: Status of
+ *     TurboQuant Support" of the walkthrough.
+ *   - a prefix-cache hit binds a new sequence's block table to existing
+ *     physical pages -- "1. Technical Mechanics of the Radix Cache" (Zero-Copy
+ *     Cache Hits) of the walkthrough.
+ * The pages give no formula; the oracle is softmax(scale * q K^T) V with an
+ * explicit gather through the block table, written out in fp64.
+ *
+ * Layout (the reading this build takes where the pages are silent):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *                      bf16 bit patterns (uint16) or E4M3 bytes (uint8)
+ *   q                : [tokens][num_q_heads][head_dim] bf16 bit patterns
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens     : int32 [num_seqs], KV tokens including this step's
+ *   slot_mapping     : int64 [tokens], slot = block * block_size + offset, <0 skip
+ *   query head h reads kv head h / (num_q_heads / num_kv_heads)
+ *
+ * Parity pins: every function here is pinned by tests that do not reuse its
+ * code (brute-force dense attention through torch's CPU SDPA, closed forms,
+ * invariants, torch's float8_e4m3fn codec); see tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KV_BF16 0
+#define KV_FP8_E4M3 1
+
+/* ---------------------------------------------------------------- bf16 */
+
+/* bf16 is the upper 16 bits of an IEEE binary32: widening is exact. */
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static float bf16_bits_to_float(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* ---------------------------------------------------------------- E4M3 */
+
+/*
+ * OCP 8-bit floating point, E4M3 variant: 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  No infinities; exponent 1111 with mantissa 111 is
+ * NaN (bytes 0x7F and 0xFF); every other pattern is finite.  Exponent field 0
+ * encodes subnormals m/8 * 2^(1-7).
+ */
+double pa_oracle_e4m3_decode(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int e = (byte >> 3) & 0xF;
+  int m = byte & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, 1 - 7);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* All 256 codes decoded once (the same definition, cached for speed). */
+static double e4m3_value[256];
+static int e4m3_value_ready = 0;
+
+static void e4m3_table_init(void) {
+  if (e4m3_value_ready) return;
+  for (int c = 0; c < 256; ++c) e4m3_value[c] = pa_oracle_e4m3_decode((uint8_t)c);
+  e4m3_value_ready = 1;
+}
+
+/*
+ * Round-to-nearest-even with saturation to the largest finite magnitude
+ * (448), NaN -> 0x7F.  Chosen the plainest way: search all 127 non-negative
+ * finite codes for the nearest value; on a tie take the code whose mantissa
+ * is even (codes are monotone in value, so that is the even code).
+ */
+uint8_t pa_oracle_e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  e4m3_table_init();
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  /* saturation: everything at or beyond the largest finite value, +-inf
+     included, maps to +-448 (a distance search cannot decide this once
+     |x| dwarfs 448 in fp64) */
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7E; ++c) {
+    double v = e4m3_value[c];
+    double err = fabs(a - v);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* Element (t, d) of one kv head, decoded to a real number (scale applied). */
+static double kv_elem(int kv_dtype, const void *cache, int64_t row_index, int head_dim, int d,
+                      double scale) {
+  if (kv_dtype == KV_BF16) {
+    const uint16_t *c = (const uint16_t *)cache;
+    return bf16_bits_to_double(c[row_index * head_dim + d]);
+  } else {
+    const uint8_t *c = (const uint8_t *)cache;
+    e4m3_table_init();
+    return e4m3_value[c[row_index * head_dim + d]] * scale;
+  }
+}
+
+/* Row index of logical token t of kv head kh for a sequence's block table. */
+static int64_t cache_row(const int32_t *table_row, int block_size, int num_kv_heads, int kh, int t) {
+  int64_t blk = table_row[t / block_size];
+  int off = t % block_size;
+  return (blk * num_kv_heads + kh) * block_size + off;
+}
+
+/* ---------------------------------------------------------- cache write */
+
+/*
+ * For each token i with slot_mapping[i] >= 0: block = slot / block_size,
+ * offset = slot % block_size, and for every kv head h the cache row
+ * (block, h, offset) receives enc(k[i][h][:]) (same for v).
+ * enc = bit copy for bf16; for E4M3, enc(x) = e4m3(fl32(fl32(x) / scale)).
+ */
+void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int head_dim,
+                           const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
+                           int num_tokens, float k_scale, float v_scale, void *k_cache,
+                           void *v_cache) {
+  for (int i = 0; i < num_tokens; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    int64_t blk = slot / block_size;
+    int64_t off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      int64_t dst_row = (blk * num_kv_heads + h) * block_size + off;
+      const uint16_t *ks = k + ((int64_t)i * num_kv_heads + h) * head_dim;
+      const uint16_t *vs = v + ((int64_t)i * num_kv_heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) {
+        if (kv_dtype == KV_BF16) {
+          ((uint16_t *)k_cache)[dst_row * head_dim + d] = ks[d];
+          ((uint16_t *)v_cache)[dst_row * head_dim + d] = vs[d];
+        } else {
+          float kq = bf16_bits_to_float(ks[d]) / k_scale;
+          float vq = bf16_bits_to_float(vs[d]) / v_scale;
+          ((uint8_t *)k_cache)[dst_row * head_dim + d] = pa_oracle_e4m3_encode((double)kq);
+          ((uint8_t *)v_cache)[dst_row * head_dim + d] = pa_oracle_e4m3_encode((double)vq);
+        }
+      }
+    }
+  }
+}
+
+/* ----------------------------------------------------- one attention row */
+
+/*
+ * Attention of one query vector over the logical key range [t_begin, t_end)
+ * of one sequence and one kv head:
+ *   x_t = scale * sum_d q[d] K_t[d]
+ *   m = max_t x_t,  l = sum_t exp(x_t - m)
+ *   out = sum_t exp(x_t - m) V_t / l,   lse = m + ln l
+ * An empty range gives out = 0 and lse = -inf.
+ */
+void pa_oracle_attend_range(int kv_dtype, int block_size, int num_kv_heads, int head_dim,
+                            const uint16_t *q_vec, const void *k_cache, const void *v_cache,
+                            const int32_t *table_row, int kh, int t_begin, int t_end,
+                            float scale, float k_scale, float v_scale, double *out, double *lse) {
+  int n = t_end - t_begin;
+  for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+  if (n <= 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double ks = (kv_dtype == KV_FP8_E4M3) ? (double)k_scale : 1.0;
+  double vs = (kv_dtype == KV_FP8_E4M3) ? (double)v_scale : 1.0;
+  double *x = (double *)malloc(sizeof(double) * (size_t)n);
+  double m = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    int64_t row = cache_row(table_row, block_size, num_kv_heads, kh, t_begin + j);
+    double dot = 0.0;
+    for (int d = 0; d < head_dim; ++d)
+      dot += bf16_bits_to_double(q_vec[d]) * kv_elem(kv_dtype, k_cache, row, head_dim, d, ks);
+    x[j] = (double)scale * dot;
+    if (x[j] > m) m = x[j];
+  }
+  double l = 0.0;
+  for (int j = 0; j < n; ++j) {
+    double p = exp(x[j] - m);
+    l += p;
+    int64_t row = cache_row(table_row, block_size, num_kv_heads, kh, t_begin + j);
+    for (int d = 0; d < head_dim; ++d)
+      out[d] += p * kv_elem(kv_dtype, v_cache, row, head_dim, d, vs);
+  }
+  for (int d = 0; d < head_dim; ++d) out[d] /= l;
+  *lse = m + log(l);
+  free(x);
+}
+
+/* ---------------------------------------------------------------- decode */
+
+/*
+ * Decode: sequence s has one new query (q[s]) at position L_s - 1 and attends
+ * every cached token [0, L_s) through its block table.  Query head h uses kv
+ * head h / g with g = num_q_heads / num_kv_heads.
+ *
+ * pairs: optional int32 [num_pairs][2] list of (s, h) to compute (NULL = all,
+ * in (s, h) row-major order).  out: [num_pairs][head_dim], lse: [num_pairs].
+ */
+void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_heads,
+                      int head_dim, const uint16_t *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, float scale, float k_scale,
+                      float v_scale, const int32_t *pairs, int num_pairs, double *out,
+                      double *lse) {
+  int g = num_q_heads / num_kv_heads;
+  int total = pairs ? num_pairs : num_seqs * num_q_heads;
+  for (int i = 0; i < total; ++i) {
+    int s = pairs ? pairs[2 * i] : i / num_q_heads;
+    int h = pairs ? pairs[2 * i + 1] : i % num_q_heads;
+    const uint16_t *q_vec = q + ((int64_t)s * num_q_heads + h) * head_dim;
+    const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+    pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
+                           row, h / g, 0, context_lens[s], scale, k_scale, v_scale,
+                           out + (int64_t)i * head_dim, lse + i);
+  }
+}
+
+/* --------------------------------------------------------------- prefill */
+
+/*
+ * Chunked prefill: sequence s owns the packed query rows
+ * [query_start_loc[s], query_start_loc[s+1]); q_len = their count.  Its KV
+ * already holds L_s tokens (the chunk's own K/V were written before), so query
+ * i sits at position L_s - q_len + i and attends keys [0, position] (causal).
+ *
+ * pairs: optional int32 [num_pairs][2] list of (token row, q head) (NULL = all
+ * rows x heads).  out: [num_pairs][head_dim], lse: [num_pairs].
+ */
+void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q_heads,
+                       int head_dim, const uint16_t *q, const int32_t *query_start_loc,
+                       const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                       int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                       float scale, float k_scale, float v_scale, const int32_t *pairs,
+                       int num_pairs, double *out, double *lse) {
+  int g = num_q_heads / num_kv_heads;
+  int num_rows = query_start_loc[num_seqs];
+  int total = pairs ? num_pairs : num_rows * num_q_heads;
+  for (int i = 0; i < total; ++i) {
+    int r = pairs ? pairs[2 * i] : i / num_q_heads;
+    int h = pairs ? pairs[2 * i + 1] : i % num_q_heads;
+    int s = 0;
+    while (s + 1 <= num_seqs && query_start_loc[s + 1] <= r) ++s;
+    int q_len = query_start_loc[s + 1] - query_start_loc[s];
+    int pos = context_lens[s] - q_len + (r - query_start_loc[s]);
+    const uint16_t *q_vec = q + ((int64_t)r * num_q_heads + h) * head_dim;
+    const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+    pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
+                           row, h / g, 0, pos + 1, scale, k_scale, v_scale,
+                           out + (int64_t)i * head_dim, lse + i);
+  }
+}
+
+/* ----------------------------------------------------------------- merge */
+
+/*
+ * Merge of attention results over disjoint key ranges (log-sum-exp
+ * weighting): M = max_p lse_p, w_p = exp(lse_p - M),
+ * out = sum_p w_p o_p / sum_p w_p, lse = M + ln sum_p w_p.  Parts with
+ * lse = -inf carry no keys and drop out; if every part is empty the result is
+ * out = 0, lse = -inf.
+ * part_o: [num_parts][head_dim], part_lse: [num_parts].
+ */
+void pa_oracle_merge(const double *part_o, const double *part_lse, int num_parts, int head_dim,
+                     double *out, double *lse) {
+  double M = -INFINITY;
+  for (int p = 0; p < num_parts; ++p)
+    if (part_lse[p] > M) M = part_lse[p];
+  for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+  if (M == -INFINITY) {
+    *lse = -INFINITY;
+    return;
+  }
+  double wsum = 0.0;
+  for (int p = 0; p < num_parts; ++p) {
+    if (part_lse[p] == -INFINITY) continue;
+    double w = exp(part_lse[p] - M);
+    wsum += w;
+    for (int d = 0; d < head_dim; ++d) out[d] += w * part_o[(int64_t)p * head_dim + d];
+  }
+  for (int d = 0; d < head_dim; ++d) out[d] /= wsum;
+  *lse = M + log(wsum);
+}

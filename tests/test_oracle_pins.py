@@ -1,0 +1,386 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test checks the oracle against a library routine (torch's CPU SDPA and
+its float8_e4m3fn codec), a closed form, an invariant, or the format
+definition's fixed points -- chosen so that a plausible slip anywhere in the
+oracle (wrong GQA index, wrong block offset, a dropped scale, an off-by-one in
+the causal position, a sign in the merge, an exponent bias) fails one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_14_gb300 import workloads as W
+
+BF16, FP8 = oracle.KV_BF16, oracle.KV_FP8_E4M3
+
+
+# ------------------------------------------------------------ helpers (independent)
+
+def _bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def _fp8_cache_to_f64(cache_u8: np.ndarray, scale: float) -> np.ndarray:
+    """Decode E4M3 bytes with torch's own float8_e4m3fn codec (library routine)."""
+    t = torch.from_numpy(np.ascontiguousarray(cache_u8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy() * float(scale)
+
+
+def _f32(x) -> float:
+    return float(np.float32(x))
+
+
+def _dense_kv(pool_f64: np.ndarray, table_row, L, kh):
+    """Gather logical tokens [0, L) of kv head kh with numpy fancy indexing."""
+    t = np.arange(L)
+    blk = np.asarray(table_row)[t // W.BLOCK_SIZE]
+    return pool_f64[blk, kh, t % W.BLOCK_SIZE, :]
+
+
+def _sdpa(q, k, v, scale, mask=None):
+    """torch CPU scaled_dot_product_attention in float64 (library routine).
+    The scale is an fp32 argument of the library, hence rounded to fp32 here."""
+    scale = _f32(scale)
+    q = torch.from_numpy(np.asarray(q, np.float64))[None, None]
+    k = torch.from_numpy(np.asarray(k, np.float64))[None, None]
+    v = torch.from_numpy(np.asarray(v, np.float64))[None, None]
+    m = None if mask is None else torch.from_numpy(mask)[None, None]
+    return torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=scale)[0, 0].numpy()
+
+
+def _oracle_caches(b: W.PagedBatch):
+    """Caches as the oracle reads them: bf16 pool as-is, or the E4M3 encoding of
+    the whole (small) pool made by the oracle's own cache write."""
+    if b.kv_dtype == W.KV_BF16:
+        return BF16, b.k_pool, b.v_pool
+    k, v, slots = b.pool_tokens_as_rows()
+    z = np.zeros(tuple(b.k_pool.shape), np.uint8)
+    kc, vc = oracle.cache_write(FP8, b.block_size, b.num_kv_heads, b.head_dim, k, v, slots, z, z,
+                                b.k_scale, b.v_scale)
+    return FP8, kc, vc
+
+
+def _oracle_decode(b: W.PagedBatch, pairs=None):
+    kd, kc, vc = _oracle_caches(b)
+    return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode,
+                         kc, vc, b.block_tables_decode, b.context_lens_decode, b.scale,
+                         b.k_scale, b.v_scale, pairs=pairs)
+
+
+# ------------------------------------------------------------------ E4M3 codec
+
+def test_e4m3_fixed_points_of_the_format_definition():
+    # OCP FP8 E4M3: bias 7, max finite 448, min normal 2^-6, min subnormal 2^-9,
+    # no infinities, S.1111.111 is NaN
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0xFE) == -448.0
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+    assert oracle.e4m3_decode(0x00) == 0.0 and math.copysign(1, oracle.e4m3_decode(0x80)) == -1
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+    assert oracle.e4m3_decode(0x78) == 256.0  # exponent field 15, mantissa 0 is finite
+
+
+def test_e4m3_decode_matches_torch_float8_for_all_256_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([oracle.e4m3_decode(int(c)) for c in codes])
+    both_nan = np.isnan(ref) & np.isnan(mine)
+    assert np.all(both_nan | (ref == mine))
+    assert np.array_equal(np.signbit(ref[~both_nan]), np.signbit(mine[~both_nan]))
+    finite_pos = mine[:0x7F]
+    assert np.all(np.diff(finite_pos) > 0), "positive codes must be strictly increasing"
+
+
+def test_e4m3_encode_matches_torch_rne_inside_the_finite_range():
+    rng = np.random.default_rng(5)
+    pos = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    mids = (pos[1:] + pos[:-1]) / 2  # exact ties: round half to even
+    xs = np.concatenate([rng.normal(0, 1, 2000), rng.normal(0, 60, 2000), rng.uniform(-448, 448, 2000),
+                         mids, -mids, pos, -pos, [2.0 ** -10, 3 * 2.0 ** -10, 2.0 ** -12, 447.99, 463.9]])
+    xs = xs.astype(np.float32)  # the encoder's input is an fp32 quotient
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = np.array([oracle.e4m3_encode(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(ref, mine), np.nonzero(ref != mine)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan_and_signed_zero():
+    # the chosen reading: finite overflow saturates to +-448 (torch's codec,
+    # which is non-saturating, returns NaN there instead)
+    assert oracle.e4m3_encode(464.0) == 0x7E
+    assert oracle.e4m3_encode(1e9) == 0x7E
+    assert oracle.e4m3_encode(-1e30) == 0xFE
+    assert oracle.e4m3_encode(float("inf")) == 0x7E
+    assert oracle.e4m3_encode(float("-inf")) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(-2.0 ** -11) == 0x80  # rounds to zero, keeps the sign
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+
+
+# --------------------------------------------------------------- cache write
+
+def test_cache_write_bf16_is_a_scatter_of_bit_patterns():
+    b = W.workload(5, poison=True)
+    kc, vc = oracle.cache_write(BF16, 16, 8, 128, b.k_new, b.v_new, b.slot_mapping, b.k_pool, b.v_pool)
+    ref_k = b.k_pool.view(torch.int16).numpy().view(np.uint16).copy()
+    ref_v = b.v_pool.view(torch.int16).numpy().view(np.uint16).copy()
+    s = b.slot_mapping.numpy()
+    ref_k[s // 16, :, s % 16, :] = b.k_new.view(torch.int16).numpy().view(np.uint16)
+    ref_v[s // 16, :, s % 16, :] = b.v_new.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
+
+
+def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation():
+    g = torch.Generator().manual_seed(3)
+    T, H, D, NB = 40, 2, 64, 8
+    k = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
+    v = (3 * torch.randn(T, H, D, generator=g)).to(torch.bfloat16)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
+    slots[::7] = -1
+    ks = float(k.float().abs().max()) / 448
+    vs = float(v.float().abs().max()) / 448
+    z = np.full((NB, H, 16, D), 0xAB, np.uint8)
+    kc, vc = oracle.cache_write(FP8, 16, H, D, k, v, slots, z, z, ks, vs)
+    ref_k = z.copy()
+    ref_v = z.copy()
+    keep = slots >= 0
+    s = slots[keep].numpy()
+    qk = (k[keep].float() / torch.tensor(ks, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    qv = (v[keep].float() / torch.tensor(vs, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    ref_k[s // 16, :, s % 16, :] = qk.numpy()
+    ref_v[s // 16, :, s % 16, :] = qv.numpy()
+    assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
+
+
+# ------------------------------------------------------------ decode attention
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+@pytest.mark.parametrize("D,Hq,Hkv", [(8, 2, 2), (64, 4, 2), (8, 10, 2), (64, 5, 1)])
+def test_decode_matches_bruteforce_sdpa(kv, D, Hq, Hkv):
+    lens = [1, 5, 16, 17, 40]
+    b = W.random_decode(11 + D + Hq, lens, Hq, Hkv, D, kv_dtype=kv, poison=True)
+    out, lse = _oracle_decode(b)
+    kd, kc, vc = _oracle_caches(b)
+    if kd == BF16:
+        kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    else:
+        kf, vf = _fp8_cache_to_f64(kc, b.k_scale), _fp8_cache_to_f64(vc, b.v_scale)
+    g = Hq // Hkv
+    qf = _bf16_to_f64(b.q_decode)
+    for s, L in enumerate(lens):
+        for h in range(Hq):
+            K = _dense_kv(kf, b.block_tables_decode[s].numpy(), L, h // g)
+            V = _dense_kv(vf, b.block_tables_decode[s].numpy(), L, h // g)
+            ref = _sdpa(qf[s, h][None], K, V, b.scale)[0]
+            i = s * Hq + h
+            np.testing.assert_allclose(out[i], ref, rtol=0, atol=1e-12)
+            x = _f32(b.scale) * K @ qf[s, h]
+            ref_lse = x.max() + math.log(np.exp(x - x.max()).sum())
+            assert abs(lse[i] - ref_lse) < 1e-12
+
+
+def test_decode_context_length_one_returns_v_exactly():
+    b = W.workload(1, poison=True)
+    out, lse = _oracle_decode(b)
+    s = 0  # context length 1
+    blk = int(b.block_tables_decode[0, 0])
+    for h in range(4):
+        v0 = b.v_pool[blk, h // 2, 0].to(torch.float64).numpy()
+        assert np.array_equal(out[s * 4 + h], v0)
+
+
+def test_decode_identical_keys_or_zero_query_give_mean_of_v():
+    b = W.random_decode(21, [3, 16, 37], 4, 2, 64, poison=True)
+    # identical keys: every cached key row of every block equals one vector
+    kpool = b.k_pool.clone()
+    kpool[:] = kpool[int(b.block_tables_decode[0, 0]), 0, 0].clone()
+    b.k_pool = kpool
+    out, _ = _oracle_decode(b)
+    qzero = W.random_decode(21, [3, 16, 37], 4, 2, 64, poison=True)
+    qzero.q_decode = torch.zeros_like(qzero.q_decode)
+    out0, lse0 = _oracle_decode(qzero)
+    vf = _bf16_to_f64(b.v_pool)
+    for s, L in enumerate([3, 16, 37]):
+        for h in range(4):
+            mean_v = _dense_kv(vf, b.block_tables_decode[s].numpy(), L, h // 2).mean(0)
+            np.testing.assert_allclose(out[s * 4 + h], mean_v, atol=1e-12, rtol=0)
+            np.testing.assert_allclose(out0[s * 4 + h], mean_v, atol=1e-12, rtol=0)
+            assert abs(lse0[s * 4 + h] - math.log(L)) < 1e-12
+
+
+def test_decode_weights_sum_to_one_and_output_is_linear_in_v():
+    b = W.random_decode(31, [9, 33], 4, 2, 64, poison=True)
+    base = b.v_pool.clone()
+    b.v_pool = torch.where(torch.isnan(base), base, torch.ones_like(base))
+    ones, _ = _oracle_decode(b)
+    np.testing.assert_allclose(ones, 1.0, atol=1e-13, rtol=0)
+    b.v_pool = base
+    o1, _ = _oracle_decode(b)
+    b.v_pool = (2 * base.float()).to(torch.bfloat16)  # exact doubling in bf16
+    o2, _ = _oracle_decode(b)
+    np.testing.assert_allclose(o2, 2 * o1, atol=1e-12, rtol=0)
+
+
+def test_decode_dominant_key_selects_its_value():
+    b = W.random_decode(41, [20], 2, 1, 64, poison=True)
+    q = b.q_decode[0, 0].float()
+    blk = int(b.block_tables_decode[0, 13 // 16])
+    kp = b.k_pool.clone()
+    kp[blk, 0, 13 % 16] = (q * 40).to(torch.bfloat16)  # score gap far above 60
+    b.k_pool = kp
+    out, _ = _oracle_decode(b)
+    v13 = b.v_pool[blk, 0, 13].to(torch.float64).numpy()
+    np.testing.assert_allclose(out[0], v13, atol=1e-12, rtol=0)
+
+
+def test_decode_invariant_under_permuting_physical_blocks():
+    b = W.random_decode(51, [7, 16, 40, 33], 4, 2, 64, poison=True)
+    out, lse = _oracle_decode(b)
+    perm = torch.randperm(b.num_blocks, generator=torch.Generator().manual_seed(9))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(b.num_blocks)
+    b2 = W.random_decode(51, [7, 16, 40, 33], 4, 2, 64, poison=True)
+    b2.k_pool = b.k_pool[inv]  # new block j holds old block inv[j] ... so old block i moves to perm[i]
+    b2.v_pool = b.v_pool[inv]
+    t = b.block_tables_decode.clone().long()
+    b2.block_tables_decode = torch.where(t >= 0, perm[t.clamp(min=0)], t).to(torch.int32)
+    out2, lse2 = _oracle_decode(b2)
+    assert np.array_equal(out, out2) and np.array_equal(lse, lse2)
+
+
+def test_decode_never_reads_poisoned_slots():
+    for n in (1,):
+        b = W.workload(n, poison=True)
+        out, lse = _oracle_decode(b)
+        assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    b = W.random_decode(61, [1, 15, 17, 31, 32], 10, 2, 8, kv_dtype=W.KV_FP8, poison=True)
+    out, _ = _oracle_decode(b)
+    assert np.all(np.isfinite(out))
+
+
+def test_decode_pairs_subset_equals_full():
+    b = W.random_decode(71, [12, 29], 4, 2, 64, poison=True)
+    full, lf = _oracle_decode(b)
+    pairs = [(1, 3), (0, 0), (1, 1)]
+    sub, ls = _oracle_decode(b, pairs=pairs)
+    for i, (s, h) in enumerate(pairs):
+        assert np.array_equal(sub[i], full[s * 4 + h]) and ls[i] == lf[s * 4 + h]
+
+
+# ------------------------------------------------------------------ merge
+
+def test_merge_of_split_ranges_equals_unsplit():
+    b = W.random_decode(81, [45], 2, 1, 64, poison=True)
+    row = b.block_tables_decode[0]
+    q = b.q_decode[0, 1]
+    full, lf = oracle.attend_range(BF16, 16, 1, 64, q, b.k_pool, b.v_pool, row, 0, 0, 45, b.scale)
+    for cuts in ([17], [1, 30], [16, 32, 44], [0, 45]):
+        edges = [0] + cuts + [45]
+        parts = [oracle.attend_range(BF16, 16, 1, 64, q, b.k_pool, b.v_pool, row, 0, a, c, b.scale)
+                 for a, c in zip(edges[:-1], edges[1:])]
+        mo, ml = oracle.merge(np.stack([p[0] for p in parts]), np.array([p[1] for p in parts]))
+        np.testing.assert_allclose(mo, full, atol=1e-12, rtol=0)
+        assert abs(ml - lf) < 1e-12
+
+
+def test_merge_closed_forms():
+    o = np.array([[1.0, 2.0], [3.0, -4.0]])
+    mo, ml = oracle.merge(o, np.array([0.7, 0.7]))
+    np.testing.assert_allclose(mo, [2.0, -1.0], atol=1e-15)
+    assert abs(ml - (0.7 + math.log(2))) < 1e-15
+    mo, ml = oracle.merge(o, np.array([-np.inf, 1.5]))
+    np.testing.assert_array_equal(mo, o[1])
+    assert ml == 1.5
+    mo, ml = oracle.merge(o, np.array([-np.inf, -np.inf]))
+    assert np.all(mo == 0) and ml == -np.inf
+    # weights e^1 : e^0
+    mo, _ = oracle.merge(o, np.array([1.0, 0.0]))
+    w = math.e / (math.e + 1)
+    np.testing.assert_allclose(mo, w * o[0] + (1 - w) * o[1], atol=1e-15)
+
+
+# ----------------------------------------------------------------- prefill
+
+def _oracle_prefill(b: W.PagedBatch, pairs=None):
+    kd, kc, vc = _oracle_caches(b)
+    return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill,
+                          b.query_start_loc, kc, vc, b.block_tables_prefill, b.context_lens_prefill,
+                          b.scale, b.k_scale, b.v_scale, pairs=pairs)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+def test_prefill_matches_bruteforce_sdpa_with_causal_mask(kv):
+    q_lens, ctx = [5, 16, 1, 23], [5, 40, 33, 64]
+    b = W.random_prefill(91, q_lens, ctx, 4, 2, 64, kv_dtype=kv, shared_prefix_blocks=1)
+    out, _ = _oracle_prefill(b)
+    kd, kc, vc = _oracle_caches(b)
+    if kd == BF16:
+        kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    else:
+        kf, vf = _fp8_cache_to_f64(kc, b.k_scale), _fp8_cache_to_f64(vc, b.v_scale)
+    qf = _bf16_to_f64(b.q_prefill)
+    qsl = b.query_start_loc.numpy()
+    for s, (n, L) in enumerate(zip(q_lens, ctx)):
+        for h in range(4):
+            K = _dense_kv(kf, b.block_tables_prefill[s].numpy(), L, h // 2)
+            V = _dense_kv(vf, b.block_tables_prefill[s].numpy(), L, h // 2)
+            Q = qf[qsl[s]:qsl[s] + n, h]
+            # bottom-right aligned causal mask: query i sits at key position L - n + i
+            mask = np.arange(L)[None, :] <= (L - n + np.arange(n))[:, None]
+            ref = _sdpa(Q, K, V, b.scale, mask)
+            got = out[(qsl[s] + np.arange(n)) * 4 + h]
+            np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
+def test_prefill_single_query_equals_decode():
+    lens = [7, 16, 41]
+    d = W.random_decode(101, lens, 4, 2, 64, poison=True)
+    p = W.random_prefill(101, [1, 1, 1], lens, 4, 2, 64)
+    p.q_prefill = d.q_decode.clone()
+    p.k_pool, p.v_pool = d.k_pool, d.v_pool
+    p.block_tables_prefill = d.block_tables_decode
+    p.context_lens_prefill = d.context_lens_decode
+    po, pl = _oracle_prefill(p)
+    do, dl = _oracle_decode(d)
+    assert np.array_equal(po, do) and np.array_equal(pl, dl)
+
+
+def test_prefill_in_two_chunks_equals_one_chunk():
+    b = W.random_prefill(111, [30], [50], 4, 2, 64)
+    one, _ = _oracle_prefill(b)
+    # first chunk: 12 queries while only 32 tokens exist; then the last 18
+    first = W.random_prefill(111, [30], [50], 4, 2, 64)
+    first.q_prefill = b.q_prefill[:12].clone()
+    first.query_start_loc = torch.tensor([0, 12], dtype=torch.int32)
+    first.context_lens_prefill = torch.tensor([32], dtype=torch.int32)
+    o1, _ = _oracle_prefill(first)
+    second = W.random_prefill(111, [30], [50], 4, 2, 64)
+    second.q_prefill = b.q_prefill[12:].clone()
+    second.query_start_loc = torch.tensor([0, 18], dtype=torch.int32)
+    o2, _ = _oracle_prefill(second)
+    assert np.array_equal(np.concatenate([o1, o2]), one)
+
+
+def test_prefill_shared_prefix_blocks_are_read_by_every_sequence():
+    b = W.random_prefill(121, [4, 4, 4], [40, 40, 40], 2, 1, 8, shared_prefix_blocks=2)
+    t = b.block_tables_prefill
+    assert torch.equal(t[0, :2], t[1, :2]) and torch.equal(t[1, :2], t[2, :2])
+    out, _ = _oracle_prefill(b)
+    assert np.all(np.isfinite(out))
+    # each sequence's queries see the shared keys: zeroing them changes every output
+    b2 = W.random_prefill(121, [4, 4, 4], [40, 40, 40], 2, 1, 8, shared_prefix_blocks=2)
+    vp = b2.v_pool.clone()
+    vp[t[0, :2].long()] = 0
+    b2.v_pool = vp
+    out2, _ = _oracle_prefill(b2)
+    for s in range(3):
+        rows = slice(s * 4 * 2, (s + 1) * 4 * 2)
+        assert not np.allclose(out[rows], out2[rows])
