@@ -1,0 +1,332 @@
+"""Benchmark of the paged-attention hot path on one GB300 (or N replicas).
+
+A step is one pass of the decode hot path over one batch of synthetic input:
+the slot-mapped cache write of each sequence's new token (pa_cache_write),
+then split-KV decode attention over the block-paged cache (pa_decode, with its
+in-launch merge).  The workload is the Qwen3-8B-shaped decode step: 32
+sequences with context lengths ~ U[512, 4096], 32 query / 8 kv heads,
+head_dim 128, block size 16, bf16 KV ~ N(0, 1), random non-contiguous block
+tables from a pool of 1.25x the blocks needed (seed 1002).
+
+Printed: one JSON line.  ``value`` is the effective KV-read bandwidth, the
+algorithmic KV bytes of the step (every valid K and V element of every
+(sequence, kv head) once) divided by the device time of the step, with the
+inputs resident in HBM and the L2 flushed before every step.
+
+``--impl reference`` times the fp64 CPU oracle instead (the only reference
+implementation of this method), on a bounded sample of the same workload.
+
+For N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the path needs no exchange between GPUs); value = all ranks' bytes / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: effective KV-read GB/s and % of GB300 HBM peak; us/step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = 2
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons of one GPU, sampled while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, out_path: str | None = None):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out_path = out_path
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        if self.out_path:
+            with open(self.out_path, "w") as f:
+                f.write(out)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_attention_14_gb300 import build as pa_build
+    from paged_kv_attention_14_gb300 import binding as B
+    from paged_kv_attention_14_gb300 import workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.load(pa_build.build())
+
+    b = W.workload(args.workload, device=dev, poison=False)
+    kv = B.PA_KV_BF16 if b.kv_dtype == W.KV_BF16 else B.PA_KV_FP8_E4M3
+    desc = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv,
+                       b.k_scale if kv else 0.0, b.v_scale if kv else 0.0, decode_impl=args.decode_impl)
+    if kv == B.PA_KV_BF16:
+        kc, vc = b.k_pool, b.v_pool
+    else:
+        kc = torch.empty(tuple(b.k_pool.shape), dtype=torch.uint8, device=dev)
+        vc = torch.empty_like(kc)
+        k_rows, v_rows, slots = b.pool_tokens_as_rows()
+        B.pa_cache_write(desc, k_rows, v_rows, kc, vc, slots)
+        del k_rows, v_rows, slots
+        b.k_pool = b.v_pool = None
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    wsp = B.decode_workspace(desc, S, maxL, dev)
+    out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
+    kv_bytes = b.decode_kv_bytes()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2 (129 MB)
+
+    def step():
+        B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
+        B.pa_decode(desc, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale,
+                    wsp)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e0, e1, e2 = ev[i]
+        e0.record()
+        B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
+        e1.record()
+        B.pa_decode(desc, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale,
+                    wsp)
+        e2.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / K
+    dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+    if ws > 1:
+        t = torch.tensor([step_ms, dec_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, dec_ms = float(t[0]), float(t[1])
+    assert int(wsp[:4].view(torch.int32)[0]) == 0, "decode kernel reported a wait timeout"
+
+    # end to end through the public API: pinned host inputs in, result out
+    host = {n: getattr(b, n).cpu().pin_memory() for n in
+            ("q_decode", "k_new", "v_new", "slot_mapping", "block_tables_decode", "context_lens_decode")}
+    dev_in = {n: torch.empty_like(getattr(b, n)) for n in host}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        B.pa_cache_write(desc, dev_in["k_new"], dev_in["v_new"], kc, vc, dev_in["slot_mapping"])
+        B.pa_decode(desc, out, dev_in["q_decode"], kc, vc, dev_in["block_tables_decode"],
+                    dev_in["context_lens_decode"], maxL, b.scale, wsp)
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    ke = max(10, min(K, 200))
+    tot = 0.0
+    for _ in range(ke):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        tot += time.perf_counter() - t0
+    e2e_s = tot / ke
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t[0])
+
+    if rank == 0:
+        peak, peak_kind = _peaks()
+        gbs = ws * kv_bytes / (step_ms * 1e-3) / 1e9
+        dec_gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC,
+            "value": round(gbs, 1),
+            "unit": "GB/s",
+            "n_gpus": ws,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 5),
+            "us_per_step": round(step_ms * 1e3, 2),
+            "pct_hbm_peak": {f"of {peak_kind} {peak:.1f} GB/s": round(100 * gbs / ws / peak, 1),
+                             f"of nominal {NOMINAL_HBM_GBS:.0f} GB/s": round(100 * gbs / ws / NOMINAL_HBM_GBS, 1)},
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if kv == B.PA_KV_BF16 else "fp8_e4m3",
+            "data": "synthetic",
+            "config": {"workload": b.name, "num_seqs": S, "kv_tokens": int(b.context_lens_decode.sum()),
+                       "kv_bytes_per_step": kv_bytes, "l2": "flushed before every step (256 MB write)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "decode (pa_decode)", "achieved": round(dec_gbs, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_gbs / peak, 4),
+                         "kernel_us": round(dec_ms * 1e3, 2), "traffic": None},
+            "e2e": {"value": round(ws * kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * K,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _oracle_sample(n_workload: int, budget_s: float):
+    """Run the fp64 oracle over whole sequences of the workload (all heads)
+    until ``budget_s`` of CPU time is used; returns (kv_bytes, seconds, n_seqs)."""
+    import oracle
+    from paged_kv_attention_14_gb300 import workloads as W
+
+    b = W.workload(n_workload, device="cpu", poison=False)
+    if b.kv_dtype != W.KV_BF16:
+        raise RuntimeError("the CPU baseline covers the bf16 workloads")
+    kc, vc = b.k_pool, b.v_pool
+    S = b.context_lens_decode.shape[0]
+    done_bytes, t_used, n = 0, 0.0, 0
+    order = list(range(S))
+    while t_used < budget_s and n < 10 * S:
+        s = order[n % S]
+        pairs = [(s, h) for h in range(b.num_q_heads)]
+        t0 = time.perf_counter()
+        oracle.decode(oracle.KV_BF16, 16, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
+                      b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs)
+        t_used += time.perf_counter() - t0
+        done_bytes += int(b.context_lens_decode[s]) * b.num_kv_heads * b.head_dim * 2 * 2
+        n += 1
+    return done_bytes, t_used, n, b.name
+
+
+def cpu_baseline(n_workload: int, budget_s: float = 10.0):
+    nbytes, secs, n, name = _oracle_sample(n_workload, budget_s)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole sequences (all 32 q heads) of '{name}', fp64 C oracle, one thread, "
+                      f"{secs:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    import oracle  # noqa: F401  (built on first use)
+    # each step: one bounded sample of the workload through the oracle
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_sample(args.workload, per_step)
+    nbytes, secs = 0, 0.0
+    for _ in range(args.steps):
+        b_, s_, n_, name = _oracle_sample(args.workload, per_step)
+        nbytes += b_
+        secs += s_
+    value = nbytes / secs / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": name},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"whole sequences of '{name}' per step, about {per_step:.1f} s each"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4])
+    ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

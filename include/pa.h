@@ -1,0 +1,209 @@
+/*
+ * pa.h -- C ABI of a paged KV attention library for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation is attention over a block-paged KV cache for a continuous
+ * batch of variable-length sequences, the "paged attention (block-paged KV
+ * cache)" and "chunked prefill" of the vllm.cpp engine ("What's implemented
+ * (CPU, behaviorally tested)", Engine core and Model forward bullets, of the
+ * vllm.cpp repository page) with its "Block-Paged KV Cache (FP8/FP16)" (the
+ * "vllm.cpp ARCHITECTURE OVERVIEW" figure of "Building and Deploying vllm.cpp
+ * ...") and block size 16 ("Step 4: Serving Qwen", --block-size 16).
+ *
+ * Interface conventions follow the pages' own C ABI ("Library API (C ABI)" of
+ * the vllm.cpp README): flat, exception-free, versioned with a runtime version
+ * query, grows only by appending struct fields whose zero value keeps the old
+ * behaviour, and reports failure as a status code plus a last-error string.
+ *
+ * Memory layout (the pages name no layout; this one is the library's choice):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *                      bf16, or one E4M3 byte per element for FP8 KV.
+ *   q (decode)       : [num_seqs][num_q_heads][head_dim] bf16
+ *   q (prefill)      : [total_query_tokens][num_q_heads][head_dim] bf16
+ *   out              : same shape as q, fp32
+ *   lse (optional)   : [rows][num_q_heads] fp32, natural-log log-sum-exp of
+ *                      the scaled scores of each output row
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq], physical block
+ *                      id of each logical block of each sequence
+ *   context_lens     : int32 [num_seqs], KV tokens of each sequence including
+ *                      the ones written this step
+ *   slot_mapping     : int64 [num_tokens], slot = block * block_size + offset;
+ *                      a negative slot means "skip this token"
+ * Query head h attends kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: every pointer is caller-owned device memory unless its comment
+ * says "host".  The library allocates no device memory and keeps no state
+ * between calls apart from the thread-local error string and a per-device
+ * cache of launch limits (SM count, occupancy).
+ *
+ * Asynchrony: every compute entry point enqueues work on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and returns without
+ * synchronising.  PA_OK means "validated and enqueued".  Argument errors are
+ * detected on the host before anything is enqueued; a CUDA launch error is
+ * reported as PA_ERR_CUDA.  Device-array contents (block ids, lengths, slots)
+ * are the caller's contract and are not checked on the device: a block id
+ * outside [0, num_blocks), a context length above max_blocks_per_seq *
+ * block_size, or a slot outside the pool reads or writes out of bounds.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+/* Symbols of the shared library; everything else in it stays hidden. */
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size or shape      */
+  PA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head_dim 96)   */
+  PA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required     */
+  PA_ERR_CUDA = 4         /* a CUDA runtime call or launch failed           */
+} pa_status;
+
+typedef enum {
+  PA_KV_BF16 = 0,    /* bf16 K/V, bit copies of the written values          */
+  PA_KV_FP8_E4M3 = 1 /* OCP E4M3 bytes with per-tensor fp32 scales        */
+} pa_kv_dtype;
+
+/* Which decode kernel pa_decode runs.  0 lets the library choose. */
+typedef enum {
+  PA_DECODE_AUTO = 0,
+  PA_DECODE_SIMT = 1,  /* CUDA-core dot products, group size <= 4          */
+  PA_DECODE_MMA = 2    /* tensor-core (mma.sync) tiles, any group size <= 16 */
+} pa_decode_impl;
+
+/*
+ * Shape of the KV pool.  Zero-initialise, then set the fields.  Fields are
+ * only ever appended; a zero in an appended field keeps earlier behaviour.
+ *   block_size   : tokens per block; 16 is the only supported value.
+ *   head_dim     : 64 or 128.
+ *   num_q_heads  : a multiple of num_kv_heads; group size g = q / kv <= 16.
+ *   k_scale, v_scale : FP8 only.  Cached value = stored E4M3 value * scale.
+ *                  0 means 1.0.  Ignored for bf16.
+ *   decode_impl  : a pa_decode_impl value.
+ */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t head_dim;
+  int32_t kv_dtype; /* pa_kv_dtype */
+  float k_scale;
+  float v_scale;
+  int32_t decode_impl; /* pa_decode_impl */
+} pa_kv_desc;
+
+/* PA_ABI_VERSION of the loaded library. */
+PA_API int pa_abi_version(void);
+
+/* Message of the last failing call on this thread ("" if none).  The pointer
+ * stays valid until the next library call on the same thread. */
+PA_API const char *pa_last_error(void);
+
+/*
+ * Slot-mapped cache write.  For every token i < num_tokens with
+ * slot_mapping[i] >= 0, block = slot / block_size and offset = slot %
+ * block_size; for every kv head h, the cache row (block, h, offset) receives
+ * k[i][h][:] (v likewise).  bf16 KV stores the bits unchanged.  FP8 KV stores
+ * e4m3(fl32(x) / k_scale) rounded to nearest even with finite saturation to
+ * +-448 and NaN kept as NaN (0x7F).
+ *   k, v : [num_tokens][num_kv_heads][head_dim] bf16, 16-byte aligned.
+ * The write of a prefix-cache hit must not target a block shared with another
+ * sequence ("Zero-Copy Cache Hits" of "1. Technical Mechanics of the Radix
+ * Cache" binds sequences to the same physical pages; writing into one would
+ * change all of them).  Duplicate slots in one call race.
+ * num_tokens == 0 enqueues nothing and returns PA_OK.
+ */
+PA_API pa_status pa_cache_write(const pa_kv_desc *desc, const void *k, const void *v, void *k_cache,
+                         void *v_cache, const int64_t *slot_mapping, int32_t num_tokens,
+                         pa_stream_t stream);
+
+/*
+ * Bytes of scratch that pa_decode needs for num_seqs sequences on the current
+ * device.  Zero-fill the workspace once before its first use; it may then be
+ * reused by consecutive calls on one stream (each call leaves its error word
+ * and merge counters at zero again; the rest holds the last call's partial
+ * results).  Calls that overlap on the GPU need separate workspaces.  After a
+ * call completes, a non-zero first int32 of the workspace means the kernel
+ * gave up waiting on its own pipeline (a bounded wait ran out).
+ */
+PA_API size_t pa_decode_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_context_len);
+
+/*
+ * Decode attention, split-KV.  Sequence s has one query q[s] at position
+ * context_lens[s] - 1; query head h attends all tokens [0, context_lens[s]) of
+ * kv head h / g through block_tables[s]:
+ *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t     (fp32)
+ *   lse[s][h] = ln sum_t exp(scale * q[s][h] . K_t)          (if lse != NULL)
+ * A sequence with context length 0 gets out = 0 and lse = -inf.
+ * The KV range of long sequences is split across CTAs and the pieces are
+ * merged by log-sum-exp inside the same launch.
+ *   max_context_len : an upper bound of context_lens (host value).
+ *   workspace       : pa_decode_workspace_size() bytes, zero-filled once.
+ */
+PA_API pa_status pa_decode(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                    const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                    int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                    pa_stream_t stream);
+
+/*
+ * Chunked-prefill causal attention over the paged cache.  Sequence s owns the
+ * packed query rows [query_start_loc[s], query_start_loc[s+1]); with q_len
+ * their count, query i of it sits at position context_lens[s] - q_len + i and
+ * attends keys [0, position] of its kv head (the chunk's own K/V must have
+ * been written by pa_cache_write first).  Blocks shared by several tables
+ * (a prefix-cache hit) are only read.
+ *   q   : [query_start_loc[num_seqs]][num_q_heads][head_dim] bf16
+ *   out : same shape, fp32; lse (optional) [rows][num_q_heads]
+ *   query_start_loc : int32 [num_seqs + 1], non-decreasing, starting at 0,
+ *                     q_len <= context_lens[s].
+ *   max_q_len : an upper bound of the q_len values (host value).
+ */
+PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                           const int32_t *query_start_loc, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
+                           float scale, pa_stream_t stream);
+
+/*
+ * Merge of attention results over disjoint key ranges (split-KV pieces, or a
+ * shared prefix and a private suffix), by log-sum-exp weighting:
+ *   M = max_p lse_p,  w_p = exp(lse_p - M),
+ *   out = sum_p w_p o_p / sum_p w_p,  lse_out = M + ln sum_p w_p.
+ * Parts with lse = -inf hold no keys and drop out; if all are empty the result
+ * is out = 0, lse_out = -inf.
+ *   part_o   : [num_seqs][num_heads][max_parts][head_dim] fp32 (each o_p
+ *              already normalised by its own softmax sum)
+ *   part_lse : [num_seqs][num_heads][max_parts] fp32, natural log
+ *   num_parts: int32 [num_seqs] parts used by each sequence (each <=
+ *              max_parts), or NULL for max_parts everywhere.
+ *   out      : [num_seqs][num_heads][head_dim] fp32; lse_out optional.
+ *   head_dim : a multiple of 4, at most 512.
+ */
+PA_API pa_status pa_merge_partials(float *out, float *lse_out, const float *part_o,
+                            const float *part_lse, const int32_t *num_parts, int32_t num_seqs,
+                            int32_t num_heads, int32_t max_parts, int32_t head_dim,
+                            pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

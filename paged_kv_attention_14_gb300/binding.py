@@ -1,0 +1,199 @@
+"""Thin Python binding of the C ABI in ``include/pa.h``.
+
+Argument marshalling only: each function takes torch tensors, checks that they
+have the dtype, device and contiguity the C ABI expects, and passes their
+device pointers and the current CUDA stream to the library function of the
+same name.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback.  If ``libpa_gb300.so`` has not been built, loading it
+raises immediately.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa_gb300.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_WORKSPACE = 3
+PA_ERR_CUDA = 4
+
+PA_KV_BF16 = 0
+PA_KV_FP8_E4M3 = 1
+
+PA_DECODE_AUTO = 0
+PA_DECODE_SIMT = 1
+PA_DECODE_MMA = 2
+
+#: every symbol include/pa.h declares
+EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
+            "pa_decode", "pa_prefill_chunk", "pa_merge_partials")
+
+
+class PaKvDesc(ctypes.Structure):
+    """``pa_kv_desc`` of include/pa.h (field order and types must match)."""
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
+        ("decode_impl", ctypes.c_int32),
+    ]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the library (once).  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with paged_kv_attention_14_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        P, I32, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        D = ctypes.POINTER(PaKvDesc)
+        lib.pa_abi_version.argtypes = []
+        lib.pa_abi_version.restype = ctypes.c_int
+        lib.pa_last_error.argtypes = []
+        lib.pa_last_error.restype = ctypes.c_char_p
+        lib.pa_cache_write.argtypes = [D, P, P, P, P, P, I32, P]
+        lib.pa_cache_write.restype = ctypes.c_int
+        lib.pa_decode_workspace_size.argtypes = [D, I32, I32]
+        lib.pa_decode_workspace_size.restype = SZ
+        lib.pa_decode.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P, SZ, P]
+        lib.pa_decode.restype = ctypes.c_int
+        lib.pa_prefill_chunk.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P]
+        lib.pa_prefill_chunk.restype = ctypes.c_int
+        lib.pa_merge_partials.argtypes = [P, P, P, P, P, I32, I32, I32, I32, P]
+        lib.pa_merge_partials.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def make_desc(num_blocks: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
+              kv_dtype: int = PA_KV_BF16, k_scale: float = 0.0, v_scale: float = 0.0,
+              block_size: int = 16, decode_impl: int = PA_DECODE_AUTO) -> PaKvDesc:
+    return PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
+                    k_scale, v_scale, decode_impl)
+
+
+def abi_version() -> int:
+    return load().pa_abi_version()
+
+
+def last_error() -> str:
+    return load().pa_last_error().decode()
+
+
+def _check(status: int):
+    if status != PA_OK:
+        raise PaError(status, last_error())
+
+
+def _ptr(t: Optional[torch.Tensor], dtypes, name: str, allow_none: bool = False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+_CACHE = (torch.bfloat16, torch.uint8, torch.float8_e4m3fn)
+_BF16 = (torch.bfloat16,)
+_F32 = (torch.float32,)
+_I32 = (torch.int32,)
+_I64 = (torch.int64,)
+
+
+def pa_cache_write(desc: PaKvDesc, k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Scatter k, v ``[T, Hkv, D]`` bf16 into the caches at ``slot_mapping`` (int64 [T])."""
+    T = int(slot_mapping.shape[0])
+    _check(load().pa_cache_write(ctypes.byref(desc), _ptr(k, _BF16, "k"), _ptr(v, _BF16, "v"),
+                                 _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                 _ptr(slot_mapping, _I64, "slot_mapping"), T, _stream(stream)))
+
+
+def pa_decode_workspace_size(desc: PaKvDesc, num_seqs: int, max_context_len: int) -> int:
+    n = load().pa_decode_workspace_size(ctypes.byref(desc), int(num_seqs), int(max_context_len))
+    if n == 0 and num_seqs > 0:
+        raise PaError(PA_ERR_UNSUPPORTED, last_error())
+    return int(n)
+
+
+def decode_workspace(desc: PaKvDesc, num_seqs: int, max_context_len: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor of the size pa_decode needs."""
+    n = pa_decode_workspace_size(desc, num_seqs, max_context_len)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_decode(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_lens,
+              max_context_len: int, scale: float, workspace, lse=None, stream=None):
+    """Decode attention: q ``[S, Hq, D]`` bf16 -> out ``[S, Hq, D]`` fp32 (lse ``[S, Hq]``)."""
+    S = int(context_lens.shape[0])
+    _check(load().pa_decode(ctypes.byref(desc), _ptr(out, _F32, "out"),
+                            _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                            _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                            _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
+                            _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
+                            float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
+                            workspace.numel(), _stream(stream)))
+
+
+def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, block_tables,
+                     context_lens, max_q_len: int, max_context_len: int, scale: float, lse=None,
+                     stream=None):
+    """Causal chunked prefill: q ``[Tq, Hq, D]`` bf16 -> out ``[Tq, Hq, D]`` fp32."""
+    S = int(context_lens.shape[0])
+    _check(load().pa_prefill_chunk(ctypes.byref(desc), _ptr(out, _F32, "out"),
+                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                                   _ptr(query_start_loc, _I32, "query_start_loc"),
+                                   _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                   _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
+                                   _ptr(context_lens, _I32, "context_lens"), S, int(max_q_len),
+                                   int(max_context_len), float(scale), _stream(stream)))
+
+
+def pa_merge_partials(out, part_o, part_lse, num_parts=None, lse_out=None, stream=None):
+    """Merge part_o ``[S, H, P, D]`` / part_lse ``[S, H, P]`` into out ``[S, H, D]``."""
+    S, H, P, D = (int(x) for x in part_o.shape)
+    _check(load().pa_merge_partials(_ptr(out, _F32, "out"), _ptr(lse_out, _F32, "lse_out", allow_none=True),
+                                    _ptr(part_o, _F32, "part_o"), _ptr(part_lse, _F32, "part_lse"),
+                                    _ptr(num_parts, _I32, "num_parts", allow_none=True), S, H, P, D,
+                                    _stream(stream)))

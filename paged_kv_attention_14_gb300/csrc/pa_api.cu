@@ -1,0 +1,183 @@
+// pa_api.cu -- the extern "C" entry points declared in include/pa.h.
+//
+// Host-side argument checks (nothing is enqueued when one fails), the
+// thread-local error string, workspace sizing and dispatch to the kernels.
+// The conventions -- flat, exception-free functions, a status code plus a
+// last-error string, a runtime ABI version, structs that only grow by
+// appending fields -- follow the pages' own "Library API (C ABI)" section of
+// the vllm.cpp README.
+#include <stdio.h>
+#include <string.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+pa_status fail(pa_status st, const char *fmt, const char *detail = nullptr) {
+  snprintf(g_last_error, sizeof g_last_error, fmt, detail ? detail : "");
+  return st;
+}
+
+pa_status ok() {
+  g_last_error[0] = '\0';
+  return PA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status check_desc(const pa_kv_desc *d) {
+  if (!d) return fail(PA_ERR_INVALID_ARG, "desc is NULL%s");
+  if (d->block_size != 16) return fail(PA_ERR_UNSUPPORTED, "block_size must be 16%s");
+  if (d->head_dim != 64 && d->head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128%s");
+  if (d->num_kv_heads <= 0 || d->num_q_heads <= 0)
+    return fail(PA_ERR_INVALID_ARG, "num_kv_heads and num_q_heads must be positive%s");
+  if (d->num_q_heads % d->num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads%s");
+  if (d->num_q_heads / d->num_kv_heads > 16)
+    return fail(PA_ERR_UNSUPPORTED, "group size num_q_heads / num_kv_heads must be <= 16%s");
+  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARG, "kv_dtype must be PA_KV_BF16 or PA_KV_FP8_E4M3%s");
+  if (d->num_blocks < 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be >= 0%s");
+  if (d->kv_dtype == PA_KV_FP8_E4M3 && (!(d->k_scale >= 0.f) || !(d->v_scale >= 0.f)))
+    return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be >= 0 (0 means 1)%s");
+  return PA_OK;
+}
+
+pa_status cuda_fail(cudaError_t e) {
+  return fail(PA_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_abi_version(void) { return PA_ABI_VERSION; }
+
+const char *pa_last_error(void) { return g_last_error; }
+
+pa_status pa_cache_write(const pa_kv_desc *desc, const void *k, const void *v, void *k_cache,
+                         void *v_cache, const int64_t *slot_mapping, int32_t num_tokens,
+                         pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "num_tokens must be >= 0%s");
+  if (num_tokens == 0) return ok();
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "k, v, k_cache, v_cache and slot_mapping must be non-NULL%s");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "k, v, k_cache and v_cache must be 16-byte aligned%s");
+  if (!aligned16(slot_mapping) && (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return fail(PA_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned%s");
+  const cudaError_t e = pa::launch_cache_write(*desc, k, v, k_cache, v_cache, slot_mapping,
+                                               num_tokens, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+size_t pa_decode_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_context_len) {
+  (void)max_context_len;
+  if (check_desc(desc) != PA_OK || num_seqs < 0) return 0;
+  pa::DecodePlan plan;
+  const char *why = "";
+  if (pa::plan_decode(*desc, num_seqs, &plan, &why) != PA_OK) {
+    fail(PA_ERR_UNSUPPORTED, "%s", why);
+    return 0;
+  }
+  return plan.workspace_bytes;
+}
+
+pa_status pa_decode(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                    const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                    int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                    pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0%s");
+  if (num_seqs == 0) return ok();
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, q, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "block_tables, context_lens and lse must be 4-byte aligned%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
+  pa::DecodePlan plan;
+  const char *why = "";
+  st = pa::plan_decode(*desc, num_seqs, &plan, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
+  if (workspace_bytes < plan.workspace_bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_decode_workspace_size()%s");
+  const cudaError_t e = pa::launch_decode(*desc, plan, out, lse, q, k_cache, v_cache, block_tables,
+                                          max_blocks_per_seq, context_lens, num_seqs, scale,
+                                          workspace, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                           const int32_t *query_start_loc, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
+                           float scale, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and max_q_len must be >= 0%s");
+  if (num_seqs == 0 || max_q_len == 0) return ok();
+  if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, q, query_start_loc, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG,
+                "block_tables, context_lens, query_start_loc and lse must be 4-byte aligned%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
+  const char *why = "";
+  st = pa::check_prefill(*desc, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  const cudaError_t e = pa::launch_prefill(*desc, out, lse, q, query_start_loc, k_cache, v_cache,
+                                           block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                           max_q_len, scale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_merge_partials(float *out, float *lse_out, const float *part_o,
+                            const float *part_lse, const int32_t *num_parts, int32_t num_seqs,
+                            int32_t num_heads, int32_t max_parts, int32_t head_dim,
+                            pa_stream_t stream) {
+  if (num_seqs < 0 || num_heads <= 0 || max_parts < 0)
+    return fail(PA_ERR_INVALID_ARG, "num_seqs >= 0, num_heads > 0 and max_parts >= 0 required%s");
+  if (head_dim <= 0 || head_dim % 4 != 0 || head_dim > 512)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim must be a positive multiple of 4, at most 512%s");
+  if (num_seqs == 0) return ok();
+  if (!out || (max_parts > 0 && (!part_o || !part_lse)))
+    return fail(PA_ERR_INVALID_ARG, "out, part_o and part_lse must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(part_o))
+    return fail(PA_ERR_INVALID_ARG, "out and part_o must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(part_lse) & 3u) || (reinterpret_cast<uintptr_t>(lse_out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(num_parts) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "part_lse, lse_out and num_parts must be 4-byte aligned%s");
+  if (static_cast<int64_t>(num_seqs) * num_heads > 0x7fffffff)
+    return fail(PA_ERR_UNSUPPORTED, "num_seqs * num_heads exceeds the grid limit%s");
+  const cudaError_t e = pa::launch_merge(out, lse_out, part_o, part_lse, num_parts, num_seqs,
+                                         num_heads, max_parts, head_dim,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// pa_cache_write.cu -- slot-mapped write of new K/V rows into the paged cache.
+//
+// The engine writes each new token's K/V into the physical block slot that
+// the scheduler assigned to it (an indexed scatter through a slot mapping:
+// "Block-Paged KV Cache (FP8/FP16)" in the architecture figure of "Building
+// and Deploying vllm.cpp ...", and the device-resident indexed gather/scatter
+// of the vllm.cpp status notes).  FP8 pages hold one byte per element
+// ("2. CLI Configuration Parameters", --kv-cache-dtype fp8).
+//
+// One thread moves 16 source bytes (8 bf16 values) of one (token, kv head)
+// row: a warp covers two 256-byte rows (head_dim 128), so loads and stores
+// are 16-byte vectorised and coalesced.  Negative slots are skipped.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int KVT>
+__global__ void __launch_bounds__(256) cache_write_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint8_t *__restrict__ k_cache,
+    uint8_t *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_vecs,
+    int vecs_per_row, int num_kv_heads, int block_size, float k_scale, float v_scale) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= total_vecs) return;
+  const int vec = static_cast<int>(i % vecs_per_row);
+  const int64_t row = i / vecs_per_row;  // token * num_kv_heads + head
+  const int64_t token = row / num_kv_heads;
+  const int head = static_cast<int>(row % num_kv_heads);
+  const int64_t slot = __ldg(slot_mapping + token);
+  if (slot < 0) return;
+  const int64_t blk = slot / block_size;
+  const int64_t off = slot % block_size;
+  // destination row (blk, head, off) of [num_blocks][num_kv_heads][block_size][D]
+  const int64_t dst_row = (blk * num_kv_heads + head) * block_size + off;
+  const uint4 kv = __ldg(k + i);
+  const uint4 vv = __ldg(v + i);
+  if (KVT == kKvBf16) {
+    reinterpret_cast<uint4 *>(k_cache)[dst_row * vecs_per_row + vec] = kv;
+    reinterpret_cast<uint4 *>(v_cache)[dst_row * vecs_per_row + vec] = vv;
+  } else {
+    // x / scale in correctly rounded fp32 division, then E4M3 RNE-satfinite
+    auto enc = [](const uint4 &u, float s) {
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint16_t b[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        b[j] = pack_e4m3x2_satfinite(__fdiv_rn(bf16lo(w[j]), s), __fdiv_rn(bf16hi(w[j]), s));
+      uint2 r;
+      r.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
+      r.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
+      return r;
+    };
+    reinterpret_cast<uint2 *>(k_cache)[dst_row * vecs_per_row + vec] = enc(kv, k_scale);
+    reinterpret_cast<uint2 *>(v_cache)[dst_row * vecs_per_row + vec] = enc(vv, v_scale);
+  }
+}
+
+cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v, void *k_cache,
+                               void *v_cache, const int64_t *slot_mapping, int32_t num_tokens,
+                               cudaStream_t stream) {
+  const int vecs_per_row = d.head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * d.num_kv_heads * vecs_per_row;
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  const float ks = d.k_scale == 0.f ? 1.f : d.k_scale;
+  const float vs = d.v_scale == 0.f ? 1.f : d.v_scale;
+  if (d.kv_dtype == PA_KV_BF16)
+    cache_write_kernel<kKvBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+  else
+    cache_write_kernel<kKvFp8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,48 @@
+// pa_internal.h -- launchers shared between the C-ABI layer and the kernels.
+// Every launcher enqueues on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v, void *k_cache,
+                               void *v_cache, const int64_t *slot_mapping, int32_t num_tokens,
+                               cudaStream_t stream);
+
+cudaError_t launch_merge(float *out, float *lse_out, const float *part_o, const float *part_lse,
+                         const int32_t *num_parts, int32_t num_seqs, int32_t num_heads,
+                         int32_t max_parts, int32_t head_dim, cudaStream_t stream);
+
+// Decode: which kernel variant runs and how many persistent CTAs it uses.
+struct DecodePlan {
+  int impl;       // PA_DECODE_SIMT or PA_DECODE_MMA
+  int group_pad;  // group size rounded up to the kernel's instantiation
+  int num_ctas;   // persistent grid size
+  size_t workspace_bytes;
+};
+
+// Fills `plan` for the descriptor; returns PA_OK or an error with a message.
+pa_status plan_decode(const pa_kv_desc &d, int32_t num_seqs, DecodePlan *plan, const char **why);
+
+cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse,
+                          const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, float scale,
+                          void *workspace, cudaStream_t stream);
+
+pa_status check_prefill(const pa_kv_desc &d, const char **why);
+
+cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const void *q,
+                           const int32_t *query_start_loc, const void *k_cache,
+                           const void *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace pa

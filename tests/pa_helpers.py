@@ -1,0 +1,131 @@
+"""Shared helpers of the GPU tests: run the CUDA library through its C ABI and
+the fp64 oracle on the same seeded inputs.  Nothing here computes attention:
+the expected values come from ``oracle`` only."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_attention_14_gb300 import binding as B
+from paged_kv_attention_14_gb300 import workloads as W
+
+#: max-abs tolerance of fp32 outputs against the fp64 oracle (bf16 KV, FP8 KV)
+TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2}
+#: tolerance of the natural-log log-sum-exp outputs
+LSE_TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2}
+
+
+def kv_code(b: W.PagedBatch) -> int:
+    return B.PA_KV_BF16 if b.kv_dtype == W.KV_BF16 else B.PA_KV_FP8_E4M3
+
+
+def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO) -> B.PaKvDesc:
+    return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
+                       b.k_scale if b.kv_dtype == W.KV_FP8 else 0.0,
+                       b.v_scale if b.kv_dtype == W.KV_FP8 else 0.0, decode_impl=decode_impl)
+
+
+def gpu_caches(b: W.PagedBatch):
+    """The caches as the CUDA path holds them: the bf16 pool itself, or the
+    E4M3 pool written by the library's own cache write."""
+    if b.kv_dtype == W.KV_BF16:
+        return b.k_pool, b.v_pool
+    k, v, slots = b.pool_tokens_as_rows()
+    kc = torch.zeros(tuple(b.k_pool.shape), dtype=torch.uint8, device=b.k_pool.device)
+    vc = torch.zeros_like(kc)
+    B.pa_cache_write(desc_of(b), k, v, kc, vc, slots)
+    return kc, vc
+
+
+def oracle_caches(b: W.PagedBatch):
+    """The caches as the oracle sees them (CPU numpy): the bf16 pool, or the
+    oracle's own E4M3 encoding of it."""
+    if b.kv_dtype == W.KV_BF16:
+        return oracle.KV_BF16, b.k_pool.cpu(), b.v_pool.cpu()
+    k, v, slots = b.pool_tokens_as_rows()
+    z = np.zeros(tuple(b.k_pool.shape), np.uint8)
+    kc, vc = oracle.cache_write(oracle.KV_FP8_E4M3, b.block_size, b.num_kv_heads, b.head_dim,
+                                k.cpu(), v.cpu(), slots.cpu(), z, z, b.k_scale, b.v_scale)
+    return oracle.KV_FP8_E4M3, kc, vc
+
+
+def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO, workspace=None):
+    kc, vc = caches if caches is not None else gpu_caches(b)
+    S = b.context_lens_decode.shape[0]
+    out = torch.full((S, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
+    lse = torch.full((S, b.num_q_heads), float("nan"), device=kc.device)
+    d = desc_of(b, decode_impl)
+    maxL = b.max_context_len_decode()
+    ws = workspace if workspace is not None else B.decode_workspace(d, S, maxL, kc.device)
+    B.pa_decode(d, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale, ws,
+                lse=lse)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32)[0]) == 0, "decode kernel reported a wait timeout"
+    return out, lse
+
+
+def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None):
+    kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
+    return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode.cpu(), kc, vc,
+                         b.block_tables_decode.cpu(), b.context_lens_decode.cpu(), b.scale, b.k_scale,
+                         b.v_scale, pairs=pairs)
+
+
+def gpu_prefill(b: W.PagedBatch, caches=None):
+    kc, vc = caches if caches is not None else gpu_caches(b)
+    Tq = b.q_prefill.shape[0]
+    out = torch.full((Tq, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
+    lse = torch.full((Tq, b.num_q_heads), float("nan"), device=kc.device)
+    qsl = b.query_start_loc
+    max_q = int((qsl[1:] - qsl[:-1]).max())
+    maxL = int(b.context_lens_prefill.max())
+    B.pa_prefill_chunk(desc_of(b), out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill,
+                       b.context_lens_prefill, max_q, maxL, b.scale, lse=lse)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None):
+    kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
+    return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill.cpu(),
+                          b.query_start_loc.cpu(), kc, vc, b.block_tables_prefill.cpu(),
+                          b.context_lens_prefill.cpu(), b.scale, b.k_scale, b.v_scale, pairs=pairs)
+
+
+def assert_close(got: torch.Tensor, want: np.ndarray, tol: float, what: str = ""):
+    g = got.detach().double().cpu().numpy().reshape(want.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output"
+    err = np.abs(g - want)
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= tol, f"{what}: max abs err {worst:.3e} > {tol:.1e} at {np.unravel_index(err.argmax(), err.shape)}"
+    return worst
+
+
+def compact_decode_batch(b: W.PagedBatch, seqs) -> W.PagedBatch:
+    """The sub-batch of sequences ``seqs`` with only their blocks, renumbered:
+    same values and same attention result, small enough for the oracle's
+    E4M3 encoder.  Built from the generator's tensors (not from GPU results)."""
+    seqs = list(seqs)
+    lens = b.context_lens_decode[seqs].cpu()
+    tables = b.block_tables_decode[seqs].cpu()
+    used = []
+    for i, L in enumerate(lens.tolist()):
+        used += tables[i, :(L + 15) // 16].tolist()
+    uniq = sorted(set(used))
+    remap = {blk: j for j, blk in enumerate(uniq)}
+    new_t = torch.full_like(tables, -1)
+    for i, L in enumerate(lens.tolist()):
+        nb = (L + 15) // 16
+        new_t[i, :nb] = torch.tensor([remap[x] for x in tables[i, :nb].tolist()], dtype=torch.int32)
+    idx = torch.tensor(uniq, dtype=torch.int64, device=b.k_pool.device)
+    c = W.PagedBatch(name=b.name + " (subset)", block_size=b.block_size, num_q_heads=b.num_q_heads,
+                     num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, kv_dtype=b.kv_dtype, scale=b.scale,
+                     k_scale=b.k_scale, v_scale=b.v_scale, num_blocks=len(uniq),
+                     k_pool=b.k_pool[idx].contiguous(), v_pool=b.v_pool[idx].contiguous())
+    c.q_decode = b.q_decode[seqs].contiguous()
+    c.block_tables_decode = new_t.to(b.k_pool.device)
+    c.context_lens_decode = lens.to(b.k_pool.device)
+    return c

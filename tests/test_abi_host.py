@@ -1,0 +1,170 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every function include/pa.h declares, and rejects bad arguments before any
+CUDA call.  No GPU is needed (no compute entry point reaches a launch here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_kv_attention_14_gb300 import build as pa_build
+from paged_kv_attention_14_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = pa_build.build()
+    return B.load(path)
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_entry_points():
+    names = _declared_functions()
+    for want in ("pa_cache_write", "pa_decode", "pa_prefill_chunk", "pa_merge_partials"):
+        assert want in names
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(pa_[a-z_0-9]+)$", out, flags=re.M))
+    declared = set(_declared_functions())
+    assert declared <= exported, declared - exported
+    # nothing else leaks out of the library under the pa_ prefix
+    assert exported == declared
+
+
+def test_abi_version(lib):
+    assert lib.pa_abi_version() == 1
+    m = re.search(r"#define\s+PA_ABI_VERSION\s+(\d+)", open(HEADER).read())
+    assert int(m.group(1)) == lib.pa_abi_version()
+
+
+def test_desc_struct_matches_header_layout():
+    # field order of pa_kv_desc in the header
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} pa_kv_desc;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b(\w+);", body)
+    assert fields == [f for f, _ in B.PaKvDesc._fields_]
+    assert ctypes.sizeof(B.PaKvDesc) == 36
+
+
+def _desc(**kw):
+    d = dict(num_blocks=64, num_kv_heads=2, num_q_heads=4, head_dim=64)
+    d.update(kw)
+    return B.make_desc(**d)
+
+
+def test_cache_write_argument_errors(lib):
+    null = None
+    d = _desc()
+    # NULL descriptor
+    assert lib.pa_cache_write(None, null, null, null, null, null, 4, null) == B.PA_ERR_INVALID_ARG
+    assert "desc" in B.last_error()
+    # zero tokens is a no-op
+    assert lib.pa_cache_write(ctypes.byref(d), null, null, null, null, null, 0, null) == B.PA_OK
+    assert B.last_error() == ""
+    # NULL pointers
+    assert lib.pa_cache_write(ctypes.byref(d), null, null, null, null, null, 4, null) == B.PA_ERR_INVALID_ARG
+    # misaligned
+    assert lib.pa_cache_write(ctypes.byref(d), 0x1008, 0x2000, 0x3000, 0x4000, 0x5000, 4, null) == B.PA_ERR_INVALID_ARG
+    assert "aligned" in B.last_error()
+    # negative count
+    assert lib.pa_cache_write(ctypes.byref(d), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, -1, null) == B.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("block_size", 32, B.PA_ERR_UNSUPPORTED),
+    ("head_dim", 96, B.PA_ERR_UNSUPPORTED),
+    ("num_q_heads", 5, B.PA_ERR_INVALID_ARG),     # not a multiple of 2 kv heads
+    ("num_kv_heads", 0, B.PA_ERR_INVALID_ARG),
+    ("num_q_heads", 34, B.PA_ERR_UNSUPPORTED),    # group size 17
+    ("kv_dtype", 7, B.PA_ERR_INVALID_ARG),
+    ("num_blocks", -1, B.PA_ERR_INVALID_ARG),
+])
+def test_descriptor_validation(lib, field, value, status):
+    d = _desc()
+    setattr(d, field, value)
+    if field == "num_q_heads" and value == 34:
+        d.num_kv_heads = 2
+    got = lib.pa_decode(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 16,
+                        0.125, 0x7000, 1 << 20, None)
+    assert got == status, B.last_error()
+    assert B.last_error() != ""
+
+
+def test_fp8_scales_must_be_non_negative(lib):
+    d = _desc(kv_dtype=B.PA_KV_FP8_E4M3, k_scale=-1.0)
+    assert lib.pa_cache_write(ctypes.byref(d), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, None) == B.PA_ERR_INVALID_ARG
+    d = _desc(kv_dtype=B.PA_KV_FP8_E4M3, k_scale=float("nan"))
+    assert lib.pa_cache_write(ctypes.byref(d), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, None) == B.PA_ERR_INVALID_ARG
+
+
+def test_decode_argument_errors(lib):
+    d = _desc()
+    ok_ptrs = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000)
+    # zero sequences: nothing to do
+    assert lib.pa_decode(ctypes.byref(d), *ok_ptrs, 4, 0x6000, 0, 16, 0.1, None, 0, None) == B.PA_OK
+    # NULL out
+    assert lib.pa_decode(ctypes.byref(d), None, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 16, 0.1,
+                         0x7000, 1 << 20, None) == B.PA_ERR_INVALID_ARG
+    # max_context_len beyond the table
+    assert lib.pa_decode(ctypes.byref(d), *ok_ptrs, 4, 0x6000, 2, 65, 0.1, 0x7000, 1 << 20,
+                         None) == B.PA_ERR_INVALID_ARG
+    # NaN scale
+    assert lib.pa_decode(ctypes.byref(d), *ok_ptrs, 4, 0x6000, 2, 16, float("nan"), 0x7000, 1 << 20,
+                         None) == B.PA_ERR_INVALID_ARG
+    # misaligned block table
+    assert lib.pa_decode(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5002, 4, 0x6000, 2, 16, 0.1,
+                         0x7000, 1 << 20, None) == B.PA_ERR_INVALID_ARG
+    # unknown decode kernel
+    d2 = _desc(decode_impl=9)
+    assert lib.pa_decode(ctypes.byref(d2), *ok_ptrs, 4, 0x6000, 2, 16, 0.1, 0x7000, 1 << 20,
+                         None) == B.PA_ERR_INVALID_ARG
+
+
+def test_prefill_argument_errors(lib):
+    d = _desc()
+    args = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000)
+    assert lib.pa_prefill_chunk(ctypes.byref(d), *args, 0, 8, 16, 0.1, None) == B.PA_OK
+    assert lib.pa_prefill_chunk(ctypes.byref(d), None, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000,
+                                2, 8, 16, 0.1, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_prefill_chunk(ctypes.byref(d), *args, 2, 8, 100, 0.1, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_prefill_chunk(ctypes.byref(d), 0x1004, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000,
+                                2, 8, 16, 0.1, None) == B.PA_ERR_INVALID_ARG
+
+
+def test_merge_argument_errors(lib):
+    assert lib.pa_merge_partials(0x1000, None, 0x2000, 0x3000, None, 0, 4, 2, 64, None) == B.PA_OK
+    assert lib.pa_merge_partials(0x1000, None, 0x2000, 0x3000, None, 2, 4, 2, 66, None) == B.PA_ERR_UNSUPPORTED
+    assert lib.pa_merge_partials(None, None, 0x2000, 0x3000, None, 2, 4, 2, 64, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_merge_partials(0x1000, None, 0x2000, 0x3000, None, 2, 0, 2, 64, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_merge_partials(0x1000, None, 0x2008, 0x3000, None, 2, 4, 2, 64, None) == B.PA_ERR_INVALID_ARG
+
+
+def test_last_error_is_per_thread(lib):
+    import threading
+    assert lib.pa_cache_write(None, None, None, None, None, None, 1, None) == B.PA_ERR_INVALID_ARG
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(B.last_error()))
+    t.start()
+    t.join()
+    assert seen == [""]
+    assert B.last_error() != ""
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        B.load(str(tmp_path / "nope.so"))

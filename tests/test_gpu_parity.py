@@ -1,0 +1,355 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bars: cache writes and block indexing bit-exact; fp32 attention outputs within
+max-abs 2e-3 of the oracle for bf16 KV and 2e-2 for E4M3 KV.  Every input is
+seeded and synthetic; pool slots that no sequence may read hold NaN, so a
+stray read shows up as a non-finite output.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_attention_14_gb300 import binding as B
+from paged_kv_attention_14_gb300 import workloads as W
+from pa_helpers import (TOL, LSE_TOL, assert_close, compact_decode_batch, desc_of, gpu_caches, gpu_decode,
+                        gpu_prefill, oracle_caches, oracle_decode, oracle_prefill)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_attention_14_gb300 import build
+    B.load(build.build())
+
+
+# ------------------------------------------------------------------ cache write
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def test_cache_write_bf16_bit_exact_on_mixed_step():
+    b = W.workload(5, device=DEV, poison=True)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(desc_of(b), b.k_new, b.v_new, kc, vc, b.slot_mapping)
+    torch.cuda.synchronize()
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, b.num_kv_heads, b.head_dim, b.k_new.cpu(), b.v_new.cpu(),
+                                b.slot_mapping.cpu(), b.k_pool.cpu(), b.v_pool.cpu())
+    assert np.array_equal(_bits(kc), ok) and np.array_equal(_bits(vc), ov)
+
+
+def _adversarial_bf16(n_random, g):
+    special = [1.0625, -1.0625, 1.1875, 464.0, -464.0, 480.0, 1e30, -1e30, float("inf"), float("-inf"),
+               2.0 ** -10, 3 * 2.0 ** -10, -2.0 ** -10, 2.0 ** -12, 0.0, -0.0, float("nan"), 448.0, 449.0,
+               2.0 ** -6, 2.0 ** -7 * 1.5, 240.0, 248.0, 232.0]
+    x = torch.randn(n_random, generator=g) * 3
+    return torch.cat([torch.tensor(special), x]).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.0123, 3.5])
+def test_cache_write_fp8_bit_exact_with_ties_saturation_and_nan(scale):
+    g = torch.Generator().manual_seed(7)
+    H, D = 2, 64
+    vals = _adversarial_bf16(H * D * 40, g)
+    T = vals.numel() // (H * D)
+    k = vals[: T * H * D].reshape(T, H, D)
+    v = k.flip(0).contiguous()
+    NB = (T + 15) // 16 + 3
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
+    slots[5] = -1
+    d = B.make_desc(NB, H, 2 * H, D, B.PA_KV_FP8_E4M3, scale, scale * 2)
+    kc = torch.full((NB, H, 16, D), 0xAB, dtype=torch.uint8, device=DEV)
+    vc = kc.clone()
+    B.pa_cache_write(d, k.to(DEV), v.to(DEV), kc, vc, slots.to(DEV))
+    torch.cuda.synchronize()
+    z = np.full((NB, H, 16, D), 0xAB, np.uint8)
+    ok, ov = oracle.cache_write(oracle.KV_FP8_E4M3, 16, H, D, k, v, slots, z, z, scale, scale * 2)
+    assert np.array_equal(kc.cpu().numpy(), ok), np.argwhere(kc.cpu().numpy() != ok)[:5]
+    assert np.array_equal(vc.cpu().numpy(), ov)
+
+
+def test_cache_write_fp8_bit_exact_on_fp8_workload_rows():
+    b = W.workload(4, device=DEV, poison=False)
+    # 4096 rows of the workload's source values, written at random slots
+    k, v, _ = b.pool_tokens_as_rows()
+    rows = torch.randperm(k.shape[0], generator=torch.Generator().manual_seed(3))[:4096].to(DEV)
+    k, v = k[rows].contiguous(), v[rows].contiguous()
+    NB = 300
+    slots = torch.randperm(NB * 16, generator=torch.Generator().manual_seed(4))[:4096].to(torch.int64)
+    d = B.make_desc(NB, 8, 40, 128, B.PA_KV_FP8_E4M3, b.k_scale, b.v_scale)
+    kc = torch.zeros((NB, 8, 16, 128), dtype=torch.uint8, device=DEV)
+    vc = torch.zeros_like(kc)
+    B.pa_cache_write(d, k, v, kc, vc, slots.to(DEV))
+    torch.cuda.synchronize()
+    z = np.zeros((NB, 8, 16, 128), np.uint8)
+    ok, ov = oracle.cache_write(oracle.KV_FP8_E4M3, 16, 8, 128, k.cpu(), v.cpu(), slots, z, z, b.k_scale, b.v_scale)
+    assert np.array_equal(kc.cpu().numpy(), ok) and np.array_equal(vc.cpu().numpy(), ov)
+
+
+# ---------------------------------------------------------------------- decode
+
+def _check_decode(b, impl=B.PA_DECODE_AUTO, pairs=None, caches=None, ocaches=None):
+    out, lse = gpu_decode(b, caches=caches, decode_impl=impl)
+    o_ref, l_ref = oracle_decode(b, ocaches=ocaches, pairs=pairs)
+    if pairs is not None:
+        idx = torch.tensor([s * b.num_q_heads + h for s, h in pairs])
+        out = out.reshape(-1, b.head_dim)[idx]
+        lse = lse.reshape(-1)[idx]
+    e = assert_close(out, o_ref, TOL[b.kv_dtype], "out")
+    assert_close(lse, l_ref, LSE_TOL[b.kv_dtype], "lse")
+    return e
+
+
+IMPLS = [B.PA_DECODE_SIMT, B.PA_DECODE_MMA]
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_decode_matches_oracle_on_workload(n, impl):
+    b = W.workload(n, device=DEV, poison=True)
+    _check_decode(b, impl=impl)
+
+
+def test_decode_matches_oracle_on_fp8_workload_subset():
+    b = W.workload(4, device=DEV, poison=True)
+    caches = gpu_caches(b)
+    out, lse = gpu_decode(b, caches=caches)
+    seqs = [0, 17, 63, 127] + [int(torch.argmax(b.context_lens_decode))]
+    sub = compact_decode_batch(b, seqs)
+    o_ref, l_ref = oracle_decode(sub)
+    assert_close(out[seqs], o_ref, TOL[W.KV_FP8], "out")
+    assert_close(lse[seqs], l_ref, LSE_TOL[W.KV_FP8], "lse")
+    # the GPU's E4M3 cache of those sequences' blocks equals the oracle's encoding
+    tables = b.block_tables_decode[seqs].cpu()
+    lens = b.context_lens_decode[seqs].cpu()
+    blocks = sorted({int(x) for i, L in enumerate(lens.tolist()) for x in tables[i, :(L + 15) // 16]})
+    _, okc, ovc = oracle_caches(sub)
+    assert np.array_equal(caches[0][blocks].cpu().numpy(), okc)
+    assert np.array_equal(caches[1][blocks].cpu().numpy(), ovc)
+
+
+CASES = [
+    # (D, Hq, Hkv, kv dtype, lengths)
+    (64, 4, 2, W.KV_BF16, [1, 7, 16, 33]),
+    (128, 8, 2, W.KV_BF16, [1, 15, 16, 17, 100, 1000, 2049]),
+    (128, 3, 1, W.KV_BF16, [5, 64, 300]),
+    (64, 1, 1, W.KV_BF16, [1, 2, 31, 500]),
+    (128, 16, 16, W.KV_BF16, [40, 41, 700]),
+    (128, 10, 2, W.KV_BF16, [1, 17, 333]),
+    (128, 16, 1, W.KV_BF16, [9, 250, 1031]),
+    (64, 12, 1, W.KV_BF16, [3, 77]),
+    (64, 4, 2, W.KV_FP8, [1, 7, 16, 33, 250]),
+    (128, 8, 2, W.KV_FP8, [1, 15, 17, 1000, 1600]),
+    (128, 2, 1, W.KV_FP8, [3, 129]),
+    (128, 40, 8, W.KV_FP8, [1, 100, 1025]),
+    (64, 12, 1, W.KV_FP8, [5, 300]),
+    (128, 16, 1, W.KV_FP8, [64, 65]),
+]
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("D,Hq,Hkv,kv,lens", CASES)
+def test_decode_random_shapes(D, Hq, Hkv, kv, lens, impl):
+    if impl == B.PA_DECODE_SIMT and Hq // Hkv > 4:
+        pytest.skip("the CUDA-core kernel takes group sizes up to 4")
+    b = W.random_decode(100 + D + Hq + len(lens), lens, Hq, Hkv, D, kv_dtype=kv, device=DEV, poison=True)
+    _check_decode(b, impl=impl)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_many_short_sequences_cross_cta_boundaries(impl):
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(1, 200, (300,), generator=g).tolist()
+    b = W.random_decode(77, lens, 8, 2, 128, device=DEV, poison=True)
+    _check_decode(b, impl=impl)
+
+
+def test_simt_and_mma_decode_agree():
+    b = W.workload(2, device=DEV, poison=True)
+    o1, l1 = gpu_decode(b, decode_impl=B.PA_DECODE_SIMT)
+    o2, l2 = gpu_decode(b, decode_impl=B.PA_DECODE_MMA)
+    assert (o1 - o2).abs().max().item() < 1e-3
+    assert (l1 - l2).abs().max().item() < 1e-3
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_context_length_one_returns_v_bit_exactly(impl):
+    b = W.workload(1, device=DEV, poison=True)
+    out, _ = gpu_decode(b, decode_impl=impl)
+    blk = int(b.block_tables_decode[0, 0])
+    for h in range(4):
+        v0 = b.v_pool[blk, h // 2, 0].float()
+        assert torch.equal(out[0, h], v0)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_empty_sequence_gives_zeros_and_minus_inf(impl):
+    b = W.random_decode(88, [9, 1, 40], 4, 2, 64, device=DEV, poison=True)
+    b.context_lens_decode = torch.tensor([9, 0, 40], dtype=torch.int32, device=DEV)
+    out, lse = gpu_decode(b, decode_impl=impl)
+    assert torch.all(out[1] == 0) and torch.all(lse[1] == -math.inf)
+    o_ref, l_ref = oracle_decode(b)
+    keep = [0, 1, 2, 3, 8, 9, 10, 11]
+    assert_close(out.reshape(-1, 64)[keep], o_ref[keep], TOL[W.KV_BF16])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_is_bit_identical_under_physical_block_permutation(impl):
+    b = W.workload(3, device=DEV, poison=True)
+    out1, lse1 = gpu_decode(b, decode_impl=impl)
+    perm = torch.randperm(b.num_blocks, generator=torch.Generator().manual_seed(9)).to(DEV)
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(b.num_blocks, device=DEV)
+    b.k_pool = b.k_pool[inv].contiguous()
+    b.v_pool = b.v_pool[inv].contiguous()
+    t = b.block_tables_decode.long()
+    b.block_tables_decode = torch.where(t >= 0, perm[t.clamp(min=0)], t).to(torch.int32)
+    out2, lse2 = gpu_decode(b, decode_impl=impl)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_decode_is_deterministic_and_workspace_reusable():
+    b = W.workload(3, device=DEV, poison=True)
+    d = desc_of(b)
+    ws = B.decode_workspace(d, b.context_lens_decode.shape[0], b.max_context_len_decode(), DEV)
+    o1, l1 = gpu_decode(b, workspace=ws)
+    # error word and merge counters (the first int32s) are back at zero
+    S, Hkv = b.context_lens_decode.shape[0], b.num_kv_heads
+    head = ws[: 256 + 4 * S * Hkv].view(torch.int32)
+    assert torch.count_nonzero(head) == 0, "error word and merge counters must be left zeroed"
+    o2, l2 = gpu_decode(b, workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_workspace_too_small_is_rejected():
+    b = W.workload(1, device=DEV)
+    d = desc_of(b)
+    n = B.pa_decode_workspace_size(d, 4, 33)
+    ws = torch.zeros(n - 256, dtype=torch.uint8, device=DEV)
+    out = torch.empty(4, 4, 64, device=DEV)
+    with pytest.raises(B.PaError) as ei:
+        B.pa_decode(d, out, b.q_decode, b.k_pool, b.v_pool, b.block_tables_decode, b.context_lens_decode, 33,
+                    b.scale, ws)
+    assert ei.value.status == B.PA_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------- merge
+
+def test_merge_partials_matches_oracle():
+    g = torch.Generator().manual_seed(11)
+    S, H, P, D = 5, 6, 7, 128
+    po = torch.randn(S, H, P, D, generator=g, dtype=torch.float32)
+    pl = torch.randn(S, H, P, generator=g, dtype=torch.float32) * 5
+    pl[0, 0, 3] = -math.inf
+    pl[1, 2, :] = -math.inf
+    nparts = torch.tensor([7, 3, 1, 0, 5], dtype=torch.int32)
+    out = torch.full((S, H, D), float("nan"), device=DEV)
+    lse = torch.full((S, H), float("nan"), device=DEV)
+    B.pa_merge_partials(out, po.to(DEV), pl.to(DEV), num_parts=nparts.to(DEV), lse_out=lse)
+    torch.cuda.synchronize()
+    for s in range(S):
+        for h in range(H):
+            n = int(nparts[s])
+            ro, rl = oracle.merge(po[s, h, :n].double().numpy().reshape(n, D), pl[s, h, :n].double().numpy())
+            if n == 0 or rl == -math.inf:
+                assert torch.all(out[s, h] == 0) and lse[s, h] == -math.inf
+            else:
+                assert_close(out[s, h], ro, 1e-5)
+                assert abs(float(lse[s, h]) - rl) < 1e-5
+
+
+def test_merge_of_gpu_split_decode_equals_unsplit():
+    """Two half-range decodes merged by pa_merge_partials equal the full decode."""
+    b = W.random_decode(55, [300, 161], 4, 2, 128, device=DEV, poison=True)
+    full, lfull = gpu_decode(b)
+    kc, vc = b.k_pool, b.v_pool
+    # first part: the first 160 tokens (ten whole blocks) of each sequence
+    first = W.random_decode(55, [300, 161], 4, 2, 128, device=DEV, poison=True)
+    first.context_lens_decode = torch.tensor([160, 160], dtype=torch.int32, device=DEV)
+    o1, l1 = gpu_decode(first, caches=(kc, vc))
+    # second part: the remaining tokens, via a table that starts at block 10
+    second = W.random_decode(55, [300, 161], 4, 2, 128, device=DEV, poison=True)
+    t = b.block_tables_decode[:, 10:].contiguous()
+    second.block_tables_decode = t
+    second.context_lens_decode = torch.tensor([140, 1], dtype=torch.int32, device=DEV)
+    o2, l2 = gpu_decode(second, caches=(kc, vc))
+    po = torch.stack([o1, o2], dim=2).contiguous()
+    pl = torch.stack([l1, l2], dim=2).contiguous()
+    out = torch.empty_like(full)
+    lse = torch.empty_like(lfull)
+    B.pa_merge_partials(out, po, pl, lse_out=lse)
+    torch.cuda.synchronize()
+    assert (out - full).abs().max().item() < 1e-5
+    assert (lse - lfull).abs().max().item() < 1e-5
+
+
+# ---------------------------------------------------------------------- prefill
+
+PREFILL_CASES = [
+    # (D, Hq, Hkv, kv, q_lens, ctx_lens, shared prefix blocks)
+    (64, 4, 2, W.KV_BF16, [5, 16, 1, 23], [5, 40, 33, 64], 1),
+    (128, 32, 8, W.KV_BF16, [100, 37], [300, 37], 0),
+    (128, 8, 2, W.KV_BF16, [200, 64, 1], [530, 64, 129], 2),
+    (128, 10, 2, W.KV_BF16, [70, 3], [150, 90], 0),
+    (128, 1, 1, W.KV_BF16, [129], [129], 0),
+    (64, 4, 2, W.KV_FP8, [5, 16, 1, 23], [5, 40, 33, 64], 1),
+    (128, 8, 2, W.KV_FP8, [90, 20], [300, 20], 1),
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,kv,q_lens,ctx,shared", PREFILL_CASES)
+def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared):
+    b = W.random_prefill(200 + D + Hq + len(q_lens), q_lens, ctx, Hq, Hkv, D, kv_dtype=kv, device=DEV,
+                         poison=True, shared_prefix_blocks=shared)
+    out, lse = gpu_prefill(b)
+    o_ref, l_ref = oracle_prefill(b)
+    assert_close(out, o_ref, TOL[kv], "out")
+    assert_close(lse, l_ref, LSE_TOL[kv], "lse")
+
+
+def test_mixed_step_write_then_decode_and_prefill():
+    """Workload 5: cache write of 2064 new tokens, then decode (16 sequences)
+    and causal prefill (4 chunks of 512 over prefix-shared blocks)."""
+    b = W.workload(5, device=DEV, poison=True)
+    d = desc_of(b)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(d, b.k_new, b.v_new, kc, vc, b.slot_mapping)
+    dec_out, dec_lse = gpu_decode(b, caches=(kc, vc))
+    pf_out, pf_lse = gpu_prefill(b, caches=(kc, vc))
+    # oracle: its own cache write of the same inputs, then attention
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+                                b.k_pool.cpu(), b.v_pool.cpu())
+    oc = (oracle.KV_BF16, ok, ov)
+    o_ref, l_ref = oracle_decode(b, ocaches=oc)
+    assert_close(dec_out, o_ref, TOL[W.KV_BF16], "decode out")
+    assert_close(dec_lse, l_ref, LSE_TOL[W.KV_BF16], "decode lse")
+    # prefill: sampled rows (first, last and random rows of every chunk) x all heads
+    gen = torch.Generator().manual_seed(12)
+    rows = set()
+    for s in range(4):
+        base = s * 512
+        rows.update([base, base + 1, base + 63, base + 64, base + 511])
+        rows.update((base + torch.randint(0, 512, (6,), generator=gen)).tolist())
+    pairs = [(r, h) for r in sorted(rows) for h in range(32)]
+    o_ref, l_ref = oracle_prefill(b, ocaches=oc, pairs=pairs)
+    idx = torch.tensor([r * 32 + h for r, h in pairs])
+    assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[W.KV_BF16], "prefill out")
+    assert_close(pf_lse.reshape(-1)[idx], l_ref, LSE_TOL[W.KV_BF16], "prefill lse")
+
+
+def test_prefill_single_query_rows_match_decode_oracle():
+    lens = [7, 16, 41, 300]
+    d = W.random_decode(301, lens, 8, 2, 128, device=DEV, poison=True)
+    p = W.random_prefill(301, [1, 1, 1, 1], lens, 8, 2, 128, device=DEV)
+    p.q_prefill = d.q_decode.clone()
+    p.k_pool, p.v_pool, p.num_blocks = d.k_pool, d.v_pool, d.num_blocks
+    p.block_tables_prefill = d.block_tables_decode
+    p.context_lens_prefill = d.context_lens_decode
+    out, _ = gpu_prefill(p)
+    o_ref, _ = oracle_decode(d)
+    assert_close(out, o_ref, TOL[W.KV_BF16])
