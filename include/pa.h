@@ -137,10 +137,11 @@ PA_API pa_status pa_cache_write(const pa_kv_desc *desc, const void *k, const voi
  * Bytes of scratch that pa_decode needs for num_seqs sequences on the current
  * device.  Zero-fill the workspace once before its first use; it may then be
  * reused by consecutive calls on one stream (each call leaves its error word
- * and merge counters at zero again; the rest holds the last call's partial
- * results).  Calls that overlap on the GPU need separate workspaces.  After a
- * call completes, a non-zero first int32 of the workspace means the kernel
- * gave up waiting on its own pipeline (a bounded wait ran out).
+ * and its merge counters at zero again; the rest holds the last call's
+ * partial results).  Calls that overlap on the GPU need separate workspaces.
+ * After a call completes, a non-zero first int32 of the workspace means the
+ * kernel gave up (a bounded wait on its own pipeline ran out, or a merge had
+ * more pieces than it supports).
  */
 PA_API size_t pa_decode_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_context_len);
 

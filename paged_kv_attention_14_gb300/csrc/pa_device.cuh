@@ -120,6 +120,16 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// One 3-D tile of a tensor map (TMA), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, int y, int z, uint64_t *bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // ----------------------------------------------------------- 16-byte cp.async
 
 // Copies 16 bytes, or zero-fills them when `valid` is false (src-size 0).
@@ -183,6 +193,21 @@ __device__ __forceinline__ uint16_t pack_e4m3x2_satfinite(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ------------------------------------------------------------ gpu atomics
+
+// atomicAdd with acquire-release semantics at GPU scope: makes this thread's
+// earlier writes (and those ordered before it by a barrier) visible before
+// the add, and later reads see what the other adders published.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(int *p, int v) {
+  asm volatile("st.relaxed.gpu.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ------------------------------------------------------------- warp helpers

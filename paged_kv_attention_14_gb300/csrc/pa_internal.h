@@ -19,9 +19,10 @@ cudaError_t launch_merge(float *out, float *lse_out, const float *part_o, const 
 
 // Decode: which kernel variant runs and how many persistent CTAs it uses.
 struct DecodePlan {
-  int impl;       // PA_DECODE_SIMT or PA_DECODE_MMA
-  int group_pad;  // group size rounded up to the kernel's instantiation
-  int num_ctas;   // persistent grid size
+  int impl;        // PA_DECODE_SIMT or PA_DECODE_MMA
+  int slot_heads;  // query heads per partial-result slot of the kernel
+  int num_groups;  // kv head groups per sequence (segments per sequence)
+  int num_ctas;    // persistent grid size
   size_t workspace_bytes;
 };
 

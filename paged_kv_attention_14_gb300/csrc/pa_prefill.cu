@@ -52,7 +52,6 @@ struct PrefillArgs {
 template <int D, int KVT, int NW>
 struct PrefillCfg {
   static constexpr int KT = 64;                 // keys per tile
-  static constexpr int MROWS = NW * 16;         // (query, head) rows per CTA
   static constexpr int NT = NW * 32;
   static constexpr int CH = D / 8;              // 16-byte bf16 chunks per row
   static constexpr int TILE = KT * D * 2;       // bf16 tile bytes
