@@ -203,6 +203,29 @@ PA_API pa_status pa_merge_partials(float *out, float *lse_out, const float *part
                             int32_t num_heads, int32_t max_parts, int32_t head_dim,
                             pa_stream_t stream);
 
+/*
+ * Decode without a workspace argument (the paper has no counterpart; this is
+ * a convenience of this library).  Same operation, arguments and results as
+ * pa_decode, for callers that cannot allocate device memory where they
+ * decode: serving loops held to a fixed device-memory budget once the KV
+ * pool is sized, runtimes whose device memory is fully planned up front, and
+ * plug-ins whose host framework owns the allocator.  The scratch is a fixed 8 MiB array in the library's own device
+ * memory (held on every GPU that loads the library until the process exits);
+ * a batch needing more scratch than that (pa_decode_workspace_size) is
+ * rejected with PA_ERR_WORKSPACE.  The call allocates nothing: it clears the
+ * array's error word and merge counters with cudaMemsetAsync on `stream` and
+ * enqueues the decode kernels there.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture.  All calls share
+ * the one array, so calls that may overlap on the GPU (different streams
+ * without ordering between them) race; serialise them, or use pa_decode with
+ * separate workspaces.
+ */
+PA_API pa_status pa_decode_static(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                                  const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t max_context_len, float scale, pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

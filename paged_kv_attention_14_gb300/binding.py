@@ -34,7 +34,7 @@ PA_DECODE_MMA = 2
 
 #: every symbol include/pa.h declares
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
-            "pa_decode", "pa_prefill_chunk", "pa_merge_partials")
+            "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -88,6 +88,8 @@ def load(path: Optional[str] = None):
         lib.pa_prefill_chunk.restype = ctypes.c_int
         lib.pa_merge_partials.argtypes = [P, P, P, P, P, I32, I32, I32, I32, P]
         lib.pa_merge_partials.restype = ctypes.c_int
+        lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
+        lib.pa_decode_static.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -174,6 +176,19 @@ def pa_decode(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_le
                             _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
                             float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
                             workspace.numel(), _stream(stream)))
+
+
+def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_lens,
+                     max_context_len: int, scale: float, lse=None, stream=None):
+    """pa_decode on the library's own fixed-size scratch (no workspace argument,
+    for callers that cannot allocate device memory where they decode)."""
+    S = int(context_lens.shape[0])
+    _check(load().pa_decode_static(ctypes.byref(desc), _ptr(out, _F32, "out"),
+                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                                   _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                   _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
+                                   _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
+                                   float(scale), _stream(stream)))
 
 
 def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, block_tables,

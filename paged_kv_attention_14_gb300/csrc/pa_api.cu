@@ -53,6 +53,10 @@ pa_status cuda_fail(cudaError_t e) {
 
 }  // namespace
 
+namespace pa {
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace pa
+
 extern "C" {
 
 int pa_abi_version(void) { return PA_ABI_VERSION; }

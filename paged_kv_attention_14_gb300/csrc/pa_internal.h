@@ -46,4 +46,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Sets the message pa_last_error() returns on this thread.
+void set_last_error(const char *msg);
+
 }  // namespace pa
