@@ -108,6 +108,19 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def _prefill_flops(b) -> int:
+    """Algorithmic flops of the causal prefill chunks: per query row and head,
+    4 * head_dim flops (QK^T and PV multiply-adds) per key at or before it."""
+    qsl = b.query_start_loc.cpu().tolist()
+    lens = b.context_lens_prefill.cpu().tolist()
+    keys = 0
+    for s, L in enumerate(lens):
+        n = qsl[s + 1] - qsl[s]
+        # query i sits at L - n + i and sees L - n + i + 1 keys
+        keys += n * (L - n) + n * (n + 1) // 2
+    return keys * 4 * b.head_dim * b.num_q_heads
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -141,17 +154,31 @@ def run_ours(args):
     wsp = B.decode_workspace(desc, S, maxL, dev)
     out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
     kv_bytes = b.decode_kv_bytes()
-    # cache write + decode (+ the merge kernel of the tensor-core decode)
-    launches_per_step = 3 if args.decode_impl != 1 else 2
+    mixed = b.q_prefill is not None
+    if mixed:
+        pf_out = torch.empty(b.q_prefill.shape, dtype=torch.float32, device=dev)
+        qsl = b.query_start_loc
+        pf_maxq = int((qsl[1:] - qsl[:-1]).max())
+        pf_maxL = int(b.context_lens_prefill.max())
+        pf_flops = _prefill_flops(b)
+    # cache write + decode (+ the merge kernel of the tensor-core decode) (+ prefill)
+    launches_per_step = (3 if args.decode_impl != 1 else 2) + (1 if mixed else 0)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
     if kv_bytes < 2 * l2_bytes:  # small working set: flush L2 by writing a buffer larger than it
         flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
 
+    def decode(q, bt, cl):
+        B.pa_decode(desc, out, q, kc, vc, bt, cl, maxL, b.scale, wsp)
+
+    def prefill(q, qs, bt, cl):
+        B.pa_prefill_chunk(desc, pf_out, q, qs, kc, vc, bt, cl, pf_maxq, pf_maxL, b.scale)
+
     def step():
         B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
-        B.pa_decode(desc, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale,
-                    wsp)
+        decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
+        if mixed:
+            prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -160,50 +187,81 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
                            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
     sampler.start()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # timed region 1: whole steps, CUDA events only at step boundaries (an
+    # event between two kernels would cut the programmatic-dependent overlap
+    # of the decode launch with the cache write)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         if flush is not None:
             flush.zero_()
-        e0, e1, e2 = ev[i]
-        e0.record()
-        B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
-        e1.record()
-        B.pa_decode(desc, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale,
-                    wsp)
-        e2.record()
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    # timed region 2: the kernels of each entry point alone, events around
+    # each call (decode = decode kernel + merge kernel; prefill)
+    K2 = max(10, K // 2)
+    ev_d = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+    ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+    for i in range(K2):
+        if flush is not None:
+            flush.zero_()
+        ev_d[i][0].record()
+        decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
+        ev_d[i][1].record()
+        if mixed:
+            ev_p[i][0].record()
+            prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
+            ev_p[i][1].record()
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = sum(e0.elapsed_time(e2) for e0, _, e2 in ev) / K
-    dec_ms = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / K
+    step_ms = sum(a.elapsed_time(c) for a, c in ev) / K
+    dec_ms = sum(a.elapsed_time(c) for a, c in ev_d) / K2
+    pf_ms = sum(a.elapsed_time(c) for a, c in ev_p) / K2 if mixed else 0.0
     if ws > 1:
-        t = torch.tensor([step_ms, dec_ms], device=dev)
+        t = torch.tensor([step_ms, dec_ms, pf_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms = float(t[0]), float(t[1])
+        step_ms, dec_ms, pf_ms = (float(x) for x in t)
     assert int(wsp[:4].view(torch.int32)[0]) == 0, "decode kernel reported a wait timeout"
 
-    # end to end through the public API: pinned host inputs in, result out
-    host = {n: getattr(b, n).cpu().pin_memory() for n in
-            ("q_decode", "k_new", "v_new", "slot_mapping", "block_tables_decode", "context_lens_decode")}
-    dev_in = {n: torch.empty_like(getattr(b, n)) for n in host}
+    # End to end through the public API: every step copies its inputs from one
+    # pinned host buffer into one device buffer (one H2D copy; the tensors the
+    # library gets are views into it) and reads the step's result back.
+    names = ["q_decode", "k_new", "v_new", "slot_mapping", "block_tables_decode", "context_lens_decode"]
+    if mixed:
+        names += ["q_prefill", "query_start_loc", "block_tables_prefill", "context_lens_prefill"]
+    srcs = [getattr(b, n).contiguous() for n in names]
+    offs, total = [], 0
+    for t in srcs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = {}
+    for n, t, o in zip(names, srcs, offs):
+        nb = t.numel() * t.element_size()
+        host_buf[o:o + nb].copy_(t.reshape(-1).view(torch.uint8).cpu())
+        views[n] = dev_buf[o:o + nb].view(t.dtype).view(t.shape)
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    pf_host = torch.empty(pf_out.shape, dtype=pf_out.dtype).pin_memory() if mixed else None
+    h2d = total
+    d2h = out_host.numel() * out_host.element_size() + (pf_host.numel() * pf_host.element_size() if mixed else 0)
 
     def e2e_step():
-        for n, t in host.items():
-            dev_in[n].copy_(t, non_blocking=True)
-        B.pa_cache_write(desc, dev_in["k_new"], dev_in["v_new"], kc, vc, dev_in["slot_mapping"])
-        B.pa_decode(desc, out, dev_in["q_decode"], kc, vc, dev_in["block_tables_decode"],
-                    dev_in["context_lens_decode"], maxL, b.scale, wsp)
+        dev_buf.copy_(host_buf, non_blocking=True)
+        B.pa_cache_write(desc, views["k_new"], views["v_new"], kc, vc, views["slot_mapping"])
+        decode(views["q_decode"], views["block_tables_decode"], views["context_lens_decode"])
+        if mixed:
+            prefill(views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
+                    views["context_lens_prefill"])
+            pf_host.copy_(pf_out, non_blocking=True)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
@@ -251,15 +309,19 @@ def run_ours(args):
                        "l2": ("flushed before every step (write of 2x L2)" if flush is not None else
                               f"inputs larger than L2 ({kv_bytes >> 20} MiB KV vs {l2_bytes >> 20} MiB L2), no flush"),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "kernel": "pa_decode (decode kernel + merge kernel)",
-                         "achieved": round(dec_gbs, 1),
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dec_gbs / peak, 4),
-                         "kernel_us": round(dec_ms * 1e3, 2), "traffic": None},
+            "roofline": {"bound": "hbm",
+                         "kernel": "pa_decode (decode kernel + merge kernel), timed alone per call",
+                         "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
+                         "traffic": None},
             "e2e": {"value": round(ws * kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": launches_per_step * K + (launches_per_step - 1) * K2,
             "clocks": clocks,
         }
+        if mixed:
+            line["prefill"] = {"kernel": "pa_prefill_chunk", "us": round(pf_ms * 1e3, 2), "flops": pf_flops,
+                               "tflops": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1)}
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
@@ -330,7 +392,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4])
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint8_t *__restrict__ k_cache,
     uint8_t *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_vecs,
     int vecs_per_row, int num_kv_heads, int block_size, float k_scale, float v_scale) {
+  // a kernel launched after this one as a programmatic dependent (pa_decode,
+  // pa_prefill_chunk) may start its launch now; it waits for this grid's
+  // writes before reading anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total_vecs) return;
   const int vec = static_cast<int>(i % vecs_per_row);

@@ -179,8 +179,21 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.rec = reinterpret_cast<dec::SegRec *>(ws + w.rec_off);
   a.slot_lse = reinterpret_cast<float *>(ws + w.slot_lse_off);
   a.slot_o = reinterpret_cast<float *>(ws + w.slot_o_off);
+  // programmatic dependent launch: the kernel's launch overlaps the tail of
+  // the preceding kernel in the stream (typically pa_cache_write); the kernel
+  // waits for that kernel's writes before reading anything
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3(plan.num_ctas);
+  dcfg.blockDim = dim3(k.threads);
+  dcfg.dynamicSmemBytes = k.smem;
+  dcfg.stream = stream;
+  dcfg.attrs = pdl;
+  dcfg.numAttrs = 1;
   void *args[] = {&a};
-  cudaError_t e = cudaLaunchKernel(k.fn, dim3(plan.num_ctas), dim3(k.threads), args, k.smem, stream);
+  cudaError_t e = cudaLaunchKernelExC(&dcfg, k.fn, args);
   if (e != cudaSuccess || !k.mma) return e;
 
   // merge of the segments split across CTAs, launched as a programmatic

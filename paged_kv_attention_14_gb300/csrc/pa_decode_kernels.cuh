@@ -535,6 +535,9 @@ template <int D, int KVT, int GP, int BPS, int NS>
 __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kernel(const __grid_constant__ DecodeArgs a) {
   using C = SimtCfg<D, KVT, GP, BPS, NS>;
   using RS = RowSlice<D, KVT>;
+  // launched as a programmatic dependent of the preceding kernel in the
+  // stream: nothing is read before that kernel's writes are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int EPL = C::EPL;
   constexpr int NC = C::NC;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -881,7 +884,10 @@ __global__ void __launch_bounds__((kConsumerWarps + 2) * 32, 1) decode_mma_kerne
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // the merge kernel may be scheduled now; it waits for this grid's results
+  // launched as a programmatic dependent of the preceding kernel in the
+  // stream: nothing is read before that kernel's writes are visible; the
+  // merge kernel may be scheduled now and waits for this grid's results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
