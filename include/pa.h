@@ -86,6 +86,13 @@ typedef enum {
   PA_DECODE_MMA = 2    /* tensor-core (mma.sync) tiles, any group size <= 16 */
 } pa_decode_impl;
 
+/* Which prefill kernel pa_prefill_chunk runs.  0 lets the library choose. */
+typedef enum {
+  PA_PREFILL_AUTO = 0,
+  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; bf16 and E4M3 caches   */
+  PA_PREFILL_TCGEN05 = 2   /* tcgen05 tensor-memory tiles; bf16 caches        */
+} pa_prefill_impl;
+
 /*
  * Shape of the KV pool.  Zero-initialise, then set the fields.  Fields are
  * only ever appended; a zero in an appended field keeps earlier behaviour.
@@ -95,6 +102,7 @@ typedef enum {
  *   k_scale, v_scale : FP8 only.  Cached value = stored E4M3 value * scale.
  *                  0 means 1.0.  Ignored for bf16.
  *   decode_impl  : a pa_decode_impl value.
+ *   prefill_impl : a pa_prefill_impl value.
  */
 typedef struct {
   int32_t num_blocks;
@@ -105,7 +113,8 @@ typedef struct {
   int32_t kv_dtype; /* pa_kv_dtype */
   float k_scale;
   float v_scale;
-  int32_t decode_impl; /* pa_decode_impl */
+  int32_t decode_impl;  /* pa_decode_impl */
+  int32_t prefill_impl; /* pa_prefill_impl */
 } pa_kv_desc;
 
 /* PA_ABI_VERSION of the loaded library. */

@@ -32,6 +32,10 @@ PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
 PA_DECODE_MMA = 2
 
+PA_PREFILL_AUTO = 0
+PA_PREFILL_MMA_SYNC = 1
+PA_PREFILL_TCGEN05 = 2
+
 #: every symbol include/pa.h declares
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static")
@@ -49,6 +53,7 @@ class PaKvDesc(ctypes.Structure):
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
         ("decode_impl", ctypes.c_int32),
+        ("prefill_impl", ctypes.c_int32),
     ]
 
 
@@ -97,9 +102,10 @@ def load(path: Optional[str] = None):
 
 def make_desc(num_blocks: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
               kv_dtype: int = PA_KV_BF16, k_scale: float = 0.0, v_scale: float = 0.0,
-              block_size: int = 16, decode_impl: int = PA_DECODE_AUTO) -> PaKvDesc:
+              block_size: int = 16, decode_impl: int = PA_DECODE_AUTO,
+              prefill_impl: int = PA_PREFILL_AUTO) -> PaKvDesc:
     return PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
-                    k_scale, v_scale, decode_impl)
+                    k_scale, v_scale, decode_impl, prefill_impl)
 
 
 def abi_version() -> int:

@@ -43,6 +43,12 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream);
 
+// tcgen05 (tensor-memory) prefill kernel for bf16 caches.
+cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const void *q,
+                              const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                              int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

@@ -354,6 +354,14 @@ pa_status check_prefill(const pa_kv_desc &d, const char **why) {
     *why = "prefill supports group sizes up to 128";
     return PA_ERR_UNSUPPORTED;
   }
+  if (d.prefill_impl < PA_PREFILL_AUTO || d.prefill_impl > PA_PREFILL_TCGEN05) {
+    *why = "prefill_impl must be PA_PREFILL_AUTO, PA_PREFILL_MMA_SYNC or PA_PREFILL_TCGEN05";
+    return PA_ERR_INVALID_ARG;
+  }
+  if (d.prefill_impl == PA_PREFILL_TCGEN05 && d.kv_dtype != PA_KV_BF16) {
+    *why = "the tcgen05 prefill kernel takes bf16 caches";
+    return PA_ERR_UNSUPPORTED;
+  }
   return PA_OK;
 }
 
@@ -363,6 +371,10 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
+  if (impl == PA_PREFILL_TCGEN05)
+    return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                             context_lens, num_seqs, max_q_len, scale, stream);
   const int g = d.num_q_heads / d.num_kv_heads;
   PrefillArgs a;
   a.out = out;

@@ -22,10 +22,12 @@ def kv_code(b: W.PagedBatch) -> int:
     return B.PA_KV_BF16 if b.kv_dtype == W.KV_BF16 else B.PA_KV_FP8_E4M3
 
 
-def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO) -> B.PaKvDesc:
+def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO,
+            prefill_impl: int = B.PA_PREFILL_AUTO) -> B.PaKvDesc:
     return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
                        b.k_scale if b.kv_dtype == W.KV_FP8 else 0.0,
-                       b.v_scale if b.kv_dtype == W.KV_FP8 else 0.0, decode_impl=decode_impl)
+                       b.v_scale if b.kv_dtype == W.KV_FP8 else 0.0, decode_impl=decode_impl,
+                       prefill_impl=prefill_impl)
 
 
 def gpu_caches(b: W.PagedBatch):
@@ -74,7 +76,7 @@ def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None):
                          b.v_scale, pairs=pairs)
 
 
-def gpu_prefill(b: W.PagedBatch, caches=None):
+def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO):
     kc, vc = caches if caches is not None else gpu_caches(b)
     Tq = b.q_prefill.shape[0]
     out = torch.full((Tq, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
@@ -82,7 +84,7 @@ def gpu_prefill(b: W.PagedBatch, caches=None):
     qsl = b.query_start_loc
     max_q = int((qsl[1:] - qsl[:-1]).max())
     maxL = int(b.context_lens_prefill.max())
-    B.pa_prefill_chunk(desc_of(b), out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill,
+    B.pa_prefill_chunk(desc_of(b, prefill_impl=prefill_impl), out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill,
                        b.context_lens_prefill, max_q, maxL, b.scale, lse=lse)
     torch.cuda.synchronize()
     return out, lse

@@ -58,7 +58,7 @@ def test_desc_struct_matches_header_layout():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in B.PaKvDesc._fields_]
-    assert ctypes.sizeof(B.PaKvDesc) == 36
+    assert ctypes.sizeof(B.PaKvDesc) == 40
 
 
 def _desc(**kw):

@@ -294,22 +294,29 @@ PREFILL_CASES = [
     (128, 8, 2, W.KV_BF16, [200, 64, 1], [530, 64, 129], 2),
     (128, 10, 2, W.KV_BF16, [70, 3], [150, 90], 0),
     (128, 1, 1, W.KV_BF16, [129], [129], 0),
+    (128, 4, 1, W.KV_BF16, [300, 64], [1000, 65], 3),
+    (64, 16, 1, W.KV_BF16, [40, 8], [200, 8], 0),
     (64, 4, 2, W.KV_FP8, [5, 16, 1, 23], [5, 40, 33, 64], 1),
     (128, 8, 2, W.KV_FP8, [90, 20], [300, 20], 1),
 ]
+PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
 
 
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("D,Hq,Hkv,kv,q_lens,ctx,shared", PREFILL_CASES)
-def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared):
+def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared, impl):
+    if impl == B.PA_PREFILL_TCGEN05 and kv != W.KV_BF16:
+        pytest.skip("the tcgen05 prefill kernel takes bf16 caches")
     b = W.random_prefill(200 + D + Hq + len(q_lens), q_lens, ctx, Hq, Hkv, D, kv_dtype=kv, device=DEV,
                          poison=True, shared_prefix_blocks=shared)
-    out, lse = gpu_prefill(b)
+    out, lse = gpu_prefill(b, prefill_impl=impl)
     o_ref, l_ref = oracle_prefill(b)
     assert_close(out, o_ref, TOL[kv], "out")
     assert_close(lse, l_ref, LSE_TOL[kv], "lse")
 
 
-def test_mixed_step_write_then_decode_and_prefill():
+@pytest.mark.parametrize("impl", PREFILL_IMPLS)
+def test_mixed_step_write_then_decode_and_prefill(impl):
     """Workload 5: cache write of 2064 new tokens, then decode (16 sequences)
     and causal prefill (4 chunks of 512 over prefix-shared blocks)."""
     b = W.workload(5, device=DEV, poison=True)
@@ -317,7 +324,7 @@ def test_mixed_step_write_then_decode_and_prefill():
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     B.pa_cache_write(d, b.k_new, b.v_new, kc, vc, b.slot_mapping)
     dec_out, dec_lse = gpu_decode(b, caches=(kc, vc))
-    pf_out, pf_lse = gpu_prefill(b, caches=(kc, vc))
+    pf_out, pf_lse = gpu_prefill(b, caches=(kc, vc), prefill_impl=impl)
     # oracle: its own cache write of the same inputs, then attention
     ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
                                 b.k_pool.cpu(), b.v_pool.cpu())
@@ -337,6 +344,17 @@ def test_mixed_step_write_then_decode_and_prefill():
     idx = torch.tensor([r * 32 + h for r, h in pairs])
     assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[W.KV_BF16], "prefill out")
     assert_close(pf_lse.reshape(-1)[idx], l_ref, LSE_TOL[W.KV_BF16], "prefill lse")
+
+
+def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
+    b = W.workload(5, device=DEV, poison=True)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(desc_of(b), b.k_new, b.v_new, kc, vc, b.slot_mapping)  # the chunks' own K/V
+    o1, l1 = gpu_prefill(b, caches=(kc, vc), prefill_impl=B.PA_PREFILL_MMA_SYNC)
+    o2, l2 = gpu_prefill(b, caches=(kc, vc), prefill_impl=B.PA_PREFILL_TCGEN05)
+    assert torch.isfinite(o1).all() and torch.isfinite(o2).all()
+    assert (o1 - o2).abs().max().item() < 2e-3
+    assert (l1 - l2).abs().max().item() < 2e-3
 
 
 def test_prefill_single_query_rows_match_decode_oracle():
