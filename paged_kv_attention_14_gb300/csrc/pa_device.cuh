@@ -210,6 +210,13 @@ __device__ __forceinline__ void st_relaxed_gpu(int *p, int v) {
   asm volatile("st.relaxed.gpu.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// 2^x by the SFU's approximate instruction (relative error ~2^-22; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------- warp helpers
 
 __device__ __forceinline__ float warp_max_xor(float v, int from, int to) {

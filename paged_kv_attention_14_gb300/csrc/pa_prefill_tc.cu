@@ -9,23 +9,33 @@
 // Technical Mechanics of the Radix Cache", Building and Deploying vllm.cpp).
 //
 // How (GB300 design):
-//  * One CTA takes 128 (query, head) rows: 128 / g consecutive queries of
+//  * One CTA takes 256 (query, head) rows: 256 / g consecutive queries of
 //    one sequence times the g query heads of one kv head, so every K/V tile
-//    feeds the whole GQA group.  Q is staged once; K/V are walked in 64-key
-//    tiles gathered block by block through the block table by TMA (two
-//    128-byte-swizzled boxes per 16-token block), double buffered.
-//  * Warp 5 (one thread) issues the MMAs: S = Q K^T (M 128, N 64, K 16 x
-//    head_dim/16) into one of two TMEM S buffers, then O += P V (M 128,
-//    N head_dim, K 16 x 4) with P from shared memory and V read MN-major.
-//    QK^T of the next tile runs while the softmax of the current one does.
-//  * Warps 0-3 (one thread per row, the row's 64 scores in registers) do the
-//    online softmax: scale, causal mask, row max, exp2, row sum, and write P
+//    feeds the whole GQA group.  The rows form two 128-row Q tiles (A, B)
+//    that ping-pong: while one tile's softmax runs, the tensor cores work on
+//    the other tile.  Q is staged once; K/V are walked in 64-key tiles
+//    gathered block by block through the block table by TMA (two
+//    128-byte-swizzled boxes per 16-token block) into two 3-stage rings, one
+//    for K and one for V, shared by both Q tiles.  A K slot is released as
+//    soon as the QKs that read it complete, a V slot after its PVs, so the
+//    copies run up to three tiles ahead of the tensor cores.
+//  * Warp 9 (one thread) issues the MMAs: S_t = Q_t K^T (M 128, N 64, K 16 x
+//    head_dim/16) into one of tile t's two TMEM S buffers, and O_t += P_t V
+//    (M 128, N head_dim, K 16 x 4) with P_t from shared memory and V read
+//    MN-major, in the order QK_A(j+1), QK_B(j+1), PV_A(j), PV_B(j): the
+//    scores of the next KV tile are computed while the softmax of this one
+//    runs.
+//  * Warps 0-3 (tile A) and 4-7 (tile B), one thread per row with the row's
+//    64 scores in registers, do the online softmax: scale, causal mask, row
+//    max, exp2, row sum, and write P
 //    as a bf16 hi + lo pair (P = hi + lo to ~2^-17 relative; two PV MMAs)
 //    so the bf16 tensor-core result keeps near-fp32 accuracy.  The running
 //    max is only raised (and O rescaled in TMEM) when it grows by more than
 //    2^8, so O is rarely touched before the end.
 //  * Keys past the chunk's last position are masked; V rows past it are
 //    zeroed in shared memory before the last PV (0 * NaN would not vanish).
+//  * Warp 8 issues the TMA copies and prefetches block-table entries one
+//    tile ahead.
 //  * Every wait is bounded; on a timeout the kernel records an error bit,
 //    lets its own MMAs and copies drain and frees its TMEM before returning.
 #include <cuda.h>
@@ -39,9 +49,14 @@ namespace pftc {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int KT = 64;        // keys per KV tile
-constexpr int MROWS = 128;    // (query, head) rows per CTA
-constexpr int NTHREADS = 192; // warps 0-3 softmax, 4 TMA producer, 5 MMA issuer
+constexpr int KT = 64;         // keys per KV tile
+constexpr int MT = 128;        // rows of one Q tile (one TMEM lane per row)
+constexpr int NQT = 2;         // Q tiles per CTA (ping-pong between two softmax warpgroups)
+constexpr int MROWS = MT * NQT;
+constexpr int NTHREADS = 320;  // warps 0-3 softmax A, 4-7 softmax B, 8 TMA producer, 9 MMA issuer
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int NST = 3;         // stages of the K ring and of the V ring
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 struct Args {
@@ -57,7 +72,7 @@ struct Args {
   int num_kv_heads;
   int num_q_heads;
   int g;
-  int qt;  // queries per CTA (128 / g)
+  int qt;  // queries per CTA (256 / g)
   float qscale;
 };
 
@@ -65,30 +80,61 @@ struct Args {
 // sets them, nothing else uses them.
 static __device__ int g_prefill_err;
 
+// Optional timeline counters (compiled only with -DPA_PREFILL_TRACE), per
+// CTA slot (blockIdx linearised, first 4096): softmax warp 0 lane 0 cycles
+// [0] waiting for S, [1] loading S from TMEM, [2] masking and max, [3]
+// waiting for the previous PV, [4] rescaling O, [5] exp2 and P stores, [6]
+// fence and arrive, [7] total; MMA thread cycles [8] waiting for K/V, [9]
+// waiting for S_FREE, [10] waiting for P, [11] total; producer [12] waiting
+// for a free K/V buffer, [13] total; [14] KV tiles.
+#ifdef PA_PREFILL_TRACE
+static __device__ unsigned long long g_pf_trace[4096][16];
+#define PF_TRACE(...) __VA_ARGS__
+#else
+#define PF_TRACE(...)
+#endif
+
 template <int D>
 struct Cfg {
   static constexpr int HALVES = D / 64;          // 128-byte column halves of a row
-  static constexpr int QHALF = MROWS * 128;      // bytes of one half of Q
-  static constexpr int QB = HALVES * QHALF;
+  static constexpr int QHALF = MT * 128;         // bytes of one half of one Q tile
+  static constexpr int QB = HALVES * QHALF;      // one Q tile
   static constexpr int KVHALF = KT * 128;        // bytes of one half of a K or V tile
   static constexpr int KVB = HALVES * KVHALF;
-  static constexpr int PB = MROWS * KT * 2;      // one P matrix (hi or lo), 128 x 64 bf16
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB;       // [2]
-  static constexpr int OFF_V = OFF_K + 2 * KVB;  // [2]
-  static constexpr int OFF_P = OFF_V + 2 * KVB;  // [2][hi, lo]
-  static constexpr int OFF_BAR = OFF_P + 4 * PB;
+  static constexpr int PB = MT * KT * 2;         // one P matrix (hi or lo), 128 x 64 bf16
+  static constexpr int OFF_Q = 0;                // [NQT]
+  static constexpr int OFF_K = OFF_Q + NQT * QB;    // [NST]
+  static constexpr int OFF_V = OFF_K + NST * KVB;   // [NST]
+  static constexpr int OFF_P = OFF_V + NST * KVB;   // [NQT][hi, lo]
+  static constexpr int OFF_BAR = OFF_P + NQT * 2 * PB;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers, TMEM slot, 1024-B alignment slack
-  static constexpr uint32_t TMEM_COLS = 256;     // S[2] (64 columns each) + O (D columns)
+  static_assert(SMEM <= 232448, "shared memory of one CTA");
+  // TMEM columns: two S buffers of each Q tile (KT each), then O of each Q
+  // tile (D each)
   static constexpr uint32_t S_COL = 0;
-  static constexpr uint32_t O_COL = 128;
-  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MROWS, KT, false, false);
-  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MROWS, D, false, true);
-  // bytes landed per 16-token block (K and V, all halves)
-  static constexpr uint32_t BLOCK_BYTES = 2u * HALVES * 16u * 128u;
+  static constexpr uint32_t O_COL = NQT * 2 * KT;
+  static constexpr uint32_t COLS_USED = NQT * 2 * KT + NQT * D;
+  static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true);
+  // bytes landed per 16-token block of K (or of V), all halves
+  static constexpr uint32_t BLOCK_BYTES = HALVES * 16u * 128u;
 };
 
-enum Bar { KV_FULL = 0, KV_EMPTY = 2, S_FULL = 4, S_FREE = 6, P_FULL = 8, PV_DONE = 10, NBAR = 12 };
+// barriers: K_FULL[NST], K_EMPTY[NST], V_FULL[NST], V_EMPTY[NST],
+// S_FULL[tile][2], S_FREE[tile][2], P_FULL[tile], PV_DONE[tile]
+enum Bar {
+  K_FULL = 0,
+  K_EMPTY = K_FULL + NST,
+  V_FULL = K_EMPTY + NST,
+  V_EMPTY = V_FULL + NST,
+  S_FULL = V_EMPTY + NST,
+  S_FREE = S_FULL + 4,
+  P_FULL = S_FREE + 4,
+  PV_DONE = P_FULL + 2,
+  NBAR = PV_DONE + 2
+};
+static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ Args a) {
@@ -101,7 +147,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + NBAR);
   int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
-  int *s_last_tile = s_abort + 1;  // last KV tile whose copies the producer issued
+  int *s_last_k = s_abort + 1;  // last KV tile whose K copies the producer issued
+  int *s_last_v = s_abort + 2;  // ... and whose V copies
 
   const int s = blockIdx.z;
   const int kvh = blockIdx.y;
@@ -122,31 +169,40 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   const int rows_used = a.qt * g;
 
   if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&bar[K_FULL + i], 1);
+      mbar_init(&bar[K_EMPTY + i], 1);
+      mbar_init(&bar[V_FULL + i], 1);
+      mbar_init(&bar[V_EMPTY + i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[KV_FULL + i], 1);
-      mbar_init(&bar[KV_EMPTY + i], 1);
-      mbar_init(&bar[S_FULL + i], 1);
-      mbar_init(&bar[S_FREE + i], 4);
       mbar_init(&bar[P_FULL + i], 4);
       mbar_init(&bar[PV_DONE + i], 1);
     }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bar[S_FULL + i], 1);
+      mbar_init(&bar[S_FREE + i], 4);
+    }
     *s_abort = 0;
-    *s_last_tile = -1;
+    *s_last_k = -1;
+    *s_last_v = -1;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, C::TMEM_COLS);
 
-  // ---- Q tile: rows r = query * g + head, [half][row][128 B], 128-B swizzle
+  // ---- Q tiles: row R = query * g + head (tile R / 128, lane R % 128),
+  // [tile][half][row][128 B], 128-B swizzle
   {
     constexpr int CHUNKS = D / 8;  // 16-byte chunks per row
     for (int i = tid; i < MROWS * CHUNKS; i += NTHREADS) {
-      const int r = i / CHUNKS;
-      const int ch = i - r * CHUNKS;
-      const int qi = r / g;
-      const bool ok = r < rows_used && qi < nq;
+      const int R = i / CHUNKS;
+      const int ch = i - R * CHUNKS;
+      const int qi = R / g;
+      const bool ok = R < rows_used && qi < nq;
       const uint16_t *src = a.q;
-      if (ok) src = a.q + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (r - qi * g)) * D + ch * 8;
-      uint8_t *dst = smem + C::OFF_Q + (ch >> 3) * C::QHALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+      if (ok) src = a.q + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * D + ch * 8;
+      const int r = R & (MT - 1);
+      uint8_t *dst = smem + C::OFF_Q + (R / MT) * C::QB + (ch >> 3) * C::QHALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
       cp_async16(dst, src, ok);
     }
     cp_async_commit();
@@ -159,7 +215,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
     const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
     const uint64_t pol = l2_evict_first_policy();
@@ -170,124 +226,199 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const bool issuer = lane < 2 * 4 * C::HALVES;
     int phys_next = 0;
     if (issuer && bi * 16 < kv_end) phys_next = __ldg(table + bi);
+    PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
     for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
+      const int st = j % NST;
+      const uint32_t ph = (j / NST) & 1;
       const int phys = phys_next;
       const int key0 = j * KT;
       const int lb = (j + 1) * 4 + bi;  // prefetch the next tile's block id
       phys_next = (issuer && lb * 16 < kv_end) ? __ldg(table + lb) : 0;
-      if (!mbar_wait(&bar[KV_EMPTY + b], ph ^ 1)) {
+      const int nblk = min(4, (kv_end - key0 + 15) / 16);
+      const int row = (phys * a.num_kv_heads + kvh) * 16;
+      // K of tile j (its slot frees once the QKs of tile j - NST completed),
+      // then V of tile j (once the PVs of tile j - NST completed)
+      bool ok = true;
+#pragma unroll 1
+      for (int part = 0; part < 2 && ok; ++part) {
+        const int full = (part ? V_FULL : K_FULL) + st;
+        PF_TRACE(const long long tw = clock64();)
+        if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1)) {
+          ok = false;
+          break;
+        }
+        PF_TRACE(tp_wait += clock64() - tw;)
+        if (lane == 0) mbar_arrive_expect_tx(&bar[full], nblk * C::BLOCK_BYTES);
+        __syncwarp();
+        if (issuer && kv == part && bi < nblk) {
+          uint8_t *dst = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB + hh * C::KVHALF + bi * 16 * 128;
+          tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
+        }
+        if (lane == 0) *(part ? s_last_v : s_last_k) = j;
+      }
+      if (!ok) {
         if (lane == 0) *s_abort = 1;
         break;
       }
-      const int nblk = min(4, (kv_end - key0 + 15) / 16);
-      if (lane == 0) mbar_arrive_expect_tx(&bar[KV_FULL + b], nblk * C::BLOCK_BYTES);
-      __syncwarp();
-      if (issuer && bi < nblk) {
-        const int row = (phys * a.num_kv_heads + kvh) * 16;
-        uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + b * C::KVB + hh * C::KVHALF + bi * 16 * 128;
-        tma_load_2d(dst, kv ? &a.vmap : &a.kmap, hh * 64, row, &bar[KV_FULL + b], pol);
-      }
-      if (lane == 0) *s_last_tile = j;
     }
-  } else if (warp == 5) {
+    PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+             if (lane == 0 && slot < 4096) { g_pf_trace[slot][12] = tp_wait; g_pf_trace[slot][13] = clock64() - tp0; g_pf_trace[slot][14] = n_tiles; })
+  } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       bool ok = true;
-      auto issue_pv = [&](int t) {
-        const int b = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait(&bar[P_FULL + b], ph)) return false;
-        tc_fence_after_sync();
-        const uint32_t pbase = sbase + C::OFF_P + b * 2 * C::PB;
-        const uint32_t vbase = sbase + C::OFF_V + b * C::KVB;
+      auto qk = [&](int t, int j) {  // S_t[j & 1] = Q_t K_j^T
+        const int b = j & 1;
+        const uint32_t qbase = sbase + C::OFF_Q + t * C::QB;
+        const uint32_t kbase = sbase + C::OFF_K + (j % NST) * C::KVB;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * C::KVHALF + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + C::S_COL + (t * 2 + b) * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bar[S_FULL + t * 2 + b]);
+      };
+      auto pv = [&](int t, int j) {  // O_t += P_t V_j
+        const uint32_t pbase = sbase + C::OFF_P + t * 2 * C::PB;
+        const uint32_t vbase = sbase + C::OFF_V + (j % NST) * C::KVB;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {  // hi, then lo
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk) {
             const uint64_t ad = umma_desc_sw128(pbase + part * C::PB + kk * 32, 16, 1024);
             const uint64_t bd = umma_desc_sw128(vbase + kk * 2048, C::KVHALF, 1024);
-            umma_bf16_ss(tmem + C::O_COL, ad, bd, C::IDESC_PV, (t > 0 || part > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ss(tmem + C::O_COL + t * D, ad, bd, C::IDESC_PV, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        umma_commit(&bar[PV_DONE + b]);
-        umma_commit(&bar[KV_EMPTY + b]);
-        return true;
+        umma_commit(&bar[PV_DONE + t]);
       };
+      // S of KV tile j + 1 is computed before the PV of tile j, so the next
+      // scores are ready when a tile's softmax finishes
+      PF_TRACE(const long long tm0 = clock64(); long long tm_kv = 0, tm_sf = 0, tm_p = 0; long long tw;)
+      if (!mbar_wait(&bar[K_FULL], 0)) ok = false;
+      if (ok) {
+        tc_fence_after_sync();
+        for (int t = 0; t < NQT; ++t) qk(t, 0);
+        umma_commit(&bar[K_EMPTY]);
+      }
       for (int j = 0; j < n_tiles && ok; ++j) {
-        const int b = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bar[KV_FULL + b], ph) || !mbar_wait(&bar[S_FREE + b], ph ^ 1)) {
+        if (j + 1 < n_tiles) {
+          const int j1 = j + 1;
+          PF_TRACE(tw = clock64();)
+          if (!mbar_wait(&bar[K_FULL + j1 % NST], (j1 / NST) & 1)) {
+            ok = false;
+            break;
+          }
+          PF_TRACE(tm_kv += clock64() - tw;)
+          for (int t = 0; t < NQT && ok; ++t) {
+            PF_TRACE(tw = clock64();)
+            if (!mbar_wait(&bar[S_FREE + t * 2 + (j1 & 1)], ((j1 >> 1) & 1) ^ 1)) {
+              ok = false;
+              break;
+            }
+            PF_TRACE(tm_sf += clock64() - tw;)
+            tc_fence_after_sync();
+            qk(t, j1);
+          }
+          if (ok) umma_commit(&bar[K_EMPTY + j1 % NST]);  // K of tile j + 1 is consumed
+        }
+        if (!ok) break;
+        PF_TRACE(tw = clock64();)
+        if (!mbar_wait(&bar[V_FULL + j % NST], (j / NST) & 1)) {
           ok = false;
           break;
         }
-        tc_fence_after_sync();
-        const uint32_t qbase = sbase + C::OFF_Q;
-        const uint32_t kbase = sbase + C::OFF_K + b * C::KVB;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * 0 + (kk & 3) * 32;
-          const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * C::QHALF + koff, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * C::KVHALF + koff, 16, 1024);
-          umma_bf16_ss(tmem + C::S_COL + b * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        PF_TRACE(tm_kv += clock64() - tw;)
+        for (int t = 0; t < NQT && ok; ++t) {
+          PF_TRACE(tw = clock64();)
+          if (!mbar_wait(&bar[P_FULL + t], j & 1)) {
+            ok = false;
+            break;
+          }
+          PF_TRACE(tm_p += clock64() - tw;)
+          tc_fence_after_sync();
+          pv(t, j);
         }
-        umma_commit(&bar[S_FULL + b]);
-        if (j > 0 && !issue_pv(j - 1)) ok = false;
+        if (ok) umma_commit(&bar[V_EMPTY + j % NST]);  // both tiles are done with V of tile j
       }
-      if (ok && !issue_pv(n_tiles - 1)) ok = false;
       if (!ok) *s_abort = 1;
+      PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+               if (slot < 4096) { g_pf_trace[slot][8] = tm_kv; g_pf_trace[slot][9] = tm_sf; g_pf_trace[slot][10] = tm_p; g_pf_trace[slot][11] = clock64() - tm0; })
     }
     __syncwarp();
   } else {
     // ------------------------------------------------ softmax, one row per thread
-    const int r = tid;  // TMEM lane = row (warp w owns lanes 32w .. 32w + 31)
-    const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int qi = r / g;
-    const bool rv = r < rows_used && qi < nq;
+    const int t = warp >> 2;  // Q tile of this warpgroup
+    const int r = tid & (MT - 1);
+    const int R = t * MT + r;
+    // TMEM lane = row; warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31
+    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t o_col = C::O_COL + t * D;
+    const int qi = R / g;
+    const bool rv = R < rows_used && qi < nq;
     const int pos = rv ? base_pos + qi : -1;  // keys <= pos are visible
+    const float qscale = a.qscale;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc;)
     for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(&bar[S_FULL + b], ph)) {
+      const int sb = j & 1;
+      PF_TRACE(tc = clock64();)
+      if (!mbar_wait(&bar[S_FULL + t * 2 + sb], (j >> 1) & 1)) {
         ok = false;
         break;
       }
+      PF_TRACE(tq[0] += clock64() - tc; tc = clock64();)
       tc_fence_after_sync();
       float sv[KT];
-      tmem_ld32(trow + C::S_COL + b * KT, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      tmem_ld32(trow + C::S_COL + b * KT + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      const uint32_t s_col = C::S_COL + (t * 2 + sb) * KT;
+      tmem_ld32(trow + s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
+      tmem_ld32(trow + s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[S_FREE + b]);
+      if (lane == 0) mbar_arrive(&bar[S_FREE + t * 2 + sb]);
+      PF_TRACE(tq[1] += clock64() - tc; tc = clock64();)
       const int key0 = j * KT;
+      // raw scores; the scale (> 0) is applied with the max subtraction
       float mx = -INFINITY;
+      if (key0 + KT - 1 <= pos) {
 #pragma unroll
-      for (int c = 0; c < KT; ++c) {
-        const float v = (key0 + c <= pos) ? sv[c] * a.qscale : -INFINITY;
-        sv[c] = v;
-        mx = fmaxf(mx, v);
+        for (int c = 0; c < KT; ++c) mx = fmaxf(mx, sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          sv[c] = (key0 + c <= pos) ? sv[c] : -INFINITY;
+          mx = fmaxf(mx, sv[c]);
+        }
       }
-      if (j == n_tiles - 1 && kv_end - key0 < KT) {
-        // V rows past the last needed key: zero (stale or poisoned data)
+      mx *= qscale;
+      if (t == 0 && j == n_tiles - 1 && kv_end - key0 < KT) {
+        // V rows past the last needed key: zero (stale or poisoned data),
+        // after this tile's V copies landed; tile 0's PV of this KV tile is
+        // issued before tile 1's
+        if (!mbar_wait(&bar[V_FULL + j % NST], (j / NST) & 1)) {
+          ok = false;
+          break;
+        }
         const int kval = kv_end - key0;
-        for (int i = tid; i < (KT - kval) * C::HALVES * 8; i += 128) {
+        for (int i = r; i < (KT - kval) * C::HALVES * 8; i += MT) {
           const int row = kval + i / (C::HALVES * 8);
           const int rem = i % (C::HALVES * 8);
-          *reinterpret_cast<uint4 *>(smem + C::OFF_V + b * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
+          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (j % NST) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      // P buffer b and O are free once the previous tile's PV completed
+      PF_TRACE(tq[2] += clock64() - tc; tc = clock64();)
+      // this tile's P buffer and O are free once its previous PV completed
       if (j > 0) {
-        if (!mbar_wait(&bar[PV_DONE + ((j - 1) & 1)], ((j - 1) >> 1) & 1)) {
+        if (!mbar_wait(&bar[PV_DONE + t], (j - 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
       }
+      PF_TRACE(tq[3] += clock64() - tc; tc = clock64();)
       const float m_new = fmaxf(m_ref, mx);
       const bool raise = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
       if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY)) {
@@ -297,23 +428,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
-          tmem_ld32(trow + C::O_COL + c0, o);
+          tmem_ld32(trow + o_col + c0, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tmem_st32(trow + C::O_COL + c0, o);
+          tmem_st32(trow + o_col + c0, o);
         }
       }
       if (raise) m_ref = m_new;
-      const float ref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint8_t *ph_ = smem + C::OFF_P + b * 2 * C::PB + r * 128;
+      PF_TRACE(tq[4] += clock64() - tc; tc = clock64();)
+      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      uint8_t *ph_ = smem + C::OFF_P + t * 2 * C::PB + r * 128;
       uint8_t *pl_ = ph_ + C::PB;
 #pragma unroll
       for (int c8 = 0; c8 < KT / 8; ++c8) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(sv[c8 * 8 + 2 * e] - ref);
-          const float p1 = exp2f(sv[c8 * 8 + 2 * e + 1] - ref);
+          const float p0 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e], qscale, nref));
+          const float p1 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e + 1], qscale, nref));
           l += p0 + p1;
           hi[e] = pack_bf16x2(p0, p1);
           lo[e] = pack_bf16x2(p0 - bf16lo(hi[e]), p1 - bf16hi(hi[e]));
@@ -322,24 +454,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         *reinterpret_cast<uint4 *>(ph_ + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(pl_ + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      PF_TRACE(tq[5] += clock64() - tc; tc = clock64();)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[P_FULL + b]);
+      if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
+      PF_TRACE(tq[6] += clock64() - tc;)
     }
-    if (ok) {
-      const int t = n_tiles - 1;
-      if (!mbar_wait(&bar[PV_DONE + (t & 1)], (t >> 1) & 1)) ok = false;
-    }
+    PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+             if (tid == 0 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
+    if (ok && !mbar_wait(&bar[PV_DONE + t], (n_tiles - 1) & 1)) ok = false;
     if (ok) {
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float *orow = nullptr;
-      if (rv) orow = a.out + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (r - qi * g)) * D;
+      if (rv) orow = a.out + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
-        tmem_ld32(trow + C::O_COL + c0, o);
+        tmem_ld32(trow + o_col + c0, o);
         if (rv) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
@@ -347,7 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         }
       }
       if (rv && a.lse)
-        a.lse[static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (r - qi * g)] = (m_ref + log2f(l)) * kLn2;
+        a.lse[static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)] = (m_ref + log2f(l)) * kLn2;
     } else if (lane == 0) {
       *s_abort = 1;
     }
@@ -358,13 +491,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   if (*s_abort) {
     if (tid == 0) atomicOr(&g_prefill_err, kErrWaitTimeout);
-    if (warp == 4 && lane == 0) {
-      // the copies of the last two issued tiles must land before exit
-      for (int t = max(0, *s_last_tile - 1); t <= *s_last_tile; ++t) mbar_wait(&bar[KV_FULL + (t & 1)], (t >> 1) & 1);
+    if (warp == kProducerWarp && lane == 0) {
+      // the copies of the last NST issued tiles must land before exit
+      for (int t = max(0, *s_last_k - NST + 1); t <= *s_last_k; ++t) mbar_wait(&bar[K_FULL + t % NST], (t / NST) & 1);
+      for (int t = max(0, *s_last_v - NST + 1); t <= *s_last_v; ++t) mbar_wait(&bar[V_FULL + t % NST], (t / NST) & 1);
     }
-    if (warp == 5 && lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
       // wait (bounded) for every MMA this thread issued before freeing TMEM
-      uint64_t *drain = &bar[S_FULL];  // reuse: commit once more and wait for it
+      uint64_t *drain = &bar[S_FULL];
       mbar_init(drain, 1);
       fence_mbar_init();
       umma_commit(drain);
@@ -372,7 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     }
     __syncthreads();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -420,7 +554,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   a.num_kv_heads = d.num_kv_heads;
   a.num_q_heads = d.num_q_heads;
   a.g = d.num_q_heads / d.num_kv_heads;
-  a.qt = MROWS / a.g;
+  a.qt = MROWS / a.g;  // queries per CTA
   a.qscale = scale * kLog2e;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
@@ -441,6 +575,13 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
 }
 
 }  // namespace pftc
+
+#ifdef PA_PREFILL_TRACE
+extern "C" PA_API int pa_debug_prefill_trace_read(unsigned long long *host, int rows) {
+  if (rows > 4096) rows = 4096;
+  return static_cast<int>(cudaMemcpyFromSymbol(host, pftc::g_pf_trace, sizeof(unsigned long long) * 16 * rows));
+}
+#endif
 
 cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const void *q,
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
