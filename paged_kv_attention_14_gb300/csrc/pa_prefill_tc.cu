@@ -13,29 +13,35 @@
 //    one sequence times the g query heads of one kv head, so every K/V tile
 //    feeds the whole GQA group.  The rows form two 128-row Q tiles (A, B)
 //    that ping-pong: while one tile's softmax runs, the tensor cores work on
-//    the other tile.  Q is staged once; K/V are walked in 64-key tiles
-//    gathered block by block through the block table by TMA (two
-//    128-byte-swizzled boxes per 16-token block) into two 3-stage rings, one
-//    for K and one for V, shared by both Q tiles.  A K slot is released as
-//    soon as the QKs that read it complete, a V slot after its PVs, so the
-//    copies run up to three tiles ahead of the tensor cores.
-//  * Warp 9 (one thread) issues the MMAs: S_t = Q_t K^T (M 128, N 64, K 16 x
-//    head_dim/16) into one of tile t's two TMEM S buffers, and O_t += P_t V
-//    (M 128, N head_dim, K 16 x 4) with P_t from shared memory and V read
-//    MN-major, in the order QK_A(j+1), QK_B(j+1), PV_A(j), PV_B(j): the
-//    scores of the next KV tile are computed while the softmax of this one
-//    runs.
-//  * Warps 0-3 (tile A) and 4-7 (tile B), one thread per row with the row's
-//    64 scores in registers, do the online softmax: scale, causal mask, row
-//    max, exp2, row sum, and write P
-//    as a bf16 hi + lo pair (P = hi + lo to ~2^-17 relative; two PV MMAs)
-//    so the bf16 tensor-core result keeps near-fp32 accuracy.  The running
-//    max is only raised (and O rescaled in TMEM) when it grows by more than
-//    2^8, so O is rarely touched before the end.
+//    the other tile.  Q is staged once in shared memory; K/V are walked in
+//    128-key tiles gathered block by block through the block table by TMA
+//    (128-byte-swizzled boxes of 16 rows) into a 3-stage K ring and a
+//    2-stage V ring shared by both Q tiles.  A K slot is released as soon
+//    as the QKs that read it complete, a V slot after its PVs.
+//  * Warp 0 (one thread) issues the MMAs.  S_t = Q_t K^T (M 128, N 128 keys,
+//    K 16 x head_dim/16; both operands in shared memory) lands in tile t's
+//    128 TMEM columns.  The softmax overwrites those columns with P_t as a
+//    bf16 hi + lo pair (each 32-key chunk's pair in that chunk's columns) (P = hi + lo to ~2^-17 relative, so the bf16 tensor
+//    core product keeps near-fp32 accuracy), and O_t += P_t V (M 128,
+//    N head_dim, K 16 x 8, twice) takes P_t straight from tensor memory
+//    as the A operand and V MN-major from shared memory.  Order per KV tile
+//    j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1); one commit after each QK
+//    tells tile t's softmax that its next scores are ready AND that its
+//    previous PV finished (so O_t may be rescaled and S_t overwritten).
+//    M 128 MMAs with N <= 128 cost the same per instruction (measured on
+//    GB300: ~84 cycles with both operands in shared memory, ~78 with A in
+//    tensor memory, 128 at N 256), hence the 128-key tile.
+//  * Warps 4-7 (tile A) and 8-11 (tile B), one thread per row, do the online
+//    softmax in one pass over the row's 128 scores in TMEM, 32 at a time
+//    (the next 32 loading meanwhile): causal mask, row max (a tree of
+//    three-input maxima), exp2 of the scaled scores, row sum and the P
+//    pair, with packed fp32x2 arithmetic.  The running max is only raised
+//    (and O and the chunks of P already written rescaled in TMEM) when it
+//    grows by more than 2^8, so that path is rare.
 //  * Keys past the chunk's last position are masked; V rows past it are
 //    zeroed in shared memory before the last PV (0 * NaN would not vanish).
-//  * Warp 8 issues the TMA copies and prefetches block-table entries one
-//    tile ahead.
+//  * Warp 1 issues the TMA copies and prefetches block-table entries one
+//    tile ahead.  Warps 2-3 only take part in staging Q.
 //  * Every wait is bounded; on a timeout the kernel records an error bit,
 //    lets its own MMAs and copies drain and frees its TMEM before returning.
 #include <cuda.h>
@@ -49,14 +55,22 @@ namespace pftc {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int KT = 64;         // keys per KV tile
+constexpr int KT = 128;        // keys per KV tile (N of the QK MMA)
+constexpr int BPT = KT / 16;   // cache blocks per KV tile
 constexpr int MT = 128;        // rows of one Q tile (one TMEM lane per row)
 constexpr int NQT = 2;         // Q tiles per CTA (ping-pong between two softmax warpgroups)
 constexpr int MROWS = MT * NQT;
-constexpr int NTHREADS = 320;  // warps 0-3 softmax A, 4-7 softmax B, 8 TMA producer, 9 MMA issuer
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int NST = 3;         // stages of the K ring and of the V ring
+// Warp roles.  The MMA issuer and the TMA producer take the lowest warp
+// numbers: they must be scheduled promptly on sub-partitions shared with
+// busy softmax warps, and the warp schedulers favour older warps.  Softmax
+// warp w may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so each
+// Q tile's warpgroup starts at a multiple of four.
+constexpr int NTHREADS = 384;  // warp 0 MMA issuer, 1 TMA producer, 2-3 idle, 4-7 softmax A, 8-11 softmax B
+constexpr int kMmaWarp = 0;
+constexpr int kProducerWarp = 1;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int NSK = 3;         // stages of the K ring
+constexpr int NSV = 2;         // stages of the V ring
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 struct Args {
@@ -82,11 +96,25 @@ static __device__ int g_prefill_err;
 
 // Optional timeline counters (compiled only with -DPA_PREFILL_TRACE), per
 // CTA slot (blockIdx linearised, first 4096): softmax warp 0 lane 0 cycles
-// [0] waiting for S, [1] loading S from TMEM, [2] masking and max, [3]
-// waiting for the previous PV, [4] rescaling O, [5] exp2 and P stores, [6]
-// fence and arrive, [7] total; MMA thread cycles [8] waiting for K/V, [9]
-// waiting for S_FREE, [10] waiting for P, [11] total; producer [12] waiting
-// for a free K/V buffer, [13] total; [14] KV tiles.
+// [0] waiting for S, [1] loading S, masking and max, [2] rescaling O, [3]
+// exp2 and P stores, [4] fence and arrive, [7] total; MMA thread cycles [8]
+// waiting for V, [9] waiting for K, [10] waiting for P, [11] total;
+// producer [12] waiting for free slots, [13] total; [14] KV tiles.
+// Optional event timeline of CTA (0, 0, 0) (compiled only with
+// -DPA_PREFILL_TIMELINE): clock64 per KV tile j of [0] P_A seen by the MMA
+// thread, [1] PV_A + QK_A issued, [2] P_B seen, [3] PV_B + QK_B issued,
+// [4] S_A seen by softmax A, [5] P_A arrived, [6] S_B seen, [7] P_B arrived,
+// [8 + w] softmax warp w arrived, [16] V seen by the MMA thread, [17]
+// V_EMPTY committed, [18] K_EMPTY committed, [19] start of the V wait,
+// softmax A: [20] after the fence, [21] first scores loaded, [22] chunks
+// done, [23] stores done.
+#ifdef PA_PREFILL_TIMELINE
+static __device__ long long g_pf_tl[24][64];
+#define PF_TL(i, j) \
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (j) < 64) g_pf_tl[i][j] = clock64()
+#else
+#define PF_TL(i, j)
+#endif
 #ifdef PA_PREFILL_TRACE
 static __device__ unsigned long long g_pf_trace[4096][16];
 #define PF_TRACE(...) __VA_ARGS__
@@ -101,38 +129,36 @@ struct Cfg {
   static constexpr int QB = HALVES * QHALF;      // one Q tile
   static constexpr int KVHALF = KT * 128;        // bytes of one half of a K or V tile
   static constexpr int KVB = HALVES * KVHALF;
-  static constexpr int PB = MT * KT * 2;         // one P matrix (hi or lo), 128 x 64 bf16
-  static constexpr int OFF_Q = 0;                // [NQT]
-  static constexpr int OFF_K = OFF_Q + NQT * QB;    // [NST]
-  static constexpr int OFF_V = OFF_K + NST * KVB;   // [NST]
-  static constexpr int OFF_P = OFF_V + NST * KVB;   // [NQT][hi, lo]
-  static constexpr int OFF_BAR = OFF_P + NQT * 2 * PB;
+  static constexpr int OFF_Q = 0;                  // [NQT]
+  static constexpr int OFF_K = OFF_Q + NQT * QB;   // [NSK]
+  static constexpr int OFF_V = OFF_K + NSK * KVB;  // [NSV]
+  static constexpr int OFF_BAR = OFF_V + NSV * KVB;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers, TMEM slot, 1024-B alignment slack
+  // at least half an SM's shared memory, so that two CTAs (each holding
+  // all 512 TMEM columns) never share an SM
+  static constexpr int SMEM_LAUNCH = SMEM > 120 * 1024 ? SMEM : 120 * 1024;
   static_assert(SMEM <= 232448, "shared memory of one CTA");
-  // TMEM columns: two S buffers of each Q tile (KT each), then O of each Q
-  // tile (D each)
-  static constexpr uint32_t S_COL = 0;
-  static constexpr uint32_t O_COL = NQT * 2 * KT;
-  static constexpr uint32_t COLS_USED = NQT * 2 * KT + NQT * D;
-  static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+  // TMEM columns: S_t of each Q tile (KT each; P_t hi | lo written over it),
+  // then O_t (D each)
+  static constexpr uint32_t O_COL = NQT * KT;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(NQT * (KT + D) <= TMEM_COLS, "TMEM columns");
   static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true);
   // bytes landed per 16-token block of K (or of V), all halves
   static constexpr uint32_t BLOCK_BYTES = HALVES * 16u * 128u;
 };
 
-// barriers: K_FULL[NST], K_EMPTY[NST], V_FULL[NST], V_EMPTY[NST],
-// S_FULL[tile][2], S_FREE[tile][2], P_FULL[tile], PV_DONE[tile]
+// barriers: K_FULL[NSK], K_EMPTY[NSK], V_FULL[NSV], V_EMPTY[NSV],
+// S_FULL[tile], P_FULL[tile]
 enum Bar {
   K_FULL = 0,
-  K_EMPTY = K_FULL + NST,
-  V_FULL = K_EMPTY + NST,
-  V_EMPTY = V_FULL + NST,
-  S_FULL = V_EMPTY + NST,
-  S_FREE = S_FULL + 4,
-  P_FULL = S_FREE + 4,
-  PV_DONE = P_FULL + 2,
-  NBAR = PV_DONE + 2
+  K_EMPTY = K_FULL + NSK,
+  V_FULL = K_EMPTY + NSK,
+  V_EMPTY = V_FULL + NSV,
+  S_FULL = V_EMPTY + NSV,
+  P_FULL = S_FULL + NQT,
+  NBAR = P_FULL + NQT
 };
 static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
@@ -169,19 +195,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   const int rows_used = a.qt * g;
 
   if (tid == 0) {
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < NSK; ++i) {
       mbar_init(&bar[K_FULL + i], 1);
       mbar_init(&bar[K_EMPTY + i], 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
       mbar_init(&bar[V_FULL + i], 1);
       mbar_init(&bar[V_EMPTY + i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[P_FULL + i], 4);
-      mbar_init(&bar[PV_DONE + i], 1);
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bar[S_FULL + i], 1);
-      mbar_init(&bar[S_FREE + i], 4);
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(&bar[S_FULL + t], 1);
+      mbar_init(&bar[P_FULL + t], 4);
     }
     *s_abort = 0;
     *s_last_k = -1;
@@ -219,28 +243,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     // ------------------------------------------------------ TMA producer
     const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
     const uint64_t pol = l2_evict_first_policy();
-    // lane -> (K or V, block of the tile, half)
-    const int kv = lane / (4 * C::HALVES);
-    const int bi = (lane / C::HALVES) & 3;
+    // lane -> (block of the tile, half); the same lanes copy K and V
+    const int bi = lane / C::HALVES;
     const int hh = lane % C::HALVES;
-    const bool issuer = lane < 2 * 4 * C::HALVES;
+    const bool issuer = lane < BPT * C::HALVES;
     int phys_next = 0;
     if (issuer && bi * 16 < kv_end) phys_next = __ldg(table + bi);
     PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % NST;
-      const uint32_t ph = (j / NST) & 1;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
       const int phys = phys_next;
       const int key0 = j * KT;
-      const int lb = (j + 1) * 4 + bi;  // prefetch the next tile's block id
+      const int lb = (j + 1) * BPT + bi;  // prefetch the next tile's block id
       phys_next = (issuer && lb * 16 < kv_end) ? __ldg(table + lb) : 0;
-      const int nblk = min(4, (kv_end - key0 + 15) / 16);
+      const int nblk = min(BPT, (kv_end - key0 + 15) / 16);
       const int row = (phys * a.num_kv_heads + kvh) * 16;
-      // K of tile j (its slot frees once the QKs of tile j - NST completed),
-      // then V of tile j (once the PVs of tile j - NST completed)
-      bool ok = true;
+      // K of tile j (its slot frees once the QKs of tile j - NSK completed),
+      // then V of tile j (once the PVs of tile j - NSV completed)
 #pragma unroll 1
-      for (int part = 0; part < 2 && ok; ++part) {
+      for (int part = 0; part < 2; ++part) {
+        const int st = part ? j % NSV : j % NSK;
+        const uint32_t ph = part ? (j / NSV) & 1 : (j / NSK) & 1;
         const int full = (part ? V_FULL : K_FULL) + st;
         PF_TRACE(const long long tw = clock64();)
         if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1)) {
@@ -250,110 +273,111 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         PF_TRACE(tp_wait += clock64() - tw;)
         if (lane == 0) mbar_arrive_expect_tx(&bar[full], nblk * C::BLOCK_BYTES);
         __syncwarp();
-        if (issuer && kv == part && bi < nblk) {
+        if (issuer && bi < nblk) {
           uint8_t *dst = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB + hh * C::KVHALF + bi * 16 * 128;
           tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
         }
         if (lane == 0) *(part ? s_last_v : s_last_k) = j;
       }
-      if (!ok) {
-        if (lane == 0) *s_abort = 1;
-        break;
-      }
     }
+    if (!ok && lane == 0) *s_abort = 1;
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
              if (lane == 0 && slot < 4096) { g_pf_trace[slot][12] = tp_wait; g_pf_trace[slot][13] = clock64() - tp0; g_pf_trace[slot][14] = n_tiles; })
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       bool ok = true;
-      auto qk = [&](int t, int j) {  // S_t[j & 1] = Q_t K_j^T
-        const int b = j & 1;
+      auto qk = [&](int t, int j) {  // S_t = Q_t K_j^T
         const uint32_t qbase = sbase + C::OFF_Q + t * C::QB;
-        const uint32_t kbase = sbase + C::OFF_K + (j % NST) * C::KVB;
+        const uint32_t kbase = sbase + C::OFF_K + (j % NSK) * C::KVB;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * C::KVHALF + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + C::S_COL + (t * 2 + b) * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + t * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bar[S_FULL + t * 2 + b]);
       };
-      auto pv = [&](int t, int j) {  // O_t += P_t V_j
-        const uint32_t pbase = sbase + C::OFF_P + t * 2 * C::PB;
-        const uint32_t vbase = sbase + C::OFF_V + (j % NST) * C::KVB;
+      auto pv = [&](int t, int j) {  // O_t += (P_t hi + P_t lo) V_j, P_t from TMEM
+        const uint32_t vbase = sbase + C::OFF_V + (j % NSV) * C::KVB;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {  // hi, then lo
+        for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk) {
-            const uint64_t ad = umma_desc_sw128(pbase + part * C::PB + kk * 32, 16, 1024);
+            // keys 16 kk .. 16 kk + 15: chunk kk / 2, hi at +0, lo at +16
             const uint64_t bd = umma_desc_sw128(vbase + kk * 2048, C::KVHALF, 1024);
-            umma_bf16_ss(tmem + C::O_COL + t * D, ad, bd, C::IDESC_PV, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + C::O_COL + t * D, tmem + t * KT + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8, bd,
+                         C::IDESC_PV, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        umma_commit(&bar[PV_DONE + t]);
       };
-      // S of KV tile j + 1 is computed before the PV of tile j, so the next
-      // scores are ready when a tile's softmax finishes
-      PF_TRACE(const long long tm0 = clock64(); long long tm_kv = 0, tm_sf = 0, tm_p = 0; long long tw;)
+      PF_TRACE(const long long tm0 = clock64(); long long tm_v = 0, tm_k = 0, tm_p = 0; long long tw;)
+      // Issue order per KV tile j: PV_A(j), QK_A(j+1), S_A commit, K_EMPTY(j)
+      // commit, PV_B(j), V_EMPTY(j) commit, QK_B(j+1), S_B commit.  The
+      // tensor pipe queues only a couple of instructions, so the buffer
+      // releases are committed between MMAs (while the pipe has work) and
+      // the thread goes straight from the last MMA of a tile to the waits
+      // for the next one.
       if (!mbar_wait(&bar[K_FULL], 0)) ok = false;
       if (ok) {
         tc_fence_after_sync();
-        for (int t = 0; t < NQT; ++t) qk(t, 0);
-        umma_commit(&bar[K_EMPTY]);
+        for (int t = 0; t < NQT; ++t) {
+          qk(t, 0);
+          umma_commit(&bar[S_FULL + t]);
+        }
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) {
-          const int j1 = j + 1;
-          PF_TRACE(tw = clock64();)
-          if (!mbar_wait(&bar[K_FULL + j1 % NST], (j1 / NST) & 1)) {
-            ok = false;
-            break;
-          }
-          PF_TRACE(tm_kv += clock64() - tw;)
-          for (int t = 0; t < NQT && ok; ++t) {
-            PF_TRACE(tw = clock64();)
-            if (!mbar_wait(&bar[S_FREE + t * 2 + (j1 & 1)], ((j1 >> 1) & 1) ^ 1)) {
-              ok = false;
-              break;
-            }
-            PF_TRACE(tm_sf += clock64() - tw;)
-            tc_fence_after_sync();
-            qk(t, j1);
-          }
-          if (ok) umma_commit(&bar[K_EMPTY + j1 % NST]);  // K of tile j + 1 is consumed
-        }
-        if (!ok) break;
+        const bool next = j + 1 < n_tiles;
         PF_TRACE(tw = clock64();)
-        if (!mbar_wait(&bar[V_FULL + j % NST], (j / NST) & 1)) {
+        PF_TL(19, j);
+        if (!mbar_wait(&bar[V_FULL + j % NSV], (j / NSV) & 1)) {
           ok = false;
           break;
         }
-        PF_TRACE(tm_kv += clock64() - tw;)
-        for (int t = 0; t < NQT && ok; ++t) {
+        PF_TRACE(tm_v += clock64() - tw;)
+        PF_TL(16, j);
+        for (int t = 0; t < NQT; ++t) {
           PF_TRACE(tw = clock64();)
-          if (!mbar_wait(&bar[P_FULL + t], j & 1)) {
+          if (!mbar_wait_hint(&bar[P_FULL + t], j & 1)) {
             ok = false;
             break;
           }
           PF_TRACE(tm_p += clock64() - tw;)
+          PF_TL(t * 2, j);
           tc_fence_after_sync();
           pv(t, j);
+          if (t == NQT - 1) umma_commit(&bar[V_EMPTY + j % NSV]);  // both tiles are done with V of tile j
+          if (next) {
+            if (t == 0) {
+              PF_TRACE(tw = clock64();)
+              if (!mbar_wait(&bar[K_FULL + (j + 1) % NSK], ((j + 1) / NSK) & 1)) {
+                ok = false;
+                break;
+              }
+              PF_TRACE(tm_k += clock64() - tw;)
+              tc_fence_after_sync();
+            }
+            qk(t, j + 1);
+          }
+          // S_t of tile j + 1 is ready and PV_t(j) has completed (after the
+          // last tile: O_t is final)
+          umma_commit(&bar[S_FULL + t]);
+          if (t == 0) umma_commit(&bar[K_EMPTY + j % NSK]);  // both tiles are done with K of tile j
+          PF_TL(t * 2 + 1, j);
         }
-        if (ok) umma_commit(&bar[V_EMPTY + j % NST]);  // both tiles are done with V of tile j
       }
       if (!ok) *s_abort = 1;
       PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-               if (slot < 4096) { g_pf_trace[slot][8] = tm_kv; g_pf_trace[slot][9] = tm_sf; g_pf_trace[slot][10] = tm_p; g_pf_trace[slot][11] = clock64() - tm0; })
+               if (slot < 4096) { g_pf_trace[slot][8] = tm_v; g_pf_trace[slot][9] = tm_k; g_pf_trace[slot][10] = tm_p; g_pf_trace[slot][11] = clock64() - tm0; })
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------ softmax, one row per thread
-    const int t = warp >> 2;  // Q tile of this warpgroup
+    const int t = (warp - kSoftmaxWarp0) >> 2;  // Q tile of this warpgroup
     const int r = tid & (MT - 1);
     const int R = t * MT + r;
     // TMEM lane = row; warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = t * KT;
     const uint32_t o_col = C::O_COL + t * D;
     const int qi = R / g;
     const bool rv = R < rows_used && qi < nq;
@@ -361,43 +385,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const float qscale = a.qscale;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc;)
+    PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc, tk;)
     for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
       PF_TRACE(tc = clock64();)
-      if (!mbar_wait(&bar[S_FULL + t * 2 + sb], (j >> 1) & 1)) {
+      if (!mbar_wait_hint(&bar[S_FULL + t], j & 1)) {
         ok = false;
         break;
       }
       PF_TRACE(tq[0] += clock64() - tc; tc = clock64();)
+      if (r == 0) PF_TL(4 + t * 2, j);
       tc_fence_after_sync();
-      float sv[KT];
-      const uint32_t s_col = C::S_COL + (t * 2 + sb) * KT;
-      tmem_ld32(trow + s_col, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      tmem_ld32(trow + s_col + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[S_FREE + t * 2 + sb]);
-      PF_TRACE(tq[1] += clock64() - tc; tc = clock64();)
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(20, j);
       const int key0 = j * KT;
-      // raw scores; the scale (> 0) is applied with the max subtraction
-      float mx = -INFINITY;
-      if (key0 + KT - 1 <= pos) {
-#pragma unroll
-        for (int c = 0; c < KT; ++c) mx = fmaxf(mx, sv[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          sv[c] = (key0 + c <= pos) ? sv[c] : -INFINITY;
-          mx = fmaxf(mx, sv[c]);
-        }
-      }
-      mx *= qscale;
       if (t == 0 && j == n_tiles - 1 && kv_end - key0 < KT) {
         // V rows past the last needed key: zero (stale or poisoned data),
         // after this tile's V copies landed; tile 0's PV of this KV tile is
         // issued before tile 1's
-        if (!mbar_wait(&bar[V_FULL + j % NST], (j / NST) & 1)) {
+        if (!mbar_wait(&bar[V_FULL + j % NSV], (j / NSV) & 1)) {
           ok = false;
           break;
         }
@@ -405,65 +409,129 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         for (int i = r; i < (KT - kval) * C::HALVES * 8; i += MT) {
           const int row = kval + i / (C::HALVES * 8);
           const int rem = i % (C::HALVES * 8);
-          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (j % NST) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
+          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (j % NSV) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      PF_TRACE(tq[2] += clock64() - tc; tc = clock64();)
-      // this tile's P buffer and O are free once its previous PV completed
-      if (j > 0) {
-        if (!mbar_wait(&bar[PV_DONE + t], (j - 1) & 1)) {
-          ok = false;
-          break;
+      PF_TRACE(tq[1] += clock64() - tc; tc = clock64();)
+      // One pass over the row's scores, 32 keys (one TMEM chunk) at a time,
+      // the next chunk's load in flight while this one is processed.  The
+      // 32 keys of chunk c (columns 32c .. 32c + 31 of this tile's block)
+      // become 16 columns of bf16 hi pairs (keys 2e, 2e + 1 in column
+      // 32c + e) and, behind them, 16 columns of lo pairs, so a chunk only
+      // overwrites its own, already loaded, scores.  The running max is
+      // checked per chunk; O_t is stable meanwhile (the commit this thread
+      // waited for follows PV_t(j - 1)).
+      uint32_t sc[2][32];
+      tmem_ld32_async(trow + s_col, sc[0]);
+      tmem_wait_ld(sc[0]);
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(21, j);
+#pragma unroll
+      for (int c = 0; c < KT / 32; ++c) {
+        uint32_t(&cur)[32] = sc[c & 1];
+        PF_TRACE(tk = clock64();)
+        if (c + 1 < KT / 32) tmem_ld32_async(trow + s_col + (c + 1) * 32, sc[(c + 1) & 1]);
+        PF_TRACE(tq[4] += clock64() - tk; tk = clock64();)
+        const int kc = key0 + c * 32;
+        const bool unmasked = kc + 31 <= pos;
+        if (!unmasked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (kc + i > pos) cur[i] = __float_as_uint(-INFINITY);
         }
-        tc_fence_after_sync();
-      }
-      PF_TRACE(tq[3] += clock64() - tc; tc = clock64();)
-      const float m_new = fmaxf(m_ref, mx);
-      const bool raise = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
-      if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY)) {
-        // rescale this warp's O rows in TMEM (rows that do not raise scale by 1)
-        const float corr = (raise && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-        if (raise) l *= corr;
+        // raw scores; the scale (> 0) is applied with the max subtraction.
+        // Tree of three-input maxima (depth 4, not a 32-long chain).
+        float mx;
+        {
+          float m[11];
+#pragma unroll
+          for (int i = 0; i < 10; ++i)
+            m[i] = fmax3(__uint_as_float(cur[3 * i]), __uint_as_float(cur[3 * i + 1]), __uint_as_float(cur[3 * i + 2]));
+          m[10] = fmaxf(__uint_as_float(cur[30]), __uint_as_float(cur[31]));
+          mx = fmaxf(fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmax3(m[6], m[7], m[8])),
+                     fmaxf(m[9], m[10]));
+        }
+        mx *= qscale;
+        const float m_new = fmaxf(m_ref, mx);
+        const bool raise = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
+        if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY)) {
+          // rare: rescale this warp's O rows and the P chunks of this tile
+          // written so far (rows that do not raise scale by 1)
+          PF_TRACE(const long long tr = clock64();)
+          const float corr = (raise && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
+          if (raise) l *= corr;
+          if (j > 0) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float o[32];
-          tmem_ld32(trow + o_col + c0, o);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              float o[32];
+              tmem_ld32(trow + o_col + c0, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tmem_st32(trow + o_col + c0, o);
+              for (int i = 0; i < 32; ++i) o[i] *= corr;
+              tmem_st32(trow + o_col + c0, o);
+            }
+          }
+          tmem_wait_st();
+#pragma unroll 1
+          for (int cp = 0; cp < c; ++cp) {
+            float pv[32];
+            tmem_ld32(trow + s_col + cp * 32, pv);
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const uint32_t h = __float_as_uint(pv[e]), w = __float_as_uint(pv[16 + e]);
+              const float p0 = (bf16lo(h) + bf16lo(w)) * corr;
+              const float p1 = (bf16hi(h) + bf16hi(w)) * corr;
+              hi[e] = pack_bf16x2(p0, p1);
+              lo[e] = pack_bf16x2(p0 - bf16lo(hi[e]), p1 - bf16hi(hi[e]));
+            }
+            tmem_st16_async(trow + s_col + cp * 32, hi);
+            tmem_st16_async(trow + s_col + cp * 32 + 16, lo);
+          }
+          PF_TRACE(tq[2] += clock64() - tr;)
         }
-      }
-      if (raise) m_ref = m_new;
-      PF_TRACE(tq[4] += clock64() - tc; tc = clock64();)
-      const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      uint8_t *ph_ = smem + C::OFF_P + t * 2 * C::PB + r * 128;
-      uint8_t *pl_ = ph_ + C::PB;
+        if (raise) m_ref = m_new;
+        PF_TRACE(tq[5] += clock64() - tk; tk = clock64();)
+        const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const uint64_t qs2 = f2_pack(qscale, qscale), nr2 = f2_pack(nref, nref);
+        // p in pairs (packed fp32x2 arithmetic); row-sum partials in two
+        // packed accumulators (four independent chains)
+        uint64_t lsum[2] = {0, 0};
+        uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int c8 = 0; c8 < KT / 8; ++c8) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e], qscale, nref));
-          const float p1 = ex2_approx(fmaf(sv[c8 * 8 + 2 * e + 1], qscale, nref));
-          l += p0 + p1;
+        for (int e = 0; e < 16; ++e) {
+          const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])),
+                                            qs2, nr2));
+          const float p0 = ex2_approx(x.x);
+          const float p1 = ex2_approx(x.y);
+          const uint64_t pp = f2_pack(p0, p1);
+          lsum[e & 1] = f2_add(lsum[e & 1], pp);
           hi[e] = pack_bf16x2(p0, p1);
-          lo[e] = pack_bf16x2(p0 - bf16lo(hi[e]), p1 - bf16hi(hi[e]));
+          const float2 d = f2_unpack(f2_sub(pp, f2_pack(bf16lo(hi[e]), bf16hi(hi[e]))));
+          lo[e] = pack_bf16x2(d.x, d.y);
         }
-        const int off = ((c8 ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4 *>(ph_ + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(pl_ + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        {
+          const float2 l2 = f2_unpack(f2_add(lsum[0], lsum[1]));
+          l += l2.x + l2.y;
+        }
+        PF_TRACE(tq[6] += clock64() - tk;)
+        tmem_st16_async(trow + s_col + c * 32, hi);
+        tmem_st16_async(trow + s_col + c * 32 + 16, lo);
+        if (c + 1 < KT / 32) tmem_wait_ld(sc[(c + 1) & 1]);
       }
-      PF_TRACE(tq[5] += clock64() - tc; tc = clock64();)
-      fence_proxy_async_smem();
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(22, j);
+      tmem_wait_st();
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(23, j);
+      PF_TRACE(tq[3] += clock64() - tc; tc = clock64();)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
-      PF_TRACE(tq[6] += clock64() - tc;)
+      if (r == 0) PF_TL(5 + t * 2, j);
+      if (lane == 0) PF_TL(8 + warp - kSoftmaxWarp0, j);
     }
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-             if (tid == 0 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
-    if (ok && !mbar_wait(&bar[PV_DONE + t], (n_tiles - 1) & 1)) ok = false;
+             if (tid == kSoftmaxWarp0 * 32 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
+    if (ok && !mbar_wait(&bar[S_FULL + t], n_tiles & 1)) ok = false;
     if (ok) {
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -492,13 +560,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   if (*s_abort) {
     if (tid == 0) atomicOr(&g_prefill_err, kErrWaitTimeout);
     if (warp == kProducerWarp && lane == 0) {
-      // the copies of the last NST issued tiles must land before exit
-      for (int t = max(0, *s_last_k - NST + 1); t <= *s_last_k; ++t) mbar_wait(&bar[K_FULL + t % NST], (t / NST) & 1);
-      for (int t = max(0, *s_last_v - NST + 1); t <= *s_last_v; ++t) mbar_wait(&bar[V_FULL + t % NST], (t / NST) & 1);
+      // the copies of the last issued tiles of each ring must land before exit
+      for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t) mbar_wait(&bar[K_FULL + t % NSK], (t / NSK) & 1);
+      for (int t = max(0, *s_last_v - NSV + 1); t <= *s_last_v; ++t) mbar_wait(&bar[V_FULL + t % NSV], (t / NSV) & 1);
     }
     if (warp == kMmaWarp && lane == 0) {
       // wait (bounded) for every MMA this thread issued before freeing TMEM
-      uint64_t *drain = &bar[S_FULL];
+      uint64_t *drain = &bar[P_FULL];
       mbar_init(drain, 1);
       fence_mbar_init();
       umma_commit(drain);
@@ -559,7 +627,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
   auto fn = &prefill_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_LAUNCH);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -567,7 +635,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs);
   cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<D>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<D>::SMEM_LAUNCH;
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
@@ -576,6 +644,11 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
 
 }  // namespace pftc
 
+#ifdef PA_PREFILL_TIMELINE
+extern "C" PA_API int pa_debug_prefill_timeline_read(long long *host) {
+  return static_cast<int>(cudaMemcpyFromSymbol(host, pftc::g_pf_tl, sizeof(long long) * 24 * 64));
+}
+#endif
 #ifdef PA_PREFILL_TRACE
 extern "C" PA_API int pa_debug_prefill_trace_read(unsigned long long *host, int rows) {
   if (rows > 4096) rows = 4096;
