@@ -26,6 +26,7 @@ slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -43,13 +44,46 @@ FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = 2
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# each hot kernel, averaged over the launches of one ncu launch-list capture
+# of this bench's own command (see the summaries in profiles/).  A figure is reported only while the kernel's
+# source files hash to what they were when it was captured.
+CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
+NCU_TRAFFIC = {
+    # decode + merge kernels (the roofline times both)
+    "decode": {"workload": 2, "bytes": 306_520_816,
+               "sha256": "68e1c5f9b49733a6dffa1a8254e2a7c75ff163846f57ffc2b87af4b5f4f69809",
+               "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
+    "prefill": {"workload": 5, "bytes": 46_277_772, "sha256": "cb5debad4f3fa99cf9443786229586d51e5eeff575c5e98affc592addf0cd6e4",
+                "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
+}
+
+
+def _src_sha256(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _traffic(kernel: str, workload: int):
+    t = NCU_TRAFFIC[kernel]
+    if t["bytes"] is None or t["workload"] != workload or _src_sha256(t["sources"]) != t["sha256"]:
+        return None
+    return t["bytes"]
+
+
 def _peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, 'measured' | 'fallback')."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def _dist():
@@ -285,7 +319,7 @@ def run_ours(args):
         e2e_s = float(t[0])
 
     if rank == 0:
-        peak, peak_kind = _peaks()
+        peak, tc_peak, peak_kind = _peaks()
         gbs = ws * kv_bytes / (step_ms * 1e-3) / 1e9
         dec_gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
         line = {
@@ -313,15 +347,25 @@ def run_ours(args):
                          "kernel": "pa_decode (decode kernel + merge kernel), timed alone per call",
                          "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
-                         "traffic": None},
+                         "traffic": _traffic("decode", args.workload)},
             "e2e": {"value": round(ws * kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * K + (launches_per_step - 1) * K2,
             "clocks": clocks,
         }
         if mixed:
+            pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
             line["prefill"] = {"kernel": "pa_prefill_chunk", "us": round(pf_ms * 1e3, 2), "flops": pf_flops,
-                               "tflops": round(pf_flops / (pf_ms * 1e-3) / 1e12, 1)}
+                               "tflops": round(pf_tf, 1)}
+            if pf_ms > dec_ms:
+                # the prefill dominates the step: the roofline is its tensor-core bound
+                # (algorithmic flops; the bf16 hi/lo split of P adds half again to PV)
+                line["roofline_decode"] = line["roofline"]
+                line["roofline"] = {"bound": "tensor", "kernel": "pa_prefill_chunk, timed alone per call",
+                                    "achieved": round(pf_tf, 1), "peak": tc_peak,
+                                    "peak_kind": f"{peak_kind} bf16 dense (burst)", "unit": "TFLOP/s",
+                                    "frac": round(pf_tf / tc_peak, 4), "kernel_us": round(pf_ms * 1e3, 2),
+                                    "traffic": _traffic("prefill", args.workload)}
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
