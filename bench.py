@@ -53,10 +53,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
     # decode + merge kernels (the roofline times both)
-    "decode": {"workload": 2, "bytes": 306_520_816,
-               "sha256": "68e1c5f9b49733a6dffa1a8254e2a7c75ff163846f57ffc2b87af4b5f4f69809",
+    "decode": {"workload": 2, "bytes": 306_494_745,
+               "sha256": "475a31949c0f12d43a94c3c94226b745014ff84c3f9391a95789047dec2a2a99",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
-    "prefill": {"workload": 5, "bytes": 46_277_772, "sha256": "cb5debad4f3fa99cf9443786229586d51e5eeff575c5e98affc592addf0cd6e4",
+    "prefill": {"workload": 5, "bytes": 46_278_070, "sha256": "bc8c2e7ae729a2b90f2c5db2f3b92ade271efd2710271e0cd2262636172a18a8",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
 }
 

@@ -85,6 +85,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 // critical path resumes sooner after the phase completes.
 __device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
+  if (mbar_test(addr, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1

@@ -312,12 +312,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       };
       PF_TRACE(const long long tm0 = clock64(); long long tm_v = 0, tm_k = 0, tm_p = 0; long long tw;)
       // Issue order per KV tile j: PV_A(j), QK_A(j+1), S_A commit, K_EMPTY(j)
-      // commit, PV_B(j), V_EMPTY(j) commit, QK_B(j+1), S_B commit.  The
-      // tensor pipe queues only a couple of instructions, so the buffer
-      // releases are committed between MMAs (while the pipe has work) and
-      // the thread goes straight from the last MMA of a tile to the waits
-      // for the next one.
-      if (!mbar_wait(&bar[K_FULL], 0)) ok = false;
+      // commit, PV_B(j), V_EMPTY(j) commit, wait for V(j+1), QK_B(j+1), S_B
+      // commit.  The tensor pipe queues only a few instructions, so buffer
+      // releases and the V wait sit between MMAs (while the pipe has work)
+      // and the thread goes straight from the last MMA of a KV tile to the
+      // wait for the next tile's P_A.
+      if (!mbar_wait(&bar[K_FULL], 0) || !mbar_wait(&bar[V_FULL], 0)) ok = false;
       if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < NQT; ++t) {
@@ -327,35 +327,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const bool next = j + 1 < n_tiles;
-        PF_TRACE(tw = clock64();)
-        PF_TL(19, j);
-        if (!mbar_wait(&bar[V_FULL + j % NSV], (j / NSV) & 1)) {
-          ok = false;
-          break;
-        }
-        PF_TRACE(tm_v += clock64() - tw;)
-        PF_TL(16, j);
         for (int t = 0; t < NQT; ++t) {
-          PF_TRACE(tw = clock64();)
           if (!mbar_wait_hint(&bar[P_FULL + t], j & 1)) {
             ok = false;
             break;
           }
-          PF_TRACE(tm_p += clock64() - tw;)
           PF_TL(t * 2, j);
           tc_fence_after_sync();
           pv(t, j);
-          if (t == NQT - 1) umma_commit(&bar[V_EMPTY + j % NSV]);  // both tiles are done with V of tile j
+          if (t == NQT - 1) {
+            umma_commit(&bar[V_EMPTY + j % NSV]);  // both tiles are done with V of tile j
+            if (next && !mbar_wait(&bar[V_FULL + (j + 1) % NSV], ((j + 1) / NSV) & 1)) {
+              ok = false;
+              break;
+            }
+          }
           if (next) {
             if (t == 0) {
-              PF_TRACE(tw = clock64();)
               if (!mbar_wait(&bar[K_FULL + (j + 1) % NSK], ((j + 1) / NSK) & 1)) {
                 ok = false;
                 break;
               }
-              PF_TRACE(tm_k += clock64() - tw;)
-              tc_fence_after_sync();
             }
+            tc_fence_after_sync();
             qk(t, j + 1);
           }
           // S_t of tile j + 1 is ready and PV_t(j) has completed (after the
