@@ -33,12 +33,13 @@ int resolve_impl(const pa_kv_desc &d) {
 }
 
 // kv heads handled together by one stage of the MMA kernel (one TMA copy
-// moves one block for all of them).  Measured on GB300: E4M3 caches gain
-// from groups of 4 (fewer, larger copies); bf16 head_dim-128 tiles are 4 KB
-// per head already and stream best one head per stage.
+// moves one block for all of them).  Measured on GB300: bf16 head_dim-128
+// tiles are 4 KB per head already and stream best one head per stage; the
+// E4M3 kernel (8 consumer warps) is fastest with pairs of heads (2 KB
+// tiles), the bf16 head_dim-64 one with groups of 4.
 int head_group(const pa_kv_desc &d) {
   if (d.kv_dtype == PA_KV_BF16 && d.head_dim == 128) return 1;
-  if (d.num_kv_heads % 4 == 0) return 4;
+  if (d.kv_dtype == PA_KV_BF16 && d.num_kv_heads % 4 == 0) return 4;
   if (d.num_kv_heads % 2 == 0) return 2;
   return 1;
 }

@@ -727,7 +727,7 @@ __device__ __forceinline__ uint32_t swz_off(int row, int ch) {
 
 // D: head_dim; KVT: cache type; GQ: largest group size served (4, 8 or 16,
 // rounded up to the MMA's 8-wide n-tiles); HG: kv heads per stage; NS: stages.
-template <int D_, int KVT_, int GQ_, int HG_, int NS_>
+template <int D_, int KVT_, int GQ_, int HG_, int NS_, int NC_>
 struct MmaCfg {
   static constexpr int D = D_;
   static constexpr int KVT = KVT_;
@@ -735,7 +735,7 @@ struct MmaCfg {
   static constexpr int NN = (GQ_ + 7) / 8;  // n-tiles of 8 query heads in the MMAs
   static constexpr int HG = HG_;
   static constexpr int NS = NS_;
-  static constexpr int NC = kConsumerWarps;  // warp NC produces, NC + 1 finishes
+  static constexpr int NC = NC_;  // consumer warps; warp NC produces, NC + 1 finishes
   static constexpr int BPS = NC / HG;        // blocks per stage: one (block, head) tile per consumer warp
   static constexpr int ESZ = (KVT == kKvBf16) ? 2 : 1;
   static constexpr int ROWB = D * ESZ;
@@ -863,9 +863,9 @@ __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *
   }
 }
 
-template <int D, int KVT, int GQ, int HG, int NS>
-__global__ void __launch_bounds__((kConsumerWarps + 2) * 32, 1) decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
-  using C = MmaCfg<D, KVT, GQ, HG, NS>;
+template <int D, int KVT, int GQ, int HG, int NS, int NCW>
+__global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
+  using C = MmaCfg<D, KVT, GQ, HG, NS, NCW>;
   constexpr int MT = D / 16;  // m-tiles of O^T (16 head_dim rows each) = k-steps of S^T
   constexpr int NN = C::NN;
   constexpr int NC = C::NC;
@@ -1311,17 +1311,22 @@ KernelInfo simt_info() {
 }
 
 // MMA: as many stages as fit next to the partial-state buffers in about
-// 220 KB of shared memory (at most 12), one CTA per SM
-template <int D, int KVT, int GQ, int HG>
+// 220 KB of shared memory (at most 12), one CTA per SM.  NCW consumer warps:
+// 4 suffice to keep up with the bf16 stream; the E4M3 consumers also
+// convert every element (about one instruction per KV byte) and need 8, two
+// per SM sub-partition, to hide each other's latency (measured on GB300:
+// 67% -> 89% of the HBM copy rate).
+template <int D, int KVT, int GQ, int HG, int NCW = kConsumerWarps>
 KernelInfo mma_info() {
   constexpr int ESZ = KVT == kKvBf16 ? 2 : 1;
-  constexpr int STAGEB = 2 * kConsumerWarps * 16 * D * ESZ + ((HG * GQ * D * 2 + 1023) / 1024) * 1024;
-  constexpr int RED = 2 * kConsumerWarps * GQ * (D + 4) * 4;
+  constexpr int STAGEB = 2 * NCW * 16 * D * ESZ + ((HG * GQ * D * 2 + 1023) / 1024) * 1024;
+  constexpr int RED = 2 * NCW * GQ * (D + 4) * 4;
   constexpr int FIT = (225280 - 2048 - RED) / STAGEB;
   constexpr int NS = FIT > 12 ? 12 : FIT;
-  using Cfg = MmaCfg<D, KVT, GQ, HG, NS>;
+  static_assert(NS >= 3, "at least three stages in flight");
+  using Cfg = MmaCfg<D, KVT, GQ, HG, NS, NCW>;
   KernelInfo k;
-  k.fn = reinterpret_cast<void *>(&decode_mma_kernel<D, KVT, GQ, HG, NS>);
+  k.fn = reinterpret_cast<void *>(&decode_mma_kernel<D, KVT, GQ, HG, NS, NCW>);
   k.smem = Cfg::SMEM;
   k.threads = Cfg::NTHREADS;
   k.slot_heads = Cfg::SLOTH;

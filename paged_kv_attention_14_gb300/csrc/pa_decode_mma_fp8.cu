@@ -1,16 +1,23 @@
 // pa_decode_mma_fp8.cu -- instantiations of the tensor-core decode kernel
 // for E4M3 caches: head_dim 64 and 128, groups of up to 4, 8 or 16 query
-// heads per kv head, 1, 2 or 4 kv heads per stage.
+// heads per kv head, 1 or 2 kv heads per stage.
 #include "pa_decode_kernels.cuh"
 
 namespace pa {
 namespace dec {
 
+// 8 consumer warps (see mma_info) while their partial-state buffers leave
+// room for enough stages (up to 8 query heads per kv head), else 4;
+// kv-head groups of 2 or 1
+template <int GQ>
+constexpr int fp8_consumer_warps() {
+  return GQ <= 8 ? 8 : 4;
+}
+
 template <int D, int GQ>
 static KernelInfo mma_for_hg(int hg) {
-  if (hg >= 4) return mma_info<D, kKvFp8, GQ, 4>();
-  if (hg >= 2) return mma_info<D, kKvFp8, GQ, 2>();
-  return mma_info<D, kKvFp8, GQ, 1>();
+  if (hg >= 2) return mma_info<D, kKvFp8, GQ, 2, fp8_consumer_warps<GQ>()>();
+  return mma_info<D, kKvFp8, GQ, 1, fp8_consumer_warps<GQ>()>();
 }
 
 template <int D>
