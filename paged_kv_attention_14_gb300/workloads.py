@@ -214,29 +214,40 @@ def _decode_batch(name, seed, lens, Hq, Hkv, D, kv_dtype, scale, device, poison,
     return b
 
 
+#: the name each workload carries (and the bench reports)
+WORKLOAD_NAMES = {
+    1: "tiny paged decode: 4 seqs, lens {1,7,16,33}, 4q/2kv heads, D=64",
+    2: "Qwen3-8B-shaped decode: 32 seqs, lens U[512,4096], 32q/8kv, D=128, bf16 KV",
+    3: "long/skewed decode: 8 lognormal seqs in [128,32768] + 1 x 131072, 32q/8kv, D=128, bf16 KV",
+    4: "FP8 KV decode: 128 seqs, lens U[1024,8192], 40q/8kv, D=128, E4M3 KV",
+    5: "mixed continuous-batch step: 16 decode (U[256,4096]) + 4 x 512-token prefill chunks on 2048-token "
+       "prefixes (1024 shared), 32q/8kv, D=128, bf16",
+}
+
+
 def workload(n: int, device="cpu", poison: bool = False) -> PagedBatch:
     """Build workload ``n`` (1..5) on ``device``."""
     seed = 1000 + n
     if n == 1:
-        return _decode_batch("tiny paged decode: 4 seqs, lens {1,7,16,33}, 4q/2kv heads, D=64",
+        return _decode_batch(WORKLOAD_NAMES[1],
                              seed, [1, 7, 16, 33], 4, 2, 64, KV_BF16, 1.0 / 8.0, device, poison,
                              num_blocks=64)
     if n == 2:
         g = _gen(seed, "cpu")
         lens = torch.randint(512, 4096 + 1, (32,), generator=g)
-        return _decode_batch("Qwen3-8B-shaped decode: 32 seqs, lens U[512,4096], 32q/8kv, D=128, bf16 KV",
+        return _decode_batch(WORKLOAD_NAMES[2],
                              seed, lens.tolist(), 32, 8, 128, KV_BF16, 1.0 / math.sqrt(128),
                              device, poison)
     if n == 3:
         g = _gen(seed, "cpu")
         ln = torch.empty(8, dtype=torch.float64).log_normal_(math.log(2048.0), 1.0, generator=g)
         lens = [int(min(max(round(float(x)), 128), 32768)) for x in ln] + [131072]
-        return _decode_batch("long/skewed decode: 8 lognormal seqs in [128,32768] + 1 x 131072, 32q/8kv, D=128, bf16 KV",
+        return _decode_batch(WORKLOAD_NAMES[3],
                              seed, lens, 32, 8, 128, KV_BF16, 1.0 / math.sqrt(128), device, poison)
     if n == 4:
         g = _gen(seed, "cpu")
         lens = torch.randint(1024, 8192 + 1, (128,), generator=g)
-        return _decode_batch("FP8 KV decode: 128 seqs, lens U[1024,8192], 40q/8kv, D=128, E4M3 KV",
+        return _decode_batch(WORKLOAD_NAMES[4],
                              seed, lens.tolist(), 40, 8, 128, KV_FP8, 1.0 / math.sqrt(128),
                              device, poison)
     if n == 5:
@@ -277,8 +288,7 @@ def _mixed_batch(seed, device, poison) -> PagedBatch:
     slots = torch.cat([dec_slots, torch.tensor(pf_slots, dtype=torch.int64)])
     T = int(slots.shape[0])
 
-    b = PagedBatch(name="mixed continuous-batch step: 16 decode (U[256,4096]) + 4 x 512-token "
-                        "prefill chunks on 2048-token prefixes (1024 shared), 32q/8kv, D=128, bf16",
+    b = PagedBatch(name=WORKLOAD_NAMES[5],
                    block_size=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, kv_dtype=KV_BF16,
                    scale=_f32(1.0 / math.sqrt(D)), k_scale=1.0, v_scale=1.0, num_blocks=NB,
                    k_pool=None, v_pool=None)
