@@ -29,6 +29,7 @@ _lib = None
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_FP8_E5M2 = 2
 
 
 def build(force: bool = False) -> str:
@@ -56,6 +57,10 @@ def _load():
         lib.pa_oracle_e4m3_decode.restype = ctypes.c_double
         lib.pa_oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.pa_oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.pa_oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
+        lib.pa_oracle_e5m2_decode.restype = ctypes.c_double
+        lib.pa_oracle_e5m2_encode.argtypes = [ctypes.c_double]
+        lib.pa_oracle_e5m2_encode.restype = ctypes.c_uint8
         lib.pa_oracle_cache_write.argtypes = [I, I, I, I, P, P, P, I, F, F, P, P]
         lib.pa_oracle_cache_write.restype = None
         lib.pa_oracle_attend_range.argtypes = [I, I, I, I, P, P, P, P, I, I, I, F, F, F, P, P]
@@ -78,7 +83,7 @@ def _np(a, dtype):
         t = a.detach().cpu().contiguous()
         if t.dtype in (torch.bfloat16, torch.float16):
             t = t.view(torch.int16)
-        elif t.dtype == torch.float8_e4m3fn:
+        elif t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
             t = t.view(torch.uint8)
         a = t.numpy()
     a = np.ascontiguousarray(a)
@@ -105,6 +110,14 @@ def e4m3_decode(byte: int) -> float:
 
 def e4m3_encode(x: float) -> int:
     return int(_load().pa_oracle_e4m3_encode(float(x)))
+
+
+def e5m2_decode(byte: int) -> float:
+    return _load().pa_oracle_e5m2_decode(int(byte) & 0xFF)
+
+
+def e5m2_encode(x: float) -> int:
+    return int(_load().pa_oracle_e5m2_encode(float(x)))
 
 
 def cache_write(kv_dtype, block_size, num_kv_heads, head_dim, k, v, slot_mapping,

@@ -15,9 +15,10 @@
  *   - "paged attention (block-paged KV cache)" and "chunked prefill" -- section
  *     "What's implemented (CPU, behaviorally tested)" of the "vllm.cpp"
  *     repository listing (Engine core and Model forward bullets).
- *   - fp8 pages of one byte per element, E4M3 -- table in "2. CLI Configuration
- *     Parameters" (--kv-cache-dtype) and the table in "Step 6: Status of
- *     TurboQuant Support" of the walkthrough.
+ *   - fp8 pages of one byte per element, E4M3 or E5M2 -- table in "2. CLI
+ *     Configuration Parameters" (--kv-cache-dtype) and the table in "Step 6:
+ *     Status of TurboQuant Support" of the walkthrough (its vllm.cpp row names
+ *     E4M3/E5M2 block-paged KV allocation).
  *   - a prefix-cache hit binds a new sequence's block table to existing
  *     physical pages -- "1. Technical Mechanics of the Radix Cache" (Zero-Copy
  *     Cache Hits) of the walkthrough.
@@ -26,7 +27,7 @@
  *
  * Layout (the reading this build takes where the pages are silent):
  *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
- *                      bf16 bit patterns (uint16) or E4M3 bytes (uint8)
+ *                      bf16 bit patterns (uint16) or E4M3 / E5M2 bytes (uint8)
  *   q                : [tokens][num_q_heads][head_dim] bf16 bit patterns
  *   block_tables     : int32 [num_seqs][max_blocks_per_seq]
  *   context_lens     : int32 [num_seqs], KV tokens including this step's
@@ -35,7 +36,8 @@
  *
  * Parity pins: every function here is pinned by tests that do not reuse its
  * code (brute-force dense attention through torch's CPU SDPA, closed forms,
- * invariants, torch's float8_e4m3fn codec); see tests/test_oracle_pins.py.
+ * invariants, torch's float8_e4m3fn and float8_e5m2 codecs); see
+ * tests/test_oracle_pins.py.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +46,7 @@
 
 #define KV_BF16 0
 #define KV_FP8_E4M3 1
+#define KV_FP8_E5M2 2
 
 /* ---------------------------------------------------------------- bf16 */
 
@@ -121,17 +124,78 @@ uint8_t pa_oracle_e4m3_encode(double x) {
   return (uint8_t)(sign | best);
 }
 
+/* ---------------------------------------------------------------- E5M2 */
+
+/*
+ * OCP 8-bit floating point, E5M2 variant: 1 sign bit, 5 exponent bits with
+ * bias 15, 2 mantissa bits, IEEE-style specials: exponent 11111 is +-inf
+ * (mantissa 0) or NaN (mantissa != 0).  Exponent field 0 encodes subnormals
+ * m/4 * 2^(1-15).  Largest finite magnitude 1.75 * 2^15 = 57344.
+ */
+double pa_oracle_e5m2_decode(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int e = (byte >> 2) & 0x1F;
+  int m = byte & 0x3;
+  double v;
+  if (e == 0x1F) {
+    if (m != 0) return NAN;
+    v = INFINITY;
+  } else if (e == 0) {
+    v = ldexp((double)m / 4.0, 1 - 15);
+  } else {
+    v = ldexp(1.0 + (double)m / 4.0, e - 15);
+  }
+  return sign ? -v : v;
+}
+
+static double e5m2_value[256];
+static int e5m2_value_ready = 0;
+
+static void e5m2_table_init(void) {
+  if (e5m2_value_ready) return;
+  for (int c = 0; c < 256; ++c) e5m2_value[c] = pa_oracle_e5m2_decode((uint8_t)c);
+  e5m2_value_ready = 1;
+}
+
+/*
+ * Round-to-nearest-even onto the finite E5M2 values with saturation to the
+ * largest finite magnitude (57344; +-inf saturates too), NaN -> 0x7F: the same
+ * plain nearest-code search as for E4M3, over the 124 non-negative finite
+ * codes 0x00 .. 0x7B.
+ */
+uint8_t pa_oracle_e5m2_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  e5m2_table_init();
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs(x);
+  if (a >= 57344.0) return (uint8_t)(sign | 0x7B);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 0x7B; ++c) {
+    double v = e5m2_value[c];
+    double err = fabs(a - v);
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
 /* Element (t, d) of one kv head, decoded to a real number (scale applied). */
 static double kv_elem(int kv_dtype, const void *cache, int64_t row_index, int head_dim, int d,
                       double scale) {
   if (kv_dtype == KV_BF16) {
     const uint16_t *c = (const uint16_t *)cache;
     return bf16_bits_to_double(c[row_index * head_dim + d]);
-  } else {
-    const uint8_t *c = (const uint8_t *)cache;
-    e4m3_table_init();
-    return e4m3_value[c[row_index * head_dim + d]] * scale;
   }
+  const uint8_t *c = (const uint8_t *)cache;
+  if (kv_dtype == KV_FP8_E5M2) {
+    e5m2_table_init();
+    return e5m2_value[c[row_index * head_dim + d]] * scale;
+  }
+  e4m3_table_init();
+  return e4m3_value[c[row_index * head_dim + d]] * scale;
 }
 
 /* Row index of logical token t of kv head kh for a sequence's block table. */
@@ -147,7 +211,8 @@ static int64_t cache_row(const int32_t *table_row, int block_size, int num_kv_he
  * For each token i with slot_mapping[i] >= 0: block = slot / block_size,
  * offset = slot % block_size, and for every kv head h the cache row
  * (block, h, offset) receives enc(k[i][h][:]) (same for v).
- * enc = bit copy for bf16; for E4M3, enc(x) = e4m3(fl32(fl32(x) / scale)).
+ * enc = bit copy for bf16; for E4M3 / E5M2, enc(x) = e4m3 / e5m2 of
+ * fl32(fl32(x) / scale).
  */
 void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int head_dim,
                            const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
@@ -169,8 +234,10 @@ void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int h
         } else {
           float kq = bf16_bits_to_float(ks[d]) / k_scale;
           float vq = bf16_bits_to_float(vs[d]) / v_scale;
-          ((uint8_t *)k_cache)[dst_row * head_dim + d] = pa_oracle_e4m3_encode((double)kq);
-          ((uint8_t *)v_cache)[dst_row * head_dim + d] = pa_oracle_e4m3_encode((double)vq);
+          uint8_t kc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)kq) : pa_oracle_e4m3_encode((double)kq);
+          uint8_t vc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)vq) : pa_oracle_e4m3_encode((double)vq);
+          ((uint8_t *)k_cache)[dst_row * head_dim + d] = kc;
+          ((uint8_t *)v_cache)[dst_row * head_dim + d] = vc;
         }
       }
     }
@@ -197,8 +264,8 @@ void pa_oracle_attend_range(int kv_dtype, int block_size, int num_kv_heads, int 
     *lse = -INFINITY;
     return;
   }
-  double ks = (kv_dtype == KV_FP8_E4M3) ? (double)k_scale : 1.0;
-  double vs = (kv_dtype == KV_FP8_E4M3) ? (double)v_scale : 1.0;
+  double ks = (kv_dtype != KV_BF16) ? (double)k_scale : 1.0;
+  double vs = (kv_dtype != KV_BF16) ? (double)v_scale : 1.0;
   double *x = (double *)malloc(sizeof(double) * (size_t)n);
   double m = -INFINITY;
   for (int j = 0; j < n; ++j) {

@@ -38,7 +38,11 @@ import torch
 BLOCK_SIZE = 16
 KV_BF16 = "bf16"
 KV_FP8 = "fp8_e4m3"
+KV_FP8_E5M2 = "fp8_e5m2"
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+#: the largest finite magnitude of each 8-bit cache format
+FP8_MAX = {KV_FP8: E4M3_MAX, KV_FP8_E5M2: E5M2_MAX}
 
 
 @dataclass
@@ -163,15 +167,15 @@ def _fill_pool(b: PagedBatch, g, device, poison: bool, readable: torch.Tensor,
     shape = (b.num_blocks, b.num_kv_heads, b.block_size, b.head_dim)
     b.k_pool = _randn(shape, g, device)
     b.v_pool = _randn(shape, g, device)
-    if b.kv_dtype == KV_FP8:
-        # per-tensor scales from the source values (amax / E4M3 max)
+    if b.kv_dtype in FP8_MAX:
+        # per-tensor scales from the source values (amax / the format's max)
         ka = float(b.k_pool.float().abs().max())
         va = float(b.v_pool.float().abs().max())
         if b.k_new is not None and b.meta.get("k_new_independent"):
             ka = max(ka, float(b.k_new.float().abs().max()))
             va = max(va, float(b.v_new.float().abs().max()))
-        b.k_scale = _f32(ka / E4M3_MAX)
-        b.v_scale = _f32(va / E4M3_MAX)
+        b.k_scale = _f32(ka / FP8_MAX[b.kv_dtype])
+        b.v_scale = _f32(va / FP8_MAX[b.kv_dtype])
     if poison:
         bad = ~readable
         if written is not None:

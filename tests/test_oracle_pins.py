@@ -1,7 +1,7 @@
 """Pins of the fp64 oracle against things other than itself.
 
 Each test checks the oracle against a library routine (torch's CPU SDPA and
-its float8_e4m3fn codec), a closed form, an invariant, or the format
+its float8_e4m3fn / float8_e5m2 codecs), a closed form, an invariant, or the format
 definition's fixed points -- chosen so that a plausible slip anywhere in the
 oracle (wrong GQA index, wrong block offset, a dropped scale, an off-by-one in
 the causal position, a sign in the merge, an exponent bias) fails one of them.
@@ -15,7 +15,9 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import workloads as W
 
-BF16, FP8 = oracle.KV_BF16, oracle.KV_FP8_E4M3
+BF16, FP8, E5M2 = oracle.KV_BF16, oracle.KV_FP8_E4M3, oracle.KV_FP8_E5M2
+#: generator cache type -> (oracle code, torch 8-bit dtype)
+_FP8_KINDS = {W.KV_FP8: (FP8, torch.float8_e4m3fn), W.KV_FP8_E5M2: (E5M2, torch.float8_e5m2)}
 
 
 # ------------------------------------------------------------ helpers (independent)
@@ -24,9 +26,9 @@ def _bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
-def _fp8_cache_to_f64(cache_u8: np.ndarray, scale: float) -> np.ndarray:
-    """Decode E4M3 bytes with torch's own float8_e4m3fn codec (library routine)."""
-    t = torch.from_numpy(np.ascontiguousarray(cache_u8)).view(torch.float8_e4m3fn)
+def _fp8_cache_to_f64(cache_u8: np.ndarray, scale: float, dtype=torch.float8_e4m3fn) -> np.ndarray:
+    """Decode 8-bit cache bytes with torch's own float8 codec (library routine)."""
+    t = torch.from_numpy(np.ascontiguousarray(cache_u8)).view(dtype)
     return t.to(torch.float64).numpy() * float(scale)
 
 
@@ -53,15 +55,24 @@ def _sdpa(q, k, v, scale, mask=None):
 
 
 def _oracle_caches(b: W.PagedBatch):
-    """Caches as the oracle reads them: bf16 pool as-is, or the E4M3 encoding of
-    the whole (small) pool made by the oracle's own cache write."""
+    """Caches as the oracle reads them: bf16 pool as-is, or the E4M3 / E5M2
+    encoding of the whole (small) pool made by the oracle's own cache write."""
     if b.kv_dtype == W.KV_BF16:
         return BF16, b.k_pool, b.v_pool
+    code = _FP8_KINDS[b.kv_dtype][0]
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)
-    kc, vc = oracle.cache_write(FP8, b.block_size, b.num_kv_heads, b.head_dim, k, v, slots, z, z,
+    kc, vc = oracle.cache_write(code, b.block_size, b.num_kv_heads, b.head_dim, k, v, slots, z, z,
                                 b.k_scale, b.v_scale)
-    return FP8, kc, vc
+    return code, kc, vc
+
+
+def _dense_pools(b: W.PagedBatch, kc, vc):
+    """K and V pools in fp64: the bf16 pool, or the 8-bit caches decoded by torch."""
+    if b.kv_dtype == W.KV_BF16:
+        return _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    dt = _FP8_KINDS[b.kv_dtype][1]
+    return _fp8_cache_to_f64(kc, b.k_scale, dt), _fp8_cache_to_f64(vc, b.v_scale, dt)
 
 
 def _oracle_decode(b: W.PagedBatch, pairs=None):
@@ -125,6 +136,57 @@ def test_e4m3_encode_saturates_and_keeps_nan_and_signed_zero():
         assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
 
 
+# ------------------------------------------------------------------ E5M2 codec
+
+def test_e5m2_fixed_points_of_the_format_definition():
+    # OCP FP8 E5M2: bias 15, max finite 57344, min normal 2^-14, min subnormal
+    # 2^-16, exponent field 31 is inf (mantissa 0) or NaN
+    assert oracle.e5m2_decode(0x7B) == 57344.0
+    assert oracle.e5m2_decode(0xFB) == -57344.0
+    assert oracle.e5m2_decode(0x3C) == 1.0
+    assert oracle.e5m2_decode(0x04) == 2.0 ** -14
+    assert oracle.e5m2_decode(0x03) == 3 * 2.0 ** -16
+    assert oracle.e5m2_decode(0x01) == 2.0 ** -16
+    assert oracle.e5m2_decode(0x00) == 0.0 and math.copysign(1, oracle.e5m2_decode(0x80)) == -1
+    assert oracle.e5m2_decode(0x7C) == math.inf and oracle.e5m2_decode(0xFC) == -math.inf
+    assert all(math.isnan(oracle.e5m2_decode(c)) for c in (0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF))
+
+
+def test_e5m2_decode_matches_torch_float8_for_all_256_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e5m2).to(torch.float64).numpy()
+    mine = np.array([oracle.e5m2_decode(int(c)) for c in codes])
+    same = (ref == mine) | (np.isnan(ref) & np.isnan(mine))
+    assert same.all(), np.nonzero(~same)
+
+
+def test_e5m2_encode_matches_torch_rne_inside_the_finite_range():
+    rng = np.random.default_rng(6)
+    pos = np.array([oracle.e5m2_decode(c) for c in range(0x7C)])
+    mids = (pos[1:] + pos[:-1]) / 2  # exact ties: round half to even
+    xs = np.concatenate([rng.normal(0, 1, 2000), rng.normal(0, 4000, 2000), rng.uniform(-57344, 57344, 2000),
+                         mids, -mids, pos, -pos, [2.0 ** -17, 3 * 2.0 ** -17, 2.0 ** -18, 57343.0, 61439.0]])
+    xs = xs.astype(np.float32)  # the encoder's input is an fp32 quotient
+    ref = torch.from_numpy(xs).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    mine = np.array([oracle.e5m2_encode(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(ref, mine), np.nonzero(ref != mine)
+
+
+def test_e5m2_encode_saturates_and_keeps_nan_and_signed_zero():
+    # the chosen reading: finite overflow and +-inf saturate to +-57344 (torch's
+    # non-saturating codec returns inf from 61440 on)
+    assert oracle.e5m2_encode(61440.0) == 0x7B
+    assert oracle.e5m2_encode(1e9) == 0x7B
+    assert oracle.e5m2_encode(-1e30) == 0xFB
+    assert oracle.e5m2_encode(float("inf")) == 0x7B
+    assert oracle.e5m2_encode(float("-inf")) == 0xFB
+    assert oracle.e5m2_encode(float("nan")) == 0x7F
+    assert oracle.e5m2_encode(-0.0) == 0x80
+    assert oracle.e5m2_encode(-2.0 ** -18) == 0x80  # rounds to zero, keeps the sign
+    for c in list(range(0x7C)) + list(range(0x80, 0xFC)):
+        assert oracle.e5m2_encode(oracle.e5m2_decode(c)) == c
+
+
 # --------------------------------------------------------------- cache write
 
 def test_cache_write_bf16_is_a_scatter_of_bit_patterns():
@@ -138,23 +200,25 @@ def test_cache_write_bf16_is_a_scatter_of_bit_patterns():
     assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
 
 
-def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation():
+@pytest.mark.parametrize("kv", [W.KV_FP8, W.KV_FP8_E5M2])
+def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation(kv):
+    code, tdt = _FP8_KINDS[kv]
     g = torch.Generator().manual_seed(3)
     T, H, D, NB = 40, 2, 64, 8
     k = torch.randn(T, H, D, generator=g).to(torch.bfloat16)
     v = (3 * torch.randn(T, H, D, generator=g)).to(torch.bfloat16)
     slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
     slots[::7] = -1
-    ks = float(k.float().abs().max()) / 448
-    vs = float(v.float().abs().max()) / 448
+    ks = float(k.float().abs().max()) / W.FP8_MAX[kv]
+    vs = float(v.float().abs().max()) / W.FP8_MAX[kv]
     z = np.full((NB, H, 16, D), 0xAB, np.uint8)
-    kc, vc = oracle.cache_write(FP8, 16, H, D, k, v, slots, z, z, ks, vs)
+    kc, vc = oracle.cache_write(code, 16, H, D, k, v, slots, z, z, ks, vs)
     ref_k = z.copy()
     ref_v = z.copy()
     keep = slots >= 0
     s = slots[keep].numpy()
-    qk = (k[keep].float() / torch.tensor(ks, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
-    qv = (v[keep].float() / torch.tensor(vs, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    qk = (k[keep].float() / torch.tensor(ks, dtype=torch.float32)).to(tdt).view(torch.uint8)
+    qv = (v[keep].float() / torch.tensor(vs, dtype=torch.float32)).to(tdt).view(torch.uint8)
     ref_k[s // 16, :, s % 16, :] = qk.numpy()
     ref_v[s // 16, :, s % 16, :] = qv.numpy()
     assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
@@ -162,17 +226,14 @@ def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation():
 
 # ------------------------------------------------------------ decode attention
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_FP8_E5M2])
 @pytest.mark.parametrize("D,Hq,Hkv", [(8, 2, 2), (64, 4, 2), (8, 10, 2), (64, 5, 1)])
 def test_decode_matches_bruteforce_sdpa(kv, D, Hq, Hkv):
     lens = [1, 5, 16, 17, 40]
     b = W.random_decode(11 + D + Hq, lens, Hq, Hkv, D, kv_dtype=kv, poison=True)
     out, lse = _oracle_decode(b)
     kd, kc, vc = _oracle_caches(b)
-    if kd == BF16:
-        kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
-    else:
-        kf, vf = _fp8_cache_to_f64(kc, b.k_scale), _fp8_cache_to_f64(vc, b.v_scale)
+    kf, vf = _dense_pools(b, kc, vc)
     g = Hq // Hkv
     qf = _bf16_to_f64(b.q_decode)
     for s, L in enumerate(lens):
@@ -316,16 +377,13 @@ def _oracle_prefill(b: W.PagedBatch, pairs=None):
                           b.scale, b.k_scale, b.v_scale, pairs=pairs)
 
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_FP8_E5M2])
 def test_prefill_matches_bruteforce_sdpa_with_causal_mask(kv):
     q_lens, ctx = [5, 16, 1, 23], [5, 40, 33, 64]
     b = W.random_prefill(91, q_lens, ctx, 4, 2, 64, kv_dtype=kv, shared_prefix_blocks=1)
     out, _ = _oracle_prefill(b)
     kd, kc, vc = _oracle_caches(b)
-    if kd == BF16:
-        kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
-    else:
-        kf, vf = _fp8_cache_to_f64(kc, b.k_scale), _fp8_cache_to_f64(vc, b.v_scale)
+    kf, vf = _dense_pools(b, kc, vc)
     qf = _bf16_to_f64(b.q_prefill)
     qsl = b.query_start_loc.numpy()
     for s, (n, L) in enumerate(zip(q_lens, ctx)):
