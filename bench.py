@@ -42,6 +42,7 @@ METRIC = "paged decode attention: effective KV-read GB/s and % of GB300 HBM peak
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 WORKLOAD = 2
+FP8_FORMATS = {"e4m3": "fp8_e4m3", "e5m2": "fp8_e5m2"}  # -> workloads.KV_FP8 / KV_FP8_E5M2
 
 
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -170,8 +171,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     B.load(pa_build.build())
 
-    b = W.workload(args.workload, device=dev, poison=False)
-    kv = B.PA_KV_BF16 if b.kv_dtype == W.KV_BF16 else B.PA_KV_FP8_E4M3
+    b = W.workload(args.workload, device=dev, poison=False, fp8_format=FP8_FORMATS[args.fp8_format])
+    kv = {W.KV_BF16: B.PA_KV_BF16, W.KV_FP8: B.PA_KV_FP8_E4M3, W.KV_FP8_E5M2: B.PA_KV_FP8_E5M2}[b.kv_dtype]
     desc = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv,
                        b.k_scale if kv else 0.0, b.v_scale if kv else 0.0, decode_impl=args.decode_impl)
     if kv == B.PA_KV_BF16:
@@ -336,7 +337,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if kv == B.PA_KV_BF16 else "fp8_e4m3",
+            "dtype": b.kv_dtype,
             "data": "synthetic",
             "config": {"workload": b.name, "num_seqs": S, "kv_tokens": int(b.context_lens_decode.sum()),
                        "kv_bytes_per_step": kv_bytes,
@@ -500,6 +501,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
+                    help="8-bit cache format of workload 4 (same shapes)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

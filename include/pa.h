@@ -16,7 +16,7 @@
  *
  * Memory layout (the pages name no layout; this one is the library's choice):
  *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
- *                      bf16, or one E4M3 byte per element for FP8 KV.
+ *                      bf16, or one E4M3 or E5M2 byte per element for FP8 KV.
  *   q (decode)       : [num_seqs][num_q_heads][head_dim] bf16
  *   q (prefill)      : [total_query_tokens][num_q_heads][head_dim] bf16
  *   out              : same shape as q, fp32
@@ -75,8 +75,9 @@ typedef enum {
 } pa_status;
 
 typedef enum {
-  PA_KV_BF16 = 0,    /* bf16 K/V, bit copies of the written values          */
-  PA_KV_FP8_E4M3 = 1 /* OCP E4M3 bytes with per-tensor fp32 scales        */
+  PA_KV_BF16 = 0,     /* bf16 K/V, bit copies of the written values          */
+  PA_KV_FP8_E4M3 = 1, /* OCP E4M3 bytes with per-tensor fp32 scales        */
+  PA_KV_FP8_E5M2 = 2  /* OCP E5M2 bytes with per-tensor fp32 scales        */
 } pa_kv_dtype;
 
 /* Which decode kernel pa_decode runs.  0 lets the library choose. */
@@ -89,7 +90,7 @@ typedef enum {
 /* Which prefill kernel pa_prefill_chunk runs.  0 lets the library choose. */
 typedef enum {
   PA_PREFILL_AUTO = 0,
-  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; bf16 and E4M3 caches   */
+  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; bf16 and FP8 caches    */
   PA_PREFILL_TCGEN05 = 2   /* tcgen05 tensor-memory tiles; bf16 caches        */
 } pa_prefill_impl;
 
@@ -99,7 +100,8 @@ typedef enum {
  *   block_size   : tokens per block; 16 is the only supported value.
  *   head_dim     : 64 or 128.
  *   num_q_heads  : a multiple of num_kv_heads; group size g = q / kv <= 16.
- *   k_scale, v_scale : FP8 only.  Cached value = stored E4M3 value * scale.
+ *   k_scale, v_scale : FP8 only.  Cached value = stored E4M3 / E5M2 value *
+ *                  scale.
  *                  0 means 1.0.  Ignored for bf16.
  *   decode_impl  : a pa_decode_impl value.
  *   prefill_impl : a pa_prefill_impl value.
@@ -129,8 +131,9 @@ PA_API const char *pa_last_error(void);
  * slot_mapping[i] >= 0, block = slot / block_size and offset = slot %
  * block_size; for every kv head h, the cache row (block, h, offset) receives
  * k[i][h][:] (v likewise).  bf16 KV stores the bits unchanged.  FP8 KV stores
- * e4m3(fl32(x) / k_scale) rounded to nearest even with finite saturation to
- * +-448 and NaN kept as NaN (0x7F).
+ * e4m3 (or e5m2) of fl32(x) / k_scale, rounded to nearest even, with finite
+ * overflow saturating to +-448 (E4M3) or +-57344 (E5M2, where +-inf
+ * saturates too), and NaN kept as a NaN code.
  *   k, v : [num_tokens][num_kv_heads][head_dim] bf16, 16-byte aligned.
  * The write of a prefix-cache hit must not target a block shared with another
  * sequence ("Zero-Copy Cache Hits" of "1. Technical Mechanics of the Radix

@@ -27,6 +27,7 @@ PA_ERR_CUDA = 4
 
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
+PA_KV_FP8_E5M2 = 2
 
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
@@ -143,7 +144,7 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-_CACHE = (torch.bfloat16, torch.uint8, torch.float8_e4m3fn)
+_CACHE = (torch.bfloat16, torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
 _BF16 = (torch.bfloat16,)
 _F32 = (torch.float32,)
 _I32 = (torch.int32,)

@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
       uint16_t b[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        b[j] = pack_e4m3x2_satfinite(__fdiv_rn(bf16lo(w[j]), s), __fdiv_rn(bf16hi(w[j]), s));
+        b[j] = pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[j]), s), __fdiv_rn(bf16hi(w[j]), s));
       uint2 r;
       r.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
       r.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
@@ -70,6 +70,11 @@ cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v
   const float vs = d.v_scale == 0.f ? 1.f : d.v_scale;
   if (d.kv_dtype == PA_KV_BF16)
     cache_write_kernel<kKvBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+  else if (d.kv_dtype == PA_KV_FP8_E5M2)
+    cache_write_kernel<kKvE5M2><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
         vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);

@@ -48,7 +48,9 @@ KernelInfo kernel_for(const pa_kv_desc &d, int impl) {
   const int g = d.num_q_heads / d.num_kv_heads;
   if (impl == PA_DECODE_SIMT) return dec::pick_simt(d.head_dim, d.kv_dtype, g);
   const int hg = head_group(d);
-  return d.kv_dtype == PA_KV_BF16 ? dec::pick_mma_bf16(d.head_dim, g, hg) : dec::pick_mma_fp8(d.head_dim, g, hg);
+  if (d.kv_dtype == PA_KV_BF16) return dec::pick_mma_bf16(d.head_dim, g, hg);
+  if (d.kv_dtype == PA_KV_FP8_E5M2) return dec::pick_mma_e5m2(d.head_dim, g, hg);
+  return dec::pick_mma_fp8(d.head_dim, g, hg);
 }
 
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime
@@ -170,7 +172,7 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.num_q_heads = d.num_q_heads;
   a.g = d.num_q_heads / d.num_kv_heads;
   a.num_groups = plan.num_groups;
-  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  const bool fp8 = d.kv_dtype != PA_KV_BF16;
   const float ks = (fp8 && d.k_scale != 0.f) ? d.k_scale : 1.f;
   a.qscale = scale * ks * dec::kLog2e;
   a.vscale = (fp8 && d.v_scale != 0.f) ? d.v_scale : 1.f;

@@ -478,16 +478,16 @@ struct RowSlice {
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        e4m3x2_to_f32(static_cast<uint16_t>(w[c] & 0xffffu), x[4 * c + 0], x[4 * c + 1]);
-        e4m3x2_to_f32(static_cast<uint16_t>(w[c] >> 16), x[4 * c + 2], x[4 * c + 3]);
+        fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] & 0xffffu), x[4 * c + 0], x[4 * c + 1]);
+        fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] >> 16), x[4 * c + 2], x[4 * c + 3]);
       }
     } else {
       const uint2 u = *reinterpret_cast<const uint2 *>(row + j8 * 8);
       const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        e4m3x2_to_f32(static_cast<uint16_t>(w[c] & 0xffffu), x[4 * c + 0], x[4 * c + 1]);
-        e4m3x2_to_f32(static_cast<uint16_t>(w[c] >> 16), x[4 * c + 2], x[4 * c + 3]);
+        fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] & 0xffffu), x[4 * c + 0], x[4 * c + 1]);
+        fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] >> 16), x[4 * c + 2], x[4 * c + 3]);
       }
     }
   }
@@ -1000,14 +1000,14 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
         for (int j = 0; j < MT; j += 2) {
           uint32_t r0, r1, r2, r3;
           ldmatrix_x4(r0, r1, r2, r3, kt + swz_off<C::ROWB, HG>(trow + lr + (lm & 1) * 8, j + (lm >> 1)));
-          const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(r0 & 0xffffu));
-          const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(r0 >> 16));
-          const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(r1 & 0xffffu));
-          const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(r1 >> 16));
-          const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(r2 & 0xffffu));
-          const uint32_t b2 = e4m3x2_to_f16x2(static_cast<uint16_t>(r2 >> 16));
-          const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(r3 & 0xffffu));
-          const uint32_t b3 = e4m3x2_to_f16x2(static_cast<uint16_t>(r3 >> 16));
+          const uint32_t a0 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r0 & 0xffffu));
+          const uint32_t a2 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r0 >> 16));
+          const uint32_t a1 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r1 & 0xffffu));
+          const uint32_t a3 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r1 >> 16));
+          const uint32_t b0 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r2 & 0xffffu));
+          const uint32_t b2 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r2 >> 16));
+          const uint32_t b1 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r3 & 0xffffu));
+          const uint32_t b3 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(r3 >> 16));
 #pragma unroll
           for (int nn = 0; nn < NN; ++nn) {
             mma_f16_16816(sa[nn], a0, a1, a2, a3, qb[j][nn][0], qb[j][nn][1]);
@@ -1086,14 +1086,14 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
           // (t,d), (t,d+1), (t+1,d), (t+1,d+1); the permute pairs the tokens
           const uint32_t x0 = __byte_perm(r0, 0, 0x3120), x1 = __byte_perm(r1, 0, 0x3120);
           const uint32_t y0 = __byte_perm(r2, 0, 0x3120), y1 = __byte_perm(r3, 0, 0x3120);
-          const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(x0 & 0xffffu)) & mk_lo;
-          const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(x0 >> 16)) & mk_lo;
-          const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(x1 & 0xffffu)) & mk_hi;
-          const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(x1 >> 16)) & mk_hi;
-          const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 & 0xffffu)) & mk_lo;
-          const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(y0 >> 16)) & mk_lo;
-          const uint32_t b2 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 & 0xffffu)) & mk_hi;
-          const uint32_t b3 = e4m3x2_to_f16x2(static_cast<uint16_t>(y1 >> 16)) & mk_hi;
+          const uint32_t a0 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(x0 & 0xffffu)) & mk_lo;
+          const uint32_t a1 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(x0 >> 16)) & mk_lo;
+          const uint32_t a2 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(x1 & 0xffffu)) & mk_hi;
+          const uint32_t a3 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(x1 >> 16)) & mk_hi;
+          const uint32_t b0 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(y0 & 0xffffu)) & mk_lo;
+          const uint32_t b1 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(y0 >> 16)) & mk_lo;
+          const uint32_t b2 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(y1 & 0xffffu)) & mk_hi;
+          const uint32_t b3 = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(y1 >> 16)) & mk_hi;
 #pragma unroll
           for (int nn = 0; nn < NN; ++nn) {
             mma_f16_16816(oacc[j][nn], a0, a1, a2, a3, pb[nn][0], pb[nn][1]);
@@ -1337,10 +1337,32 @@ KernelInfo mma_info() {
   return k;
 }
 
+// 8-bit caches (E4M3 or E5M2, per KVT): 8 consumer warps (see mma_info)
+// while their partial-state buffers leave room for enough stages (up to 8
+// query heads per kv head), else 4; kv-head groups of 2 or 1.
+template <int GQ>
+constexpr int fp8_consumer_warps() {
+  return GQ <= 8 ? 8 : 4;
+}
+
+template <int KVT, int D, int GQ>
+KernelInfo fp8_mma_for_hg(int hg) {
+  if (hg >= 2) return mma_info<D, KVT, GQ, 2, fp8_consumer_warps<GQ>()>();
+  return mma_info<D, KVT, GQ, 1, fp8_consumer_warps<GQ>()>();
+}
+
+template <int KVT, int D>
+KernelInfo fp8_mma_for(int gq, int hg) {
+  if (gq <= 4) return fp8_mma_for_hg<KVT, D, 4>(hg);
+  if (gq <= 8) return fp8_mma_for_hg<KVT, D, 8>(hg);
+  return fp8_mma_for_hg<KVT, D, 16>(hg);
+}
+
 // Defined in the translation units that instantiate the kernels.
 KernelInfo pick_simt(int head_dim, int kv_dtype, int g);
 KernelInfo pick_mma_bf16(int head_dim, int gq, int hg);
-KernelInfo pick_mma_fp8(int head_dim, int gq, int hg);
+KernelInfo pick_mma_fp8(int head_dim, int gq, int hg);   // E4M3
+KernelInfo pick_mma_e5m2(int head_dim, int gq, int hg);
 
 }  // namespace dec
 }  // namespace pa

@@ -1,5 +1,5 @@
 // pa_decode_simt.cu -- instantiations of the CUDA-core decode kernel
-// (group sizes 1, 2 and 4; head_dim 64 and 128; bf16 and E4M3 caches).
+// (group sizes 1, 2 and 4; head_dim 64 and 128; bf16, E4M3 and E5M2 caches).
 #include "pa_decode_kernels.cuh"
 
 namespace pa {
@@ -12,9 +12,15 @@ static KernelInfo simt_for(int g) {
   return simt_info<D, KVT, 4>();
 }
 
+template <int D>
+static KernelInfo simt_for_dtype(int kv_dtype, int g) {
+  if (kv_dtype == PA_KV_BF16) return simt_for<D, kKvBf16>(g);
+  if (kv_dtype == PA_KV_FP8_E5M2) return simt_for<D, kKvE5M2>(g);
+  return simt_for<D, kKvFp8>(g);
+}
+
 KernelInfo pick_simt(int head_dim, int kv_dtype, int g) {
-  if (head_dim == 128) return kv_dtype == PA_KV_BF16 ? simt_for<128, kKvBf16>(g) : simt_for<128, kKvFp8>(g);
-  return kv_dtype == PA_KV_BF16 ? simt_for<64, kKvBf16>(g) : simt_for<64, kKvFp8>(g);
+  return head_dim == 128 ? simt_for_dtype<128>(kv_dtype, g) : simt_for_dtype<64>(kv_dtype, g);
 }
 
 }  // namespace dec

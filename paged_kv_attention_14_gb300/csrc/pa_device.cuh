@@ -14,7 +14,8 @@
 namespace pa {
 
 constexpr int kKvBf16 = 0;
-constexpr int kKvFp8 = 1;
+constexpr int kKvFp8 = 1;   // E4M3
+constexpr int kKvE5M2 = 2;  // E5M2
 
 // A wait on an mbarrier gives up after this many nanoseconds.  Every
 // legitimate wait in these kernels lasts microseconds.
@@ -196,6 +197,29 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t two, float &a, float &b) 
   b = f.y;
 }
 
+// Two E5M2 bytes to f16x2 (E5M2 is the upper byte of an f16); exact.
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+
+// Two bytes of an 8-bit cache (E4M3 or E5M2 per KVT) to f16x2 / fp32; exact.
+template <int KVT>
+__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint16_t two) {
+  if constexpr (KVT == kKvE5M2) return e5m2x2_to_f16x2(two);
+  return e4m3x2_to_f16x2(two);
+}
+
+template <int KVT>
+__device__ __forceinline__ void fp8x2_to_f32(uint16_t two, float &a, float &b) {
+  const uint32_t h = fp8x2_to_f16x2<KVT>(two);
+  __half2 hh = *reinterpret_cast<const __half2 *>(&h);
+  const float2 f = __half22float2(hh);
+  a = f.x;
+  b = f.y;
+}
+
 // Two fp32 values to packed bf16x2 (low half = lo), round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -216,6 +240,20 @@ __device__ __forceinline__ uint16_t pack_e4m3x2_satfinite(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two fp32 values to E5M2 bytes, round to nearest even, finite overflow
+// and +-inf saturate to +-57344, NaN stays NaN.
+__device__ __forceinline__ uint16_t pack_e5m2x2_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int KVT>
+__device__ __forceinline__ uint16_t pack_fp8x2_satfinite(float lo, float hi) {
+  if constexpr (KVT == kKvE5M2) return pack_e5m2x2_satfinite(lo, hi);
+  return pack_e4m3x2_satfinite(lo, hi);
 }
 
 // ------------------------------------------------------------ gpu atomics

@@ -151,8 +151,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float f0, f1, f2, f3;
-          e4m3x2_to_f32(static_cast<uint16_t>(w[c] & 0xffffu), f0, f1);
-          e4m3x2_to_f32(static_cast<uint16_t>(w[c] >> 16), f2, f3);
+          fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] & 0xffffu), f0, f1);
+          fp8x2_to_f32<KVT>(static_cast<uint16_t>(w[c] >> 16), f2, f3);
           o[2 * c] = pack_bf16x2(f0, f1);
           o[2 * c + 1] = pack_bf16x2(f2, f3);
         }
@@ -370,7 +370,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            const void *v_cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
-  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3;
+  const bool fp8 = d.kv_dtype != PA_KV_BF16;
   const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
   if (impl == PA_PREFILL_TCGEN05)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
@@ -396,11 +396,19 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   void *fn;
   size_t smem;
   if (d.head_dim == 128) {
-    fn = fp8 ? prefill_fn<128, kKvFp8>() : prefill_fn<128, kKvBf16>();
-    smem = fp8 ? PrefillCfg<128, kKvFp8, kPrefillWarps>::SMEM : PrefillCfg<128, kKvBf16, kPrefillWarps>::SMEM;
+    fn = d.kv_dtype == PA_KV_FP8_E5M2 ? prefill_fn<128, kKvE5M2>()
+         : fp8                         ? prefill_fn<128, kKvFp8>()
+                                       : prefill_fn<128, kKvBf16>();
+    smem = d.kv_dtype == PA_KV_FP8_E5M2 ? PrefillCfg<128, kKvE5M2, kPrefillWarps>::SMEM
+           : fp8                         ? PrefillCfg<128, kKvFp8, kPrefillWarps>::SMEM
+                                         : PrefillCfg<128, kKvBf16, kPrefillWarps>::SMEM;
   } else {
-    fn = fp8 ? prefill_fn<64, kKvFp8>() : prefill_fn<64, kKvBf16>();
-    smem = fp8 ? PrefillCfg<64, kKvFp8, kPrefillWarps>::SMEM : PrefillCfg<64, kKvBf16, kPrefillWarps>::SMEM;
+    fn = d.kv_dtype == PA_KV_FP8_E5M2 ? prefill_fn<64, kKvE5M2>()
+         : fp8                         ? prefill_fn<64, kKvFp8>()
+                                       : prefill_fn<64, kKvBf16>();
+    smem = d.kv_dtype == PA_KV_FP8_E5M2 ? PrefillCfg<64, kKvE5M2, kPrefillWarps>::SMEM
+           : fp8                         ? PrefillCfg<64, kKvFp8, kPrefillWarps>::SMEM
+                                         : PrefillCfg<64, kKvBf16, kPrefillWarps>::SMEM;
   }
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

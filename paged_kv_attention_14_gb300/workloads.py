@@ -229,8 +229,9 @@ WORKLOAD_NAMES = {
 }
 
 
-def workload(n: int, device="cpu", poison: bool = False) -> PagedBatch:
-    """Build workload ``n`` (1..5) on ``device``."""
+def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP8) -> PagedBatch:
+    """Build workload ``n`` (1..5) on ``device``.  ``fp8_format`` picks the
+    8-bit cache format of workload 4 (E4M3, or E5M2 for the same shapes)."""
     seed = 1000 + n
     if n == 1:
         return _decode_batch(WORKLOAD_NAMES[1],
@@ -251,8 +252,9 @@ def workload(n: int, device="cpu", poison: bool = False) -> PagedBatch:
     if n == 4:
         g = _gen(seed, "cpu")
         lens = torch.randint(1024, 8192 + 1, (128,), generator=g)
-        return _decode_batch(WORKLOAD_NAMES[4],
-                             seed, lens.tolist(), 40, 8, 128, KV_FP8, 1.0 / math.sqrt(128),
+        name = WORKLOAD_NAMES[4] if fp8_format == KV_FP8 else WORKLOAD_NAMES[4].replace("E4M3", "E5M2")
+        return _decode_batch(name,
+                             seed, lens.tolist(), 40, 8, 128, fp8_format, 1.0 / math.sqrt(128),
                              device, poison)
     if n == 5:
         return _mixed_batch(seed, device, poison)

@@ -13,26 +13,29 @@ from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
 
 #: max-abs tolerance of fp32 outputs against the fp64 oracle (bf16 KV, FP8 KV)
-TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2}
+TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
 #: tolerance of the natural-log log-sum-exp outputs
-LSE_TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2}
+LSE_TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
+#: generator cache type -> (library code, oracle code)
+_CODES = {W.KV_BF16: (B.PA_KV_BF16, oracle.KV_BF16), W.KV_FP8: (B.PA_KV_FP8_E4M3, oracle.KV_FP8_E4M3),
+          W.KV_FP8_E5M2: (B.PA_KV_FP8_E5M2, oracle.KV_FP8_E5M2)}
 
 
 def kv_code(b: W.PagedBatch) -> int:
-    return B.PA_KV_BF16 if b.kv_dtype == W.KV_BF16 else B.PA_KV_FP8_E4M3
+    return _CODES[b.kv_dtype][0]
 
 
 def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO,
             prefill_impl: int = B.PA_PREFILL_AUTO) -> B.PaKvDesc:
     return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
-                       b.k_scale if b.kv_dtype == W.KV_FP8 else 0.0,
-                       b.v_scale if b.kv_dtype == W.KV_FP8 else 0.0, decode_impl=decode_impl,
+                       b.k_scale if b.kv_dtype != W.KV_BF16 else 0.0,
+                       b.v_scale if b.kv_dtype != W.KV_BF16 else 0.0, decode_impl=decode_impl,
                        prefill_impl=prefill_impl)
 
 
 def gpu_caches(b: W.PagedBatch):
     """The caches as the CUDA path holds them: the bf16 pool itself, or the
-    E4M3 pool written by the library's own cache write."""
+    8-bit pool written by the library's own cache write."""
     if b.kv_dtype == W.KV_BF16:
         return b.k_pool, b.v_pool
     k, v, slots = b.pool_tokens_as_rows()
@@ -44,14 +47,15 @@ def gpu_caches(b: W.PagedBatch):
 
 def oracle_caches(b: W.PagedBatch):
     """The caches as the oracle sees them (CPU numpy): the bf16 pool, or the
-    oracle's own E4M3 encoding of it."""
+    oracle's own 8-bit encoding of it."""
     if b.kv_dtype == W.KV_BF16:
         return oracle.KV_BF16, b.k_pool.cpu(), b.v_pool.cpu()
+    code = _CODES[b.kv_dtype][1]
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)
-    kc, vc = oracle.cache_write(oracle.KV_FP8_E4M3, b.block_size, b.num_kv_heads, b.head_dim,
+    kc, vc = oracle.cache_write(code, b.block_size, b.num_kv_heads, b.head_dim,
                                 k.cpu(), v.cpu(), slots.cpu(), z, z, b.k_scale, b.v_scale)
-    return oracle.KV_FP8_E4M3, kc, vc
+    return code, kc, vc
 
 
 def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO, workspace=None):

@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
 Bars: cache writes and block indexing bit-exact; fp32 attention outputs within
-max-abs 2e-3 of the oracle for bf16 KV and 2e-2 for E4M3 KV.  Every input is
+max-abs 2e-3 of the oracle for bf16 KV and 2e-2 for E4M3 / E5M2 KV.  Every input is
 seeded and synthetic; pool slots that no sequence may read hold NaN, so a
 stray read shows up as a non-finite output.
 """
@@ -46,13 +46,21 @@ def test_cache_write_bf16_bit_exact_on_mixed_step():
 def _adversarial_bf16(n_random, g):
     special = [1.0625, -1.0625, 1.1875, 464.0, -464.0, 480.0, 1e30, -1e30, float("inf"), float("-inf"),
                2.0 ** -10, 3 * 2.0 ** -10, -2.0 ** -10, 2.0 ** -12, 0.0, -0.0, float("nan"), 448.0, 449.0,
-               2.0 ** -6, 2.0 ** -7 * 1.5, 240.0, 248.0, 232.0]
+               2.0 ** -6, 2.0 ** -7 * 1.5, 240.0, 248.0, 232.0,
+               # E5M2 ties, saturation and subnormals
+               1.125, 1.375, 57344.0, 61440.0, 65536.0, -61440.0, 2.0 ** -16, 3 * 2.0 ** -17, 2.0 ** -17,
+               2.0 ** -14, 5 * 2.0 ** -16, 28672.0, 30720.0]
     x = torch.randn(n_random, generator=g) * 3
     return torch.cat([torch.tensor(special), x]).to(torch.bfloat16)
 
 
+_FP8_CODES = {"e4m3": (B.PA_KV_FP8_E4M3, oracle.KV_FP8_E4M3), "e5m2": (B.PA_KV_FP8_E5M2, oracle.KV_FP8_E5M2)}
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("scale", [1.0, 0.0123, 3.5])
-def test_cache_write_fp8_bit_exact_with_ties_saturation_and_nan(scale):
+def test_cache_write_fp8_bit_exact_with_ties_saturation_and_nan(scale, fmt):
+    lib_code, oracle_code = _FP8_CODES[fmt]
     g = torch.Generator().manual_seed(7)
     H, D = 2, 64
     vals = _adversarial_bf16(H * D * 40, g)
@@ -62,13 +70,13 @@ def test_cache_write_fp8_bit_exact_with_ties_saturation_and_nan(scale):
     NB = (T + 15) // 16 + 3
     slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
     slots[5] = -1
-    d = B.make_desc(NB, H, 2 * H, D, B.PA_KV_FP8_E4M3, scale, scale * 2)
+    d = B.make_desc(NB, H, 2 * H, D, lib_code, scale, scale * 2)
     kc = torch.full((NB, H, 16, D), 0xAB, dtype=torch.uint8, device=DEV)
     vc = kc.clone()
     B.pa_cache_write(d, k.to(DEV), v.to(DEV), kc, vc, slots.to(DEV))
     torch.cuda.synchronize()
     z = np.full((NB, H, 16, D), 0xAB, np.uint8)
-    ok, ov = oracle.cache_write(oracle.KV_FP8_E4M3, 16, H, D, k, v, slots, z, z, scale, scale * 2)
+    ok, ov = oracle.cache_write(oracle_code, 16, H, D, k, v, slots, z, z, scale, scale * 2)
     assert np.array_equal(kc.cpu().numpy(), ok), np.argwhere(kc.cpu().numpy() != ok)[:5]
     assert np.array_equal(vc.cpu().numpy(), ov)
 
@@ -149,6 +157,10 @@ CASES = [
     (128, 40, 8, W.KV_FP8, [1, 100, 1025]),
     (64, 12, 1, W.KV_FP8, [5, 300]),
     (128, 16, 1, W.KV_FP8, [64, 65]),
+    (64, 4, 2, W.KV_FP8_E5M2, [1, 7, 16, 33, 250]),
+    (128, 8, 2, W.KV_FP8_E5M2, [1, 15, 17, 1000, 1600]),
+    (128, 40, 8, W.KV_FP8_E5M2, [1, 100, 1025]),
+    (128, 16, 1, W.KV_FP8_E5M2, [64, 65]),
 ]
 
 
@@ -298,6 +310,8 @@ PREFILL_CASES = [
     (64, 16, 1, W.KV_BF16, [40, 8], [200, 8], 0),
     (64, 4, 2, W.KV_FP8, [5, 16, 1, 23], [5, 40, 33, 64], 1),
     (128, 8, 2, W.KV_FP8, [90, 20], [300, 20], 1),
+    (64, 4, 2, W.KV_FP8_E5M2, [5, 16, 1, 23], [5, 40, 33, 64], 1),
+    (128, 8, 2, W.KV_FP8_E5M2, [90, 20], [300, 20], 1),
 ]
 PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
 
