@@ -65,9 +65,9 @@ def _load():
         lib.pa_oracle_cache_write.restype = None
         lib.pa_oracle_attend_range.argtypes = [I, I, I, I, P, P, P, P, I, I, I, F, F, F, P, P]
         lib.pa_oracle_attend_range.restype = None
-        lib.pa_oracle_decode.argtypes = [I, I, I, I, I, P, P, P, P, I, P, I, F, F, F, P, I, P, P]
+        lib.pa_oracle_decode.argtypes = [I, I, I, I, I, P, P, P, P, I, P, I, F, F, F, I, I, P, I, P, P]
         lib.pa_oracle_decode.restype = None
-        lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, P, I, P, P]
+        lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, I, I, P, I, P, P]
         lib.pa_oracle_prefill.restype = None
         lib.pa_oracle_merge.argtypes = [P, P, I, I, P, P]
         lib.pa_oracle_merge.restype = None
@@ -152,9 +152,10 @@ def attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v
 
 
 def decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, k_cache, v_cache,
-           block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None):
+           block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None, window=0, chunk=0):
     """Decode attention.  Returns (out [n, D], lse [n]) in fp64 for the (s, h)
-    pairs given (default: all, row-major over (s, h))."""
+    pairs given (default: all, row-major over (s, h)).  ``window`` / ``chunk``:
+    sliding-window / chunked-local attention (0: off)."""
     lib = _load()
     qn = _np(q, np.uint16)
     kc = _cache_np(k_cache, kv_dtype)
@@ -171,16 +172,17 @@ def decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, k_cache
     lse = np.zeros(n, np.float64)
     lib.pa_oracle_decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
                          _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
-                         float(scale), float(k_scale), float(v_scale),
+                         float(scale), float(k_scale), float(v_scale), int(window), int(chunk),
                          None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
     return out, lse
 
 
 def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_start_loc,
             k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0,
-            pairs=None):
+            pairs=None, window=0, chunk=0):
     """Causal chunked-prefill attention.  Returns (out [n, D], lse [n]) in fp64
-    for the (token row, head) pairs given (default: all rows x heads)."""
+    for the (token row, head) pairs given (default: all rows x heads).
+    ``window`` / ``chunk``: sliding-window / chunked-local attention (0: off)."""
     lib = _load()
     qn = _np(q, np.uint16)
     qsl = _np(query_start_loc, np.int32)
@@ -198,7 +200,7 @@ def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_
     lse = np.zeros(n, np.float64)
     lib.pa_oracle_prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
                           _ptr(qsl), _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
-                          float(scale), float(k_scale), float(v_scale),
+                          float(scale), float(k_scale), float(v_scale), int(window), int(chunk),
                           None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
     return out, lse
 

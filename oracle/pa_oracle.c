@@ -289,12 +289,33 @@ void pa_oracle_attend_range(int kv_dtype, int block_size, int num_kv_heads, int 
   free(x);
 }
 
+/* ------------------------------------------------------- local attention */
+
+/*
+ * First key a query at position pos may attend ("Local-attention KV +
+ * sliding-window operator -- SlidingWindowSpec and ChunkedLocalAttentionSpec"
+ * of the vllm.cpp repository listing; the pages give no formula, the plain
+ * readings are taken): a sliding window of W keys ending at pos starts at
+ * pos - W + 1; chunked-local attention with chunks of C positions starts at
+ * the query's chunk, floor(pos / C) * C.  0 disables either; with both the
+ * later start applies.
+ */
+static int local_first_key(int pos, int window, int chunk) {
+  int lo = 0;
+  if (window > 0 && pos - window + 1 > lo) lo = pos - window + 1;
+  if (chunk > 0 && (pos / chunk) * chunk > lo) lo = (pos / chunk) * chunk;
+  return lo;
+}
+
 /* ---------------------------------------------------------------- decode */
 
 /*
  * Decode: sequence s has one new query (q[s]) at position L_s - 1 and attends
  * every cached token [0, L_s) through its block table.  Query head h uses kv
  * head h / g with g = num_q_heads / num_kv_heads.
+ *
+ * With a sliding window or chunked-local attention the range starts at
+ * local_first_key(L_s - 1).
  *
  * pairs: optional int32 [num_pairs][2] list of (s, h) to compute (NULL = all,
  * in (s, h) row-major order).  out: [num_pairs][head_dim], lse: [num_pairs].
@@ -303,8 +324,8 @@ void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_
                       int head_dim, const uint16_t *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int num_seqs, float scale, float k_scale,
-                      float v_scale, const int32_t *pairs, int num_pairs, double *out,
-                      double *lse) {
+                      float v_scale, int window, int chunk, const int32_t *pairs, int num_pairs,
+                      double *out, double *lse) {
   int g = num_q_heads / num_kv_heads;
   int total = pairs ? num_pairs : num_seqs * num_q_heads;
   for (int i = 0; i < total; ++i) {
@@ -312,9 +333,11 @@ void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_
     int h = pairs ? pairs[2 * i + 1] : i % num_q_heads;
     const uint16_t *q_vec = q + ((int64_t)s * num_q_heads + h) * head_dim;
     const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
+    int L = context_lens[s];
+    int lo = L > 0 ? local_first_key(L - 1, window, chunk) : 0;
     pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
-                           row, h / g, 0, context_lens[s], scale, k_scale, v_scale,
-                           out + (int64_t)i * head_dim, lse + i);
+                           row, h / g, lo, L, scale, k_scale, v_scale, out + (int64_t)i * head_dim,
+                           lse + i);
   }
 }
 
@@ -324,7 +347,8 @@ void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_
  * Chunked prefill: sequence s owns the packed query rows
  * [query_start_loc[s], query_start_loc[s+1]); q_len = their count.  Its KV
  * already holds L_s tokens (the chunk's own K/V were written before), so query
- * i sits at position L_s - q_len + i and attends keys [0, position] (causal).
+ * i sits at position L_s - q_len + i and attends keys [0, position] (causal),
+ * or [local_first_key(position), position] with local attention.
  *
  * pairs: optional int32 [num_pairs][2] list of (token row, q head) (NULL = all
  * rows x heads).  out: [num_pairs][head_dim], lse: [num_pairs].
@@ -333,8 +357,8 @@ void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q
                        int head_dim, const uint16_t *q, const int32_t *query_start_loc,
                        const void *k_cache, const void *v_cache, const int32_t *block_tables,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                       float scale, float k_scale, float v_scale, const int32_t *pairs,
-                       int num_pairs, double *out, double *lse) {
+                       float scale, float k_scale, float v_scale, int window, int chunk,
+                       const int32_t *pairs, int num_pairs, double *out, double *lse) {
   int g = num_q_heads / num_kv_heads;
   int num_rows = query_start_loc[num_seqs];
   int total = pairs ? num_pairs : num_rows * num_q_heads;
@@ -348,8 +372,8 @@ void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q
     const uint16_t *q_vec = q + ((int64_t)r * num_q_heads + h) * head_dim;
     const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
     pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
-                           row, h / g, 0, pos + 1, scale, k_scale, v_scale,
-                           out + (int64_t)i * head_dim, lse + i);
+                           row, h / g, local_first_key(pos, window, chunk), pos + 1, scale, k_scale,
+                           v_scale, out + (int64_t)i * head_dim, lse + i);
   }
 }
 

@@ -442,3 +442,84 @@ def test_prefill_shared_prefix_blocks_are_read_by_every_sequence():
     for s in range(3):
         rows = slice(s * 4 * 2, (s + 1) * 4 * 2)
         assert not np.allclose(out[rows], out2[rows])
+
+
+# ------------------------------------------------------ local attention
+
+def _band_mask(n_q, L, first_pos, window=0, chunk=0):
+    """Query rows at positions first_pos .. first_pos + n_q - 1 over keys 0 .. L-1:
+    causal (torch.tril), within `window` keys ending at the query (torch.triu
+    with diagonal -(window - 1)), and within the query's chunk of `chunk`
+    positions (torch.block_diag of all-ones chunks).  Built from library
+    routines, not from the oracle's formula."""
+    full = torch.ones(L, L, dtype=torch.bool)
+    m = torch.tril(full)
+    if window:
+        m &= torch.triu(full, diagonal=-(window - 1))
+    if chunk:
+        blocks = [torch.ones(min(chunk, L - i), min(chunk, L - i), dtype=torch.bool) for i in range(0, L, chunk)]
+        m &= torch.block_diag(*blocks).bool()
+    return m[first_pos:first_pos + n_q].numpy()
+
+
+@pytest.mark.parametrize("window,chunk", [(1, 0), (5, 0), (16, 0), (23, 0), (0, 7), (0, 16), (9, 16), (40, 0)])
+def test_local_attention_prefill_matches_sdpa_with_band_masks(window, chunk):
+    q_lens, ctx = [5, 16, 1, 23], [5, 40, 33, 64]
+    b = W.random_prefill(93, q_lens, ctx, 4, 2, 64, shared_prefix_blocks=1)
+    out, lse = _oracle_prefill_local(b, window, chunk)
+    kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    qf = _bf16_to_f64(b.q_prefill)
+    qsl = b.query_start_loc.numpy()
+    for s, (n, L) in enumerate(zip(q_lens, ctx)):
+        mask = _band_mask(n, L, L - n, window, chunk)
+        for h in range(4):
+            K = _dense_kv(kf, b.block_tables_prefill[s].numpy(), L, h // 2)
+            V = _dense_kv(vf, b.block_tables_prefill[s].numpy(), L, h // 2)
+            ref = _sdpa(qf[qsl[s]:qsl[s] + n, h], K, V, b.scale, mask)
+            got = out[(qsl[s] + np.arange(n)) * 4 + h]
+            np.testing.assert_allclose(got, ref, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("window,chunk", [(1, 0), (7, 0), (16, 0), (100, 0), (0, 16), (0, 5), (12, 32)])
+def test_local_attention_decode_matches_sdpa_with_band_masks(window, chunk):
+    lens = [1, 5, 16, 17, 40]
+    b = W.random_decode(63, lens, 4, 2, 64, poison=True)
+    kd, kc, vc = _oracle_caches(b)
+    out, _ = oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
+                           b.block_tables_decode, b.context_lens_decode, b.scale, window=window, chunk=chunk)
+    kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    qf = _bf16_to_f64(b.q_decode)
+    for s, L in enumerate(lens):
+        mask = _band_mask(1, L, L - 1, window, chunk)
+        for h in range(4):
+            K = _dense_kv(kf, b.block_tables_decode[s].numpy(), L, h // 2)
+            V = _dense_kv(vf, b.block_tables_decode[s].numpy(), L, h // 2)
+            ref = _sdpa(qf[s, h][None], K, V, b.scale, mask)[0]
+            np.testing.assert_allclose(out[s * 4 + h], ref, atol=1e-12, rtol=0)
+
+
+def test_local_attention_closed_forms():
+    lens = [1, 9, 33]
+    b = W.random_decode(64, lens, 4, 2, 64, poison=True)
+    kd, kc, vc = _oracle_caches(b)
+    args = (kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc, b.block_tables_decode,
+            b.context_lens_decode, b.scale)
+    full, full_lse = oracle.decode(*args)
+    # a window at least as long as every sequence changes nothing
+    wide, wide_lse = oracle.decode(*args, window=max(lens))
+    assert np.array_equal(wide, full) and np.array_equal(wide_lse, full_lse)
+    # a window (or chunk) of one key returns the V of the query's own position
+    for kw in ({"window": 1}, {"chunk": 1}):
+        one, one_lse = oracle.decode(*args, **kw)
+        for s, L in enumerate(lens):
+            blk = int(b.block_tables_decode[s, (L - 1) // 16])
+            for h in range(4):
+                v_last = b.v_pool[blk, h // 2, (L - 1) % 16].to(torch.float64).numpy()
+                assert np.array_equal(one[s * 4 + h], v_last)
+
+
+def _oracle_prefill_local(b: W.PagedBatch, window, chunk):
+    kd, kc, vc = _oracle_caches(b)
+    return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill,
+                          b.query_start_loc, kc, vc, b.block_tables_prefill, b.context_lens_prefill,
+                          b.scale, b.k_scale, b.v_scale, window=window, chunk=chunk)
