@@ -70,9 +70,9 @@ def _src_sha256(files):
     return h.hexdigest()
 
 
-def _traffic(kernel: str, workload: int):
+def _traffic(kernel: str, workload: int, local: bool = False):
     t = NCU_TRAFFIC[kernel]
-    if t["bytes"] is None or t["workload"] != workload or _src_sha256(t["sources"]) != t["sha256"]:
+    if local or t["bytes"] is None or t["workload"] != workload or _src_sha256(t["sources"]) != t["sha256"]:
         return None
     return t["bytes"]
 
@@ -143,16 +143,49 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _prefill_flops(b) -> int:
+def _first_key(pos: int, window: int, chunk: int) -> int:
+    """First key a query at ``pos`` sees: sliding window of ``window`` keys,
+    chunked-local attention with chunks of ``chunk`` positions (0: off)."""
+    lo = 0
+    if window:
+        lo = max(lo, pos - window + 1)
+    if chunk:
+        lo = max(lo, (pos // chunk) * chunk)
+    return lo
+
+
+def _local_config(args) -> dict:
+    """Local-attention settings of the run, for the JSON line's config (none when off)."""
+    d = {}
+    if args.sliding_window:
+        d["sliding_window"] = args.sliding_window
+    if args.attention_chunk:
+        d["attention_chunk"] = args.attention_chunk
+    return d
+
+
+def _decode_kv_bytes(b, window: int, chunk: int) -> int:
+    """Algorithmic KV bytes of the decode part: every K and V element the
+    queries may see, of every (sequence, kv head), read once."""
+    lens = b.context_lens_decode.cpu().tolist()
+    tokens = sum(L - _first_key(L - 1, window, chunk) for L in lens if L > 0)
+    return tokens * b.num_kv_heads * b.head_dim * 2 * b.kv_elem_bytes
+
+
+def _prefill_flops(b, window: int = 0, chunk: int = 0) -> int:
     """Algorithmic flops of the causal prefill chunks: per query row and head,
-    4 * head_dim flops (QK^T and PV multiply-adds) per key at or before it."""
+    4 * head_dim flops (QK^T and PV multiply-adds) per key it may see (at or
+    before it, and within its window / chunk)."""
     qsl = b.query_start_loc.cpu().tolist()
     lens = b.context_lens_prefill.cpu().tolist()
     keys = 0
     for s, L in enumerate(lens):
         n = qsl[s + 1] - qsl[s]
-        # query i sits at L - n + i and sees L - n + i + 1 keys
-        keys += n * (L - n) + n * (n + 1) // 2
+        if not window and not chunk:
+            # query i sits at L - n + i and sees L - n + i + 1 keys
+            keys += n * (L - n) + n * (n + 1) // 2
+        else:
+            keys += sum(p + 1 - _first_key(p, window, chunk) for p in range(L - n, L))
     return keys * 4 * b.head_dim * b.num_q_heads
 
 
@@ -174,7 +207,8 @@ def run_ours(args):
     b = W.workload(args.workload, device=dev, poison=False, fp8_format=FP8_FORMATS[args.fp8_format])
     kv = {W.KV_BF16: B.PA_KV_BF16, W.KV_FP8: B.PA_KV_FP8_E4M3, W.KV_FP8_E5M2: B.PA_KV_FP8_E5M2}[b.kv_dtype]
     desc = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv,
-                       b.k_scale if kv else 0.0, b.v_scale if kv else 0.0, decode_impl=args.decode_impl)
+                       b.k_scale if kv else 0.0, b.v_scale if kv else 0.0, decode_impl=args.decode_impl,
+                       sliding_window=args.sliding_window, attention_chunk=args.attention_chunk)
     if kv == B.PA_KV_BF16:
         kc, vc = b.k_pool, b.v_pool
     else:
@@ -188,14 +222,15 @@ def run_ours(args):
     maxL = b.max_context_len_decode()
     wsp = B.decode_workspace(desc, S, maxL, dev)
     out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
-    kv_bytes = b.decode_kv_bytes()
+    kv_bytes = _decode_kv_bytes(b, args.sliding_window, args.attention_chunk)
+    local = bool(args.sliding_window or args.attention_chunk)
     mixed = b.q_prefill is not None
     if mixed:
         pf_out = torch.empty(b.q_prefill.shape, dtype=torch.float32, device=dev)
         qsl = b.query_start_loc
         pf_maxq = int((qsl[1:] - qsl[:-1]).max())
         pf_maxL = int(b.context_lens_prefill.max())
-        pf_flops = _prefill_flops(b)
+        pf_flops = _prefill_flops(b, args.sliding_window, args.attention_chunk)
     # cache write + decode (+ the merge kernel of the tensor-core decode) (+ prefill)
     launches_per_step = (3 if args.decode_impl != 1 else 2) + (1 if mixed else 0)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -343,12 +378,12 @@ def run_ours(args):
                        "kv_bytes_per_step": kv_bytes,
                        "l2": ("flushed before every step (write of 2x L2)" if flush is not None else
                               f"inputs larger than L2 ({kv_bytes >> 20} MiB KV vs {l2_bytes >> 20} MiB L2), no flush"),
-                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", **_local_config(args)},
             "roofline": {"bound": "hbm",
                          "kernel": "pa_decode (decode kernel + merge kernel), timed alone per call",
                          "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
-                         "traffic": _traffic("decode", args.workload)},
+                         "traffic": _traffic("decode", args.workload, local)},
             "e2e": {"value": round(ws * kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * K + (launches_per_step - 1) * K2,
@@ -366,15 +401,16 @@ def run_ours(args):
                                     "achieved": round(pf_tf, 1), "peak": tc_peak,
                                     "peak_kind": f"{peak_kind} bf16 dense (burst)", "unit": "TFLOP/s",
                                     "frac": round(pf_tf / tc_peak, 4), "kernel_us": round(pf_ms * 1e3, 2),
-                                    "traffic": _traffic("prefill", args.workload)}
+                                    "traffic": _traffic("prefill", args.workload, local)}
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget,
+                                                window=args.sliding_window, chunk=args.attention_chunk)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def _oracle_sample(n_workload: int, budget_s: float):
+def _oracle_sample(n_workload: int, budget_s: float, window: int = 0, chunk: int = 0):
     """Run the fp64 oracle over whole sequences of the workload (all heads)
     until ``budget_s`` of CPU time is used; returns (kv_bytes, seconds, n_seqs)."""
     import oracle
@@ -392,14 +428,15 @@ def _oracle_sample(n_workload: int, budget_s: float):
         pairs = [(s, h) for h in range(b.num_q_heads)]
         t0 = time.perf_counter()
         oracle.decode(oracle.KV_BF16, 16, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
-                      b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs)
+                      b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs, window=window, chunk=chunk)
         t_used += time.perf_counter() - t0
-        done_bytes += int(b.context_lens_decode[s]) * b.num_kv_heads * b.head_dim * 2 * 2
+        L = int(b.context_lens_decode[s])
+        done_bytes += (L - _first_key(L - 1, window, chunk)) * b.num_kv_heads * b.head_dim * 2 * 2
         n += 1
     return done_bytes, t_used, n, b.name
 
 
-def _oracle_worker(rank, nproc, n_workload, phases, barrier, results):
+def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, chunk=0):
     """One process of the all-cores oracle run: builds the (seeded) workload,
     then for each phase of ``phases`` seconds runs the oracle over (sequence,
     kv head) units rank, rank + nproc, ... (the g query heads of one kv head,
@@ -423,14 +460,16 @@ def _oracle_worker(rank, nproc, n_workload, phases, barrier, results):
             s, kvh = divmod(u, Hkv)
             pairs = [(s, kvh * g + i) for i in range(g)]
             oracle.decode(oracle.KV_BF16, 16, Hkv, b.num_q_heads, b.head_dim, b.q_decode, b.k_pool, b.v_pool,
-                          b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs)
-            done += int(b.context_lens_decode[s]) * b.head_dim * 2 * 2
+                          b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs, window=window,
+                          chunk=chunk)
+            L = int(b.context_lens_decode[s])
+            done += (L - _first_key(L - 1, window, chunk)) * b.head_dim * 2 * 2
             n += 1
             u = (u + nproc) % (S * Hkv)
         results.put((rank, done, time.perf_counter() - t0, n))
 
 
-def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None):
+def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None, window: int = 0, chunk: int = 0):
     """The oracle on every host core: ``nproc`` spawned processes (the GPU is
     already in use in this process, so no fork), one thread each.  Returns per
     phase (kv_bytes, wall seconds, sequences), the workload name and nproc."""
@@ -440,7 +479,7 @@ def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None):
     ctx = mp.get_context("spawn")
     barrier = ctx.Barrier(nproc)
     results = ctx.Queue()
-    procs = [ctx.Process(target=_oracle_worker, args=(r, nproc, n_workload, list(phases), barrier, results))
+    procs = [ctx.Process(target=_oracle_worker, args=(r, nproc, n_workload, list(phases), barrier, results, window, chunk))
              for r in range(nproc)]
     for p in procs:
         p.start()
@@ -453,11 +492,11 @@ def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None):
     return out, nproc
 
 
-def cpu_baseline(n_workload: int, budget_s: float = 10.0):
+def cpu_baseline(n_workload: int, budget_s: float = 10.0, window: int = 0, chunk: int = 0):
     """The oracle on all host cores for about ``budget_s`` seconds (the
     reported baseline), plus one thread for ``budget_s / 2``."""
-    nbytes1, secs1, n1, name = _oracle_sample(n_workload, budget_s / 2)
-    (res,), nproc = _oracle_all_cores(n_workload, [budget_s])
+    nbytes1, secs1, n1, name = _oracle_sample(n_workload, budget_s / 2, window, chunk)
+    (res,), nproc = _oracle_all_cores(n_workload, [budget_s], window=window, chunk=chunk)
     nbytes, secs, n = res
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
             "sample": f"{n} (sequence, kv head) units (their g query heads each) of '{name}', fp64 C oracle, "
@@ -476,7 +515,8 @@ def run_reference(args):
     # each step: one bounded sample of the workload through the oracle on all
     # host cores, sized so that the whole run takes about two minutes
     per_step = max(0.01, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
-    phases, nproc = _oracle_all_cores(args.workload, [per_step] * (args.warmup + args.steps))
+    phases, nproc = _oracle_all_cores(args.workload, [per_step] * (args.warmup + args.steps),
+                                      window=args.sliding_window, chunk=args.attention_chunk)
     timed = phases[args.warmup:]
     nbytes = sum(p[0] for p in timed)
     secs = sum(p[1] for p in timed)
@@ -485,7 +525,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": name},
+            "data": "synthetic", "config": {"workload": name, **_local_config(args)},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
                              "sample": f"(sequence, kv head) units of '{name}' per step on {nproc} processes x 1 "
                                        f"thread, about {per_step:.3f} s each"},
@@ -503,6 +543,8 @@ def main():
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
                     help="8-bit cache format of workload 4 (same shapes)")
+    ap.add_argument("--sliding-window", type=int, default=0, help="sliding-window attention of W keys (0: off)")
+    ap.add_argument("--attention-chunk", type=int, default=0, help="chunked-local attention over chunks of C (0: off)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -105,6 +105,15 @@ typedef enum {
  *                  0 means 1.0.  Ignored for bf16.
  *   decode_impl  : a pa_decode_impl value.
  *   prefill_impl : a pa_prefill_impl value.
+ *   sliding_window, attention_chunk : local attention ("Local-attention KV +
+ *                  sliding-window operator -- SlidingWindowSpec and
+ *                  ChunkedLocalAttentionSpec" of the vllm.cpp repository
+ *                  listing).  A query at position p attends keys from
+ *                  p - sliding_window + 1 (a window of sliding_window keys
+ *                  ending at p) and from (p / attention_chunk) *
+ *                  attention_chunk (its own chunk) up to p; 0 disables either,
+ *                  with both the later start applies.  Applies to pa_decode,
+ *                  pa_decode_static and pa_prefill_chunk; must be >= 0.
  */
 typedef struct {
   int32_t num_blocks;
@@ -115,8 +124,10 @@ typedef struct {
   int32_t kv_dtype; /* pa_kv_dtype */
   float k_scale;
   float v_scale;
-  int32_t decode_impl;  /* pa_decode_impl */
-  int32_t prefill_impl; /* pa_prefill_impl */
+  int32_t decode_impl;     /* pa_decode_impl */
+  int32_t prefill_impl;    /* pa_prefill_impl */
+  int32_t sliding_window;  /* 0: none */
+  int32_t attention_chunk; /* 0: none */
 } pa_kv_desc;
 
 /* PA_ABI_VERSION of the loaded library. */

@@ -55,6 +55,8 @@ class PaKvDesc(ctypes.Structure):
         ("v_scale", ctypes.c_float),
         ("decode_impl", ctypes.c_int32),
         ("prefill_impl", ctypes.c_int32),
+        ("sliding_window", ctypes.c_int32),
+        ("attention_chunk", ctypes.c_int32),
     ]
 
 
@@ -104,9 +106,10 @@ def load(path: Optional[str] = None):
 def make_desc(num_blocks: int, num_kv_heads: int, num_q_heads: int, head_dim: int,
               kv_dtype: int = PA_KV_BF16, k_scale: float = 0.0, v_scale: float = 0.0,
               block_size: int = 16, decode_impl: int = PA_DECODE_AUTO,
-              prefill_impl: int = PA_PREFILL_AUTO) -> PaKvDesc:
+              prefill_impl: int = PA_PREFILL_AUTO, sliding_window: int = 0,
+              attention_chunk: int = 0) -> PaKvDesc:
     return PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
-                    k_scale, v_scale, decode_impl, prefill_impl)
+                    k_scale, v_scale, decode_impl, prefill_impl, sliding_window, attention_chunk)
 
 
 def abi_version() -> int:

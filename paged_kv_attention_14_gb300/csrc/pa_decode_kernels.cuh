@@ -65,9 +65,10 @@ struct __align__(16) StageHdr {
   int kind;
   int s;
   int grp;     // kv head group (kv heads grp * HG .. grp * HG + HG - 1)
-  int ntok;    // valid tokens in this stage
+  int ntok;    // tokens of this stage before the sequence's end
   int flags;   // kFlagFirst / kFlagLast of a piece
   int seg_nb;  // blocks of the segment
+  int tlo;     // tokens at the stage's start before the first key (local attention)
 };
 
 // A segment split across CTAs, recorded by the CTA in whose range it starts
@@ -96,6 +97,8 @@ struct DecodeArgs {
   int num_groups;  // kv head groups per sequence (num_kv_heads / HG)
   float qscale;    // scale * k_scale * log2(e)
   float vscale;    // v_scale (1 for bf16)
+  int window;      // sliding window (0: none)
+  int chunk;       // chunked-local attention (0: none)
   int32_t *err;
   int32_t *seg_counter;  // [num_seqs * num_groups]
   float *slot_lse;       // [grid][2][slot heads], log2 domain
@@ -115,6 +118,15 @@ static __device__ unsigned long long g_pa_trace[4096][8];
 #else
 #define PA_TRACE(...)
 #endif
+
+// Blocks of a sequence of L tokens the decode query reads: from the block
+// holding its first key (local attention) to the last one.
+__device__ __forceinline__ int seq_first_block(const DecodeArgs &a, int L) {
+  return local_first_key(L - 1, a.window, a.chunk) >> 4;
+}
+__device__ __forceinline__ int seq_blocks(const DecodeArgs &a, int L) {
+  return ((L + 15) >> 4) - seq_first_block(a, L);
+}
 
 // ---------------------------------------------------------------- workspace
 
@@ -164,7 +176,7 @@ __device__ long long count_blocks(const DecodeArgs &a, int lane) {
       if (s < S) {
         const int L = __ldg(a.context_lens + s);
         if (L > 0)
-          acc += static_cast<unsigned>((L + 15) >> 4);
+          acc += static_cast<unsigned>(seq_blocks(a, L));
         else if (s % G == static_cast<int>(blockIdx.x))
           zero_sequence(a, s, D);
       }
@@ -201,7 +213,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     for (int base = 0; base < S && s < 0; base += 32) {
       const int si = base + lane;
       const int L = si < S ? __ldg(a.context_lens + si) : 0;
-      const long long v = L > 0 ? static_cast<long long>((L + 15) >> 4) * NG : 0;
+      const long long v = L > 0 ? static_cast<long long>(seq_blocks(a, L)) * NG : 0;
       long long incl = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -220,7 +232,8 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
       }
     }
     int L = __ldg(a.context_lens + s);
-    int nb = (L + 15) >> 4;
+    int fb = seq_first_block(a, L);  // logical block of the segment's first unit
+    int nb = ((L + 15) >> 4) - fb;
     int grp = static_cast<int>((b0 - pre) / nb);
     int off = static_cast<int>((b0 - pre) % nb);
     long long cur = b0;
@@ -229,14 +242,14 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     // ones are used, so table latency stays off the copy stream
     int win_s = -1, wb = 0, w_cur = 0, w_nxt = 0;
     const int32_t *trow = a.block_tables;
-    auto tload = [&](int e) { return e < nb ? __ldg(trow + e) : 0; };
+    auto tload = [&](int e) { return e < fb + nb ? __ldg(trow + e) : 0; };
     while (cur < b1 && ok) {
       const long long seg_start = pre + static_cast<long long>(grp) * nb;
       const long long piece_end = min(b1, seg_start + nb);
       const int npb = static_cast<int>(piece_end - cur);
       for (int k = 0; k < npb; k += BPS) {
         const int nblk = min(BPS, npb - k);
-        const int lb0 = off + k;
+        const int lb0 = fb + off + k;  // logical block of the stage's first block
         PA_TRACE(const long long tt0 = clock64();)
         if (win_s != s || lb0 < wb || lb0 + nblk > wb + 64) {
           win_s = s;
@@ -271,6 +284,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
           h.ntok = min(L - lb0 * 16, nblk * 16);
           h.flags = (first ? kFlagFirst : 0) | (k + BPS >= npb ? kFlagLast : 0);
           h.seg_nb = nb;
+          h.tlo = max(0, local_first_key(L - 1, a.window, a.chunk) - lb0 * 16);
           hdr[stage] = h;
           mbar_arrive_expect_tx(&full[stage], 2u * nblk * Cfg::GTILE + (first ? qbytes : 0u));
         }
@@ -304,7 +318,8 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
         } while (s < S && __ldg(a.context_lens + s) <= 0);
         if (s < S) {
           L = __ldg(a.context_lens + s);
-          nb = (L + 15) >> 4;
+          fb = seq_first_block(a, L);
+          nb = ((L + 15) >> 4) - fb;
         }
       }
     }
@@ -600,7 +615,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
 #pragma unroll
     for (int i = 0; i < C::TPG; ++i) {
       const int r = gid + C::NG * i;
-      const bool valid = r < h.ntok;
+      const bool valid = r < h.ntok && r >= h.tlo;
       float acc[GP];
 #pragma unroll
       for (int j = 0; j < GP; ++j) acc[j] = 0.f;
@@ -641,7 +656,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
 #pragma unroll
     for (int i = 0; i < C::TPG; ++i) {
       const int r = gid + C::NG * i;
-      if (r < h.ntok) {
+      if (r < h.ntok && r >= h.tlo) {
         float kv[EPL];
         RS::load(Vs + (r >> 4) * C::TILEB + (r & 15) * C::ROWB, j8, kv);
 #pragma unroll
@@ -1017,7 +1032,10 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
       }
       // ---- online softmax over the block's tokens, per head (column)
       uint32_t pb[NN][2], pbl[NN][2];
-      const bool v_lo = r < vt, v_hi = r + 8 < vt;
+      // tokens of this warp's block before the first key (local attention)
+      // or past the sequence's end are out
+      const int vl = h.tlo - 16 * bw;
+      const bool v_lo = r < vt && r >= vl, v_hi = r + 8 < vt && r + 8 >= vl;
 #pragma unroll
       for (int nn = 0; nn < NN; ++nn) {
         const float s0 = v_lo ? (sa[nn][0] + sb[nn][0]) * a.qscale : -INFINITY;
@@ -1056,12 +1074,13 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
           pb[nn][1] = movmatrix_trans(pack_f16x2(p2, p3));
         }
       }
-      // ---- O^T += V^T P^T.  Tokens past the block's valid count may hold
+      // ---- O^T += V^T P^T.  Tokens outside the block's valid range may hold
       // anything (NaN included); a zero probability does not cancel them
       // (0 * NaN = NaN), so their V^T fragment entries are zeroed: mk_lo
       // covers tokens 2c, 2c+1 and mk_hi tokens 2c+8, 2c+9 of this lane.
-      const uint32_t mk_lo = (2 * c < vt ? 0x0000ffffu : 0u) | (2 * c + 1 < vt ? 0xffff0000u : 0u);
-      const uint32_t mk_hi = (2 * c + 8 < vt ? 0x0000ffffu : 0u) | (2 * c + 9 < vt ? 0xffff0000u : 0u);
+      auto in = [&](int t) { return t < vt && t >= vl; };
+      const uint32_t mk_lo = (in(2 * c) ? 0x0000ffffu : 0u) | (in(2 * c + 1) ? 0xffff0000u : 0u);
+      const uint32_t mk_hi = (in(2 * c + 8) ? 0x0000ffffu : 0u) | (in(2 * c + 9) ? 0xffff0000u : 0u);
       if (KVT == kKvBf16) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {

@@ -17,6 +17,18 @@ constexpr int kKvBf16 = 0;
 constexpr int kKvFp8 = 1;   // E4M3
 constexpr int kKvE5M2 = 2;  // E5M2
 
+// First key a query at position pos attends under local attention: a sliding
+// window of `window` keys ending at pos starts at pos - window + 1;
+// chunked-local attention over chunks of `chunk` positions starts at the
+// query's chunk, (pos / chunk) * chunk.  0 disables either; with both the
+// later start applies; never below 0.
+__host__ __device__ __forceinline__ int local_first_key(int pos, int window, int chunk) {
+  int lo = 0;
+  if (window > 0) lo = pos - window + 1 > lo ? pos - window + 1 : lo;
+  if (chunk > 0) lo = (pos / chunk) * chunk > lo ? (pos / chunk) * chunk : lo;
+  return lo;
+}
+
 // A wait on an mbarrier gives up after this many nanoseconds.  Every
 // legitimate wait in these kernels lasts microseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

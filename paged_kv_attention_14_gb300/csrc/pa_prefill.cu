@@ -47,6 +47,8 @@ struct PrefillArgs {
   int qt;  // queries per CTA
   float qscale;
   float vscale;
+  int window;  // local attention (see pa_kv_desc), 0: none
+  int chunk;
 };
 
 template <int D, int KVT, int NW>
@@ -79,7 +81,12 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);  // queries of this CTA
   const int base_pos = L - q_len + qt0;   // position of query qt0
-  const int kv_end = base_pos + nq;       // keys [0, kv_end) are needed
+  const int kv_end = base_pos + nq;       // keys [kv_lo, kv_end) are needed
+  // local attention: the CTA's earliest query sees keys from kv_lo on (the
+  // first key never decreases with the position); its latest from lo_max
+  const int kv_lo = local_first_key(base_pos, a.window, a.chunk);
+  const int lo_max = local_first_key(kv_end - 1, a.window, a.chunk);
+  const int kt0 = kv_lo / C::KT;
   const int n_tiles = (kv_end + C::KT - 1) / C::KT;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -103,14 +110,14 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
     vraw[1] = kraw[1] + C::RAW;
   }
 
-  // gather one 64-key tile (zero-filled past kv_end) into buffer `b`
+  // gather one 64-key tile (zero-filled outside [kv_lo, kv_end)) into buffer `b`
   auto load_tile = [&](int kt, int b) {
     if (KVT == kKvBf16) {
       for (int i = tid; i < C::KT * C::CH; i += C::NT) {
         const int key = i / C::CH;
         const int ch = i - key * C::CH;
         const int t = kt * C::KT + key;
-        const bool ok = t < kv_end;
+        const bool ok = t < kv_end && t >= kv_lo;
         int64_t off = 0;
         if (ok) {
           const int phys = __ldg(table + (t >> 4));
@@ -125,7 +132,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
         const int key = i / RCH;
         const int ch = i - key * RCH;
         const int t = kt * C::KT + key;
-        const bool ok = t < kv_end;
+        const bool ok = t < kv_end && t >= kv_lo;
         int64_t off = 0;
         if (ok) {
           const int phys = __ldg(table + (t >> 4));
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
     }
   };
 
-  load_tile(0, 0);
+  load_tile(kt0, kt0 & 1);
 
   // ---- Q fragments of this warp's 16 rows (row = query * g + head)
   const int r_lo = warp * 16 + (lane >> 2);
@@ -184,9 +191,12 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
     qa[ks][2] = ok_lo ? __ldg(reinterpret_cast<const uint32_t *>(q_lo + d0 + 8)) : 0u;
     qa[ks][3] = ok_hi ? __ldg(reinterpret_cast<const uint32_t *>(q_hi + d0 + 8)) : 0u;
   }
-  // causal limit of each row (keys <= pos); invalid rows see no key
+  // causal limit of each row (keys <= pos); invalid rows see no key; first
+  // key of each row under local attention
   const int pos_lo = ok_lo ? base_pos + row_query(r_lo) : -1;
   const int pos_hi = ok_hi ? base_pos + row_query(r_hi) : -1;
+  const int first_lo = local_first_key(pos_lo, a.window, a.chunk);
+  const int first_hi = local_first_key(pos_hi, a.window, a.chunk);
   // the lowest position of any row of the CTA: tiles entirely below it need no mask
   const int pos_min = base_pos;
 
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   for (int n = 0; n < D / 8; ++n) oacc[n][0] = oacc[n][1] = oacc[n][2] = oacc[n][3] = 0.f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
-  for (int kt = 0; kt < n_tiles; ++kt) {
+  for (int kt = kt0; kt < n_tiles; ++kt) {
     const int b = (KVT == kKvBf16) ? (kt & 1) : 0;
     if (kt + 1 < n_tiles) {
       load_tile(kt + 1, (kt + 1) & 1);
@@ -232,7 +242,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
       }
     }
     // scale, mask, row max
-    const bool need_mask = kt * C::KT + C::KT - 1 > pos_min;
+    const bool need_mask = kt * C::KT + C::KT - 1 > pos_min || kt * C::KT < lo_max;
     float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
@@ -242,8 +252,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
         float vlo = sacc[n][e] * a.qscale;
         float vhi = sacc[n][2 + e] * a.qscale;
         if (need_mask) {
-          vlo = t <= pos_lo ? vlo : -INFINITY;
-          vhi = t <= pos_hi ? vhi : -INFINITY;
+          vlo = (t <= pos_lo && t >= first_lo) ? vlo : -INFINITY;
+          vhi = (t <= pos_hi && t >= first_hi) ? vhi : -INFINITY;
         }
         sacc[n][e] = vlo;
         sacc[n][2 + e] = vhi;
@@ -393,6 +403,8 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   const float ks = (fp8 && d.k_scale != 0.f) ? d.k_scale : 1.f;
   a.qscale = scale * ks * kLog2e;
   a.vscale = (fp8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
+  a.window = d.sliding_window;
+  a.chunk = d.attention_chunk;
   void *fn;
   size_t smem;
   if (d.head_dim == 128) {

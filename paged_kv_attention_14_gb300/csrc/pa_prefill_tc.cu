@@ -88,6 +88,8 @@ struct Args {
   int g;
   int qt;  // queries per CTA (256 / g)
   float qscale;
+  int window;  // local attention (see pa_kv_desc), 0: none
+  int chunk;
 };
 
 // Error bits of the prefill kernel (a bounded wait ran out); device code
@@ -186,8 +188,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);
   const int base_pos = L - q_len + qt0;  // position of query qt0
-  const int kv_end = base_pos + nq;      // keys [0, kv_end) are needed
+  const int kv_end = base_pos + nq;      // keys [kv_lo, kv_end) are needed
+  // local attention: the CTA's earliest query sees keys from kv_lo on (the
+  // first key never decreases with the position).  KV tiles j0 .. n_tiles - 1
+  // are walked; the rings and barriers count iterations jj = j - j0.
+  const int kv_lo = local_first_key(base_pos, a.window, a.chunk);
+  const int j0 = kv_lo / KT;
   const int n_tiles = (kv_end + KT - 1) / KT;
+  const int n_iter = n_tiles - j0;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -248,22 +256,26 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const int hh = lane % C::HALVES;
     const bool issuer = lane < BPT * C::HALVES;
     int phys_next = 0;
-    if (issuer && bi * 16 < kv_end) phys_next = __ldg(table + bi);
+    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = __ldg(table + j0 * BPT + bi);
     PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    for (int jj = 0; jj < n_iter && ok; ++jj) {
+      const int j = j0 + jj;
       const int phys = phys_next;
       const int key0 = j * KT;
       const int lb = (j + 1) * BPT + bi;  // prefetch the next tile's block id
       phys_next = (issuer && lb * 16 < kv_end) ? __ldg(table + lb) : 0;
       const int nblk = min(BPT, (kv_end - key0 + 15) / 16);
+      // blocks of the first tile entirely before the CTA's first key are not
+      // read (under local attention their pages may be gone)
+      const int bskip = jj == 0 ? (kv_lo >> 4) - j * BPT : 0;
       const int row = (phys * a.num_kv_heads + kvh) * 16;
       // K of tile j (its slot frees once the QKs of tile j - NSK completed),
       // then V of tile j (once the PVs of tile j - NSV completed)
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {
-        const int st = part ? j % NSV : j % NSK;
-        const uint32_t ph = part ? (j / NSV) & 1 : (j / NSK) & 1;
+        const int st = part ? jj % NSV : jj % NSK;
+        const uint32_t ph = part ? (jj / NSV) & 1 : (jj / NSK) & 1;
         const int full = (part ? V_FULL : K_FULL) + st;
         PF_TRACE(const long long tw = clock64();)
         if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1)) {
@@ -271,13 +283,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           break;
         }
         PF_TRACE(tp_wait += clock64() - tw;)
-        if (lane == 0) mbar_arrive_expect_tx(&bar[full], nblk * C::BLOCK_BYTES);
+        if (part == 1 && bskip > 0) {
+          // V rows of the skipped blocks: zero (0 * NaN would not vanish in
+          // the PV), before the copies of the other blocks start
+          for (int i = lane; i < bskip * 16 * C::HALVES * 8; i += 32) {
+            const int rr = i / (C::HALVES * 8);
+            const int rem = i % (C::HALVES * 8);
+            *reinterpret_cast<uint4 *>(smem + C::OFF_V + st * C::KVB + (rem >> 3) * C::KVHALF + rr * 128 +
+                                       (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&bar[full], (nblk - bskip) * C::BLOCK_BYTES);
         __syncwarp();
-        if (issuer && bi < nblk) {
+        if (issuer && bi < nblk && bi >= bskip) {
           uint8_t *dst = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB + hh * C::KVHALF + bi * 16 * 128;
           tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
         }
-        if (lane == 0) *(part ? s_last_v : s_last_k) = j;
+        if (lane == 0) *(part ? s_last_v : s_last_k) = jj;
       }
     }
     if (!ok && lane == 0) *s_abort = 1;
@@ -287,9 +310,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       bool ok = true;
-      auto qk = [&](int t, int j) {  // S_t = Q_t K_j^T
+      auto qk = [&](int t, int jj) {  // S_t = Q_t K^T of iteration jj
         const uint32_t qbase = sbase + C::OFF_Q + t * C::QB;
-        const uint32_t kbase = sbase + C::OFF_K + (j % NSK) * C::KVB;
+        const uint32_t kbase = sbase + C::OFF_K + (jj % NSK) * C::KVB;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024);
@@ -297,8 +320,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           umma_bf16_ss(tmem + t * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
-      auto pv = [&](int t, int j) {  // O_t += (P_t hi + P_t lo) V_j, P_t from TMEM
-        const uint32_t vbase = sbase + C::OFF_V + (j % NSV) * C::KVB;
+      auto pv = [&](int t, int jj) {  // O_t += (P_t hi + P_t lo) V of iteration jj, P_t from TMEM
+        const uint32_t vbase = sbase + C::OFF_V + (jj % NSV) * C::KVB;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -306,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
             // keys 16 kk .. 16 kk + 15: chunk kk / 2, hi at +0, lo at +16
             const uint64_t bd = umma_desc_sw128(vbase + kk * 2048, C::KVHALF, 1024);
             umma_bf16_ts(tmem + C::O_COL + t * D, tmem + t * KT + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8, bd,
-                         C::IDESC_PV, (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                         C::IDESC_PV, (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
           }
         }
       };
@@ -325,38 +348,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           umma_commit(&bar[S_FULL + t]);
         }
       }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const bool next = j + 1 < n_tiles;
+      for (int jj = 0; jj < n_iter && ok; ++jj) {
+        const bool next = jj + 1 < n_iter;
         for (int t = 0; t < NQT; ++t) {
-          if (!mbar_wait_hint(&bar[P_FULL + t], j & 1)) {
+          if (!mbar_wait_hint(&bar[P_FULL + t], jj & 1)) {
             ok = false;
             break;
           }
-          PF_TL(t * 2, j);
+          PF_TL(t * 2, jj);
           tc_fence_after_sync();
-          pv(t, j);
+          pv(t, jj);
           if (t == NQT - 1) {
-            umma_commit(&bar[V_EMPTY + j % NSV]);  // both tiles are done with V of tile j
-            if (next && !mbar_wait(&bar[V_FULL + (j + 1) % NSV], ((j + 1) / NSV) & 1)) {
+            umma_commit(&bar[V_EMPTY + jj % NSV]);  // both tiles are done with V of iteration jj
+            if (next && !mbar_wait(&bar[V_FULL + (jj + 1) % NSV], ((jj + 1) / NSV) & 1)) {
               ok = false;
               break;
             }
           }
           if (next) {
             if (t == 0) {
-              if (!mbar_wait(&bar[K_FULL + (j + 1) % NSK], ((j + 1) / NSK) & 1)) {
+              if (!mbar_wait(&bar[K_FULL + (jj + 1) % NSK], ((jj + 1) / NSK) & 1)) {
                 ok = false;
                 break;
               }
             }
             tc_fence_after_sync();
-            qk(t, j + 1);
+            qk(t, jj + 1);
           }
-          // S_t of tile j + 1 is ready and PV_t(j) has completed (after the
-          // last tile: O_t is final)
+          // S_t of the next KV tile is ready and PV_t(jj) has completed
+          // (after the last tile: O_t is final)
           umma_commit(&bar[S_FULL + t]);
-          if (t == 0) umma_commit(&bar[K_EMPTY + j % NSK]);  // both tiles are done with K of tile j
-          PF_TL(t * 2 + 1, j);
+          if (t == 0) umma_commit(&bar[K_EMPTY + jj % NSK]);  // both tiles are done with K of iteration jj
+          PF_TL(t * 2 + 1, jj);
         }
       }
       if (!ok) *s_abort = 1;
@@ -376,26 +399,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const int qi = R / g;
     const bool rv = R < rows_used && qi < nq;
     const int pos = rv ? base_pos + qi : -1;  // keys <= pos are visible
+    const int first = local_first_key(pos, a.window, a.chunk);  // ... and keys >= first
     const float qscale = a.qscale;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc, tk;)
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int jj = 0; jj < n_iter; ++jj) {
+      const int j = j0 + jj;
       PF_TRACE(tc = clock64();)
-      if (!mbar_wait_hint(&bar[S_FULL + t], j & 1)) {
+      if (!mbar_wait_hint(&bar[S_FULL + t], jj & 1)) {
         ok = false;
         break;
       }
       PF_TRACE(tq[0] += clock64() - tc; tc = clock64();)
-      if (r == 0) PF_TL(4 + t * 2, j);
+      if (r == 0) PF_TL(4 + t * 2, jj);
       tc_fence_after_sync();
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(20, j);
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(20, jj);
       const int key0 = j * KT;
-      if (t == 0 && j == n_tiles - 1 && kv_end - key0 < KT) {
+      if (t == 0 && jj == n_iter - 1 && kv_end - key0 < KT) {
         // V rows past the last needed key: zero (stale or poisoned data),
         // after this tile's V copies landed; tile 0's PV of this KV tile is
         // issued before tile 1's
-        if (!mbar_wait(&bar[V_FULL + j % NSV], (j / NSV) & 1)) {
+        if (!mbar_wait(&bar[V_FULL + jj % NSV], (jj / NSV) & 1)) {
           ok = false;
           break;
         }
@@ -403,7 +428,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         for (int i = r; i < (KT - kval) * C::HALVES * 8; i += MT) {
           const int row = kval + i / (C::HALVES * 8);
           const int rem = i % (C::HALVES * 8);
-          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (j % NSV) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
+          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (jj % NSV) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
@@ -420,7 +445,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       uint32_t sc[2][32];
       tmem_ld32_async(trow + s_col, sc[0]);
       tmem_wait_ld(sc[0]);
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(21, j);
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(21, jj);
 #pragma unroll
       for (int c = 0; c < KT / 32; ++c) {
         uint32_t(&cur)[32] = sc[c & 1];
@@ -428,11 +453,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         if (c + 1 < KT / 32) tmem_ld32_async(trow + s_col + (c + 1) * 32, sc[(c + 1) & 1]);
         PF_TRACE(tq[4] += clock64() - tk; tk = clock64();)
         const int kc = key0 + c * 32;
-        const bool unmasked = kc + 31 <= pos;
+        const bool unmasked = kc + 31 <= pos && kc >= first;
         if (!unmasked) {
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (kc + i > pos) cur[i] = __float_as_uint(-INFINITY);
+            if (kc + i > pos || kc + i < first) cur[i] = __float_as_uint(-INFINITY);
         }
         // raw scores; the scale (> 0) is applied with the max subtraction.
         // Tree of three-input maxima (depth 4, not a 32-long chain).
@@ -455,7 +480,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           PF_TRACE(const long long tr = clock64();)
           const float corr = (raise && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
           if (raise) l *= corr;
-          if (j > 0) {
+          if (jj > 0) {
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
               float o[32];
@@ -513,19 +538,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         tmem_st16_async(trow + s_col + c * 32 + 16, lo);
         if (c + 1 < KT / 32) tmem_wait_ld(sc[(c + 1) & 1]);
       }
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(22, j);
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(22, jj);
       tmem_wait_st();
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(23, j);
+      if (tid == kSoftmaxWarp0 * 32) PF_TL(23, jj);
       PF_TRACE(tq[3] += clock64() - tc; tc = clock64();)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
-      if (r == 0) PF_TL(5 + t * 2, j);
-      if (lane == 0) PF_TL(8 + warp - kSoftmaxWarp0, j);
+      if (r == 0) PF_TL(5 + t * 2, jj);
+      if (lane == 0) PF_TL(8 + warp - kSoftmaxWarp0, jj);
     }
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
              if (tid == kSoftmaxWarp0 * 32 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
-    if (ok && !mbar_wait(&bar[S_FULL + t], n_tiles & 1)) ok = false;
+    if (ok && !mbar_wait(&bar[S_FULL + t], n_iter & 1)) ok = false;
     if (ok) {
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -618,6 +643,8 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   a.g = d.num_q_heads / d.num_kv_heads;
   a.qt = MROWS / a.g;  // queries per CTA
   a.qscale = scale * kLog2e;
+  a.window = d.sliding_window;
+  a.chunk = d.attention_chunk;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
   auto fn = &prefill_tc_kernel<D>;

@@ -26,11 +26,11 @@ def kv_code(b: W.PagedBatch) -> int:
 
 
 def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO,
-            prefill_impl: int = B.PA_PREFILL_AUTO) -> B.PaKvDesc:
+            prefill_impl: int = B.PA_PREFILL_AUTO, window: int = 0, chunk: int = 0) -> B.PaKvDesc:
     return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
                        b.k_scale if b.kv_dtype != W.KV_BF16 else 0.0,
                        b.v_scale if b.kv_dtype != W.KV_BF16 else 0.0, decode_impl=decode_impl,
-                       prefill_impl=prefill_impl)
+                       prefill_impl=prefill_impl, sliding_window=window, attention_chunk=chunk)
 
 
 def gpu_caches(b: W.PagedBatch):
@@ -58,12 +58,13 @@ def oracle_caches(b: W.PagedBatch):
     return code, kc, vc
 
 
-def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO, workspace=None):
+def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO, workspace=None, window=0,
+               chunk=0):
     kc, vc = caches if caches is not None else gpu_caches(b)
     S = b.context_lens_decode.shape[0]
     out = torch.full((S, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
     lse = torch.full((S, b.num_q_heads), float("nan"), device=kc.device)
-    d = desc_of(b, decode_impl)
+    d = desc_of(b, decode_impl, window=window, chunk=chunk)
     maxL = b.max_context_len_decode()
     ws = workspace if workspace is not None else B.decode_workspace(d, S, maxL, kc.device)
     B.pa_decode(d, out, b.q_decode, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL, b.scale, ws,
@@ -73,14 +74,14 @@ def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO
     return out, lse
 
 
-def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None):
+def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
     return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode.cpu(), kc, vc,
                          b.block_tables_decode.cpu(), b.context_lens_decode.cpu(), b.scale, b.k_scale,
-                         b.v_scale, pairs=pairs)
+                         b.v_scale, pairs=pairs, window=window, chunk=chunk)
 
 
-def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO):
+def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO, window=0, chunk=0):
     kc, vc = caches if caches is not None else gpu_caches(b)
     Tq = b.q_prefill.shape[0]
     out = torch.full((Tq, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
@@ -88,17 +89,19 @@ def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_A
     qsl = b.query_start_loc
     max_q = int((qsl[1:] - qsl[:-1]).max())
     maxL = int(b.context_lens_prefill.max())
-    B.pa_prefill_chunk(desc_of(b, prefill_impl=prefill_impl), out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill,
+    B.pa_prefill_chunk(desc_of(b, prefill_impl=prefill_impl, window=window, chunk=chunk), out, b.q_prefill, qsl, kc,
+                       vc, b.block_tables_prefill,
                        b.context_lens_prefill, max_q, maxL, b.scale, lse=lse)
     torch.cuda.synchronize()
     return out, lse
 
 
-def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None):
+def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
     return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill.cpu(),
                           b.query_start_loc.cpu(), kc, vc, b.block_tables_prefill.cpu(),
-                          b.context_lens_prefill.cpu(), b.scale, b.k_scale, b.v_scale, pairs=pairs)
+                          b.context_lens_prefill.cpu(), b.scale, b.k_scale, b.v_scale, pairs=pairs,
+                          window=window, chunk=chunk)
 
 
 def assert_close(got: torch.Tensor, want: np.ndarray, tol: float, what: str = ""):

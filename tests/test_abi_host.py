@@ -58,7 +58,7 @@ def test_desc_struct_matches_header_layout():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in B.PaKvDesc._fields_]
-    assert ctypes.sizeof(B.PaKvDesc) == 40
+    assert ctypes.sizeof(B.PaKvDesc) == 48
 
 
 def _desc(**kw):
@@ -93,6 +93,8 @@ def test_cache_write_argument_errors(lib):
     ("num_q_heads", 34, B.PA_ERR_UNSUPPORTED),    # group size 17
     ("kv_dtype", 7, B.PA_ERR_INVALID_ARG),
     ("num_blocks", -1, B.PA_ERR_INVALID_ARG),
+    ("sliding_window", -1, B.PA_ERR_INVALID_ARG),
+    ("attention_chunk", -5, B.PA_ERR_INVALID_ARG),
 ])
 def test_descriptor_validation(lib, field, value, status):
     d = _desc()
