@@ -14,7 +14,9 @@ algorithmic KV bytes of the step (every valid K and V element of every
 (sequence, kv head) once) divided by the device time of the step, with the
 inputs resident in HBM.  The step's KV (304 MB) is larger than the 129 MB L2
 and read in the same order every step, so no L2 flush is needed between steps
-(smaller working sets are flushed by writing a buffer of twice the L2 size).
+(smaller working sets are flushed between steps: a write of a buffer of twice
+the L2 size, then a read of another one, so that no dirty line of the flush is
+written back inside the timed region).
 
 ``--impl reference`` times the fp64 CPU oracle instead (the only reference
 implementation of this method), on a bounded sample of the same workload.
@@ -95,52 +97,110 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons of one GPU, sampled while running."""
+    """nvidia-smi clocks and throttle reasons of one GPU, sampled while running.
+
+    A reader thread stamps every sample with the host clock; ``stop()`` keeps
+    the samples taken between ``mark_start()`` and ``mark_end()`` (the timed
+    region), or all of them if that region was shorter than the sampling
+    period.  The GPU is named by its UUID, which nvidia-smi and CUDA agree on
+    whatever the device numbering."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index: int, out_path: str | None = None):
         self.gpu = gpu_index
         self.proc = None
         self.out_path = out_path
+        self.lines = []
+        self.thread = None
+        self.t0 = self.t1 = None
+        self.stopping = False
+
+    def _target(self) -> str:
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.gpu).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.gpu)
+
+    def _spawn(self):
+        return subprocess.Popen(["nvidia-smi", "-i", self._target(), f"--query-gpu={self.FIELDS}",
+                                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
+                                stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+
+    def _read(self):
+        # nvidia-smi sometimes exits at once with "No devices were found" (NVML
+        # busy); it is started again until stop() is called
+        while True:
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line))
+            self.proc.wait()
+            if self.stopping:
+                return
+            time.sleep(self.PERIOD_MS / 1000)
+            try:
+                self.proc = self._spawn()
+            except OSError:
+                return
 
     def start(self):
+        import threading
+        self.stopping = False
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = self._spawn()
         except OSError:
             self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
         time.sleep(0.3)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.15)
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        self.stopping = True
+        for _ in range(3):  # the reader may have just started a new nvidia-smi
+            p = self.proc
+            p.terminate()
+            try:
+                p.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                p.kill()
+            self.thread.join(timeout=1)
+            if not self.thread.is_alive():
+                break
         if self.out_path:
             with open(self.out_path, "w") as f:
-                f.write(out)
-        sm, smax, reasons = [], [], set()
+                f.write("".join(f"{t:.4f},{line}" for t, line in self.lines))
+        parsed = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for t, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                parsed.append((t, float(parts[1]), float(parts[2]),
+                               {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not parsed:
+            first = self.lines[0][1].strip() if self.lines else ""
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples" + (f": {first}" if first else "")]}
+        inside = [p for p in parsed if self.t0 is not None and self.t1 is not None and self.t0 <= p[0] <= self.t1]
+        use = inside or parsed
+        return {"sm_mhz": statistics.median(p[1] for p in use), "sm_max_mhz": max(p[2] for p in use),
+                "reasons": sorted(set().union(*(p[3] for p in use))), "samples": len(use),
+                "samples_in_timed_region": len(inside)}
 
 
 def _first_key(pos: int, window: int, chunk: int) -> int:
@@ -162,6 +222,22 @@ def _local_config(args) -> dict:
     if args.attention_chunk:
         d["attention_chunk"] = args.attention_chunk
     return d
+
+
+class _L2Flush:
+    """Evicts the L2 between timed steps: a write of one buffer of ``nbytes``
+    and a read (a sum) of another."""
+
+    def __init__(self, nbytes: int, dev):
+        import torch
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 8, dtype=torch.int64, device=dev)
+        self.acc = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.acc)
 
 
 def _decode_kv_bytes(b, window: int, chunk: int) -> int:
@@ -235,8 +311,11 @@ def run_ours(args):
     launches_per_step = (3 if args.decode_impl != 1 else 2) + (1 if mixed else 0)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
-    if kv_bytes < 2 * l2_bytes:  # small working set: flush L2 by writing a buffer larger than it
-        flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+    if kv_bytes < 2 * l2_bytes:
+        # small working set: flush L2 by writing a buffer larger than it, then
+        # reading another one, which evicts the written (dirty) lines before
+        # the timed kernels start instead of during them
+        flush = _L2Flush(2 * l2_bytes, dev)
 
     def decode(q, bt, cl):
         B.pa_decode(desc, out, q, kc, vc, bt, cl, maxL, b.scale, wsp)
@@ -252,7 +331,7 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         if flush is not None:
-            flush.zero_()
+            flush()
         step()
     torch.cuda.synchronize()
 
@@ -263,13 +342,14 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    sampler.mark_start()
     # timed region 1: whole steps, CUDA events only at step boundaries (an
     # event between two kernels would cut the programmatic-dependent overlap
     # of the decode launch with the cache write)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K):
         if flush is not None:
-            flush.zero_()
+            flush()
         ev[i][0].record()
         step()
         ev[i][1].record()
@@ -280,7 +360,7 @@ def run_ours(args):
     ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
     for i in range(K2):
         if flush is not None:
-            flush.zero_()
+            flush()
         ev_d[i][0].record()
         decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
         ev_d[i][1].record()
@@ -289,6 +369,7 @@ def run_ours(args):
             prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
             ev_p[i][1].record()
     torch.cuda.synchronize()
+    sampler.mark_end()
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -337,13 +418,13 @@ def run_ours(args):
 
     for _ in range(max(3, args.warmup)):
         if flush is not None:
-            flush.zero_()
+            flush()
         e2e_step()
     ke = max(10, min(K, 200))
     tot = 0.0
     for _ in range(ke):
         if flush is not None:
-            flush.zero_()
+            flush()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step()
@@ -376,7 +457,7 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": b.name, "num_seqs": S, "kv_tokens": int(b.context_lens_decode.sum()),
                        "kv_bytes_per_step": kv_bytes,
-                       "l2": ("flushed before every step (write of 2x L2)" if flush is not None else
+                       "l2": ("flushed before every step (write of 2x L2, then read of 2x L2)" if flush is not None else
                               f"inputs larger than L2 ({kv_bytes >> 20} MiB KV vs {l2_bytes >> 20} MiB L2), no flush"),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", **_local_config(args)},
             "roofline": {"bound": "hbm",
