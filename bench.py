@@ -55,11 +55,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # source files hash to what they were when it was captured.
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
-    # decode + merge kernels (the roofline times both)
-    "decode": {"workload": 2, "bytes": 306_494_745,
-               "sha256": "475a31949c0f12d43a94c3c94226b745014ff84c3f9391a95789047dec2a2a99",
+    # the decode kernel (split segments are merged inside it)
+    "decode": {"workload": 2, "bytes": 306_007_734,
+               "sha256": "e6b1557f485fecf67ee7b888797de6f57be18a6a486efbe9ca43339e2b2ac4a8",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
-    "prefill": {"workload": 5, "bytes": 46_278_070, "sha256": "bc8c2e7ae729a2b90f2c5db2f3b92ade271efd2710271e0cd2262636172a18a8",
+    "prefill": {"workload": 5, "bytes": 46_295_106, "sha256": "341e3e145083b1f30129dd55e240d938754b81bc1a83734de218afa480e69ecb",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
 }
 
@@ -307,8 +307,8 @@ def run_ours(args):
         pf_maxq = int((qsl[1:] - qsl[:-1]).max())
         pf_maxL = int(b.context_lens_prefill.max())
         pf_flops = _prefill_flops(b, args.sliding_window, args.attention_chunk)
-    # cache write + decode (+ the merge kernel of the tensor-core decode) (+ prefill)
-    launches_per_step = (3 if args.decode_impl != 1 else 2) + (1 if mixed else 0)
+    # cache write + decode (+ prefill)
+    launches_per_step = 2 + (1 if mixed else 0)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
     if kv_bytes < 2 * l2_bytes:
@@ -461,7 +461,7 @@ def run_ours(args):
                               f"inputs larger than L2 ({kv_bytes >> 20} MiB KV vs {l2_bytes >> 20} MiB L2), no flush"),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", **_local_config(args)},
             "roofline": {"bound": "hbm",
-                         "kernel": "pa_decode (decode kernel + merge kernel), timed alone per call",
+                         "kernel": "pa_decode (one decode kernel launch), timed alone per call",
                          "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
                          "traffic": _traffic("decode", args.workload, local)},

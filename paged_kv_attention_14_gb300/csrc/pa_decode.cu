@@ -179,9 +179,7 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
   a.err = reinterpret_cast<int32_t *>(ws);
-  a.per_cta_out = reinterpret_cast<long long *>(ws + 8);
   a.seg_counter = reinterpret_cast<int32_t *>(ws + w.counter_off);
-  a.rec = reinterpret_cast<dec::SegRec *>(ws + w.rec_off);
   a.slot_lse = reinterpret_cast<float *>(ws + w.slot_lse_off);
   a.slot_o = reinterpret_cast<float *>(ws + w.slot_o_off);
   // programmatic dependent launch: the kernel's launch overlaps the tail of
@@ -198,38 +196,7 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   dcfg.attrs = pdl;
   dcfg.numAttrs = 1;
   void *args[] = {&a};
-  cudaError_t e = cudaLaunchKernelExC(&dcfg, k.fn, args);
-  if (e != cudaSuccess || !k.mma) return e;
-
-  // merge of the segments split across CTAs, launched as a programmatic
-  // dependent of the decode grid so that its launch overlaps the decode tail
-  dec::MergeArgs mg;
-  mg.out = out;
-  mg.lse = lse;
-  mg.slot_lse = a.slot_lse;
-  mg.slot_o = a.slot_o;
-  mg.rec = a.rec;
-  mg.per_cta = a.per_cta_out;
-  mg.num_q_heads = d.num_q_heads;
-  mg.g = a.g;
-  mg.hg = k.hg;
-  mg.gq = k.slot_heads / k.hg;
-  mg.slot_heads = k.slot_heads;
-  mg.vscale = a.vscale;
-  mg.err = a.err;
-  const int nh = k.hg * a.g;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.num_ctas, (nh + dec::kMergeHeads - 1) / dec::kMergeHeads);
-  cfg.blockDim = dim3(dec::kMergeHeads * (d.head_dim / 4) * dec::kMergeGroups);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (d.head_dim == 128) return cudaLaunchKernelEx(&cfg, dec::decode_merge_kernel<128>, mg);
-  return cudaLaunchKernelEx(&cfg, dec::decode_merge_kernel<64>, mg);
+  return cudaLaunchKernelExC(&dcfg, k.fn, args);
 }
 
 }  // namespace pa
