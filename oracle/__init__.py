@@ -30,6 +30,7 @@ _lib = None
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 KV_FP8_E5M2 = 2
+KV_F16 = 3
 
 
 def build(force: bool = False) -> str:
@@ -61,6 +62,8 @@ def _load():
         lib.pa_oracle_e5m2_decode.restype = ctypes.c_double
         lib.pa_oracle_e5m2_encode.argtypes = [ctypes.c_double]
         lib.pa_oracle_e5m2_encode.restype = ctypes.c_uint8
+        lib.pa_oracle_f16_decode.argtypes = [ctypes.c_uint16]
+        lib.pa_oracle_f16_decode.restype = ctypes.c_double
         lib.pa_oracle_cache_write.argtypes = [I, I, I, I, P, P, P, I, F, F, P, P]
         lib.pa_oracle_cache_write.restype = None
         lib.pa_oracle_attend_range.argtypes = [I, I, I, I, P, P, P, P, I, I, I, F, F, F, P, P]
@@ -101,7 +104,7 @@ def _ptr(a: np.ndarray):
 
 
 def _cache_np(cache, kv_dtype):
-    return _np(cache, np.uint16 if kv_dtype == KV_BF16 else np.uint8)
+    return _np(cache, np.uint16 if kv_dtype in (KV_BF16, KV_F16) else np.uint8)
 
 
 def e4m3_decode(byte: int) -> float:
@@ -118,6 +121,10 @@ def e5m2_decode(byte: int) -> float:
 
 def e5m2_encode(x: float) -> int:
     return int(_load().pa_oracle_e5m2_encode(float(x)))
+
+
+def f16_decode(bits: int) -> float:
+    return _load().pa_oracle_f16_decode(int(bits) & 0xFFFF)
 
 
 def cache_write(kv_dtype, block_size, num_kv_heads, head_dim, k, v, slot_mapping,

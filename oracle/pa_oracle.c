@@ -27,8 +27,11 @@
  *
  * Layout (the reading this build takes where the pages are silent):
  *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
- *                      bf16 bit patterns (uint16) or E4M3 / E5M2 bytes (uint8)
- *   q                : [tokens][num_q_heads][head_dim] bf16 bit patterns
+ *                      bf16 or fp16 bit patterns (uint16), or E4M3 / E5M2
+ *                      bytes (uint8)
+ *   q, new k / v rows: [tokens][heads][head_dim] bf16 bit patterns; fp16 bit
+ *                      patterns with an fp16 cache (the cache of an fp16
+ *                      model, whose activations are fp16 too)
  *   block_tables     : int32 [num_seqs][max_blocks_per_seq]
  *   context_lens     : int32 [num_seqs], KV tokens including this step's
  *   slot_mapping     : int64 [tokens], slot = block * block_size + offset, <0 skip
@@ -47,6 +50,10 @@
 #define KV_BF16 0
 #define KV_FP8_E4M3 1
 #define KV_FP8_E5M2 2
+#define KV_F16 3
+
+/* scales apply to the 8-bit formats only */
+static int kv_is_8bit(int kv_dtype) { return kv_dtype == KV_FP8_E4M3 || kv_dtype == KV_FP8_E5M2; }
 
 /* ---------------------------------------------------------------- bf16 */
 
@@ -63,6 +70,33 @@ static float bf16_bits_to_float(uint16_t b) {
   float f;
   memcpy(&f, &u, sizeof f);
   return f;
+}
+
+/* ---------------------------------------------------------------- fp16 */
+
+/*
+ * IEEE 754 binary16: 1 sign bit, 5 exponent bits with bias 15, 10 mantissa
+ * bits.  Exponent field 0 encodes subnormals m/1024 * 2^-14; exponent 31
+ * encodes infinity (m = 0) and NaN (m != 0); otherwise (1 + m/1024) *
+ * 2^(e - 15).  Every value is exact in double.
+ */
+double pa_oracle_f16_decode(uint16_t b) {
+  int sign = (b >> 15) & 1;
+  int e = (b >> 10) & 31;
+  int m = b & 1023;
+  double v;
+  if (e == 31)
+    v = m ? NAN : INFINITY;
+  else if (e == 0)
+    v = ldexp((double)m, -24);
+  else
+    v = ldexp((double)(1024 + m), e - 25);
+  return sign ? -v : v;
+}
+
+/* A query or new-row element: fp16 bits with an fp16 cache, bf16 bits otherwise. */
+static double act_to_double(int kv_dtype, uint16_t b) {
+  return kv_dtype == KV_F16 ? pa_oracle_f16_decode(b) : bf16_bits_to_double(b);
 }
 
 /* ---------------------------------------------------------------- E4M3 */
@@ -189,6 +223,10 @@ static double kv_elem(int kv_dtype, const void *cache, int64_t row_index, int he
     const uint16_t *c = (const uint16_t *)cache;
     return bf16_bits_to_double(c[row_index * head_dim + d]);
   }
+  if (kv_dtype == KV_F16) {
+    const uint16_t *c = (const uint16_t *)cache;
+    return pa_oracle_f16_decode(c[row_index * head_dim + d]);
+  }
   const uint8_t *c = (const uint8_t *)cache;
   if (kv_dtype == KV_FP8_E5M2) {
     e5m2_table_init();
@@ -211,8 +249,8 @@ static int64_t cache_row(const int32_t *table_row, int block_size, int num_kv_he
  * For each token i with slot_mapping[i] >= 0: block = slot / block_size,
  * offset = slot % block_size, and for every kv head h the cache row
  * (block, h, offset) receives enc(k[i][h][:]) (same for v).
- * enc = bit copy for bf16; for E4M3 / E5M2, enc(x) = e4m3 / e5m2 of
- * fl32(fl32(x) / scale).
+ * enc = bit copy for bf16 and fp16 (the rows arrive in the cache's own
+ * type); for E4M3 / E5M2, enc(x) = e4m3 / e5m2 of fl32(fl32(x) / scale).
  */
 void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int head_dim,
                            const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
@@ -228,7 +266,7 @@ void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int h
       const uint16_t *ks = k + ((int64_t)i * num_kv_heads + h) * head_dim;
       const uint16_t *vs = v + ((int64_t)i * num_kv_heads + h) * head_dim;
       for (int d = 0; d < head_dim; ++d) {
-        if (kv_dtype == KV_BF16) {
+        if (!kv_is_8bit(kv_dtype)) {
           ((uint16_t *)k_cache)[dst_row * head_dim + d] = ks[d];
           ((uint16_t *)v_cache)[dst_row * head_dim + d] = vs[d];
         } else {
@@ -264,15 +302,15 @@ void pa_oracle_attend_range(int kv_dtype, int block_size, int num_kv_heads, int 
     *lse = -INFINITY;
     return;
   }
-  double ks = (kv_dtype != KV_BF16) ? (double)k_scale : 1.0;
-  double vs = (kv_dtype != KV_BF16) ? (double)v_scale : 1.0;
+  double ks = kv_is_8bit(kv_dtype) ? (double)k_scale : 1.0;
+  double vs = kv_is_8bit(kv_dtype) ? (double)v_scale : 1.0;
   double *x = (double *)malloc(sizeof(double) * (size_t)n);
   double m = -INFINITY;
   for (int j = 0; j < n; ++j) {
     int64_t row = cache_row(table_row, block_size, num_kv_heads, kh, t_begin + j);
     double dot = 0.0;
     for (int d = 0; d < head_dim; ++d)
-      dot += bf16_bits_to_double(q_vec[d]) * kv_elem(kv_dtype, k_cache, row, head_dim, d, ks);
+      dot += act_to_double(kv_dtype, q_vec[d]) * kv_elem(kv_dtype, k_cache, row, head_dim, d, ks);
     x[j] = (double)scale * dot;
     if (x[j] > m) m = x[j];
   }

@@ -39,6 +39,7 @@ BLOCK_SIZE = 16
 KV_BF16 = "bf16"
 KV_FP8 = "fp8_e4m3"
 KV_FP8_E5M2 = "fp8_e5m2"
+KV_F16 = "fp16"
 E4M3_MAX = 448.0
 E5M2_MAX = 57344.0
 #: the largest finite magnitude of each 8-bit cache format
@@ -48,7 +49,8 @@ FP8_MAX = {KV_FP8: E4M3_MAX, KV_FP8_E5M2: E5M2_MAX}
 @dataclass
 class PagedBatch:
     """One step's inputs.  All tensors live on ``device``; bf16 tensors hold the
-    values, E4M3 caches are produced from ``k_pool``/``v_pool`` by a cache write."""
+    values (fp16 ones for an fp16 cache), 8-bit caches are produced from
+    ``k_pool``/``v_pool`` by a cache write."""
 
     name: str
     block_size: int
@@ -81,7 +83,7 @@ class PagedBatch:
 
     @property
     def kv_elem_bytes(self) -> int:
-        return 2 if self.kv_dtype == KV_BF16 else 1
+        return 2 if self.kv_dtype in (KV_BF16, KV_F16) else 1
 
     def decode_kv_bytes(self) -> int:
         """Algorithmic KV bytes of the decode part: every valid K and V element
@@ -119,8 +121,14 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def _randn(shape, g, device) -> torch.Tensor:
-    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+def act_dtype(kv_dtype: str) -> torch.dtype:
+    """Element type of q and of new K/V rows: fp16 for an fp16 cache (the cache
+    of an fp16 model), bf16 otherwise."""
+    return torch.float16 if kv_dtype == KV_F16 else torch.bfloat16
+
+
+def _randn(shape, g, device, dtype=torch.bfloat16) -> torch.Tensor:
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(dtype)
 
 
 def _pool_size(blocks_needed: int) -> int:
@@ -165,8 +173,8 @@ def _readable_mask(num_blocks, block_size, tables_and_lens):
 def _fill_pool(b: PagedBatch, g, device, poison: bool, readable: torch.Tensor,
                written: Optional[torch.Tensor]):
     shape = (b.num_blocks, b.num_kv_heads, b.block_size, b.head_dim)
-    b.k_pool = _randn(shape, g, device)
-    b.v_pool = _randn(shape, g, device)
+    b.k_pool = _randn(shape, g, device, act_dtype(b.kv_dtype))
+    b.v_pool = _randn(shape, g, device, act_dtype(b.kv_dtype))
     if b.kv_dtype in FP8_MAX:
         # per-tensor scales from the source values (amax / the format's max)
         ka = float(b.k_pool.float().abs().max())
@@ -184,7 +192,7 @@ def _fill_pool(b: PagedBatch, g, device, poison: bool, readable: torch.Tensor,
             wo = written % b.block_size
             bad[wb, wo] = True
         bad = bad.to(device)[:, None, :, None].expand(shape)
-        nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device=device)
+        nan = torch.tensor(float("nan"), dtype=b.k_pool.dtype, device=device)
         b.k_pool = torch.where(bad, nan, b.k_pool)
         b.v_pool = torch.where(bad, nan, b.v_pool)
 
@@ -202,7 +210,7 @@ def _decode_batch(name, seed, lens, Hq, Hkv, D, kv_dtype, scale, device, poison,
                    head_dim=D, kv_dtype=kv_dtype, scale=_f32(scale), k_scale=1.0, v_scale=1.0,
                    num_blocks=NB, k_pool=None, v_pool=None)
     g = _gen(seed + 7, device)
-    b.q_decode = _randn((S, Hq, D), g, device)
+    b.q_decode = _randn((S, Hq, D), g, device, act_dtype(kv_dtype))
     readable = _readable_mask(NB, BLOCK_SIZE, [(tables, lens)])
     _fill_pool(b, g, device, poison, readable, None)
     b.block_tables_decode = tables.to(device)
@@ -229,39 +237,49 @@ WORKLOAD_NAMES = {
 }
 
 
-def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP8) -> PagedBatch:
+def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP8,
+             fp16: bool = False) -> PagedBatch:
     """Build workload ``n`` (1..5) on ``device``.  ``fp8_format`` picks the
-    8-bit cache format of workload 4 (E4M3, or E5M2 for the same shapes)."""
+    8-bit cache format of workload 4 (E4M3, or E5M2 for the same shapes);
+    ``fp16`` turns the bf16 workloads (1, 2, 3, 5) into fp16 ones: fp16 cache,
+    q and new rows, from the same random draws."""
     seed = 1000 + n
+    kv16 = KV_F16 if fp16 else KV_BF16
+
+    def name(i):
+        return WORKLOAD_NAMES[i].replace("bf16", "fp16") if fp16 else WORKLOAD_NAMES[i]
+
     if n == 1:
-        return _decode_batch(WORKLOAD_NAMES[1],
-                             seed, [1, 7, 16, 33], 4, 2, 64, KV_BF16, 1.0 / 8.0, device, poison,
+        return _decode_batch(name(1) + (", fp16" if fp16 else ""),
+                             seed, [1, 7, 16, 33], 4, 2, 64, kv16, 1.0 / 8.0, device, poison,
                              num_blocks=64)
     if n == 2:
         g = _gen(seed, "cpu")
         lens = torch.randint(512, 4096 + 1, (32,), generator=g)
-        return _decode_batch(WORKLOAD_NAMES[2],
-                             seed, lens.tolist(), 32, 8, 128, KV_BF16, 1.0 / math.sqrt(128),
+        return _decode_batch(name(2),
+                             seed, lens.tolist(), 32, 8, 128, kv16, 1.0 / math.sqrt(128),
                              device, poison)
     if n == 3:
         g = _gen(seed, "cpu")
         ln = torch.empty(8, dtype=torch.float64).log_normal_(math.log(2048.0), 1.0, generator=g)
         lens = [int(min(max(round(float(x)), 128), 32768)) for x in ln] + [131072]
-        return _decode_batch(WORKLOAD_NAMES[3],
-                             seed, lens, 32, 8, 128, KV_BF16, 1.0 / math.sqrt(128), device, poison)
+        return _decode_batch(name(3),
+                             seed, lens, 32, 8, 128, kv16, 1.0 / math.sqrt(128), device, poison)
     if n == 4:
+        if fp16:
+            raise ValueError("workload 4 is the 8-bit cache workload")
         g = _gen(seed, "cpu")
         lens = torch.randint(1024, 8192 + 1, (128,), generator=g)
-        name = WORKLOAD_NAMES[4] if fp8_format == KV_FP8 else WORKLOAD_NAMES[4].replace("E4M3", "E5M2")
-        return _decode_batch(name,
+        nm = WORKLOAD_NAMES[4] if fp8_format == KV_FP8 else WORKLOAD_NAMES[4].replace("E4M3", "E5M2")
+        return _decode_batch(nm,
                              seed, lens.tolist(), 40, 8, 128, fp8_format, 1.0 / math.sqrt(128),
                              device, poison)
     if n == 5:
-        return _mixed_batch(seed, device, poison)
+        return _mixed_batch(seed, device, poison, kv16, name(5))
     raise ValueError(f"unknown workload {n}")
 
 
-def _mixed_batch(seed, device, poison) -> PagedBatch:
+def _mixed_batch(seed, device, poison, kv_dtype=KV_BF16, name=WORKLOAD_NAMES[5]) -> PagedBatch:
     Hq, Hkv, D, B = 32, 8, 128, BLOCK_SIZE
     g_cpu = _gen(seed, "cpu")
     dec_lens = torch.randint(256, 4096 + 1, (16,), generator=g_cpu).to(torch.int32)
@@ -294,15 +312,16 @@ def _mixed_batch(seed, device, poison) -> PagedBatch:
     slots = torch.cat([dec_slots, torch.tensor(pf_slots, dtype=torch.int64)])
     T = int(slots.shape[0])
 
-    b = PagedBatch(name=WORKLOAD_NAMES[5],
-                   block_size=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, kv_dtype=KV_BF16,
+    b = PagedBatch(name=name,
+                   block_size=B, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, kv_dtype=kv_dtype,
                    scale=_f32(1.0 / math.sqrt(D)), k_scale=1.0, v_scale=1.0, num_blocks=NB,
                    k_pool=None, v_pool=None)
     g = _gen(seed + 7, device)
-    b.q_decode = _randn((16, Hq, D), g, device)
-    b.q_prefill = _randn((n_pf * chunk, Hq, D), g, device)
-    b.k_new = _randn((T, Hkv, D), g, device)
-    b.v_new = _randn((T, Hkv, D), g, device)
+    act = act_dtype(kv_dtype)
+    b.q_decode = _randn((16, Hq, D), g, device, act)
+    b.q_prefill = _randn((n_pf * chunk, Hq, D), g, device, act)
+    b.k_new = _randn((T, Hkv, D), g, device, act)
+    b.v_new = _randn((T, Hkv, D), g, device, act)
     b.meta["k_new_independent"] = True
     readable = _readable_mask(NB, B, [(dec_tables, dec_lens), (pf_tables, pf_lens)])
     _fill_pool(b, g, device, poison, readable, slots)
@@ -356,7 +375,7 @@ def random_prefill(seed: int, q_lens, ctx_lens, Hq, Hkv, D, kv_dtype=KV_BF16, sc
                    num_kv_heads=Hkv, head_dim=D, kv_dtype=kv_dtype, scale=_f32(scale), k_scale=1.0,
                    v_scale=1.0, num_blocks=NB, k_pool=None, v_pool=None)
     g = _gen(seed + 7, device)
-    b.q_prefill = _randn((int(qsl[-1]), Hq, D), g, device)
+    b.q_prefill = _randn((int(qsl[-1]), Hq, D), g, device, act_dtype(kv_dtype))
     readable = _readable_mask(NB, B, [(tables, lens)])
     _fill_pool(b, g, device, poison, readable, None)
     b.block_tables_prefill = tables.to(device)

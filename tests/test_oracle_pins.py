@@ -1,7 +1,7 @@
 """Pins of the fp64 oracle against things other than itself.
 
 Each test checks the oracle against a library routine (torch's CPU SDPA and
-its float8_e4m3fn / float8_e5m2 codecs), a closed form, an invariant, or the format
+its float8_e4m3fn / float8_e5m2 codecs, numpy's float16), a closed form, an invariant, or the format
 definition's fixed points -- chosen so that a plausible slip anywhere in the
 oracle (wrong GQA index, wrong block offset, a dropped scale, an off-by-one in
 the causal position, a sign in the merge, an exponent bias) fails one of them.
@@ -15,7 +15,9 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import workloads as W
 
-BF16, FP8, E5M2 = oracle.KV_BF16, oracle.KV_FP8_E4M3, oracle.KV_FP8_E5M2
+BF16, FP8, E5M2, F16 = oracle.KV_BF16, oracle.KV_FP8_E4M3, oracle.KV_FP8_E5M2, oracle.KV_F16
+#: 16-bit cache types: generator name -> oracle code
+_KV16 = {W.KV_BF16: BF16, W.KV_F16: F16}
 #: generator cache type -> (oracle code, torch 8-bit dtype)
 _FP8_KINDS = {W.KV_FP8: (FP8, torch.float8_e4m3fn), W.KV_FP8_E5M2: (E5M2, torch.float8_e5m2)}
 
@@ -57,8 +59,8 @@ def _sdpa(q, k, v, scale, mask=None):
 def _oracle_caches(b: W.PagedBatch):
     """Caches as the oracle reads them: bf16 pool as-is, or the E4M3 / E5M2
     encoding of the whole (small) pool made by the oracle's own cache write."""
-    if b.kv_dtype == W.KV_BF16:
-        return BF16, b.k_pool, b.v_pool
+    if b.kv_dtype in _KV16:
+        return _KV16[b.kv_dtype], b.k_pool, b.v_pool
     code = _FP8_KINDS[b.kv_dtype][0]
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)
@@ -68,8 +70,8 @@ def _oracle_caches(b: W.PagedBatch):
 
 
 def _dense_pools(b: W.PagedBatch, kc, vc):
-    """K and V pools in fp64: the bf16 pool, or the 8-bit caches decoded by torch."""
-    if b.kv_dtype == W.KV_BF16:
+    """K and V pools in fp64: the bf16 / fp16 pool, or the 8-bit caches decoded by torch."""
+    if b.kv_dtype in _KV16:
         return _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
     dt = _FP8_KINDS[b.kv_dtype][1]
     return _fp8_cache_to_f64(kc, b.k_scale, dt), _fp8_cache_to_f64(vc, b.v_scale, dt)
@@ -187,11 +189,26 @@ def test_e5m2_encode_saturates_and_keeps_nan_and_signed_zero():
         assert oracle.e5m2_encode(oracle.e5m2_decode(c)) == c
 
 
+def test_f16_decode_matches_numpy_float16_for_all_65536_codes():
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = codes.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_decode(int(c)) for c in codes])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # fixed points of the binary16 definition
+    assert oracle.f16_decode(0x3C00) == 1.0 and oracle.f16_decode(0x7BFF) == 65504.0
+    assert oracle.f16_decode(0x0001) == 2.0 ** -24 and oracle.f16_decode(0x0400) == 2.0 ** -14
+    assert oracle.f16_decode(0xFC00) == -math.inf and math.copysign(1, oracle.f16_decode(0x8000)) < 0
+
+
 # --------------------------------------------------------------- cache write
 
-def test_cache_write_bf16_is_a_scatter_of_bit_patterns():
-    b = W.workload(5, poison=True)
-    kc, vc = oracle.cache_write(BF16, 16, 8, 128, b.k_new, b.v_new, b.slot_mapping, b.k_pool, b.v_pool)
+@pytest.mark.parametrize("fp16", [False, True])
+def test_cache_write_16bit_is_a_scatter_of_bit_patterns(fp16):
+    b = W.workload(5, poison=True, fp16=fp16)
+    kc, vc = oracle.cache_write(F16 if fp16 else BF16, 16, 8, 128, b.k_new, b.v_new, b.slot_mapping,
+                                b.k_pool, b.v_pool)
     ref_k = b.k_pool.view(torch.int16).numpy().view(np.uint16).copy()
     ref_v = b.v_pool.view(torch.int16).numpy().view(np.uint16).copy()
     s = b.slot_mapping.numpy()
@@ -226,7 +243,7 @@ def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation(kv)
 
 # ------------------------------------------------------------ decode attention
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_FP8_E5M2])
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_F16, W.KV_FP8, W.KV_FP8_E5M2])
 @pytest.mark.parametrize("D,Hq,Hkv", [(8, 2, 2), (64, 4, 2), (8, 10, 2), (64, 5, 1)])
 def test_decode_matches_bruteforce_sdpa(kv, D, Hq, Hkv):
     lens = [1, 5, 16, 17, 40]
@@ -377,7 +394,7 @@ def _oracle_prefill(b: W.PagedBatch, pairs=None):
                           b.scale, b.k_scale, b.v_scale, pairs=pairs)
 
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_FP8_E5M2])
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_F16, W.KV_FP8, W.KV_FP8_E5M2])
 def test_prefill_matches_bruteforce_sdpa_with_causal_mask(kv):
     q_lens, ctx = [5, 16, 1, 23], [5, 40, 33, 64]
     b = W.random_prefill(91, q_lens, ctx, 4, 2, 64, kv_dtype=kv, shared_prefix_blocks=1)
