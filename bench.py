@@ -215,8 +215,11 @@ def _first_key(pos: int, window: int, chunk: int) -> int:
 
 
 def _local_config(args) -> dict:
-    """Local-attention settings of the run, for the JSON line's config (none when off)."""
+    """Non-default settings of the run (fp16 cache, local attention), for the
+    JSON line's config (none when off)."""
     d = {}
+    if args.fp16:
+        d["kv_cache"] = "fp16"
     if args.sliding_window:
         d["sliding_window"] = args.sliding_window
     if args.attention_chunk:
@@ -280,12 +283,15 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     B.load(pa_build.build())
 
-    b = W.workload(args.workload, device=dev, poison=False, fp8_format=FP8_FORMATS[args.fp8_format])
-    kv = {W.KV_BF16: B.PA_KV_BF16, W.KV_FP8: B.PA_KV_FP8_E4M3, W.KV_FP8_E5M2: B.PA_KV_FP8_E5M2}[b.kv_dtype]
+    b = W.workload(args.workload, device=dev, poison=False, fp8_format=FP8_FORMATS[args.fp8_format],
+                   fp16=args.fp16)
+    kv = {W.KV_BF16: B.PA_KV_BF16, W.KV_F16: B.PA_KV_F16, W.KV_FP8: B.PA_KV_FP8_E4M3,
+          W.KV_FP8_E5M2: B.PA_KV_FP8_E5M2}[b.kv_dtype]
+    kv8 = kv in (B.PA_KV_FP8_E4M3, B.PA_KV_FP8_E5M2)
     desc = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv,
-                       b.k_scale if kv else 0.0, b.v_scale if kv else 0.0, decode_impl=args.decode_impl,
+                       b.k_scale if kv8 else 0.0, b.v_scale if kv8 else 0.0, decode_impl=args.decode_impl,
                        sliding_window=args.sliding_window, attention_chunk=args.attention_chunk)
-    if kv == B.PA_KV_BF16:
+    if not kv8:
         kc, vc = b.k_pool, b.v_pool
     else:
         kc = torch.empty(tuple(b.k_pool.shape), dtype=torch.uint8, device=dev)
@@ -299,7 +305,8 @@ def run_ours(args):
     wsp = B.decode_workspace(desc, S, maxL, dev)
     out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
     kv_bytes = _decode_kv_bytes(b, args.sliding_window, args.attention_chunk)
-    local = bool(args.sliding_window or args.attention_chunk)
+    # the captured traffic figures are for the default settings only
+    local = bool(args.sliding_window or args.attention_chunk or args.fp16)
     mixed = b.q_prefill is not None
     if mixed:
         pf_out = torch.empty(b.q_prefill.shape, dtype=torch.float32, device=dev)
@@ -485,21 +492,23 @@ def run_ours(args):
                                     "traffic": _traffic("prefill", args.workload, local)}
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget,
-                                                window=args.sliding_window, chunk=args.attention_chunk)
+                                                window=args.sliding_window, chunk=args.attention_chunk,
+                                                fp16=args.fp16)
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def _oracle_sample(n_workload: int, budget_s: float, window: int = 0, chunk: int = 0):
+def _oracle_sample(n_workload: int, budget_s: float, window: int = 0, chunk: int = 0, fp16: bool = False):
     """Run the fp64 oracle over whole sequences of the workload (all heads)
     until ``budget_s`` of CPU time is used; returns (kv_bytes, seconds, n_seqs)."""
     import oracle
     from paged_kv_attention_14_gb300 import workloads as W
 
-    b = W.workload(n_workload, device="cpu", poison=False)
-    if b.kv_dtype != W.KV_BF16:
-        raise RuntimeError("the CPU baseline covers the bf16 workloads")
+    b = W.workload(n_workload, device="cpu", poison=False, fp16=fp16)
+    if b.kv_dtype not in (W.KV_BF16, W.KV_F16):
+        raise RuntimeError("the CPU baseline covers the 16-bit workloads")
+    code = oracle.KV_F16 if fp16 else oracle.KV_BF16
     kc, vc = b.k_pool, b.v_pool
     S = b.context_lens_decode.shape[0]
     done_bytes, t_used, n = 0, 0.0, 0
@@ -508,7 +517,7 @@ def _oracle_sample(n_workload: int, budget_s: float, window: int = 0, chunk: int
         s = order[n % S]
         pairs = [(s, h) for h in range(b.num_q_heads)]
         t0 = time.perf_counter()
-        oracle.decode(oracle.KV_BF16, 16, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
+        oracle.decode(code, 16, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
                       b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs, window=window, chunk=chunk)
         t_used += time.perf_counter() - t0
         L = int(b.context_lens_decode[s])
@@ -517,7 +526,7 @@ def _oracle_sample(n_workload: int, budget_s: float, window: int = 0, chunk: int
     return done_bytes, t_used, n, b.name
 
 
-def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, chunk=0):
+def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, chunk=0, fp16=False):
     """One process of the all-cores oracle run: builds the (seeded) workload,
     then for each phase of ``phases`` seconds runs the oracle over (sequence,
     kv head) units rank, rank + nproc, ... (the g query heads of one kv head,
@@ -529,7 +538,8 @@ def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, 
     import oracle
     from paged_kv_attention_14_gb300 import workloads as W
 
-    b = W.workload(n_workload, device="cpu", poison=False)
+    b = W.workload(n_workload, device="cpu", poison=False, fp16=fp16)
+    code = oracle.KV_F16 if fp16 else oracle.KV_BF16
     S, Hkv = b.context_lens_decode.shape[0], b.num_kv_heads
     g = b.num_q_heads // Hkv
     u = rank % (S * Hkv)
@@ -540,7 +550,7 @@ def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, 
         while time.perf_counter() - t0 < phase_s:
             s, kvh = divmod(u, Hkv)
             pairs = [(s, kvh * g + i) for i in range(g)]
-            oracle.decode(oracle.KV_BF16, 16, Hkv, b.num_q_heads, b.head_dim, b.q_decode, b.k_pool, b.v_pool,
+            oracle.decode(code, 16, Hkv, b.num_q_heads, b.head_dim, b.q_decode, b.k_pool, b.v_pool,
                           b.block_tables_decode, b.context_lens_decode, b.scale, pairs=pairs, window=window,
                           chunk=chunk)
             L = int(b.context_lens_decode[s])
@@ -550,7 +560,8 @@ def _oracle_worker(rank, nproc, n_workload, phases, barrier, results, window=0, 
         results.put((rank, done, time.perf_counter() - t0, n))
 
 
-def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None, window: int = 0, chunk: int = 0):
+def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None, window: int = 0, chunk: int = 0,
+                      fp16: bool = False):
     """The oracle on every host core: ``nproc`` spawned processes (the GPU is
     already in use in this process, so no fork), one thread each.  Returns per
     phase (kv_bytes, wall seconds, sequences), the workload name and nproc."""
@@ -560,7 +571,7 @@ def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None, window:
     ctx = mp.get_context("spawn")
     barrier = ctx.Barrier(nproc)
     results = ctx.Queue()
-    procs = [ctx.Process(target=_oracle_worker, args=(r, nproc, n_workload, list(phases), barrier, results, window, chunk))
+    procs = [ctx.Process(target=_oracle_worker, args=(r, nproc, n_workload, list(phases), barrier, results, window, chunk, fp16))
              for r in range(nproc)]
     for p in procs:
         p.start()
@@ -573,11 +584,11 @@ def _oracle_all_cores(n_workload: int, phases, nproc: int | None = None, window:
     return out, nproc
 
 
-def cpu_baseline(n_workload: int, budget_s: float = 10.0, window: int = 0, chunk: int = 0):
+def cpu_baseline(n_workload: int, budget_s: float = 10.0, window: int = 0, chunk: int = 0, fp16: bool = False):
     """The oracle on all host cores for about ``budget_s`` seconds (the
     reported baseline), plus one thread for ``budget_s / 2``."""
-    nbytes1, secs1, n1, name = _oracle_sample(n_workload, budget_s / 2, window, chunk)
-    (res,), nproc = _oracle_all_cores(n_workload, [budget_s], window=window, chunk=chunk)
+    nbytes1, secs1, n1, name = _oracle_sample(n_workload, budget_s / 2, window, chunk, fp16)
+    (res,), nproc = _oracle_all_cores(n_workload, [budget_s], window=window, chunk=chunk, fp16=fp16)
     nbytes, secs, n = res
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
             "sample": f"{n} (sequence, kv head) units (their g query heads each) of '{name}', fp64 C oracle, "
@@ -597,12 +608,12 @@ def run_reference(args):
     # host cores, sized so that the whole run takes about two minutes
     per_step = max(0.01, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
     phases, nproc = _oracle_all_cores(args.workload, [per_step] * (args.warmup + args.steps),
-                                      window=args.sliding_window, chunk=args.attention_chunk)
+                                      window=args.sliding_window, chunk=args.attention_chunk, fp16=args.fp16)
     timed = phases[args.warmup:]
     nbytes = sum(p[0] for p in timed)
     secs = sum(p[1] for p in timed)
     value = nbytes / secs / 1e9
-    name = W.WORKLOAD_NAMES[args.workload]
+    name = W.WORKLOAD_NAMES[args.workload] + (" (fp16 variant)" if args.fp16 else "")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -624,11 +635,15 @@ def main():
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
                     help="8-bit cache format of workload 4 (same shapes)")
+    ap.add_argument("--fp16", action="store_true",
+                    help="fp16 variant of a bf16 workload (fp16 cache, q and new rows)")
     ap.add_argument("--sliding-window", type=int, default=0, help="sliding-window attention of W keys (0: off)")
     ap.add_argument("--attention-chunk", type=int, default=0, help="chunked-local attention over chunks of C (0: off)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.fp16 and args.workload == 4:
+        ap.error("--fp16 applies to the bf16 workloads (1, 2, 3, 5)")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

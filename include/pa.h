@@ -16,9 +16,11 @@
  *
  * Memory layout (the pages name no layout; this one is the library's choice):
  *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
- *                      bf16, or one E4M3 or E5M2 byte per element for FP8 KV.
- *   q (decode)       : [num_seqs][num_q_heads][head_dim] bf16
- *   q (prefill)      : [total_query_tokens][num_q_heads][head_dim] bf16
+ *                      bf16 or fp16, or one E4M3 or E5M2 byte per element for
+ *                      FP8 KV.
+ *   q (decode)       : [num_seqs][num_q_heads][head_dim] bf16 (fp16 with an
+ *                      fp16 cache)
+ *   q (prefill)      : [total_query_tokens][num_q_heads][head_dim], same type
  *   out              : same shape as q, fp32
  *   lse (optional)   : [rows][num_q_heads] fp32, natural-log log-sum-exp of
  *                      the scaled scores of each output row
@@ -77,7 +79,10 @@ typedef enum {
 typedef enum {
   PA_KV_BF16 = 0,     /* bf16 K/V, bit copies of the written values          */
   PA_KV_FP8_E4M3 = 1, /* OCP E4M3 bytes with per-tensor fp32 scales        */
-  PA_KV_FP8_E5M2 = 2  /* OCP E5M2 bytes with per-tensor fp32 scales        */
+  PA_KV_FP8_E5M2 = 2, /* OCP E5M2 bytes with per-tensor fp32 scales        */
+  PA_KV_F16 = 3       /* fp16 K/V of an fp16 model: q and the written rows
+                         are fp16 too; bit copies ("Block-Paged KV Cache
+                         (FP8/FP16)")                                      */
 } pa_kv_dtype;
 
 /* Which decode kernel pa_decode runs.  0 lets the library choose. */
@@ -90,8 +95,8 @@ typedef enum {
 /* Which prefill kernel pa_prefill_chunk runs.  0 lets the library choose. */
 typedef enum {
   PA_PREFILL_AUTO = 0,
-  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; bf16 and FP8 caches    */
-  PA_PREFILL_TCGEN05 = 2   /* tcgen05 tensor-memory tiles; bf16 caches        */
+  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; every cache type      */
+  PA_PREFILL_TCGEN05 = 2   /* tcgen05 tensor-memory tiles; bf16, fp16 caches  */
 } pa_prefill_impl;
 
 /*
@@ -102,7 +107,7 @@ typedef enum {
  *   num_q_heads  : a multiple of num_kv_heads; group size g = q / kv <= 16.
  *   k_scale, v_scale : FP8 only.  Cached value = stored E4M3 / E5M2 value *
  *                  scale.
- *                  0 means 1.0.  Ignored for bf16.
+ *                  0 means 1.0.  Ignored for bf16 and fp16.
  *   decode_impl  : a pa_decode_impl value.
  *   prefill_impl : a pa_prefill_impl value.
  *   sliding_window, attention_chunk : local attention ("Local-attention KV +
@@ -141,11 +146,12 @@ PA_API const char *pa_last_error(void);
  * Slot-mapped cache write.  For every token i < num_tokens with
  * slot_mapping[i] >= 0, block = slot / block_size and offset = slot %
  * block_size; for every kv head h, the cache row (block, h, offset) receives
- * k[i][h][:] (v likewise).  bf16 KV stores the bits unchanged.  FP8 KV stores
+ * k[i][h][:] (v likewise).  bf16 and fp16 KV store the bits unchanged.  FP8 KV stores
  * e4m3 (or e5m2) of fl32(x) / k_scale, rounded to nearest even, with finite
  * overflow saturating to +-448 (E4M3) or +-57344 (E5M2, where +-inf
  * saturates too), and NaN kept as a NaN code.
- *   k, v : [num_tokens][num_kv_heads][head_dim] bf16, 16-byte aligned.
+ *   k, v : [num_tokens][num_kv_heads][head_dim] bf16 (fp16 for an fp16
+ *          cache), 16-byte aligned.
  * The write of a prefix-cache hit must not target a block shared with another
  * sequence ("Zero-Copy Cache Hits" of "1. Technical Mechanics of the Radix
  * Cache" binds sequences to the same physical pages; writing into one would
@@ -193,7 +199,8 @@ PA_API pa_status pa_decode(const pa_kv_desc *desc, float *out, float *lse, const
  * attends keys [0, position] of its kv head (the chunk's own K/V must have
  * been written by pa_cache_write first).  Blocks shared by several tables
  * (a prefix-cache hit) are only read.
- *   q   : [query_start_loc[num_seqs]][num_q_heads][head_dim] bf16
+ *   q   : [query_start_loc[num_seqs]][num_q_heads][head_dim] bf16 (fp16 for
+ *         an fp16 cache)
  *   out : same shape, fp32; lse (optional) [rows][num_q_heads]
  *   query_start_loc : int32 [num_seqs + 1], non-decreasing, starting at 0,
  *                     q_len <= context_lens[s].

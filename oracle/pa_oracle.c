@@ -94,9 +94,23 @@ double pa_oracle_f16_decode(uint16_t b) {
   return sign ? -v : v;
 }
 
+/* The value of every fp16 code, filled once from pa_oracle_f16_decode. */
+static double f16_value[65536];
+static int f16_value_ready;
+
+static void f16_table_init(void) {
+  if (f16_value_ready) return;
+  for (int c = 0; c < 65536; ++c) f16_value[c] = pa_oracle_f16_decode((uint16_t)c);
+  f16_value_ready = 1;
+}
+
 /* A query or new-row element: fp16 bits with an fp16 cache, bf16 bits otherwise. */
 static double act_to_double(int kv_dtype, uint16_t b) {
-  return kv_dtype == KV_F16 ? pa_oracle_f16_decode(b) : bf16_bits_to_double(b);
+  if (kv_dtype == KV_F16) {
+    f16_table_init();
+    return f16_value[b];
+  }
+  return bf16_bits_to_double(b);
 }
 
 /* ---------------------------------------------------------------- E4M3 */
@@ -225,7 +239,8 @@ static double kv_elem(int kv_dtype, const void *cache, int64_t row_index, int he
   }
   if (kv_dtype == KV_F16) {
     const uint16_t *c = (const uint16_t *)cache;
-    return pa_oracle_f16_decode(c[row_index * head_dim + d]);
+    f16_table_init();
+    return f16_value[c[row_index * head_dim + d]];
   }
   const uint8_t *c = (const uint8_t *)cache;
   if (kv_dtype == KV_FP8_E5M2) {

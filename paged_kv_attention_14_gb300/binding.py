@@ -28,6 +28,7 @@ PA_ERR_CUDA = 4
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
 PA_KV_FP8_E5M2 = 2
+PA_KV_F16 = 3
 
 PA_DECODE_AUTO = 0
 PA_DECODE_SIMT = 1
@@ -147,8 +148,14 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-_CACHE = (torch.bfloat16, torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
+_CACHE = (torch.bfloat16, torch.float16, torch.uint8, torch.float8_e4m3fn, torch.float8_e5m2)
 _BF16 = (torch.bfloat16,)
+_F16 = (torch.float16,)
+
+
+def _act(desc) -> tuple:
+    """Element type of q and of new K/V rows: fp16 with an fp16 cache, else bf16."""
+    return _F16 if desc.kv_dtype == PA_KV_F16 else _BF16
 _F32 = (torch.float32,)
 _I32 = (torch.int32,)
 _I64 = (torch.int64,)
@@ -157,7 +164,7 @@ _I64 = (torch.int64,)
 def pa_cache_write(desc: PaKvDesc, k, v, k_cache, v_cache, slot_mapping, stream=None):
     """Scatter k, v ``[T, Hkv, D]`` bf16 into the caches at ``slot_mapping`` (int64 [T])."""
     T = int(slot_mapping.shape[0])
-    _check(load().pa_cache_write(ctypes.byref(desc), _ptr(k, _BF16, "k"), _ptr(v, _BF16, "v"),
+    _check(load().pa_cache_write(ctypes.byref(desc), _ptr(k, _act(desc), "k"), _ptr(v, _act(desc), "v"),
                                  _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                                  _ptr(slot_mapping, _I64, "slot_mapping"), T, _stream(stream)))
 
@@ -180,7 +187,7 @@ def pa_decode(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_le
     """Decode attention: q ``[S, Hq, D]`` bf16 -> out ``[S, Hq, D]`` fp32 (lse ``[S, Hq]``)."""
     S = int(context_lens.shape[0])
     _check(load().pa_decode(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                            _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                            _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
                             _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                             _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
                             _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
@@ -194,7 +201,7 @@ def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, con
     for callers that cannot allocate device memory where they decode)."""
     S = int(context_lens.shape[0])
     _check(load().pa_decode_static(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
                                    _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                                    _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
                                    _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
@@ -207,7 +214,7 @@ def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, 
     """Causal chunked prefill: q ``[Tq, Hq, D]`` bf16 -> out ``[Tq, Hq, D]`` fp32."""
     S = int(context_lens.shape[0])
     _check(load().pa_prefill_chunk(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _BF16, "q"),
+                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
                                    _ptr(query_start_loc, _I32, "query_start_loc"),
                                    _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                                    _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),

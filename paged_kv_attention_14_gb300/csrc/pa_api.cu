@@ -39,12 +39,14 @@ pa_status check_desc(const pa_kv_desc *d) {
     return fail(PA_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads%s");
   if (d->num_q_heads / d->num_kv_heads > 16)
     return fail(PA_ERR_UNSUPPORTED, "group size num_q_heads / num_kv_heads must be <= 16%s");
-  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_FP8_E4M3 && d->kv_dtype != PA_KV_FP8_E5M2)
-    return fail(PA_ERR_INVALID_ARG, "kv_dtype must be PA_KV_BF16, PA_KV_FP8_E4M3 or PA_KV_FP8_E5M2%s");
+  if (d->kv_dtype != PA_KV_BF16 && d->kv_dtype != PA_KV_FP8_E4M3 && d->kv_dtype != PA_KV_FP8_E5M2 &&
+      d->kv_dtype != PA_KV_F16)
+    return fail(PA_ERR_INVALID_ARG, "kv_dtype must be PA_KV_BF16, PA_KV_F16, PA_KV_FP8_E4M3 or PA_KV_FP8_E5M2%s");
   if (d->num_blocks < 0) return fail(PA_ERR_INVALID_ARG, "num_blocks must be >= 0%s");
   if (d->sliding_window < 0 || d->attention_chunk < 0)
     return fail(PA_ERR_INVALID_ARG, "sliding_window and attention_chunk must be >= 0%s");
-  if (d->kv_dtype != PA_KV_BF16 && (!(d->k_scale >= 0.f) || !(d->v_scale >= 0.f)))
+  const bool kv8 = d->kv_dtype == PA_KV_FP8_E4M3 || d->kv_dtype == PA_KV_FP8_E5M2;
+  if (kv8 && (!(d->k_scale >= 0.f) || !(d->v_scale >= 0.f)))
     return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be >= 0 (0 means 1)%s");
   return PA_OK;
 }

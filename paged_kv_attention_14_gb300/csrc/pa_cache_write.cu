@@ -68,7 +68,7 @@ cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v
   const int64_t blocks = (total + threads - 1) / threads;
   const float ks = d.k_scale == 0.f ? 1.f : d.k_scale;
   const float vs = d.v_scale == 0.f ? 1.f : d.v_scale;
-  if (d.kv_dtype == PA_KV_BF16)
+  if (d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16)  // 16-bit: bit copies
     cache_write_kernel<kKvBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,

@@ -38,8 +38,9 @@ int resolve_impl(const pa_kv_desc &d) {
 // E4M3 kernel (8 consumer warps) is fastest with pairs of heads (2 KB
 // tiles), the bf16 head_dim-64 one with groups of 4.
 int head_group(const pa_kv_desc &d) {
-  if (d.kv_dtype == PA_KV_BF16 && d.head_dim == 128) return 1;
-  if (d.kv_dtype == PA_KV_BF16 && d.num_kv_heads % 4 == 0) return 4;
+  const bool b16 = d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16;
+  if (b16 && d.head_dim == 128) return 1;
+  if (b16 && d.num_kv_heads % 4 == 0) return 4;
   if (d.num_kv_heads % 2 == 0) return 2;
   return 1;
 }
@@ -49,6 +50,7 @@ KernelInfo kernel_for(const pa_kv_desc &d, int impl) {
   if (impl == PA_DECODE_SIMT) return dec::pick_simt(d.head_dim, d.kv_dtype, g);
   const int hg = head_group(d);
   if (d.kv_dtype == PA_KV_BF16) return dec::pick_mma_bf16(d.head_dim, g, hg);
+  if (d.kv_dtype == PA_KV_F16) return dec::pick_mma_f16(d.head_dim, g, hg);
   if (d.kv_dtype == PA_KV_FP8_E5M2) return dec::pick_mma_e5m2(d.head_dim, g, hg);
   return dec::pick_mma_fp8(d.head_dim, g, hg);
 }
@@ -78,12 +80,14 @@ EncodeTiledFn encode_tiled() {
 bool make_cache_map(CUtensorMap *map, const void *base, const pa_kv_desc &d, const KernelInfo &k) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
-  const bool bf = d.kv_dtype == PA_KV_BF16;
+  const bool bf = d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16;  // 2-byte elements
   const int esz = bf ? 2 : 1;
   const cuuint64_t rowb = static_cast<cuuint64_t>(d.head_dim) * esz;
   const cuuint64_t rows = static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * 16;
   const cuuint32_t box_rows = static_cast<cuuint32_t>(k.hg * 16);
-  const CUtensorMapDataType dt = bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType dt = d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                 : bf                      ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUtensorMapSwizzle sw = k.swizzle == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r;
@@ -172,7 +176,7 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.num_q_heads = d.num_q_heads;
   a.g = d.num_q_heads / d.num_kv_heads;
   a.num_groups = plan.num_groups;
-  const bool fp8 = d.kv_dtype != PA_KV_BF16;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   const float ks = (fp8 && d.k_scale != 0.f) ? d.k_scale : 1.f;
   a.qscale = scale * ks * dec::kLog2e;
   a.vscale = (fp8 && d.v_scale != 0.f) ? d.v_scale : 1.f;

@@ -481,29 +481,29 @@ __device__ long long prologue(const DecodeArgs &a, uint64_t *full, uint64_t *emp
 // ============================================================ SIMT consumer
 
 // Which head_dim elements lane j8 (0..7) of an 8-lane token group holds, and
-// how it loads them from a cached row.  bf16 rows: 16-byte chunks j8,
-// j8 + 8, ... (each quarter-warp reads one contiguous 128-byte span).  E4M3
-// rows: one contiguous run of D/8 bytes per lane.
+// how it loads them from a cached row.  2-byte rows (bf16, fp16): 16-byte
+// chunks j8, j8 + 8, ... (each quarter-warp reads one contiguous 128-byte
+// span).  8-bit rows: one contiguous run of D/8 bytes per lane.
 template <int D, int KVT>
 struct RowSlice {
   static constexpr int EPL = D / 8;
   __device__ static __forceinline__ int dim(int j8, int e) {
-    if (KVT == kKvBf16) return ((e >> 3) * 8 + j8) * 8 + (e & 7);
+    if (kv16(KVT)) return ((e >> 3) * 8 + j8) * 8 + (e & 7);
     return j8 * EPL + e;
   }
   __device__ static __forceinline__ void load(const uint8_t *row, int j8, float (&x)[EPL]) {
-    if (KVT == kKvBf16) {
+    if constexpr (kv16(KVT)) {
 #pragma unroll
       for (int c = 0; c < EPL / 8; ++c) {
         const uint4 u = *reinterpret_cast<const uint4 *>(row + (c * 8 + j8) * 16);
-        x[c * 8 + 0] = bf16lo(u.x);
-        x[c * 8 + 1] = bf16hi(u.x);
-        x[c * 8 + 2] = bf16lo(u.y);
-        x[c * 8 + 3] = bf16hi(u.y);
-        x[c * 8 + 4] = bf16lo(u.z);
-        x[c * 8 + 5] = bf16hi(u.z);
-        x[c * 8 + 6] = bf16lo(u.w);
-        x[c * 8 + 7] = bf16hi(u.w);
+        x[c * 8 + 0] = lo16<KVT>(u.x);
+        x[c * 8 + 1] = hi16<KVT>(u.x);
+        x[c * 8 + 2] = lo16<KVT>(u.y);
+        x[c * 8 + 3] = hi16<KVT>(u.y);
+        x[c * 8 + 4] = lo16<KVT>(u.z);
+        x[c * 8 + 5] = hi16<KVT>(u.z);
+        x[c * 8 + 6] = lo16<KVT>(u.w);
+        x[c * 8 + 7] = hi16<KVT>(u.w);
       }
     } else if (EPL == 16) {
       const uint4 u = *reinterpret_cast<const uint4 *>(row + j8 * 16);
@@ -533,7 +533,7 @@ struct SimtCfg {
   static constexpr int BPS = BPS_;
   static constexpr int NS = NS_;
   static constexpr int NC = kConsumerWarps;
-  static constexpr int ESZ = (KVT == kKvBf16) ? 2 : 1;
+  static constexpr int ESZ = kv16(KVT) ? 2 : 1;
   static constexpr int ROWB = D * ESZ;
   static constexpr int TILEB = 16 * ROWB;       // one (block, kv head) tile
   static constexpr int KVB = BPS * TILEB;       // K (or V) bytes of a stage
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
         l[j] = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
-          q[j][e] = j < a.g ? __uint_as_float(static_cast<uint32_t>(Qs[j * D + RS::dim(j8, e)]) << 16) * a.qscale : 0.f;
+          q[j][e] = j < a.g ? lo16<KVT == kKvF16 ? kKvF16 : kKvBf16>(Qs[j * D + RS::dim(j8, e)]) * a.qscale : 0.f;
           o[j][e] = 0.f;
         }
       }
@@ -768,7 +768,7 @@ struct MmaCfg {
   static constexpr int NS = NS_;
   static constexpr int NC = NC_;  // consumer warps; warp NC produces, NC + 1 finishes
   static constexpr int BPS = NC / HG;        // blocks per stage: one (block, head) tile per consumer warp
-  static constexpr int ESZ = (KVT == kKvBf16) ? 2 : 1;
+  static constexpr int ESZ = kv16(KVT) ? 2 : 1;
   static constexpr int ROWB = D * ESZ;
   static constexpr int TILEB = 16 * ROWB;    // one (block, kv head)
   static constexpr int GTILE = HG * TILEB;   // one block of a head group: one copy
@@ -1084,7 +1084,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
         const bool hv = n < a.g;
 #pragma unroll
         for (int ks = 0; ks < MT; ++ks) {
-          if (KVT == kKvBf16) {
+          if constexpr (kv16(KVT)) {
             // k = 2c, 2c+1 <-> d = 16ks + 2c + {0,1};  k + 8 <-> d + 8
             const int d0 = ks * 16 + 2 * c;
             qb[ks][nn][0] = hv ? *reinterpret_cast<const uint32_t *>(Qs + n * D + d0) : 0u;
@@ -1118,7 +1118,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
       for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sa[nn][e] = sb[nn][e] = 0.f;
-      if (KVT == kKvBf16) {
+      if constexpr (kv16(KVT)) {
 #pragma unroll
         for (int ks = 0; ks < MT; ++ks) {
           uint32_t a0, a1, a2, a3;
@@ -1126,9 +1126,9 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
 #pragma unroll
           for (int nn = 0; nn < NN; ++nn) {
             if (ks & 1)
-              mma_bf16_16816(sb[nn], a0, a1, a2, a3, qb[ks][nn][0], qb[ks][nn][1]);
+              mma16_16816<KVT>(sb[nn], a0, a1, a2, a3, qb[ks][nn][0], qb[ks][nn][1]);
             else
-              mma_bf16_16816(sa[nn], a0, a1, a2, a3, qb[ks][nn][0], qb[ks][nn][1]);
+              mma16_16816<KVT>(sa[nn], a0, a1, a2, a3, qb[ks][nn][0], qb[ks][nn][1]);
           }
         }
       } else {
@@ -1184,12 +1184,13 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
           oacc[mt][nn][1] *= k1;
           oacc[mt][nn][3] *= k1;
         }
-        if (KVT == kKvBf16) {
-          const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        if constexpr (kv16(KVT)) {
+          // P as a hi + lo pair of the cache's 16-bit type
+          const uint32_t h01 = pack16x2<KVT>(p0, p1), h23 = pack16x2<KVT>(p2, p3);
           pb[nn][0] = movmatrix_trans(h01);
           pb[nn][1] = movmatrix_trans(h23);
-          pbl[nn][0] = movmatrix_trans(pack_bf16x2(p0 - bf16lo(h01), p1 - bf16hi(h01)));
-          pbl[nn][1] = movmatrix_trans(pack_bf16x2(p2 - bf16lo(h23), p3 - bf16hi(h23)));
+          pbl[nn][0] = movmatrix_trans(pack16x2<KVT>(p0 - lo16<KVT>(h01), p1 - hi16<KVT>(h01)));
+          pbl[nn][1] = movmatrix_trans(pack16x2<KVT>(p2 - lo16<KVT>(h23), p3 - hi16<KVT>(h23)));
         } else {
           pb[nn][0] = movmatrix_trans(pack_f16x2(p0, p1));
           pb[nn][1] = movmatrix_trans(pack_f16x2(p2, p3));
@@ -1202,7 +1203,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
       auto in = [&](int t) { return t < vt && t >= vl; };
       const uint32_t mk_lo = (in(2 * c) ? 0x0000ffffu : 0u) | (in(2 * c + 1) ? 0xffff0000u : 0u);
       const uint32_t mk_hi = (in(2 * c + 8) ? 0x0000ffffu : 0u) | (in(2 * c + 9) ? 0xffff0000u : 0u);
-      if (KVT == kKvBf16) {
+      if constexpr (kv16(KVT)) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t a0, a1, a2, a3;
@@ -1213,8 +1214,8 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
           a3 &= mk_hi;
 #pragma unroll
           for (int nn = 0; nn < NN; ++nn) {
-            mma_bf16_16816(oacc[mt][nn], a0, a1, a2, a3, pb[nn][0], pb[nn][1]);
-            mma_bf16_16816(oacc[mt][nn], a0, a1, a2, a3, pbl[nn][0], pbl[nn][1]);
+            mma16_16816<KVT>(oacc[mt][nn], a0, a1, a2, a3, pb[nn][0], pb[nn][1]);
+            mma16_16816<KVT>(oacc[mt][nn], a0, a1, a2, a3, pbl[nn][0], pbl[nn][1]);
           }
         }
       } else {
@@ -1277,8 +1278,8 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
         for (int mt = 0; mt < MT; ++mt) {
           // bf16: rows r, r+8 of m-tile mt are d = 16mt + r, 16mt + 8 + r;
           // E4M3: d = 16mt + 2r, 16mt + 2r + 1
-          const int dlo = (KVT == kKvBf16) ? mt * 16 + r : mt * 16 + 2 * r;
-          const int dhi = (KVT == kKvBf16) ? dlo + 8 : dlo + 1;
+          const int dlo = kv16(KVT) ? mt * 16 + r : mt * 16 + 2 * r;
+          const int dhi = kv16(KVT) ? dlo + 8 : dlo + 1;
           rw[h0 * C::RSTR + dlo] = oacc[mt][nn][0];
           rw[(h0 + 1) * C::RSTR + dlo] = oacc[mt][nn][1];
           rw[h0 * C::RSTR + dhi] = oacc[mt][nn][2];
@@ -1327,7 +1328,7 @@ struct KernelInfo {
 // SIMT: stages of about 32 KB, three of them, two CTAs per SM
 template <int D, int KVT, int GP>
 KernelInfo simt_info() {
-  constexpr int ESZ = KVT == kKvBf16 ? 2 : 1;
+  constexpr int ESZ = kv16(KVT) ? 2 : 1;
   constexpr int BPS = (D * ESZ >= 256) ? 4 : 8;
   using Cfg = SimtCfg<D, KVT, GP, BPS, 3>;
   KernelInfo k;
@@ -1347,7 +1348,7 @@ KernelInfo simt_info() {
 // 67% -> 89% of the HBM copy rate).
 template <int D, int KVT, int GQ, int HG, int NCW = kConsumerWarps>
 KernelInfo mma_info() {
-  constexpr int ESZ = KVT == kKvBf16 ? 2 : 1;
+  constexpr int ESZ = kv16(KVT) ? 2 : 1;
   constexpr int STAGEB = 2 * NCW * 16 * D * ESZ + ((HG * GQ * D * 2 + 1023) / 1024) * 1024;
   constexpr int RED = 2 * NCW * GQ * (D + 4) * 4;
   constexpr int FIT = (225280 - 2048 - RED) / STAGEB;
@@ -1390,6 +1391,7 @@ KernelInfo fp8_mma_for(int gq, int hg) {
 // Defined in the translation units that instantiate the kernels.
 KernelInfo pick_simt(int head_dim, int kv_dtype, int g);
 KernelInfo pick_mma_bf16(int head_dim, int gq, int hg);
+KernelInfo pick_mma_f16(int head_dim, int gq, int hg);
 KernelInfo pick_mma_fp8(int head_dim, int gq, int hg);   // E4M3
 KernelInfo pick_mma_e5m2(int head_dim, int gq, int hg);
 

@@ -16,6 +16,10 @@ namespace pa {
 constexpr int kKvBf16 = 0;
 constexpr int kKvFp8 = 1;   // E4M3
 constexpr int kKvE5M2 = 2;  // E5M2
+constexpr int kKvF16 = 3;   // fp16 (an fp16 model: q and new rows are fp16 too)
+
+// 2-byte cache elements (bf16 or fp16) versus 1-byte ones (E4M3, E5M2).
+constexpr bool kv16(int kvt) { return kvt == kKvBf16 || kvt == kKvF16; }
 
 // First key a query at position pos attends under local attention: a sliding
 // window of `window` keys ending at pos starts at pos - window + 1;
@@ -246,6 +250,28 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
+// fp16 halves of a packed pair to fp32 (exact).
+__device__ __forceinline__ float f16lo(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu))); }
+__device__ __forceinline__ float f16hi(uint32_t u) { return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16))); }
+
+// The 16-bit element type of a 2-byte cache (bf16, or fp16 for kKvF16): its
+// pair packing (round to nearest even) and unpacking.
+template <int KVT>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (KVT == kKvF16) return pack_f16x2(lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+template <int KVT>
+__device__ __forceinline__ float lo16(uint32_t u) {
+  if constexpr (KVT == kKvF16) return f16lo(u);
+  return bf16lo(u);
+}
+template <int KVT>
+__device__ __forceinline__ float hi16(uint32_t u) {
+  if constexpr (KVT == kKvF16) return f16hi(u);
+  return bf16hi(u);
+}
+
 // Two fp32 values to E4M3 bytes (low byte = lo), round to nearest even,
 // finite overflow saturates to +-448, NaN stays NaN.
 __device__ __forceinline__ uint16_t pack_e4m3x2_satfinite(float lo, float hi) {
@@ -386,6 +412,16 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The m16n8k16 MMA of a 2-byte cache's element type.
+template <int KVT>
+__device__ __forceinline__ void mma16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+  if constexpr (KVT == kKvF16)
+    mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
+  else
+    mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+}
+
 // ---------------------------------------------------- tcgen05 / TMEM (sm_100+)
 
 // Allocates `ncols` TMEM columns (a power of two >= 32) for this CTA; one
@@ -413,11 +449,13 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D,
-// A and B K-major unless transposed (MN-major), shape M x N.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (fp16 with
+// f16 = true; A and B always share the type), fp32 D, A and B K-major unless
+// transposed (MN-major), shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                       bool f16 = false) {
+  return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // D[tmem] (+)= A[smem] * B[smem], issued by one thread.

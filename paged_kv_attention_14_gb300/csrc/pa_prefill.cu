@@ -58,7 +58,10 @@ struct PrefillCfg {
   static constexpr int CH = D / 8;              // 16-byte bf16 chunks per row
   static constexpr int TILE = KT * D * 2;       // bf16 tile bytes
   static constexpr int RAW = KT * D;            // E4M3 tile bytes
-  static constexpr size_t SMEM = (KVT == kKvBf16) ? size_t(4) * TILE : size_t(2) * TILE + size_t(4) * RAW;
+  static constexpr size_t SMEM = kv16(KVT) ? size_t(4) * TILE : size_t(2) * TILE + size_t(4) * RAW;
+  // element type of the MMAs: fp16 for an fp16 cache; bf16 for bf16 and for
+  // the 8-bit caches, whose tiles are decoded to bf16 in shared memory
+  static constexpr int MT16 = KVT == kKvF16 ? kKvF16 : kKvBf16;
 };
 
 // byte offset of 16-byte chunk `ch` of row `key` in a swizzled bf16 tile
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
 
   uint8_t *kt_s[2], *vt_s[2];
   uint8_t *kraw[2], *vraw[2];
-  if (KVT == kKvBf16) {
+  if (kv16(KVT)) {
     kt_s[0] = smem;
     vt_s[0] = smem + C::TILE;
     kt_s[1] = smem + 2 * C::TILE;
@@ -112,7 +115,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
 
   // gather one 64-key tile (zero-filled outside [kv_lo, kv_end)) into buffer `b`
   auto load_tile = [&](int kt, int b) {
-    if (KVT == kKvBf16) {
+    if (kv16(KVT)) {
       for (int i = tid; i < C::KT * C::CH; i += C::NT) {
         const int key = i / C::CH;
         const int ch = i - key * C::CH;
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
   for (int kt = kt0; kt < n_tiles; ++kt) {
-    const int b = (KVT == kKvBf16) ? (kt & 1) : 0;
+    const int b = kv16(KVT) ? (kt & 1) : 0;
     if (kt + 1 < n_tiles) {
       load_tile(kt + 1, (kt + 1) & 1);
       cp_async_wait<1>();
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
       cp_async_wait<0>();
     }
     __syncthreads();
-    if (KVT != kKvBf16) {
+    if (!kv16(KVT)) {
       convert_tile(kt & 1);
       __syncthreads();
     }
@@ -236,8 +239,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
           const int ch = ks * 2 + (mat & 1);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4(b0, b1, b2, b3, ks_base + swz<D>(key, ch));
-          mma_bf16_16816(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma_bf16_16816(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          mma16_16816<C::MT16>(sacc[2 * np], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+          mma16_16816<C::MT16>(sacc[2 * np + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
         }
       }
     }
@@ -282,8 +285,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
       oacc[n][2] *= corr_hi;
       oacc[n][3] *= corr_hi;
     }
-    // P as bf16 hi + lo parts: p = hi + lo to about 2^-17 relative, so the
-    // PV product keeps close to fp32 accuracy on bf16 tensor cores
+    // P as hi + lo parts of the MMA type: p = hi + lo to about 2^-17 relative
+    // (bf16; closer for fp16), so PV keeps close to fp32 accuracy
     uint32_t ph[4][4], pl[4][4];
 #pragma unroll
     for (int n = 0; n < 8; ++n) {
@@ -295,12 +298,12 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
       l_hi += p2 + p3;
       const int kk = n >> 1;
       const int i0 = (n & 1) ? 2 : 0;
-      const uint32_t h01 = pack_bf16x2(p0, p1);
-      const uint32_t h23 = pack_bf16x2(p2, p3);
+      const uint32_t h01 = pack16x2<C::MT16>(p0, p1);
+      const uint32_t h23 = pack16x2<C::MT16>(p2, p3);
       ph[kk][i0] = h01;
       ph[kk][i0 + 1] = h23;
-      pl[kk][i0] = pack_bf16x2(p0 - bf16lo(h01), p1 - bf16hi(h01));
-      pl[kk][i0 + 1] = pack_bf16x2(p2 - bf16lo(h23), p3 - bf16hi(h23));
+      pl[kk][i0] = pack16x2<C::MT16>(p0 - lo16<C::MT16>(h01), p1 - hi16<C::MT16>(h01));
+      pl[kk][i0 + 1] = pack16x2<C::MT16>(p2 - lo16<C::MT16>(h23), p3 - hi16<C::MT16>(h23));
     }
     // O += P V
     {
@@ -314,10 +317,10 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
           const int ch = np * 2 + (mat >> 1);
           uint32_t b0, b1, b2, b3;
           ldmatrix_x4_trans(b0, b1, b2, b3, vs_base + swz<D>(key, ch));
-          mma_bf16_16816(oacc[2 * np], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b0, b1);
-          mma_bf16_16816(oacc[2 * np + 1], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b2, b3);
-          mma_bf16_16816(oacc[2 * np], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b0, b1);
-          mma_bf16_16816(oacc[2 * np + 1], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b2, b3);
+          mma16_16816<C::MT16>(oacc[2 * np], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b0, b1);
+          mma16_16816<C::MT16>(oacc[2 * np + 1], ph[kk][0], ph[kk][1], ph[kk][2], ph[kk][3], b2, b3);
+          mma16_16816<C::MT16>(oacc[2 * np], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b0, b1);
+          mma16_16816<C::MT16>(oacc[2 * np + 1], pl[kk][0], pl[kk][1], pl[kk][2], pl[kk][3], b2, b3);
         }
       }
     }
@@ -368,8 +371,8 @@ pa_status check_prefill(const pa_kv_desc &d, const char **why) {
     *why = "prefill_impl must be PA_PREFILL_AUTO, PA_PREFILL_MMA_SYNC or PA_PREFILL_TCGEN05";
     return PA_ERR_INVALID_ARG;
   }
-  if (d.prefill_impl == PA_PREFILL_TCGEN05 && d.kv_dtype != PA_KV_BF16) {
-    *why = "the tcgen05 prefill kernel takes bf16 caches";
+  if (d.prefill_impl == PA_PREFILL_TCGEN05 && d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_F16) {
+    *why = "the tcgen05 prefill kernel takes bf16 and fp16 caches";
     return PA_ERR_UNSUPPORTED;
   }
   return PA_OK;
@@ -380,7 +383,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            const void *v_cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
-  const bool fp8 = d.kv_dtype != PA_KV_BF16;
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
   if (impl == PA_PREFILL_TCGEN05)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
@@ -410,6 +413,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   if (d.head_dim == 128) {
     fn = d.kv_dtype == PA_KV_FP8_E5M2 ? prefill_fn<128, kKvE5M2>()
          : fp8                         ? prefill_fn<128, kKvFp8>()
+         : d.kv_dtype == PA_KV_F16     ? prefill_fn<128, kKvF16>()
                                        : prefill_fn<128, kKvBf16>();
     smem = d.kv_dtype == PA_KV_FP8_E5M2 ? PrefillCfg<128, kKvE5M2, kPrefillWarps>::SMEM
            : fp8                         ? PrefillCfg<128, kKvFp8, kPrefillWarps>::SMEM
@@ -417,6 +421,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   } else {
     fn = d.kv_dtype == PA_KV_FP8_E5M2 ? prefill_fn<64, kKvE5M2>()
          : fp8                         ? prefill_fn<64, kKvFp8>()
+         : d.kv_dtype == PA_KV_F16     ? prefill_fn<64, kKvF16>()
                                        : prefill_fn<64, kKvBf16>();
     smem = d.kv_dtype == PA_KV_FP8_E5M2 ? PrefillCfg<64, kKvE5M2, kPrefillWarps>::SMEM
            : fp8                         ? PrefillCfg<64, kKvFp8, kPrefillWarps>::SMEM

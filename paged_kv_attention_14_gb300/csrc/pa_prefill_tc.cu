@@ -1,5 +1,6 @@
 // pa_prefill_tc.cu -- causal chunked-prefill attention on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory), bf16 KV.
+// tensor cores (tcgen05.mma, accumulators in tensor memory), bf16 or fp16
+// KV (the MMAs, and the P pair below, take the cache's 16-bit type).
 //
 // What it computes is the same as pa_prefill.cu: sequence s brings q_len
 // new queries (a "chunked prefill" chunk, vllm.cpp implementation notes,
@@ -21,8 +22,9 @@
 //  * Warp 0 (one thread) issues the MMAs.  S_t = Q_t K^T (M 128, N 128 keys,
 //    K 16 x head_dim/16; both operands in shared memory) lands in tile t's
 //    128 TMEM columns.  The softmax overwrites those columns with P_t as a
-//    bf16 hi + lo pair (each 32-key chunk's pair in that chunk's columns) (P = hi + lo to ~2^-17 relative, so the bf16 tensor
-//    core product keeps near-fp32 accuracy), and O_t += P_t V (M 128,
+//    hi + lo pair of the cache's 16-bit type (each 32-key chunk's pair in
+//    that chunk's columns; P = hi + lo to ~2^-17 relative with bf16, so the
+//    tensor core product keeps near-fp32 accuracy), and O_t += P_t V (M 128,
 //    N head_dim, K 16 x 8, twice) takes P_t straight from tensor memory
 //    as the A operand and V MN-major from shared memory.  Order per KV tile
 //    j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1); one commit after each QK
@@ -124,7 +126,7 @@ static __device__ unsigned long long g_pf_trace[4096][16];
 #define PF_TRACE(...)
 #endif
 
-template <int D>
+template <int D, int KVT>
 struct Cfg {
   static constexpr int HALVES = D / 64;          // 128-byte column halves of a row
   static constexpr int QHALF = MT * 128;         // bytes of one half of one Q tile
@@ -145,8 +147,8 @@ struct Cfg {
   static constexpr uint32_t O_COL = NQT * KT;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(NQT * (KT + D) <= TMEM_COLS, "TMEM columns");
-  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false);
-  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true);
+  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false, KVT == kKvF16);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true, KVT == kKvF16);
   // bytes landed per 16-token block of K (or of V), all halves
   static constexpr uint32_t BLOCK_BYTES = HALVES * 16u * 128u;
 };
@@ -164,9 +166,9 @@ enum Bar {
 };
 static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
-template <int D>
+template <int D, int KVT>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ Args a) {
-  using C = Cfg<D>;
+  using C = Cfg<D, KVT>;
   // launched as a programmatic dependent of the preceding kernel (typically
   // the cache write): nothing is read before its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -499,10 +501,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               const uint32_t h = __float_as_uint(pv[e]), w = __float_as_uint(pv[16 + e]);
-              const float p0 = (bf16lo(h) + bf16lo(w)) * corr;
-              const float p1 = (bf16hi(h) + bf16hi(w)) * corr;
-              hi[e] = pack_bf16x2(p0, p1);
-              lo[e] = pack_bf16x2(p0 - bf16lo(hi[e]), p1 - bf16hi(hi[e]));
+              const float p0 = (lo16<KVT>(h) + lo16<KVT>(w)) * corr;
+              const float p1 = (hi16<KVT>(h) + hi16<KVT>(w)) * corr;
+              hi[e] = pack16x2<KVT>(p0, p1);
+              lo[e] = pack16x2<KVT>(p0 - lo16<KVT>(hi[e]), p1 - hi16<KVT>(hi[e]));
             }
             tmem_st16_async(trow + s_col + cp * 32, hi);
             tmem_st16_async(trow + s_col + cp * 32 + 16, lo);
@@ -525,9 +527,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           const float p1 = ex2_approx(x.y);
           const uint64_t pp = f2_pack(p0, p1);
           lsum[e & 1] = f2_add(lsum[e & 1], pp);
-          hi[e] = pack_bf16x2(p0, p1);
-          const float2 d = f2_unpack(f2_sub(pp, f2_pack(bf16lo(hi[e]), bf16hi(hi[e]))));
-          lo[e] = pack_bf16x2(d.x, d.y);
+          hi[e] = pack16x2<KVT>(p0, p1);
+          const float2 d = f2_unpack(f2_sub(pp, f2_pack(lo16<KVT>(hi[e]), hi16<KVT>(hi[e]))));
+          lo[e] = pack16x2<KVT>(d.x, d.y);
         }
         {
           const float2 l2 = f2_unpack(f2_add(lsum[0], lsum[1]));
@@ -601,6 +603,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
 template <int D>
 bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
+  const CUtensorMapDataType dt = d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -618,12 +622,12 @@ bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
   const cuuint32_t box[2] = {64, 16};
   const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+  return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int KVT>
 cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, const int32_t *query_start_loc,
                    const void *k_cache, const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
                    const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len, float scale,
@@ -647,8 +651,8 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   a.chunk = d.attention_chunk;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
-  auto fn = &prefill_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_LAUNCH);
+  auto fn = &prefill_tc_kernel<D, KVT>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, KVT>::SMEM_LAUNCH);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -656,7 +660,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs);
   cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<D>::SMEM_LAUNCH;
+  cfg.dynamicSmemBytes = Cfg<D, KVT>::SMEM_LAUNCH;
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
@@ -681,11 +685,16 @@ cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                               int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
+  const bool f16 = d.kv_dtype == PA_KV_F16;
   if (d.head_dim == 128)
-    return pftc::launch<128>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                             context_lens, num_seqs, max_q_len, scale, stream);
-  return pftc::launch<64>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                          context_lens, num_seqs, max_q_len, scale, stream);
+    return f16 ? pftc::launch<128, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                           max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream)
+               : pftc::launch<128, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream);
+  return f16 ? pftc::launch<64, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                        max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream)
+             : pftc::launch<64, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                         max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream);
 }
 
 }  // namespace pa

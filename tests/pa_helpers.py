@@ -12,13 +12,16 @@ import oracle
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
 
-#: max-abs tolerance of fp32 outputs against the fp64 oracle (bf16 KV, FP8 KV)
-TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
+#: max-abs tolerance of fp32 outputs against the fp64 oracle (16-bit KV: 2e-3,
+#: FP8 KV: 2e-2; the fp16 cache takes the bf16 bound, its type being finer)
+TOL = {W.KV_BF16: 2e-3, W.KV_F16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
 #: tolerance of the natural-log log-sum-exp outputs
-LSE_TOL = {W.KV_BF16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
+LSE_TOL = {W.KV_BF16: 2e-3, W.KV_F16: 2e-3, W.KV_FP8: 2e-2, W.KV_FP8_E5M2: 2e-2}
 #: generator cache type -> (library code, oracle code)
-_CODES = {W.KV_BF16: (B.PA_KV_BF16, oracle.KV_BF16), W.KV_FP8: (B.PA_KV_FP8_E4M3, oracle.KV_FP8_E4M3),
-          W.KV_FP8_E5M2: (B.PA_KV_FP8_E5M2, oracle.KV_FP8_E5M2)}
+_CODES = {W.KV_BF16: (B.PA_KV_BF16, oracle.KV_BF16), W.KV_F16: (B.PA_KV_F16, oracle.KV_F16),
+          W.KV_FP8: (B.PA_KV_FP8_E4M3, oracle.KV_FP8_E4M3), W.KV_FP8_E5M2: (B.PA_KV_FP8_E5M2, oracle.KV_FP8_E5M2)}
+#: cache types stored as 16-bit values (the pool itself is the cache)
+KV16 = (W.KV_BF16, W.KV_F16)
 
 
 def kv_code(b: W.PagedBatch) -> int:
@@ -28,15 +31,15 @@ def kv_code(b: W.PagedBatch) -> int:
 def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO,
             prefill_impl: int = B.PA_PREFILL_AUTO, window: int = 0, chunk: int = 0) -> B.PaKvDesc:
     return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
-                       b.k_scale if b.kv_dtype != W.KV_BF16 else 0.0,
-                       b.v_scale if b.kv_dtype != W.KV_BF16 else 0.0, decode_impl=decode_impl,
+                       b.k_scale if b.kv_dtype not in KV16 else 0.0,
+                       b.v_scale if b.kv_dtype not in KV16 else 0.0, decode_impl=decode_impl,
                        prefill_impl=prefill_impl, sliding_window=window, attention_chunk=chunk)
 
 
 def gpu_caches(b: W.PagedBatch):
-    """The caches as the CUDA path holds them: the bf16 pool itself, or the
-    8-bit pool written by the library's own cache write."""
-    if b.kv_dtype == W.KV_BF16:
+    """The caches as the CUDA path holds them: the bf16 / fp16 pool itself, or
+    the 8-bit pool written by the library's own cache write."""
+    if b.kv_dtype in KV16:
         return b.k_pool, b.v_pool
     k, v, slots = b.pool_tokens_as_rows()
     kc = torch.zeros(tuple(b.k_pool.shape), dtype=torch.uint8, device=b.k_pool.device)
@@ -46,10 +49,10 @@ def gpu_caches(b: W.PagedBatch):
 
 
 def oracle_caches(b: W.PagedBatch):
-    """The caches as the oracle sees them (CPU numpy): the bf16 pool, or the
-    oracle's own 8-bit encoding of it."""
-    if b.kv_dtype == W.KV_BF16:
-        return oracle.KV_BF16, b.k_pool.cpu(), b.v_pool.cpu()
+    """The caches as the oracle sees them (CPU numpy): the bf16 / fp16 pool, or
+    the oracle's own 8-bit encoding of it."""
+    if b.kv_dtype in KV16:
+        return _CODES[b.kv_dtype][1], b.k_pool.cpu(), b.v_pool.cpu()
     code = _CODES[b.kv_dtype][1]
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)

@@ -114,6 +114,15 @@ def test_fp8_scales_must_be_non_negative(lib):
     assert lib.pa_cache_write(ctypes.byref(d), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 4, None) == B.PA_ERR_INVALID_ARG
 
 
+def test_fp16_cache_is_accepted_and_ignores_scales(lib):
+    # 16-bit caches take no scales: a negative one is not an error there
+    for kv in (B.PA_KV_F16, B.PA_KV_BF16):
+        d = _desc(kv_dtype=kv, k_scale=-1.0, v_scale=-2.0)
+        assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK, B.last_error()
+    d = _desc(kv_dtype=B.PA_KV_F16 + 1)
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+
+
 def test_decode_argument_errors(lib):
     d = _desc()
     ok_ptrs = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000)

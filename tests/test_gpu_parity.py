@@ -1,7 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle.
 
 Bars: cache writes and block indexing bit-exact; fp32 attention outputs within
-max-abs 2e-3 of the oracle for bf16 KV and 2e-2 for E4M3 / E5M2 KV.  Every input is
+max-abs 2e-3 of the oracle for bf16 / fp16 KV and 2e-2 for E4M3 / E5M2 KV.  Every input is
 seeded and synthetic; pool slots that no sequence may read hold NaN, so a
 stray read shows up as a non-finite output.
 """
@@ -30,15 +30,19 @@ def _lib():
 # ------------------------------------------------------------------ cache write
 
 def _bits(t):
-    return t.view(torch.int16).cpu().numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
 
 
-def test_cache_write_bf16_bit_exact_on_mixed_step():
-    b = W.workload(5, device=DEV, poison=True)
+@pytest.mark.parametrize("fp16", [False, True])
+def test_cache_write_16bit_bit_exact_on_mixed_step(fp16):
+    b = W.workload(5, device=DEV, poison=True, fp16=fp16)
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     B.pa_cache_write(desc_of(b), b.k_new, b.v_new, kc, vc, b.slot_mapping)
     torch.cuda.synchronize()
-    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, b.num_kv_heads, b.head_dim, b.k_new.cpu(), b.v_new.cpu(),
+    ok, ov = oracle.cache_write(oracle.KV_F16 if fp16 else oracle.KV_BF16, 16, b.num_kv_heads, b.head_dim,
+                                b.k_new.cpu(), b.v_new.cpu(),
                                 b.slot_mapping.cpu(), b.k_pool.cpu(), b.v_pool.cpu())
     assert np.array_equal(_bits(kc), ok) and np.array_equal(_bits(vc), ov)
 
@@ -117,9 +121,9 @@ IMPLS = [B.PA_DECODE_SIMT, B.PA_DECODE_MMA]
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("n", [1, 2, 3])
-def test_decode_matches_oracle_on_workload(n, impl):
-    b = W.workload(n, device=DEV, poison=True)
+@pytest.mark.parametrize("n,fp16", [(1, False), (2, False), (3, False), (1, True), (2, True)])
+def test_decode_matches_oracle_on_workload(n, fp16, impl):
+    b = W.workload(n, device=DEV, poison=True, fp16=fp16)
     _check_decode(b, impl=impl)
 
 
@@ -161,6 +165,11 @@ CASES = [
     (128, 8, 2, W.KV_FP8_E5M2, [1, 15, 17, 1000, 1600]),
     (128, 40, 8, W.KV_FP8_E5M2, [1, 100, 1025]),
     (128, 16, 1, W.KV_FP8_E5M2, [64, 65]),
+    (64, 4, 2, W.KV_F16, [1, 7, 16, 33, 250]),
+    (128, 8, 2, W.KV_F16, [1, 15, 16, 17, 100, 1000, 2049]),
+    (128, 32, 8, W.KV_F16, [1, 100, 1025]),
+    (128, 16, 1, W.KV_F16, [64, 65, 700]),
+    (64, 12, 1, W.KV_F16, [3, 77]),
 ]
 
 
@@ -189,9 +198,10 @@ def test_simt_and_mma_decode_agree():
     assert (l1 - l2).abs().max().item() < 1e-3
 
 
+@pytest.mark.parametrize("fp16", [False, True])
 @pytest.mark.parametrize("impl", IMPLS)
-def test_decode_context_length_one_returns_v_bit_exactly(impl):
-    b = W.workload(1, device=DEV, poison=True)
+def test_decode_context_length_one_returns_v_bit_exactly(impl, fp16):
+    b = W.workload(1, device=DEV, poison=True, fp16=fp16)
     out, _ = gpu_decode(b, decode_impl=impl)
     blk = int(b.block_tables_decode[0, 0])
     for h in range(4):
@@ -312,6 +322,10 @@ PREFILL_CASES = [
     (128, 8, 2, W.KV_FP8, [90, 20], [300, 20], 1),
     (64, 4, 2, W.KV_FP8_E5M2, [5, 16, 1, 23], [5, 40, 33, 64], 1),
     (128, 8, 2, W.KV_FP8_E5M2, [90, 20], [300, 20], 1),
+    (64, 4, 2, W.KV_F16, [5, 16, 1, 23], [5, 40, 33, 64], 1),
+    (128, 32, 8, W.KV_F16, [100, 37], [300, 37], 0),
+    (128, 8, 2, W.KV_F16, [200, 64, 1], [530, 64, 129], 2),
+    (128, 10, 2, W.KV_F16, [70, 3], [150, 90], 0),
 ]
 PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
 
@@ -319,8 +333,8 @@ PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("D,Hq,Hkv,kv,q_lens,ctx,shared", PREFILL_CASES)
 def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared, impl):
-    if impl == B.PA_PREFILL_TCGEN05 and kv != W.KV_BF16:
-        pytest.skip("the tcgen05 prefill kernel takes bf16 caches")
+    if impl == B.PA_PREFILL_TCGEN05 and kv not in (W.KV_BF16, W.KV_F16):
+        pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
     b = W.random_prefill(200 + D + Hq + len(q_lens), q_lens, ctx, Hq, Hkv, D, kv_dtype=kv, device=DEV,
                          poison=True, shared_prefix_blocks=shared)
     out, lse = gpu_prefill(b, prefill_impl=impl)
@@ -329,23 +343,27 @@ def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared, impl):
     assert_close(lse, l_ref, LSE_TOL[kv], "lse")
 
 
+@pytest.mark.parametrize("fp16", [False, True])
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
-def test_mixed_step_write_then_decode_and_prefill(impl):
+def test_mixed_step_write_then_decode_and_prefill(impl, fp16):
     """Workload 5: cache write of 2064 new tokens, then decode (16 sequences)
-    and causal prefill (4 chunks of 512 over prefix-shared blocks)."""
-    b = W.workload(5, device=DEV, poison=True)
+    and causal prefill (4 chunks of 512 over prefix-shared blocks); bf16, and
+    the same step of an fp16 model."""
+    b = W.workload(5, device=DEV, poison=True, fp16=fp16)
+    kv = b.kv_dtype
     d = desc_of(b)
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     B.pa_cache_write(d, b.k_new, b.v_new, kc, vc, b.slot_mapping)
     dec_out, dec_lse = gpu_decode(b, caches=(kc, vc))
     pf_out, pf_lse = gpu_prefill(b, caches=(kc, vc), prefill_impl=impl)
     # oracle: its own cache write of the same inputs, then attention
-    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+    code = oracle.KV_F16 if fp16 else oracle.KV_BF16
+    ok, ov = oracle.cache_write(code, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
                                 b.k_pool.cpu(), b.v_pool.cpu())
-    oc = (oracle.KV_BF16, ok, ov)
+    oc = (code, ok, ov)
     o_ref, l_ref = oracle_decode(b, ocaches=oc)
-    assert_close(dec_out, o_ref, TOL[W.KV_BF16], "decode out")
-    assert_close(dec_lse, l_ref, LSE_TOL[W.KV_BF16], "decode lse")
+    assert_close(dec_out, o_ref, TOL[kv], "decode out")
+    assert_close(dec_lse, l_ref, LSE_TOL[kv], "decode lse")
     # prefill: sampled rows (first, last and random rows of every chunk) x all heads
     gen = torch.Generator().manual_seed(12)
     rows = set()
@@ -356,8 +374,8 @@ def test_mixed_step_write_then_decode_and_prefill(impl):
     pairs = [(r, h) for r in sorted(rows) for h in range(32)]
     o_ref, l_ref = oracle_prefill(b, ocaches=oc, pairs=pairs)
     idx = torch.tensor([r * 32 + h for r, h in pairs])
-    assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[W.KV_BF16], "prefill out")
-    assert_close(pf_lse.reshape(-1)[idx], l_ref, LSE_TOL[W.KV_BF16], "prefill lse")
+    assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[kv], "prefill out")
+    assert_close(pf_lse.reshape(-1)[idx], l_ref, LSE_TOL[kv], "prefill lse")
 
 
 def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
