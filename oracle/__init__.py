@@ -64,13 +64,13 @@ def _load():
         lib.pa_oracle_e5m2_encode.restype = ctypes.c_uint8
         lib.pa_oracle_f16_decode.argtypes = [ctypes.c_uint16]
         lib.pa_oracle_f16_decode.restype = ctypes.c_double
-        lib.pa_oracle_cache_write.argtypes = [I, I, I, I, P, P, P, I, F, F, P, P]
+        lib.pa_oracle_cache_write.argtypes = [I, I, I, I, P, P, P, I, F, F, P, P, P, P]
         lib.pa_oracle_cache_write.restype = None
         lib.pa_oracle_attend_range.argtypes = [I, I, I, I, P, P, P, P, I, I, I, F, F, F, P, P]
         lib.pa_oracle_attend_range.restype = None
-        lib.pa_oracle_decode.argtypes = [I, I, I, I, I, P, P, P, P, I, P, I, F, F, F, I, I, P, I, P, P]
+        lib.pa_oracle_decode.argtypes = [I, I, I, I, I, P, P, P, P, I, P, I, F, F, F, P, P, I, I, P, I, P, P]
         lib.pa_oracle_decode.restype = None
-        lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, I, I, P, I, P, P]
+        lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, P, P, I, I, P, I, P, P]
         lib.pa_oracle_prefill.restype = None
         lib.pa_oracle_merge.argtypes = [P, P, I, I, P, P]
         lib.pa_oracle_merge.restype = None
@@ -127,17 +127,28 @@ def f16_decode(bits: int) -> float:
     return _load().pa_oracle_f16_decode(int(bits) & 0xFFFF)
 
 
+def _scales(a):
+    """Optional per-kv-head fp32 scales -> (keep-alive array or None, pointer or None)."""
+    if a is None:
+        return None, None
+    arr = _np(a, np.float32)
+    return arr, _ptr(arr)
+
+
 def cache_write(kv_dtype, block_size, num_kv_heads, head_dim, k, v, slot_mapping,
-                k_cache, v_cache, k_scale=1.0, v_scale=1.0):
-    """Scatter new K/V rows into copies of the caches; returns (k_cache, v_cache)."""
+                k_cache, v_cache, k_scale=1.0, v_scale=1.0, k_scales=None, v_scales=None):
+    """Scatter new K/V rows into copies of the caches; returns (k_cache, v_cache).
+    ``k_scales`` / ``v_scales``: optional per-kv-head scales of an 8-bit cache."""
     lib = _load()
+    ksa, ksp = _scales(k_scales)
+    vsa, vsp = _scales(v_scales)
     k = _np(k, np.uint16)
     v = _np(v, np.uint16)
     sm = _np(slot_mapping, np.int64)
     kc = _cache_np(k_cache, kv_dtype).copy()
     vc = _cache_np(v_cache, kv_dtype).copy()
     lib.pa_oracle_cache_write(kv_dtype, block_size, num_kv_heads, head_dim, _ptr(k), _ptr(v),
-                              _ptr(sm), int(sm.shape[0]), float(k_scale), float(v_scale),
+                              _ptr(sm), int(sm.shape[0]), float(k_scale), float(v_scale), ksp, vsp,
                               _ptr(kc), _ptr(vc))
     return kc, vc
 
@@ -159,11 +170,15 @@ def attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v
 
 
 def decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, k_cache, v_cache,
-           block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None, window=0, chunk=0):
+           block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None, window=0, chunk=0,
+           k_scales=None, v_scales=None):
     """Decode attention.  Returns (out [n, D], lse [n]) in fp64 for the (s, h)
     pairs given (default: all, row-major over (s, h)).  ``window`` / ``chunk``:
-    sliding-window / chunked-local attention (0: off)."""
+    sliding-window / chunked-local attention (0: off); ``k_scales`` /
+    ``v_scales``: per-kv-head scales of an 8-bit cache."""
     lib = _load()
+    ksa, ksp = _scales(k_scales)
+    vsa, vsp = _scales(v_scales)
     qn = _np(q, np.uint16)
     kc = _cache_np(k_cache, kv_dtype)
     vc = _cache_np(v_cache, kv_dtype)
@@ -179,18 +194,21 @@ def decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, k_cache
     lse = np.zeros(n, np.float64)
     lib.pa_oracle_decode(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
                          _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
-                         float(scale), float(k_scale), float(v_scale), int(window), int(chunk),
+                         float(scale), float(k_scale), float(v_scale), ksp, vsp, int(window), int(chunk),
                          None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
     return out, lse
 
 
 def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_start_loc,
             k_cache, v_cache, block_tables, context_lens, scale, k_scale=1.0, v_scale=1.0,
-            pairs=None, window=0, chunk=0):
+            pairs=None, window=0, chunk=0, k_scales=None, v_scales=None):
     """Causal chunked-prefill attention.  Returns (out [n, D], lse [n]) in fp64
     for the (token row, head) pairs given (default: all rows x heads).
-    ``window`` / ``chunk``: sliding-window / chunked-local attention (0: off)."""
+    ``window`` / ``chunk``: sliding-window / chunked-local attention (0: off);
+    ``k_scales`` / ``v_scales``: per-kv-head scales of an 8-bit cache."""
     lib = _load()
+    ksa, ksp = _scales(k_scales)
+    vsa, vsp = _scales(v_scales)
     qn = _np(q, np.uint16)
     qsl = _np(query_start_loc, np.int32)
     kc = _cache_np(k_cache, kv_dtype)
@@ -207,7 +225,7 @@ def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_
     lse = np.zeros(n, np.float64)
     lib.pa_oracle_prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn),
                           _ptr(qsl), _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), S,
-                          float(scale), float(k_scale), float(v_scale), int(window), int(chunk),
+                          float(scale), float(k_scale), float(v_scale), ksp, vsp, int(window), int(chunk),
                           None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
     return out, lse
 

@@ -265,12 +265,14 @@ static int64_t cache_row(const int32_t *table_row, int block_size, int num_kv_he
  * offset = slot % block_size, and for every kv head h the cache row
  * (block, h, offset) receives enc(k[i][h][:]) (same for v).
  * enc = bit copy for bf16 and fp16 (the rows arrive in the cache's own
- * type); for E4M3 / E5M2, enc(x) = e4m3 / e5m2 of fl32(fl32(x) / scale).
+ * type); for E4M3 / E5M2, enc(x) = e4m3 / e5m2 of fl32(fl32(x) / scale),
+ * scale being kv head h's entry of k_scales / v_scales when those are given
+ * (per-head scales), else the per-tensor k_scale / v_scale.
  */
 void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int head_dim,
                            const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
-                           int num_tokens, float k_scale, float v_scale, void *k_cache,
-                           void *v_cache) {
+                           int num_tokens, float k_scale, float v_scale, const float *k_scales,
+                           const float *v_scales, void *k_cache, void *v_cache) {
   for (int i = 0; i < num_tokens; ++i) {
     int64_t slot = slot_mapping[i];
     if (slot < 0) continue;
@@ -285,8 +287,8 @@ void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int h
           ((uint16_t *)k_cache)[dst_row * head_dim + d] = ks[d];
           ((uint16_t *)v_cache)[dst_row * head_dim + d] = vs[d];
         } else {
-          float kq = bf16_bits_to_float(ks[d]) / k_scale;
-          float vq = bf16_bits_to_float(vs[d]) / v_scale;
+          float kq = bf16_bits_to_float(ks[d]) / (k_scales ? k_scales[h] : k_scale);
+          float vq = bf16_bits_to_float(vs[d]) / (v_scales ? v_scales[h] : v_scale);
           uint8_t kc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)kq) : pa_oracle_e4m3_encode((double)kq);
           uint8_t vc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)vq) : pa_oracle_e4m3_encode((double)vq);
           ((uint8_t *)k_cache)[dst_row * head_dim + d] = kc;
@@ -377,8 +379,8 @@ void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_
                       int head_dim, const uint16_t *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int num_seqs, float scale, float k_scale,
-                      float v_scale, int window, int chunk, const int32_t *pairs, int num_pairs,
-                      double *out, double *lse) {
+                      float v_scale, const float *k_scales, const float *v_scales, int window,
+                      int chunk, const int32_t *pairs, int num_pairs, double *out, double *lse) {
   int g = num_q_heads / num_kv_heads;
   int total = pairs ? num_pairs : num_seqs * num_q_heads;
   for (int i = 0; i < total; ++i) {
@@ -389,8 +391,8 @@ void pa_oracle_decode(int kv_dtype, int block_size, int num_kv_heads, int num_q_
     int L = context_lens[s];
     int lo = L > 0 ? local_first_key(L - 1, window, chunk) : 0;
     pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
-                           row, h / g, lo, L, scale, k_scale, v_scale, out + (int64_t)i * head_dim,
-                           lse + i);
+                           row, h / g, lo, L, scale, k_scales ? k_scales[h / g] : k_scale,
+                           v_scales ? v_scales[h / g] : v_scale, out + (int64_t)i * head_dim, lse + i);
   }
 }
 
@@ -410,8 +412,9 @@ void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q
                        int head_dim, const uint16_t *q, const int32_t *query_start_loc,
                        const void *k_cache, const void *v_cache, const int32_t *block_tables,
                        int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
-                       float scale, float k_scale, float v_scale, int window, int chunk,
-                       const int32_t *pairs, int num_pairs, double *out, double *lse) {
+                       float scale, float k_scale, float v_scale, const float *k_scales,
+                       const float *v_scales, int window, int chunk, const int32_t *pairs,
+                       int num_pairs, double *out, double *lse) {
   int g = num_q_heads / num_kv_heads;
   int num_rows = query_start_loc[num_seqs];
   int total = pairs ? num_pairs : num_rows * num_q_heads;
@@ -425,8 +428,9 @@ void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q
     const uint16_t *q_vec = q + ((int64_t)r * num_q_heads + h) * head_dim;
     const int32_t *row = block_tables + (int64_t)s * max_blocks_per_seq;
     pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
-                           row, h / g, local_first_key(pos, window, chunk), pos + 1, scale, k_scale,
-                           v_scale, out + (int64_t)i * head_dim, lse + i);
+                           row, h / g, local_first_key(pos, window, chunk), pos + 1, scale,
+                           k_scales ? k_scales[h / g] : k_scale, v_scales ? v_scales[h / g] : v_scale,
+                           out + (int64_t)i * head_dim, lse + i);
   }
 }
 

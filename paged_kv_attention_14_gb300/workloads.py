@@ -79,6 +79,9 @@ class PagedBatch:
     k_new: Optional[torch.Tensor] = None             # [T, Hkv, D] bf16
     v_new: Optional[torch.Tensor] = None
     slot_mapping: Optional[torch.Tensor] = None      # int64 [T]
+    # per-kv-head scales of an 8-bit cache (fp32 [Hkv]); None: per-tensor
+    k_scales: Optional[torch.Tensor] = None
+    v_scales: Optional[torch.Tensor] = None
     meta: dict = field(default_factory=dict)
 
     @property
@@ -171,10 +174,19 @@ def _readable_mask(num_blocks, block_size, tables_and_lens):
 
 
 def _fill_pool(b: PagedBatch, g, device, poison: bool, readable: torch.Tensor,
-               written: Optional[torch.Tensor]):
+               written: Optional[torch.Tensor], per_head_scales: bool = False):
     shape = (b.num_blocks, b.num_kv_heads, b.block_size, b.head_dim)
     b.k_pool = _randn(shape, g, device, act_dtype(b.kv_dtype))
     b.v_pool = _randn(shape, g, device, act_dtype(b.kv_dtype))
+    if per_head_scales:
+        # heads of different magnitudes (x 2^(h - Hkv/2)), each quantised with
+        # its own scale amax(head) / the format's max
+        f = torch.pow(2.0, torch.arange(b.num_kv_heads, dtype=torch.float32, device=device) - b.num_kv_heads // 2)
+        b.k_pool = (b.k_pool.float() * f[None, :, None, None]).to(b.k_pool.dtype)
+        b.v_pool = (b.v_pool.float() * f.flip(0)[None, :, None, None]).to(b.v_pool.dtype)
+        mx = FP8_MAX[b.kv_dtype]
+        b.k_scales = (b.k_pool.float().abs().amax(dim=(0, 2, 3)) / mx).to(torch.float32).contiguous()
+        b.v_scales = (b.v_pool.float().abs().amax(dim=(0, 2, 3)) / mx).to(torch.float32).contiguous()
     if b.kv_dtype in FP8_MAX:
         # per-tensor scales from the source values (amax / the format's max)
         ka = float(b.k_pool.float().abs().max())
@@ -198,7 +210,7 @@ def _fill_pool(b: PagedBatch, g, device, poison: bool, readable: torch.Tensor,
 
 
 def _decode_batch(name, seed, lens, Hq, Hkv, D, kv_dtype, scale, device, poison,
-                  num_blocks=None) -> PagedBatch:
+                  num_blocks=None, per_head_scales=False) -> PagedBatch:
     g_cpu = _gen(seed, "cpu")
     lens = torch.as_tensor(lens, dtype=torch.int32)
     needed = int(sum((int(L) + BLOCK_SIZE - 1) // BLOCK_SIZE for L in lens))
@@ -212,7 +224,7 @@ def _decode_batch(name, seed, lens, Hq, Hkv, D, kv_dtype, scale, device, poison,
     g = _gen(seed + 7, device)
     b.q_decode = _randn((S, Hq, D), g, device, act_dtype(kv_dtype))
     readable = _readable_mask(NB, BLOCK_SIZE, [(tables, lens)])
-    _fill_pool(b, g, device, poison, readable, None)
+    _fill_pool(b, g, device, poison, readable, None, per_head_scales)
     b.block_tables_decode = tables.to(device)
     b.context_lens_decode = lens.to(device)
     # this step's new token of every sequence is its last one (position L - 1);
@@ -238,11 +250,12 @@ WORKLOAD_NAMES = {
 
 
 def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP8,
-             fp16: bool = False) -> PagedBatch:
+             fp16: bool = False, per_head_scales: bool = False) -> PagedBatch:
     """Build workload ``n`` (1..5) on ``device``.  ``fp8_format`` picks the
     8-bit cache format of workload 4 (E4M3, or E5M2 for the same shapes);
     ``fp16`` turns the bf16 workloads (1, 2, 3, 5) into fp16 ones: fp16 cache,
-    q and new rows, from the same random draws."""
+    q and new rows, from the same random draws; ``per_head_scales`` gives
+    workload 4's kv heads different magnitudes and one scale each."""
     seed = 1000 + n
     kv16 = KV_F16 if fp16 else KV_BF16
 
@@ -271,9 +284,11 @@ def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP
         g = _gen(seed, "cpu")
         lens = torch.randint(1024, 8192 + 1, (128,), generator=g)
         nm = WORKLOAD_NAMES[4] if fp8_format == KV_FP8 else WORKLOAD_NAMES[4].replace("E4M3", "E5M2")
+        if per_head_scales:
+            nm += ", per-head scales"
         return _decode_batch(nm,
                              seed, lens.tolist(), 40, 8, 128, fp8_format, 1.0 / math.sqrt(128),
-                             device, poison)
+                             device, poison, per_head_scales=per_head_scales)
     if n == 5:
         return _mixed_batch(seed, device, poison, kv16, name(5))
     raise ValueError(f"unknown workload {n}")
@@ -336,16 +351,17 @@ def _mixed_batch(seed, device, poison, kv_dtype=KV_BF16, name=WORKLOAD_NAMES[5])
 
 
 def random_decode(seed: int, lens, Hq, Hkv, D, kv_dtype=KV_BF16, scale=None, device="cpu",
-                  poison=True, num_blocks=None) -> PagedBatch:
+                  poison=True, num_blocks=None, per_head_scales=False) -> PagedBatch:
     """Small randomized decode case for property tests (same recipe as above)."""
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     return _decode_batch(f"random decode seed {seed}", seed, lens, Hq, Hkv, D, kv_dtype, scale,
-                         device, poison, num_blocks=num_blocks)
+                         device, poison, num_blocks=num_blocks, per_head_scales=per_head_scales)
 
 
 def random_prefill(seed: int, q_lens, ctx_lens, Hq, Hkv, D, kv_dtype=KV_BF16, scale=None,
-                   device="cpu", poison=True, shared_prefix_blocks: int = 0) -> PagedBatch:
+                   device="cpu", poison=True, shared_prefix_blocks: int = 0,
+                   per_head_scales: bool = False) -> PagedBatch:
     """Small randomized chunked-prefill case: sequence s has ctx_lens[s] cached
     tokens of which the last q_lens[s] are its chunk's queries.  Optionally the
     first ``shared_prefix_blocks`` blocks are the same physical blocks in every
@@ -377,7 +393,7 @@ def random_prefill(seed: int, q_lens, ctx_lens, Hq, Hkv, D, kv_dtype=KV_BF16, sc
     g = _gen(seed + 7, device)
     b.q_prefill = _randn((int(qsl[-1]), Hq, D), g, device, act_dtype(kv_dtype))
     readable = _readable_mask(NB, B, [(tables, lens)])
-    _fill_pool(b, g, device, poison, readable, None)
+    _fill_pool(b, g, device, poison, readable, None, per_head_scales)
     b.block_tables_prefill = tables.to(device)
     b.context_lens_prefill = lens.to(device)
     b.query_start_loc = qsl.to(device)

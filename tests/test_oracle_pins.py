@@ -65,7 +65,7 @@ def _oracle_caches(b: W.PagedBatch):
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)
     kc, vc = oracle.cache_write(code, b.block_size, b.num_kv_heads, b.head_dim, k, v, slots, z, z,
-                                b.k_scale, b.v_scale)
+                                b.k_scale, b.v_scale, k_scales=b.k_scales, v_scales=b.v_scales)
     return code, kc, vc
 
 
@@ -74,6 +74,10 @@ def _dense_pools(b: W.PagedBatch, kc, vc):
     if b.kv_dtype in _KV16:
         return _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
     dt = _FP8_KINDS[b.kv_dtype][1]
+    if b.k_scales is not None:  # per-kv-head scales
+        ks = b.k_scales.double().numpy()[None, :, None, None]
+        vs = b.v_scales.double().numpy()[None, :, None, None]
+        return _fp8_cache_to_f64(kc, 1.0, dt) * ks, _fp8_cache_to_f64(vc, 1.0, dt) * vs
     return _fp8_cache_to_f64(kc, b.k_scale, dt), _fp8_cache_to_f64(vc, b.v_scale, dt)
 
 
@@ -81,7 +85,7 @@ def _oracle_decode(b: W.PagedBatch, pairs=None):
     kd, kc, vc = _oracle_caches(b)
     return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode,
                          kc, vc, b.block_tables_decode, b.context_lens_decode, b.scale,
-                         b.k_scale, b.v_scale, pairs=pairs)
+                         b.k_scale, b.v_scale, pairs=pairs, k_scales=b.k_scales, v_scales=b.v_scales)
 
 
 # ------------------------------------------------------------------ E4M3 codec
@@ -241,13 +245,47 @@ def test_cache_write_skips_negative_slots_and_fp8_matches_torch_quantisation(kv)
     assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
 
 
+@pytest.mark.parametrize("kv", [W.KV_FP8, W.KV_FP8_E5M2])
+def test_cache_write_per_head_scales_match_torch_quantisation_per_head(kv):
+    code, tdt = _FP8_KINDS[kv]
+    g = torch.Generator().manual_seed(4)
+    T, H, D, NB = 33, 3, 64, 6
+    f = torch.tensor([0.25, 1.0, 8.0])[None, :, None]
+    k = (torch.randn(T, H, D, generator=g) * f).to(torch.bfloat16)
+    v = (torch.randn(T, H, D, generator=g) / f).to(torch.bfloat16)
+    slots = torch.randperm(NB * 16, generator=g)[:T].to(torch.int64)
+    ks = (k.float().abs().amax(dim=(0, 2)) / W.FP8_MAX[kv]).float()
+    vs = (v.float().abs().amax(dim=(0, 2)) / W.FP8_MAX[kv]).float()
+    z = np.zeros((NB, H, 16, D), np.uint8)
+    # the per-tensor arguments are deliberately wrong: the per-head ones win
+    kc, vc = oracle.cache_write(code, 16, H, D, k, v, slots, z, z, 123.0, 456.0, k_scales=ks, v_scales=vs)
+    s = slots.numpy()
+    qk = (k.float() / ks[None, :, None]).to(tdt).view(torch.uint8).numpy()
+    qv = (v.float() / vs[None, :, None]).to(tdt).view(torch.uint8).numpy()
+    ref_k, ref_v = z.copy(), z.copy()
+    ref_k[s // 16, :, s % 16, :] = qk
+    ref_v[s // 16, :, s % 16, :] = qv
+    assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
+
+
+def test_per_head_scales_all_equal_to_the_tensor_scale_change_nothing():
+    b = W.random_decode(17, [3, 40, 100], 8, 4, 64, kv_dtype=W.KV_FP8, poison=True)
+    kd, kc, vc = _oracle_caches(b)
+    args = (kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, kc, vc,
+            b.block_tables_decode, b.context_lens_decode, b.scale, b.k_scale, b.v_scale)
+    o1, l1 = oracle.decode(*args)
+    o2, l2 = oracle.decode(*args, k_scales=np.full(4, b.k_scale, np.float32), v_scales=np.full(4, b.v_scale, np.float32))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
 # ------------------------------------------------------------ decode attention
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_F16, W.KV_FP8, W.KV_FP8_E5M2])
+@pytest.mark.parametrize("kv,per_head", [(W.KV_BF16, False), (W.KV_F16, False), (W.KV_FP8, False),
+                                         (W.KV_FP8_E5M2, False), (W.KV_FP8, True), (W.KV_FP8_E5M2, True)])
 @pytest.mark.parametrize("D,Hq,Hkv", [(8, 2, 2), (64, 4, 2), (8, 10, 2), (64, 5, 1)])
-def test_decode_matches_bruteforce_sdpa(kv, D, Hq, Hkv):
+def test_decode_matches_bruteforce_sdpa(kv, per_head, D, Hq, Hkv):
     lens = [1, 5, 16, 17, 40]
-    b = W.random_decode(11 + D + Hq, lens, Hq, Hkv, D, kv_dtype=kv, poison=True)
+    b = W.random_decode(11 + D + Hq, lens, Hq, Hkv, D, kv_dtype=kv, poison=True, per_head_scales=per_head)
     out, lse = _oracle_decode(b)
     kd, kc, vc = _oracle_caches(b)
     kf, vf = _dense_pools(b, kc, vc)
@@ -391,13 +429,14 @@ def _oracle_prefill(b: W.PagedBatch, pairs=None):
     kd, kc, vc = _oracle_caches(b)
     return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill,
                           b.query_start_loc, kc, vc, b.block_tables_prefill, b.context_lens_prefill,
-                          b.scale, b.k_scale, b.v_scale, pairs=pairs)
+                          b.scale, b.k_scale, b.v_scale, pairs=pairs, k_scales=b.k_scales, v_scales=b.v_scales)
 
 
-@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_F16, W.KV_FP8, W.KV_FP8_E5M2])
-def test_prefill_matches_bruteforce_sdpa_with_causal_mask(kv):
+@pytest.mark.parametrize("kv,per_head", [(W.KV_BF16, False), (W.KV_F16, False), (W.KV_FP8, False),
+                                         (W.KV_FP8_E5M2, False), (W.KV_FP8, True), (W.KV_FP8_E5M2, True)])
+def test_prefill_matches_bruteforce_sdpa_with_causal_mask(kv, per_head):
     q_lens, ctx = [5, 16, 1, 23], [5, 40, 33, 64]
-    b = W.random_prefill(91, q_lens, ctx, 4, 2, 64, kv_dtype=kv, shared_prefix_blocks=1)
+    b = W.random_prefill(91, q_lens, ctx, 4, 2, 64, kv_dtype=kv, shared_prefix_blocks=1, per_head_scales=per_head)
     out, _ = _oracle_prefill(b)
     kd, kc, vc = _oracle_caches(b)
     kf, vf = _dense_pools(b, kc, vc)
