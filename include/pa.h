@@ -119,6 +119,15 @@ typedef enum {
  *                  attention_chunk (its own chunk) up to p; 0 disables either,
  *                  with both the later start applies.  Applies to pa_decode,
  *                  pa_decode_static and pa_prefill_chunk; must be >= 0.
+ *   k_scales, v_scales : FP8 only, optional.  Device arrays of num_kv_heads
+ *                  fp32 scales, one per kv head (per-head scaling of the
+ *                  8-bit pages; the pages name E4M3/E5M2 pages but no
+ *                  scaling scheme).  Where given, kv head h uses its entry
+ *                  instead of k_scale / v_scale in the cache write, decode
+ *                  and prefill; NULL keeps the per-tensor scale.  4-byte
+ *                  aligned, owned by the caller, read by the kernels at run
+ *                  time (so they must stay valid until the work completes).
+ *                  Must be NULL for bf16 and fp16 caches.
  */
 typedef struct {
   int32_t num_blocks;
@@ -133,6 +142,8 @@ typedef struct {
   int32_t prefill_impl;    /* pa_prefill_impl */
   int32_t sliding_window;  /* 0: none */
   int32_t attention_chunk; /* 0: none */
+  const float *k_scales;   /* NULL: per-tensor k_scale */
+  const float *v_scales;   /* NULL: per-tensor v_scale */
 } pa_kv_desc;
 
 /* PA_ABI_VERSION of the loaded library. */

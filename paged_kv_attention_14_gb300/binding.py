@@ -58,6 +58,8 @@ class PaKvDesc(ctypes.Structure):
         ("prefill_impl", ctypes.c_int32),
         ("sliding_window", ctypes.c_int32),
         ("attention_chunk", ctypes.c_int32),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
     ]
 
 
@@ -108,9 +110,21 @@ def make_desc(num_blocks: int, num_kv_heads: int, num_q_heads: int, head_dim: in
               kv_dtype: int = PA_KV_BF16, k_scale: float = 0.0, v_scale: float = 0.0,
               block_size: int = 16, decode_impl: int = PA_DECODE_AUTO,
               prefill_impl: int = PA_PREFILL_AUTO, sliding_window: int = 0,
-              attention_chunk: int = 0) -> PaKvDesc:
-    return PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
-                    k_scale, v_scale, decode_impl, prefill_impl, sliding_window, attention_chunk)
+              attention_chunk: int = 0, k_scales: Optional[torch.Tensor] = None,
+              v_scales: Optional[torch.Tensor] = None) -> PaKvDesc:
+    """``k_scales`` / ``v_scales``: optional per-kv-head fp32 scales of an
+    8-bit cache, CUDA tensors of num_kv_heads elements; the descriptor keeps a
+    reference to them (the kernels read them at run time)."""
+    for t, name in ((k_scales, "k_scales"), (v_scales, "v_scales")):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()
+                              or t.numel() != num_kv_heads):
+            raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of num_kv_heads elements")
+    d = PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
+                 k_scale, v_scale, decode_impl, prefill_impl, sliding_window, attention_chunk,
+                 k_scales.data_ptr() if k_scales is not None else None,
+                 v_scales.data_ptr() if v_scales is not None else None)
+    d._keep = (k_scales, v_scales)
+    return d
 
 
 def abi_version() -> int:

@@ -48,6 +48,10 @@ pa_status check_desc(const pa_kv_desc *d) {
   const bool kv8 = d->kv_dtype == PA_KV_FP8_E4M3 || d->kv_dtype == PA_KV_FP8_E5M2;
   if (kv8 && (!(d->k_scale >= 0.f) || !(d->v_scale >= 0.f)))
     return fail(PA_ERR_INVALID_ARG, "k_scale and v_scale must be >= 0 (0 means 1)%s");
+  if (!kv8 && (d->k_scales || d->v_scales))
+    return fail(PA_ERR_INVALID_ARG, "per-head k_scales / v_scales apply to FP8 caches only%s");
+  if ((reinterpret_cast<uintptr_t>(d->k_scales) | reinterpret_cast<uintptr_t>(d->v_scales)) & 3u)
+    return fail(PA_ERR_INVALID_ARG, "k_scales and v_scales must be 4-byte aligned%s");
   return PA_OK;
 }
 

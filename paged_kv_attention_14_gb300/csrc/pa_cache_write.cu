@@ -19,7 +19,8 @@ template <int KVT>
 __global__ void __launch_bounds__(256) cache_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint8_t *__restrict__ k_cache,
     uint8_t *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_vecs,
-    int vecs_per_row, int num_kv_heads, int block_size, float k_scale, float v_scale) {
+    int vecs_per_row, int num_kv_heads, int block_size, float k_scale, float v_scale,
+    const float *__restrict__ k_scales, const float *__restrict__ v_scales) {
   // a kernel launched after this one as a programmatic dependent (pa_decode,
   // pa_prefill_chunk) may start its launch now; it waits for this grid's
   // writes before reading anything
@@ -54,8 +55,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
       r.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
       return r;
     };
-    reinterpret_cast<uint2 *>(k_cache)[dst_row * vecs_per_row + vec] = enc(kv, k_scale);
-    reinterpret_cast<uint2 *>(v_cache)[dst_row * vecs_per_row + vec] = enc(vv, v_scale);
+    // per-kv-head scales where given
+    const float ks = k_scales ? __ldg(k_scales + head) : k_scale;
+    const float vs = v_scales ? __ldg(v_scales + head) : v_scale;
+    reinterpret_cast<uint2 *>(k_cache)[dst_row * vecs_per_row + vec] = enc(kv, ks);
+    reinterpret_cast<uint2 *>(v_cache)[dst_row * vecs_per_row + vec] = enc(vv, vs);
   }
 }
 
@@ -72,17 +76,17 @@ cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v
     cache_write_kernel<kKvBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
   else if (d.kv_dtype == PA_KV_FP8_E5M2)
     cache_write_kernel<kKvE5M2><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
   else
     cache_write_kernel<kKvFp8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs);
+        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
   return cudaGetLastError();
 }
 

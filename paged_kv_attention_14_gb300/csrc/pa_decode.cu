@@ -180,6 +180,9 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   const float ks = (fp8 && d.k_scale != 0.f) ? d.k_scale : 1.f;
   a.qscale = scale * ks * dec::kLog2e;
   a.vscale = (fp8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
+  a.qscale0 = scale * dec::kLog2e;
+  a.k_scales = fp8 ? d.k_scales : nullptr;
+  a.v_scales = fp8 ? d.v_scales : nullptr;
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
   a.err = reinterpret_cast<int32_t *>(ws);

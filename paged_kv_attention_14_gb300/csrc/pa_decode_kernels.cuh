@@ -89,6 +89,9 @@ struct DecodeArgs {
   int num_groups;  // kv head groups per sequence (num_kv_heads / HG)
   float qscale;    // scale * k_scale * log2(e)
   float vscale;    // v_scale (1 for bf16)
+  float qscale0;   // scale * log2(e): qscale before the k scale
+  const float *k_scales;  // per-kv-head scales of an 8-bit cache (NULL: k_scale, v_scale)
+  const float *v_scales;
   int window;      // sliding window (0: none)
   int chunk;       // chunked-local attention (0: none)
   int32_t *err;
@@ -116,6 +119,15 @@ __device__ __forceinline__ int seq_first_block(const DecodeArgs &a, int L) {
 }
 __device__ __forceinline__ int seq_blocks(const DecodeArgs &a, int L) {
   return ((L + 15) >> 4) - seq_first_block(a, L);
+}
+
+// Score and output scales of kv head kvh: its per-head k / v scale where the
+// cache has them, else the per-tensor ones folded in on the host.
+__device__ __forceinline__ float head_qscale(const DecodeArgs &a, int kvh) {
+  return a.k_scales ? a.qscale0 * __ldg(a.k_scales + kvh) : a.qscale;
+}
+__device__ __forceinline__ float head_vscale(const DecodeArgs &a, int kvh) {
+  return a.v_scales ? __ldg(a.v_scales + kvh) : a.vscale;
 }
 
 // ---------------------------------------------------------------- workspace
@@ -411,7 +423,7 @@ __device__ void finish_piece(const DecodeArgs &a, const StageHdr &h, const float
     const float res = O / Ls;
     const float lse2 = M + log2f(Ls);
     if (!split) {
-      a.out[(static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j) * D + d] = res * a.vscale;
+      a.out[(static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j) * D + d] = res * head_vscale(a, h.grp);
       if (a.lse && d == 0) a.lse[static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j] = lse2 * kLn2;
     } else {
       const int64_t sl = (static_cast<int64_t>(me) * 2 + my_slot) * HP + j;
@@ -447,7 +459,7 @@ __device__ void finish_piece(const DecodeArgs &a, const StageHdr &h, const float
           W += w;
           O += w * __ldcg(a.slot_o + base * D + d);
         }
-        a.out[(static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j) * D + d] = O / W * a.vscale;
+        a.out[(static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j) * D + d] = O / W * head_vscale(a, h.grp);
         if (a.lse && d == 0) a.lse[static_cast<int64_t>(h.s) * a.num_q_heads + hq0 + j] = (M + log2f(W)) * kLn2;
       }
     }
@@ -616,13 +628,14 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
     const uint8_t *Vs = Ks + C::KVB;
     if (h.flags & kFlagFirst) {
       const uint16_t *Qs = reinterpret_cast<const uint16_t *>(Ks + C::QOFF);
+      const float qsc = head_qscale(a, h.grp);  // one kv head per segment
 #pragma unroll
       for (int j = 0; j < GP; ++j) {
         m[j] = -INFINITY;
         l[j] = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
-          q[j][e] = j < a.g ? lo16<KVT == kKvF16 ? kKvF16 : kKvBf16>(Qs[j * D + RS::dim(j8, e)]) * a.qscale : 0.f;
+          q[j][e] = j < a.g ? lo16<KVT == kKvF16 ? kKvF16 : kKvBf16>(Qs[j * D + RS::dim(j8, e)]) * qsc : 0.f;
           o[j][e] = 0.f;
         }
       }
@@ -868,7 +881,7 @@ __device__ void merge_segment(const DecodeArgs &a, const StageHdr &h, long long 
     const float Mk = __shfl_sync(0xffffffffu, M, k);
     const float Wk = __shfl_sync(0xffffffffu, W, k);
     if (sk % GQ >= a.g) continue;
-    const float inv = Mk == -INFINITY ? 0.f : a.vscale / Wk;
+    const float inv = Mk == -INFINITY ? 0.f : head_vscale(a, h.grp * C::HG + sk / GQ) / Wk;
     float *o = a.out + (static_cast<int64_t>(h.s) * a.num_q_heads + qhead(sk)) * D + part * DPL;
     for (int f0 = 0; f0 < DPL / 4; f0 += NF4) {
       float4 acc[NF4];
@@ -959,7 +972,7 @@ __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *
             acc.w += v.w * cw[k];
           }
           if (!split) {
-            const float sc = inv * a.vscale;
+            const float sc = inv * head_vscale(a, h.grp * HG + hw);
             *reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(h.s) * a.num_q_heads + qh) * D + d4) =
                 make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
           } else {
@@ -1063,6 +1076,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
   uint32_t cpar = 0;
   int rb = 0;
   uint32_t rpar = 1;  // the partial-state buffers start out free
+  float qsc = a.qscale;  // score scale of this warp's kv head (set per segment)
   PA_TRACE(const long long tc0 = clock64(); long long tc_full = 0, tc_fin = 0, n_st = 0, n_pc = 0;)
   for (;;) {
     PA_TRACE(const long long tw0 = clock64();)
@@ -1076,6 +1090,7 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
     const uint8_t *Ks = stages + size_t(stage) * C::STAGEB;
     const uint8_t *Vs = Ks + C::KVB;
     if (h.flags & kFlagFirst) {
+      qsc = head_qscale(a, h.grp * HG + hw);
       // Q^T fragments of this kv head's query heads (zero past g)
       const uint16_t *Qs = reinterpret_cast<const uint16_t *>(Ks + C::QOFF) + hw * a.g * D;
 #pragma unroll
@@ -1159,10 +1174,10 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
       const bool v_lo = r < vt && r >= vl, v_hi = r + 8 < vt && r + 8 >= vl;
 #pragma unroll
       for (int nn = 0; nn < NN; ++nn) {
-        const float s0 = v_lo ? (sa[nn][0] + sb[nn][0]) * a.qscale : -INFINITY;
-        const float s1 = v_lo ? (sa[nn][1] + sb[nn][1]) * a.qscale : -INFINITY;
-        const float s2 = v_hi ? (sa[nn][2] + sb[nn][2]) * a.qscale : -INFINITY;
-        const float s3 = v_hi ? (sa[nn][3] + sb[nn][3]) * a.qscale : -INFINITY;
+        const float s0 = v_lo ? (sa[nn][0] + sb[nn][0]) * qsc : -INFINITY;
+        const float s1 = v_lo ? (sa[nn][1] + sb[nn][1]) * qsc : -INFINITY;
+        const float s2 = v_hi ? (sa[nn][2] + sb[nn][2]) * qsc : -INFINITY;
+        const float s3 = v_hi ? (sa[nn][3] + sb[nn][3]) * qsc : -INFINITY;
         float c0 = fmaxf(s0, s2), c1 = fmaxf(s1, s3);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {

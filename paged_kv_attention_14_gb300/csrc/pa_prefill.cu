@@ -47,6 +47,9 @@ struct PrefillArgs {
   int qt;  // queries per CTA
   float qscale;
   float vscale;
+  float qscale0;  // scale * log2(e): qscale before the k scale
+  const float *k_scales;  // per-kv-head scales of an 8-bit cache (NULL: per-tensor)
+  const float *v_scales;
   int window;  // local attention (see pa_kv_desc), 0: none
   int chunk;
 };
@@ -96,6 +99,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   const int lane = tid & 31;
   const int g = a.g;
   const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
+  // score scale of this CTA's kv head (its own k scale where the cache has per-head scales)
+  const float qscale = a.k_scales ? a.qscale0 * __ldg(a.k_scales + kvh) : a.qscale;
 
   uint8_t *kt_s[2], *vt_s[2];
   uint8_t *kraw[2], *vraw[2];
@@ -252,8 +257,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = kt * C::KT + n * 8 + 2 * c4 + e;
-        float vlo = sacc[n][e] * a.qscale;
-        float vhi = sacc[n][2 + e] * a.qscale;
+        float vlo = sacc[n][e] * qscale;
+        float vhi = sacc[n][2 + e] * qscale;
         if (need_mask) {
           vlo = (t <= pos_lo && t >= first_lo) ? vlo : -INFINITY;
           vhi = (t <= pos_hi && t >= first_hi) ? vhi : -INFINITY;
@@ -332,8 +337,9 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  const float inv_lo = l_lo > 0.f ? a.vscale / l_lo : 0.f;
-  const float inv_hi = l_hi > 0.f ? a.vscale / l_hi : 0.f;
+  const float vscale = a.v_scales ? __ldg(a.v_scales + kvh) : a.vscale;
+  const float inv_lo = l_lo > 0.f ? vscale / l_lo : 0.f;
+  const float inv_hi = l_hi > 0.f ? vscale / l_hi : 0.f;
   if (ok_lo) {
     const int64_t row = static_cast<int64_t>(qs + qt0 + row_query(r_lo)) * a.num_q_heads + kvh * g + r_lo % g;
     float *o = a.out + row * D;
@@ -406,6 +412,9 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   const float ks = (fp8 && d.k_scale != 0.f) ? d.k_scale : 1.f;
   a.qscale = scale * ks * kLog2e;
   a.vscale = (fp8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
+  a.qscale0 = scale * kLog2e;
+  a.k_scales = fp8 ? d.k_scales : nullptr;
+  a.v_scales = fp8 ? d.v_scales : nullptr;
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
   void *fn;

@@ -24,6 +24,10 @@ _CODES = {W.KV_BF16: (B.PA_KV_BF16, oracle.KV_BF16), W.KV_F16: (B.PA_KV_F16, ora
 KV16 = (W.KV_BF16, W.KV_F16)
 
 
+def _cpu(t):
+    return None if t is None else t.cpu()
+
+
 def kv_code(b: W.PagedBatch) -> int:
     return _CODES[b.kv_dtype][0]
 
@@ -33,7 +37,8 @@ def desc_of(b: W.PagedBatch, decode_impl: int = B.PA_DECODE_AUTO,
     return B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv_code(b),
                        b.k_scale if b.kv_dtype not in KV16 else 0.0,
                        b.v_scale if b.kv_dtype not in KV16 else 0.0, decode_impl=decode_impl,
-                       prefill_impl=prefill_impl, sliding_window=window, attention_chunk=chunk)
+                       prefill_impl=prefill_impl, sliding_window=window, attention_chunk=chunk,
+                       k_scales=b.k_scales, v_scales=b.v_scales)
 
 
 def gpu_caches(b: W.PagedBatch):
@@ -57,7 +62,8 @@ def oracle_caches(b: W.PagedBatch):
     k, v, slots = b.pool_tokens_as_rows()
     z = np.zeros(tuple(b.k_pool.shape), np.uint8)
     kc, vc = oracle.cache_write(code, b.block_size, b.num_kv_heads, b.head_dim,
-                                k.cpu(), v.cpu(), slots.cpu(), z, z, b.k_scale, b.v_scale)
+                                k.cpu(), v.cpu(), slots.cpu(), z, z, b.k_scale, b.v_scale,
+                                k_scales=_cpu(b.k_scales), v_scales=_cpu(b.v_scales))
     return code, kc, vc
 
 
@@ -81,7 +87,8 @@ def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
     return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode.cpu(), kc, vc,
                          b.block_tables_decode.cpu(), b.context_lens_decode.cpu(), b.scale, b.k_scale,
-                         b.v_scale, pairs=pairs, window=window, chunk=chunk)
+                         b.v_scale, pairs=pairs, window=window, chunk=chunk, k_scales=_cpu(b.k_scales),
+                         v_scales=_cpu(b.v_scales))
 
 
 def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO, window=0, chunk=0):
@@ -104,7 +111,7 @@ def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0)
     return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill.cpu(),
                           b.query_start_loc.cpu(), kc, vc, b.block_tables_prefill.cpu(),
                           b.context_lens_prefill.cpu(), b.scale, b.k_scale, b.v_scale, pairs=pairs,
-                          window=window, chunk=chunk)
+                          window=window, chunk=chunk, k_scales=_cpu(b.k_scales), v_scales=_cpu(b.v_scales))
 
 
 def assert_close(got: torch.Tensor, want: np.ndarray, tol: float, what: str = ""):
@@ -136,7 +143,8 @@ def compact_decode_batch(b: W.PagedBatch, seqs) -> W.PagedBatch:
     c = W.PagedBatch(name=b.name + " (subset)", block_size=b.block_size, num_q_heads=b.num_q_heads,
                      num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, kv_dtype=b.kv_dtype, scale=b.scale,
                      k_scale=b.k_scale, v_scale=b.v_scale, num_blocks=len(uniq),
-                     k_pool=b.k_pool[idx].contiguous(), v_pool=b.v_pool[idx].contiguous())
+                     k_pool=b.k_pool[idx].contiguous(), v_pool=b.v_pool[idx].contiguous(),
+                     k_scales=b.k_scales, v_scales=b.v_scales)
     c.q_decode = b.q_decode[seqs].contiguous()
     c.block_tables_decode = new_t.to(b.k_pool.device)
     c.context_lens_decode = lens.to(b.k_pool.device)

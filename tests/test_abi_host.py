@@ -58,7 +58,7 @@ def test_desc_struct_matches_header_layout():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in B.PaKvDesc._fields_]
-    assert ctypes.sizeof(B.PaKvDesc) == 48
+    assert ctypes.sizeof(B.PaKvDesc) == 64
 
 
 def _desc(**kw):
@@ -121,6 +121,19 @@ def test_fp16_cache_is_accepted_and_ignores_scales(lib):
         assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK, B.last_error()
     d = _desc(kv_dtype=B.PA_KV_F16 + 1)
     assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+
+
+def test_per_head_scales_only_with_fp8_and_aligned(lib):
+    d = _desc(kv_dtype=B.PA_KV_BF16)
+    d.k_scales = 0x1000
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+    assert "FP8" in B.last_error()
+    d = _desc(kv_dtype=B.PA_KV_FP8_E4M3)
+    d.v_scales = 0x1002
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+    assert "aligned" in B.last_error()
+    d.v_scales = 0x1004
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK
 
 
 def test_decode_argument_errors(lib):
