@@ -72,6 +72,10 @@ def _load():
         lib.pa_oracle_decode.restype = None
         lib.pa_oracle_prefill.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, P, P, I, I, P, I, P, P]
         lib.pa_oracle_prefill.restype = None
+        lib.pa_oracle_prefix.argtypes = [I, I, I, I, I, P, P, P, P, P, I, P, I, F, F, F, P, P, P, I, P, P]
+        lib.pa_oracle_prefix.restype = None
+        lib.pa_oracle_copy_blocks.argtypes = [I, I, I, I, P, P, I, P, P]
+        lib.pa_oracle_copy_blocks.restype = None
         lib.pa_oracle_merge.argtypes = [P, P, I, I, P, P]
         lib.pa_oracle_merge.restype = None
         _lib = lib
@@ -228,6 +232,47 @@ def prefill(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_
                           float(scale), float(k_scale), float(v_scale), ksp, vsp, int(window), int(chunk),
                           None if pp is None else _ptr(pp), n, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def prefix(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, q, query_start_loc, k_cache, v_cache,
+           block_tables, prefix_lens, scale, k_scale=1.0, v_scale=1.0, pairs=None, k_scales=None, v_scales=None):
+    """Shared-prefix attention of query groups (group j: rows
+    [query_start_loc[j], query_start_loc[j+1]) over the prefix_lens[j] tokens
+    of block_tables[j], no causal mask).  Returns (out [n, D], lse [n])."""
+    lib = _load()
+    ksa, ksp = _scales(k_scales)
+    vsa, vsp = _scales(v_scales)
+    qn = _np(q, np.uint16)
+    qsl = _np(query_start_loc, np.int32)
+    kc = _cache_np(k_cache, kv_dtype)
+    vc = _cache_np(v_cache, kv_dtype)
+    bt = _np(block_tables, np.int32)
+    pl = _np(prefix_lens, np.int32)
+    G = int(pl.shape[0])
+    if pairs is None:
+        n, pp = int(qsl[G]) * num_q_heads, None
+    else:
+        pp = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+        n = int(pp.shape[0])
+    out = np.zeros((n, head_dim), np.float64)
+    lse = np.zeros(n, np.float64)
+    lib.pa_oracle_prefix(kv_dtype, block_size, num_kv_heads, num_q_heads, head_dim, _ptr(qn), _ptr(qsl),
+                         _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(pl), G, float(scale),
+                         float(k_scale), float(v_scale), ksp, vsp, None if pp is None else _ptr(pp), n,
+                         _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def copy_blocks(kv_dtype, block_size, num_kv_heads, head_dim, src_blocks, dst_blocks, k_cache, v_cache):
+    """Copy-on-write of whole blocks into copies of the caches; returns (k_cache, v_cache)."""
+    lib = _load()
+    kc = _cache_np(k_cache, kv_dtype).copy()
+    vc = _cache_np(v_cache, kv_dtype).copy()
+    src = _np(src_blocks, np.int32)
+    dst = _np(dst_blocks, np.int32)
+    lib.pa_oracle_copy_blocks(2 if kv_dtype in (KV_BF16, KV_F16) else 1, block_size, num_kv_heads, head_dim,
+                              _ptr(src), _ptr(dst), int(src.shape[0]), _ptr(kc), _ptr(vc))
+    return kc, vc
 
 
 def merge(part_o, part_lse):

@@ -434,6 +434,62 @@ void pa_oracle_prefill(int kv_dtype, int block_size, int num_kv_heads, int num_q
   }
 }
 
+/* ------------------------------------------------ shared-prefix (cascade) */
+
+/*
+ * Attention of groups of queries over a shared prefix (cascade attention:
+ * the pages a prefix-cache hit binds to several sequences -- "Zero-Copy Cache
+ * Hits" of "1. Technical Mechanics of the Radix Cache" -- attended once for
+ * all of them; the result is merged with each sequence's own suffix by the
+ * log-sum-exp merge below).  Group j owns the packed query rows
+ * [query_start_loc[j], query_start_loc[j+1]) and the prefix of prefix_lens[j]
+ * tokens behind block_tables[j]; every query of the group attends all of it
+ * (the queries come after the prefix, so no causal mask applies inside it).
+ * pairs: optional (row, q head) list as in prefill.
+ */
+void pa_oracle_prefix(int kv_dtype, int block_size, int num_kv_heads, int num_q_heads, int head_dim,
+                      const uint16_t *q, const int32_t *query_start_loc, const void *k_cache,
+                      const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *prefix_lens, int num_groups, float scale, float k_scale,
+                      float v_scale, const float *k_scales, const float *v_scales,
+                      const int32_t *pairs, int num_pairs, double *out, double *lse) {
+  int g = num_q_heads / num_kv_heads;
+  int num_rows = query_start_loc[num_groups];
+  int total = pairs ? num_pairs : num_rows * num_q_heads;
+  for (int i = 0; i < total; ++i) {
+    int r = pairs ? pairs[2 * i] : i / num_q_heads;
+    int h = pairs ? pairs[2 * i + 1] : i % num_q_heads;
+    int j = 0;
+    while (j + 1 <= num_groups && query_start_loc[j + 1] <= r) ++j;
+    const uint16_t *q_vec = q + ((int64_t)r * num_q_heads + h) * head_dim;
+    const int32_t *row = block_tables + (int64_t)j * max_blocks_per_seq;
+    pa_oracle_attend_range(kv_dtype, block_size, num_kv_heads, head_dim, q_vec, k_cache, v_cache,
+                           row, h / g, 0, prefix_lens[j], scale, k_scales ? k_scales[h / g] : k_scale,
+                           v_scales ? v_scales[h / g] : v_scale, out + (int64_t)i * head_dim, lse + i);
+  }
+}
+
+/* ----------------------------------------------------------- block copies */
+
+/*
+ * Copy-on-write of whole pages: for every pair i, block dst_blocks[i] of both
+ * caches receives the contents of block src_blocks[i] (all kv heads, all
+ * slots), so that a sequence about to write into a page it shares with others
+ * (the partly filled last page of a prefix-cache hit) gets a private copy.
+ * elem_bytes: 2 for bf16 / fp16, 1 for the 8-bit formats.
+ */
+void pa_oracle_copy_blocks(int elem_bytes, int block_size, int num_kv_heads, int head_dim,
+                           const int32_t *src_blocks, const int32_t *dst_blocks, int num_pairs,
+                           void *k_cache, void *v_cache) {
+  int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elem_bytes;
+  for (int i = 0; i < num_pairs; ++i) {
+    memcpy((char *)k_cache + dst_blocks[i] * block_bytes, (char *)k_cache + src_blocks[i] * block_bytes,
+           (size_t)block_bytes);
+    memcpy((char *)v_cache + dst_blocks[i] * block_bytes, (char *)v_cache + src_blocks[i] * block_bytes,
+           (size_t)block_bytes);
+  }
+}
+
 /* ----------------------------------------------------------------- merge */
 
 /*

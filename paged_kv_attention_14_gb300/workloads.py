@@ -398,3 +398,67 @@ def random_prefill(seed: int, q_lens, ctx_lens, Hq, Hkv, D, kv_dtype=KV_BF16, sc
     b.context_lens_prefill = lens.to(device)
     b.query_start_loc = qsl.to(device)
     return b
+
+
+def shared_prefix_decode(seed: int, group_sizes, prefix_lens, suffix_lens, Hq, Hkv, D, kv_dtype=KV_BF16,
+                         scale=None, device="cpu", poison=True) -> PagedBatch:
+    """Decode batch whose sequences come in groups sharing a prefix (a
+    prefix-cache hit binds every sequence of group j to the same first
+    prefix_lens[j] / 16 physical blocks; prefixes are whole blocks).  Sequence
+    i of the batch (groups in order) has prefix_lens[j] + suffix_lens[i]
+    tokens.  Besides the usual decode fields, ``meta["cascade"]`` holds the
+    split a cascade needs: per group its query rows (query_start_loc over the
+    batch's sequences), prefix block table and length; per sequence its
+    suffix block table (its own blocks) and length."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    B = BLOCK_SIZE
+    assert all(p % B == 0 for p in prefix_lens), "shared prefixes are whole blocks"
+    S = sum(group_sizes)
+    assert len(suffix_lens) == S
+    g_cpu = _gen(seed, "cpu")
+    pre_blocks = [p // B for p in prefix_lens]
+    suf_blocks = [(int(x) + B - 1) // B for x in suffix_lens]
+    needed = sum(pre_blocks) + sum(suf_blocks)
+    NB = _pool_size(needed) + 2
+    perm = torch.randperm(NB, generator=g_cpu).to(torch.int32)
+    used = 0
+    pre_ids = []
+    for nbp in pre_blocks:
+        pre_ids.append(perm[used:used + nbp])
+        used += nbp
+    MBp = max(max(pre_blocks), 1)
+    MBs = max(max(suf_blocks), 1)
+    prefix_tables = torch.full((len(group_sizes), MBp), -1, dtype=torch.int32)
+    for j, ids in enumerate(pre_ids):
+        prefix_tables[j, :len(ids)] = ids
+    tables = torch.full((S, MBp + MBs), -1, dtype=torch.int32)
+    suffix_tables = torch.full((S, MBs), -1, dtype=torch.int32)
+    lens = torch.zeros(S, dtype=torch.int32)
+    qsl = torch.zeros(len(group_sizes) + 1, dtype=torch.int32)
+    i = 0
+    for j, n in enumerate(group_sizes):
+        for _ in range(n):
+            own = perm[used:used + suf_blocks[i]]
+            used += suf_blocks[i]
+            tables[i, :pre_blocks[j]] = pre_ids[j]
+            tables[i, pre_blocks[j]:pre_blocks[j] + suf_blocks[i]] = own
+            suffix_tables[i, :suf_blocks[i]] = own
+            lens[i] = prefix_lens[j] + int(suffix_lens[i])
+            i += 1
+        qsl[j + 1] = qsl[j] + n
+    b = PagedBatch(name=f"shared-prefix decode seed {seed}", block_size=B, num_q_heads=Hq, num_kv_heads=Hkv,
+                   head_dim=D, kv_dtype=kv_dtype, scale=_f32(scale), k_scale=1.0, v_scale=1.0, num_blocks=NB,
+                   k_pool=None, v_pool=None)
+    g = _gen(seed + 7, device)
+    b.q_decode = _randn((S, Hq, D), g, device, act_dtype(kv_dtype))
+    readable = _readable_mask(NB, B, [(tables, lens)])
+    _fill_pool(b, g, device, poison, readable, None)
+    b.block_tables_decode = tables.to(device)
+    b.context_lens_decode = lens.to(device)
+    b.meta["cascade"] = dict(query_start_loc=qsl.to(device), prefix_tables=prefix_tables.to(device),
+                             prefix_lens=torch.tensor(prefix_lens, dtype=torch.int32, device=device),
+                             suffix_tables=suffix_tables.to(device),
+                             suffix_lens=torch.tensor([int(x) for x in suffix_lens], dtype=torch.int32,
+                                                      device=device))
+    return b

@@ -579,3 +579,74 @@ def _oracle_prefill_local(b: W.PagedBatch, window, chunk):
     return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill,
                           b.query_start_loc, kc, vc, b.block_tables_prefill, b.context_lens_prefill,
                           b.scale, b.k_scale, b.v_scale, window=window, chunk=chunk)
+
+
+# ---------------------------------------------------- shared prefix (cascade)
+
+def _cascade_batch(kv=W.KV_BF16):
+    return W.shared_prefix_decode(71, [3, 1, 2], [32, 16, 64], [1, 15, 16, 40, 7, 33], 4, 2, 64, kv_dtype=kv)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_F16])
+def test_prefix_matches_bruteforce_sdpa_without_mask(kv):
+    b = _cascade_batch(kv)
+    c = b.meta["cascade"]
+    code = _KV16[kv]
+    out, lse = oracle.prefix(code, 16, 2, 4, 64, b.q_decode, c["query_start_loc"], b.k_pool, b.v_pool,
+                             c["prefix_tables"], c["prefix_lens"], b.scale)
+    kf, vf = _bf16_to_f64(b.k_pool), _bf16_to_f64(b.v_pool)
+    qf = _bf16_to_f64(b.q_decode)
+    qsl = c["query_start_loc"].numpy()
+    for j in range(3):
+        P = int(c["prefix_lens"][j])
+        rows = np.arange(qsl[j], qsl[j + 1])
+        for h in range(4):
+            K = _dense_kv(kf, c["prefix_tables"][j].numpy(), P, h // 2)
+            V = _dense_kv(vf, c["prefix_tables"][j].numpy(), P, h // 2)
+            ref = _sdpa(qf[rows, h], K, V, b.scale)
+            np.testing.assert_allclose(out[rows * 4 + h], ref, atol=1e-12, rtol=0)
+
+
+def test_cascade_prefix_then_suffix_merged_equals_full_decode():
+    """Closed form of the cascade: attention over [0, L) is the log-sum-exp
+    merge of attention over the shared prefix and over the own suffix."""
+    b = _cascade_batch()
+    c = b.meta["cascade"]
+    full, full_lse = oracle.decode(BF16, 16, 2, 4, 64, b.q_decode, b.k_pool, b.v_pool, b.block_tables_decode,
+                                   b.context_lens_decode, b.scale)
+    pre, pre_lse = oracle.prefix(BF16, 16, 2, 4, 64, b.q_decode, c["query_start_loc"], b.k_pool, b.v_pool,
+                                 c["prefix_tables"], c["prefix_lens"], b.scale)
+    suf, suf_lse = oracle.decode(BF16, 16, 2, 4, 64, b.q_decode, b.k_pool, b.v_pool, c["suffix_tables"],
+                                 c["suffix_lens"], b.scale)
+    for i in range(full.shape[0]):
+        o, l = oracle.merge(np.stack([pre[i], suf[i]]), np.array([pre_lse[i], suf_lse[i]]))
+        np.testing.assert_allclose(o, full[i], atol=1e-12, rtol=0)
+        assert abs(l - full_lse[i]) < 1e-12
+
+
+def test_prefix_of_zero_tokens_is_empty():
+    b = _cascade_batch()
+    c = b.meta["cascade"]
+    out, lse = oracle.prefix(BF16, 16, 2, 4, 64, b.q_decode, c["query_start_loc"], b.k_pool, b.v_pool,
+                             c["prefix_tables"], torch.zeros(3, dtype=torch.int32), b.scale)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+
+
+@pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8])
+def test_copy_blocks_is_a_whole_block_copy(kv):
+    g = torch.Generator().manual_seed(9)
+    NB, H, D = 12, 3, 64
+    if kv == W.KV_BF16:
+        k = torch.randn(NB, H, 16, D, generator=g).to(torch.bfloat16)
+        v = torch.randn(NB, H, 16, D, generator=g).to(torch.bfloat16)
+        kn, vn = k.view(torch.int16).numpy().view(np.uint16), v.view(torch.int16).numpy().view(np.uint16)
+        code = BF16
+    else:
+        kn = torch.randint(0, 256, (NB, H, 16, D), generator=g, dtype=torch.uint8).numpy()
+        vn = torch.randint(0, 256, (NB, H, 16, D), generator=g, dtype=torch.uint8).numpy()
+        code = FP8
+    src, dst = np.array([3, 0, 7], np.int32), np.array([9, 11, 4], np.int32)
+    kc, vc = oracle.copy_blocks(code, 16, H, D, src, dst, kn, vn)
+    ref_k, ref_v = kn.copy(), vn.copy()
+    ref_k[dst], ref_v[dst] = kn[src], vn[src]
+    assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
