@@ -225,6 +225,56 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
                            float scale, pa_stream_t stream);
 
 /*
+ * Shared-prefix (cascade) attention.  A prefix-cache hit binds several
+ * sequences to the same physical pages ("Zero-Copy Cache Hits" of "1.
+ * Technical Mechanics of the Radix Cache"); their queries can attend that
+ * prefix together, reading it once per kv head instead of once per sequence,
+ * and then merge the result with each sequence's own suffix (pa_decode over
+ * the suffix's blocks) by pa_merge_partials.  Group j owns the packed query
+ * rows [query_start_loc[j], query_start_loc[j+1]) and the prefix of
+ * prefix_lens[j] tokens behind prefix_tables[j]; every query of the group
+ * attends all of it (no causal mask: the queries come after the prefix).
+ * The prefix keys are cut into num_splits splits of c tokens each, c =
+ * ceil(max_prefix_len / num_splits) rounded up to a multiple of 128; split i
+ * covers keys [i c, min(prefix_len, (i + 1) c)) and is computed by its own
+ * CTAs, so that a few long prefixes still fill the GPU.  Split i of row r,
+ * head h is written to slot i of out_slots:
+ *   q   : [query_start_loc[num_groups]][num_q_heads][head_dim] (q's type as in
+ *         pa_prefill_chunk)
+ *   out : [rows][num_q_heads][out_slots][head_dim] fp32, each split's result
+ *         normalised by its own sum; lse : [rows][num_q_heads][out_slots]
+ *         fp32, natural log, required.  A split without keys (an empty or
+ *         short prefix) gets out = 0 and lse = -inf, which drop out of the
+ *         merge.  Slots >= num_splits are left untouched, so out / lse can be
+ *         pa_merge_partials' part_o / part_lse with the suffix in the last slot.
+ *   num_splits : >= 1; out_slots : >= num_splits, or 0 for num_splits.
+ *   prefix_tables : int32 [num_groups][max_blocks_per_prefix]
+ *   prefix_lens   : int32 [num_groups]; max_prefix_len bounds them (host).
+ * Local attention does not apply (sliding_window and attention_chunk must be
+ * 0).  The kernel is the one pa_prefill_chunk would run for the descriptor.
+ */
+PA_API pa_status pa_prefix_attention(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                                     const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                                     const int32_t *prefix_tables, int32_t max_blocks_per_prefix,
+                                     const int32_t *prefix_lens, int32_t num_groups, int32_t max_q_len,
+                                     int32_t max_prefix_len, int32_t num_splits, int32_t out_slots, float scale,
+                                     pa_stream_t stream);
+
+/*
+ * Copy-on-write of whole pages: for every i < num_pairs, block dst_blocks[i]
+ * of both caches receives the contents of block src_blocks[i] (every kv head
+ * and slot), so that a sequence about to write into a page it shares with
+ * other sequences (the partly filled last page of a prefix-cache hit) gets a
+ * private copy first.
+ *   src_blocks, dst_blocks : int32 [num_pairs] device arrays of block ids in
+ *                            [0, num_blocks); no dst may repeat or appear
+ *                            among the srcs (copies of one call race).
+ * num_pairs == 0 enqueues nothing and returns PA_OK.
+ */
+PA_API pa_status pa_copy_blocks(const pa_kv_desc *desc, void *k_cache, void *v_cache, const int32_t *src_blocks,
+                                const int32_t *dst_blocks, int32_t num_pairs, pa_stream_t stream);
+
+/*
  * Merge of attention results over disjoint key ranges (split-KV pieces, or a
  * shared prefix and a private suffix), by log-sum-exp weighting:
  *   M = max_p lse_p,  w_p = exp(lse_p - M),

@@ -40,7 +40,8 @@ PA_PREFILL_TCGEN05 = 2
 
 #: every symbol include/pa.h declares
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
-            "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static")
+            "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
+            "pa_copy_blocks")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -97,6 +98,10 @@ def load(path: Optional[str] = None):
         lib.pa_decode.restype = ctypes.c_int
         lib.pa_prefill_chunk.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P]
         lib.pa_prefill_chunk.restype = ctypes.c_int
+        lib.pa_prefix_attention.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, F, P]
+        lib.pa_prefix_attention.restype = ctypes.c_int
+        lib.pa_copy_blocks.argtypes = [D, P, P, P, P, I32, P]
+        lib.pa_copy_blocks.restype = ctypes.c_int
         lib.pa_merge_partials.argtypes = [P, P, P, P, P, I32, I32, I32, I32, P]
         lib.pa_merge_partials.restype = ctypes.c_int
         lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
@@ -234,6 +239,40 @@ def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, 
                                    _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
                                    _ptr(context_lens, _I32, "context_lens"), S, int(max_q_len),
                                    int(max_context_len), float(scale), _stream(stream)))
+
+
+def pa_prefix_attention(desc: PaKvDesc, out, lse, q, query_start_loc, k_cache, v_cache, prefix_tables,
+                        prefix_lens, max_q_len: int, max_prefix_len: int, scale: float, num_splits: int = 1,
+                        out_slots: int = 0, stream=None):
+    """Shared-prefix (cascade) attention of query groups: q ``[Nq, Hq, D]`` ->
+    out ``[Nq, Hq, out_slots, D]`` fp32 and lse ``[Nq, Hq, out_slots]``, split
+    i of the prefix keys in slot i (group j: rows query_start_loc[j] ..
+    query_start_loc[j+1] over its prefix, no mask).  With one split and
+    out_slots 0 the outputs may be ``[Nq, Hq, D]`` / ``[Nq, Hq]``."""
+    G = int(prefix_lens.shape[0])
+    _check(load().pa_prefix_attention(ctypes.byref(desc), _ptr(out, _F32, "out"), _ptr(lse, _F32, "lse"),
+                                      _ptr(q, _act(desc), "q"), _ptr(query_start_loc, _I32, "query_start_loc"),
+                                      _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                      _ptr(prefix_tables, _I32, "prefix_tables"), int(prefix_tables.shape[1]),
+                                      _ptr(prefix_lens, _I32, "prefix_lens"), G, int(max_q_len),
+                                      int(max_prefix_len), int(num_splits), int(out_slots), float(scale),
+                                      _stream(stream)))
+
+
+def prefix_splits(num_groups: int, num_kv_heads: int, q_tiles: int, max_prefix_len: int, sm_count: int) -> int:
+    """A key-split count for pa_prefix_attention that gives about one CTA per
+    SM: groups x kv heads x query tiles x splits ~ sm_count, each split at
+    least 512 keys."""
+    base = max(1, num_groups * num_kv_heads * q_tiles)
+    return max(1, min(sm_count // base if base < sm_count else 1, max(1, max_prefix_len // 512)))
+
+
+def pa_copy_blocks(desc: PaKvDesc, k_cache, v_cache, src_blocks, dst_blocks, stream=None):
+    """Copy-on-write: block dst_blocks[i] of both caches gets block src_blocks[i]."""
+    _check(load().pa_copy_blocks(ctypes.byref(desc), _ptr(k_cache, _CACHE, "k_cache"),
+                                 _ptr(v_cache, _CACHE, "v_cache"), _ptr(src_blocks, _I32, "src_blocks"),
+                                 _ptr(dst_blocks, _I32, "dst_blocks"), int(src_blocks.shape[0]),
+                                 _stream(stream)))
 
 
 def pa_merge_partials(out, part_o, part_lse, num_parts=None, lse_out=None, stream=None):

@@ -168,6 +168,67 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 
+pa_status pa_prefix_attention(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                              const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                              const int32_t *prefix_tables, int32_t max_blocks_per_prefix,
+                              const int32_t *prefix_lens, int32_t num_groups, int32_t max_q_len,
+                              int32_t max_prefix_len, int32_t num_splits, int32_t out_slots, float scale,
+                              pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (desc->sliding_window != 0 || desc->attention_chunk != 0)
+    return fail(PA_ERR_UNSUPPORTED, "shared-prefix attention takes no local attention (sliding_window, "
+                                    "attention_chunk must be 0)%s");
+  if (num_groups < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "num_groups and max_q_len must be >= 0%s");
+  if (num_groups == 0 || max_q_len == 0) return ok();
+  if (!out || !lse || !q || !query_start_loc || !k_cache || !v_cache || !prefix_tables || !prefix_lens)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, lse, q, query_start_loc, k_cache, v_cache, prefix_tables and prefix_lens must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(prefix_tables) & 3u) || (reinterpret_cast<uintptr_t>(prefix_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG,
+                "prefix_tables, prefix_lens, query_start_loc and lse must be 4-byte aligned%s");
+  if (max_blocks_per_prefix <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_prefix must be positive%s");
+  if (max_prefix_len < 0 || static_cast<int64_t>(max_prefix_len) > static_cast<int64_t>(max_blocks_per_prefix) * 16)
+    return fail(PA_ERR_INVALID_ARG, "max_prefix_len must lie in [0, max_blocks_per_prefix * block_size]%s");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
+  if (num_splits < 1 || num_splits > 4096) return fail(PA_ERR_INVALID_ARG, "num_splits must lie in [1, 4096]%s");
+  if (out_slots == 0) out_slots = num_splits;
+  if (out_slots < num_splits) return fail(PA_ERR_INVALID_ARG, "out_slots must be >= num_splits (or 0)%s");
+  if (static_cast<int64_t>(num_groups) * num_splits > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "num_groups * num_splits must be at most 65535%s");
+  const char *why = "";
+  st = pa::check_prefill(*desc, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  // keys per split: a whole number of 128-key tiles
+  int split_len = (max_prefix_len + num_splits - 1) / num_splits;
+  split_len = split_len < 128 ? 128 : (split_len + 127) / 128 * 128;
+  const cudaError_t e = pa::launch_prefill(*desc, out, lse, q, query_start_loc, k_cache, v_cache, prefix_tables,
+                                           max_blocks_per_prefix, prefix_lens, num_groups, max_q_len, scale,
+                                           reinterpret_cast<cudaStream_t>(stream), /*prefix_mode=*/true,
+                                           num_splits, split_len, out_slots);
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_copy_blocks(const pa_kv_desc *desc, void *k_cache, void *v_cache, const int32_t *src_blocks,
+                         const int32_t *dst_blocks, int32_t num_pairs, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs must be >= 0%s");
+  if (num_pairs == 0) return ok();
+  if (!k_cache || !v_cache || !src_blocks || !dst_blocks)
+    return fail(PA_ERR_INVALID_ARG, "k_cache, v_cache, src_blocks and dst_blocks must be non-NULL%s");
+  if (!aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(src_blocks) & 3u) || (reinterpret_cast<uintptr_t>(dst_blocks) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "src_blocks and dst_blocks must be 4-byte aligned%s");
+  const cudaError_t e = pa::launch_copy_blocks(*desc, k_cache, v_cache, src_blocks, dst_blocks, num_pairs,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
 pa_status pa_merge_partials(float *out, float *lse_out, const float *part_o,
                             const float *part_lse, const int32_t *num_parts, int32_t num_seqs,
                             int32_t num_heads, int32_t max_parts, int32_t head_dim,

@@ -37,17 +37,28 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
 
 pa_status check_prefill(const pa_kv_desc &d, const char **why);
 
+// prefix_mode: every query of sequence s comes after all context_lens[s]
+// keys and sees them all (shared-prefix / cascade attention) instead of the
+// causal chunk positions; the keys are cut into num_splits splits of
+// split_len (a multiple of 128) and split i writes output slot i of
+// out_slots per (row, head).
 cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const void *q,
                            const int32_t *query_start_loc, const void *k_cache,
                            const void *v_cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
-                           int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream);
+                           int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
+                           bool prefix_mode = false, int num_splits = 1, int split_len = 0, int out_slots = 1);
 
-// tcgen05 (tensor-memory) prefill kernel for bf16 caches.
+// tcgen05 (tensor-memory) prefill kernel for bf16 and fp16 caches.
 cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const void *q,
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                              int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream);
+                              int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
+                              bool prefix_mode, int num_splits, int split_len, int out_slots);
+
+// Copy-on-write of whole blocks (all kv heads) of both caches.
+cudaError_t launch_copy_blocks(const pa_kv_desc &d, void *k_cache, void *v_cache, const int32_t *src_blocks,
+                               const int32_t *dst_blocks, int32_t num_pairs, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -52,6 +52,10 @@ struct PrefillArgs {
   const float *v_scales;
   int window;  // local attention (see pa_kv_desc), 0: none
   int chunk;
+  int prefix_mode;  // 1: every query after all L keys, no causal mask (shared prefix)
+  int num_splits;   // prefix mode: key splits per sequence (grid.z = sequences x splits)
+  int split_len;    // prefix mode: keys per split (a multiple of 128)
+  int out_slots;    // prefix mode: output slots per (row, head); split i writes slot i
 };
 
 template <int D, int KVT, int NW>
@@ -77,7 +81,8 @@ template <int D, int KVT, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a) {
   using C = PrefillCfg<D, KVT, NW>;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int s = blockIdx.z;
+  const int split = a.prefix_mode ? static_cast<int>(blockIdx.z) % a.num_splits : 0;
+  const int s = a.prefix_mode ? static_cast<int>(blockIdx.z) / a.num_splits : static_cast<int>(blockIdx.z);
   const int kvh = blockIdx.y;
   const int qtile = gridDim.x - 1 - blockIdx.x;  // longest key ranges first
   const int qs = __ldg(a.query_start_loc + s);
@@ -86,12 +91,16 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   if (qt0 >= q_len) return;
   const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);  // queries of this CTA
-  const int base_pos = L - q_len + qt0;   // position of query qt0
-  const int kv_end = base_pos + nq;       // keys [kv_lo, kv_end) are needed
+  // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
+  // query comes after them all; otherwise query i sits at L - q_len + i
+  const int p_lo = a.prefix_mode ? min(L, split * a.split_len) : 0;
+  const int p_hi = a.prefix_mode ? min(L, p_lo + a.split_len) : 0;
+  const int base_pos = a.prefix_mode ? p_hi - 1 : L - q_len + qt0;  // position of query qt0
+  const int kv_end = a.prefix_mode ? p_hi : base_pos + nq;         // keys [kv_lo, kv_end) are needed
   // local attention: the CTA's earliest query sees keys from kv_lo on (the
   // first key never decreases with the position); its latest from lo_max
-  const int kv_lo = local_first_key(base_pos, a.window, a.chunk);
-  const int lo_max = local_first_key(kv_end - 1, a.window, a.chunk);
+  const int kv_lo = a.prefix_mode ? p_lo : local_first_key(base_pos, a.window, a.chunk);
+  const int lo_max = a.prefix_mode ? p_lo : local_first_key(kv_end - 1, a.window, a.chunk);
   const int kt0 = kv_lo / C::KT;
   const int n_tiles = (kv_end + C::KT - 1) / C::KT;
   const int tid = threadIdx.x;
@@ -201,10 +210,10 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   }
   // causal limit of each row (keys <= pos); invalid rows see no key; first
   // key of each row under local attention
-  const int pos_lo = ok_lo ? base_pos + row_query(r_lo) : -1;
-  const int pos_hi = ok_hi ? base_pos + row_query(r_hi) : -1;
-  const int first_lo = local_first_key(pos_lo, a.window, a.chunk);
-  const int first_hi = local_first_key(pos_hi, a.window, a.chunk);
+  const int pos_lo = ok_lo ? (a.prefix_mode ? base_pos : base_pos + row_query(r_lo)) : -1;
+  const int pos_hi = ok_hi ? (a.prefix_mode ? base_pos : base_pos + row_query(r_hi)) : -1;
+  const int first_lo = a.prefix_mode ? p_lo : local_first_key(pos_lo, a.window, a.chunk);
+  const int first_hi = a.prefix_mode ? p_lo : local_first_key(pos_hi, a.window, a.chunk);
   // the lowest position of any row of the CTA: tiles entirely below it need no mask
   const int pos_min = base_pos;
 
@@ -341,7 +350,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   const float inv_lo = l_lo > 0.f ? vscale / l_lo : 0.f;
   const float inv_hi = l_hi > 0.f ? vscale / l_hi : 0.f;
   if (ok_lo) {
-    const int64_t row = static_cast<int64_t>(qs + qt0 + row_query(r_lo)) * a.num_q_heads + kvh * g + r_lo % g;
+    const int64_t row = (static_cast<int64_t>(qs + qt0 + row_query(r_lo)) * a.num_q_heads + kvh * g + r_lo % g) *
+                            a.out_slots + split;
     float *o = a.out + row * D;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
@@ -349,7 +359,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
     if (a.lse && c4 == 0) a.lse[row] = (m_lo + log2f(l_lo)) * kLn2;
   }
   if (ok_hi) {
-    const int64_t row = static_cast<int64_t>(qs + qt0 + row_query(r_hi)) * a.num_q_heads + kvh * g + r_hi % g;
+    const int64_t row = (static_cast<int64_t>(qs + qt0 + row_query(r_hi)) * a.num_q_heads + kvh * g + r_hi % g) *
+                            a.out_slots + split;
     float *o = a.out + row * D;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n)
@@ -388,12 +399,14 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            const int32_t *query_start_loc, const void *k_cache,
                            const void *v_cache, const int32_t *block_tables,
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
-                           int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
+                           int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
+                           bool prefix_mode, int num_splits, int split_len, int out_slots) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
   if (impl == PA_PREFILL_TCGEN05)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                             context_lens, num_seqs, max_q_len, scale, stream);
+                             context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len,
+                             out_slots);
   const int g = d.num_q_heads / d.num_kv_heads;
   PrefillArgs a;
   a.out = out;
@@ -417,6 +430,10 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   a.v_scales = fp8 ? d.v_scales : nullptr;
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
+  a.prefix_mode = prefix_mode ? 1 : 0;
+  a.num_splits = prefix_mode ? num_splits : 1;
+  a.split_len = split_len;
+  a.out_slots = prefix_mode ? out_slots : 1;
   void *fn;
   size_t smem;
   if (d.head_dim == 128) {
@@ -440,7 +457,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   if (e != cudaSuccess) return e;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
-  dim3 grid(qtiles, d.num_kv_heads, num_seqs);
+  dim3 grid(qtiles, d.num_kv_heads, num_seqs * a.num_splits);
   void *args[] = {&a};
   return cudaLaunchKernel(fn, grid, dim3(kPrefillWarps * 32), args, smem, stream);
 }

@@ -92,6 +92,10 @@ struct Args {
   float qscale;
   int window;  // local attention (see pa_kv_desc), 0: none
   int chunk;
+  int prefix_mode;  // 1: every query after all L keys, no causal mask (shared prefix)
+  int num_splits;   // prefix mode: key splits per sequence (grid.z = sequences x splits)
+  int split_len;    // prefix mode: keys per split (a multiple of KT)
+  int out_slots;    // prefix mode: output slots per (row, head); split i writes slot i
 };
 
 // Error bits of the prefill kernel (a bounded wait ran out); device code
@@ -180,7 +184,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   int *s_last_k = s_abort + 1;  // last KV tile whose K copies the producer issued
   int *s_last_v = s_abort + 2;  // ... and whose V copies
 
-  const int s = blockIdx.z;
+  const int split = a.prefix_mode ? static_cast<int>(blockIdx.z) % a.num_splits : 0;
+  const int s = a.prefix_mode ? static_cast<int>(blockIdx.z) / a.num_splits : static_cast<int>(blockIdx.z);
   const int kvh = blockIdx.y;
   const int qtile = gridDim.x - 1 - blockIdx.x;  // longest key ranges first
   const int qs = __ldg(a.query_start_loc + s);
@@ -189,12 +194,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   if (qt0 >= q_len) return;
   const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);
-  const int base_pos = L - q_len + qt0;  // position of query qt0
-  const int kv_end = base_pos + nq;      // keys [kv_lo, kv_end) are needed
+  // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
+  // query comes after them all; otherwise query i sits at L - q_len + i
+  const int p_lo = a.prefix_mode ? min(L, split * a.split_len) : 0;
+  const int p_hi = a.prefix_mode ? min(L, p_lo + a.split_len) : 0;
+  const int base_pos = a.prefix_mode ? p_hi - 1 : L - q_len + qt0;  // position of query qt0
+  const int kv_end = a.prefix_mode ? p_hi : base_pos + nq;         // keys [kv_lo, kv_end) are needed
+  if (a.prefix_mode && p_hi <= p_lo) {
+    // no key in this split (an empty or short shared prefix): out = 0,
+    // lse = -inf, before any barrier or tensor memory is set up
+    for (int i = threadIdx.x; i < nq * a.g; i += NTHREADS) {
+      const int64_t row =
+          (static_cast<int64_t>(qs + qt0 + i / a.g) * a.num_q_heads + blockIdx.y * a.g + i % a.g) * a.out_slots + split;
+      for (int d = 0; d < D; d += 4) *reinterpret_cast<float4 *>(a.out + row * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.lse) a.lse[row] = -INFINITY;
+    }
+    return;
+  }
   // local attention: the CTA's earliest query sees keys from kv_lo on (the
   // first key never decreases with the position).  KV tiles j0 .. n_tiles - 1
   // are walked; the rings and barriers count iterations jj = j - j0.
-  const int kv_lo = local_first_key(base_pos, a.window, a.chunk);
+  const int kv_lo = a.prefix_mode ? p_lo : local_first_key(base_pos, a.window, a.chunk);
   const int j0 = kv_lo / KT;
   const int n_tiles = (kv_end + KT - 1) / KT;
   const int n_iter = n_tiles - j0;
@@ -400,8 +420,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const uint32_t o_col = C::O_COL + t * D;
     const int qi = R / g;
     const bool rv = R < rows_used && qi < nq;
-    const int pos = rv ? base_pos + qi : -1;  // keys <= pos are visible
-    const int first = local_first_key(pos, a.window, a.chunk);  // ... and keys >= first
+    const int pos = rv ? (a.prefix_mode ? base_pos : base_pos + qi) : -1;  // keys <= pos are visible
+    const int first = a.prefix_mode ? kv_lo : local_first_key(pos, a.window, a.chunk);  // ... and keys >= first
     const float qscale = a.qscale;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
@@ -557,7 +577,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float *orow = nullptr;
-      if (rv) orow = a.out + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * D;
+      const int64_t orow_i =
+          (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * a.out_slots + split;
+      if (rv) orow = a.out + orow_i * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
@@ -569,7 +591,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         }
       }
       if (rv && a.lse)
-        a.lse[static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)] = (m_ref + log2f(l)) * kLn2;
+        a.lse[orow_i] = (m_ref + log2f(l)) * kLn2;
     } else if (lane == 0) {
       *s_abort = 1;
     }
@@ -631,7 +653,7 @@ template <int D, int KVT>
 cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, const int32_t *query_start_loc,
                    const void *k_cache, const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
                    const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len, float scale,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, bool prefix_mode, int num_splits, int split_len, int out_slots) {
   Args a;
   memset(&a, 0, sizeof a);
   if (!make_map<D>(&a.kmap, k_cache, d) || !make_map<D>(&a.vmap, v_cache, d)) return cudaErrorInvalidValue;
@@ -649,6 +671,10 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   a.qscale = scale * kLog2e;
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
+  a.prefix_mode = prefix_mode ? 1 : 0;
+  a.num_splits = prefix_mode ? num_splits : 1;
+  a.split_len = split_len;
+  a.out_slots = prefix_mode ? out_slots : 1;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
   auto fn = &prefill_tc_kernel<D, KVT>;
@@ -658,7 +684,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs);
+  cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs * a.num_splits);
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = Cfg<D, KVT>::SMEM_LAUNCH;
   cfg.stream = stream;
@@ -684,17 +710,22 @@ extern "C" PA_API int pa_debug_prefill_trace_read(unsigned long long *host, int 
 cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const void *q,
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
-                              int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream) {
+                              int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
+                              bool prefix_mode, int num_splits, int split_len, int out_slots) {
   const bool f16 = d.kv_dtype == PA_KV_F16;
   if (d.head_dim == 128)
     return f16 ? pftc::launch<128, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                           max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream)
+                                           max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
+                                           split_len, out_slots)
                : pftc::launch<128, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream);
+                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
+                                           split_len, out_slots);
   return f16 ? pftc::launch<64, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                        max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream)
+                                        max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
+                                           split_len, out_slots)
              : pftc::launch<64, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                         max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream);
+                                         max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
+                                           split_len, out_slots);
 }
 
 }  // namespace pa

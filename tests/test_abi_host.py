@@ -136,6 +136,35 @@ def test_per_head_scales_only_with_fp8_and_aligned(lib):
     assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK
 
 
+def test_prefix_attention_and_copy_blocks_argument_errors(lib):
+    d = _desc()
+    P = ctypes.c_void_p
+    ok = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000)
+    # nothing to do
+    assert lib.pa_prefix_attention(ctypes.byref(d), *ok[:2], 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4, 0x8000,
+                                   0, 16, 64, 1, 0, 0.1, None) == B.PA_OK
+    # lse is required
+    assert lib.pa_prefix_attention(ctypes.byref(d), 0x1000, None, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4,
+                                   0x8000, 2, 16, 64, 1, 0, 0.1, None) == B.PA_ERR_INVALID_ARG
+    # prefix longer than its table
+    assert lib.pa_prefix_attention(ctypes.byref(d), *ok[:2], 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4, 0x8000,
+                                   2, 16, 65, 1, 0, 0.1, None) == B.PA_ERR_INVALID_ARG
+    # zero splits, or fewer slots than splits
+    assert lib.pa_prefix_attention(ctypes.byref(d), *ok[:2], 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4, 0x8000,
+                                   2, 16, 64, 0, 0, 0.1, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_prefix_attention(ctypes.byref(d), *ok[:2], 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4, 0x8000,
+                                   2, 16, 64, 3, 2, 0.1, None) == B.PA_ERR_INVALID_ARG
+    # local attention does not apply to a shared prefix
+    dw = _desc(sliding_window=8)
+    assert lib.pa_prefix_attention(ctypes.byref(dw), *ok[:2], 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 4, 0x8000,
+                                   2, 16, 64, 1, 0, 0.1, None) == B.PA_ERR_UNSUPPORTED
+    # block copies: none to do; NULL arrays; misaligned cache
+    assert lib.pa_copy_blocks(ctypes.byref(d), None, None, None, None, 0, None) == B.PA_OK
+    assert lib.pa_copy_blocks(ctypes.byref(d), 0x1000, 0x2000, None, 0x3000, 3, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(ctypes.byref(d), 0x1008, 0x2000, 0x3000, 0x4000, 3, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_copy_blocks(ctypes.byref(d), 0x1000, 0x2000, 0x3002, 0x4000, 3, None) == B.PA_ERR_INVALID_ARG
+
+
 def test_decode_argument_errors(lib):
     d = _desc()
     ok_ptrs = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000)
