@@ -56,10 +56,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
     # the decode kernel (split segments are merged inside it)
-    "decode": {"workload": 2, "bytes": 306_007_734,
-               "sha256": "e6b1557f485fecf67ee7b888797de6f57be18a6a486efbe9ca43339e2b2ac4a8",
+    "decode": {"workload": 2, "bytes": 306_021_236,
+               "sha256": "3886f3865061cd78dac892f12b70ce0c5c8b5125863f0e32fe59e5458a9e5e77",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
-    "prefill": {"workload": 5, "bytes": 46_295_106, "sha256": "341e3e145083b1f30129dd55e240d938754b81bc1a83734de218afa480e69ecb",
+    "prefill": {"workload": 5, "bytes": 46_282_802, "sha256": "e52cfcb27c5265ba09e4d627b54cddba2121615df53e0e4bf0d4031742e6bfbd",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
 }
 
