@@ -222,6 +222,9 @@ def _local_config(args) -> dict:
         d["kv_cache"] = "fp16"
     if args.per_head_scales:
         d["fp8_scales"] = "per kv head"
+    if args.workload == 5:
+        d["mixed_step"] = ("decode and prefill in order on one stream" if args.serial_mixed else
+                           "decode on a second stream beside the prefill, after the cache write")
     if args.sliding_window:
         d["sliding_window"] = args.sliding_window
     if args.attention_chunk:
@@ -333,11 +336,32 @@ def run_ours(args):
     def prefill(q, qs, bt, cl):
         B.pa_prefill_chunk(desc, pf_out, q, qs, kc, vc, bt, cl, pf_maxq, pf_maxL, b.scale)
 
+    # mixed step: after the cache write, the decode runs on a second stream
+    # beside the prefill, so that its CTAs take the SMs the prefill's last
+    # wave leaves idle (--serial-mixed issues them one after the other)
+    overlap = mixed and not args.serial_mixed
+    side = torch.cuda.Stream(device=dev) if overlap else None
+    ev_written = torch.cuda.Event()
+    ev_decoded = torch.cuda.Event()
+
+    def attend(dec_args, pf_args):
+        if overlap:
+            ev_written.record()
+            side.wait_event(ev_written)
+            with torch.cuda.stream(side):
+                decode(*dec_args)
+            ev_decoded.record(side)
+            prefill(*pf_args)
+            torch.cuda.current_stream().wait_event(ev_decoded)
+        else:
+            decode(*dec_args)
+            if mixed:
+                prefill(*pf_args)
+
     def step():
         B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
-        decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
-        if mixed:
-            prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
+        attend((b.q_decode, b.block_tables_decode, b.context_lens_decode),
+               (b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill))
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -418,10 +442,10 @@ def run_ours(args):
     def e2e_step():
         dev_buf.copy_(host_buf, non_blocking=True)
         B.pa_cache_write(desc, views["k_new"], views["v_new"], kc, vc, views["slot_mapping"])
-        decode(views["q_decode"], views["block_tables_decode"], views["context_lens_decode"])
+        attend((views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
+               (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
+                views["context_lens_prefill"]))
         if mixed:
-            prefill(views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
-                    views["context_lens_prefill"])
             pf_host.copy_(pf_out, non_blocking=True)
         out_host.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -648,6 +672,8 @@ def main():
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
     ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
                     help="8-bit cache format of workload 4 (same shapes)")
+    ap.add_argument("--serial-mixed", action="store_true",
+                    help="mixed step (workload 5): decode and prefill one after the other on one stream")
     ap.add_argument("--per-head-scales", action="store_true",
                     help="workload 4 with one FP8 scale per kv head (heads of different magnitudes)")
     ap.add_argument("--fp16", action="store_true",
