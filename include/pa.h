@@ -56,7 +56,10 @@
 extern "C" {
 #endif
 
-#define PA_ABI_VERSION 1
+/* 1: pa_kv_desc up to prefill_impl; cache write, decode, prefill, merge.
+ * 2: pa_kv_desc gains sliding_window, attention_chunk, k_scales, v_scales
+ *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks. */
+#define PA_ABI_VERSION 2
 
 /* Symbols of the shared library; everything else in it stays hidden. */
 #if defined(__GNUC__)

@@ -39,6 +39,8 @@ PA_PREFILL_MMA_SYNC = 1
 PA_PREFILL_TCGEN05 = 2
 
 #: every symbol include/pa.h declares
+#: PA_ABI_VERSION this binding is written against (pa_kv_desc layout, entry points)
+ABI_VERSION = 2
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
             "pa_copy_blocks")
@@ -106,6 +108,9 @@ def load(path: Optional[str] = None):
         lib.pa_merge_partials.restype = ctypes.c_int
         lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
         lib.pa_decode_static.restype = ctypes.c_int
+        if lib.pa_abi_version() != ABI_VERSION:
+            raise RuntimeError(f"{p} has ABI version {lib.pa_abi_version()}, this binding expects {ABI_VERSION}: "
+                               "rebuild it")
         if path is None:
             _lib = lib
         return lib
