@@ -81,8 +81,8 @@ typedef enum {
 
 typedef enum {
   PA_KV_BF16 = 0,     /* bf16 K/V, bit copies of the written values          */
-  PA_KV_FP8_E4M3 = 1, /* OCP E4M3 bytes with per-tensor fp32 scales        */
-  PA_KV_FP8_E5M2 = 2, /* OCP E5M2 bytes with per-tensor fp32 scales        */
+  PA_KV_FP8_E4M3 = 1, /* OCP E4M3 bytes, fp32 scales per tensor or kv head */
+  PA_KV_FP8_E5M2 = 2, /* OCP E5M2 bytes, fp32 scales per tensor or kv head */
   PA_KV_F16 = 3       /* fp16 K/V of an fp16 model: q and the written rows
                          are fp16 too; bit copies ("Block-Paged KV Cache
                          (FP8/FP16)")                                      */

@@ -8,8 +8,11 @@
 // forward bullet) over its "Block-Paged KV Cache (FP8/FP16)" (architecture
 // figure of "Building and Deploying vllm.cpp ..."), block size 16.  With FP8
 // pages ("fp8 halves page size to 1 byte per element", CLI table of the same
-// walkthrough) the E4M3 bytes are decoded inside the load and the per-tensor
-// scales are folded into the softmax scale (K) and the output (V).
+// walkthrough) the E4M3 / E5M2 bytes are decoded inside the load and the
+// scales (per tensor, or per kv head) are folded into the softmax scale (K)
+// and the output (V).  fp16 pages (an fp16 model) take fp16 MMAs.  Local
+// attention (sliding window, chunked-local) starts each sequence's stream at
+// the block of its first visible key.
 //
 // How (GB300 design, not taken from the pages):
 //  * Persistent grid, stream-K work split.  A segment is (sequence, group of
@@ -19,7 +22,8 @@
 //    within one block.  A range cuts a segment into at most two pieces per
 //    CTA; pieces are written to per-CTA slots and the last CTA to finish a
 //    segment (an atomic counter, no waiting) merges them by log-sum-exp in
-//    the same launch.
+//    the same launch.  Each CTA streams the piece at the end of its range
+//    first, so that most merges overlap the stream.
 //  * One producer warp streams KV with the TMA engine into an NS-stage
 //    shared-memory ring guarded by mbarriers.  In this cache layout the HG kv
 //    heads of one block are contiguous, so one copy moves a block for a whole
@@ -35,9 +39,9 @@
 //      of the group as N (padded to 8 or 16); P^T comes from the S^T
 //      accumulators by an in-register 8x8 transpose (movmatrix).  Tiles
 //      arrive 128B/64B-swizzled, so every ldmatrix is bank-conflict free.
-//      bf16 KV uses bf16 MMAs with the probabilities split into a bf16 hi + lo
-//      pair (near-fp32 accuracy); E4M3 KV is converted exactly to f16 in
-//      registers and uses f16 MMAs.  A separate epilogue warp folds the
+//      bf16 / fp16 KV uses MMAs of that type with the probabilities split into
+//      a hi + lo pair (near-fp32 accuracy); 8-bit KV is converted exactly to
+//      f16 in registers and uses f16 MMAs.  A separate epilogue warp folds the
 //      consumer warps' partial states of each finished piece and writes the
 //      output or the slot (and merges), so consumers never stop streaming.
 #pragma once

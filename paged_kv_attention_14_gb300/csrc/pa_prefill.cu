@@ -13,14 +13,18 @@
 // (query, head) pairs and every K/V tile is loaded once for the whole GQA
 // group.  64-key K/V tiles are gathered block by block through the block
 // table with 16-byte cp.async into XOR-swizzled shared memory (double
-// buffered), then QK^T and PV run on the tensor cores as bf16 m16n8k16 MMAs
-// with fp32 accumulators and online softmax in registers; the probabilities
-// enter PV as a bf16 hi + lo pair so the result keeps near-fp32 accuracy.  Keys past the
-// sequence end are zero-filled, so poisoned tails never reach an MMA; the
-// causal mask is applied only on tiles that cross the diagonal.  FP8 tiles
-// are staged raw and decoded to bf16 in shared memory (exact: every E4M3
-// value is a bf16 value), with k_scale folded into the softmax scale and
-// v_scale into the output.
+// buffered), then QK^T and PV run on the tensor cores as bf16 (fp16 for an
+// fp16 cache) m16n8k16 MMAs with fp32 accumulators and online softmax in
+// registers; the probabilities enter PV as a hi + lo pair so the result
+// keeps near-fp32 accuracy.  Keys past the sequence end are zero-filled, so
+// poisoned tails never reach an MMA; the causal mask is applied only on
+// tiles that cross the diagonal.  FP8 tiles are staged raw and decoded to
+// bf16 in shared memory (exact: every E4M3 / E5M2 value is a bf16 value),
+// with k_scale folded into the softmax scale and v_scale into the output
+// (per kv head where the cache has per-head scales).  Local attention
+// starts the key walk at the tile of the first visible key.  In prefix mode
+// (pa_prefix_attention) every query comes after all the keys of its split
+// of a shared prefix, and the outputs go to that split's part slot.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
