@@ -57,7 +57,7 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
     # the decode kernel (split segments are merged inside it)
     "decode": {"workload": 2, "bytes": 306_021_236,
-               "sha256": "3886f3865061cd78dac892f12b70ce0c5c8b5125863f0e32fe59e5458a9e5e77",
+               "sha256": "ad71555c11e126bb234633e31267180038cf03a69ed60903284b3f42e16bff6d",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     "prefill": {"workload": 5, "bytes": 46_282_802, "sha256": "e52cfcb27c5265ba09e4d627b54cddba2121615df53e0e4bf0d4031742e6bfbd",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
