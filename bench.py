@@ -89,6 +89,22 @@ def _peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def _max_over_ranks(vals, dev):
+    """Element-wise maximum over the ranks of per-rank values (times: the
+    slowest rank's), through the default process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def _job_throughput(world_size: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job rate of independent replicas: all ranks' units over the
+    slowest rank's time."""
+    return world_size * units_per_rank / seconds
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -411,9 +427,7 @@ def run_ours(args):
     dec_ms = sum(a.elapsed_time(c) for a, c in ev_d) / K2
     pf_ms = sum(a.elapsed_time(c) for a, c in ev_p) / K2 if mixed else 0.0
     if ws > 1:
-        t = torch.tensor([step_ms, dec_ms, pf_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, dec_ms, pf_ms = (float(x) for x in t)
+        step_ms, dec_ms, pf_ms = _max_over_ranks([step_ms, dec_ms, pf_ms], dev)
     assert int(wsp[:4].view(torch.int32)[0]) == 0, "decode kernel reported a wait timeout"
 
     # End to end through the public API: every step copies its inputs from one
@@ -465,13 +479,11 @@ def run_ours(args):
         tot += time.perf_counter() - t0
     e2e_s = tot / ke
     if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t[0])
+        (e2e_s,) = _max_over_ranks([e2e_s], dev)
 
     if rank == 0:
         peak, tc_peak, peak_kind = _peaks()
-        gbs = ws * kv_bytes / (step_ms * 1e-3) / 1e9
+        gbs = _job_throughput(ws, kv_bytes, step_ms * 1e-3) / 1e9
         dec_gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
         line = {
             "metric": METRIC,
@@ -499,7 +511,7 @@ def run_ours(args):
                          "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
                          "traffic": _traffic("decode", args.workload, local)},
-            "e2e": {"value": round(ws * kv_bytes / e2e_s / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
+            "e2e": {"value": round(_job_throughput(ws, kv_bytes, e2e_s) / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * K + (launches_per_step - 1) * K2,
             "clocks": clocks,
