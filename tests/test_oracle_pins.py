@@ -7,6 +7,7 @@ oracle (wrong GQA index, wrong block offset, a dropped scale, an off-by-one in
 the causal position, a sign in the merge, an exponent bias) fails one of them.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -650,3 +651,33 @@ def test_copy_blocks_is_a_whole_block_copy(kv):
     ref_k, ref_v = kn.copy(), vn.copy()
     ref_k[dst], ref_v[dst] = kn[src], vn[src]
     assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
+
+
+# ------------------------------------------------------------- golden fixtures
+
+_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_codes(name):
+    with open(os.path.join(_GOLDEN, name)) as f:
+        return {int(a, 16): float(b) for a, b in (line.split() for line in f)}
+
+
+def test_oracle_matches_its_golden_fixtures():
+    """tests/golden/ holds values written by make_golden.py from the oracle;
+    any change of the oracle's arithmetic shows here."""
+    for name, fn in (("e4m3_codes.txt", oracle.e4m3_decode), ("e5m2_codes.txt", oracle.e5m2_decode),
+                     ("f16_specials.txt", oracle.f16_decode)):
+        for c, v in _read_codes(name).items():
+            got = fn(c)
+            assert (math.isnan(v) and math.isnan(got)) or got == v, (name, c, got, v)
+    b = W.workload(1, poison=True)
+    out, lse = oracle.decode(BF16, 16, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode, b.k_pool, b.v_pool,
+                             b.block_tables_decode, b.context_lens_decode, b.scale)
+    with open(os.path.join(_GOLDEN, "workload1_decode.txt")) as f:
+        rows = [line.split() for line in f if not line.startswith("#")]
+    assert len(rows) == out.shape[0]
+    # exp / log come from the host's libm: equal to the last few ulps across hosts
+    for i, r in enumerate(rows):
+        assert abs(float(r[2]) - lse[i]) <= 1e-13 * max(1.0, abs(lse[i]))
+        np.testing.assert_allclose(out[i], np.array([float(x) for x in r[3:]]), rtol=1e-13, atol=1e-15)
