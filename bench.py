@@ -386,8 +386,8 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    # the raw nvidia-smi samples go to the file PA_BENCH_CLOCKS_CSV names, if any
+    sampler = ClockSampler(local, os.environ.get("PA_BENCH_CLOCKS_CSV") or None)
     sampler.start()
     if ws > 1:
         dist.barrier()
