@@ -377,7 +377,7 @@ def run_ours(args):
     def step():
         B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
         attend((b.q_decode, b.block_tables_decode, b.context_lens_decode),
-               (b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill))
+               (b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill) if mixed else None)
 
     for _ in range(args.warmup):
         if flush is not None:
@@ -458,7 +458,7 @@ def run_ours(args):
         B.pa_cache_write(desc, views["k_new"], views["v_new"], kc, vc, views["slot_mapping"])
         attend((views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
                (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
-                views["context_lens_prefill"]))
+                views["context_lens_prefill"]) if mixed else None)
         if mixed:
             pf_host.copy_(pf_out, non_blocking=True)
         out_host.copy_(out, non_blocking=True)
