@@ -219,6 +219,7 @@ PA_API pa_status pa_decode(const pa_kv_desc *desc, float *out, float *lse, const
  *   query_start_loc : int32 [num_seqs + 1], non-decreasing, starting at 0,
  *                     q_len <= context_lens[s].
  *   max_q_len : an upper bound of the q_len values (host value).
+ * num_seqs is at most 65535 per call (PA_ERR_UNSUPPORTED above).
  */
 PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const void *q,
                            const int32_t *query_start_loc, const void *k_cache,

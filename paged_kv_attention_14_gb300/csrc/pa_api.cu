@@ -146,6 +146,8 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
   if (st != PA_OK) return st;
   if (num_seqs < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and max_q_len must be >= 0%s");
   if (num_seqs == 0 || max_q_len == 0) return ok();
+  if (num_seqs > 65535)  // one grid row of CTAs per sequence
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk takes at most 65535 sequences per call%s");
   if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
     return fail(PA_ERR_INVALID_ARG,
                 "out, q, query_start_loc, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");

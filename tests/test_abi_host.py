@@ -165,6 +165,14 @@ def test_prefix_attention_and_copy_blocks_argument_errors(lib):
     assert lib.pa_copy_blocks(ctypes.byref(d), 0x1000, 0x2000, 0x3002, 0x4000, 3, None) == B.PA_ERR_INVALID_ARG
 
 
+def test_prefill_sequence_count_limit(lib):
+    d = _desc()
+    # more sequences than one grid dimension holds: rejected before any launch
+    assert lib.pa_prefill_chunk(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000,
+                                70000, 16, 64, 0.1, None) == B.PA_ERR_UNSUPPORTED
+    assert "65535" in B.last_error()
+
+
 def test_decode_argument_errors(lib):
     d = _desc()
     ok_ptrs = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000)
