@@ -229,3 +229,32 @@ def test_last_error_is_per_thread(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         B.load(str(tmp_path / "nope.so"))
+
+
+def test_header_is_valid_c_and_links_every_entry_point(tmp_path):
+    """A C99 caller: pa.h compiles with -Wall -Wextra -Werror, every declared
+    entry point links against the library, and the descriptor's size and field
+    offsets seen from C match the binding's."""
+    import shutil
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    names = _declared_functions()
+    fields = [f for f, _ in B.PaKvDesc._fields_]
+    src = tmp_path / "caller.c"
+    src.write_text(
+        "#include <stdio.h>\n#include <stddef.h>\n#include \"pa.h\"\n"
+        "int main(void) {\n"
+        "  void (*fns[])(void) = {" + ", ".join(f"(void (*)(void)){n}" for n in names) + "};\n"
+        "  printf(\"%zu %d\\n\", sizeof(fns) / sizeof(fns[0]), pa_abi_version());\n"
+        "  printf(\"%zu\\n\", sizeof(pa_kv_desc));\n"
+        + "".join(f"  printf(\"%zu\\n\", offsetof(pa_kv_desc, {f}));\n" for f in fields) +
+        "  return 0;\n}\n")
+    exe = tmp_path / "caller"
+    lib_dir = os.path.dirname(B.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER), str(src),
+                    "-o", str(exe), "-L", lib_dir, "-l:" + os.path.basename(B.LIB_PATH),
+                    "-Wl,-rpath," + lib_dir], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == len(names) and int(out[1]) == B.ABI_VERSION
+    assert int(out[2]) == ctypes.sizeof(B.PaKvDesc)
+    assert [int(x) for x in out[3:]] == [getattr(B.PaKvDesc, f).offset for f in fields]
