@@ -296,6 +296,7 @@ def run_ours(args):
     from paged_kv_attention_14_gb300 import build as pa_build
     from paged_kv_attention_14_gb300 import binding as B
     from paged_kv_attention_14_gb300 import workloads as W
+    from paged_kv_attention_14_gb300.step import MixedStep
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -346,38 +347,17 @@ def run_ours(args):
         # the timed kernels start instead of during them
         flush = _L2Flush(2 * l2_bytes, dev)
 
-    def decode(q, bt, cl):
-        B.pa_decode(desc, out, q, kc, vc, bt, cl, maxL, b.scale, wsp)
-
-    def prefill(q, qs, bt, cl):
-        B.pa_prefill_chunk(desc, pf_out, q, qs, kc, vc, bt, cl, pf_maxq, pf_maxL, b.scale)
-
     # mixed step: after the cache write, the decode runs on a second stream
     # beside the prefill, so that its CTAs take the SMs the prefill's last
     # wave leaves idle (--serial-mixed issues them one after the other)
-    overlap = mixed and not args.serial_mixed
-    side = torch.cuda.Stream(device=dev) if overlap else None
-    ev_written = torch.cuda.Event()
-    ev_decoded = torch.cuda.Event()
-
-    def attend(dec_args, pf_args):
-        if overlap:
-            ev_written.record()
-            side.wait_event(ev_written)
-            with torch.cuda.stream(side):
-                decode(*dec_args)
-            ev_decoded.record(side)
-            prefill(*pf_args)
-            torch.cuda.current_stream().wait_event(ev_decoded)
-        else:
-            decode(*dec_args)
-            if mixed:
-                prefill(*pf_args)
+    ms = MixedStep(desc, kc, vc, b.scale, decode_out=out, workspace=wsp, max_context_len_decode=maxL,
+                   prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
+                   max_context_len_prefill=pf_maxL if mixed else 0, overlap=not args.serial_mixed)
+    decode, prefill, attend = ms.decode, ms.prefill, ms.attend
 
     def step():
-        B.pa_cache_write(desc, b.k_new, b.v_new, kc, vc, b.slot_mapping)
-        attend((b.q_decode, b.block_tables_decode, b.context_lens_decode),
-               (b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill) if mixed else None)
+        ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
+           (b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill) if mixed else None)
 
     for _ in range(args.warmup):
         if flush is not None:

@@ -261,6 +261,42 @@ static int64_t cache_row(const int32_t *table_row, int block_size, int num_kv_he
 /* ---------------------------------------------------------- cache write */
 
 /*
+ * The 8-bit code of one bf16 input x under one scale: e4m3 / e5m2 of
+ * fl32(fl32(x) / scale).
+ */
+static uint8_t encode_bf16(int kv_dtype, uint16_t x, float scale) {
+  float q = bf16_bits_to_float(x) / scale;
+  return kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)q) : pa_oracle_e4m3_encode((double)q);
+}
+
+/*
+ * The code depends only on the 16 input bits and the scale, so a large write
+ * encodes each distinct (input, scale) once and looks the rest up: a memo of
+ * encode_bf16, filled lazily, valid for one (format, scale) at a time.  It
+ * changes how often the search runs, not what it returns.
+ */
+typedef struct {
+  int kv_dtype;
+  float scale;
+  uint8_t code[65536];
+  uint8_t done[65536];
+} encode_memo;
+
+static void memo_reset(encode_memo *m, int kv_dtype, float scale) {
+  m->kv_dtype = kv_dtype;
+  m->scale = scale;
+  memset(m->done, 0, sizeof m->done);
+}
+
+static uint8_t memo_encode(encode_memo *m, uint16_t x) {
+  if (!m->done[x]) {
+    m->code[x] = encode_bf16(m->kv_dtype, x, m->scale);
+    m->done[x] = 1;
+  }
+  return m->code[x];
+}
+
+/*
  * For each token i with slot_mapping[i] >= 0: block = slot / block_size,
  * offset = slot % block_size, and for every kv head h the cache row
  * (block, h, offset) receives enc(k[i][h][:]) (same for v).
@@ -273,6 +309,16 @@ void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int h
                            const uint16_t *k, const uint16_t *v, const int64_t *slot_mapping,
                            int num_tokens, float k_scale, float v_scale, const float *k_scales,
                            const float *v_scales, void *k_cache, void *v_cache) {
+  encode_memo *km = NULL, *vm = NULL;
+  if (kv_is_8bit(kv_dtype)) {
+    /* one memo per kv head and tensor (per-head scales differ by head) */
+    km = (encode_memo *)malloc(sizeof(encode_memo) * (size_t)num_kv_heads);
+    vm = (encode_memo *)malloc(sizeof(encode_memo) * (size_t)num_kv_heads);
+    for (int h = 0; h < num_kv_heads; ++h) {
+      memo_reset(&km[h], kv_dtype, k_scales ? k_scales[h] : k_scale);
+      memo_reset(&vm[h], kv_dtype, v_scales ? v_scales[h] : v_scale);
+    }
+  }
   for (int i = 0; i < num_tokens; ++i) {
     int64_t slot = slot_mapping[i];
     if (slot < 0) continue;
@@ -287,16 +333,14 @@ void pa_oracle_cache_write(int kv_dtype, int block_size, int num_kv_heads, int h
           ((uint16_t *)k_cache)[dst_row * head_dim + d] = ks[d];
           ((uint16_t *)v_cache)[dst_row * head_dim + d] = vs[d];
         } else {
-          float kq = bf16_bits_to_float(ks[d]) / (k_scales ? k_scales[h] : k_scale);
-          float vq = bf16_bits_to_float(vs[d]) / (v_scales ? v_scales[h] : v_scale);
-          uint8_t kc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)kq) : pa_oracle_e4m3_encode((double)kq);
-          uint8_t vc = kv_dtype == KV_FP8_E5M2 ? pa_oracle_e5m2_encode((double)vq) : pa_oracle_e4m3_encode((double)vq);
-          ((uint8_t *)k_cache)[dst_row * head_dim + d] = kc;
-          ((uint8_t *)v_cache)[dst_row * head_dim + d] = vc;
+          ((uint8_t *)k_cache)[dst_row * head_dim + d] = memo_encode(&km[h], ks[d]);
+          ((uint8_t *)v_cache)[dst_row * head_dim + d] = memo_encode(&vm[h], vs[d]);
         }
       }
     }
   }
+  free(km);
+  free(vm);
 }
 
 /* ----------------------------------------------------- one attention row */

@@ -1,0 +1,84 @@
+"""One continuous-batching step of the paged attention path.
+
+A step writes the new tokens' K/V into the cache through the slot mapping
+(``pa_cache_write``), then runs decode attention for the sequences that
+generate one token (``pa_decode``) and causal chunked-prefill attention for
+the sequences that bring a chunk of prompt tokens (``pa_prefill_chunk``) --
+the unified continuous batch of the vllm.cpp engine ("C++20 Continuous
+Batching Loop" in the "vllm.cpp ARCHITECTURE OVERVIEW" figure of "Building
+and Deploying vllm.cpp ..."; chunked prefill in the Engine core bullet of the
+vllm.cpp repository's "What's implemented").
+
+This module only orders the library's calls on CUDA streams; every step of
+the computation runs in the library's kernels.  Decode and prefill read
+disjoint outputs and only read the cache, so after the write they may run
+concurrently: ``overlap=True`` issues the decode on a second stream that
+waits for the write, beside the prefill on the caller's stream, so that the
+decode's CTAs take the SMs the prefill's last wave leaves idle.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class MixedStep:
+    """Issues one step: cache write, then decode and prefill.
+
+    Buffers that persist across steps (the caches, the decode workspace and
+    the outputs) are given once; the per-step inputs are passed to
+    ``__call__``.  Either part may be absent (``decode_out`` or
+    ``prefill_out`` None)."""
+
+    def __init__(self, desc: B.PaKvDesc, k_cache, v_cache, scale: float, *, decode_out=None, decode_lse=None,
+                 workspace=None, max_context_len_decode: int = 0, prefill_out=None, prefill_lse=None,
+                 max_q_len: int = 0, max_context_len_prefill: int = 0, overlap: bool = True):
+        self.desc = desc
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.scale = float(scale)
+        self.decode_out, self.decode_lse, self.workspace = decode_out, decode_lse, workspace
+        self.max_context_len_decode = int(max_context_len_decode)
+        self.prefill_out, self.prefill_lse = prefill_out, prefill_lse
+        self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
+        both = decode_out is not None and prefill_out is not None
+        self.overlap = bool(overlap) and both
+        dev = k_cache.device
+        self.side: Optional[torch.cuda.Stream] = torch.cuda.Stream(device=dev) if self.overlap else None
+        self.ev_written = torch.cuda.Event()
+        self.ev_decoded = torch.cuda.Event()
+
+    def decode(self, q, block_tables, context_lens, stream=None):
+        B.pa_decode(self.desc, self.decode_out, q, self.k_cache, self.v_cache, block_tables, context_lens,
+                    self.max_context_len_decode, self.scale, self.workspace, lse=self.decode_lse, stream=stream)
+
+    def prefill(self, q, query_start_loc, block_tables, context_lens, stream=None):
+        B.pa_prefill_chunk(self.desc, self.prefill_out, q, query_start_loc, self.k_cache, self.v_cache,
+                           block_tables, context_lens, self.max_q_len, self.max_context_len_prefill, self.scale,
+                           lse=self.prefill_lse, stream=stream)
+
+    def attend(self, dec_args, pf_args):
+        """Decode and prefill after a cache write already issued on the current stream."""
+        if self.overlap:
+            main = torch.cuda.current_stream()
+            self.ev_written.record(main)
+            self.side.wait_event(self.ev_written)
+            with torch.cuda.stream(self.side):
+                self.decode(*dec_args)
+            self.ev_decoded.record(self.side)
+            self.prefill(*pf_args)
+            main.wait_event(self.ev_decoded)
+            return
+        if dec_args is not None and self.decode_out is not None:
+            self.decode(*dec_args)
+        if pf_args is not None and self.prefill_out is not None:
+            self.prefill(*pf_args)
+
+    def __call__(self, k_new, v_new, slot_mapping, dec_args=None, pf_args=None):
+        """dec_args: (q, block_tables, context_lens); pf_args: (q, query_start_loc,
+        block_tables, context_lens)."""
+        if slot_mapping is not None and slot_mapping.numel() > 0:
+            B.pa_cache_write(self.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping)
+        self.attend(dec_args, pf_args)

@@ -3,7 +3,9 @@ the fp64 oracle on the same seeded inputs.  Nothing here computes attention:
 the expected values come from ``oracle`` only."""
 from __future__ import annotations
 
+import concurrent.futures as cf
 import math
+import os
 
 import numpy as np
 import torch
@@ -83,12 +85,42 @@ def gpu_decode(b: W.PagedBatch, caches=None, decode_impl: int = B.PA_DECODE_AUTO
     return out, lse
 
 
+def _threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def oracle_in_parallel(call, pairs, num_rows: int, num_heads: int):
+    """Runs ``call(pairs_chunk) -> (out [n, D], lse [n])`` of the oracle over
+    the (row, head) pairs given (None: every row x head, row-major), in
+    chunks on a thread per host core.  The oracle is a C library called
+    through ctypes, which releases the GIL, so the chunks run in parallel;
+    each pair is computed exactly as in a single call, and the results are
+    put back in order."""
+    if pairs is None:
+        i = np.arange(num_rows * num_heads, dtype=np.int64)
+        pairs = np.stack([i // num_heads, i % num_heads], axis=1)
+    pairs = np.ascontiguousarray(np.asarray(pairs, np.int32).reshape(-1, 2))
+    n = pairs.shape[0]
+    if n == 0:
+        return call(pairs)
+    bounds = np.linspace(0, n, min(n, 8 * _threads()) + 1).astype(np.int64)
+    chunks = [pairs[bounds[i]:bounds[i + 1]] for i in range(len(bounds) - 1) if bounds[i + 1] > bounds[i]]
+    with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        parts = list(ex.map(call, chunks))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
 def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
-    return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_decode.cpu(), kc, vc,
-                         b.block_tables_decode.cpu(), b.context_lens_decode.cpu(), b.scale, b.k_scale,
-                         b.v_scale, pairs=pairs, window=window, chunk=chunk, k_scales=_cpu(b.k_scales),
-                         v_scales=_cpu(b.v_scales))
+    q, bt, cl = b.q_decode.cpu(), b.block_tables_decode.cpu(), b.context_lens_decode.cpu()
+    ks, vs = _cpu(b.k_scales), _cpu(b.v_scales)
+
+    def call(pp):
+        return oracle.decode(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, q, kc, vc, bt, cl,
+                             b.scale, b.k_scale, b.v_scale, pairs=pp, window=window, chunk=chunk, k_scales=ks,
+                             v_scales=vs)
+
+    return oracle_in_parallel(call, pairs, int(cl.shape[0]), b.num_q_heads)
 
 
 def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO, window=0, chunk=0):
@@ -108,10 +140,16 @@ def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_A
 
 def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     kd, kc, vc = ocaches if ocaches is not None else oracle_caches(b)
-    return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, b.q_prefill.cpu(),
-                          b.query_start_loc.cpu(), kc, vc, b.block_tables_prefill.cpu(),
-                          b.context_lens_prefill.cpu(), b.scale, b.k_scale, b.v_scale, pairs=pairs,
-                          window=window, chunk=chunk, k_scales=_cpu(b.k_scales), v_scales=_cpu(b.v_scales))
+    q, qsl = b.q_prefill.cpu(), b.query_start_loc.cpu()
+    bt, cl = b.block_tables_prefill.cpu(), b.context_lens_prefill.cpu()
+    ks, vs = _cpu(b.k_scales), _cpu(b.v_scales)
+
+    def call(pp):
+        return oracle.prefill(kd, b.block_size, b.num_kv_heads, b.num_q_heads, b.head_dim, q, qsl, kc, vc, bt, cl,
+                              b.scale, b.k_scale, b.v_scale, pairs=pp, window=window, chunk=chunk, k_scales=ks,
+                              v_scales=vs)
+
+    return oracle_in_parallel(call, pairs, int(q.shape[0]), b.num_q_heads)
 
 
 def assert_close(got: torch.Tensor, want: np.ndarray, tol: float, what: str = ""):
@@ -121,31 +159,3 @@ def assert_close(got: torch.Tensor, want: np.ndarray, tol: float, what: str = ""
     worst = float(err.max()) if err.size else 0.0
     assert worst <= tol, f"{what}: max abs err {worst:.3e} > {tol:.1e} at {np.unravel_index(err.argmax(), err.shape)}"
     return worst
-
-
-def compact_decode_batch(b: W.PagedBatch, seqs) -> W.PagedBatch:
-    """The sub-batch of sequences ``seqs`` with only their blocks, renumbered:
-    same values and same attention result, small enough for the oracle's
-    E4M3 encoder.  Built from the generator's tensors (not from GPU results)."""
-    seqs = list(seqs)
-    lens = b.context_lens_decode[seqs].cpu()
-    tables = b.block_tables_decode[seqs].cpu()
-    used = []
-    for i, L in enumerate(lens.tolist()):
-        used += tables[i, :(L + 15) // 16].tolist()
-    uniq = sorted(set(used))
-    remap = {blk: j for j, blk in enumerate(uniq)}
-    new_t = torch.full_like(tables, -1)
-    for i, L in enumerate(lens.tolist()):
-        nb = (L + 15) // 16
-        new_t[i, :nb] = torch.tensor([remap[x] for x in tables[i, :nb].tolist()], dtype=torch.int32)
-    idx = torch.tensor(uniq, dtype=torch.int64, device=b.k_pool.device)
-    c = W.PagedBatch(name=b.name + " (subset)", block_size=b.block_size, num_q_heads=b.num_q_heads,
-                     num_kv_heads=b.num_kv_heads, head_dim=b.head_dim, kv_dtype=b.kv_dtype, scale=b.scale,
-                     k_scale=b.k_scale, v_scale=b.v_scale, num_blocks=len(uniq),
-                     k_pool=b.k_pool[idx].contiguous(), v_pool=b.v_pool[idx].contiguous(),
-                     k_scales=b.k_scales, v_scales=b.v_scales)
-    c.q_decode = b.q_decode[seqs].contiguous()
-    c.block_tables_decode = new_t.to(b.k_pool.device)
-    c.context_lens_decode = lens.to(b.k_pool.device)
-    return c

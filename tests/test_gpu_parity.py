@@ -14,7 +14,7 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
-from pa_helpers import (TOL, LSE_TOL, assert_close, compact_decode_batch, desc_of, gpu_caches, gpu_decode,
+from pa_helpers import (TOL, LSE_TOL, assert_close, desc_of, gpu_caches, gpu_decode,
                         gpu_prefill, oracle_caches, oracle_decode, oracle_prefill)
 
 pytestmark = pytest.mark.gpu
@@ -127,22 +127,19 @@ def test_decode_matches_oracle_on_workload(n, fp16, impl):
     _check_decode(b, impl=impl)
 
 
-def test_decode_matches_oracle_on_fp8_workload_subset():
+def test_decode_matches_oracle_on_fp8_workload():
+    """Workload 4 in full: the library's E4M3 cache write of the whole pool is
+    bit-exact against the oracle's encoding, and decode of all 128 sequences
+    x 40 heads is within the FP8 tolerance of the oracle over that cache."""
     b = W.workload(4, device=DEV, poison=True)
     caches = gpu_caches(b)
     out, lse = gpu_decode(b, caches=caches)
-    seqs = [0, 17, 63, 127] + [int(torch.argmax(b.context_lens_decode))]
-    sub = compact_decode_batch(b, seqs)
-    o_ref, l_ref = oracle_decode(sub)
-    assert_close(out[seqs], o_ref, TOL[W.KV_FP8], "out")
-    assert_close(lse[seqs], l_ref, LSE_TOL[W.KV_FP8], "lse")
-    # the GPU's E4M3 cache of those sequences' blocks equals the oracle's encoding
-    tables = b.block_tables_decode[seqs].cpu()
-    lens = b.context_lens_decode[seqs].cpu()
-    blocks = sorted({int(x) for i, L in enumerate(lens.tolist()) for x in tables[i, :(L + 15) // 16]})
-    _, okc, ovc = oracle_caches(sub)
-    assert np.array_equal(caches[0][blocks].cpu().numpy(), okc)
-    assert np.array_equal(caches[1][blocks].cpu().numpy(), ovc)
+    code, okc, ovc = oracle_caches(b)
+    assert np.array_equal(caches[0].cpu().numpy(), okc), "E4M3 K cache differs from the oracle's encoding"
+    assert np.array_equal(caches[1].cpu().numpy(), ovc), "E4M3 V cache differs from the oracle's encoding"
+    o_ref, l_ref = oracle_decode(b, ocaches=(code, okc, ovc))
+    assert_close(out, o_ref, TOL[W.KV_FP8], "out")
+    assert_close(lse, l_ref, LSE_TOL[W.KV_FP8], "lse")
 
 
 CASES = [
@@ -364,18 +361,48 @@ def test_mixed_step_write_then_decode_and_prefill(impl, fp16):
     o_ref, l_ref = oracle_decode(b, ocaches=oc)
     assert_close(dec_out, o_ref, TOL[kv], "decode out")
     assert_close(dec_lse, l_ref, LSE_TOL[kv], "decode lse")
-    # prefill: sampled rows (first, last and random rows of every chunk) x all heads
-    gen = torch.Generator().manual_seed(12)
-    rows = set()
-    for s in range(4):
-        base = s * 512
-        rows.update([base, base + 1, base + 63, base + 64, base + 511])
-        rows.update((base + torch.randint(0, 512, (6,), generator=gen)).tolist())
-    pairs = [(r, h) for r in sorted(rows) for h in range(32)]
-    o_ref, l_ref = oracle_prefill(b, ocaches=oc, pairs=pairs)
-    idx = torch.tensor([r * 32 + h for r, h in pairs])
-    assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[kv], "prefill out")
-    assert_close(pf_lse.reshape(-1)[idx], l_ref, LSE_TOL[kv], "prefill lse")
+    # prefill: every query row of the four chunks x all heads
+    o_ref, l_ref = oracle_prefill(b, ocaches=oc)
+    assert_close(pf_out, o_ref, TOL[kv], "prefill out")
+    assert_close(pf_lse, l_ref, LSE_TOL[kv], "prefill lse")
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_mixed_step_as_the_bench_runs_it(overlap):
+    """Workload 5 through MixedStep, the step bench.py times: cache write,
+    then the decode on a second stream beside the prefill (overlap) or both
+    on one stream; every decode and prefill output against the oracle."""
+    from paged_kv_attention_14_gb300.step import MixedStep
+    b = W.workload(5, device=DEV, poison=True)
+    d = desc_of(b)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    ws = B.decode_workspace(d, S, maxL, DEV)
+    dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
+    dec_lse = torch.full((S, 32), float("nan"), device=DEV)
+    pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
+    pf_lse = torch.full((b.q_prefill.shape[0], 32), float("nan"), device=DEV)
+    qsl = b.query_start_loc
+    ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, decode_lse=dec_lse, workspace=ws,
+                   max_context_len_decode=maxL, prefill_out=pf_out, prefill_lse=pf_lse,
+                   max_q_len=int((qsl[1:] - qsl[:-1]).max()),
+                   max_context_len_prefill=int(b.context_lens_prefill.max()), overlap=overlap)
+    assert ms.overlap == overlap
+    ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
+       (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill))
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32)[0]) == 0
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+                                b.k_pool.cpu(), b.v_pool.cpu())
+    assert np.array_equal(_bits(kc), ok) and np.array_equal(_bits(vc), ov)
+    oc = (oracle.KV_BF16, ok, ov)
+    o_ref, l_ref = oracle_decode(b, ocaches=oc)
+    assert_close(dec_out, o_ref, TOL[W.KV_BF16], "decode out")
+    assert_close(dec_lse, l_ref, LSE_TOL[W.KV_BF16], "decode lse")
+    o_ref, l_ref = oracle_prefill(b, ocaches=oc)
+    assert_close(pf_out, o_ref, TOL[W.KV_BF16], "prefill out")
+    assert_close(pf_lse, l_ref, LSE_TOL[W.KV_BF16], "prefill lse")
 
 
 def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
