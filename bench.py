@@ -30,6 +30,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -48,6 +49,9 @@ FP8_FORMATS = {"e4m3": "fp8_e4m3", "e5m2": "fp8_e5m2"}  # -> workloads.KV_FP8 / 
 
 
 FALLBACK_BF16_TFLOPS = 1900.0
+# the timed K-step measurement is repeated until the timed region lasts about
+# this long, so that the clock sampler sees it
+MIN_TIMED_S = 0.5
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
 # each hot kernel, averaged over the launches of one ncu launch-list capture
@@ -366,6 +370,22 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
+    # A repeat times exactly K steps.  The K-step measurement is repeated
+    # until the timed region lasts about MIN_TIMED_S, so that nvidia-smi
+    # clock samples fall inside it; the reported time per step is the
+    # median repeat's.
+    t_est = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_est[0].record()
+    for _ in range(3):
+        if flush is not None:
+            flush()
+        step()
+    t_est[1].record()
+    torch.cuda.synchronize()
+    est_s = max(t_est[0].elapsed_time(t_est[1]) * 1e-3 / 3, 1e-6)
+    R = max(1, min(2000, int(math.ceil(MIN_TIMED_S / (K * est_s)))))
+    K2 = max(10, K // 2)
+    R2 = max(1, min(2000, int(math.ceil(MIN_TIMED_S / 2 / (K2 * est_s)))))
     # the raw nvidia-smi samples go to the file PA_BENCH_CLOCKS_CSV names, if any
     sampler = ClockSampler(local, os.environ.get("PA_BENCH_CLOCKS_CSV") or None)
     sampler.start()
@@ -375,37 +395,48 @@ def run_ours(args):
     sampler.mark_start()
     # timed region 1: whole steps, CUDA events only at step boundaries (an
     # event between two kernels would cut the programmatic-dependent overlap
-    # of the decode launch with the cache write)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for i in range(K):
-        if flush is not None:
-            flush()
-        ev[i][0].record()
-        step()
-        ev[i][1].record()
+    # of the decode launch with the cache write); with an L2 flush between
+    # steps, events around each step leave the flush out
+    rep_ms = []
+    for _ in range(R):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            if flush is not None:
+                flush()
+            ev[i][0].record()
+            step()
+            ev[i][1].record()
+        rep_ms.append(ev)
     # timed region 2: the kernels of each entry point alone, events around
-    # each call (decode = decode kernel + merge kernel; prefill)
-    K2 = max(10, K // 2)
-    ev_d = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
-    ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
-    for i in range(K2):
-        if flush is not None:
-            flush()
-        ev_d[i][0].record()
-        decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
-        ev_d[i][1].record()
-        if mixed:
-            ev_p[i][0].record()
-            prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
-            ev_p[i][1].record()
+    # each call (decode; prefill)
+    rep_d, rep_p = [], []
+    for _ in range(R2):
+        ev_d = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+        ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+        for i in range(K2):
+            if flush is not None:
+                flush()
+            ev_d[i][0].record()
+            decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
+            ev_d[i][1].record()
+            if mixed:
+                ev_p[i][0].record()
+                prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
+                ev_p[i][1].record()
+        rep_d.append(ev_d)
+        rep_p.append(ev_p)
     torch.cuda.synchronize()
     sampler.mark_end()
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = sum(a.elapsed_time(c) for a, c in ev) / K
-    dec_ms = sum(a.elapsed_time(c) for a, c in ev_d) / K2
-    pf_ms = sum(a.elapsed_time(c) for a, c in ev_p) / K2 if mixed else 0.0
+
+    def per_step(reps, n):
+        return statistics.median(sum(a.elapsed_time(c) for a, c in ev) / n for ev in reps)
+
+    step_ms = per_step(rep_ms, K)
+    dec_ms = per_step(rep_d, K2)
+    pf_ms = per_step(rep_p, K2) if mixed else 0.0
     if ws > 1:
         step_ms, dec_ms, pf_ms = _max_over_ranks([step_ms, dec_ms, pf_ms], dev)
     assert int(wsp[:4].view(torch.int32)[0]) == 0, "decode kernel reported a wait timeout"
@@ -493,9 +524,14 @@ def run_ours(args):
                          "traffic": _traffic("decode", args.workload, local)},
             "e2e": {"value": round(_job_throughput(ws, kv_bytes, e2e_s) / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * K + (launches_per_step - 1) * K2,
+            "gpu_launches": launches_per_step * K * R + (launches_per_step - 1) * K2 * R2,
+            "timed_repeats": {"steps": R, "kernels_alone": R2,
+                              "note": f"each repeat times exactly {K} steps ({K2} calls of each entry point alone); "
+                                      "ms_per_step is the median repeat"},
             "clocks": clocks,
         }
+        if clocks.get("sm_mhz"):
+            line["cycles_per_step"] = round(step_ms * 1e-3 * clocks["sm_mhz"] * 1e6)
         if mixed:
             pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
             line["prefill"] = {"kernel": "pa_prefill_chunk", "us": round(pf_ms * 1e3, 2), "flops": pf_flops,

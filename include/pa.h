@@ -41,10 +41,27 @@
  * cudaStream_t; NULL = the legacy default stream) and returns without
  * synchronising.  PA_OK means "validated and enqueued".  Argument errors are
  * detected on the host before anything is enqueued; a CUDA launch error is
- * reported as PA_ERR_CUDA.  Device-array contents (block ids, lengths, slots)
- * are the caller's contract and are not checked on the device: a block id
- * outside [0, num_blocks), a context length above max_blocks_per_seq *
- * block_size, or a slot outside the pool reads or writes out of bounds.
+ * reported as PA_ERR_CUDA.
+ *
+ * Device-array contents (block ids, lengths, slots) are the caller's
+ * contract.  With pa_kv_desc.check_indices == 0 (the default) they are not
+ * checked on the device: a block id outside [0, num_blocks), a context
+ * length outside [0, max_blocks_per_seq * block_size], or a slot outside the
+ * pool reads or writes out of bounds.  With check_indices == 1 every such
+ * value is range-checked on the device before it is used; a value out of
+ * range sets PA_DEVERR_BAD_INDEX in the error words, and the access is
+ * redirected into the cache (a block id becomes block 0, a length is clamped
+ * into its range) or skipped (a cache-write slot, a block copy), so that no
+ * access leaves the buffers.  The results of a call that reported
+ * PA_DEVERR_BAD_INDEX are meaningless.
+ *
+ * Failures on the device: every wait of a kernel on its own pipeline (a copy
+ * landing, a tensor-core product finishing) is bounded by a 2 s limit.  A
+ * kernel whose wait runs out sets PA_DEVERR_WAIT_TIMEOUT in its error words,
+ * waits (bounded) for its own copies and products in flight, frees what it
+ * holds and returns; its outputs are then incomplete.  The error words are
+ * the caller's pa_kv_desc.error_word (every kernel, when given) and, for
+ * pa_decode, the first int32 of its workspace.  Kernels never trap.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -58,8 +75,10 @@ extern "C" {
 
 /* 1: pa_kv_desc up to prefill_impl; cache write, decode, prefill, merge.
  * 2: pa_kv_desc gains sliding_window, attention_chunk, k_scales, v_scales
- *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks. */
-#define PA_ABI_VERSION 2
+ *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks.
+ * 3: pa_kv_desc gains error_word, check_indices (appended); PA_DEVERR_*;
+ *    pa_test_stall_pipelines. */
+#define PA_ABI_VERSION 3
 
 /* Symbols of the shared library; everything else in it stays hidden. */
 #if defined(__GNUC__)
@@ -87,6 +106,11 @@ typedef enum {
                          are fp16 too; bit copies ("Block-Paged KV Cache
                          (FP8/FP16)")                                      */
 } pa_kv_dtype;
+
+/* Bits the kernels OR into an error word (see "Failures on the device"). */
+#define PA_DEVERR_WAIT_TIMEOUT 1 /* a bounded wait ran out; outputs incomplete */
+#define PA_DEVERR_BAD_INDEX 2    /* check_indices: a block id, length or slot
+                                    was out of range; results meaningless      */
 
 /* Which decode kernel pa_decode runs.  0 lets the library choose. */
 typedef enum {
@@ -131,6 +155,15 @@ typedef enum {
  *                  aligned, owned by the caller, read by the kernels at run
  *                  time (so they must stay valid until the work completes).
  *                  Must be NULL for bf16 and fp16 caches.
+ *   error_word   : optional device int32, owned by the caller, 4-byte
+ *                  aligned.  Every kernel of a call made with this
+ *                  descriptor ORs its PA_DEVERR_* bits into it (atomically);
+ *                  nothing clears it, so zero it before the calls it should
+ *                  watch and read it after they complete.  NULL: no such
+ *                  word (pa_decode still reports into its workspace).
+ *   check_indices: 0 or 1; 1 range-checks block ids, context lengths,
+ *                  query-chunk lengths, cache-write slots and block-copy ids
+ *                  on the device (see "Device-array contents" above).
  */
 typedef struct {
   int32_t num_blocks;
@@ -147,6 +180,8 @@ typedef struct {
   int32_t attention_chunk; /* 0: none */
   const float *k_scales;   /* NULL: per-tensor k_scale */
   const float *v_scales;   /* NULL: per-tensor v_scale */
+  int32_t *error_word;     /* NULL: none */
+  int32_t check_indices;   /* 0: contents unchecked */
 } pa_kv_desc;
 
 /* PA_ABI_VERSION of the loaded library. */
@@ -179,12 +214,13 @@ PA_API pa_status pa_cache_write(const pa_kv_desc *desc, const void *k, const voi
 /*
  * Bytes of scratch that pa_decode needs for num_seqs sequences on the current
  * device.  Zero-fill the workspace once before its first use; it may then be
- * reused by consecutive calls on one stream (each call leaves its error word
- * and its merge counters at zero again; the rest holds the last call's
- * partial results).  Calls that overlap on the GPU need separate workspaces.
- * After a call completes, a non-zero first int32 of the workspace means the
- * kernel gave up (a bounded wait on its own pipeline ran out, or a merge had
- * more pieces than it supports).
+ * reused by consecutive calls on one stream (each call that completes without
+ * error leaves its error word and its merge counters at zero again; the rest
+ * holds the last call's partial results).  Calls that overlap on the GPU need
+ * separate workspaces.  After a call completes, the first int32 of the
+ * workspace holds the PA_DEVERR_* bits it reported; if it is not zero, the
+ * merge counters may be left behind too: zero-fill the whole workspace again
+ * before its next use.
  */
 PA_API size_t pa_decode_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_context_len);
 
@@ -314,12 +350,27 @@ PA_API pa_status pa_merge_partials(float *out, float *lse_out, const float *part
  * current); make that first call before any stream capture.  All calls share
  * the one array, so calls that may overlap on the GPU (different streams
  * without ordering between them) race; serialise them, or use pa_decode with
- * separate workspaces.
+ * separate workspaces.  The array's own error word is cleared by every call,
+ * so device failures (PA_DEVERR_*) of pa_decode_static are visible only
+ * through desc->error_word: pass one to see them.  Arguments are validated
+ * as in pa_decode before anything is enqueued.
  */
 PA_API pa_status pa_decode_static(const pa_kv_desc *desc, float *out, float *lse, const void *q,
                                   const void *k_cache, const void *v_cache, const int32_t *block_tables,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                                   int32_t max_context_len, float scale, pa_stream_t stream);
+
+/*
+ * Test hook for the failure path (no counterpart on the pages).  While
+ * enabled (enable != 0), the producers of the decode and tcgen05 prefill
+ * kernels launched afterwards issue no copies and signal nothing, so the
+ * kernels' bounded waits run out: they report PA_DEVERR_WAIT_TIMEOUT, free
+ * what they hold and return, with nothing in flight.  wait_limit_ns (> 0)
+ * replaces the 2 s limit of every bounded wait while enabled, so a test
+ * does not wait long.  Process-wide; pass enable = 0 to restore normal
+ * launches.  Never enable it outside tests.
+ */
+PA_API pa_status pa_test_stall_pipelines(int32_t enable, int64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -38,12 +38,15 @@ PA_PREFILL_AUTO = 0
 PA_PREFILL_MMA_SYNC = 1
 PA_PREFILL_TCGEN05 = 2
 
+PA_DEVERR_WAIT_TIMEOUT = 1
+PA_DEVERR_BAD_INDEX = 2
+
 #: every symbol include/pa.h declares
 #: PA_ABI_VERSION this binding is written against (pa_kv_desc layout, entry points)
-ABI_VERSION = 2
+ABI_VERSION = 3
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
-            "pa_copy_blocks")
+            "pa_copy_blocks", "pa_test_stall_pipelines")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -63,6 +66,8 @@ class PaKvDesc(ctypes.Structure):
         ("attention_chunk", ctypes.c_int32),
         ("k_scales", ctypes.c_void_p),
         ("v_scales", ctypes.c_void_p),
+        ("error_word", ctypes.c_void_p),
+        ("check_indices", ctypes.c_int32),
     ]
 
 
@@ -108,6 +113,8 @@ def load(path: Optional[str] = None):
         lib.pa_merge_partials.restype = ctypes.c_int
         lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
         lib.pa_decode_static.restype = ctypes.c_int
+        lib.pa_test_stall_pipelines.argtypes = [I32, ctypes.c_int64]
+        lib.pa_test_stall_pipelines.restype = ctypes.c_int
         if lib.pa_abi_version() != ABI_VERSION:
             raise RuntimeError(f"{p} has ABI version {lib.pa_abi_version()}, this binding expects {ABI_VERSION}: "
                                "rebuild it")
@@ -121,19 +128,27 @@ def make_desc(num_blocks: int, num_kv_heads: int, num_q_heads: int, head_dim: in
               block_size: int = 16, decode_impl: int = PA_DECODE_AUTO,
               prefill_impl: int = PA_PREFILL_AUTO, sliding_window: int = 0,
               attention_chunk: int = 0, k_scales: Optional[torch.Tensor] = None,
-              v_scales: Optional[torch.Tensor] = None) -> PaKvDesc:
+              v_scales: Optional[torch.Tensor] = None, error_word: Optional[torch.Tensor] = None,
+              check_indices: bool = False) -> PaKvDesc:
     """``k_scales`` / ``v_scales``: optional per-kv-head fp32 scales of an
-    8-bit cache, CUDA tensors of num_kv_heads elements; the descriptor keeps a
-    reference to them (the kernels read them at run time)."""
+    8-bit cache, CUDA tensors of num_kv_heads elements; ``error_word``: an
+    optional CUDA int32 tensor (one element) that the kernels OR their
+    PA_DEVERR_* bits into; the descriptor keeps a reference to these (the
+    kernels use them at run time).  ``check_indices``: range-check the
+    device arrays' block ids, lengths and slots on the device."""
     for t, name in ((k_scales, "k_scales"), (v_scales, "v_scales")):
         if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()
                               or t.numel() != num_kv_heads):
             raise ValueError(f"{name} must be a contiguous CUDA float32 tensor of num_kv_heads elements")
+    if error_word is not None and (error_word.dtype != torch.int32 or not error_word.is_cuda
+                                   or error_word.numel() < 1):
+        raise ValueError("error_word must be a CUDA int32 tensor")
     d = PaKvDesc(num_blocks, block_size, num_kv_heads, num_q_heads, head_dim, kv_dtype,
                  k_scale, v_scale, decode_impl, prefill_impl, sliding_window, attention_chunk,
                  k_scales.data_ptr() if k_scales is not None else None,
-                 v_scales.data_ptr() if v_scales is not None else None)
-    d._keep = (k_scales, v_scales)
+                 v_scales.data_ptr() if v_scales is not None else None,
+                 error_word.data_ptr() if error_word is not None else None, 1 if check_indices else 0)
+    d._keep = (k_scales, v_scales, error_word)
     return d
 
 
@@ -278,6 +293,13 @@ def pa_copy_blocks(desc: PaKvDesc, k_cache, v_cache, src_blocks, dst_blocks, str
                                  _ptr(v_cache, _CACHE, "v_cache"), _ptr(src_blocks, _I32, "src_blocks"),
                                  _ptr(dst_blocks, _I32, "dst_blocks"), int(src_blocks.shape[0]),
                                  _stream(stream)))
+
+
+def pa_test_stall_pipelines(enable: bool, wait_limit_ns: int = 20_000_000):
+    """Test hook of the failure path: while enabled, the decode and tcgen05
+    prefill kernels issue no copies and their bounded waits (limited to
+    ``wait_limit_ns``) run out; they report PA_DEVERR_WAIT_TIMEOUT and return."""
+    _check(load().pa_test_stall_pipelines(1 if enable else 0, int(wait_limit_ns)))
 
 
 def pa_merge_partials(out, part_o, part_lse, num_parts=None, lse_out=None, stream=None):

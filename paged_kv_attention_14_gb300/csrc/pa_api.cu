@@ -9,6 +9,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "pa.h"
 #include "pa_internal.h"
 
@@ -52,8 +54,15 @@ pa_status check_desc(const pa_kv_desc *d) {
     return fail(PA_ERR_INVALID_ARG, "per-head k_scales / v_scales apply to FP8 caches only%s");
   if ((reinterpret_cast<uintptr_t>(d->k_scales) | reinterpret_cast<uintptr_t>(d->v_scales)) & 3u)
     return fail(PA_ERR_INVALID_ARG, "k_scales and v_scales must be 4-byte aligned%s");
+  if (reinterpret_cast<uintptr_t>(d->error_word) & 3u)
+    return fail(PA_ERR_INVALID_ARG, "error_word must be 4-byte aligned%s");
+  if (d->check_indices != 0 && d->check_indices != 1)
+    return fail(PA_ERR_INVALID_ARG, "check_indices must be 0 or 1%s");
   return PA_OK;
 }
+
+std::atomic<int> g_test_stall{0};
+std::atomic<unsigned long long> g_test_wait_ns{0};
 
 pa_status cuda_fail(cudaError_t e) {
   return fail(PA_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
@@ -62,7 +71,43 @@ pa_status cuda_fail(cudaError_t e) {
 }  // namespace
 
 namespace pa {
+
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
+TestHooks test_hooks() {
+  TestHooks h;
+  h.stall = g_test_stall.load(std::memory_order_relaxed);
+  const unsigned long long w = g_test_wait_ns.load(std::memory_order_relaxed);
+  h.wait_ns = (h.stall && w) ? w : kDefaultWaitNs;
+  return h;
+}
+
+pa_status validate_decode(const pa_kv_desc *desc, const float *out, const float *lse, const void *q,
+                          const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                          int32_t max_context_len, float scale, DecodePlan *plan) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0%s");
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, q, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG, "block_tables, context_lens and lse must be 4-byte aligned%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
+  const char *why = "";
+  st = plan_decode(*desc, num_seqs, plan, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  return PA_OK;
+}
+
 }  // namespace pa
 
 extern "C" {
@@ -106,26 +151,11 @@ pa_status pa_decode(const pa_kv_desc *desc, float *out, float *lse, const void *
                     int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                     int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
                     pa_stream_t stream) {
-  pa_status st = check_desc(desc);
-  if (st != PA_OK) return st;
-  if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs must be >= 0%s");
-  if (num_seqs == 0) return ok();
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
-    return fail(PA_ERR_INVALID_ARG,
-                "out, q, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
-  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return fail(PA_ERR_INVALID_ARG, "block_tables, context_lens and lse must be 4-byte aligned%s");
-  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
-  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
-    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
-  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
   pa::DecodePlan plan;
-  const char *why = "";
-  st = pa::plan_decode(*desc, num_seqs, &plan, &why);
-  if (st != PA_OK) return fail(st, "%s", why);
+  pa_status st = pa::validate_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                     context_lens, num_seqs, max_context_len, scale, &plan);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
   if (!workspace || !aligned16(workspace))
     return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
   if (workspace_bytes < plan.workspace_bytes)
@@ -253,6 +283,13 @@ pa_status pa_merge_partials(float *out, float *lse_out, const float *part_o,
                                          num_heads, max_parts, head_dim,
                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_test_stall_pipelines(int32_t enable, int64_t wait_limit_ns) {
+  if (enable && wait_limit_ns <= 0) return fail(PA_ERR_INVALID_ARG, "wait_limit_ns must be positive%s");
+  g_test_wait_ns.store(enable ? static_cast<unsigned long long>(wait_limit_ns) : 0ull, std::memory_order_relaxed);
+  g_test_stall.store(enable ? 1 : 0, std::memory_order_relaxed);
+  return ok();
 }
 
 }  // extern "C"

@@ -7,9 +7,12 @@
 // of the vllm.cpp status notes).  FP8 pages hold one byte per element
 // ("2. CLI Configuration Parameters", --kv-cache-dtype fp8).
 //
-// One thread moves 16 source bytes (8 bf16 values) of one (token, kv head)
-// row: a warp covers two 256-byte rows (head_dim 128), so loads and stores
-// are 16-byte vectorised and coalesced.  Negative slots are skipped.
+// One thread moves one 16-byte vector of a cache row: 8 bf16 / fp16 values
+// (16 source bytes), or 16 values of an 8-bit cache (32 source bytes
+// quantised to 16 bytes).  Consecutive threads cover consecutive vectors of
+// a (token, kv head) row, so loads and stores are 16-byte vectorised and
+// coalesced.  Negative slots are skipped; with checked indices a slot past
+// the pool is skipped and reported.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -20,7 +23,8 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, uint8_t *__restrict__ k_cache,
     uint8_t *__restrict__ v_cache, const int64_t *__restrict__ slot_mapping, int64_t total_vecs,
     int vecs_per_row, int num_kv_heads, int block_size, float k_scale, float v_scale,
-    const float *__restrict__ k_scales, const float *__restrict__ v_scales) {
+    const float *__restrict__ k_scales, const float *__restrict__ v_scales, int64_t num_slots, int checked,
+    int32_t *err) {
   // a kernel launched after this one as a programmatic dependent (pa_decode,
   // pa_prefill_chunk) may start its launch now; it waits for this grid's
   // writes before reading anything
@@ -33,60 +37,58 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
   const int head = static_cast<int>(row % num_kv_heads);
   const int64_t slot = __ldg(slot_mapping + token);
   if (slot < 0) return;
+  if (checked && slot >= num_slots) {
+    if (vec == 0) report_error(err, nullptr, kErrBadIndex);
+    return;
+  }
   const int64_t blk = slot / block_size;
   const int64_t off = slot % block_size;
   // destination row (blk, head, off) of [num_blocks][num_kv_heads][block_size][D]
-  const int64_t dst_row = (blk * num_kv_heads + head) * block_size + off;
-  const uint4 kv = __ldg(k + i);
-  const uint4 vv = __ldg(v + i);
-  if (KVT == kKvBf16) {
-    reinterpret_cast<uint4 *>(k_cache)[dst_row * vecs_per_row + vec] = kv;
-    reinterpret_cast<uint4 *>(v_cache)[dst_row * vecs_per_row + vec] = vv;
+  const int64_t dst = ((blk * num_kv_heads + head) * block_size + off) * vecs_per_row + vec;
+  if constexpr (kv16(KVT)) {
+    reinterpret_cast<uint4 *>(k_cache)[dst] = __ldg(k + i);
+    reinterpret_cast<uint4 *>(v_cache)[dst] = __ldg(v + i);
   } else {
-    // x / scale in correctly rounded fp32 division, then E4M3 RNE-satfinite
-    auto enc = [](const uint4 &u, float s) {
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint16_t b[4];
+    // x / scale in correctly rounded fp32 division, then E4M3 / E5M2
+    // round-to-nearest-even with finite saturation, 16 values per store
+    auto enc = [](const uint4 &a, const uint4 &b, float s) {
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t r[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        b[j] = pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[j]), s), __fdiv_rn(bf16hi(w[j]), s));
-      uint2 r;
-      r.x = static_cast<uint32_t>(b[0]) | (static_cast<uint32_t>(b[1]) << 16);
-      r.y = static_cast<uint32_t>(b[2]) | (static_cast<uint32_t>(b[3]) << 16);
-      return r;
+      for (int j = 0; j < 4; ++j) {
+        const uint16_t lo = pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j]), s), __fdiv_rn(bf16hi(w[2 * j]), s));
+        const uint16_t hi =
+            pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j + 1]), s), __fdiv_rn(bf16hi(w[2 * j + 1]), s));
+        r[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      return make_uint4(r[0], r[1], r[2], r[3]);
     };
     // per-kv-head scales where given
     const float ks = k_scales ? __ldg(k_scales + head) : k_scale;
     const float vs = v_scales ? __ldg(v_scales + head) : v_scale;
-    reinterpret_cast<uint2 *>(k_cache)[dst_row * vecs_per_row + vec] = enc(kv, ks);
-    reinterpret_cast<uint2 *>(v_cache)[dst_row * vecs_per_row + vec] = enc(vv, vs);
+    reinterpret_cast<uint4 *>(k_cache)[dst] = enc(__ldg(k + 2 * i), __ldg(k + 2 * i + 1), ks);
+    reinterpret_cast<uint4 *>(v_cache)[dst] = enc(__ldg(v + 2 * i), __ldg(v + 2 * i + 1), vs);
   }
 }
 
 cudaError_t launch_cache_write(const pa_kv_desc &d, const void *k, const void *v, void *k_cache,
                                void *v_cache, const int64_t *slot_mapping, int32_t num_tokens,
                                cudaStream_t stream) {
-  const int vecs_per_row = d.head_dim / 8;
+  const bool b16 = d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16;
+  const int vecs_per_row = d.head_dim / (b16 ? 8 : 16);  // 16-byte cache vectors per row
   const int64_t total = static_cast<int64_t>(num_tokens) * d.num_kv_heads * vecs_per_row;
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   const float ks = d.k_scale == 0.f ? 1.f : d.k_scale;
   const float vs = d.v_scale == 0.f ? 1.f : d.v_scale;
-  if (d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16)  // 16-bit: bit copies
-    cache_write_kernel<kKvBf16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
-  else if (d.kv_dtype == PA_KV_FP8_E5M2)
-    cache_write_kernel<kKvE5M2><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
-  else
-    cache_write_kernel<kKvFp8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), slot_mapping, total,
-        vecs_per_row, d.num_kv_heads, d.block_size, ks, vs, d.k_scales, d.v_scales);
+  const int64_t num_slots = static_cast<int64_t>(d.num_blocks) * d.block_size;
+  auto kern = b16 ? &cache_write_kernel<kKvBf16>  // 16-bit: bit copies
+              : d.kv_dtype == PA_KV_FP8_E5M2 ? &cache_write_kernel<kKvE5M2>
+                                             : &cache_write_kernel<kKvFp8>;
+  kern<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint8_t *>(k_cache),
+      static_cast<uint8_t *>(v_cache), slot_mapping, total, vecs_per_row, d.num_kv_heads, d.block_size, ks, vs,
+      d.k_scales, d.v_scales, num_slots, d.check_indices, d.error_word);
   return cudaGetLastError();
 }
 

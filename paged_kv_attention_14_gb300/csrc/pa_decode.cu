@@ -186,6 +186,12 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.window = d.sliding_window;
   a.chunk = d.attention_chunk;
   a.err = reinterpret_cast<int32_t *>(ws);
+  a.user_err = d.error_word;
+  a.checked = d.check_indices;
+  a.num_blocks = d.num_blocks;
+  const TestHooks hooks = test_hooks();
+  a.stall = hooks.stall;
+  a.wait_ns = hooks.wait_ns;
   a.seg_counter = reinterpret_cast<int32_t *>(ws + w.counter_off);
   a.slot_lse = reinterpret_cast<float *>(ws + w.slot_lse_off);
   a.slot_o = reinterpret_cast<float *>(ws + w.slot_o_off);

@@ -98,7 +98,12 @@ struct DecodeArgs {
   const float *v_scales;
   int window;      // sliding window (0: none)
   int chunk;       // chunked-local attention (0: none)
-  int32_t *err;
+  int32_t *err;          // the workspace's error word
+  int32_t *user_err;     // the caller's error word (pa_kv_desc.error_word), or NULL
+  unsigned long long wait_ns;  // limit of every bounded wait
+  int checked;     // range-check block ids and lengths (pa_kv_desc.check_indices)
+  int stall;       // test hook: the producer issues nothing, so the waits run out
+  int num_blocks;  // blocks of the cache (checked mode)
   int32_t *seg_counter;  // [num_seqs * num_groups] pieces of each split segment finished
   float *slot_lse;       // [grid][2][slot heads], log2 domain
   float *slot_o;         // [grid][2][slot heads][D]
@@ -132,6 +137,16 @@ __device__ __forceinline__ float head_qscale(const DecodeArgs &a, int kvh) {
 }
 __device__ __forceinline__ float head_vscale(const DecodeArgs &a, int kvh) {
   return a.v_scales ? __ldg(a.v_scales + kvh) : a.vscale;
+}
+
+// Error bits into the workspace's error word and the caller's.
+__device__ __forceinline__ void report(const DecodeArgs &a, int bits) { report_error(a.err, a.user_err, bits); }
+
+// Context length of sequence s; in checked mode clamped to the block table's
+// capacity (and reported when outside it).
+__device__ __forceinline__ int seq_len(const DecodeArgs &a, int s) {
+  const int L = __ldg(a.context_lens + s);
+  return a.checked ? checked_len(L, a.max_blocks_per_seq * 16, a.err, a.user_err) : L;
 }
 
 // ---------------------------------------------------------------- workspace
@@ -179,7 +194,7 @@ __device__ long long count_blocks(const DecodeArgs &a, int lane) {
     for (int i = 0; i < 8; ++i) {
       const int s = base + i * 32 + lane;
       if (s < S) {
-        const int L = __ldg(a.context_lens + s);
+        const int L = seq_len(a, s);
         if (L > 0)
           acc += static_cast<unsigned>(seq_blocks(a, L));
         else if (s % G == static_cast<int>(blockIdx.x))
@@ -211,6 +226,9 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
   const long long b0 = static_cast<long long>(blockIdx.x) * per_cta;
   const long long b1 = min(b0 + per_cta, total);
   const uint64_t pol = l2_evict_first_policy();
+  // test hook: issue nothing and signal nothing, so that every consumer
+  // wait runs out (nothing is in flight when the kernel gives up)
+  if (a.stall) return;
   int stage = 0;
   uint32_t ppar = 1;  // a fresh barrier counts its preceding phase (parity 1) as complete
   bool ok = true;
@@ -225,7 +243,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
       long long pre = 0;
       for (int base = 0; base < S && sz < 0; base += 32) {
         const int si = base + lane;
-        const int Li = si < S ? __ldg(a.context_lens + si) : 0;
+        const int Li = si < S ? seq_len(a, si) : 0;
         const long long v = Li > 0 ? static_cast<long long>(seq_blocks(a, Li)) * NG : 0;
         long long incl = v;
 #pragma unroll
@@ -256,7 +274,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     auto locate = [&](int s_, long long pre_, long long pos) {
       s = s_;
       pre = pre_;
-      L = __ldg(a.context_lens + s);
+      L = seq_len(a, s);
       fb = seq_first_block(a, L);
       nb = ((L + 15) >> 4) - fb;
       grp = static_cast<int>((pos - pre) / nb);
@@ -270,7 +288,11 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     // slower on GB300, the producer running further ahead of the consumers.)
     int win_s = -1, wb = 0, w_cur = 0, w_nxt = 0;
     const int32_t *trow = a.block_tables;
-    auto tload = [&](int e) { return e < fb + nb ? __ldg(trow + e) : 0; };
+    auto tload = [&](int e) {
+      if (e >= fb + nb) return 0;
+      const int v = __ldg(trow + e);
+      return a.checked ? checked_block(v, a.num_blocks, a.err, a.user_err) : v;
+    };
     // streams flat units [from, to), starting from the located state
     auto stream = [&](long long from, long long to) {
       long long cur = from;
@@ -299,7 +321,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
             w_nxt = tload(wb + 32 + lane);
           }
           PA_TRACE(const long long tt1 = clock64(); tp_table += tt1 - tt0;)
-          if (!mbar_wait(&empty[stage], ppar)) {
+          if (!mbar_wait(&empty[stage], ppar, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -339,9 +361,9 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
           pre += static_cast<long long>(nb) * NG;
           do {
             ++s;
-          } while (s < S && __ldg(a.context_lens + s) <= 0);
+          } while (s < S && seq_len(a, s) <= 0);
           if (s < S) {
-            L = __ldg(a.context_lens + s);
+            L = seq_len(a, s);
             fb = seq_first_block(a, L);
             nb = ((L + 15) >> 4) - fb;
           }
@@ -349,7 +371,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
       }
     };
     // the segment holding the range's last unit
-    const int nbz = seq_blocks(a, __ldg(a.context_lens + sz));
+    const int nbz = seq_blocks(a, seq_len(a, sz));
     const long long segz = prez + (b1 - 1 - prez) / nbz * nbz;
     if (segz > b0 && segz + nbz > b1) {
       locate(sz, prez, segz);
@@ -362,7 +384,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     }
   }
   if (ok) {
-    if (mbar_wait(&empty[stage], ppar)) {
+    if (mbar_wait(&empty[stage], ppar, a.wait_ns)) {
       if (lane == 0) {
         hdr[stage].kind = kStageEnd;
         mbar_arrive(&full[stage]);
@@ -377,7 +399,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     g_pa_trace[blockIdx.x][5] = clock64() - tp0;
   })
   if (!ok) {
-    if (lane == 0) atomicOr(a.err, kErrWaitTimeout);
+    if (lane == 0) report(a, kErrWaitTimeout);
     // let the copies already issued land before the CTA can exit
     for (int i = 1; i <= min(issued, NS); ++i) {
       int st = stage - i;
@@ -386,7 +408,7 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
         st += NS;
         par ^= 1;
       }
-      mbar_wait(&full[st], par);
+      mbar_wait(&full[st], par, a.wait_ns);
     }
   }
 }
@@ -622,8 +644,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
   int stage = 0;
   uint32_t cpar = 0;
   for (;;) {
-    if (!mbar_wait(&full[stage], cpar)) {
-      if (lane == 0) atomicOr(a.err, kErrWaitTimeout);
+    if (!mbar_wait(&full[stage], cpar, a.wait_ns)) {
+      if (lane == 0) report(a, kErrWaitTimeout);
       break;
     }
     const StageHdr h = hdr[stage];
@@ -934,8 +956,8 @@ __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *
   int rb = 0;
   uint32_t par = 0;
   for (;;) {
-    if (!mbar_wait(&rfull[rb], par)) {
-      if (lane == 0) atomicOr(a.err, kErrWaitTimeout);
+    if (!mbar_wait(&rfull[rb], par, a.wait_ns)) {
+      if (lane == 0) report(a, kErrWaitTimeout);
       break;
     }
     const StageHdr h = rhdr[rb];
@@ -1084,8 +1106,8 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
   PA_TRACE(const long long tc0 = clock64(); long long tc_full = 0, tc_fin = 0, n_st = 0, n_pc = 0;)
   for (;;) {
     PA_TRACE(const long long tw0 = clock64();)
-    if (!mbar_wait(&full[stage], cpar)) {
-      if (lane == 0) atomicOr(a.err, kErrWaitTimeout);
+    if (!mbar_wait(&full[stage], cpar, a.wait_ns)) {
+      if (lane == 0) report(a, kErrWaitTimeout);
       break;
     }
     PA_TRACE(tc_full += clock64() - tw0; ++n_st;)
@@ -1278,8 +1300,8 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
       for (int e = 0; e < 2; ++e)
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], o);
-    if (!mbar_wait(&rempty[rb], rpar)) {
-      if (lane == 0) atomicOr(a.err, kErrWaitTimeout);
+    if (!mbar_wait(&rempty[rb], rpar, a.wait_ns)) {
+      if (lane == 0) report(a, kErrWaitTimeout);
       break;
     }
     float *rw = red + (size_t(rb) * NC + warp) * C::REDW;
@@ -1314,12 +1336,12 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
     PA_TRACE(tc_fin += clock64() - tf0;)
   }
   // tell the epilogue warp that no piece follows
-  if (mbar_wait(&rempty[rb], rpar)) {
+  if (mbar_wait(&rempty[rb], rpar, a.wait_ns)) {
     if (warp == 0 && lane == 0) rhdr[rb].kind = kStageEnd;
     __syncwarp();
     if (lane == 0) mbar_arrive(&rfull[rb]);
   } else if (lane == 0) {
-    atomicOr(a.err, kErrWaitTimeout);
+    report(a, kErrWaitTimeout);
   }
   PA_TRACE(if (tid == 0) {
     g_pa_trace[blockIdx.x][0] = tc_full;

@@ -65,15 +65,17 @@ PA_API pa_status pa_decode_static(const pa_kv_desc *desc, float *out, float *lse
                                   const void *k_cache, const void *v_cache, const int32_t *block_tables,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                                   int32_t max_context_len, float scale, pa_stream_t stream) {
-  if (!desc) return static_fail(PA_ERR_INVALID_ARG, "desc is NULL");
-  if (num_seqs <= 0) {
-    // argument checks only; nothing to run
-    return pa_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                     num_seqs, max_context_len, scale, nullptr, 0, stream);
+  // every argument check of pa_decode first, so that a call that fails on
+  // its arguments enqueues nothing
+  pa::DecodePlan plan;
+  const pa_status st = pa::validate_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                           context_lens, num_seqs, max_context_len, scale, &plan);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) {
+    pa::set_last_error("");
+    return PA_OK;
   }
-  const size_t need = pa_decode_workspace_size(desc, num_seqs, max_context_len);
-  if (need == 0) return PA_ERR_UNSUPPORTED;  // pa_last_error() already says why
-  if (need > kStaticScratchBytes)
+  if (plan.workspace_bytes > kStaticScratchBytes)
     return static_fail(PA_ERR_WORKSPACE,
                        "this batch needs more decode scratch than the 8 MiB static array; use pa_decode");
   void *scratch = nullptr;
@@ -83,10 +85,14 @@ PA_API pa_status pa_decode_static(const pa_kv_desc *desc, float *out, float *lse
   // counters (the first 256 bytes plus one int32 per sequence and kv head)
   // must start at zero, the rest is rewritten by every launch.
   const size_t head = 256 + sizeof(int32_t) * static_cast<size_t>(num_seqs) * desc->num_kv_heads;
-  e = cudaMemsetAsync(scratch, 0, head < need ? head : need, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(scratch, 0, head < plan.workspace_bytes ? head : plan.workspace_bytes, s);
   if (e != cudaSuccess) return static_fail(PA_ERR_CUDA, cudaGetErrorString(e));
-  return pa_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
-                   max_context_len, scale, scratch, kStaticScratchBytes, stream);
+  e = pa::launch_decode(*desc, plan, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        num_seqs, scale, scratch, s);
+  if (e != cudaSuccess) return static_fail(PA_ERR_CUDA, cudaGetErrorString(e));
+  pa::set_last_error("");
+  return PA_OK;
 }
 
 }  // extern "C"

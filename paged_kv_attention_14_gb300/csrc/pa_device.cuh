@@ -33,12 +33,42 @@ __host__ __device__ __forceinline__ int local_first_key(int pos, int window, int
   return lo;
 }
 
-// A wait on an mbarrier gives up after this many nanoseconds.  Every
-// legitimate wait in these kernels lasts microseconds.
+// A wait on an mbarrier gives up after this many nanoseconds unless the
+// launch passes another limit.  Every legitimate wait in these kernels lasts
+// microseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-// Error bits a kernel may set in its error word.
-constexpr int kErrWaitTimeout = 1;
+// Error bits a kernel may set in its error words (PA_DEVERR_* of pa.h).
+constexpr int kErrWaitTimeout = 1;  // a bounded wait ran out; the kernel gave up
+constexpr int kErrBadIndex = 2;     // checked mode: a block id, length or slot out of range
+
+// ORs error bits into the error words that exist (either may be NULL).
+__device__ __forceinline__ void report_error(int32_t *w1, int32_t *w2, int bits) {
+  if (w1) atomicOr(w1, bits);
+  if (w2) atomicOr(w2, bits);
+}
+
+// Checked mode: a physical block id read from a block table must lie in
+// [0, num_blocks).  An id outside is reported and replaced by block 0, so
+// that no copy or load leaves the cache.
+__device__ __forceinline__ int checked_block(int phys, int num_blocks, int32_t *w1, int32_t *w2) {
+  if (phys < 0 || phys >= num_blocks) {
+    report_error(w1, w2, kErrBadIndex);
+    return 0;
+  }
+  return phys;
+}
+
+// Checked mode: a context length must lie in [0, max_len] (max_len = the
+// table's max_blocks_per_seq * 16).  A length outside is reported and
+// clamped into the range.
+__device__ __forceinline__ int checked_len(int L, int max_len, int32_t *w1, int32_t *w2) {
+  if (L < 0 || L > max_len) {
+    report_error(w1, w2, kErrBadIndex);
+    return L < 0 ? 0 : max_len;
+  }
+  return L;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -85,8 +115,9 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
 }
 
 // Waits until the phase of `bar` with the given parity has completed.
-// Returns false if that does not happen within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Returns false if that does not happen within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_test(addr, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
@@ -94,13 +125,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_test(addr, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
 // mbar_wait with a suspend-time hint (ns) for each try: a waiter on the
 // critical path resumes sooner after the phase completes.
-__device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_test(addr, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
@@ -117,7 +149,7 @@ __device__ __forceinline__ bool mbar_wait_hint(uint64_t *bar, uint32_t parity) {
           : "memory");
       if (ok) return true;
     }
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -29,6 +29,14 @@ struct DecodePlan {
 // Fills `plan` for the descriptor; returns PA_OK or an error with a message.
 pa_status plan_decode(const pa_kv_desc &d, int32_t num_seqs, DecodePlan *plan, const char **why);
 
+// Every host-side check of pa_decode's arguments except the workspace, and
+// the launch plan (num_seqs == 0 validates the descriptor only); sets the
+// last-error string on failure.  Nothing is enqueued.
+pa_status validate_decode(const pa_kv_desc *desc, const float *out, const float *lse, const void *q,
+                          const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                          int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                          int32_t max_context_len, float scale, DecodePlan *plan);
+
 cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse,
                           const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -62,6 +70,16 @@ cudaError_t launch_copy_blocks(const pa_kv_desc &d, void *k_cache, void *v_cache
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Test hook (pa_test_stall_pipelines): while `stall` is set, the decode and
+// tcgen05 prefill kernels launched issue no copies, so that their bounded
+// waits run out; every bounded wait of every launch gives up after wait_ns.
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+struct TestHooks {
+  int stall;
+  unsigned long long wait_ns;
+};
+TestHooks test_hooks();
 
 // Sets the message pa_last_error() returns on this thread.
 void set_last_error(const char *msg);

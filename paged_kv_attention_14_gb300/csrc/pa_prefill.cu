@@ -60,6 +60,9 @@ struct PrefillArgs {
   int num_splits;   // prefix mode: key splits per sequence (grid.z = sequences x splits)
   int split_len;    // prefix mode: keys per split (a multiple of 128)
   int out_slots;    // prefix mode: output slots per (row, head); split i writes slot i
+  int32_t *err;     // the caller's error word (pa_kv_desc.error_word), or NULL
+  int checked;      // range-check block ids and lengths (pa_kv_desc.check_indices)
+  int num_blocks;   // blocks of the cache (checked mode)
 };
 
 template <int D, int KVT, int NW>
@@ -90,10 +93,21 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
   const int kvh = blockIdx.y;
   const int qtile = gridDim.x - 1 - blockIdx.x;  // longest key ranges first
   const int qs = __ldg(a.query_start_loc + s);
-  const int q_len = __ldg(a.query_start_loc + s + 1) - qs;
+  int q_len = __ldg(a.query_start_loc + s + 1) - qs;
+  int L = __ldg(a.context_lens + s);
+  if (a.checked) {
+    // lengths within the table's capacity; a chunk no longer than its context
+    // nor than the launch's query tiles; rows start at a row >= 0
+    L = checked_len(L, a.max_blocks_per_seq * 16, a.err, nullptr);
+    q_len = checked_len(q_len, a.prefix_mode ? static_cast<int>(gridDim.x) * a.qt
+                                             : min(L, static_cast<int>(gridDim.x) * a.qt), a.err, nullptr);
+    if (qs < 0) {
+      if (threadIdx.x == 0) report_error(a.err, nullptr, kErrBadIndex);
+      return;
+    }
+  }
   const int qt0 = qtile * a.qt;
   if (qt0 >= q_len) return;
-  const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);  // queries of this CTA
   // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
   // query comes after them all; otherwise query i sits at L - q_len + i
@@ -141,7 +155,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
         const bool ok = t < kv_end && t >= kv_lo;
         int64_t off = 0;
         if (ok) {
-          const int phys = __ldg(table + (t >> 4));
+          int phys = __ldg(table + (t >> 4));
+          if (a.checked) phys = checked_block(phys, a.num_blocks, a.err, nullptr);
           off = ((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * 16 + (t & 15)) * (D * 2) + ch * 16;
         }
         cp_async16(kt_s[b] + swz<D>(key, ch), a.k_cache + off, ok);
@@ -156,7 +171,8 @@ __global__ void __launch_bounds__(NW * 32, 1) prefill_kernel(const PrefillArgs a
         const bool ok = t < kv_end && t >= kv_lo;
         int64_t off = 0;
         if (ok) {
-          const int phys = __ldg(table + (t >> 4));
+          int phys = __ldg(table + (t >> 4));
+          if (a.checked) phys = checked_block(phys, a.num_blocks, a.err, nullptr);
           off = ((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * 16 + (t & 15)) * D + ch * 16;
         }
         cp_async16(kraw[b] + key * D + ch * 16, a.k_cache + off, ok);
@@ -438,6 +454,9 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
   a.num_splits = prefix_mode ? num_splits : 1;
   a.split_len = split_len;
   a.out_slots = prefix_mode ? out_slots : 1;
+  a.err = d.error_word;
+  a.checked = d.check_indices;
+  a.num_blocks = d.num_blocks;
   void *fn;
   size_t smem;
   if (d.head_dim == 128) {

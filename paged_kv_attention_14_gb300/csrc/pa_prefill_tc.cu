@@ -96,11 +96,12 @@ struct Args {
   int num_splits;   // prefix mode: key splits per sequence (grid.z = sequences x splits)
   int split_len;    // prefix mode: keys per split (a multiple of KT)
   int out_slots;    // prefix mode: output slots per (row, head); split i writes slot i
+  int32_t *err;     // the caller's error word (pa_kv_desc.error_word), or NULL
+  unsigned long long wait_ns;  // limit of every bounded wait
+  int checked;      // range-check block ids and lengths (pa_kv_desc.check_indices)
+  int stall;        // test hook: the producer issues nothing, so the waits run out
+  int num_blocks;   // blocks of the cache (checked mode)
 };
-
-// Error bits of the prefill kernel (a bounded wait ran out); device code
-// sets them, nothing else uses them.
-static __device__ int g_prefill_err;
 
 // Optional timeline counters (compiled only with -DPA_PREFILL_TRACE), per
 // CTA slot (blockIdx linearised, first 4096): softmax warp 0 lane 0 cycles
@@ -189,10 +190,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   const int kvh = blockIdx.y;
   const int qtile = gridDim.x - 1 - blockIdx.x;  // longest key ranges first
   const int qs = __ldg(a.query_start_loc + s);
-  const int q_len = __ldg(a.query_start_loc + s + 1) - qs;
+  int q_len = __ldg(a.query_start_loc + s + 1) - qs;
+  int L = __ldg(a.context_lens + s);
+  if (a.checked) {
+    // lengths within the table's capacity; a chunk no longer than its context
+    // nor than the launch's query tiles; rows start at a row >= 0
+    L = checked_len(L, a.max_blocks_per_seq * 16, a.err, nullptr);
+    q_len = checked_len(q_len, a.prefix_mode ? static_cast<int>(gridDim.x) * a.qt
+                                             : min(L, static_cast<int>(gridDim.x) * a.qt), a.err, nullptr);
+    if (qs < 0) {
+      if (threadIdx.x == 0) report_error(a.err, nullptr, kErrBadIndex);
+      return;
+    }
+  }
   const int qt0 = qtile * a.qt;
   if (qt0 >= q_len) return;
-  const int L = __ldg(a.context_lens + s);
   const int nq = min(a.qt, q_len - qt0);
   // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
   // query comes after them all; otherwise query i sits at L - q_len + i
@@ -277,16 +289,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     const int bi = lane / C::HALVES;
     const int hh = lane % C::HALVES;
     const bool issuer = lane < BPT * C::HALVES;
+    auto block_id = [&](int lb) {
+      const int v = __ldg(table + lb);
+      return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
+    };
     int phys_next = 0;
-    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = __ldg(table + j0 * BPT + bi);
+    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = block_id(j0 * BPT + bi);
     PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
     bool ok = true;
-    for (int jj = 0; jj < n_iter && ok; ++jj) {
+    // test hook: issue nothing and signal nothing, so the other warps' waits
+    // run out with nothing in flight
+    for (int jj = 0; jj < (a.stall ? 0 : n_iter) && ok; ++jj) {
       const int j = j0 + jj;
       const int phys = phys_next;
       const int key0 = j * KT;
       const int lb = (j + 1) * BPT + bi;  // prefetch the next tile's block id
-      phys_next = (issuer && lb * 16 < kv_end) ? __ldg(table + lb) : 0;
+      phys_next = (issuer && lb * 16 < kv_end) ? block_id(lb) : 0;
       const int nblk = min(BPT, (kv_end - key0 + 15) / 16);
       // blocks of the first tile entirely before the CTA's first key are not
       // read (under local attention their pages may be gone)
@@ -300,7 +318,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         const uint32_t ph = part ? (jj / NSV) & 1 : (jj / NSK) & 1;
         const int full = (part ? V_FULL : K_FULL) + st;
         PF_TRACE(const long long tw = clock64();)
-        if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1)) {
+        if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -362,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       // releases and the V wait sit between MMAs (while the pipe has work)
       // and the thread goes straight from the last MMA of a KV tile to the
       // wait for the next tile's P_A.
-      if (!mbar_wait(&bar[K_FULL], 0) || !mbar_wait(&bar[V_FULL], 0)) ok = false;
+      if (!mbar_wait(&bar[K_FULL], 0, a.wait_ns) || !mbar_wait(&bar[V_FULL], 0, a.wait_ns)) ok = false;
       if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < NQT; ++t) {
@@ -373,7 +391,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       for (int jj = 0; jj < n_iter && ok; ++jj) {
         const bool next = jj + 1 < n_iter;
         for (int t = 0; t < NQT; ++t) {
-          if (!mbar_wait_hint(&bar[P_FULL + t], jj & 1)) {
+          if (!mbar_wait_hint(&bar[P_FULL + t], jj & 1, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -382,14 +400,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
           pv(t, jj);
           if (t == NQT - 1) {
             umma_commit(&bar[V_EMPTY + jj % NSV]);  // both tiles are done with V of iteration jj
-            if (next && !mbar_wait(&bar[V_FULL + (jj + 1) % NSV], ((jj + 1) / NSV) & 1)) {
+            if (next && !mbar_wait(&bar[V_FULL + (jj + 1) % NSV], ((jj + 1) / NSV) & 1, a.wait_ns)) {
               ok = false;
               break;
             }
           }
           if (next) {
             if (t == 0) {
-              if (!mbar_wait(&bar[K_FULL + (jj + 1) % NSK], ((jj + 1) / NSK) & 1)) {
+              if (!mbar_wait(&bar[K_FULL + (jj + 1) % NSK], ((jj + 1) / NSK) & 1, a.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -429,7 +447,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     for (int jj = 0; jj < n_iter; ++jj) {
       const int j = j0 + jj;
       PF_TRACE(tc = clock64();)
-      if (!mbar_wait_hint(&bar[S_FULL + t], jj & 1)) {
+      if (!mbar_wait_hint(&bar[S_FULL + t], jj & 1, a.wait_ns)) {
         ok = false;
         break;
       }
@@ -442,7 +460,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
         // V rows past the last needed key: zero (stale or poisoned data),
         // after this tile's V copies landed; tile 0's PV of this KV tile is
         // issued before tile 1's
-        if (!mbar_wait(&bar[V_FULL + jj % NSV], (jj / NSV) & 1)) {
+        if (!mbar_wait(&bar[V_FULL + jj % NSV], (jj / NSV) & 1, a.wait_ns)) {
           ok = false;
           break;
         }
@@ -572,7 +590,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
     }
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
              if (tid == kSoftmaxWarp0 * 32 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
-    if (ok && !mbar_wait(&bar[S_FULL + t], n_iter & 1)) ok = false;
+    if (ok && !mbar_wait(&bar[S_FULL + t], n_iter & 1, a.wait_ns)) ok = false;
     if (ok) {
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -601,11 +619,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   tc_fence_before_sync();
   __syncthreads();
   if (*s_abort) {
-    if (tid == 0) atomicOr(&g_prefill_err, kErrWaitTimeout);
+    if (tid == 0) report_error(a.err, nullptr, kErrWaitTimeout);
     if (warp == kProducerWarp && lane == 0) {
       // the copies of the last issued tiles of each ring must land before exit
-      for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t) mbar_wait(&bar[K_FULL + t % NSK], (t / NSK) & 1);
-      for (int t = max(0, *s_last_v - NSV + 1); t <= *s_last_v; ++t) mbar_wait(&bar[V_FULL + t % NSV], (t / NSV) & 1);
+      for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t)
+        mbar_wait(&bar[K_FULL + t % NSK], (t / NSK) & 1, a.wait_ns);
+      for (int t = max(0, *s_last_v - NSV + 1); t <= *s_last_v; ++t)
+        mbar_wait(&bar[V_FULL + t % NSV], (t / NSV) & 1, a.wait_ns);
     }
     if (warp == kMmaWarp && lane == 0) {
       // wait (bounded) for every MMA this thread issued before freeing TMEM
@@ -613,7 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
       mbar_init(drain, 1);
       fence_mbar_init();
       umma_commit(drain);
-      mbar_wait(drain, 0);
+      mbar_wait(drain, 0, a.wait_ns);
     }
     __syncthreads();
   }
@@ -675,6 +695,12 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   a.num_splits = prefix_mode ? num_splits : 1;
   a.split_len = split_len;
   a.out_slots = prefix_mode ? out_slots : 1;
+  a.err = d.error_word;
+  a.checked = d.check_indices;
+  a.num_blocks = d.num_blocks;
+  const TestHooks hooks = test_hooks();
+  a.stall = hooks.stall;
+  a.wait_ns = hooks.wait_ns;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
   auto fn = &prefill_tc_kernel<D, KVT>;

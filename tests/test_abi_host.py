@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.pa_abi_version() == B.ABI_VERSION == 2
+    assert lib.pa_abi_version() == B.ABI_VERSION == 3
     m = re.search(r"#define\s+PA_ABI_VERSION\s+(\d+)", open(HEADER).read())
     assert int(m.group(1)) == lib.pa_abi_version()
 
@@ -58,7 +58,7 @@ def test_desc_struct_matches_header_layout():
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = re.findall(r"\b(\w+);", body)
     assert fields == [f for f, _ in B.PaKvDesc._fields_]
-    assert ctypes.sizeof(B.PaKvDesc) == 64
+    assert ctypes.sizeof(B.PaKvDesc) == 80
 
 
 def _desc(**kw):
@@ -194,6 +194,43 @@ def test_decode_argument_errors(lib):
     d2 = _desc(decode_impl=9)
     assert lib.pa_decode(ctypes.byref(d2), *ok_ptrs, 4, 0x6000, 2, 16, 0.1, 0x7000, 1 << 20,
                          None) == B.PA_ERR_INVALID_ARG
+
+
+def test_error_word_and_check_flag_validation(lib):
+    d = _desc()
+    d.error_word = 0x1002  # not 4-byte aligned
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+    assert "error_word" in B.last_error()
+    d.error_word = 0x1004
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK
+    d.check_indices = 2
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_ERR_INVALID_ARG
+    assert "check_indices" in B.last_error()
+    d.check_indices = 1
+    assert lib.pa_cache_write(ctypes.byref(d), None, None, None, None, None, 0, None) == B.PA_OK
+
+
+def test_stall_hook_arguments(lib):
+    assert lib.pa_test_stall_pipelines(1, 0) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_test_stall_pipelines(1, -5) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_test_stall_pipelines(0, 0) == B.PA_OK
+
+
+def test_static_decode_checks_arguments_like_pa_decode(lib):
+    # an argument error is reported with pa_decode's status, before anything
+    # is enqueued (no GPU is touched here)
+    assert lib.pa_decode_static(None, 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 16, 0.1,
+                                None) == B.PA_ERR_INVALID_ARG
+    d = _desc(head_dim=96)
+    assert lib.pa_decode_static(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 16,
+                                0.1, None) == B.PA_ERR_UNSUPPORTED
+    d = _desc()
+    assert lib.pa_decode_static(ctypes.byref(d), None, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 16,
+                                0.1, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_static(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 2, 65,
+                                0.1, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_static(ctypes.byref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 4, 0x6000, 0, 16,
+                                0.1, None) == B.PA_OK
 
 
 def test_prefill_argument_errors(lib):

@@ -4,16 +4,18 @@ Callers that cannot allocate device memory where they decode (a serving loop
 held to a fixed device-memory budget, a runtime whose memory is planned up
 front, a plug-in whose host framework owns the allocator) use this entry
 point instead of pa_decode with a workspace.  These tests call it through the
-C ABI twice in a row and compare with pa_decode on the same inputs, within
-the tolerance the parity tests use.  The file sorts last so that a run that
-stops at the first failure has already run every other test.
+C ABI twice in a row and compare with pa_decode on the same inputs: the same
+kernel on the same inputs, so the results must be identical, which is
+stricter than the parity tests' tolerance.  A caller-owned error word in the
+descriptor must stay zero.  The file sorts last so that a run that stops at
+the first failure has already run every other test.
 """
 import pytest
 import torch
 
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
-from pa_helpers import TOL, LSE_TOL, desc_of, gpu_caches
+from pa_helpers import desc_of, gpu_caches
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -28,7 +30,10 @@ def _lib():
 def _both(b, caches):
     kc, vc = caches
     S = b.context_lens_decode.shape[0]
-    d = desc_of(b)
+    base = desc_of(b)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d = B.make_desc(base.num_blocks, base.num_kv_heads, base.num_q_heads, base.head_dim, base.kv_dtype, base.k_scale,
+                    base.v_scale, k_scales=b.k_scales, v_scales=b.v_scales, error_word=err)
     maxL = b.max_context_len_decode()
     ws = B.decode_workspace(d, S, maxL, DEV)
     ref = torch.full((S, b.num_q_heads, b.head_dim), float("nan"), device=DEV)
@@ -43,6 +48,8 @@ def _both(b, caches):
                            b.scale, lse=lse)
         outs.append((out, lse))
     torch.cuda.synchronize()
+    assert int(err[0]) == 0, "a kernel reported a device error"
+    assert int(ws[:4].view(torch.int32)[0]) == 0
     return ref, ref_lse, outs
 
 
@@ -52,16 +59,14 @@ def test_static_decode_matches_pa_decode_on_two_calls(n):
     ref, ref_lse, outs = _both(b, gpu_caches(b))
     for out, lse in outs:
         assert torch.isfinite(out).all()
-        assert (out - ref).abs().max().item() <= TOL[b.kv_dtype]
-        assert (lse - ref_lse).abs().max().item() <= LSE_TOL[b.kv_dtype]
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
 
 
 def test_static_decode_fp8_after_bf16_call():
     b = W.random_decode(909, [1, 17, 300, 1025], 40, 8, 128, kv_dtype=W.KV_FP8, device=DEV, poison=True)
     ref, ref_lse, outs = _both(b, gpu_caches(b))
     for out, lse in outs:
-        assert (out - ref).abs().max().item() <= TOL[b.kv_dtype]
-        assert (lse - ref_lse).abs().max().item() <= LSE_TOL[b.kv_dtype]
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
 
 
 def test_static_decode_rejects_batches_beyond_its_scratch():
