@@ -78,6 +78,10 @@ def _load():
         lib.pa_oracle_copy_blocks.restype = None
         lib.pa_oracle_merge.argtypes = [P, P, I, I, P, P]
         lib.pa_oracle_merge.restype = None
+        lib.pa_oracle_bind_blocks.argtypes = [P, I, P, P, P, I, P, I, P]
+        lib.pa_oracle_bind_blocks.restype = None
+        lib.pa_oracle_release_blocks.argtypes = [P, I, P, P, I, P, I, P, P, P]
+        lib.pa_oracle_release_blocks.restype = None
         _lib = lib
         return lib
 
@@ -273,6 +277,40 @@ def copy_blocks(kv_dtype, block_size, num_kv_heads, head_dim, src_blocks, dst_bl
     lib.pa_oracle_copy_blocks(2 if kv_dtype in (KV_BF16, KV_F16) else 1, block_size, num_kv_heads, head_dim,
                               _ptr(src), _ptr(dst), int(src.shape[0]), _ptr(kc), _ptr(vc))
     return kc, vc
+
+
+def bind_blocks(block_tables, seq_rows, hit_start, hit_blocks, refcounts):
+    """Zero-copy prefix hit: binds each new sequence's table row to its hit's
+    pages and counts one more owner per page.  Returns (block_tables,
+    refcounts, errors) as new arrays."""
+    lib = _load()
+    bt = _np(block_tables, np.int32).copy()
+    rc = _np(refcounts, np.int32).copy()
+    rows = _np(seq_rows, np.int32)
+    hs = _np(hit_start, np.int32)
+    hb = _np(hit_blocks, np.int32) if len(hit_blocks) else np.zeros(1, np.int32)
+    err = np.zeros(1, np.int32)
+    lib.pa_oracle_bind_blocks(_ptr(bt), int(bt.shape[1]), _ptr(rows), _ptr(hs), _ptr(hb), int(rows.shape[0]),
+                              _ptr(rc), int(rc.shape[0]), _ptr(err))
+    return bt, rc, int(err[0])
+
+
+def release_blocks(block_tables, seq_rows, block_counts, refcounts):
+    """Release of finished sequences (or evicted entries): one owner less for
+    each page of the given rows, entries set to -1, pages left without an
+    owner returned to the pool.  Returns (block_tables, refcounts, free_list,
+    errors) as new arrays."""
+    lib = _load()
+    bt = _np(block_tables, np.int32).copy()
+    rc = _np(refcounts, np.int32).copy()
+    rows = _np(seq_rows, np.int32)
+    cnt = _np(block_counts, np.int32)
+    free = np.zeros(max(1, rc.shape[0]), np.int32)
+    nfree = np.zeros(1, np.int32)
+    err = np.zeros(1, np.int32)
+    lib.pa_oracle_release_blocks(_ptr(bt), int(bt.shape[1]), _ptr(rows), _ptr(cnt), int(rows.shape[0]), _ptr(rc),
+                                 int(rc.shape[0]), _ptr(free), _ptr(nfree), _ptr(err))
+    return bt, rc, free[:int(nfree[0])].copy(), int(err[0])
 
 
 def merge(part_o, part_lse):

@@ -534,6 +534,64 @@ void pa_oracle_copy_blocks(int elem_bytes, int block_size, int num_kv_heads, int
   }
 }
 
+/* ------------------------------------------ prefix-cache page bookkeeping */
+
+/*
+ * Zero-copy cache hit ("Zero-Copy Cache Hits" of "1. Technical Mechanics of
+ * the Radix Cache"): the engine binds a new sequence's block table directly
+ * to the physical pages its matched prefix already occupies, and each bound
+ * page gains one owner.  For every i < num_seqs, with row = seq_rows[i] and
+ * the hit's pages hit_blocks[hit_start[i] .. hit_start[i+1]):
+ *   block_tables[row][j] = hit_blocks[hit_start[i] + j]   for each j,
+ *   refcounts[that page] += 1.
+ * A page outside [0, num_blocks) is not bound (counted in *errors).
+ */
+void pa_oracle_bind_blocks(int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_rows,
+                           const int32_t *hit_start, const int32_t *hit_blocks, int num_seqs, int32_t *refcounts,
+                           int num_blocks, int32_t *errors) {
+  for (int i = 0; i < num_seqs; ++i) {
+    int32_t *row = block_tables + (int64_t)seq_rows[i] * max_blocks_per_seq;
+    for (int j = 0; j < hit_start[i + 1] - hit_start[i]; ++j) {
+      int32_t blk = hit_blocks[hit_start[i] + j];
+      if (blk < 0 || blk >= num_blocks) {
+        ++*errors;
+        continue;
+      }
+      row[j] = blk;
+      refcounts[blk] += 1;
+    }
+  }
+}
+
+/*
+ * Release ("LRU Eviction": dropped entries return their memory blocks to
+ * the global page pool).  Each of the first block_counts[i] pages of table
+ * row seq_rows[i] loses one owner and its table entry becomes -1; a page
+ * whose owner count reaches zero goes back to the pool: it is appended to
+ * free_list at free_count, which grows by one.  (A finished sequence
+ * releases its own row; an evicted cache entry passes its pages as a row.)
+ * A page with no owner left, or outside [0, num_blocks), is left as it is
+ * (counted in *errors).  The order of the free list follows the pages in
+ * row-major order here; any order of the same pages is as valid.
+ */
+void pa_oracle_release_blocks(int32_t *block_tables, int max_blocks_per_seq, const int32_t *seq_rows,
+                              const int32_t *block_counts, int num_seqs, int32_t *refcounts, int num_blocks,
+                              int32_t *free_list, int32_t *free_count, int32_t *errors) {
+  for (int i = 0; i < num_seqs; ++i) {
+    int32_t *row = block_tables + (int64_t)seq_rows[i] * max_blocks_per_seq;
+    for (int j = 0; j < block_counts[i]; ++j) {
+      int32_t blk = row[j];
+      if (blk < 0 || blk >= num_blocks || refcounts[blk] <= 0) {
+        ++*errors;
+        continue;
+      }
+      row[j] = -1;
+      refcounts[blk] -= 1;
+      if (refcounts[blk] == 0) free_list[(*free_count)++] = blk;
+    }
+  }
+}
+
 /* ----------------------------------------------------------------- merge */
 
 /*

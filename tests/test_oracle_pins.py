@@ -681,3 +681,66 @@ def test_oracle_matches_its_golden_fixtures():
     for i, r in enumerate(rows):
         assert abs(float(r[2]) - lse[i]) <= 1e-13 * max(1.0, abs(lse[i]))
         np.testing.assert_allclose(out[i], np.array([float(x) for x in r[3:]]), rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------ prefix-cache page bookkeeping
+
+def _hit_case(seed=21, NB=64, S=6, MB=10):
+    rng = np.random.default_rng(seed)
+    tables = np.full((S, MB), -1, np.int32)
+    refc = rng.integers(0, 3, NB).astype(np.int32)
+    # two trie entries (page lists); sequences 1, 3, 4 hit them
+    a = rng.permutation(NB)[:5].astype(np.int32)
+    b = np.concatenate([a[:3], rng.permutation(NB)[:2].astype(np.int32)])
+    rows = np.array([1, 3, 4], np.int32)
+    hits = [a, b, a[:2]]
+    start = np.concatenate([[0], np.cumsum([len(h) for h in hits])]).astype(np.int32)
+    return tables, refc, rows, start, np.concatenate(hits), hits
+
+
+def test_bind_blocks_against_numpy_slices_and_bincount():
+    tables, refc, rows, start, flat, hits = _hit_case()
+    bt, rc, err = oracle.bind_blocks(tables, rows, start, flat, refc)
+    want_t = tables.copy()
+    for r, h in zip(rows, hits):
+        want_t[r, :len(h)] = h
+    want_rc = refc + np.bincount(flat, minlength=refc.shape[0]).astype(np.int32)
+    assert err == 0 and np.array_equal(bt, want_t) and np.array_equal(rc, want_rc)
+    # pages shared by several hits gain one owner per hit
+    assert rc[hits[0][0]] == refc[hits[0][0]] + 3
+
+
+def test_release_blocks_closed_form_and_round_trip():
+    tables, refc, rows, start, flat, hits = _hit_case()
+    bt, rc, _ = oracle.bind_blocks(tables, rows, start, flat, refc)
+    counts = np.array([len(h) for h in hits], np.int32)
+    bt2, rc2, free, err = oracle.release_blocks(bt, rows, counts, rc)
+    # releasing what was bound restores every count and empties the rows
+    assert err == 0 and np.array_equal(rc2, refc) and np.all(bt2[rows] == -1)
+    # pages that had no owner before the hit go back to the pool, each once
+    assert sorted(free.tolist()) == sorted(p for p in set(flat.tolist()) if refc[p] == 0)
+
+
+def test_release_returns_a_page_only_when_its_last_owner_leaves():
+    NB = 8
+    tables = np.array([[3, 5, -1], [3, 6, 7]], np.int32)
+    refc = np.zeros(NB, np.int32)
+    refc[[3, 5, 6, 7]] = [2, 1, 3, 1]
+    bt, rc, free, err = oracle.release_blocks(tables, np.array([0], np.int32), np.array([2], np.int32), refc)
+    assert err == 0 and rc.tolist() == [0, 0, 0, 1, 0, 0, 3, 1] and free.tolist() == [5]
+    assert bt.tolist() == [[-1, -1, -1], [3, 6, 7]]
+    bt, rc, free, err = oracle.release_blocks(bt, np.array([1], np.int32), np.array([3], np.int32), rc)
+    assert err == 0 and rc.tolist() == [0, 0, 0, 0, 0, 0, 2, 0] and sorted(free.tolist()) == [3, 7]
+
+
+def test_bookkeeping_errors_leave_pages_untouched():
+    NB = 4
+    refc = np.array([0, 1, 0, 0], np.int32)
+    tables = np.array([[0, 1, 9]], np.int32)
+    bt, rc, free, err = oracle.release_blocks(tables, np.array([0], np.int32), np.array([3], np.int32), refc)
+    # page 0 has no owner, page 9 is outside the pool: both errors; page 1 freed
+    assert err == 2 and rc.tolist() == [0, 0, 0, 0] and free.tolist() == [1]
+    assert bt.tolist() == [[0, -1, 9]]
+    bt, rc, err = oracle.bind_blocks(np.full((1, 3), -1, np.int32), np.array([0], np.int32),
+                                     np.array([0, 2], np.int32), np.array([2, -1], np.int32), rc)
+    assert err == 1 and bt.tolist() == [[2, -1, -1]] and rc.tolist() == [0, 0, 1, 0]
