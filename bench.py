@@ -137,17 +137,33 @@ class ClockSampler:
         self.thread = None
         self.t0 = self.t1 = None
         self.stopping = False
+        self.target = None
 
     def _target(self) -> str:
+        """The GPU as nvidia-smi names it: CUDA's UUID where nvidia-smi reports
+        the same one (some boxes hide UUIDs from nvidia-smi), else the
+        nvidia-smi index of the visible device (CUDA_VISIBLE_DEVICES maps
+        CUDA's numbering onto it)."""
         try:
             import torch
             u = str(torch.cuda.get_device_properties(self.gpu).uuid)
-            return u if u.startswith("GPU-") else "GPU-" + u
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            r = subprocess.run(["nvidia-smi", "-i", u, "--query-gpu=index", "--format=csv,noheader"],
+                               capture_output=True, text=True, timeout=20)
+            if r.returncode == 0 and r.stdout.strip().isdigit():
+                return u
         except Exception:
-            return str(self.gpu)
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if len(ids) > self.gpu and ids[self.gpu].isdigit():
+            return ids[self.gpu]
+        return str(self.gpu)
 
     def _spawn(self):
-        return subprocess.Popen(["nvidia-smi", "-i", self._target(), f"--query-gpu={self.FIELDS}",
+        if self.target is None:
+            self.target = self._target()
+        return subprocess.Popen(["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}",
                                  "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                 stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
 
@@ -243,8 +259,11 @@ def _local_config(args) -> dict:
     if args.per_head_scales:
         d["fp8_scales"] = "per kv head"
     if args.workload == 5:
-        d["mixed_step"] = ("decode and prefill in order on one stream" if args.serial_mixed else
-                           "decode on a second stream beside the prefill, after the cache write")
+        d["mixed_step"] = {"fused": "cache write, then decode and prefill in one persistent launch",
+                           "streams": "cache write, then the decode on a second stream beside the prefill",
+                           "serial": "cache write, decode, prefill in order on one stream"}[args.mixed_mode]
+    if args.prefill_impl:
+        d["prefill_impl"] = {1: "mma.sync", 2: "tcgen05, fp16 P.V", 3: "tcgen05, P as a hi + lo pair"}[args.prefill_impl]
     if args.sliding_window:
         d["sliding_window"] = args.sliding_window
     if args.attention_chunk:
@@ -300,7 +319,7 @@ def run_ours(args):
     from paged_kv_attention_14_gb300 import build as pa_build
     from paged_kv_attention_14_gb300 import binding as B
     from paged_kv_attention_14_gb300 import workloads as W
-    from paged_kv_attention_14_gb300.step import MixedStep
+    from paged_kv_attention_14_gb300.step import GraphedStep, MixedStep
 
     ws, rank, local = _dist()
     if ws > 1:
@@ -316,6 +335,7 @@ def run_ours(args):
     kv8 = kv in (B.PA_KV_FP8_E4M3, B.PA_KV_FP8_E5M2)
     desc = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, kv,
                        b.k_scale if kv8 else 0.0, b.v_scale if kv8 else 0.0, decode_impl=args.decode_impl,
+                       prefill_impl=args.prefill_impl,
                        sliding_window=args.sliding_window, attention_chunk=args.attention_chunk,
                        k_scales=b.k_scales, v_scales=b.v_scales)
     if not kv8:
@@ -333,7 +353,7 @@ def run_ours(args):
     out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
     kv_bytes = _decode_kv_bytes(b, args.sliding_window, args.attention_chunk)
     # the captured traffic figures are for the default settings only
-    local = bool(args.sliding_window or args.attention_chunk or args.fp16 or args.per_head_scales)
+    local = bool(args.sliding_window or args.attention_chunk or args.fp16 or args.per_head_scales or args.prefill_impl)
     mixed = b.q_prefill is not None
     if mixed:
         pf_out = torch.empty(b.q_prefill.shape, dtype=torch.float32, device=dev)
@@ -351,12 +371,12 @@ def run_ours(args):
         # the timed kernels start instead of during them
         flush = _L2Flush(2 * l2_bytes, dev)
 
-    # mixed step: after the cache write, the decode runs on a second stream
-    # beside the prefill, so that its CTAs take the SMs the prefill's last
-    # wave leaves idle (--serial-mixed issues them one after the other)
+    # mixed step: after the cache write, decode and prefill in one persistent
+    # launch (--mixed-mode fused), the decode on a second stream beside the
+    # prefill (streams) or one after the other (serial)
     ms = MixedStep(desc, kc, vc, b.scale, decode_out=out, workspace=wsp, max_context_len_decode=maxL,
                    prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
-                   max_context_len_prefill=pf_maxL if mixed else 0, overlap=not args.serial_mixed)
+                   max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode)
     decode, prefill, attend = ms.decode, ms.prefill, ms.attend
 
     def step():
@@ -464,16 +484,22 @@ def run_ours(args):
     h2d = total
     d2h = out_host.numel() * out_host.element_size() + (pf_host.numel() * pf_host.element_size() if mixed else 0)
 
-    def e2e_step():
+    def e2e_issue():
         dev_buf.copy_(host_buf, non_blocking=True)
-        B.pa_cache_write(desc, views["k_new"], views["v_new"], kc, vc, views["slot_mapping"])
-        attend((views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
-               (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
-                views["context_lens_prefill"]) if mixed else None)
+        ms(views["k_new"], views["v_new"], views["slot_mapping"],
+           (views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
+           (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
+            views["context_lens_prefill"]) if mixed else None)
         if mixed:
             pf_host.copy_(pf_out, non_blocking=True)
         out_host.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+
+    # the public API's step as a user drives it: one CUDA-graph replay of the
+    # copies in, the step and the copies out, then a wait for the result
+    graphed = GraphedStep(e2e_issue)
+
+    def e2e_step():
+        graphed()
 
     for _ in range(max(3, args.warmup)):
         if flush is not None:
@@ -523,7 +549,10 @@ def run_ours(args):
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
                          "traffic": _traffic("decode", args.workload, local)},
             "e2e": {"value": round(_job_throughput(ws, kv_bytes, e2e_s) / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "how": "step.GraphedStep: one CUDA-graph replay per step of the pinned-host-to-device copy of the "
+                           "inputs, the cache write and attention, and the copy of the outputs to pinned host memory, "
+                           "then a wait; host wall clock"},
             "gpu_launches": launches_per_step * K * R + (launches_per_step - 1) * K2 * R2,
             "timed_repeats": {"steps": R, "kernels_alone": R2,
                               "note": f"each repeat times exactly {K} steps ({K2} calls of each entry point alone); "
@@ -698,10 +727,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--decode-impl", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--prefill-impl", type=int, default=0,
+                    help="0 auto, 1 mma.sync, 2 tcgen05 (fp16 P.V), 3 tcgen05 (P as a hi + lo pair)")
     ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
                     help="8-bit cache format of workload 4 (same shapes)")
-    ap.add_argument("--serial-mixed", action="store_true",
-                    help="mixed step (workload 5): decode and prefill one after the other on one stream")
+    ap.add_argument("--mixed-mode", choices=["fused", "streams", "serial"], default="fused",
+                    help="mixed step (workload 5): one persistent launch, two streams, or one after the other")
     ap.add_argument("--per-head-scales", action="store_true",
                     help="workload 4 with one FP8 scale per kv head (heads of different magnitudes)")
     ap.add_argument("--fp16", action="store_true",

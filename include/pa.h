@@ -77,7 +77,8 @@ extern "C" {
  * 2: pa_kv_desc gains sliding_window, attention_chunk, k_scales, v_scales
  *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks.
  * 3: pa_kv_desc gains error_word, check_indices (appended); PA_DEVERR_*;
- *    pa_test_stall_pipelines. */
+ *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
+ *    pa_release_blocks, pa_mixed_attention. */
 #define PA_ABI_VERSION 3
 
 /* Symbols of the shared library; everything else in it stays hidden. */
@@ -111,6 +112,12 @@ typedef enum {
 #define PA_DEVERR_WAIT_TIMEOUT 1 /* a bounded wait ran out; outputs incomplete */
 #define PA_DEVERR_BAD_INDEX 2    /* check_indices: a block id, length or slot
                                     was out of range; results meaningless      */
+#define PA_DEVERR_FP16_RANGE 4   /* the tcgen05 prefill (PA_PREFILL_TCGEN05) met a
+                                    finite bf16 V value of magnitude >= 65536,
+                                    beyond its fp16 P.V product; the rows using
+                                    it are wrong: use PA_PREFILL_TCGEN05_PAIR */
+#define PA_DEVERR_REFCOUNT 8     /* pa_release_blocks met a page with no owner
+                                    left; that entry was left untouched        */
 
 /* Which decode kernel pa_decode runs.  0 lets the library choose. */
 typedef enum {
@@ -122,8 +129,12 @@ typedef enum {
 /* Which prefill kernel pa_prefill_chunk runs.  0 lets the library choose. */
 typedef enum {
   PA_PREFILL_AUTO = 0,
-  PA_PREFILL_MMA_SYNC = 1, /* warp-level mma.sync tiles; every cache type      */
-  PA_PREFILL_TCGEN05 = 2   /* tcgen05 tensor-memory tiles; bf16, fp16 caches  */
+  PA_PREFILL_MMA_SYNC = 1,    /* warp-level mma.sync tiles; every cache type; P
+                                 as a hi + lo pair                              */
+  PA_PREFILL_TCGEN05 = 2,     /* tcgen05 tensor-memory tiles; bf16, fp16
+                                 caches; P.V in fp16 (see PA_DEVERR_FP16_RANGE) */
+  PA_PREFILL_TCGEN05_PAIR = 3 /* tcgen05 tiles with P as a hi + lo pair of the
+                                 cache's type: any bf16 range, more tensor work */
 } pa_prefill_impl;
 
 /*
@@ -265,6 +276,37 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
                            float scale, pa_stream_t stream);
 
 /*
+ * Decode and chunked-prefill attention of one continuous-batch step in a
+ * single launch (the step of the "C++20 Continuous Batching Loop" in the
+ * "vllm.cpp ARCHITECTURE OVERVIEW" figure; the unified scheduler with
+ * chunked prefill of the vllm.cpp repository's Engine core bullet).  It
+ * computes what pa_decode computes for the dec_* arguments and what
+ * pa_prefill_chunk computes for the pf_* arguments, over the same caches,
+ * in one persistent launch whose CTAs take the prefill's tiles (longest key
+ * ranges first) and then the decode's partitions from one work list: the
+ * decode fills the SMs the prefill's last wave leaves idle.  Issue the
+ * step's pa_cache_write first, on the same stream.
+ *   workspace : pa_decode_workspace_size(desc, num_dec_seqs,
+ *               dec_max_context_len) bytes, zero-filled before its first use;
+ *               every call that completes without error leaves it ready for
+ *               the next (its counters back at zero).  Calls that overlap on
+ *               the GPU need separate workspaces.
+ * Either part may be empty (num_dec_seqs == 0 or num_pf_seqs == 0).  Takes
+ * bf16 and fp16 caches with head_dim 128, decode_impl AUTO or MMA and
+ * prefill_impl AUTO or TCGEN05; PA_ERR_UNSUPPORTED otherwise (make the two
+ * calls instead).
+ */
+PA_API pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
+                                    const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                    const int32_t *dec_context_lens, int32_t num_dec_seqs,
+                                    int32_t dec_max_context_len, float *pf_out, float *pf_lse, const void *pf_q,
+                                    const int32_t *query_start_loc, const int32_t *pf_block_tables,
+                                    int32_t pf_max_blocks_per_seq, const int32_t *pf_context_lens,
+                                    int32_t num_pf_seqs, int32_t max_q_len, int32_t pf_max_context_len,
+                                    const void *k_cache, const void *v_cache, float scale, void *workspace,
+                                    size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * Shared-prefix (cascade) attention.  A prefix-cache hit binds several
  * sequences to the same physical pages ("Zero-Copy Cache Hits" of "1.
  * Technical Mechanics of the Radix Cache"); their queries can attend that
@@ -313,6 +355,51 @@ PA_API pa_status pa_prefix_attention(const pa_kv_desc *desc, float *out, float *
  */
 PA_API pa_status pa_copy_blocks(const pa_kv_desc *desc, void *k_cache, void *v_cache, const int32_t *src_blocks,
                                 const int32_t *dst_blocks, int32_t num_pairs, pa_stream_t stream);
+
+/*
+ * Prefix-cache page bookkeeping on the device ("1. Technical Mechanics of
+ * the Radix Cache": a hit binds the new sequence's block table directly to
+ * the pages of its matched prefix, "Zero-Copy Cache Hits"; eviction returns
+ * pages to the global page pool, "LRU Eviction").  The radix tree, the LRU
+ * order and the choice of what to evict stay with the caller; these calls
+ * keep the page tables and the owner counts on the device.
+ *   block_tables : int32 [num_table_rows][max_blocks_per_seq]
+ *   refcounts    : int32 [desc->num_blocks], owners of each page
+ * Table rows, hit lengths and page ids are always range-checked: an entry
+ * outside the table or the pool is skipped and sets PA_DEVERR_BAD_INDEX in
+ * desc->error_word (when given).  Owner counts change atomically, so
+ * several sequences of one call may share pages; two entries of one call
+ * must not write the same table slot.
+ *
+ * pa_bind_blocks: for every i < num_seqs, table row seq_rows[i] gets the
+ * hit's pages hit_blocks[hit_start[i] .. hit_start[i+1]) in its first
+ * entries, and each of those pages gains one owner.
+ *   seq_rows   : int32 [num_seqs]
+ *   hit_start  : int32 [num_seqs + 1], non-decreasing
+ *   hit_blocks : int32 [hit_start[num_seqs]]
+ */
+PA_API pa_status pa_bind_blocks(const pa_kv_desc *desc, int32_t *block_tables, int32_t max_blocks_per_seq,
+                                int32_t num_table_rows, const int32_t *seq_rows, const int32_t *hit_start,
+                                const int32_t *hit_blocks, int32_t num_seqs, int32_t *refcounts,
+                                pa_stream_t stream);
+
+/*
+ * pa_release_blocks: for every i < num_seqs, each of the first
+ * block_counts[i] pages of table row seq_rows[i] loses one owner and its
+ * entry becomes -1 (a finished sequence releases its own row; an evicted
+ * cache entry can pass its pages as a row of its own table).  A page whose
+ * owner count reaches zero returns to the pool: it is written to
+ * free_list[*free_count] and *free_count grows by one (atomically, so the
+ * order of the pages a call frees is unspecified).  A page with no owner
+ * left is not touched and sets PA_DEVERR_REFCOUNT.
+ *   block_counts : int32 [num_seqs]
+ *   free_list    : int32 [desc->num_blocks]; free_count : one int32, the
+ *                  number of entries already in it (device)
+ */
+PA_API pa_status pa_release_blocks(const pa_kv_desc *desc, int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   int32_t num_table_rows, const int32_t *seq_rows, const int32_t *block_counts,
+                                   int32_t num_seqs, int32_t *refcounts, int32_t *free_list, int32_t *free_count,
+                                   pa_stream_t stream);
 
 /*
  * Merge of attention results over disjoint key ranges (split-KV pieces, or a

@@ -37,16 +37,20 @@ PA_DECODE_MMA = 2
 PA_PREFILL_AUTO = 0
 PA_PREFILL_MMA_SYNC = 1
 PA_PREFILL_TCGEN05 = 2
+PA_PREFILL_TCGEN05_PAIR = 3
 
 PA_DEVERR_WAIT_TIMEOUT = 1
 PA_DEVERR_BAD_INDEX = 2
+PA_DEVERR_FP16_RANGE = 4
+PA_DEVERR_REFCOUNT = 8
 
 #: every symbol include/pa.h declares
 #: PA_ABI_VERSION this binding is written against (pa_kv_desc layout, entry points)
 ABI_VERSION = 3
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
-            "pa_copy_blocks", "pa_test_stall_pipelines")
+            "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
+            "pa_mixed_attention")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -113,6 +117,13 @@ def load(path: Optional[str] = None):
         lib.pa_merge_partials.restype = ctypes.c_int
         lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
         lib.pa_decode_static.restype = ctypes.c_int
+        lib.pa_mixed_attention.argtypes = [D, P, P, P, P, I32, P, I32, I32, P, P, P, P, P, I32, P, I32, I32, I32,
+                                           P, P, F, P, SZ, P]
+        lib.pa_mixed_attention.restype = ctypes.c_int
+        lib.pa_bind_blocks.argtypes = [D, P, I32, I32, P, P, P, I32, P, P]
+        lib.pa_bind_blocks.restype = ctypes.c_int
+        lib.pa_release_blocks.argtypes = [D, P, I32, I32, P, P, I32, P, P, P, P]
+        lib.pa_release_blocks.restype = ctypes.c_int
         lib.pa_test_stall_pipelines.argtypes = [I32, ctypes.c_int64]
         lib.pa_test_stall_pipelines.restype = ctypes.c_int
         if lib.pa_abi_version() != ABI_VERSION:
@@ -247,6 +258,35 @@ def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, con
                                    float(scale), _stream(stream)))
 
 
+def pa_mixed_attention(desc: PaKvDesc, k_cache, v_cache, scale: float, workspace, dec=None, pf=None, stream=None):
+    """Decode and prefill attention of one step in one launch.  ``dec``:
+    (out, q, block_tables, context_lens, max_context_len[, lse]) or None;
+    ``pf``: (out, q, query_start_loc, block_tables, context_lens, max_q_len,
+    max_context_len[, lse]) or None.  ``workspace``: a decode workspace
+    (decode_workspace) for the decode part's batch."""
+    if dec is not None:
+        d_out, d_q, d_bt, d_cl, d_maxL = dec[:5]
+        d_lse = dec[5] if len(dec) > 5 else None
+        dargs = (_ptr(d_out, _F32, "dec out"), _ptr(d_lse, _F32, "dec lse", allow_none=True), _ptr(d_q, _act(desc), "dec q"),
+                 _ptr(d_bt, _I32, "dec block_tables"), int(d_bt.shape[1]), _ptr(d_cl, _I32, "dec context_lens"),
+                 int(d_cl.shape[0]), int(d_maxL))
+    else:
+        dargs = (None, None, None, None, 1, None, 0, 0)
+    if pf is not None:
+        p_out, p_q, p_qsl, p_bt, p_cl, p_maxq, p_maxL = pf[:7]
+        p_lse = pf[7] if len(pf) > 7 else None
+        pargs = (_ptr(p_out, _F32, "prefill out"), _ptr(p_lse, _F32, "prefill lse", allow_none=True),
+                 _ptr(p_q, _act(desc), "prefill q"), _ptr(p_qsl, _I32, "query_start_loc"),
+                 _ptr(p_bt, _I32, "prefill block_tables"), int(p_bt.shape[1]), _ptr(p_cl, _I32, "prefill context_lens"),
+                 int(p_cl.shape[0]), int(p_maxq), int(p_maxL))
+    else:
+        pargs = (None, None, None, None, None, 1, None, 0, 0, 0)
+    _check(load().pa_mixed_attention(ctypes.byref(desc), *dargs, *pargs, _ptr(k_cache, _CACHE, "k_cache"),
+                                     _ptr(v_cache, _CACHE, "v_cache"), float(scale),
+                                     _ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
+                                     _stream(stream)))
+
+
 def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, block_tables,
                      context_lens, max_q_len: int, max_context_len: int, scale: float, lse=None,
                      stream=None):
@@ -293,6 +333,29 @@ def pa_copy_blocks(desc: PaKvDesc, k_cache, v_cache, src_blocks, dst_blocks, str
                                  _ptr(v_cache, _CACHE, "v_cache"), _ptr(src_blocks, _I32, "src_blocks"),
                                  _ptr(dst_blocks, _I32, "dst_blocks"), int(src_blocks.shape[0]),
                                  _stream(stream)))
+
+
+def pa_bind_blocks(desc: PaKvDesc, block_tables, seq_rows, hit_start, hit_blocks, refcounts, stream=None):
+    """Zero-copy prefix hits: row seq_rows[i] of block_tables gets the pages
+    hit_blocks[hit_start[i]:hit_start[i+1]]; each page gains an owner in refcounts."""
+    _check(load().pa_bind_blocks(ctypes.byref(desc), _ptr(block_tables, _I32, "block_tables"),
+                                 int(block_tables.shape[1]), int(block_tables.shape[0]),
+                                 _ptr(seq_rows, _I32, "seq_rows"), _ptr(hit_start, _I32, "hit_start"),
+                                 _ptr(hit_blocks, _I32, "hit_blocks"), int(seq_rows.shape[0]),
+                                 _ptr(refcounts, _I32, "refcounts"), _stream(stream)))
+
+
+def pa_release_blocks(desc: PaKvDesc, block_tables, seq_rows, block_counts, refcounts, free_list, free_count,
+                      stream=None):
+    """Release: the first block_counts[i] pages of row seq_rows[i] lose an owner
+    (entries set to -1); pages left without owners are appended to free_list at
+    free_count."""
+    _check(load().pa_release_blocks(ctypes.byref(desc), _ptr(block_tables, _I32, "block_tables"),
+                                    int(block_tables.shape[1]), int(block_tables.shape[0]),
+                                    _ptr(seq_rows, _I32, "seq_rows"), _ptr(block_counts, _I32, "block_counts"),
+                                    int(seq_rows.shape[0]), _ptr(refcounts, _I32, "refcounts"),
+                                    _ptr(free_list, _I32, "free_list"), _ptr(free_count, _I32, "free_count"),
+                                    _stream(stream)))
 
 
 def pa_test_stall_pipelines(enable: bool, wait_limit_ns: int = 20_000_000):

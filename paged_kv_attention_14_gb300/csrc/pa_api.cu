@@ -108,6 +108,35 @@ pa_status validate_decode(const pa_kv_desc *desc, const float *out, const float 
   return PA_OK;
 }
 
+pa_status validate_prefill(const pa_kv_desc *desc, const float *out, const float *lse, const void *q,
+                           const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t max_q_len, int32_t max_context_len, float scale) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and max_q_len must be >= 0%s");
+  if (num_seqs == 0 || max_q_len == 0) return PA_OK;
+  if (num_seqs > 65535)  // one grid row of CTAs per sequence
+    return fail(PA_ERR_UNSUPPORTED, "a prefill takes at most 65535 sequences per call%s");
+  if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PA_ERR_INVALID_ARG,
+                "out, q, query_start_loc, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(PA_ERR_INVALID_ARG,
+                "block_tables, context_lens, query_start_loc and lse must be 4-byte aligned%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
+  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
+  const char *why = "";
+  st = check_prefill(*desc, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  return PA_OK;
+}
+
 }  // namespace pa
 
 extern "C" {
@@ -172,31 +201,52 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
                            float scale, pa_stream_t stream) {
-  pa_status st = check_desc(desc);
+  const pa_status st = pa::validate_prefill(desc, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, max_context_len,
+                                            scale);
   if (st != PA_OK) return st;
-  if (num_seqs < 0 || max_q_len < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and max_q_len must be >= 0%s");
   if (num_seqs == 0 || max_q_len == 0) return ok();
-  if (num_seqs > 65535)  // one grid row of CTAs per sequence
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill_chunk takes at most 65535 sequences per call%s");
-  if (!out || !q || !query_start_loc || !k_cache || !v_cache || !block_tables || !context_lens)
-    return fail(PA_ERR_INVALID_ARG,
-                "out, q, query_start_loc, k_cache, v_cache, block_tables and context_lens must be non-NULL%s");
-  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
-    return fail(PA_ERR_INVALID_ARG, "out, q, k_cache and v_cache must be 16-byte aligned%s");
-  if ((reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(query_start_loc) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return fail(PA_ERR_INVALID_ARG,
-                "block_tables, context_lens, query_start_loc and lse must be 4-byte aligned%s");
-  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
-  if (max_context_len < 0 || static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
-    return fail(PA_ERR_INVALID_ARG, "max_context_len must lie in [0, max_blocks_per_seq * block_size]%s");
-  if (!(scale == scale)) return fail(PA_ERR_INVALID_ARG, "scale is NaN%s");
-  const char *why = "";
-  st = pa::check_prefill(*desc, &why);
-  if (st != PA_OK) return fail(st, "%s", why);
   const cudaError_t e = pa::launch_prefill(*desc, out, lse, q, query_start_loc, k_cache, v_cache,
                                            block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                            max_q_len, scale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
+                             const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
+                             const int32_t *dec_context_lens, int32_t num_dec_seqs, int32_t dec_max_context_len,
+                             float *pf_out, float *pf_lse, const void *pf_q, const int32_t *query_start_loc,
+                             const int32_t *pf_block_tables, int32_t pf_max_blocks_per_seq,
+                             const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
+                             int32_t pf_max_context_len, const void *k_cache, const void *v_cache, float scale,
+                             void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  // the decode part's checks (and its plan, whose workspace the call uses);
+  // with no decode sequence only the descriptor and the plan of an empty batch
+  pa::DecodePlan plan;
+  pa_status st = pa::validate_decode(desc, dec_out, dec_lse, dec_q, k_cache, v_cache, dec_block_tables,
+                                     dec_max_blocks_per_seq, dec_context_lens, num_dec_seqs, dec_max_context_len,
+                                     scale, &plan);
+  if (st != PA_OK) return st;
+  if (num_dec_seqs == 0) {
+    const char *why = "";
+    st = pa::plan_decode(*desc, 0, &plan, &why);
+    if (st != PA_OK) return fail(st, "%s", why);
+  }
+  st = pa::validate_prefill(desc, pf_out, pf_lse, pf_q, query_start_loc, k_cache, v_cache, pf_block_tables,
+                            pf_max_blocks_per_seq, pf_context_lens, num_pf_seqs, max_q_len, pf_max_context_len, scale);
+  if (st != PA_OK) return st;
+  const char *why = "";
+  st = pa::check_mixed(*desc, plan, &why);
+  if (st != PA_OK) return fail(st, "%s", why);
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
+  if (workspace_bytes < plan.workspace_bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_decode_workspace_size()%s");
+  const cudaError_t e = pa::launch_mixed(*desc, plan, dec_out, dec_lse, dec_q, dec_block_tables,
+                                         dec_max_blocks_per_seq, dec_context_lens, num_dec_seqs, pf_out, pf_lse, pf_q,
+                                         query_start_loc, pf_block_tables, pf_max_blocks_per_seq, pf_context_lens,
+                                         num_pf_seqs, max_q_len, k_cache, v_cache, scale, workspace,
+                                         reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 
@@ -258,6 +308,50 @@ pa_status pa_copy_blocks(const pa_kv_desc *desc, void *k_cache, void *v_cache, c
     return fail(PA_ERR_INVALID_ARG, "src_blocks and dst_blocks must be 4-byte aligned%s");
   const cudaError_t e = pa::launch_copy_blocks(*desc, k_cache, v_cache, src_blocks, dst_blocks, num_pairs,
                                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_bind_blocks(const pa_kv_desc *desc, int32_t *block_tables, int32_t max_blocks_per_seq,
+                         int32_t num_table_rows, const int32_t *seq_rows, const int32_t *hit_start,
+                         const int32_t *hit_blocks, int32_t num_seqs, int32_t *refcounts, pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_table_rows < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and num_table_rows must be >= 0%s");
+  if (num_seqs == 0) return ok();
+  if (num_seqs > 0x7fffffff / 2) return fail(PA_ERR_UNSUPPORTED, "too many sequences%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (!block_tables || !seq_rows || !hit_start || !hit_blocks || !refcounts)
+    return fail(PA_ERR_INVALID_ARG, "block_tables, seq_rows, hit_start, hit_blocks and refcounts must be non-NULL%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(seq_rows) |
+       reinterpret_cast<uintptr_t>(hit_start) | reinterpret_cast<uintptr_t>(hit_blocks) |
+       reinterpret_cast<uintptr_t>(refcounts)) & 3u)
+    return fail(PA_ERR_INVALID_ARG, "the page-table arrays must be 4-byte aligned%s");
+  const cudaError_t e = pa::launch_bind_blocks(*desc, block_tables, max_blocks_per_seq, num_table_rows, seq_rows,
+                                               hit_start, hit_blocks, num_seqs, refcounts,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_release_blocks(const pa_kv_desc *desc, int32_t *block_tables, int32_t max_blocks_per_seq,
+                            int32_t num_table_rows, const int32_t *seq_rows, const int32_t *block_counts,
+                            int32_t num_seqs, int32_t *refcounts, int32_t *free_list, int32_t *free_count,
+                            pa_stream_t stream) {
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs < 0 || num_table_rows < 0) return fail(PA_ERR_INVALID_ARG, "num_seqs and num_table_rows must be >= 0%s");
+  if (num_seqs == 0) return ok();
+  if (num_seqs > 0x7fffffff / 2) return fail(PA_ERR_UNSUPPORTED, "too many sequences%s");
+  if (max_blocks_per_seq <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq must be positive%s");
+  if (!block_tables || !seq_rows || !block_counts || !refcounts || !free_list || !free_count)
+    return fail(PA_ERR_INVALID_ARG,
+                "block_tables, seq_rows, block_counts, refcounts, free_list and free_count must be non-NULL%s");
+  if ((reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(seq_rows) |
+       reinterpret_cast<uintptr_t>(block_counts) | reinterpret_cast<uintptr_t>(refcounts) |
+       reinterpret_cast<uintptr_t>(free_list) | reinterpret_cast<uintptr_t>(free_count)) & 3u)
+    return fail(PA_ERR_INVALID_ARG, "the page-table arrays must be 4-byte aligned%s");
+  const cudaError_t e = pa::launch_release_blocks(*desc, block_tables, max_blocks_per_seq, num_table_rows, seq_rows,
+                                                  block_counts, num_seqs, refcounts, free_list, free_count,
+                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 

@@ -3,6 +3,7 @@
 // pa_decode_kernels.cuh (instantiated by pa_decode_simt.cu and
 // pa_decode_mma_*.cu).
 #include "pa_decode_kernels.cuh"
+#include "pa_host_cache.h"
 
 namespace pa {
 
@@ -77,7 +78,7 @@ EncodeTiledFn encode_tiled() {
 // one block.  Rows of 256 bytes (bf16, head_dim 128) are cut into two
 // 128-byte halves so that the 128-byte swizzle applies: by a third
 // dimension (one box per tile) or by two boxes per tile (see kWideMode).
-bool make_cache_map(CUtensorMap *map, const void *base, const pa_kv_desc &d, const KernelInfo &k) {
+bool encode_cache_map(CUtensorMap *map, const void *base, const pa_kv_desc &d, const KernelInfo &k) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return false;
   const bool bf = d.kv_dtype == PA_KV_BF16 || d.kv_dtype == PA_KV_F16;  // 2-byte elements
@@ -111,6 +112,16 @@ bool make_cache_map(CUtensorMap *map, const void *base, const pa_kv_desc &d, con
   return r == CUDA_SUCCESS;
 }
 
+// encode_cache_map, remembered per thread for the last few caches
+bool make_cache_map(CUtensorMap *map, const void *base, const pa_kv_desc &d, const KernelInfo &k) {
+  thread_local MapCache<> cache;
+  const MapKey key = map_key(base, d.num_blocks, d.num_kv_heads, d.head_dim, d.kv_dtype, k.hg, k.swizzle, k.wide_mode);
+  if (cache.find(key, map)) return true;
+  if (!encode_cache_map(map, base, d, k)) return false;
+  cache.put(key, *map);
+  return true;
+}
+
 }  // namespace
 
 int device_sm_count() { return device_info().sm_count; }
@@ -131,12 +142,8 @@ pa_status plan_decode(const pa_kv_desc &d, int32_t num_seqs, DecodePlan *plan, c
     return PA_ERR_UNSUPPORTED;
   }
   const KernelInfo k = kernel_for(d, impl);
-  if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(k.smem)) != cudaSuccess) {
-    *why = "cudaFuncSetAttribute(MaxDynamicSharedMemorySize) failed";
-    return PA_ERR_CUDA;
-  }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k.fn, k.threads, k.smem) != cudaSuccess || occ < 1) {
+  const int occ = prepare_kernel(k.fn, k.threads, k.smem);
+  if (occ < 1) {
     *why = "the decode kernel does not fit on this device";
     return PA_ERR_CUDA;
   }
@@ -149,19 +156,19 @@ pa_status plan_decode(const pa_kv_desc &d, int32_t num_seqs, DecodePlan *plan, c
   return PA_OK;
 }
 
-cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse,
-                          const void *q, const void *k_cache, const void *v_cache,
-                          const int32_t *block_tables, int32_t max_blocks_per_seq,
-                          const int32_t *context_lens, int32_t num_seqs, float scale,
-                          void *workspace, cudaStream_t stream) {
+namespace dec {
+
+bool make_decode_args(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse, const void *q,
+                      const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs, float scale,
+                      void *workspace, DecodeArgs *ap) {
   const KernelInfo k = kernel_for(d, plan.impl);
   const dec::WsLayout w = dec::ws_layout(num_seqs, plan.num_groups, plan.num_ctas, plan.slot_heads, d.head_dim);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  dec::DecodeArgs a;
+  DecodeArgs &a = *ap;
   memset(&a, 0, sizeof a);
   if (k.mma) {
-    if (!make_cache_map(&a.kmap, k_cache, d, k) || !make_cache_map(&a.vmap, v_cache, d, k))
-      return cudaErrorInvalidValue;
+    if (!make_cache_map(&a.kmap, k_cache, d, k) || !make_cache_map(&a.vmap, v_cache, d, k)) return false;
   }
   a.out = out;
   a.lse = lse;
@@ -195,6 +202,21 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
   a.seg_counter = reinterpret_cast<int32_t *>(ws + w.counter_off);
   a.slot_lse = reinterpret_cast<float *>(ws + w.slot_lse_off);
   a.slot_o = reinterpret_cast<float *>(ws + w.slot_o_off);
+  return true;
+}
+
+}  // namespace dec
+
+cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse,
+                          const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          const int32_t *context_lens, int32_t num_seqs, float scale,
+                          void *workspace, cudaStream_t stream) {
+  const KernelInfo k = kernel_for(d, plan.impl);
+  dec::DecodeArgs a;
+  if (!dec::make_decode_args(d, plan, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                             num_seqs, scale, workspace, &a))
+    return cudaErrorInvalidValue;
   // programmatic dependent launch: the kernel's launch overlaps the tail of
   // the preceding kernel in the stream (typically pa_cache_write); the kernel
   // waits for that kernel's writes before reading anything

@@ -182,12 +182,12 @@ __device__ inline void zero_sequence(const DecodeArgs &a, int s, int D) {
 // --------------------------------------------------------- shared framework
 
 // Pass over context_lens by one warp: the number of 16-token blocks of all
-// sequences; empty sequences are zero-filled by the CTA s % gridDim.x.
+// sequences; empty sequences are zero-filled by the CTA (or partition) me
+// = s % G of the G that split the work.
 template <int D>
-__device__ long long count_blocks(const DecodeArgs &a, int lane) {
+__device__ long long count_blocks(const DecodeArgs &a, int lane, int me, int G) {
   long long nb_sum = 0;
   const int S = a.num_seqs;
-  const int G = gridDim.x;
   for (int base = 0; base < S; base += 256) {
     unsigned acc = 0;
 #pragma unroll
@@ -197,7 +197,7 @@ __device__ long long count_blocks(const DecodeArgs &a, int lane) {
         const int L = seq_len(a, s);
         if (L > 0)
           acc += static_cast<unsigned>(seq_blocks(a, L));
-        else if (s % G == static_cast<int>(blockIdx.x))
+        else if (s % G == me)
           zero_sequence(a, s, D);
       }
     }
@@ -218,12 +218,12 @@ __device__ long long count_blocks(const DecodeArgs &a, int lane) {
 // the launch.
 template <class Cfg>
 __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uint64_t *full,
-                        uint64_t *empty, long long per_cta, long long total, int lane) {
+                        uint64_t *empty, long long per_cta, long long total, int lane, int me) {
   constexpr int NS = Cfg::NS;
   constexpr int BPS = Cfg::BPS;
   const int S = a.num_seqs;
   const int NG = a.num_groups;
-  const long long b0 = static_cast<long long>(blockIdx.x) * per_cta;
+  const long long b0 = static_cast<long long>(me) * per_cta;
   const long long b1 = min(b0 + per_cta, total);
   const uint64_t pol = l2_evict_first_policy();
   // test hook: issue nothing and signal nothing, so that every consumer
@@ -394,9 +394,9 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
     }
   }
   PA_TRACE(if (lane == 0) {
-    g_pa_trace[blockIdx.x][3] = tp_empty;
-    g_pa_trace[blockIdx.x][4] = tp_table;
-    g_pa_trace[blockIdx.x][5] = clock64() - tp0;
+    g_pa_trace[me][3] = tp_empty;
+    g_pa_trace[me][4] = tp_table;
+    g_pa_trace[me][5] = clock64() - tp0;
   })
   if (!ok) {
     if (lane == 0) report(a, kErrWaitTimeout);
@@ -421,13 +421,12 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
 // a split segment merges all slots of that segment.
 template <int D, int HP, int NP, int NC>
 __device__ void finish_piece(const DecodeArgs &a, const StageHdr &h, const float *red, long long per_cta,
-                             int *s_flag, int tid) {
+                             int *s_flag, int tid, int me) {
   constexpr int CT = NC * 32;
   constexpr int REDW = HP * (D + 2);
   const long long c1 = h.seg_start / per_cta;
   const long long c2 = (h.seg_start + h.seg_nb - 1) / per_cta;
   const bool split = c1 != c2;
-  const int me = blockIdx.x;
   const int my_slot = (h.seg_start <= static_cast<long long>(me) * per_cta) ? 0 : 1;
   const int hq0 = h.grp * a.g;
   for (int idx = tid; idx < a.g * D; idx += CT) {
@@ -494,10 +493,11 @@ __device__ void finish_piece(const DecodeArgs &a, const StageHdr &h, const float
 }
 
 // Kernel prologue shared by both consumers: barrier init, block count,
-// per-CTA range.  Returns per_cta and (for the producer warp) the total.
+// per-CTA range (G CTAs or partitions split the work; this is number me).
+// Returns per_cta and (for the producer warp) the total.
 template <class Cfg>
 __device__ long long prologue(const DecodeArgs &a, uint64_t *full, uint64_t *empty, long long *total_out,
-                              long long *s_per_cta) {
+                              long long *s_per_cta, int me, int G) {
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   if (tid == 0) {
@@ -508,9 +508,9 @@ __device__ long long prologue(const DecodeArgs &a, uint64_t *full, uint64_t *emp
     fence_mbar_init();
   }
   if (warp == Cfg::NC) {
-    const long long nb_sum = count_blocks<Cfg::D>(a, tid & 31);
+    const long long nb_sum = count_blocks<Cfg::D>(a, tid & 31, me, G);
     *total_out = nb_sum * a.num_groups;
-    if ((tid & 31) == 0) *s_per_cta = (*total_out + gridDim.x - 1) / gridDim.x;
+    if ((tid & 31) == 0) *s_per_cta = (*total_out + G - 1) / G;
   }
   __syncthreads();
   return *s_per_cta;
@@ -622,9 +622,10 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
   const int warp = tid >> 5;
   const int lane = tid & 31;
   long long total = 0;
-  const long long per_cta = prologue<C>(a, full, empty, &total, &s_per_cta);
+  const int me = blockIdx.x;
+  const long long per_cta = prologue<C>(a, full, empty, &total, &s_per_cta, me, gridDim.x);
   if (warp == NC) {
-    produce<C>(a, stages, hdr, full, empty, per_cta, total, lane);
+    produce<C>(a, stages, hdr, full, empty, per_cta, total, lane, me);
     return;
   }
 
@@ -757,7 +758,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 2) decode_simt_kern
       }
     }
     named_bar_sync(1, NC * 32);
-    finish_piece<D, C::HP, NC, NC>(a, h, red, per_cta, &s_flag, tid);
+    finish_piece<D, C::HP, NC, NC>(a, h, red, per_cta, &s_flag, tid, me);
   }
 }
 
@@ -947,7 +948,7 @@ __device__ void merge_segment(const DecodeArgs &a, const StageHdr &h, long long 
 // concurrently with the consumers, which move on to the next piece.
 template <class C>
 __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *rhdr, uint64_t *rfull,
-                         uint64_t *rempty, long long per_cta, int lane) {
+                         uint64_t *rempty, long long per_cta, int lane, int me) {
   constexpr int D = C::D;
   constexpr int NC = C::NC;
   constexpr int HG = C::HG;
@@ -966,7 +967,6 @@ __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *
     const long long c1 = h.seg_start / per_cta;
     const long long c2 = (h.seg_start + h.seg_nb - 1) / per_cta;
     const bool split = c1 != c2;
-    const int me = blockIdx.x;
     const int my_slot = (h.seg_start <= static_cast<long long>(me) * per_cta) ? 0 : 1;
     const int hq0 = h.grp * HG * a.g;  // first query head of the group
     for (int hw = 0; hw < HG; ++hw) {
@@ -1038,13 +1038,17 @@ __device__ void epilogue(const DecodeArgs &a, const float *red, const StageHdr *
   }
 }
 
+// One partition of the decode work: number me of G equal ranges of the
+// flat (segment, block) list (a CTA of the decode kernel, or a work item of
+// the mixed-step kernel).  Run by all threads of a CTA; warps past the
+// epilogue warp leave after the prologue.  smem_raw: the CTA's dynamic
+// shared memory (MmaCfg::SMEM bytes).
 template <int D, int KVT, int GQ, int HG, int NS, int NCW>
-__global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
+__device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me, int G) {
   using C = MmaCfg<D, KVT, GQ, HG, NS, NCW>;
   constexpr int MT = D / 16;  // m-tiles of O^T (16 head_dim rows each) = k-steps of S^T
   constexpr int NN = C::NN;
   constexpr int NC = C::NC;
-  extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *stages = smem;
   float *red = reinterpret_cast<float *>(smem + size_t(NS) * C::STAGEB);  // [2][NC][GQ][RSTR]
@@ -1059,11 +1063,6 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // launched as a programmatic dependent of the preceding kernel in the
-  // stream: nothing is read before that kernel's writes are visible.  (No
-  // early launch_dependents: CTAs of a following grid parked on the SMs
-  // while this one drains measured 0.2-0.9 us slower per launch.)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&rfull[i], NC);
@@ -1071,15 +1070,16 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
     }
   }
   long long total = 0;
-  const long long per_cta = prologue<C>(a, full, empty, &total, &s_per_cta);
+  const long long per_cta = prologue<C>(a, full, empty, &total, &s_per_cta, me, G);
   if (warp == NC) {
-    produce<C>(a, stages, hdr, full, empty, per_cta, total, lane);
+    produce<C>(a, stages, hdr, full, empty, per_cta, total, lane, me);
     return;
   }
   if (warp == NC + 1) {
-    epilogue<C>(a, red, rhdr, rfull, rempty, per_cta, lane);
+    epilogue<C>(a, red, rhdr, rfull, rempty, per_cta, lane, me);
     return;
   }
+  if (warp > NC + 1) return;
 
   const int hw = warp % HG;  // this warp's kv head within the group
   const int bw = warp / HG;  // and its block within the stage
@@ -1344,12 +1344,23 @@ __global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __g
     report(a, kErrWaitTimeout);
   }
   PA_TRACE(if (tid == 0) {
-    g_pa_trace[blockIdx.x][0] = tc_full;
-    g_pa_trace[blockIdx.x][1] = tc_fin;
-    g_pa_trace[blockIdx.x][2] = clock64() - tc0;
-    g_pa_trace[blockIdx.x][6] = n_st;
-    g_pa_trace[blockIdx.x][7] = n_pc;
+    g_pa_trace[me][0] = tc_full;
+    g_pa_trace[me][1] = tc_fin;
+    g_pa_trace[me][2] = clock64() - tc0;
+    g_pa_trace[me][6] = n_st;
+    g_pa_trace[me][7] = n_pc;
   })
+}
+
+template <int D, int KVT, int GQ, int HG, int NS, int NCW>
+__global__ void __launch_bounds__((NCW + 2) * 32, 1) decode_mma_kernel(const __grid_constant__ DecodeArgs a) {
+  // launched as a programmatic dependent of the preceding kernel in the
+  // stream: nothing is read before that kernel's writes are visible.  (No
+  // early launch_dependents: CTAs of a following grid parked on the SMs
+  // while this one drains measured 0.2-0.9 us slower per launch.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ uint8_t smem_raw[];
+  decode_partition<D, KVT, GQ, HG, NS, NCW>(a, smem_raw, blockIdx.x, gridDim.x);
 }
 
 // ------------------------------------------------------------ kernel lookup
@@ -1388,12 +1399,17 @@ KernelInfo simt_info() {
 // per SM sub-partition, to hide each other's latency (measured on GB300:
 // 67% -> 89% of the HBM copy rate).
 template <int D, int KVT, int GQ, int HG, int NCW = kConsumerWarps>
-KernelInfo mma_info() {
+constexpr int mma_stages() {
   constexpr int ESZ = kv16(KVT) ? 2 : 1;
   constexpr int STAGEB = 2 * NCW * 16 * D * ESZ + ((HG * GQ * D * 2 + 1023) / 1024) * 1024;
   constexpr int RED = 2 * NCW * GQ * (D + 4) * 4;
   constexpr int FIT = (225280 - 2048 - RED) / STAGEB;
-  constexpr int NS = FIT > 12 ? 12 : FIT;
+  return FIT > 12 ? 12 : FIT;
+}
+
+template <int D, int KVT, int GQ, int HG, int NCW = kConsumerWarps>
+KernelInfo mma_info() {
+  constexpr int NS = mma_stages<D, KVT, GQ, HG, NCW>();
   static_assert(NS >= 3, "at least three stages in flight");
   using Cfg = MmaCfg<D, KVT, GQ, HG, NS, NCW>;
   KernelInfo k;
@@ -1428,6 +1444,13 @@ KernelInfo fp8_mma_for(int gq, int hg) {
   if (gq <= 8) return fp8_mma_for_hg<KVT, D, 8>(hg);
   return fp8_mma_for_hg<KVT, D, 16>(hg);
 }
+
+// The kernel arguments of a decode call planned as `plan` (tensor maps for
+// the MMA kernel); false if a tensor map cannot be made.  pa_decode.cu.
+bool make_decode_args(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse, const void *q,
+                      const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                      int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs, float scale,
+                      void *workspace, DecodeArgs *a);
 
 // Defined in the translation units that instantiate the kernels.
 KernelInfo pick_simt(int head_dim, int kv_dtype, int g);

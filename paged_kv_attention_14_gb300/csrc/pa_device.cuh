@@ -41,6 +41,8 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Error bits a kernel may set in its error words (PA_DEVERR_* of pa.h).
 constexpr int kErrWaitTimeout = 1;  // a bounded wait ran out; the kernel gave up
 constexpr int kErrBadIndex = 2;     // checked mode: a block id, length or slot out of range
+constexpr int kErrFp16Range = 4;    // a bf16 V value beyond fp16's range met an fp16 product
+constexpr int kErrRefcount = 8;     // a page release found no owner left
 
 // ORs error bits into the error words that exist (either may be NULL).
 __device__ __forceinline__ void report_error(int32_t *w1, int32_t *w2, int bits) {
@@ -223,6 +225,21 @@ __device__ __forceinline__ void cp_async_wait() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs `pred` over the participating threads: every
+// thread gets the same answer, so a group can agree to go on or to stop.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------- conversions

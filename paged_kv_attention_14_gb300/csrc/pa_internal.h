@@ -45,6 +45,26 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
 
 pa_status check_prefill(const pa_kv_desc &d, const char **why);
 
+// Every host-side check of pa_prefill_chunk's arguments (num_seqs == 0 or
+// max_q_len == 0 validates the descriptor only); sets the last-error string
+// on failure.  Nothing is enqueued.
+pa_status validate_prefill(const pa_kv_desc *desc, const float *out, const float *lse, const void *q,
+                           const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
+                           int32_t num_seqs, int32_t max_q_len, int32_t max_context_len, float scale);
+
+// The single-launch mixed step (pa_mixed.cu): which descriptors it takes,
+// and its launch.  The decode plan sizes the decode partitions and the
+// workspace, whose head also holds the launch's work counters.
+pa_status check_mixed(const pa_kv_desc &d, const DecodePlan &plan, const char **why);
+cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec_out, float *dec_lse,
+                         const void *dec_q, const int32_t *dec_block_tables, int32_t dec_max_blocks,
+                         const int32_t *dec_context_lens, int32_t num_dec_seqs, float *pf_out, float *pf_lse,
+                         const void *pf_q, const int32_t *query_start_loc, const int32_t *pf_block_tables,
+                         int32_t pf_max_blocks, const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
+                         const void *k_cache, const void *v_cache, float scale, void *workspace,
+                         cudaStream_t stream);
+
 // prefix_mode: every query of sequence s comes after all context_lens[s]
 // keys and sees them all (shared-prefix / cascade attention) instead of the
 // causal chunk positions; the keys are cut into num_splits splits of
@@ -57,16 +77,26 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
                            bool prefix_mode = false, int num_splits = 1, int split_len = 0, int out_slots = 1);
 
-// tcgen05 (tensor-memory) prefill kernel for bf16 and fp16 caches.
+// tcgen05 (tensor-memory) prefill kernel for bf16 and fp16 caches; pair_p:
+// P as a hi + lo pair of the cache's type instead of one fp16 value.
 cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const void *q,
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                               int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
-                              bool prefix_mode, int num_splits, int split_len, int out_slots);
+                              bool prefix_mode, int num_splits, int split_len, int out_slots, bool pair_p);
 
 // Copy-on-write of whole blocks (all kv heads) of both caches.
 cudaError_t launch_copy_blocks(const pa_kv_desc &d, void *k_cache, void *v_cache, const int32_t *src_blocks,
                                const int32_t *dst_blocks, int32_t num_pairs, cudaStream_t stream);
+
+// Prefix-cache page bookkeeping (bind a hit's pages, release owners).
+cudaError_t launch_bind_blocks(const pa_kv_desc &d, int32_t *block_tables, int32_t max_blocks_per_seq,
+                               int32_t num_rows, const int32_t *seq_rows, const int32_t *hit_start,
+                               const int32_t *hit_blocks, int32_t num_seqs, int32_t *refcounts, cudaStream_t stream);
+cudaError_t launch_release_blocks(const pa_kv_desc &d, int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  int32_t num_rows, const int32_t *seq_rows, const int32_t *block_counts,
+                                  int32_t num_seqs, int32_t *refcounts, int32_t *free_list, int32_t *free_count,
+                                  cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

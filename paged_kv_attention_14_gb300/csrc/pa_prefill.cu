@@ -26,6 +26,7 @@
 // (pa_prefix_attention) every query comes after all the keys of its split
 // of a shared prefix, and the outputs go to that split's part slot.
 #include "pa_device.cuh"
+#include "pa_host_cache.h"
 #include "pa_internal.h"
 
 namespace pa {
@@ -404,11 +405,12 @@ pa_status check_prefill(const pa_kv_desc &d, const char **why) {
     *why = "prefill supports group sizes up to 128";
     return PA_ERR_UNSUPPORTED;
   }
-  if (d.prefill_impl < PA_PREFILL_AUTO || d.prefill_impl > PA_PREFILL_TCGEN05) {
-    *why = "prefill_impl must be PA_PREFILL_AUTO, PA_PREFILL_MMA_SYNC or PA_PREFILL_TCGEN05";
+  if (d.prefill_impl < PA_PREFILL_AUTO || d.prefill_impl > PA_PREFILL_TCGEN05_PAIR) {
+    *why = "prefill_impl must be PA_PREFILL_AUTO, PA_PREFILL_MMA_SYNC, PA_PREFILL_TCGEN05 or PA_PREFILL_TCGEN05_PAIR";
     return PA_ERR_INVALID_ARG;
   }
-  if (d.prefill_impl == PA_PREFILL_TCGEN05 && d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_F16) {
+  if ((d.prefill_impl == PA_PREFILL_TCGEN05 || d.prefill_impl == PA_PREFILL_TCGEN05_PAIR) &&
+      d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_F16) {
     *why = "the tcgen05 prefill kernel takes bf16 and fp16 caches";
     return PA_ERR_UNSUPPORTED;
   }
@@ -423,10 +425,10 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            bool prefix_mode, int num_splits, int split_len, int out_slots) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
-  if (impl == PA_PREFILL_TCGEN05)
+  if (impl == PA_PREFILL_TCGEN05 || impl == PA_PREFILL_TCGEN05_PAIR)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len,
-                             out_slots);
+                             out_slots, impl == PA_PREFILL_TCGEN05_PAIR);
   const int g = d.num_q_heads / d.num_kv_heads;
   PrefillArgs a;
   a.out = out;
@@ -476,8 +478,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
            : fp8                         ? PrefillCfg<64, kKvFp8, kPrefillWarps>::SMEM
                                          : PrefillCfg<64, kKvBf16, kPrefillWarps>::SMEM;
   }
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  if (prepare_kernel(fn, kPrefillWarps * 32, smem) < 1) return cudaErrorInvalidConfiguration;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
   dim3 grid(qtiles, d.num_kv_heads, num_seqs * a.num_splits);

@@ -1,718 +1,32 @@
-// pa_prefill_tc.cu -- causal chunked-prefill attention on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory), bf16 or fp16
-// KV (the MMAs, and the P pair below, take the cache's 16-bit type).
-//
-// What it computes is the same as pa_prefill.cu: sequence s brings q_len
-// new queries (a "chunked prefill" chunk, vllm.cpp implementation notes,
-// Engine core bullet); query i sits at position context_lens[s] - q_len + i
-// and attends keys [0, position] through the block table, reading blocks
-// that may be shared with other sequences ("Zero-Copy Cache Hits" of "1.
-// Technical Mechanics of the Radix Cache", Building and Deploying vllm.cpp).
-//
-// How (GB300 design):
-//  * One CTA takes 256 (query, head) rows: 256 / g consecutive queries of
-//    one sequence times the g query heads of one kv head, so every K/V tile
-//    feeds the whole GQA group.  The rows form two 128-row Q tiles (A, B)
-//    that ping-pong: while one tile's softmax runs, the tensor cores work on
-//    the other tile.  Q is staged once in shared memory; K/V are walked in
-//    128-key tiles gathered block by block through the block table by TMA
-//    (128-byte-swizzled boxes of 16 rows) into a 3-stage K ring and a
-//    2-stage V ring shared by both Q tiles.  A K slot is released as soon
-//    as the QKs that read it complete, a V slot after its PVs.
-//  * Warp 0 (one thread) issues the MMAs.  S_t = Q_t K^T (M 128, N 128 keys,
-//    K 16 x head_dim/16; both operands in shared memory) lands in tile t's
-//    128 TMEM columns.  The softmax overwrites those columns with P_t as a
-//    hi + lo pair of the cache's 16-bit type (each 32-key chunk's pair in
-//    that chunk's columns; P = hi + lo to ~2^-17 relative with bf16, so the
-//    tensor core product keeps near-fp32 accuracy), and O_t += P_t V (M 128,
-//    N head_dim, K 16 x 8, twice) takes P_t straight from tensor memory
-//    as the A operand and V MN-major from shared memory.  Order per KV tile
-//    j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1); one commit after each QK
-//    tells tile t's softmax that its next scores are ready AND that its
-//    previous PV finished (so O_t may be rescaled and S_t overwritten).
-//    M 128 MMAs with N <= 128 cost the same per instruction (measured on
-//    GB300: ~84 cycles with both operands in shared memory, ~78 with A in
-//    tensor memory, 128 at N 256), hence the 128-key tile.
-//  * Warps 4-7 (tile A) and 8-11 (tile B), one thread per row, do the online
-//    softmax in one pass over the row's 128 scores in TMEM, 32 at a time
-//    (the next 32 loading meanwhile): causal mask, row max (a tree of
-//    three-input maxima), exp2 of the scaled scores, row sum and the P
-//    pair, with packed fp32x2 arithmetic.  The running max is only raised
-//    (and O and the chunks of P already written rescaled in TMEM) when it
-//    grows by more than 2^8, so that path is rare.
-//  * Keys past the chunk's last position are masked; V rows past it are
-//    zeroed in shared memory before the last PV (0 * NaN would not vanish).
-//  * Warp 1 issues the TMA copies and prefetches block-table entries one
-//    tile ahead.  Warps 2-3 only take part in staging Q.
-//  * Every wait is bounded; on a timeout the kernel records an error bit,
-//    lets its own MMAs and copies drain and frees its TMEM before returning.
-#include <cuda.h>
-#include <string.h>
-
-#include "pa_device.cuh"
-#include "pa_internal.h"
+// pa_prefill_tc.cu -- launch of the tcgen05 chunked-prefill kernel
+// (pa_prefill_tc.cuh) for pa_prefill_chunk and pa_prefix_attention: one CTA
+// per (query tile, kv head, sequence or sequence x key split).
+#include "pa_prefill_tc.cuh"
 
 namespace pa {
 namespace pftc {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr int KT = 128;        // keys per KV tile (N of the QK MMA)
-constexpr int BPT = KT / 16;   // cache blocks per KV tile
-constexpr int MT = 128;        // rows of one Q tile (one TMEM lane per row)
-constexpr int NQT = 2;         // Q tiles per CTA (ping-pong between two softmax warpgroups)
-constexpr int MROWS = MT * NQT;
-// Warp roles.  The MMA issuer and the TMA producer take the lowest warp
-// numbers: they must be scheduled promptly on sub-partitions shared with
-// busy softmax warps, and the warp schedulers favour older warps.  Softmax
-// warp w may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so each
-// Q tile's warpgroup starts at a multiple of four.
-constexpr int NTHREADS = 384;  // warp 0 MMA issuer, 1 TMA producer, 2-3 idle, 4-7 softmax A, 8-11 softmax B
-constexpr int kMmaWarp = 0;
-constexpr int kProducerWarp = 1;
-constexpr int kSoftmaxWarp0 = 4;
-constexpr int NSK = 3;         // stages of the K ring
-constexpr int NSV = 2;         // stages of the V ring
-constexpr float kRescaleThreshold = 8.f;  // log2 units
-
-struct Args {
-  CUtensorMap kmap;  // cache as [rows = blocks * kv heads * 16][D], box {64, 16}
-  CUtensorMap vmap;
-  float *out;
-  float *lse;
-  const uint16_t *q;
-  const int32_t *query_start_loc;
-  const int32_t *block_tables;
-  const int32_t *context_lens;
-  int max_blocks_per_seq;
-  int num_kv_heads;
-  int num_q_heads;
-  int g;
-  int qt;  // queries per CTA (256 / g)
-  float qscale;
-  int window;  // local attention (see pa_kv_desc), 0: none
-  int chunk;
-  int prefix_mode;  // 1: every query after all L keys, no causal mask (shared prefix)
-  int num_splits;   // prefix mode: key splits per sequence (grid.z = sequences x splits)
-  int split_len;    // prefix mode: keys per split (a multiple of KT)
-  int out_slots;    // prefix mode: output slots per (row, head); split i writes slot i
-  int32_t *err;     // the caller's error word (pa_kv_desc.error_word), or NULL
-  unsigned long long wait_ns;  // limit of every bounded wait
-  int checked;      // range-check block ids and lengths (pa_kv_desc.check_indices)
-  int stall;        // test hook: the producer issues nothing, so the waits run out
-  int num_blocks;   // blocks of the cache (checked mode)
-};
-
-// Optional timeline counters (compiled only with -DPA_PREFILL_TRACE), per
-// CTA slot (blockIdx linearised, first 4096): softmax warp 0 lane 0 cycles
-// [0] waiting for S, [1] loading S, masking and max, [2] rescaling O, [3]
-// exp2 and P stores, [4] fence and arrive, [7] total; MMA thread cycles [8]
-// waiting for V, [9] waiting for K, [10] waiting for P, [11] total;
-// producer [12] waiting for free slots, [13] total; [14] KV tiles.
-// Optional event timeline of CTA (0, 0, 0) (compiled only with
-// -DPA_PREFILL_TIMELINE): clock64 per KV tile j of [0] P_A seen by the MMA
-// thread, [1] PV_A + QK_A issued, [2] P_B seen, [3] PV_B + QK_B issued,
-// [4] S_A seen by softmax A, [5] P_A arrived, [6] S_B seen, [7] P_B arrived,
-// [8 + w] softmax warp w arrived, [16] V seen by the MMA thread, [17]
-// V_EMPTY committed, [18] K_EMPTY committed, [19] start of the V wait,
-// softmax A: [20] after the fence, [21] first scores loaded, [22] chunks
-// done, [23] stores done.
-#ifdef PA_PREFILL_TIMELINE
-static __device__ long long g_pf_tl[24][64];
-#define PF_TL(i, j) \
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (j) < 64) g_pf_tl[i][j] = clock64()
-#else
-#define PF_TL(i, j)
-#endif
-#ifdef PA_PREFILL_TRACE
-static __device__ unsigned long long g_pf_trace[4096][16];
-#define PF_TRACE(...) __VA_ARGS__
-#else
-#define PF_TRACE(...)
-#endif
-
-template <int D, int KVT>
-struct Cfg {
-  static constexpr int HALVES = D / 64;          // 128-byte column halves of a row
-  static constexpr int QHALF = MT * 128;         // bytes of one half of one Q tile
-  static constexpr int QB = HALVES * QHALF;      // one Q tile
-  static constexpr int KVHALF = KT * 128;        // bytes of one half of a K or V tile
-  static constexpr int KVB = HALVES * KVHALF;
-  static constexpr int OFF_Q = 0;                  // [NQT]
-  static constexpr int OFF_K = OFF_Q + NQT * QB;   // [NSK]
-  static constexpr int OFF_V = OFF_K + NSK * KVB;  // [NSV]
-  static constexpr int OFF_BAR = OFF_V + NSV * KVB;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + barriers, TMEM slot, 1024-B alignment slack
-  // at least half an SM's shared memory, so that two CTAs (each holding
-  // all 512 TMEM columns) never share an SM
-  static constexpr int SMEM_LAUNCH = SMEM > 120 * 1024 ? SMEM : 120 * 1024;
-  static_assert(SMEM <= 232448, "shared memory of one CTA");
-  // TMEM columns: S_t of each Q tile (KT each; P_t hi | lo written over it),
-  // then O_t (D each)
-  static constexpr uint32_t O_COL = NQT * KT;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(NQT * (KT + D) <= TMEM_COLS, "TMEM columns");
-  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false, KVT == kKvF16);
-  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true, KVT == kKvF16);
-  // bytes landed per 16-token block of K (or of V), all halves
-  static constexpr uint32_t BLOCK_BYTES = HALVES * 16u * 128u;
-};
-
-// barriers: K_FULL[NSK], K_EMPTY[NSK], V_FULL[NSV], V_EMPTY[NSV],
-// S_FULL[tile], P_FULL[tile]
-enum Bar {
-  K_FULL = 0,
-  K_EMPTY = K_FULL + NSK,
-  V_FULL = K_EMPTY + NSK,
-  V_EMPTY = V_FULL + NSV,
-  S_FULL = V_EMPTY + NSV,
-  P_FULL = S_FULL + NQT,
-  NBAR = P_FULL + NQT
-};
-static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
-
-template <int D, int KVT>
-__global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_constant__ Args a) {
-  using C = Cfg<D, KVT>;
-  // launched as a programmatic dependent of the preceding kernel (typically
-  // the cache write): nothing is read before its writes are visible
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + NBAR);
-  int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
-  int *s_last_k = s_abort + 1;  // last KV tile whose K copies the producer issued
-  int *s_last_v = s_abort + 2;  // ... and whose V copies
-
-  const int split = a.prefix_mode ? static_cast<int>(blockIdx.z) % a.num_splits : 0;
-  const int s = a.prefix_mode ? static_cast<int>(blockIdx.z) / a.num_splits : static_cast<int>(blockIdx.z);
-  const int kvh = blockIdx.y;
-  const int qtile = gridDim.x - 1 - blockIdx.x;  // longest key ranges first
-  const int qs = __ldg(a.query_start_loc + s);
-  int q_len = __ldg(a.query_start_loc + s + 1) - qs;
-  int L = __ldg(a.context_lens + s);
-  if (a.checked) {
-    // lengths within the table's capacity; a chunk no longer than its context
-    // nor than the launch's query tiles; rows start at a row >= 0
-    L = checked_len(L, a.max_blocks_per_seq * 16, a.err, nullptr);
-    q_len = checked_len(q_len, a.prefix_mode ? static_cast<int>(gridDim.x) * a.qt
-                                             : min(L, static_cast<int>(gridDim.x) * a.qt), a.err, nullptr);
-    if (qs < 0) {
-      if (threadIdx.x == 0) report_error(a.err, nullptr, kErrBadIndex);
-      return;
-    }
-  }
-  const int qt0 = qtile * a.qt;
-  if (qt0 >= q_len) return;
-  const int nq = min(a.qt, q_len - qt0);
-  // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
-  // query comes after them all; otherwise query i sits at L - q_len + i
-  const int p_lo = a.prefix_mode ? min(L, split * a.split_len) : 0;
-  const int p_hi = a.prefix_mode ? min(L, p_lo + a.split_len) : 0;
-  const int base_pos = a.prefix_mode ? p_hi - 1 : L - q_len + qt0;  // position of query qt0
-  const int kv_end = a.prefix_mode ? p_hi : base_pos + nq;         // keys [kv_lo, kv_end) are needed
-  if (a.prefix_mode && p_hi <= p_lo) {
-    // no key in this split (an empty or short shared prefix): out = 0,
-    // lse = -inf, before any barrier or tensor memory is set up
-    for (int i = threadIdx.x; i < nq * a.g; i += NTHREADS) {
-      const int64_t row =
-          (static_cast<int64_t>(qs + qt0 + i / a.g) * a.num_q_heads + blockIdx.y * a.g + i % a.g) * a.out_slots + split;
-      for (int d = 0; d < D; d += 4) *reinterpret_cast<float4 *>(a.out + row * D + d) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (a.lse) a.lse[row] = -INFINITY;
-    }
-    return;
-  }
-  // local attention: the CTA's earliest query sees keys from kv_lo on (the
-  // first key never decreases with the position).  KV tiles j0 .. n_tiles - 1
-  // are walked; the rings and barriers count iterations jj = j - j0.
-  const int kv_lo = a.prefix_mode ? p_lo : local_first_key(base_pos, a.window, a.chunk);
-  const int j0 = kv_lo / KT;
-  const int n_tiles = (kv_end + KT - 1) / KT;
-  const int n_iter = n_tiles - j0;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int g = a.g;
-  const int rows_used = a.qt * g;
-
-  if (tid == 0) {
-    for (int i = 0; i < NSK; ++i) {
-      mbar_init(&bar[K_FULL + i], 1);
-      mbar_init(&bar[K_EMPTY + i], 1);
-    }
-    for (int i = 0; i < NSV; ++i) {
-      mbar_init(&bar[V_FULL + i], 1);
-      mbar_init(&bar[V_EMPTY + i], 1);
-    }
-    for (int t = 0; t < NQT; ++t) {
-      mbar_init(&bar[S_FULL + t], 1);
-      mbar_init(&bar[P_FULL + t], 4);
-    }
-    *s_abort = 0;
-    *s_last_k = -1;
-    *s_last_v = -1;
-    fence_mbar_init();
-  }
-  if (warp == kMmaWarp) tmem_alloc(tmem_slot, C::TMEM_COLS);
-
-  // ---- Q tiles: row R = query * g + head (tile R / 128, lane R % 128),
-  // [tile][half][row][128 B], 128-B swizzle
-  {
-    constexpr int CHUNKS = D / 8;  // 16-byte chunks per row
-    for (int i = tid; i < MROWS * CHUNKS; i += NTHREADS) {
-      const int R = i / CHUNKS;
-      const int ch = i - R * CHUNKS;
-      const int qi = R / g;
-      const bool ok = R < rows_used && qi < nq;
-      const uint16_t *src = a.q;
-      if (ok) src = a.q + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * D + ch * 8;
-      const int r = R & (MT - 1);
-      uint8_t *dst = smem + C::OFF_Q + (R / MT) * C::QB + (ch >> 3) * C::QHALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      cp_async16(dst, src, ok);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t sbase = smem_u32(smem);
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------ TMA producer
-    const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
-    const uint64_t pol = l2_evict_first_policy();
-    // lane -> (block of the tile, half); the same lanes copy K and V
-    const int bi = lane / C::HALVES;
-    const int hh = lane % C::HALVES;
-    const bool issuer = lane < BPT * C::HALVES;
-    auto block_id = [&](int lb) {
-      const int v = __ldg(table + lb);
-      return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
-    };
-    int phys_next = 0;
-    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = block_id(j0 * BPT + bi);
-    PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
-    bool ok = true;
-    // test hook: issue nothing and signal nothing, so the other warps' waits
-    // run out with nothing in flight
-    for (int jj = 0; jj < (a.stall ? 0 : n_iter) && ok; ++jj) {
-      const int j = j0 + jj;
-      const int phys = phys_next;
-      const int key0 = j * KT;
-      const int lb = (j + 1) * BPT + bi;  // prefetch the next tile's block id
-      phys_next = (issuer && lb * 16 < kv_end) ? block_id(lb) : 0;
-      const int nblk = min(BPT, (kv_end - key0 + 15) / 16);
-      // blocks of the first tile entirely before the CTA's first key are not
-      // read (under local attention their pages may be gone)
-      const int bskip = jj == 0 ? (kv_lo >> 4) - j * BPT : 0;
-      const int row = (phys * a.num_kv_heads + kvh) * 16;
-      // K of tile j (its slot frees once the QKs of tile j - NSK completed),
-      // then V of tile j (once the PVs of tile j - NSV completed)
-#pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        const int st = part ? jj % NSV : jj % NSK;
-        const uint32_t ph = part ? (jj / NSV) & 1 : (jj / NSK) & 1;
-        const int full = (part ? V_FULL : K_FULL) + st;
-        PF_TRACE(const long long tw = clock64();)
-        if (!mbar_wait(&bar[(part ? V_EMPTY : K_EMPTY) + st], ph ^ 1, a.wait_ns)) {
-          ok = false;
-          break;
-        }
-        PF_TRACE(tp_wait += clock64() - tw;)
-        if (part == 1 && bskip > 0) {
-          // V rows of the skipped blocks: zero (0 * NaN would not vanish in
-          // the PV), before the copies of the other blocks start
-          for (int i = lane; i < bskip * 16 * C::HALVES * 8; i += 32) {
-            const int rr = i / (C::HALVES * 8);
-            const int rem = i % (C::HALVES * 8);
-            *reinterpret_cast<uint4 *>(smem + C::OFF_V + st * C::KVB + (rem >> 3) * C::KVHALF + rr * 128 +
-                                       (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        if (lane == 0) mbar_arrive_expect_tx(&bar[full], (nblk - bskip) * C::BLOCK_BYTES);
-        __syncwarp();
-        if (issuer && bi < nblk && bi >= bskip) {
-          uint8_t *dst = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB + hh * C::KVHALF + bi * 16 * 128;
-          tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
-        }
-        if (lane == 0) *(part ? s_last_v : s_last_k) = jj;
-      }
-    }
-    if (!ok && lane == 0) *s_abort = 1;
-    PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-             if (lane == 0 && slot < 4096) { g_pf_trace[slot][12] = tp_wait; g_pf_trace[slot][13] = clock64() - tp0; g_pf_trace[slot][14] = n_tiles; })
-  } else if (warp == kMmaWarp) {
-    // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      auto qk = [&](int t, int jj) {  // S_t = Q_t K^T of iteration jj
-        const uint32_t qbase = sbase + C::OFF_Q + t * C::QB;
-        const uint32_t kbase = sbase + C::OFF_K + (jj % NSK) * C::KVB;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = umma_desc_sw128(qbase + (kk >> 2) * C::QHALF + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = umma_desc_sw128(kbase + (kk >> 2) * C::KVHALF + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + t * KT, ad, bd, C::IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto pv = [&](int t, int jj) {  // O_t += (P_t hi + P_t lo) V of iteration jj, P_t from TMEM
-        const uint32_t vbase = sbase + C::OFF_V + (jj % NSV) * C::KVB;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-#pragma unroll
-          for (int kk = 0; kk < KT / 16; ++kk) {
-            // keys 16 kk .. 16 kk + 15: chunk kk / 2, hi at +0, lo at +16
-            const uint64_t bd = umma_desc_sw128(vbase + kk * 2048, C::KVHALF, 1024);
-            umma_bf16_ts(tmem + C::O_COL + t * D, tmem + t * KT + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8, bd,
-                         C::IDESC_PV, (jj > 0 || part > 0 || kk > 0) ? 1u : 0u);
-          }
-        }
-      };
-      PF_TRACE(const long long tm0 = clock64(); long long tm_v = 0, tm_k = 0, tm_p = 0; long long tw;)
-      // Issue order per KV tile j: PV_A(j), QK_A(j+1), S_A commit, K_EMPTY(j)
-      // commit, PV_B(j), V_EMPTY(j) commit, wait for V(j+1), QK_B(j+1), S_B
-      // commit.  The tensor pipe queues only a few instructions, so buffer
-      // releases and the V wait sit between MMAs (while the pipe has work)
-      // and the thread goes straight from the last MMA of a KV tile to the
-      // wait for the next tile's P_A.
-      if (!mbar_wait(&bar[K_FULL], 0, a.wait_ns) || !mbar_wait(&bar[V_FULL], 0, a.wait_ns)) ok = false;
-      if (ok) {
-        tc_fence_after_sync();
-        for (int t = 0; t < NQT; ++t) {
-          qk(t, 0);
-          umma_commit(&bar[S_FULL + t]);
-        }
-      }
-      for (int jj = 0; jj < n_iter && ok; ++jj) {
-        const bool next = jj + 1 < n_iter;
-        for (int t = 0; t < NQT; ++t) {
-          if (!mbar_wait_hint(&bar[P_FULL + t], jj & 1, a.wait_ns)) {
-            ok = false;
-            break;
-          }
-          PF_TL(t * 2, jj);
-          tc_fence_after_sync();
-          pv(t, jj);
-          if (t == NQT - 1) {
-            umma_commit(&bar[V_EMPTY + jj % NSV]);  // both tiles are done with V of iteration jj
-            if (next && !mbar_wait(&bar[V_FULL + (jj + 1) % NSV], ((jj + 1) / NSV) & 1, a.wait_ns)) {
-              ok = false;
-              break;
-            }
-          }
-          if (next) {
-            if (t == 0) {
-              if (!mbar_wait(&bar[K_FULL + (jj + 1) % NSK], ((jj + 1) / NSK) & 1, a.wait_ns)) {
-                ok = false;
-                break;
-              }
-            }
-            tc_fence_after_sync();
-            qk(t, jj + 1);
-          }
-          // S_t of the next KV tile is ready and PV_t(jj) has completed
-          // (after the last tile: O_t is final)
-          umma_commit(&bar[S_FULL + t]);
-          if (t == 0) umma_commit(&bar[K_EMPTY + jj % NSK]);  // both tiles are done with K of iteration jj
-          PF_TL(t * 2 + 1, jj);
-        }
-      }
-      if (!ok) *s_abort = 1;
-      PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-               if (slot < 4096) { g_pf_trace[slot][8] = tm_v; g_pf_trace[slot][9] = tm_k; g_pf_trace[slot][10] = tm_p; g_pf_trace[slot][11] = clock64() - tm0; })
-    }
-    __syncwarp();
-  } else if (warp >= kSoftmaxWarp0) {
-    // ------------------------------------------------ softmax, one row per thread
-    const int t = (warp - kSoftmaxWarp0) >> 2;  // Q tile of this warpgroup
-    const int r = tid & (MT - 1);
-    const int R = t * MT + r;
-    // TMEM lane = row; warp w reads lanes 32 (w % 4) .. 32 (w % 4) + 31
-    const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const uint32_t s_col = t * KT;
-    const uint32_t o_col = C::O_COL + t * D;
-    const int qi = R / g;
-    const bool rv = R < rows_used && qi < nq;
-    const int pos = rv ? (a.prefix_mode ? base_pos : base_pos + qi) : -1;  // keys <= pos are visible
-    const int first = a.prefix_mode ? kv_lo : local_first_key(pos, a.window, a.chunk);  // ... and keys >= first
-    const float qscale = a.qscale;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc, tk;)
-    for (int jj = 0; jj < n_iter; ++jj) {
-      const int j = j0 + jj;
-      PF_TRACE(tc = clock64();)
-      if (!mbar_wait_hint(&bar[S_FULL + t], jj & 1, a.wait_ns)) {
-        ok = false;
-        break;
-      }
-      PF_TRACE(tq[0] += clock64() - tc; tc = clock64();)
-      if (r == 0) PF_TL(4 + t * 2, jj);
-      tc_fence_after_sync();
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(20, jj);
-      const int key0 = j * KT;
-      if (t == 0 && jj == n_iter - 1 && kv_end - key0 < KT) {
-        // V rows past the last needed key: zero (stale or poisoned data),
-        // after this tile's V copies landed; tile 0's PV of this KV tile is
-        // issued before tile 1's
-        if (!mbar_wait(&bar[V_FULL + jj % NSV], (jj / NSV) & 1, a.wait_ns)) {
-          ok = false;
-          break;
-        }
-        const int kval = kv_end - key0;
-        for (int i = r; i < (KT - kval) * C::HALVES * 8; i += MT) {
-          const int row = kval + i / (C::HALVES * 8);
-          const int rem = i % (C::HALVES * 8);
-          *reinterpret_cast<uint4 *>(smem + C::OFF_V + (jj % NSV) * C::KVB + (rem >> 3) * C::KVHALF + row * 128 +
-                                     (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
-      PF_TRACE(tq[1] += clock64() - tc; tc = clock64();)
-      // One pass over the row's scores, 32 keys (one TMEM chunk) at a time,
-      // the next chunk's load in flight while this one is processed.  The
-      // 32 keys of chunk c (columns 32c .. 32c + 31 of this tile's block)
-      // become 16 columns of bf16 hi pairs (keys 2e, 2e + 1 in column
-      // 32c + e) and, behind them, 16 columns of lo pairs, so a chunk only
-      // overwrites its own, already loaded, scores.  The running max is
-      // checked per chunk; O_t is stable meanwhile (the commit this thread
-      // waited for follows PV_t(j - 1)).
-      uint32_t sc[2][32];
-      tmem_ld32_async(trow + s_col, sc[0]);
-      tmem_wait_ld(sc[0]);
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(21, jj);
-#pragma unroll
-      for (int c = 0; c < KT / 32; ++c) {
-        uint32_t(&cur)[32] = sc[c & 1];
-        PF_TRACE(tk = clock64();)
-        if (c + 1 < KT / 32) tmem_ld32_async(trow + s_col + (c + 1) * 32, sc[(c + 1) & 1]);
-        PF_TRACE(tq[4] += clock64() - tk; tk = clock64();)
-        const int kc = key0 + c * 32;
-        const bool unmasked = kc + 31 <= pos && kc >= first;
-        if (!unmasked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kc + i > pos || kc + i < first) cur[i] = __float_as_uint(-INFINITY);
-        }
-        // raw scores; the scale (> 0) is applied with the max subtraction.
-        // Tree of three-input maxima (depth 4, not a 32-long chain).
-        float mx;
-        {
-          float m[11];
-#pragma unroll
-          for (int i = 0; i < 10; ++i)
-            m[i] = fmax3(__uint_as_float(cur[3 * i]), __uint_as_float(cur[3 * i + 1]), __uint_as_float(cur[3 * i + 2]));
-          m[10] = fmaxf(__uint_as_float(cur[30]), __uint_as_float(cur[31]));
-          mx = fmaxf(fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmax3(m[6], m[7], m[8])),
-                     fmaxf(m[9], m[10]));
-        }
-        mx *= qscale;
-        const float m_new = fmaxf(m_ref, mx);
-        const bool raise = m_new > m_ref + kRescaleThreshold || (m_ref == -INFINITY && m_new != -INFINITY);
-        if (__any_sync(0xffffffffu, raise && m_ref != -INFINITY)) {
-          // rare: rescale this warp's O rows and the P chunks of this tile
-          // written so far (rows that do not raise scale by 1)
-          PF_TRACE(const long long tr = clock64();)
-          const float corr = (raise && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
-          if (raise) l *= corr;
-          if (jj > 0) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-              float o[32];
-              tmem_ld32(trow + o_col + c0, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= corr;
-              tmem_st32(trow + o_col + c0, o);
-            }
-          }
-          tmem_wait_st();
-#pragma unroll 1
-          for (int cp = 0; cp < c; ++cp) {
-            float pv[32];
-            tmem_ld32(trow + s_col + cp * 32, pv);
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const uint32_t h = __float_as_uint(pv[e]), w = __float_as_uint(pv[16 + e]);
-              const float p0 = (lo16<KVT>(h) + lo16<KVT>(w)) * corr;
-              const float p1 = (hi16<KVT>(h) + hi16<KVT>(w)) * corr;
-              hi[e] = pack16x2<KVT>(p0, p1);
-              lo[e] = pack16x2<KVT>(p0 - lo16<KVT>(hi[e]), p1 - hi16<KVT>(hi[e]));
-            }
-            tmem_st16_async(trow + s_col + cp * 32, hi);
-            tmem_st16_async(trow + s_col + cp * 32 + 16, lo);
-          }
-          PF_TRACE(tq[2] += clock64() - tr;)
-        }
-        if (raise) m_ref = m_new;
-        PF_TRACE(tq[5] += clock64() - tk; tk = clock64();)
-        const float nref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-        const uint64_t qs2 = f2_pack(qscale, qscale), nr2 = f2_pack(nref, nref);
-        // p in pairs (packed fp32x2 arithmetic); row-sum partials in two
-        // packed accumulators (four independent chains)
-        uint64_t lsum[2] = {0, 0};
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 x = f2_unpack(f2_fma(f2_pack(__uint_as_float(cur[2 * e]), __uint_as_float(cur[2 * e + 1])),
-                                            qs2, nr2));
-          const float p0 = ex2_approx(x.x);
-          const float p1 = ex2_approx(x.y);
-          const uint64_t pp = f2_pack(p0, p1);
-          lsum[e & 1] = f2_add(lsum[e & 1], pp);
-          hi[e] = pack16x2<KVT>(p0, p1);
-          const float2 d = f2_unpack(f2_sub(pp, f2_pack(lo16<KVT>(hi[e]), hi16<KVT>(hi[e]))));
-          lo[e] = pack16x2<KVT>(d.x, d.y);
-        }
-        {
-          const float2 l2 = f2_unpack(f2_add(lsum[0], lsum[1]));
-          l += l2.x + l2.y;
-        }
-        PF_TRACE(tq[6] += clock64() - tk;)
-        tmem_st16_async(trow + s_col + c * 32, hi);
-        tmem_st16_async(trow + s_col + c * 32 + 16, lo);
-        if (c + 1 < KT / 32) tmem_wait_ld(sc[(c + 1) & 1]);
-      }
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(22, jj);
-      tmem_wait_st();
-      if (tid == kSoftmaxWarp0 * 32) PF_TL(23, jj);
-      PF_TRACE(tq[3] += clock64() - tc; tc = clock64();)
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[P_FULL + t]);
-      if (r == 0) PF_TL(5 + t * 2, jj);
-      if (lane == 0) PF_TL(8 + warp - kSoftmaxWarp0, jj);
-    }
-    PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-             if (tid == kSoftmaxWarp0 * 32 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
-    if (ok && !mbar_wait(&bar[S_FULL + t], n_iter & 1, a.wait_ns)) ok = false;
-    if (ok) {
-      tc_fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float *orow = nullptr;
-      const int64_t orow_i =
-          (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * a.out_slots + split;
-      if (rv) orow = a.out + orow_i * D;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float o[32];
-        tmem_ld32(trow + o_col + c0, o);
-        if (rv) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4 *>(orow + c0 + i) = make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
-        }
-      }
-      if (rv && a.lse)
-        a.lse[orow_i] = (m_ref + log2f(l)) * kLn2;
-    } else if (lane == 0) {
-      *s_abort = 1;
-    }
-  }
-
-  // ---- teardown: drain on abort, free TMEM
-  tc_fence_before_sync();
-  __syncthreads();
-  if (*s_abort) {
-    if (tid == 0) report_error(a.err, nullptr, kErrWaitTimeout);
-    if (warp == kProducerWarp && lane == 0) {
-      // the copies of the last issued tiles of each ring must land before exit
-      for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t)
-        mbar_wait(&bar[K_FULL + t % NSK], (t / NSK) & 1, a.wait_ns);
-      for (int t = max(0, *s_last_v - NSV + 1); t <= *s_last_v; ++t)
-        mbar_wait(&bar[V_FULL + t % NSV], (t / NSV) & 1, a.wait_ns);
-    }
-    if (warp == kMmaWarp && lane == 0) {
-      // wait (bounded) for every MMA this thread issued before freeing TMEM
-      uint64_t *drain = &bar[P_FULL];
-      mbar_init(drain, 1);
-      fence_mbar_init();
-      umma_commit(drain);
-      mbar_wait(drain, 0, a.wait_ns);
-    }
-    __syncthreads();
-  }
-  if (warp == kMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-template <int D>
-bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
-  const CUtensorMapDataType dt = d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                     CUtensorMapFloatOOBfill);
-  static EncodeTiledFn enc = [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * 16};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, 16};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int D, int KVT>
+template <int D, int KVT, int PVM>
 cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, const int32_t *query_start_loc,
                    const void *k_cache, const void *v_cache, const int32_t *block_tables, int32_t max_blocks_per_seq,
                    const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len, float scale,
                    cudaStream_t stream, bool prefix_mode, int num_splits, int split_len, int out_slots) {
   Args a;
-  memset(&a, 0, sizeof a);
-  if (!make_map<D>(&a.kmap, k_cache, d) || !make_map<D>(&a.vmap, v_cache, d)) return cudaErrorInvalidValue;
-  a.out = out;
-  a.lse = lse;
-  a.q = static_cast<const uint16_t *>(q);
-  a.query_start_loc = query_start_loc;
-  a.block_tables = block_tables;
-  a.context_lens = context_lens;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.num_kv_heads = d.num_kv_heads;
-  a.num_q_heads = d.num_q_heads;
-  a.g = d.num_q_heads / d.num_kv_heads;
-  a.qt = MROWS / a.g;  // queries per CTA
-  a.qscale = scale * kLog2e;
-  a.window = d.sliding_window;
-  a.chunk = d.attention_chunk;
-  a.prefix_mode = prefix_mode ? 1 : 0;
-  a.num_splits = prefix_mode ? num_splits : 1;
-  a.split_len = split_len;
-  a.out_slots = prefix_mode ? out_slots : 1;
-  a.err = d.error_word;
-  a.checked = d.check_indices;
-  a.num_blocks = d.num_blocks;
-  const TestHooks hooks = test_hooks();
-  a.stall = hooks.stall;
-  a.wait_ns = hooks.wait_ns;
+  if (!make_args<D>(&a, d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                    context_lens, scale, prefix_mode, num_splits, split_len, out_slots))
+    return cudaErrorInvalidValue;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
-  auto fn = &prefill_tc_kernel<D, KVT>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, KVT>::SMEM_LAUNCH);
-  if (e != cudaSuccess) return e;
+  auto fn = &prefill_tc_kernel<D, KVT, PVM>;
+  if (prepare_kernel(reinterpret_cast<const void *>(fn), NTHREADS, Cfg<D, KVT, PVM>::SMEM_LAUNCH) < 1)
+    return cudaErrorInvalidConfiguration;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs * a.num_splits);
   cfg.blockDim = dim3(NTHREADS);
-  cfg.dynamicSmemBytes = Cfg<D, KVT>::SMEM_LAUNCH;
+  cfg.dynamicSmemBytes = Cfg<D, KVT, PVM>::SMEM_LAUNCH;
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
@@ -737,21 +51,20 @@ cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const
                               const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *context_lens,
                               int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
-                              bool prefix_mode, int num_splits, int split_len, int out_slots) {
+                              bool prefix_mode, int num_splits, int split_len, int out_slots, bool pair_p) {
   const bool f16 = d.kv_dtype == PA_KV_F16;
-  if (d.head_dim == 128)
-    return f16 ? pftc::launch<128, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                           max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
-                                           split_len, out_slots)
-               : pftc::launch<128, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
-                                           split_len, out_slots);
-  return f16 ? pftc::launch<64, kKvF16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                        max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
-                                           split_len, out_slots)
-             : pftc::launch<64, kKvBf16>(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
-                                         max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits,
-                                           split_len, out_slots);
+  // one instantiation per (head_dim, cache type, P mode)
+  auto pick = [&](auto launcher) {
+    return launcher(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                    context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len, out_slots);
+  };
+  using namespace pftc;
+  if (d.head_dim == 128) {
+    if (f16) return pair_p ? pick(launch<128, kKvF16, kPvPair>) : pick(launch<128, kKvF16, kPvF16>);
+    return pair_p ? pick(launch<128, kKvBf16, kPvPair>) : pick(launch<128, kKvBf16, kPvF16>);
+  }
+  if (f16) return pair_p ? pick(launch<64, kKvF16, kPvPair>) : pick(launch<64, kKvF16, kPvF16>);
+  return pair_p ? pick(launch<64, kKvBf16, kPvPair>) : pick(launch<64, kKvBf16, kPvF16>);
 }
 
 }  // namespace pa

@@ -12,9 +12,15 @@ vllm.cpp repository's "What's implemented").
 This module only orders the library's calls on CUDA streams; every step of
 the computation runs in the library's kernels.  Decode and prefill read
 disjoint outputs and only read the cache, so after the write they may run
-concurrently: ``overlap=True`` issues the decode on a second stream that
-waits for the write, beside the prefill on the caller's stream, so that the
-decode's CTAs take the SMs the prefill's last wave leaves idle.
+concurrently.  Three ways to issue them (``mode``):
+  * "fused"  -- one launch of pa_mixed_attention: one persistent kernel whose
+                CTAs take the prefill tiles and then the decode partitions
+                from one work list (with both parts present and a descriptor
+                it takes; "streams" otherwise);
+  * "streams" -- the decode on a second stream that waits for the write,
+                beside the prefill on the caller's stream, so that the
+                decode's CTAs take the SMs the prefill's last wave leaves idle;
+  * "serial" -- the decode, then the prefill, on the caller's stream.
 """
 from __future__ import annotations
 
@@ -33,9 +39,13 @@ class MixedStep:
     ``__call__``.  Either part may be absent (``decode_out`` or
     ``prefill_out`` None)."""
 
+    MODES = ("fused", "streams", "serial")
+
     def __init__(self, desc: B.PaKvDesc, k_cache, v_cache, scale: float, *, decode_out=None, decode_lse=None,
                  workspace=None, max_context_len_decode: int = 0, prefill_out=None, prefill_lse=None,
-                 max_q_len: int = 0, max_context_len_prefill: int = 0, overlap: bool = True):
+                 max_q_len: int = 0, max_context_len_prefill: int = 0, mode: str = "fused"):
+        if mode not in self.MODES:
+            raise ValueError(f"mode must be one of {self.MODES}")
         self.desc = desc
         self.k_cache, self.v_cache = k_cache, v_cache
         self.scale = float(scale)
@@ -44,7 +54,12 @@ class MixedStep:
         self.prefill_out, self.prefill_lse = prefill_out, prefill_lse
         self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
         both = decode_out is not None and prefill_out is not None
-        self.overlap = bool(overlap) and both
+        fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
+                    and desc.decode_impl in (B.PA_DECODE_AUTO, B.PA_DECODE_MMA)
+                    and desc.prefill_impl in (B.PA_PREFILL_AUTO, B.PA_PREFILL_TCGEN05) and workspace is not None)
+        # fused needs both parts and a descriptor pa_mixed_attention takes
+        self.mode = "streams" if mode == "fused" and not (fused_ok and both) else mode
+        self.overlap = self.mode == "streams" and both
         dev = k_cache.device
         self.side: Optional[torch.cuda.Stream] = torch.cuda.Stream(device=dev) if self.overlap else None
         self.ev_written = torch.cuda.Event()
@@ -61,6 +76,15 @@ class MixedStep:
 
     def attend(self, dec_args, pf_args):
         """Decode and prefill after a cache write already issued on the current stream."""
+        if self.mode == "fused":
+            dec = None
+            if dec_args is not None and self.decode_out is not None:
+                dec = (self.decode_out, *dec_args, self.max_context_len_decode, self.decode_lse)
+            pf = None
+            if pf_args is not None and self.prefill_out is not None:
+                pf = (self.prefill_out, *pf_args, self.max_q_len, self.max_context_len_prefill, self.prefill_lse)
+            B.pa_mixed_attention(self.desc, self.k_cache, self.v_cache, self.scale, self.workspace, dec=dec, pf=pf)
+            return
         if self.overlap:
             main = torch.cuda.current_stream()
             self.ev_written.record(main)
@@ -82,3 +106,34 @@ class MixedStep:
         if slot_mapping is not None and slot_mapping.numel() > 0:
             B.pa_cache_write(self.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping)
         self.attend(dec_args, pf_args)
+
+
+class GraphedStep:
+    """A whole step replayed from a CUDA graph.
+
+    ``issue`` is a callable that enqueues one step on the current stream
+    without allocating: typically the copy of the step's inputs from pinned
+    host memory into device buffers, a MixedStep call on those buffers, and
+    the copy of the outputs back into pinned host memory.  It is run a few
+    times on a side stream (to settle every lazy set-up), then captured once;
+    each call replays the graph on the current stream and waits for it.  The
+    buffers ``issue`` names must stay alive and in place while the object is
+    used: the graph holds their addresses."""
+
+    def __init__(self, issue, warmup: int = 2):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                issue()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            issue()
+        torch.cuda.synchronize()
+
+    def __call__(self, wait: bool = True):
+        self.graph.replay()
+        if wait:
+            torch.cuda.current_stream().synchronize()

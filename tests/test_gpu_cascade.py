@@ -18,7 +18,7 @@ from pa_helpers import LSE_TOL, TOL, assert_close, desc_of, gpu_caches, oracle_c
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
+IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -74,7 +74,7 @@ CASES = [
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("kv,groups,plens,slens,Hq,Hkv,D", CASES)
 def test_prefix_attention_matches_oracle(kv, groups, plens, slens, Hq, Hkv, D, impl, splits):
-    if impl == B.PA_PREFILL_TCGEN05 and kv not in (W.KV_BF16, W.KV_F16):
+    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
         pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
     b = W.shared_prefix_decode(300 + sum(plens), groups, plens, slens, Hq, Hkv, D, kv_dtype=kv, device=DEV)
     out, lse = _merged(*_gpu_prefix(b, gpu_caches(b), impl, splits))
@@ -91,7 +91,7 @@ def test_prefix_attention_matches_oracle(kv, groups, plens, slens, Hq, Hkv, D, i
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("kv,groups,plens,slens,Hq,Hkv,D", CASES)
 def test_cascade_prefix_suffix_merge_equals_full_decode(kv, groups, plens, slens, Hq, Hkv, D, impl, splits):
-    if impl == B.PA_PREFILL_TCGEN05 and kv not in (W.KV_BF16, W.KV_F16):
+    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
         pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
     b = W.shared_prefix_decode(400 + sum(plens), groups, plens, slens, Hq, Hkv, D, kv_dtype=kv, device=DEV)
     c = b.meta["cascade"]

@@ -90,14 +90,15 @@ def test_decode_wait_timeout_is_reported_and_the_next_call_is_correct(impl):
     assert_close(lse, l_ref, LSE_TOL[b.kv_dtype], "lse")
 
 
+@pytest.mark.parametrize("impl", [B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR])
 @pytest.mark.parametrize("prefix_mode", [False, True])
-def test_tcgen05_prefill_wait_timeout_frees_tensor_memory(prefix_mode):
+def test_tcgen05_prefill_wait_timeout_frees_tensor_memory(prefix_mode, impl):
     """The stalled kernel gives up, frees its tensor memory and returns: the
     next launches (which allocate tensor memory on the same SMs) run and are
     correct."""
     b = W.random_prefill(502, [300, 64, 1, 200], [700, 64, 129, 530], 8, 2, 128, device=DEV, poison=True,
                          shared_prefix_blocks=2)
-    d, ew = _with_error_word(b, prefill_impl=B.PA_PREFILL_TCGEN05)
+    d, ew = _with_error_word(b, prefill_impl=impl)
     kc, vc = b.k_pool, b.v_pool
     Tq = b.q_prefill.shape[0]
     out = torch.full((Tq, 8, 128), float("nan"), device=DEV)
@@ -116,11 +117,48 @@ def test_tcgen05_prefill_wait_timeout_frees_tensor_memory(prefix_mode):
     assert int(ew[0]) == B.PA_DEVERR_WAIT_TIMEOUT
     ew.zero_()
     for _ in range(3):
-        o2, l2 = gpu_prefill(b, prefill_impl=B.PA_PREFILL_TCGEN05, caches=(kc, vc))
+        o2, l2 = gpu_prefill(b, prefill_impl=impl, caches=(kc, vc))
     o_ref, l_ref = oracle_prefill(b)
     assert_close(o2, o_ref, TOL[b.kv_dtype], "out")
     assert_close(l2, l_ref, LSE_TOL[b.kv_dtype], "lse")
     assert int(ew[0]) == 0
+
+
+def test_mixed_attention_wait_timeout_frees_tensor_memory():
+    """The single-launch step stalled: every decode partition and prefill tile
+    gives up and reports; the counters are back at zero and the next step
+    is correct."""
+    from paged_kv_attention_14_gb300.step import MixedStep
+    b = W.workload(5, device=DEV, poison=True)
+    d, ew = _with_error_word(b)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(d, b.k_new, b.v_new, kc, vc, b.slot_mapping)
+    S = b.context_lens_decode.shape[0]
+    ws = B.decode_workspace(d, S, b.max_context_len_decode(), DEV)
+    dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
+    pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
+    qsl = b.query_start_loc
+    ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, workspace=ws, max_context_len_decode=b.max_context_len_decode(),
+                   prefill_out=pf_out, max_q_len=512, max_context_len_prefill=2560, mode="fused")
+    args = ((b.q_decode, b.block_tables_decode, b.context_lens_decode), (b.q_prefill, qsl, b.block_tables_prefill,
+                                                                           b.context_lens_prefill))
+    _stalled(lambda: ms.attend(*args))
+    assert int(ew[0]) == B.PA_DEVERR_WAIT_TIMEOUT
+    assert ws[4:12].view(torch.int32).tolist() == [0, 0], "work counters reset"
+    ws.zero_()
+    ew.zero_()
+    ms.attend(*args)
+    torch.cuda.synchronize()
+    assert int(ew[0]) == 0
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+                                b.k_pool.cpu(), b.v_pool.cpu())
+    rows = [0, 511, 512 + 300, 2047]
+    pairs = [(r, h) for r in rows for h in range(32)]
+    o_ref, _ = oracle_prefill(b, ocaches=(oracle.KV_BF16, ok, ov), pairs=pairs)
+    idx = torch.tensor([r * 32 + h for r, h in pairs])
+    assert_close(pf_out.reshape(-1, 128)[idx], o_ref, TOL[W.KV_BF16], "prefill out")
+    o_ref, _ = oracle_decode(b, ocaches=(oracle.KV_BF16, ok, ov))
+    assert_close(dec_out, o_ref, TOL[W.KV_BF16], "decode out")
 
 
 def test_static_decode_reports_through_the_callers_error_word():
@@ -176,7 +214,7 @@ def test_checked_decode_reports_corrupt_tables_and_lengths(impl, corrupt):
     assert int(ws[:4].view(torch.int32)[0]) & B.PA_DEVERR_BAD_INDEX
 
 
-@pytest.mark.parametrize("impl", [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05])
+@pytest.mark.parametrize("impl", [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR])
 @pytest.mark.parametrize("corrupt", ["none", "block_id", "chunk_longer_than_context", "length_too_long"])
 def test_checked_prefill(impl, corrupt):
     b = W.random_prefill(505, [100, 37], [300, 37], 8, 2, 128, device=DEV, poison=True, shared_prefix_blocks=1)

@@ -61,11 +61,11 @@ def test_decode_local_attention(kv, window, chunk, impl):
     assert_close(lse, l_ref, LSE_TOL[kv], "lse")
 
 
-@pytest.mark.parametrize("impl", [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05])
+@pytest.mark.parametrize("impl", [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR])
 @pytest.mark.parametrize("window,chunk", [(1, 0), (64, 0), (200, 0), (0, 48), (0, 128), (100, 256), (5000, 0)])
 @pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_F16])
 def test_prefill_local_attention(kv, window, chunk, impl):
-    if impl == B.PA_PREFILL_TCGEN05 and kv not in (W.KV_BF16, W.KV_F16):
+    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
         pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
     q_lens, ctx = [300, 37, 1, 129], [700, 37, 200, 900]
     b = W.random_prefill(800 + window + chunk, q_lens, ctx, 8, 2, 128, kv_dtype=kv, device=DEV, poison=True,

@@ -324,13 +324,14 @@ PREFILL_CASES = [
     (128, 8, 2, W.KV_F16, [200, 64, 1], [530, 64, 129], 2),
     (128, 10, 2, W.KV_F16, [70, 3], [150, 90], 0),
 ]
-PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05]
+PREFILL_IMPLS = [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR]
+TC_IMPLS = (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR)
 
 
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("D,Hq,Hkv,kv,q_lens,ctx,shared", PREFILL_CASES)
 def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared, impl):
-    if impl == B.PA_PREFILL_TCGEN05 and kv not in (W.KV_BF16, W.KV_F16):
+    if impl in TC_IMPLS and kv not in (W.KV_BF16, W.KV_F16):
         pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
     b = W.random_prefill(200 + D + Hq + len(q_lens), q_lens, ctx, Hq, Hkv, D, kv_dtype=kv, device=DEV,
                          poison=True, shared_prefix_blocks=shared)
@@ -367,13 +368,17 @@ def test_mixed_step_write_then_decode_and_prefill(impl, fp16):
     assert_close(pf_lse, l_ref, LSE_TOL[kv], "prefill lse")
 
 
-@pytest.mark.parametrize("overlap", [True, False])
-def test_mixed_step_as_the_bench_runs_it(overlap):
+@pytest.mark.parametrize("fp16", [False, True])
+@pytest.mark.parametrize("mode", ["fused", "streams", "serial"])
+def test_mixed_step_as_the_bench_runs_it(mode, fp16):
     """Workload 5 through MixedStep, the step bench.py times: cache write,
-    then the decode on a second stream beside the prefill (overlap) or both
-    on one stream; every decode and prefill output against the oracle."""
+    then decode and prefill in one persistent launch (fused), the decode on a
+    second stream beside the prefill (streams) or both in order on one
+    stream (serial); every decode and prefill output against the oracle,
+    the cache bit-exact, and the workspace's counters back at zero."""
     from paged_kv_attention_14_gb300.step import MixedStep
-    b = W.workload(5, device=DEV, poison=True)
+    b = W.workload(5, device=DEV, poison=True, fp16=fp16)
+    kv = b.kv_dtype
     d = desc_of(b)
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     S = b.context_lens_decode.shape[0]
@@ -387,22 +392,69 @@ def test_mixed_step_as_the_bench_runs_it(overlap):
     ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, decode_lse=dec_lse, workspace=ws,
                    max_context_len_decode=maxL, prefill_out=pf_out, prefill_lse=pf_lse,
                    max_q_len=int((qsl[1:] - qsl[:-1]).max()),
-                   max_context_len_prefill=int(b.context_lens_prefill.max()), overlap=overlap)
-    assert ms.overlap == overlap
-    ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
-       (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill))
-    torch.cuda.synchronize()
-    assert int(ws[:4].view(torch.int32)[0]) == 0
-    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+                   max_context_len_prefill=int(b.context_lens_prefill.max()), mode=mode)
+    assert ms.mode == mode
+    for _ in range(2):  # the second call reuses the workspace the first left behind
+        dec_out.fill_(float("nan"))
+        pf_out.fill_(float("nan"))
+        kc.copy_(b.k_pool)
+        vc.copy_(b.v_pool)
+        ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
+           (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill))
+        torch.cuda.synchronize()
+        assert ws[:12].view(torch.int32).tolist() == [0, 0, 0], "error word and work counters"
+    code = oracle.KV_F16 if fp16 else oracle.KV_BF16
+    ok, ov = oracle.cache_write(code, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
                                 b.k_pool.cpu(), b.v_pool.cpu())
     assert np.array_equal(_bits(kc), ok) and np.array_equal(_bits(vc), ov)
-    oc = (oracle.KV_BF16, ok, ov)
+    oc = (code, ok, ov)
     o_ref, l_ref = oracle_decode(b, ocaches=oc)
-    assert_close(dec_out, o_ref, TOL[W.KV_BF16], "decode out")
-    assert_close(dec_lse, l_ref, LSE_TOL[W.KV_BF16], "decode lse")
+    assert_close(dec_out, o_ref, TOL[kv], "decode out")
+    assert_close(dec_lse, l_ref, LSE_TOL[kv], "decode lse")
     o_ref, l_ref = oracle_prefill(b, ocaches=oc)
-    assert_close(pf_out, o_ref, TOL[W.KV_BF16], "prefill out")
-    assert_close(pf_lse, l_ref, LSE_TOL[W.KV_BF16], "prefill lse")
+    assert_close(pf_out, o_ref, TOL[kv], "prefill out")
+    assert_close(pf_lse, l_ref, LSE_TOL[kv], "prefill lse")
+
+
+def test_graphed_step_replays_the_step_bit_for_bit():
+    """step.GraphedStep (the bench's end-to-end path): the copies in, the
+    single-launch step and the copies out captured as a CUDA graph; each
+    replay gives exactly the outputs of a direct call on the same inputs."""
+    from paged_kv_attention_14_gb300.step import GraphedStep, MixedStep
+    b = W.workload(5, device=DEV, poison=True)
+    d = desc_of(b)
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    ws = B.decode_workspace(d, S, maxL, DEV)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    dec_out = torch.empty(S, 32, 128, device=DEV)
+    pf_out = torch.empty(b.q_prefill.shape[0], 32, 128, device=DEV)
+    qsl = b.query_start_loc
+    ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, workspace=ws, max_context_len_decode=maxL,
+                   prefill_out=pf_out, max_q_len=512, max_context_len_prefill=2560, mode="fused")
+    q_host = b.q_decode.cpu().pin_memory()
+    q_dev = torch.empty_like(b.q_decode)
+    out_host = torch.empty(dec_out.shape).pin_memory()
+    pf_host = torch.empty(pf_out.shape).pin_memory()
+    dec_args = (q_dev, b.block_tables_decode, b.context_lens_decode)
+    pf_args = (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill)
+
+    def issue():
+        q_dev.copy_(q_host, non_blocking=True)
+        ms(b.k_new, b.v_new, b.slot_mapping, dec_args, pf_args)
+        out_host.copy_(dec_out, non_blocking=True)
+        pf_host.copy_(pf_out, non_blocking=True)
+
+    g = GraphedStep(issue)
+    ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode), pf_args)
+    torch.cuda.synchronize()
+    ref_dec, ref_pf = dec_out.cpu(), pf_out.cpu()
+    for _ in range(3):
+        out_host.zero_()
+        pf_host.zero_()
+        g()
+        assert torch.equal(out_host, ref_dec) and torch.equal(pf_host, ref_pf)
+    assert ws[:12].view(torch.int32).tolist() == [0, 0, 0]
 
 
 def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
@@ -414,6 +466,36 @@ def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
     assert torch.isfinite(o1).all() and torch.isfinite(o2).all()
     assert (o1 - o2).abs().max().item() < 2e-3
     assert (l1 - l2).abs().max().item() < 2e-3
+
+
+def test_tcgen05_prefill_reports_bf16_values_beyond_fp16():
+    """A bf16 V element of magnitude >= 2^16 does not fit the fp16 P.V product
+    of PA_PREFILL_TCGEN05: the call reports PA_DEVERR_FP16_RANGE; the pair
+    mode (P as a bf16 hi + lo pair, V as cached) computes it within tolerance
+    and reports nothing.  Values just below the limit are exact in fp16."""
+    b = W.random_prefill(330, [90, 20], [300, 20], 8, 2, 128, device=DEV, poison=True, shared_prefix_blocks=1)
+    t0 = int(b.block_tables_prefill[0, 2])
+    b.v_pool = b.v_pool.clone()
+    b.v_pool[t0, 1, 3, 17] = 65280.0   # the largest bf16 below 2^16: fits fp16
+    for impl, big, want in ((B.PA_PREFILL_TCGEN05, False, 0), (B.PA_PREFILL_TCGEN05_PAIR, True, 0),
+                            (B.PA_PREFILL_TCGEN05, True, B.PA_DEVERR_FP16_RANGE)):
+        if big:
+            b.v_pool[t0, 1, 5, 9] = -70000.0
+        ew = torch.zeros(1, dtype=torch.int32, device=DEV)
+        d = B.make_desc(b.num_blocks, 2, 8, 128, prefill_impl=impl, error_word=ew)
+        Tq = b.q_prefill.shape[0]
+        out = torch.full((Tq, 8, 128), float("nan"), device=DEV)
+        qsl = b.query_start_loc
+        B.pa_prefill_chunk(d, out, b.q_prefill, qsl, b.k_pool, b.v_pool, b.block_tables_prefill,
+                           b.context_lens_prefill, 90, 300, b.scale)
+        torch.cuda.synchronize()
+        assert int(ew[0]) == want, (impl, big)
+        if want == 0:
+            o_ref, _ = oracle_prefill(b)
+            # the rounding of P (2^-11 relative in fp16) scales with |v|: the
+            # bound is relative to the largest |v| here
+            vmax = float(b.v_pool[torch.isfinite(b.v_pool)].float().abs().max())
+            assert_close(out, o_ref, 1e-3 * vmax, "out")
 
 
 def test_prefill_single_query_rows_match_decode_oracle():
