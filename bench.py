@@ -256,6 +256,8 @@ def _local_config(args) -> dict:
     d = {}
     if args.fp16:
         d["kv_cache"] = "fp16"
+    if args.fp8_cache:
+        d["kv_cache"] = args.fp8_format
     if args.per_head_scales:
         d["fp8_scales"] = "per kv head"
     if args.workload == 5:
@@ -329,7 +331,7 @@ def run_ours(args):
     B.load(pa_build.build())
 
     b = W.workload(args.workload, device=dev, poison=False, fp8_format=FP8_FORMATS[args.fp8_format],
-                   fp16=args.fp16, per_head_scales=args.per_head_scales)
+                   fp16=args.fp16, per_head_scales=args.per_head_scales, fp8_cache=args.fp8_cache)
     kv = {W.KV_BF16: B.PA_KV_BF16, W.KV_F16: B.PA_KV_F16, W.KV_FP8: B.PA_KV_FP8_E4M3,
           W.KV_FP8_E5M2: B.PA_KV_FP8_E5M2}[b.kv_dtype]
     kv8 = kv in (B.PA_KV_FP8_E4M3, B.PA_KV_FP8_E5M2)
@@ -349,11 +351,13 @@ def run_ours(args):
         b.k_pool = b.v_pool = None
     S = b.context_lens_decode.shape[0]
     maxL = b.max_context_len_decode()
-    wsp = B.decode_workspace(desc, S, maxL, dev)
+    # the single-launch mixed step's workspace (it also serves pa_decode)
+    wsp = B.mixed_workspace(desc, S, maxL, dev)
     out = torch.empty(S, b.num_q_heads, b.head_dim, device=dev)
     kv_bytes = _decode_kv_bytes(b, args.sliding_window, args.attention_chunk)
     # the captured traffic figures are for the default settings only
-    local = bool(args.sliding_window or args.attention_chunk or args.fp16 or args.per_head_scales or args.prefill_impl)
+    local = bool(args.sliding_window or args.attention_chunk or args.fp16 or args.per_head_scales or args.prefill_impl
+                 or args.fp8_cache)
     mixed = b.q_prefill is not None
     if mixed:
         pf_out = torch.empty(b.q_prefill.shape, dtype=torch.float32, device=dev)
@@ -362,6 +366,8 @@ def run_ours(args):
         pf_maxL = int(b.context_lens_prefill.max())
         pf_flops = _prefill_flops(b, args.sliding_window, args.attention_chunk)
     # cache write + decode (+ prefill)
+    # cache write + decode (+ prefill); a fused mixed step launches one
+    # kernel for decode and prefill together
     launches_per_step = 2 + (1 if mixed else 0)
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
@@ -378,6 +384,9 @@ def run_ours(args):
                    prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
                    max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode)
     decode, prefill, attend = ms.decode, ms.prefill, ms.attend
+    if ms.mode == "fused":
+        launches_per_step = 2
+    args.mixed_mode = ms.mode  # the mode that runs (fused falls back to streams where it does not apply)
 
     def step():
         ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
@@ -553,7 +562,8 @@ def run_ours(args):
                     "how": "step.GraphedStep: one CUDA-graph replay per step of the pinned-host-to-device copy of the "
                            "inputs, the cache write and attention, and the copy of the outputs to pinned host memory, "
                            "then a wait; host wall clock"},
-            "gpu_launches": launches_per_step * K * R + (launches_per_step - 1) * K2 * R2,
+            # timed region 2 calls each entry point alone: decode (and prefill)
+            "gpu_launches": launches_per_step * K * R + (2 if mixed else 1) * K2 * R2,
             "timed_repeats": {"steps": R, "kernels_alone": R2,
                               "note": f"each repeat times exactly {K} steps ({K2} calls of each entry point alone); "
                                       "ms_per_step is the median repeat"},
@@ -735,6 +745,8 @@ def main():
                     help="mixed step (workload 5): one persistent launch, two streams, or one after the other")
     ap.add_argument("--per-head-scales", action="store_true",
                     help="workload 4 with one FP8 scale per kv head (heads of different magnitudes)")
+    ap.add_argument("--fp8-cache", action="store_true",
+                    help="workload 5 with an 8-bit cache (format --fp8-format; the same draws quantised)")
     ap.add_argument("--fp16", action="store_true",
                     help="fp16 variant of a bf16 workload (fp16 cache, q and new rows)")
     ap.add_argument("--sliding-window", type=int, default=0, help="sliding-window attention of W keys (0: off)")
@@ -746,6 +758,8 @@ def main():
         ap.error("--fp16 applies to the bf16 workloads (1, 2, 3, 5)")
     if args.per_head_scales and args.workload != 4:
         ap.error("--per-head-scales applies to the FP8 workload (4)")
+    if args.fp8_cache and (args.workload != 5 or args.fp16):
+        ap.error("--fp8-cache applies to workload 5")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -78,7 +78,7 @@ extern "C" {
  *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks.
  * 3: pa_kv_desc gains error_word, check_indices (appended); PA_DEVERR_*;
  *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
- *    pa_release_blocks, pa_mixed_attention. */
+ *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention. */
 #define PA_ABI_VERSION 3
 
 /* Symbols of the shared library; everything else in it stays hidden. */
@@ -113,9 +113,12 @@ typedef enum {
 #define PA_DEVERR_BAD_INDEX 2    /* check_indices: a block id, length or slot
                                     was out of range; results meaningless      */
 #define PA_DEVERR_FP16_RANGE 4   /* the tcgen05 prefill (PA_PREFILL_TCGEN05) met a
-                                    finite bf16 V value of magnitude >= 65536,
-                                    beyond its fp16 P.V product; the rows using
-                                    it are wrong: use PA_PREFILL_TCGEN05_PAIR */
+                                    finite bf16 V value (or, with an 8-bit
+                                    cache, a bf16 q value) of magnitude >=
+                                    65536, beyond its fp16 products; the rows
+                                    using it are wrong: use
+                                    PA_PREFILL_TCGEN05_PAIR (V) or
+                                    PA_PREFILL_MMA_SYNC                       */
 #define PA_DEVERR_REFCOUNT 8     /* pa_release_blocks met a page with no owner
                                     left; that entry was left untouched        */
 
@@ -131,10 +134,14 @@ typedef enum {
   PA_PREFILL_AUTO = 0,
   PA_PREFILL_MMA_SYNC = 1,    /* warp-level mma.sync tiles; every cache type; P
                                  as a hi + lo pair                              */
-  PA_PREFILL_TCGEN05 = 2,     /* tcgen05 tensor-memory tiles; bf16, fp16
-                                 caches; P.V in fp16 (see PA_DEVERR_FP16_RANGE) */
+  PA_PREFILL_TCGEN05 = 2,     /* tcgen05 tensor-memory tiles; bf16 and fp16
+                                 caches, and 8-bit caches with head_dim 128
+                                 (widened to fp16 in shared memory, q staged
+                                 in fp16); P.V in fp16 (see
+                                 PA_DEVERR_FP16_RANGE)                          */
   PA_PREFILL_TCGEN05_PAIR = 3 /* tcgen05 tiles with P as a hi + lo pair of the
-                                 cache's type: any bf16 range, more tensor work */
+                                 cache's type: any bf16 range, more tensor
+                                 work; bf16 and fp16 caches                     */
 } pa_prefill_impl;
 
 /*
@@ -286,7 +293,7 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
  * ranges first) and then the decode's partitions from one work list: the
  * decode fills the SMs the prefill's last wave leaves idle.  Issue the
  * step's pa_cache_write first, on the same stream.
- *   workspace : pa_decode_workspace_size(desc, num_dec_seqs,
+ *   workspace : pa_mixed_workspace_size(desc, num_dec_seqs,
  *               dec_max_context_len) bytes, zero-filled before its first use;
  *               every call that completes without error leaves it ready for
  *               the next (its counters back at zero).  Calls that overlap on
@@ -296,6 +303,10 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
  * prefill_impl AUTO or TCGEN05; PA_ERR_UNSUPPORTED otherwise (make the two
  * calls instead).
  */
+/* Bytes of scratch pa_mixed_attention needs for num_dec_seqs decode
+ * sequences on the current device (0 if the descriptor is invalid). */
+PA_API size_t pa_mixed_workspace_size(const pa_kv_desc *desc, int32_t num_dec_seqs, int32_t dec_max_context_len);
+
 PA_API pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
                                     const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
                                     const int32_t *dec_context_lens, int32_t num_dec_seqs,

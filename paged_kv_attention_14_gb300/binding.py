@@ -50,7 +50,7 @@ ABI_VERSION = 3
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
             "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
-            "pa_mixed_attention")
+            "pa_mixed_workspace_size", "pa_mixed_attention")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -117,6 +117,8 @@ def load(path: Optional[str] = None):
         lib.pa_merge_partials.restype = ctypes.c_int
         lib.pa_decode_static.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P]
         lib.pa_decode_static.restype = ctypes.c_int
+        lib.pa_mixed_workspace_size.argtypes = [D, I32, I32]
+        lib.pa_mixed_workspace_size.restype = SZ
         lib.pa_mixed_attention.argtypes = [D, P, P, P, P, I32, P, I32, I32, P, P, P, P, P, I32, P, I32, I32, I32,
                                            P, P, F, P, SZ, P]
         lib.pa_mixed_attention.restype = ctypes.c_int
@@ -258,12 +260,20 @@ def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, con
                                    float(scale), _stream(stream)))
 
 
+def mixed_workspace(desc: PaKvDesc, num_dec_seqs: int, max_context_len: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor of the size pa_mixed_attention needs."""
+    n = load().pa_mixed_workspace_size(ctypes.byref(desc), int(num_dec_seqs), int(max_context_len))
+    if n == 0:
+        raise PaError(PA_ERR_UNSUPPORTED, last_error())
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
 def pa_mixed_attention(desc: PaKvDesc, k_cache, v_cache, scale: float, workspace, dec=None, pf=None, stream=None):
     """Decode and prefill attention of one step in one launch.  ``dec``:
     (out, q, block_tables, context_lens, max_context_len[, lse]) or None;
     ``pf``: (out, q, query_start_loc, block_tables, context_lens, max_q_len,
-    max_context_len[, lse]) or None.  ``workspace``: a decode workspace
-    (decode_workspace) for the decode part's batch."""
+    max_context_len[, lse]) or None.  ``workspace``: mixed_workspace() for
+    the decode part's batch."""
     if dec is not None:
         d_out, d_q, d_bt, d_cl, d_maxL = dec[:5]
         d_lse = dec[5] if len(dec) > 5 else None

@@ -212,6 +212,18 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 
+size_t pa_mixed_workspace_size(const pa_kv_desc *desc, int32_t num_dec_seqs, int32_t dec_max_context_len) {
+  (void)dec_max_context_len;
+  if (check_desc(desc) != PA_OK || num_dec_seqs < 0) return 0;
+  pa::DecodePlan plan;
+  const char *why = "";
+  if (pa::plan_decode(*desc, num_dec_seqs, &plan, &why) != PA_OK) {
+    fail(PA_ERR_UNSUPPORTED, "%s", why);
+    return 0;
+  }
+  return pa::mixed_plan(*desc, num_dec_seqs, plan).workspace_bytes;
+}
+
 pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
                              const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
                              const int32_t *dec_context_lens, int32_t num_dec_seqs, int32_t dec_max_context_len,
@@ -238,10 +250,11 @@ pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_
   const char *why = "";
   st = pa::check_mixed(*desc, plan, &why);
   if (st != PA_OK) return fail(st, "%s", why);
+  plan = pa::mixed_plan(*desc, num_dec_seqs, plan);
   if (!workspace || !aligned16(workspace))
     return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
   if (workspace_bytes < plan.workspace_bytes)
-    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_decode_workspace_size()%s");
+    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_mixed_workspace_size()%s");
   const cudaError_t e = pa::launch_mixed(*desc, plan, dec_out, dec_lse, dec_q, dec_block_tables,
                                          dec_max_blocks_per_seq, dec_context_lens, num_dec_seqs, pf_out, pf_lse, pf_q,
                                          query_start_loc, pf_block_tables, pf_max_blocks_per_seq, pf_context_lens,

@@ -57,6 +57,9 @@ pa_status validate_prefill(const pa_kv_desc *desc, const float *out, const float
 // and its launch.  The decode plan sizes the decode partitions and the
 // workspace, whose head also holds the launch's work counters.
 pa_status check_mixed(const pa_kv_desc &d, const DecodePlan &plan, const char **why);
+// The decode part's plan in the single-launch step (more partitions than SMs)
+// from pa_decode's plan for the same batch.
+DecodePlan mixed_plan(const pa_kv_desc &d, int32_t num_dec_seqs, const DecodePlan &plan);
 cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec_out, float *dec_lse,
                          const void *dec_q, const int32_t *dec_block_tables, int32_t dec_max_blocks,
                          const int32_t *dec_context_lens, int32_t num_dec_seqs, float *pf_out, float *pf_lse,

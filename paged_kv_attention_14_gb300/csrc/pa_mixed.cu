@@ -42,9 +42,19 @@ struct MixedArgs {
   int32_t *finished;    // workspace: CTAs that ran out of work
 };
 
+// Consumer warps of a decode partition in the single-launch step: a
+// partition runs alone on its SM, where four consumer warps stream well
+// below the SM's share of the HBM bandwidth; the CTA has 12 warps, and six
+// consumers still leave room for three stages (GQ <= 8).
+template <int GQ>
+constexpr int mixed_decode_warps() {
+  return GQ <= 8 ? 6 : dec::kConsumerWarps;
+}
+
 template <int D, int KVT, int GQ>
 __global__ void __launch_bounds__(pftc::NTHREADS, 1) mixed_kernel(const __grid_constant__ MixedArgs m) {
-  constexpr int NS = dec::mma_stages<D, KVT, GQ, 1>();
+  constexpr int NCW = mixed_decode_warps<GQ>();
+  constexpr int NS = dec::mma_stages<D, KVT, GQ, 1, NCW>();
   // launched as a programmatic dependent of the preceding kernel (the cache
   // write): nothing is read before its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(pftc::NTHREADS, 1) mixed_kernel(const __grid_c
       const int x = item / yz, y = (item % yz) % m.pf_gy, z = (item % yz) / m.pf_gy;
       pftc::prefill_tile<D, KVT, pftc::kPvF16>(m.pf, smem, tmem, x, y, z, m.pf_gx);
     } else {
-      dec::decode_partition<D, KVT, GQ, 1, NS, dec::kConsumerWarps>(m.dec, smem_raw, item - m.n_pf, m.n_dec);
+      dec::decode_partition<D, KVT, GQ, 1, NS, NCW>(m.dec, smem_raw, item - m.n_pf, m.n_dec);
     }
     __syncthreads();
 #ifdef PA_MIXED_TRACE
@@ -112,8 +122,10 @@ __global__ void __launch_bounds__(pftc::NTHREADS, 1) mixed_kernel(const __grid_c
 template <int D, int KVT, int GQ>
 cudaError_t launch_mixed_t(const MixedArgs &m, cudaStream_t stream) {
   using PC = pftc::Cfg<D, KVT, pftc::kPvF16>;
-  constexpr int NS = dec::mma_stages<D, KVT, GQ, 1>();
-  using DC = dec::MmaCfg<D, KVT, GQ, 1, NS, dec::kConsumerWarps>;
+  constexpr int NCW = mixed_decode_warps<GQ>();
+  constexpr int NS = dec::mma_stages<D, KVT, GQ, 1, NCW>();
+  static_assert(NS >= 3, "at least three decode stages in flight");
+  using DC = dec::MmaCfg<D, KVT, GQ, 1, NS, NCW>;
   constexpr size_t smem = static_cast<size_t>(PC::SMEM_LAUNCH) > DC::SMEM ? static_cast<size_t>(PC::SMEM_LAUNCH)
                                                                              : DC::SMEM;
   static_assert(DC::NTHREADS <= pftc::NTHREADS, "the decode body fits the CTA");
@@ -144,6 +156,21 @@ extern "C" PA_API int pa_debug_mixed_trace_clear() {
   return static_cast<int>(cudaMemcpyToSymbol(g_mix_trace, zero, sizeof zero));
 }
 #endif
+
+// The decode plan of the single-launch step: kMixedDecodeSplit partitions
+// per SM.  A decode partition alone on its SM streams far below its share
+// of the HBM bandwidth (about 34 GB/s on GB300, workload 5), so finer
+// partitions were tried to spread the decode's tail over more SMs: two per
+// SM took 18 us each instead of 28 us, but the per-partition set-up grew
+// the total and the step got slower (146 against 140 us); one it is.
+constexpr int kMixedDecodeSplit = 1;
+
+DecodePlan mixed_plan(const pa_kv_desc &d, int32_t num_dec_seqs, const DecodePlan &plan) {
+  DecodePlan p = plan;
+  p.num_ctas = plan.num_ctas * kMixedDecodeSplit;
+  p.workspace_bytes = dec::ws_layout(num_dec_seqs, p.num_groups, p.num_ctas, p.slot_heads, d.head_dim).total;
+  return p;
+}
 
 pa_status check_mixed(const pa_kv_desc &d, const DecodePlan &plan, const char **why) {
   if (d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_F16) {

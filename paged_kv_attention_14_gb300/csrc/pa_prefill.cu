@@ -409,9 +409,13 @@ pa_status check_prefill(const pa_kv_desc &d, const char **why) {
     *why = "prefill_impl must be PA_PREFILL_AUTO, PA_PREFILL_MMA_SYNC, PA_PREFILL_TCGEN05 or PA_PREFILL_TCGEN05_PAIR";
     return PA_ERR_INVALID_ARG;
   }
-  if ((d.prefill_impl == PA_PREFILL_TCGEN05 || d.prefill_impl == PA_PREFILL_TCGEN05_PAIR) &&
-      d.kv_dtype != PA_KV_BF16 && d.kv_dtype != PA_KV_F16) {
-    *why = "the tcgen05 prefill kernel takes bf16 and fp16 caches";
+  const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
+  if (d.prefill_impl == PA_PREFILL_TCGEN05 && kv8 && d.head_dim != 128) {
+    *why = "the tcgen05 prefill kernel takes 8-bit caches with head_dim 128";
+    return PA_ERR_UNSUPPORTED;
+  }
+  if (d.prefill_impl == PA_PREFILL_TCGEN05_PAIR && kv8) {
+    *why = "the tcgen05 prefill's pair mode takes bf16 and fp16 caches";
     return PA_ERR_UNSUPPORTED;
   }
   return PA_OK;
@@ -424,7 +428,10 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
                            bool prefix_mode, int num_splits, int split_len, int out_slots) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
-  const int impl = d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl : (fp8 ? PA_PREFILL_MMA_SYNC : PA_PREFILL_TCGEN05);
+  // automatic choice: the tcgen05 kernel, except 8-bit caches of head_dim 64
+  const int impl = d.prefill_impl != PA_PREFILL_AUTO       ? d.prefill_impl
+                   : (fp8 && d.head_dim != 128)             ? PA_PREFILL_MMA_SYNC
+                                                            : PA_PREFILL_TCGEN05;
   if (impl == PA_PREFILL_TCGEN05 || impl == PA_PREFILL_TCGEN05_PAIR)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len,

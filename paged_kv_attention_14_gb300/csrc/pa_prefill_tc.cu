@@ -53,12 +53,15 @@ cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const
                               int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
                               bool prefix_mode, int num_splits, int split_len, int out_slots, bool pair_p) {
   const bool f16 = d.kv_dtype == PA_KV_F16;
+  const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   // one instantiation per (head_dim, cache type, P mode)
   auto pick = [&](auto launcher) {
     return launcher(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
                     context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len, out_slots);
   };
   using namespace pftc;
+  if (kv8)  // head_dim 128 and fp16 P (check_prefill)
+    return d.kv_dtype == PA_KV_FP8_E5M2 ? pick(launch<128, kKvE5M2, kPvF16>) : pick(launch<128, kKvFp8, kPvF16>);
   if (d.head_dim == 128) {
     if (f16) return pair_p ? pick(launch<128, kKvF16, kPvPair>) : pick(launch<128, kKvF16, kPvF16>);
     return pair_p ? pick(launch<128, kKvBf16, kPvPair>) : pick(launch<128, kKvBf16, kPvF16>);

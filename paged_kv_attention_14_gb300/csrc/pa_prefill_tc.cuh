@@ -94,7 +94,11 @@ struct Args {
   int num_q_heads;
   int g;
   int qt;  // queries per CTA (256 / g)
-  float qscale;
+  float qscale;     // scale * k_scale * log2(e)
+  float qscale0;    // scale * log2(e) (8-bit caches with per-head scales)
+  float vscale;     // v_scale (8-bit caches; 1 otherwise)
+  const float *k_scales;  // per-kv-head scales of an 8-bit cache, or NULL
+  const float *v_scales;
   int window;  // local attention (see pa_kv_desc), 0: none
   int chunk;
   int prefix_mode;  // 1: every query after all L keys, no causal mask (shared prefix)
@@ -148,6 +152,12 @@ template <int D, int KVT, int PVM>
 struct Cfg {
   static constexpr bool P16 = PVM == kPvF16;           // single fp16 P
   static constexpr bool CONVERT = P16 && KVT == kKvBf16;  // V tiles converted bf16 -> fp16
+  // 8-bit caches (E4M3, E5M2): K and V tiles land as bytes in the second
+  // half of their slot and are widened in place to fp16 (exact); Q is staged
+  // in fp16, so both products take fp16 operands
+  static constexpr bool KV8 = !kv16(KVT);
+  static constexpr bool F16OPS = KVT == kKvF16 || KV8;  // QK in fp16
+  static_assert(!KV8 || (P16 && D == 128), "8-bit caches: fp16 P, head_dim 128");
   static constexpr int HALVES = D / 64;          // 128-byte column halves of a row
   static constexpr int QHALF = MT * 128;         // bytes of one half of one Q tile
   static constexpr int QB = HALVES * QHALF;      // one Q tile
@@ -168,15 +178,16 @@ struct Cfg {
   static constexpr uint32_t O_COL = NQT * KT;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(NQT * (KT + D) <= TMEM_COLS, "TMEM columns");
-  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false, KVT == kKvF16);
+  static constexpr uint32_t IDESC_QK = umma_idesc_bf16(MT, KT, false, false, F16OPS);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(MT, D, false, true, P16 || KVT == kKvF16);
   // bytes landed per 16-token block of K (or of V), all halves
-  static constexpr uint32_t BLOCK_BYTES = HALVES * 16u * 128u;
+  static constexpr uint32_t BLOCK_BYTES = KV8 ? 16u * D : HALVES * 16u * 128u;
 };
 
 // barriers: K_FULL[NSK], K_EMPTY[NSK], V_FULL[NSV], V_EMPTY[NSV],
 // S_FULL[tile], P_FULL[tile], V_READY[NSV] (fp16 P: the V tile is in fp16,
-// rows outside the needed keys zeroed)
+// rows outside the needed keys zeroed), K_READY[NSK] (8-bit caches: the K
+// tile widened to fp16)
 enum Bar {
   K_FULL = 0,
   K_EMPTY = K_FULL + NSK,
@@ -185,7 +196,8 @@ enum Bar {
   S_FULL = V_EMPTY + NSV,
   P_FULL = S_FULL + NQT,
   V_READY = P_FULL + NQT,
-  NBAR = V_READY + NSV
+  K_READY = V_READY + NSV,  // 8-bit caches: the K tile widened to fp16
+  NBAR = K_READY + NSK
 };
 static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
@@ -275,6 +287,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       mbar_init(&bar[P_FULL + t], 8);
     }
     for (int i = 0; i < NSV; ++i) mbar_init(&bar[V_READY + i], 2);
+    for (int i = 0; i < NSK; ++i) mbar_init(&bar[K_READY + i], 2);
     *s_abort = 0;
     *s_last_k = -1;
     *s_last_v = -1;
@@ -282,9 +295,12 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   }
 
   // ---- Q tiles: row R = query * g + head (tile R / 128, lane R % 128),
-  // [tile][half][row][128 B], 128-B swizzle
+  // [tile][half][row][128 B], 128-B swizzle.  With an 8-bit cache the bf16
+  // queries are staged as fp16 (round to nearest; a finite |q| >= 2^16 does
+  // not fit and is reported).
   {
     constexpr int CHUNKS = D / 8;  // 16-byte chunks per row
+    float qmax = 0.f;
     for (int i = tid; i < MROWS * CHUNKS; i += NTHREADS) {
       const int R = i / CHUNKS;
       const int ch = i - R * CHUNKS;
@@ -294,8 +310,26 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       if (ok) src = a.q + (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * D + ch * 8;
       const int r = R & (MT - 1);
       uint8_t *dst = smem + C::OFF_Q + (R / MT) * C::QB + (ch >> 3) * C::QHALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-      cp_async16(dst, src, ok);
+      if constexpr (C::KV8) {
+        uint4 y = make_uint4(0, 0, 0, 0);
+        if (ok) {
+          const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src));
+          const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float f0 = bf16lo(w[e]), f1 = bf16hi(w[e]);
+            qmax = fmaxf(qmax, fmaxf(fabsf(f0), fabsf(f1)));
+            o[e] = pack_f16x2(f0, f1);
+          }
+          y = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4 *>(dst) = y;
+      } else {
+        cp_async16(dst, src, ok);
+      }
     }
+    if (C::KV8 && qmax >= 65536.f && qmax <= FLT_MAX) report_error(a.err, nullptr, kErrFp16Range);
     cp_async_commit();
     cp_async_wait<0>();
     fence_proxy_async_smem();
@@ -309,10 +343,13 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     // ------------------------------------------------------ TMA producer
     const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
     const uint64_t pol = l2_evict_first_policy();
-    // lane -> (block of the tile, half); the same lanes copy K and V
-    const int bi = lane / C::HALVES;
-    const int hh = lane % C::HALVES;
-    const bool issuer = lane < BPT * C::HALVES;
+    // lane -> (block of the tile, half); the same lanes copy K and V.  An
+    // 8-bit block is one box of 16 rows of D bytes, landing in the second
+    // half of the slot (widened in place by warps 2-3)
+    constexpr int BOXES = C::KV8 ? 1 : C::HALVES;
+    const int bi = lane / BOXES;
+    const int hh = lane % BOXES;
+    const bool issuer = lane < BPT * BOXES;
     auto block_id = [&](int lb) {
       const int v = __ldg(table + lb);
       return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
@@ -361,7 +398,8 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
         if (lane == 0) mbar_arrive_expect_tx(&bar[full], (nblk - bskip) * C::BLOCK_BYTES);
         __syncwarp();
         if (issuer && bi < nblk && bi >= bskip) {
-          uint8_t *dst = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB + hh * C::KVHALF + bi * 16 * 128;
+          uint8_t *slot = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB;
+          uint8_t *dst = C::KV8 ? slot + C::KVHALF + bi * 16 * D : slot + hh * C::KVHALF + bi * 16 * 128;
           tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
         }
         if (lane == 0) *(part ? s_last_v : s_last_k) = jj;
@@ -408,7 +446,8 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       // V is ready for the MMAs once it landed (pair mode) or once warps 2-3
       // converted it (fp16 P)
       constexpr int VB = C::P16 ? V_READY : V_FULL;
-      if (!mbar_wait(&bar[K_FULL], 0, a.wait_ns) || !mbar_wait(&bar[VB], 0, a.wait_ns)) ok = false;
+      constexpr int KB = C::KV8 ? K_READY : K_FULL;  // 8-bit: once widened to fp16
+      if (!mbar_wait(&bar[KB], 0, a.wait_ns) || !mbar_wait(&bar[VB], 0, a.wait_ns)) ok = false;
       if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < NQT; ++t) {
@@ -437,7 +476,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
           }
           if (next) {
             if (t == 0) {
-              if (!mbar_wait(&bar[K_FULL + (jj + 1) % NSK], ((jj + 1) / NSK) & 1, a.wait_ns)) {
+              if (!mbar_wait(&bar[KB + (jj + 1) % NSK], ((jj + 1) / NSK) & 1, a.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -458,30 +497,92 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     __syncwarp();
   } else if (C::P16 && warp >= kConvWarp0 && warp < kConvWarp0 + 2) {
-    // ------------------------------------------ V tile preparation (fp16 P)
+    // --------------------------------- K / V tile preparation (fp16 P)
     // Each landed V tile: rows outside the needed keys [kv_lo, kv_end)
     // zeroed (stale or poisoned data; 0 * NaN would not vanish in the PV),
     // and for a bf16 cache every element converted to fp16 in place (round
-    // to nearest; exact for |v| in [2^-14, 2^16), within 2^-25 below).  The
-    // MMA issuer waits for V_READY.  A finite |v| >= 2^16 does not fit fp16:
-    // it is reported (PA_DEVERR_FP16_RANGE) and its products are wrong.
+    // to nearest; exact for |v| in [2^-14, 2^16), within 2^-25 below).  A
+    // finite |v| >= 2^16 does not fit fp16: it is reported
+    // (PA_DEVERR_FP16_RANGE) and its products are wrong.  With an 8-bit
+    // cache the K tile is widened to fp16 as well (exact).  The MMA issuer
+    // waits for V_READY (and K_READY).
     const int ct = tid - kConvWarp0 * 32;
     bool ok = true;
     float vmax = 0.f;
     constexpr int UNITS = C::KVB / 16;   // 16-byte units of a V tile
     constexpr int UROW = KT * 8;         // units of one 128-byte column half
+    // 8-bit caches: widen the tile of a slot in place.  The bytes landed in
+    // the slot's second half as rows of 128 bytes (16-byte chunk c of row r
+    // at (c ^ (r & 7)) * 16, the TMA's 128-byte swizzle); the fp16 tile
+    // takes the whole slot as [half][row][128 B], same swizzle.  Dims 0-63
+    // (chunks 0-3) go to the first half, which the bytes do not occupy;
+    // dims 64-127 are read first, then (after a barrier of the two
+    // converter warps) written over them.  Rows outside [r_lo, r_hi) become
+    // zero where zero_rows is set (V: 0 * NaN would not vanish).
+    auto widen8 = [&](uint8_t *slot, int r_lo, int r_hi, bool zero_rows) {
+      const uint8_t *land = slot + C::KVHALF;
+      auto put = [&](int half, int r, int c4, const uint4 &x) {
+        const bool keep = !zero_rows || (r >= r_lo && r < r_hi);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          o[2 * e] = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(w[e] & 0xffffu));
+          o[2 * e + 1] = fp8x2_to_f16x2<KVT>(static_cast<uint16_t>(w[e] >> 16));
+        }
+        uint8_t *row = slot + half * C::KVHALF + r * 128;
+        const int k0 = 2 * c4, k1 = 2 * c4 + 1;  // output chunks of 8 fp16
+        *reinterpret_cast<uint4 *>(row + ((k0 ^ (r & 7)) << 4)) =
+            keep ? make_uint4(o[0], o[1], o[2], o[3]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(row + ((k1 ^ (r & 7)) << 4)) =
+            keep ? make_uint4(o[4], o[5], o[6], o[7]) : make_uint4(0, 0, 0, 0);
+      };
+#pragma unroll 2
+      for (int u = ct; u < KT * 4; u += 64) {
+        const int r = u >> 2, c = u & 3;
+        put(0, r, c, *reinterpret_cast<const uint4 *>(land + r * 128 + ((c ^ (r & 7)) << 4)));
+      }
+      constexpr int PER = KT * 4 / 64;
+      uint4 x[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int u = ct + 64 * k, r = u >> 2, c = 4 + (u & 3);
+        x[k] = *reinterpret_cast<const uint4 *>(land + r * 128 + ((c ^ (r & 7)) << 4));
+      }
+      named_bar_sync(2, 64);  // every read of the landed bytes is done
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int u = ct + 64 * k;
+        put(1, u >> 2, u & 3, x[k]);
+      }
+    };
     for (int jj = 0; jj < n_iter; ++jj) {
+      const int key0 = (j0 + jj) * KT;
+      const int r_lo = max(kv_lo - key0, 0);
+      const int r_hi = min(kv_end - key0, KT);
+      if constexpr (C::KV8) {
+        // K of this tile first (the MMAs need it before V); both warps agree
+        // to go on, so their barrier in widen8 stays matched
+        const int stk = jj % NSK;
+        if (!named_bar_and(2, 64, mbar_wait(&bar[K_FULL + stk], (jj / NSK) & 1, a.wait_ns))) {
+          ok = false;
+          break;
+        }
+        widen8(smem + C::OFF_K + stk * C::KVB, r_lo, r_hi, false);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[K_READY + stk]);
+      }
       const int st = jj % NSV;
-      if (!mbar_wait(&bar[V_FULL + st], (jj / NSV) & 1, a.wait_ns)) {
+      if (!named_bar_and(2, 64, mbar_wait(&bar[V_FULL + st], (jj / NSV) & 1, a.wait_ns))) {
         ok = false;
         break;
       }
       if (ct == 0) PF_TL(17, jj);
-      const int key0 = (j0 + jj) * KT;
-      const int r_lo = max(kv_lo - key0, 0);
-      const int r_hi = min(kv_end - key0, KT);
       uint4 *vt = reinterpret_cast<uint4 *>(smem + C::OFF_V + st * C::KVB);
-      if constexpr (C::CONVERT) {
+      if constexpr (C::KV8) {
+        widen8(smem + C::OFF_V + st * C::KVB, r_lo, r_hi, true);
+      } else if constexpr (C::CONVERT) {
         // eight 16-byte units per step, all loads issued before any
         // conversion so that their latencies overlap
         constexpr int ILP = 8;
@@ -540,7 +641,10 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float *xch = reinterpret_cast<float *>(smem + C::OFF_X);  // [2][MT] maxima / sums of the halves
     constexpr int kSoftmaxThreads = 256;
-    const float qscale = a.qscale;
+    // score scale and output scale of this kv head (its own k / v scale
+    // where an 8-bit cache has per-head scales)
+    const float qscale = a.k_scales ? a.qscale0 * __ldg(a.k_scales + kvh) : a.qscale;
+    const float vscale = a.v_scales ? __ldg(a.v_scales + kvh) : a.vscale;
     float m_ref[NQT], l[NQT];
     int pos[NQT], first[NQT];
 #pragma unroll
@@ -708,7 +812,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       const int qi = R / g;
       const bool rv = R < rows_used && qi < nq;
       const uint32_t o_col = C::O_COL + t * D;
-      const float inv = lt[t] > 0.f ? 1.f / lt[t] : 0.f;
+      const float inv = lt[t] > 0.f ? vscale / lt[t] : 0.f;
       const int64_t orow_i =
           (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * a.out_slots + split;
       float *orow = rv ? a.out + orow_i * D : nullptr;
@@ -782,8 +886,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
 
 template <int D>
 inline bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
-  const CUtensorMapDataType dt = d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
+  const CUtensorMapDataType dt = kv8                      ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                      const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                      CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
@@ -801,8 +907,10 @@ inline bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
   const MapKey key = map_key(base, d.num_blocks, d.num_kv_heads, D, d.kv_dtype);
   if (cache.find(key, map)) return true;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(d.num_blocks) * d.num_kv_heads * 16};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, 16};
+  // 16-bit caches: boxes of 64 columns (128 bytes) x 16 rows; 8-bit caches:
+  // a whole row of D bytes (128) x 16 rows
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * (kv8 ? 1 : 2)};
+  const cuuint32_t box[2] = {kv8 ? static_cast<cuuint32_t>(D) : 64u, 16};
   const cuuint32_t estr[2] = {1, 1};
   if (enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -832,7 +940,12 @@ inline bool make_args(Args *a, const pa_kv_desc &d, float *out, float *lse, cons
   a->num_q_heads = d.num_q_heads;
   a->g = d.num_q_heads / d.num_kv_heads;
   a->qt = MROWS / a->g;  // queries per CTA
-  a->qscale = scale * kLog2e;
+  const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
+  a->qscale = scale * ((kv8 && d.k_scale != 0.f) ? d.k_scale : 1.f) * kLog2e;
+  a->qscale0 = scale * kLog2e;
+  a->vscale = (kv8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
+  a->k_scales = kv8 ? d.k_scales : nullptr;
+  a->v_scales = kv8 ? d.v_scales : nullptr;
   a->window = d.sliding_window;
   a->chunk = d.attention_chunk;
   a->prefix_mode = prefix_mode ? 1 : 0;

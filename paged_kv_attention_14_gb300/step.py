@@ -57,6 +57,11 @@ class MixedStep:
         fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
                     and desc.decode_impl in (B.PA_DECODE_AUTO, B.PA_DECODE_MMA)
                     and desc.prefill_impl in (B.PA_PREFILL_AUTO, B.PA_PREFILL_TCGEN05) and workspace is not None)
+        if mode == "fused" and fused_ok and both:
+            need = B.load().pa_mixed_workspace_size(B.ctypes.byref(desc), int(decode_out.shape[0]),
+                                                    int(max_context_len_decode))
+            if workspace.numel() < need:
+                raise ValueError(f"the fused step needs a workspace of {need} bytes (binding.mixed_workspace)")
         # fused needs both parts and a descriptor pa_mixed_attention takes
         self.mode = "streams" if mode == "fused" and not (fused_ok and both) else mode
         self.overlap = self.mode == "streams" and both

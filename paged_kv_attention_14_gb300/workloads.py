@@ -250,12 +250,14 @@ WORKLOAD_NAMES = {
 
 
 def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP8,
-             fp16: bool = False, per_head_scales: bool = False) -> PagedBatch:
+             fp16: bool = False, per_head_scales: bool = False, fp8_cache: bool = False) -> PagedBatch:
     """Build workload ``n`` (1..5) on ``device``.  ``fp8_format`` picks the
     8-bit cache format of workload 4 (E4M3, or E5M2 for the same shapes);
     ``fp16`` turns the bf16 workloads (1, 2, 3, 5) into fp16 ones: fp16 cache,
     q and new rows, from the same random draws; ``per_head_scales`` gives
-    workload 4's kv heads different magnitudes and one scale each."""
+    workload 4's kv heads different magnitudes and one scale each;
+    ``fp8_cache`` gives workload 5 an 8-bit cache of format ``fp8_format``
+    (the same draws, quantised with per-tensor amax / format-max scales)."""
     seed = 1000 + n
     kv16 = KV_F16 if fp16 else KV_BF16
 
@@ -290,6 +292,9 @@ def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP
                              seed, lens.tolist(), 40, 8, 128, fp8_format, 1.0 / math.sqrt(128),
                              device, poison, per_head_scales=per_head_scales)
     if n == 5:
+        if fp8_cache:
+            nm = WORKLOAD_NAMES[5].replace("bf16", "E4M3 KV" if fp8_format == KV_FP8 else "E5M2 KV")
+            return _mixed_batch(seed, device, poison, fp8_format, nm)
         return _mixed_batch(seed, device, poison, kv16, name(5))
     raise ValueError(f"unknown workload {n}")
 

@@ -26,6 +26,15 @@ _CODES = {W.KV_BF16: (B.PA_KV_BF16, oracle.KV_BF16), W.KV_F16: (B.PA_KV_F16, ora
 KV16 = (W.KV_BF16, W.KV_F16)
 
 
+def tcgen05_takes(impl: int, kv: str, head_dim: int) -> bool:
+    """Whether the prefill kernel ``impl`` takes this cache type and head_dim:
+    the mma.sync kernel every one; the tcgen05 kernel 16-bit caches, and
+    8-bit caches at head_dim 128 outside its pair mode."""
+    if impl == B.PA_PREFILL_MMA_SYNC or kv in KV16:
+        return True
+    return impl == B.PA_PREFILL_TCGEN05 and head_dim == 128
+
+
 def _cpu(t):
     return None if t is None else t.cpu()
 

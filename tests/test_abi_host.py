@@ -233,6 +233,20 @@ def test_static_decode_checks_arguments_like_pa_decode(lib):
                                 0.1, None) == B.PA_OK
 
 
+def test_mixed_attention_argument_errors(lib):
+    d = _desc()
+    assert lib.pa_mixed_workspace_size(None, 4, 16) == 0
+    null = None
+    args = (null, null, null, null, 4, null, 0, 0, null, null, null, null, null, 4, null, 0, 0, 0, 0x3000, 0x4000,
+            0.1, 0x7000, 1 << 20, null)
+    assert lib.pa_mixed_attention(None, *args) == B.PA_ERR_INVALID_ARG
+    # a decode part with a NULL output
+    bad = (null, null, 0x2000, 0x5000, 4, 0x6000, 2, 16) + args[8:]
+    assert lib.pa_mixed_attention(ctypes.byref(d), *bad) == B.PA_ERR_INVALID_ARG
+    # an unsupported cache type for the single launch (head_dim 64) is refused on the host
+    assert B.last_error() != ""
+
+
 def test_prefill_argument_errors(lib):
     d = _desc()
     args = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000)

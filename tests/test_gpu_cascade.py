@@ -14,7 +14,8 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
-from pa_helpers import LSE_TOL, TOL, assert_close, desc_of, gpu_caches, oracle_caches, oracle_decode, _CODES
+from pa_helpers import (LSE_TOL, TOL, assert_close, desc_of, gpu_caches, oracle_caches, oracle_decode, _CODES,
+                        tcgen05_takes)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -74,8 +75,8 @@ CASES = [
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("kv,groups,plens,slens,Hq,Hkv,D", CASES)
 def test_prefix_attention_matches_oracle(kv, groups, plens, slens, Hq, Hkv, D, impl, splits):
-    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
-        pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
+    if not tcgen05_takes(impl, kv, D):
+        pytest.skip("the tcgen05 prefill takes 16-bit caches, and 8-bit ones at head_dim 128 outside the pair mode")
     b = W.shared_prefix_decode(300 + sum(plens), groups, plens, slens, Hq, Hkv, D, kv_dtype=kv, device=DEV)
     out, lse = _merged(*_gpu_prefix(b, gpu_caches(b), impl, splits))
     o_ref, l_ref = _oracle_prefix(b, oracle_caches(b))
@@ -91,8 +92,8 @@ def test_prefix_attention_matches_oracle(kv, groups, plens, slens, Hq, Hkv, D, i
 @pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("kv,groups,plens,slens,Hq,Hkv,D", CASES)
 def test_cascade_prefix_suffix_merge_equals_full_decode(kv, groups, plens, slens, Hq, Hkv, D, impl, splits):
-    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
-        pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
+    if not tcgen05_takes(impl, kv, D):
+        pytest.skip("the tcgen05 prefill takes 16-bit caches, and 8-bit ones at head_dim 128 outside the pair mode")
     b = W.shared_prefix_decode(400 + sum(plens), groups, plens, slens, Hq, Hkv, D, kv_dtype=kv, device=DEV)
     c = b.meta["cascade"]
     caches = gpu_caches(b)

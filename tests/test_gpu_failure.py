@@ -134,7 +134,7 @@ def test_mixed_attention_wait_timeout_frees_tensor_memory():
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     B.pa_cache_write(d, b.k_new, b.v_new, kc, vc, b.slot_mapping)
     S = b.context_lens_decode.shape[0]
-    ws = B.decode_workspace(d, S, b.max_context_len_decode(), DEV)
+    ws = B.mixed_workspace(d, S, b.max_context_len_decode(), DEV)
     dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
     pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
     qsl = b.query_start_loc

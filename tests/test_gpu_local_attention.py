@@ -11,7 +11,7 @@ import torch
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
 from pa_helpers import LSE_TOL, TOL, assert_close, gpu_caches, gpu_decode, gpu_prefill, oracle_caches, oracle_decode, \
-    oracle_prefill
+    oracle_prefill, tcgen05_takes
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -65,8 +65,8 @@ def test_decode_local_attention(kv, window, chunk, impl):
 @pytest.mark.parametrize("window,chunk", [(1, 0), (64, 0), (200, 0), (0, 48), (0, 128), (100, 256), (5000, 0)])
 @pytest.mark.parametrize("kv", [W.KV_BF16, W.KV_FP8, W.KV_F16])
 def test_prefill_local_attention(kv, window, chunk, impl):
-    if impl in (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR) and kv not in (W.KV_BF16, W.KV_F16):
-        pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
+    if not tcgen05_takes(impl, kv, 128):
+        pytest.skip("the tcgen05 prefill takes 16-bit caches, and 8-bit ones at head_dim 128 outside the pair mode")
     q_lens, ctx = [300, 37, 1, 129], [700, 37, 200, 900]
     b = W.random_prefill(800 + window + chunk, q_lens, ctx, 8, 2, 128, kv_dtype=kv, device=DEV, poison=True,
                          shared_prefix_blocks=2)

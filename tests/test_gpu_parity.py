@@ -14,7 +14,7 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
-from pa_helpers import (TOL, LSE_TOL, assert_close, desc_of, gpu_caches, gpu_decode,
+from pa_helpers import (TOL, LSE_TOL, assert_close, desc_of, tcgen05_takes, gpu_caches, gpu_decode,
                         gpu_prefill, oracle_caches, oracle_decode, oracle_prefill)
 
 pytestmark = pytest.mark.gpu
@@ -331,8 +331,8 @@ TC_IMPLS = (B.PA_PREFILL_TCGEN05, B.PA_PREFILL_TCGEN05_PAIR)
 @pytest.mark.parametrize("impl", PREFILL_IMPLS)
 @pytest.mark.parametrize("D,Hq,Hkv,kv,q_lens,ctx,shared", PREFILL_CASES)
 def test_prefill_random_shapes(D, Hq, Hkv, kv, q_lens, ctx, shared, impl):
-    if impl in TC_IMPLS and kv not in (W.KV_BF16, W.KV_F16):
-        pytest.skip("the tcgen05 prefill kernel takes bf16 and fp16 caches")
+    if not tcgen05_takes(impl, kv, D):
+        pytest.skip("the tcgen05 prefill takes 16-bit caches, and 8-bit ones at head_dim 128 outside the pair mode")
     b = W.random_prefill(200 + D + Hq + len(q_lens), q_lens, ctx, Hq, Hkv, D, kv_dtype=kv, device=DEV,
                          poison=True, shared_prefix_blocks=shared)
     out, lse = gpu_prefill(b, prefill_impl=impl)
@@ -383,7 +383,7 @@ def test_mixed_step_as_the_bench_runs_it(mode, fp16):
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     S = b.context_lens_decode.shape[0]
     maxL = b.max_context_len_decode()
-    ws = B.decode_workspace(d, S, maxL, DEV)
+    ws = B.mixed_workspace(d, S, maxL, DEV)
     dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
     dec_lse = torch.full((S, 32), float("nan"), device=DEV)
     pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
@@ -416,6 +416,41 @@ def test_mixed_step_as_the_bench_runs_it(mode, fp16):
     assert_close(pf_lse, l_ref, LSE_TOL[kv], "prefill lse")
 
 
+@pytest.mark.parametrize("fmt", [W.KV_FP8, W.KV_FP8_E5M2])
+def test_mixed_step_with_8bit_cache(fmt):
+    """Workload 5 with an 8-bit cache: the pool and the step's new tokens
+    written by the library bit-exact against the oracle's encoding, then
+    decode and the tcgen05 prefill (8-bit tiles widened to fp16) over it,
+    every row against the oracle within the FP8 tolerance."""
+    from paged_kv_attention_14_gb300.step import MixedStep
+    b = W.workload(5, device=DEV, poison=True, fp8_cache=True, fp8_format=fmt)
+    d = desc_of(b)
+    kc, vc = gpu_caches(b)  # the whole pool, through the library's cache write
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    ws = B.decode_workspace(d, S, maxL, DEV)
+    dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
+    pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
+    pf_lse = torch.full((b.q_prefill.shape[0], 32), float("nan"), device=DEV)
+    qsl = b.query_start_loc
+    ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, workspace=ws, max_context_len_decode=maxL,
+                   prefill_out=pf_out, prefill_lse=pf_lse, max_q_len=512,
+                   max_context_len_prefill=int(b.context_lens_prefill.max()), mode="streams")
+    ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode),
+       (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill))
+    torch.cuda.synchronize()
+    code, okc, ovc = oracle_caches(b)
+    okc, ovc = oracle.cache_write(code, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(), okc, ovc,
+                                  b.k_scale, b.v_scale)
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    oc = (code, okc, ovc)
+    o_ref, _ = oracle_decode(b, ocaches=oc)
+    assert_close(dec_out, o_ref, TOL[fmt], "decode out")
+    o_ref, l_ref = oracle_prefill(b, ocaches=oc)
+    assert_close(pf_out, o_ref, TOL[fmt], "prefill out")
+    assert_close(pf_lse, l_ref, LSE_TOL[fmt], "prefill lse")
+
+
 def test_graphed_step_replays_the_step_bit_for_bit():
     """step.GraphedStep (the bench's end-to-end path): the copies in, the
     single-launch step and the copies out captured as a CUDA graph; each
@@ -425,7 +460,7 @@ def test_graphed_step_replays_the_step_bit_for_bit():
     d = desc_of(b)
     S = b.context_lens_decode.shape[0]
     maxL = b.max_context_len_decode()
-    ws = B.decode_workspace(d, S, maxL, DEV)
+    ws = B.mixed_workspace(d, S, maxL, DEV)
     kc, vc = b.k_pool.clone(), b.v_pool.clone()
     dec_out = torch.empty(S, 32, 128, device=DEV)
     pf_out = torch.empty(b.q_prefill.shape[0], 32, 128, device=DEV)

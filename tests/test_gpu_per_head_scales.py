@@ -50,10 +50,11 @@ def test_decode_with_per_head_scales(kv, D, Hq, Hkv, lens, impl):
 
 
 @pytest.mark.parametrize("kv", FMTS)
-def test_prefill_with_per_head_scales(kv):
+@pytest.mark.parametrize("impl", [B.PA_PREFILL_MMA_SYNC, B.PA_PREFILL_TCGEN05])
+def test_prefill_with_per_head_scales(kv, impl):
     b = W.random_prefill(55, [5, 100, 1, 37], [5, 300, 33, 64], 8, 4, 128, kv_dtype=kv, device=DEV, poison=True,
                          shared_prefix_blocks=1, per_head_scales=True)
-    out, lse = gpu_prefill(b, prefill_impl=B.PA_PREFILL_MMA_SYNC)
+    out, lse = gpu_prefill(b, prefill_impl=impl)
     o_ref, l_ref = oracle_prefill(b)
     assert_close(out, o_ref, TOL[kv], "out")
     assert_close(lse, l_ref, LSE_TOL[kv], "lse")
