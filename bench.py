@@ -59,12 +59,16 @@ MIN_TIMED_S = 0.5
 # source files hash to what they were when it was captured.
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
-    # the decode kernel (split segments are merged inside it)
-    "decode": {"workload": 2, "bytes": 306_021_236,
-               "sha256": "ad71555c11e126bb234633e31267180038cf03a69ed60903284b3f42e16bff6d",
+    # the decode kernel (split segments are merged inside it):
+    # dram__bytes_read.sum 305,456,896 + dram__bytes_write.sum 2,784,000
+    "decode": {"workload": 2, "bytes": 308_240_896,
+               "sha256": "9ca86cdcfd97a2e26209f9ca64685d713057722e877e2743b49fc9abb16e9519",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
-    "prefill": {"workload": 5, "bytes": 46_282_802, "sha256": "e52cfcb27c5265ba09e4d627b54cddba2121615df53e0e4bf0d4031742e6bfbd",
-                "sources": ["pa_device.cuh", "pa_prefill_tc.cu"]},
+    # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
+    # dram__bytes_read.sum 46,233,344 + dram__bytes_write.sum 968,448
+    "prefill": {"workload": 5, "bytes": 47_201_792,
+                "sha256": "6b59545d9447162775888b1db86f4a699018118e12ea99f77a1efc15c8db5d2a",
+                "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
 
@@ -140,20 +144,35 @@ class ClockSampler:
         self.target = None
 
     def _target(self) -> str:
-        """The GPU as nvidia-smi names it: CUDA's UUID where nvidia-smi reports
-        the same one (some boxes hide UUIDs from nvidia-smi), else the
-        nvidia-smi index of the visible device (CUDA_VISIBLE_DEVICES maps
-        CUDA's numbering onto it)."""
+        """The GPU as nvidia-smi names it: its nvidia-smi index, found by
+        CUDA's UUID in nvidia-smi's list; where nvidia-smi hides UUIDs, the
+        only GPU it lists, else the CUDA_VISIBLE_DEVICES entry of the device.
+        nvidia-smi sometimes answers "No devices were found" while NVML is
+        busy, so the list is asked for a few times."""
+        uuid = None
         try:
             import torch
             u = str(torch.cuda.get_device_properties(self.gpu).uuid)
-            u = u if u.startswith("GPU-") else "GPU-" + u
-            r = subprocess.run(["nvidia-smi", "-i", u, "--query-gpu=index", "--format=csv,noheader"],
-                               capture_output=True, text=True, timeout=20)
-            if r.returncode == 0 and r.stdout.strip().isdigit():
-                return u
+            uuid = u if u.startswith("GPU-") else "GPU-" + u
         except Exception:
             pass
+        listed = []
+        for _ in range(10):
+            try:
+                r = subprocess.run(["nvidia-smi", "--query-gpu=index,uuid", "--format=csv,noheader"],
+                                   capture_output=True, text=True, timeout=20)
+            except (OSError, subprocess.TimeoutExpired):
+                break
+            listed = [[x.strip() for x in line.split(",")] for line in r.stdout.splitlines() if "," in line]
+            listed = [x for x in listed if x[0].isdigit()]
+            if r.returncode == 0 and listed:
+                break
+            time.sleep(0.2)
+        for idx, u in listed:
+            if uuid is not None and u == uuid:
+                return idx
+        if len(listed) == 1:
+            return listed[0][0]
         vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
         ids = [x.strip() for x in vis.split(",") if x.strip()]
         if len(ids) > self.gpu and ids[self.gpu].isdigit():
@@ -176,6 +195,8 @@ class ClockSampler:
             self.proc.wait()
             if self.stopping:
                 return
+            if self.lines and "No devices were found" in self.lines[-1][1]:
+                self.target = None  # named again at the next start
             time.sleep(self.PERIOD_MS / 1000)
             try:
                 self.proc = self._spawn()
@@ -415,6 +436,8 @@ def run_ours(args):
     R = max(1, min(2000, int(math.ceil(MIN_TIMED_S / (K * est_s)))))
     K2 = max(10, K // 2)
     R2 = max(1, min(2000, int(math.ceil(MIN_TIMED_S / 2 / (K2 * est_s)))))
+    if args.repeats:  # a fixed count (profiling runs, where launches are slow)
+        R = R2 = args.repeats
     # the raw nvidia-smi samples go to the file PA_BENCH_CLOCKS_CSV names, if any
     sampler = ClockSampler(local, os.environ.get("PA_BENCH_CLOCKS_CSV") or None)
     sampler.start()
@@ -752,6 +775,8 @@ def main():
     ap.add_argument("--sliding-window", type=int, default=0, help="sliding-window attention of W keys (0: off)")
     ap.add_argument("--attention-chunk", type=int, default=0, help="chunked-local attention over chunks of C (0: off)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--repeats", type=int, default=0,
+                    help="repeats of the timed K steps (0: as many as fill about half a second)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.fp16 and args.workload == 4:
