@@ -83,6 +83,11 @@ constexpr float kRescaleThreshold = 8.f;  // log2 units
 struct Args {
   CUtensorMap kmap;  // cache as [rows = blocks * kv heads * 16][D], box {64, 16}
   CUtensorMap vmap;
+  // queries as [tokens][q heads][D] of 16-bit values, box {64, g, 128 / g}:
+  // one box is one 128-byte column half of a Q tile (its 128 / g queries
+  // times the g heads of one kv head).  Used when qtma is set.
+  CUtensorMap qmap;
+  int qtma;          // the full Q tiles come by TMA (16-bit caches, g divides 128)
   float *out;
   float *lse;
   const uint16_t *q;
@@ -187,7 +192,7 @@ struct Cfg {
 // barriers: K_FULL[NSK], K_EMPTY[NSK], V_FULL[NSV], V_EMPTY[NSV],
 // S_FULL[tile], P_FULL[tile], V_READY[NSV] (fp16 P: the V tile is in fp16,
 // rows outside the needed keys zeroed), K_READY[NSK] (8-bit caches: the K
-// tile widened to fp16)
+// tile widened to fp16), Q_FULL (the Q tiles that come by TMA)
 enum Bar {
   K_FULL = 0,
   K_EMPTY = K_FULL + NSK,
@@ -197,7 +202,8 @@ enum Bar {
   P_FULL = S_FULL + NQT,
   V_READY = P_FULL + NQT,
   K_READY = V_READY + NSV,  // 8-bit caches: the K tile widened to fp16
-  NBAR = K_READY + NSK
+  Q_FULL = K_READY + NSK,   // the Q tiles copied by TMA have landed
+  NBAR = Q_FULL + 1
 };
 static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
@@ -288,6 +294,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     for (int i = 0; i < NSV; ++i) mbar_init(&bar[V_READY + i], 2);
     for (int i = 0; i < NSK; ++i) mbar_init(&bar[K_READY + i], 2);
+    mbar_init(&bar[Q_FULL], 1);
     *s_abort = 0;
     *s_last_k = -1;
     *s_last_v = -1;
@@ -295,14 +302,55 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   }
 
   // ---- Q tiles: row R = query * g + head (tile R / 128, lane R % 128),
-  // [tile][half][row][128 B], 128-B swizzle.  With an 8-bit cache the bf16
-  // queries are staged as fp16 (round to nearest; a finite |q| >= 2^16 does
-  // not fit and is reported).
-  {
+  // [tile][half][row][128 B], 128-B swizzle.  A tile whose 128 / g queries
+  // all belong to the chunk comes by TMA (16-bit caches, g dividing 128):
+  // the box's rows are its queries times the g heads of the kv head, in
+  // the order of R.  The producer issues those copies at once and goes on
+  // to the K/V copies; the MMA thread waits for them (Q_FULL).  Every other
+  // tile is staged by the threads (rows past the chunk zeroed).  With an
+  // 8-bit cache the bf16 queries are staged as fp16 (round to nearest; a
+  // finite |q| >= 2^16 does not fit and is reported).
+  uint32_t qtma_tiles = 0;
+  if (!C::KV8 && a.qtma) {
+#pragma unroll
+    for (int t = 0; t < NQT; ++t)
+      if ((t + 1) * (MT / g) <= nq) qtma_tiles |= 1u << t;
+  }
+  const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
+  // producer: lane -> (block of the tile, half); the same lanes copy K and
+  // V.  An 8-bit block is one box of 16 rows of D bytes, landing in the
+  // second half of the slot (widened in place by warps 2-3)
+  constexpr int BOXES = C::KV8 ? 1 : C::HALVES;
+  const int bi = lane / BOXES;
+  const int hh = lane % BOXES;
+  const bool issuer = lane < BPT * BOXES;
+  auto block_id = [&](int lb) {
+    const int v = __ldg(table + lb);
+    return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
+  };
+  int phys_next = 0;
+  if (qtma_tiles != 0) __syncthreads();  // the barriers are set up
+  if (warp == kProducerWarp) {
+    // the first KV tile's block ids load while Q is set up
+    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = block_id(j0 * BPT + bi);
+    if (qtma_tiles != 0 && lane == 0 && !a.stall) {
+      const uint64_t pol = l2_evict_first_policy();
+      mbar_arrive_expect_tx(&bar[Q_FULL], __popc(qtma_tiles) * C::QB);
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+        if (qtma_tiles >> t & 1)
+#pragma unroll
+          for (int q2 = 0; q2 < C::HALVES; ++q2)
+            tma_load_3d(smem + C::OFF_Q + t * C::QB + q2 * C::QHALF, &a.qmap, q2 * 64, kvh * g,
+                        qs + qt0 + t * (MT / g), &bar[Q_FULL], pol);
+    }
+  }
+  if (qtma_tiles != (1u << NQT) - 1) {
     constexpr int CHUNKS = D / 8;  // 16-byte chunks per row
     float qmax = 0.f;
     for (int i = tid; i < MROWS * CHUNKS; i += NTHREADS) {
       const int R = i / CHUNKS;
+      if (qtma_tiles >> (R / MT) & 1) continue;
       const int ch = i - R * CHUNKS;
       const int qi = R / g;
       const bool ok = R < rows_used && qi < nq;
@@ -341,21 +389,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------ TMA producer
-    const int32_t *table = a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq;
     const uint64_t pol = l2_evict_first_policy();
-    // lane -> (block of the tile, half); the same lanes copy K and V.  An
-    // 8-bit block is one box of 16 rows of D bytes, landing in the second
-    // half of the slot (widened in place by warps 2-3)
-    constexpr int BOXES = C::KV8 ? 1 : C::HALVES;
-    const int bi = lane / BOXES;
-    const int hh = lane % BOXES;
-    const bool issuer = lane < BPT * BOXES;
-    auto block_id = [&](int lb) {
-      const int v = __ldg(table + lb);
-      return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
-    };
-    int phys_next = 0;
-    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = block_id(j0 * BPT + bi);
     PF_TRACE(const long long tp0 = clock64(); long long tp_wait = 0;)
     bool ok = true;
     // test hook: issue nothing and signal nothing, so the other warps' waits
@@ -447,13 +481,17 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       // converted it (fp16 P)
       constexpr int VB = C::P16 ? V_READY : V_FULL;
       constexpr int KB = C::KV8 ? K_READY : K_FULL;  // 8-bit: once widened to fp16
-      if (!mbar_wait(&bar[KB], 0, a.wait_ns) || !mbar_wait(&bar[VB], 0, a.wait_ns)) ok = false;
+      // the first QKs need Q and K only; V of the first tile (and its
+      // conversion) is waited for behind them
+      if ((qtma_tiles != 0 && !mbar_wait(&bar[Q_FULL], 0, a.wait_ns)) || !mbar_wait(&bar[KB], 0, a.wait_ns))
+        ok = false;
       if (ok) {
         tc_fence_after_sync();
         for (int t = 0; t < NQT; ++t) {
           qk(t, 0);
           umma_commit(&bar[S_FULL + t]);
         }
+        if (!mbar_wait(&bar[VB], 0, a.wait_ns)) ok = false;
       }
       for (int jj = 0; jj < n_iter && ok; ++jj) {
         const bool next = jj + 1 < n_iter;
@@ -841,6 +879,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   if (*s_abort) {
     if (tid == 0) report_error(a.err, nullptr, kErrWaitTimeout);
     if (warp == kProducerWarp && lane == 0) {
+      if (qtma_tiles != 0 && !a.stall) mbar_wait(&bar[Q_FULL], 0, a.wait_ns);
       for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t)
         mbar_wait(&bar[K_FULL + t % NSK], (t / NSK) & 1, a.wait_ns);
       for (int t = max(0, *s_last_v - NSV + 1); t <= *s_last_v; ++t)
@@ -920,6 +959,43 @@ inline bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
   return true;
 }
 
+// The queries' tensor map: [tokens][q heads][D] 16-bit values, box {64
+// columns, g heads, 128 / g tokens}, 128-byte swizzle.  The token extent is
+// not known on the host (the chunk offsets live on the device); it is set
+// to 2^30, and the kernel only asks for boxes of tokens inside a chunk.
+// False if the map cannot be made (q not 16-byte aligned, g not dividing
+// 128): the threads then stage every Q tile.
+template <int D>
+inline bool make_qmap(CUtensorMap *map, const void *q, int num_q_heads, int g) {
+  if ((reinterpret_cast<uintptr_t>(q) & 15) != 0 || g <= 0 || MT % g != 0) return false;
+  using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+  static EncodeTiledFn enc = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) != cudaSuccess ||
+        r != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  if (!enc) return false;
+  thread_local MapCache<> cache;
+  const MapKey key = map_key(q, num_q_heads, D, g, -1);
+  if (cache.find(key, map)) return true;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_q_heads), cuuint64_t(1) << 30};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(num_q_heads) * D * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(MT / g)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache.put(key, *map);
+  return true;
+}
+
 // The kernel's arguments for a call (everything but the grid); false if a
 // tensor map of the caches cannot be made.
 template <int D>
@@ -941,6 +1017,7 @@ inline bool make_args(Args *a, const pa_kv_desc &d, float *out, float *lse, cons
   a->g = d.num_q_heads / d.num_kv_heads;
   a->qt = MROWS / a->g;  // queries per CTA
   const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
+  a->qtma = !kv8 && make_qmap<D>(&a->qmap, q, d.num_q_heads, a->g) ? 1 : 0;
   a->qscale = scale * ((kv8 && d.k_scale != 0.f) ? d.k_scale : 1.f) * kLog2e;
   a->qscale0 = scale * kLog2e;
   a->vscale = (kv8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
