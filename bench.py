@@ -65,9 +65,9 @@ NCU_TRAFFIC = {
                "sha256": "9ca86cdcfd97a2e26209f9ca64685d713057722e877e2743b49fc9abb16e9519",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 46,233,344 + dram__bytes_write.sum 968,448
-    "prefill": {"workload": 5, "bytes": 47_201_792,
-                "sha256": "6b59545d9447162775888b1db86f4a699018118e12ea99f77a1efc15c8db5d2a",
+    # dram__bytes_read.sum 46,227,712 + dram__bytes_write.sum 878,848
+    "prefill": {"workload": 5, "bytes": 47_106_560,
+                "sha256": "f7f885488792c7f097ee1b951b34072e29b8293f38253ac5985618b810455f50",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
