@@ -449,32 +449,58 @@ def run_ours(args):
     # event between two kernels would cut the programmatic-dependent overlap
     # of the decode launch with the cache write); with an L2 flush between
     # steps, events around each step leave the flush out
+    # Without a flush (inputs larger than L2) one event pair brackets the K
+    # back-to-back steps of a repeat; with one, events bracket each step so
+    # that the flush stays outside the timed region.  (An event pair alone
+    # measures a few microseconds on these boxes: per-step events would add
+    # that to every step.)
+    def ev_pair():
+        return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
     rep_ms = []
     for _ in range(R):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for i in range(K):
-            if flush is not None:
+        if flush is None:
+            ev = [ev_pair()]
+            ev[0][0].record()
+            for i in range(K):
+                step()
+            ev[0][1].record()
+        else:
+            ev = [ev_pair() for _ in range(K)]
+            for i in range(K):
                 flush()
-            ev[i][0].record()
-            step()
-            ev[i][1].record()
+                ev[i][0].record()
+                step()
+                ev[i][1].record()
         rep_ms.append(ev)
-    # timed region 2: the kernels of each entry point alone, events around
-    # each call (decode; prefill)
+    # timed region 2: the kernels of each entry point alone (decode; prefill),
+    # K2 back-to-back calls under one event pair, or events around each call
+    # after a flush
     rep_d, rep_p = [], []
     for _ in range(R2):
-        ev_d = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
-        ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
-        for i in range(K2):
-            if flush is not None:
-                flush()
-            ev_d[i][0].record()
-            decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
-            ev_d[i][1].record()
+        if flush is None:
+            ev_d, ev_p = [ev_pair()], [ev_pair()]
+            ev_d[0][0].record()
+            for i in range(K2):
+                decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
+            ev_d[0][1].record()
             if mixed:
-                ev_p[i][0].record()
-                prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
-                ev_p[i][1].record()
+                ev_p[0][0].record()
+                for i in range(K2):
+                    prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
+                ev_p[0][1].record()
+        else:
+            ev_d = [ev_pair() for _ in range(K2)]
+            ev_p = [ev_pair() for _ in range(K2)]
+            for i in range(K2):
+                flush()
+                ev_d[i][0].record()
+                decode(b.q_decode, b.block_tables_decode, b.context_lens_decode)
+                ev_d[i][1].record()
+                if mixed:
+                    ev_p[i][0].record()
+                    prefill(b.q_prefill, b.query_start_loc, b.block_tables_prefill, b.context_lens_prefill)
+                    ev_p[i][1].record()
         rep_d.append(ev_d)
         rep_p.append(ev_p)
     torch.cuda.synchronize()
@@ -554,6 +580,8 @@ def run_ours(args):
         peak, tc_peak, peak_kind = _peaks()
         gbs = _job_throughput(ws, kv_bytes, step_ms * 1e-3) / 1e9
         dec_gbs = kv_bytes / (dec_ms * 1e-3) / 1e9
+        alone_how = ("timed alone: back-to-back calls under one event pair" if flush is None
+                     else "timed alone: events around each call after an L2 flush")
         line = {
             "metric": METRIC,
             "value": round(gbs, 1),
@@ -576,7 +604,7 @@ def run_ours(args):
                               f"inputs larger than L2 ({kv_bytes >> 20} MiB KV vs {l2_bytes >> 20} MiB L2), no flush"),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU", **_local_config(args)},
             "roofline": {"bound": "hbm",
-                         "kernel": "pa_decode (one decode kernel launch), timed alone per call",
+                         "kernel": "pa_decode (one decode kernel launch), " + alone_how,
                          "achieved": round(dec_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(dec_gbs / peak, 4), "kernel_us": round(dec_ms * 1e3, 2),
                          "traffic": _traffic("decode", args.workload, local)},
@@ -589,7 +617,10 @@ def run_ours(args):
             "gpu_launches": launches_per_step * K * R + (2 if mixed else 1) * K2 * R2,
             "timed_repeats": {"steps": R, "kernels_alone": R2,
                               "note": f"each repeat times exactly {K} steps ({K2} calls of each entry point alone); "
-                                      "ms_per_step is the median repeat"},
+                                      "ms_per_step is the median repeat",
+                              "events": ("one event pair around the repeat's back-to-back steps (calls)"
+                                         if flush is None else "an event pair around each step (call), "
+                                         "after its L2 flush")},
             "clocks": clocks,
         }
         if clocks.get("sm_mhz"):
@@ -602,7 +633,7 @@ def run_ours(args):
                 # the prefill dominates the step: the roofline is its tensor-core bound
                 # (algorithmic flops; the bf16 hi/lo split of P adds half again to PV)
                 line["roofline_decode"] = line["roofline"]
-                line["roofline"] = {"bound": "tensor", "kernel": "pa_prefill_chunk, timed alone per call",
+                line["roofline"] = {"bound": "tensor", "kernel": "pa_prefill_chunk, " + alone_how,
                                     "achieved": round(pf_tf, 1), "peak": tc_peak,
                                     "peak_kind": f"{peak_kind} bf16 dense (burst)", "unit": "TFLOP/s",
                                     "frac": round(pf_tf / tc_peak, 4), "kernel_us": round(pf_ms * 1e3, 2),
