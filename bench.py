@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
     # dram__bytes_read.sum 46,227,712 + dram__bytes_write.sum 878,848
     "prefill": {"workload": 5, "bytes": 47_106_560,
-                "sha256": "f7f885488792c7f097ee1b951b34072e29b8293f38253ac5985618b810455f50",
+                "sha256": "235913a9eea83da27e90ef2fba1886e743e3e240935295ed49416b4941fcae8a",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 

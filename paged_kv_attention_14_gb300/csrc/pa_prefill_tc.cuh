@@ -1,6 +1,6 @@
 // pa_prefill_tc.cuh -- causal chunked-prefill attention on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory), bf16 or fp16
-// KV (the MMAs, and the P pair below, take the cache's 16-bit type).
+// tensor cores (tcgen05.mma, accumulators in tensor memory): bf16, fp16 or
+// 8-bit (E4M3, E5M2) KV.
 //
 // What it computes is the same as pa_prefill.cu: sequence s brings q_len
 // new queries (a "chunked prefill" chunk, vllm.cpp implementation notes,
@@ -14,36 +14,42 @@
 //    one sequence times the g query heads of one kv head, so every K/V tile
 //    feeds the whole GQA group.  The rows form two 128-row Q tiles (A, B)
 //    that ping-pong: while one tile's softmax runs, the tensor cores work on
-//    the other tile.  Q is staged once in shared memory; K/V are walked in
+//    the other tile.  A Q tile whose queries all belong to the chunk comes
+//    by TMA (16-bit caches, g dividing 128), issued together with the first
+//    K/V copies; other tiles are staged by the threads.  K/V are walked in
 //    128-key tiles gathered block by block through the block table by TMA
 //    (128-byte-swizzled boxes of 16 rows) into a 3-stage K ring and a
 //    2-stage V ring shared by both Q tiles.  A K slot is released as soon
 //    as the QKs that read it complete, a V slot after its PVs.
 //  * Warp 0 (one thread) issues the MMAs.  S_t = Q_t K^T (M 128, N 128 keys,
 //    K 16 x head_dim/16; both operands in shared memory) lands in tile t's
-//    128 TMEM columns.  The softmax overwrites those columns with P_t as a
-//    hi + lo pair of the cache's 16-bit type (each 32-key chunk's pair in
-//    that chunk's columns; P = hi + lo to ~2^-17 relative with bf16, so the
-//    tensor core product keeps near-fp32 accuracy), and O_t += P_t V (M 128,
-//    N head_dim, K 16 x 8, twice) takes P_t straight from tensor memory
-//    as the A operand and V MN-major from shared memory.  Order per KV tile
-//    j: PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1); one commit after each QK
-//    tells tile t's softmax that its next scores are ready AND that its
-//    previous PV finished (so O_t may be rescaled and S_t overwritten).
-//    M 128 MMAs with N <= 128 cost the same per instruction (measured on
-//    GB300: ~84 cycles with both operands in shared memory, ~78 with A in
-//    tensor memory, 128 at N 256), hence the 128-key tile.
-//  * Warps 4-7 (tile A) and 8-11 (tile B), one thread per row, do the online
-//    softmax in one pass over the row's 128 scores in TMEM, 32 at a time
-//    (the next 32 loading meanwhile): causal mask, row max (a tree of
-//    three-input maxima), exp2 of the scaled scores, row sum and the P
-//    pair, with packed fp32x2 arithmetic.  The running max is only raised
-//    (and O and the chunks of P already written rescaled in TMEM) when it
-//    grows by more than 2^8, so that path is rare.
-//  * Keys past the chunk's last position are masked; V rows past it are
-//    zeroed in shared memory before the last PV (0 * NaN would not vanish).
+//    128 TMEM columns.  The softmax overwrites those columns with P_t: one
+//    fp16 value per key (kPvF16, the default), or a hi + lo pair of the
+//    cache's 16-bit type in pair mode (P = hi + lo to ~2^-17 relative with
+//    bf16).  O_t += P_t V (M 128, N head_dim, K 16 x 8, twice in pair mode)
+//    takes P_t straight from tensor memory as the A operand and V MN-major
+//    from shared memory.  Order per KV tile j: PV_A(j), QK_A(j+1), PV_B(j),
+//    QK_B(j+1); one commit after each QK tells tile t's softmax that its
+//    next scores are ready AND that its previous PV finished (so O_t may be
+//    rescaled and S_t overwritten).  M 128 MMAs with N <= 128 cost the same
+//    per instruction (measured on GB300: ~84 cycles with both operands in
+//    shared memory, ~78 with A in tensor memory, 128 at N 256), hence the
+//    128-key tile.
+//  * With fp16 P, warps 2-3 prepare each landed V tile: a bf16 tile is
+//    converted to fp16 in place (both MMA operands are then fp16), and rows
+//    outside the keys the CTA needs are zeroed (0 * NaN would not vanish).
+//    8-bit K and V tiles are widened to fp16 in place, and the queries are
+//    then staged in fp16.
+//  * Warps 4-11 do the online softmax, two threads per row: warps 4-7 take
+//    keys 0-63 and warps 8-11 keys 64-127 of every tile, for tile A and then
+//    tile B.  Per tile: the scores from TMEM, causal and local masks, the
+//    half-row max (a tree of three-input maxima) exchanged with the partner
+//    thread through shared memory, exp2 of the scaled scores, the row sum
+//    and P, with packed fp32x2 arithmetic.  The running max is only raised
+//    (and O rescaled in TMEM) when it grows by more than 2^8, so that path
+//    is rare.
 //  * Warp 1 issues the TMA copies and prefetches block-table entries one
-//    tile ahead.  Warps 2-3 only take part in staging Q.
+//    tile ahead.
 //  * Every wait is bounded; on a timeout the kernel records an error bit,
 //    lets its own MMAs and copies drain and frees its TMEM before returning.
 #pragma once
@@ -64,14 +70,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int KT = 128;        // keys per KV tile (N of the QK MMA)
 constexpr int BPT = KT / 16;   // cache blocks per KV tile
 constexpr int MT = 128;        // rows of one Q tile (one TMEM lane per row)
-constexpr int NQT = 2;         // Q tiles per CTA (ping-pong between two softmax warpgroups)
+constexpr int NQT = 2;         // Q tiles per CTA (their softmaxes alternate with their MMAs)
 constexpr int MROWS = MT * NQT;
 // Warp roles.  The MMA issuer and the TMA producer take the lowest warp
 // numbers: they must be scheduled promptly on sub-partitions shared with
 // busy softmax warps, and the warp schedulers favour older warps.  Softmax
 // warp w may only touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31, so each
-// Q tile's warpgroup starts at a multiple of four.
-constexpr int NTHREADS = 384;  // warp 0 MMA issuer, 1 TMA producer, 2-3 idle, 4-7 softmax A, 8-11 softmax B
+// half of the keys' warpgroup starts at a multiple of four.
+constexpr int NTHREADS = 384;  // warp 0 MMA issuer, 1 TMA producer, 2-3 K / V preparation, 4-11 softmax
 constexpr int kMmaWarp = 0;
 constexpr int kProducerWarp = 1;
 constexpr int kSoftmaxWarp0 = 4;
