@@ -676,15 +676,16 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     // so two softmax warps per SM sub-partition share each tile.  A thread
     // holds row r = 32 (warp % 4) + lane (its TMEM lane) and its half h of
     // the keys.  The two threads of a row exchange their maxima through
-    // shared memory (named barrier 1 over the 256 softmax threads), so the
-    // tile's row maximum is known before any P is written: a rise of the
-    // running maximum rescales O (each thread its half of the columns) and
-    // never P.
+    // shared memory, so the tile's row maximum is known before any P is
+    // written: a rise of the running maximum rescales O (each thread its
+    // half of the columns) and never P.  Only partner warps w and w + 4 (the
+    // same rows) exchange anything, so each pair has its own named barrier
+    // (3 + w % 4, 64 threads) and never waits for the other pairs.
     const int h = (warp - kSoftmaxWarp0) >> 2;  // half of the keys
     const int r = ((warp & 3) << 5) | lane;     // row of a Q tile = TMEM lane
     const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     float *xch = reinterpret_cast<float *>(smem + C::OFF_X);  // [2][MT] maxima / sums of the halves
-    constexpr int kSoftmaxThreads = 256;
+    const int pair_bar = 3 + (warp & 3);  // named barrier of this partner pair (64 threads)
     // score scale and output scale of this kv head (its own k / v scale
     // where an 8-bit cache has per-head scales)
     const float qscale = a.k_scales ? a.qscale0 * __ldg(a.k_scales + kvh) : a.qscale;
@@ -729,10 +730,10 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
           }
           fence_proxy_async_smem();
         }
-        // all softmax threads go on, or all stop (a bounded wait ran out):
-        // the named barriers below stay matched.  This barrier also tells a
+        // both warps of the pair go on, or both stop (a bounded wait ran
+        // out): the pair's named barriers below stay matched.  This barrier also tells a
         // thread that its partner has read the previous exchange.
-        if (!named_bar_and(1, kSoftmaxThreads, got)) {
+        if (!named_bar_and(pair_bar, 64, got)) {
           ok = false;
           break;
         }
@@ -766,7 +767,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
         }
         // the row's maximum over both halves
         xch[h * MT + r] = mx;
-        named_bar_sync(1, kSoftmaxThreads);
+        named_bar_sync(pair_bar, 64);
         mx = fmaxf(mx, xch[(h ^ 1) * MT + r]) * qscale;
         PF_TRACE(tq[4] += clock64() - tc; tk = clock64();)
         const float m_new = fmaxf(m_ref[t], mx);
@@ -837,14 +838,14 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
              if (tid == kSoftmaxWarp0 * 32 && slot < 4096) { for (int i = 0; i < 7; ++i) g_pf_trace[slot][i] = tq[i]; g_pf_trace[slot][7] = clock64() - ts0; })
-    // the row sums of both halves (every softmax thread takes part, even
-    // after a timeout, so that the named barriers stay matched)
+    // the row sums of both halves (both warps of a pair take part, even
+    // after a timeout, so that the pair's named barriers stay matched)
     float lt[NQT];
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
-      named_bar_sync(1, kSoftmaxThreads);
+      named_bar_sync(pair_bar, 64);
       xch[h * MT + r] = l[t];
-      named_bar_sync(1, kSoftmaxThreads);
+      named_bar_sync(pair_bar, 64);
       lt[t] = l[t] + xch[(h ^ 1) * MT + r];
     }
 #pragma unroll
