@@ -65,9 +65,9 @@ NCU_TRAFFIC = {
                "sha256": "9ca86cdcfd97a2e26209f9ca64685d713057722e877e2743b49fc9abb16e9519",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 46,227,712 + dram__bytes_write.sum 878,848
-    "prefill": {"workload": 5, "bytes": 47_106_560,
-                "sha256": "235913a9eea83da27e90ef2fba1886e743e3e240935295ed49416b4941fcae8a",
+    # dram__bytes_read.sum 46,226,432 + dram__bytes_write.sum 948,736
+    "prefill": {"workload": 5, "bytes": 47_175_168,
+                "sha256": "7c150b3b1c081a16f4bfc18ea93927179d385208f0a8bbe57464f03a0ca9cfa4",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
