@@ -204,6 +204,25 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int x, 
       : "memory");
 }
 
+// One 3-D tile from shared memory to a tensor map (TMA store), in the
+// thread's current bulk group.  The source is generic-proxy writes: fence
+// them first (fence_proxy_async_smem) and make them visible to this thread.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Closes the thread's current bulk group of TMA stores.
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every bulk group of the thread has finished reading its
+// shared-memory source (the bytes may then be overwritten).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // ----------------------------------------------------------- 16-byte cp.async
 
 // Copies 16 bytes, or zero-fills them when `valid` is false (src-size 0).

@@ -94,6 +94,11 @@ struct Args {
   // times the g heads of one kv head).  Used when qtma is set.
   CUtensorMap qmap;
   int qtma;          // the full Q tiles come by TMA (16-bit caches, g divides 128)
+  // the output as [tokens][q heads][D] fp32, box {32, g, 128 / g}: one box
+  // is 32 columns of an output tile, in the order of its rows.  Used when
+  // otma is set (chunk mode, g divides 128).
+  CUtensorMap omap;
+  int otma;
   float *out;
   float *lse;
   const uint16_t *q;
@@ -841,6 +846,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     // the row sums of both halves (both warps of a pair take part, even
     // after a timeout, so that the pair's named barriers stay matched)
     float lt[NQT];
+    bool stored = false;  // TMA stores of output tiles issued by this thread
 #pragma unroll
     for (int t = 0; t < NQT; ++t) {
       named_bar_sync(pair_bar, 64);
@@ -860,21 +866,51 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       const float inv = lt[t] > 0.f ? vscale / lt[t] : 0.f;
       const int64_t orow_i =
           (static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g)) * a.out_slots + split;
-      float *orow = rv ? a.out + orow_i * D : nullptr;
-      // this half's columns of the output row
+      if (a.otma && (t + 1) * (MT / g) <= nq) {
+        // a full tile: this half's columns go through shared memory (the K
+        // ring and beyond, free once the tile's last products completed:
+        // tile 0's boxes stay inside the K ring, whose last reader, the
+        // final QK, precedes tile 0's final commit) as 128-byte-swizzled
+        // boxes of 32 columns, then out by TMA stores
+        uint8_t *stage = smem + C::OFF_K + t * (D / 32) * 16384;
 #pragma unroll 1
-      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
-        float o[32];
-        tmem_ld32(trow + o_col + c0, o);
-        if (rv) {
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+          float o[32];
+          tmem_ld32(trow + o_col + c0, o);
+          uint8_t *rowp = stage + (c0 / 32) * 16384 + r * 128;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4 *>(orow + c0 + i) =
-                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4 *>(rowp + ((k ^ (r & 7)) << 4)) =
+                make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv, o[4 * k + 3] * inv);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(7 + h, 128);  // the half's four warps wrote their rows
+        if ((warp & 3) == 0 && lane == 0) {
+          for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32)
+            tma_store_3d(&a.omap, stage + (c0 / 32) * 16384, c0, kvh * g, qs + qt0 + t * (MT / g));
+          bulk_commit_group();
+          stored = true;
+        }
+      } else {
+        float *orow = rv ? a.out + orow_i * D : nullptr;
+        // this half's columns of the output row
+#pragma unroll 1
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+          float o[32];
+          tmem_ld32(trow + o_col + c0, o);
+          if (rv) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4 *>(orow + c0 + i) =
+                  make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+          }
         }
       }
       if (rv && h == 0 && a.lse) a.lse[orow_i] = (m_ref[t] + log2f(lt[t])) * kLn2;
     }
+    // the stores' shared-memory sources are read before the CTA (or the next
+    // tile of a persistent launch) reuses the bytes
+    if (stored) bulk_wait_group_read0();
     if (!ok && lane == 0) *s_abort = 1;
   }
 
@@ -1003,6 +1039,41 @@ inline bool make_qmap(CUtensorMap *map, const void *q, int num_q_heads, int g) {
   return true;
 }
 
+// The output's tensor map: [tokens][q heads][D] fp32, box {32 columns, g
+// heads, 128 / g tokens}, 128-byte swizzle (the token extent as for q).
+// False if it cannot be made (out not 16-byte aligned, g not dividing 128):
+// the threads then store every output row themselves.
+template <int D>
+inline bool make_omap(CUtensorMap *map, const float *out, int num_q_heads, int g) {
+  if ((reinterpret_cast<uintptr_t>(out) & 15) != 0 || g <= 0 || MT % g != 0) return false;
+  using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+  static EncodeTiledFn enc = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) != cudaSuccess ||
+        r != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  if (!enc) return false;
+  thread_local MapCache<> cache;
+  const MapKey key = map_key(out, num_q_heads, D, g, -2);
+  if (cache.find(key, map)) return true;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_q_heads), cuuint64_t(1) << 30};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(num_q_heads) * D * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(MT / g)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(out), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache.put(key, *map);
+  return true;
+}
+
 // The kernel's arguments for a call (everything but the grid); false if a
 // tensor map of the caches cannot be made.
 template <int D>
@@ -1025,6 +1096,7 @@ inline bool make_args(Args *a, const pa_kv_desc &d, float *out, float *lse, cons
   a->qt = MROWS / a->g;  // queries per CTA
   const bool kv8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
   a->qtma = !kv8 && make_qmap<D>(&a->qmap, q, d.num_q_heads, a->g) ? 1 : 0;
+  a->otma = !prefix_mode && make_omap<D>(&a->omap, out, d.num_q_heads, a->g) ? 1 : 0;
   a->qscale = scale * ((kv8 && d.k_scale != 0.f) ? d.k_scale : 1.f) * kLog2e;
   a->qscale0 = scale * kLog2e;
   a->vscale = (kv8 && d.v_scale != 0.f) ? d.v_scale : 1.f;
