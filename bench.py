@@ -60,14 +60,14 @@ MIN_TIMED_S = 0.5
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
     # the decode kernel (split segments are merged inside it):
-    # dram__bytes_read.sum 305,456,896 + dram__bytes_write.sum 2,784,000
-    "decode": {"workload": 2, "bytes": 308_240_896,
-               "sha256": "9ca86cdcfd97a2e26209f9ca64685d713057722e877e2743b49fc9abb16e9519",
+    # dram__bytes_read.sum 305,458,176 + dram__bytes_write.sum 3,253,760
+    "decode": {"workload": 2, "bytes": 308_711_936,
+               "sha256": "9dab5f410c2821164ca2057a06aaf1a2a5cf2ec7d48f8e15b5a73c2a18088b18",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 46,226,432 + dram__bytes_write.sum 948,736
-    "prefill": {"workload": 5, "bytes": 47_175_168,
-                "sha256": "7c150b3b1c081a16f4bfc18ea93927179d385208f0a8bbe57464f03a0ca9cfa4",
+    # dram__bytes_read.sum 46,217,472 + dram__bytes_write.sum 1,360,640
+    "prefill": {"workload": 5, "bytes": 47_578_112,
+                "sha256": "146b1841c98fa573cd40dcdd038a9a19f805b4ff0604973e767533771201425b",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
