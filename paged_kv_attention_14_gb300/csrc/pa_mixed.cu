@@ -161,8 +161,9 @@ extern "C" PA_API int pa_debug_mixed_trace_clear() {
 // per SM.  A decode partition alone on its SM streams far below its share
 // of the HBM bandwidth (about 34 GB/s on GB300, workload 5), so finer
 // partitions were tried to spread the decode's tail over more SMs: two per
-// SM took 18 us each instead of 28 us, but the per-partition set-up grew
-// the total and the step got slower (146 against 140 us); one it is.
+// SM took 18 us each instead of 28 us, but the per-partition set-up and the
+// extra merges grew the total and the step got slower (141 against 133 us
+// on workload 5's shapes); one it is.
 constexpr int kMixedDecodeSplit = 1;
 
 DecodePlan mixed_plan(const pa_kv_desc &d, int32_t num_dec_seqs, const DecodePlan &plan) {
