@@ -503,6 +503,32 @@ def test_tcgen05_and_mma_sync_prefill_agree_on_mixed_step():
     assert (l1 - l2).abs().max().item() < 2e-3
 
 
+def test_tcgen05_prefill_with_q_and_out_at_16_byte_offsets():
+    """q and out may start at any 16-byte boundary: the TMA maps of the Q
+    tiles and of the output tiles then start off a 128-byte line.  The
+    results equal those of aligned buffers bit for bit."""
+    b = W.workload(5, device=DEV, poison=True)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(desc_of(b), b.k_new, b.v_new, kc, vc, b.slot_mapping)
+    o_ref, l_ref = gpu_prefill(b, caches=(kc, vc), prefill_impl=B.PA_PREFILL_TCGEN05)
+    Tq, Hq, D = b.q_prefill.shape
+    qbuf = torch.empty(b.q_prefill.numel() + 8, dtype=b.q_prefill.dtype, device=DEV)
+    q_off = qbuf[8:].view(Tq, Hq, D)  # 16 bytes in
+    q_off.copy_(b.q_prefill)
+    obuf = torch.full((Tq * Hq * D + 4,), float("nan"), device=DEV)
+    out_off = obuf[4:].view(Tq, Hq, D)  # 16 bytes in
+    lbuf = torch.full((Tq * Hq + 1,), float("nan"), device=DEV)
+    lse_off = lbuf[1:].view(Tq, Hq)  # 4 bytes in
+    qsl = b.query_start_loc
+    B.pa_prefill_chunk(desc_of(b, prefill_impl=B.PA_PREFILL_TCGEN05), out_off, q_off, qsl, kc, vc,
+                       b.block_tables_prefill, b.context_lens_prefill, int((qsl[1:] - qsl[:-1]).max()),
+                       int(b.context_lens_prefill.max()), b.scale, lse=lse_off)
+    torch.cuda.synchronize()
+    assert torch.equal(out_off, o_ref)
+    assert torch.equal(lse_off, l_ref)
+    assert torch.isnan(obuf[:4]).all() and torch.isnan(lbuf[:1]).all()  # nothing written before the views
+
+
 def test_tcgen05_prefill_reports_bf16_values_beyond_fp16():
     """A bf16 V element of magnitude >= 2^16 does not fit the fp16 P.V product
     of PA_PREFILL_TCGEN05: the call reports PA_DEVERR_FP16_RANGE; the pair
