@@ -64,10 +64,8 @@ NCU_TRAFFIC = {
     "decode": {"workload": 2, "bytes": 308_711_936,
                "sha256": "9dab5f410c2821164ca2057a06aaf1a2a5cf2ec7d48f8e15b5a73c2a18088b18",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
-    # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 46,217,472 + dram__bytes_write.sum 1,360,640
-    "prefill": {"workload": 5, "bytes": 47_578_112,
-                "sha256": "146b1841c98fa573cd40dcdd038a9a19f805b4ff0604973e767533771201425b",
+    # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V)
+    "prefill": {"workload": 5, "bytes": None, "sha256": "",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
@@ -401,9 +399,14 @@ def run_ours(args):
     # mixed step: after the cache write, decode and prefill in one persistent
     # launch (--mixed-mode fused), the decode on a second stream beside the
     # prefill (streams) or one after the other (serial)
+    pf_ws = None
+    if mixed and args.prefill_entry == "balanced":
+        pf_ws = B.prefill_workspace(desc, int(b.context_lens_prefill.shape[0]), pf_maxq, dev)
+    pf_entry = "pa_prefill_chunk_balanced" if pf_ws is not None else "pa_prefill_chunk"
     ms = MixedStep(desc, kc, vc, b.scale, decode_out=out, workspace=wsp, max_context_len_decode=maxL,
                    prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
-                   max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode)
+                   max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode,
+                   prefill_workspace=pf_ws)
     decode, prefill, attend = ms.decode, ms.prefill, ms.attend
     if ms.mode == "fused":
         launches_per_step = 2
@@ -627,17 +630,17 @@ def run_ours(args):
             line["cycles_per_step"] = round(step_ms * 1e-3 * clocks["sm_mhz"] * 1e6)
         if mixed:
             pf_tf = pf_flops / (pf_ms * 1e-3) / 1e12
-            line["prefill"] = {"kernel": "pa_prefill_chunk", "us": round(pf_ms * 1e3, 2), "flops": pf_flops,
+            line["prefill"] = {"kernel": pf_entry, "us": round(pf_ms * 1e3, 2), "flops": pf_flops,
                                "tflops": round(pf_tf, 1)}
             if pf_ms > dec_ms:
                 # the prefill dominates the step: the roofline is its tensor-core bound
                 # (algorithmic flops; the bf16 hi/lo split of P adds half again to PV)
                 line["roofline_decode"] = line["roofline"]
-                line["roofline"] = {"bound": "tensor", "kernel": "pa_prefill_chunk, " + alone_how,
+                line["roofline"] = {"bound": "tensor", "kernel": pf_entry + ", " + alone_how,
                                     "achieved": round(pf_tf, 1), "peak": tc_peak,
                                     "peak_kind": f"{peak_kind} bf16 dense (burst)", "unit": "TFLOP/s",
                                     "frac": round(pf_tf / tc_peak, 4), "kernel_us": round(pf_ms * 1e3, 2),
-                                    "traffic": _traffic("prefill", args.workload, local)}
+                                    "traffic": _traffic("prefill", args.workload, local or pf_ws is not None)}
         if not args.no_cpu_baseline:
             if b.kv_dtype in (W.KV_BF16, W.KV_F16):
                 line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget,
@@ -795,6 +798,9 @@ def main():
                     help="0 auto, 1 mma.sync, 2 tcgen05 (fp16 P.V), 3 tcgen05 (P as a hi + lo pair)")
     ap.add_argument("--fp8-format", choices=sorted(FP8_FORMATS), default="e4m3",
                     help="8-bit cache format of workload 4 (same shapes)")
+    ap.add_argument("--prefill-entry", choices=["chunk", "balanced"], default="chunk",
+                    help="prefill entry point: pa_prefill_chunk (a CTA per query tile and kv head) or "
+                         "pa_prefill_chunk_balanced (the library's choice of that grid or the balanced kernel)")
     ap.add_argument("--mixed-mode", choices=["fused", "streams", "serial"], default="fused",
                     help="mixed step (workload 5): one persistent launch, two streams, or one after the other")
     ap.add_argument("--per-head-scales", action="store_true",

@@ -61,7 +61,8 @@
  * waits (bounded) for its own copies and products in flight, frees what it
  * holds and returns; its outputs are then incomplete.  The error words are
  * the caller's pa_kv_desc.error_word (every kernel, when given) and, for
- * pa_decode, the first int32 of its workspace.  Kernels never trap.
+ * pa_decode and pa_prefill_chunk_balanced, the first int32 of the
+ * workspace.  Kernels never trap.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -78,8 +79,10 @@ extern "C" {
  *    (appended); PA_KV_F16; pa_prefix_attention, pa_copy_blocks.
  * 3: pa_kv_desc gains error_word, check_indices (appended); PA_DEVERR_*;
  *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
- *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention. */
-#define PA_ABI_VERSION 3
+ *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention.
+ * 4: pa_prefill_workspace_size, pa_prefill_chunk_balanced,
+ *    pa_test_prefill_schedule. */
+#define PA_ABI_VERSION 4
 
 /* Symbols of the shared library; everything else in it stays hidden. */
 #if defined(__GNUC__)
@@ -283,6 +286,46 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
                            float scale, pa_stream_t stream);
 
 /*
+ * Bytes of scratch that pa_prefill_chunk_balanced needs for num_seqs chunks
+ * of at most max_q_len queries on the current device (0 if the descriptor is
+ * invalid).  Same rules as pa_decode's workspace: zero-fill it once before
+ * its first use; consecutive calls on one stream may reuse it (a call that
+ * completes without error leaves its error word and its piece counters at
+ * zero); calls that overlap on the GPU need separate workspaces.  After a
+ * call completes, its first int32 holds the PA_DEVERR_* bits the balanced
+ * kernel reported; if it is not zero, zero-fill the whole workspace again
+ * before its next use.
+ */
+PA_API size_t pa_prefill_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len);
+
+/*
+ * pa_prefill_chunk, with the work spread evenly over the SMs where that pays.
+ * Same arguments, same result up to fp32 rounding (within the library's
+ * tolerances of pa_prefill_chunk).  pa_prefill_chunk gives every (query tile
+ * of 256 / g queries, kv head) item its own CTA, so a batch of n items runs
+ * in ceil(n / SMs) waves, and a batch of fewer items than SMs (a few long
+ * chunks) leaves SMs idle for the whole launch.  The balanced kernel runs one
+ * CTA per SM, each taking an equal share of all items' 128-key tiles; an
+ * item whose tiles fall to several CTAs is computed in pieces (the "chunked
+ * prefill" chunk cut along its keys), and the last piece to finish merges
+ * them by log-sum-exp, as pa_merge_partials does, inside the same launch.
+ * It runs when the descriptor selects a tcgen05 prefill kernel, num_seqs *
+ * ceil(max_q_len * g / 256) <= 16384, the batch has fewer items than SMs and
+ * ceil(max_context_len / 128) * (SMs - items) > 12 * SMs (the SMs the grid
+ * would leave idle outweigh the pieces' merges); other batches run
+ * pa_prefill_chunk's grid (pa_test_prefill_schedule overrides the choice).
+ *   workspace : pa_prefill_workspace_size(desc, num_seqs, max_q_len) bytes,
+ *               16-byte aligned, zero-filled before its first use.
+ */
+PA_API pa_status pa_prefill_chunk_balanced(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                                           const int32_t *query_start_loc, const void *k_cache,
+                                           const void *v_cache, const int32_t *block_tables,
+                                           int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                           int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
+                                           float scale, void *workspace, size_t workspace_bytes,
+                                           pa_stream_t stream);
+
+/*
  * Decode and chunked-prefill attention of one continuous-batch step in a
  * single launch (the step of the "C++20 Continuous Batching Loop" in the
  * "vllm.cpp ARCHITECTURE OVERVIEW" figure; the unified scheduler with
@@ -469,6 +512,15 @@ PA_API pa_status pa_decode_static(const pa_kv_desc *desc, float *out, float *lse
  * launches.  Never enable it outside tests.
  */
 PA_API pa_status pa_test_stall_pipelines(int32_t enable, int64_t wait_limit_ns);
+
+/*
+ * Test hook (no counterpart on the pages): which schedule
+ * pa_prefill_chunk_balanced runs.  0 (the default): the library's choice; 1:
+ * the balanced kernel wherever it applies (a tcgen05 prefill kernel, the
+ * batch within its limits); 2: always pa_prefill_chunk's grid.
+ * Process-wide; returns PA_ERR_INVALID_ARG for other values.
+ */
+PA_API pa_status pa_test_prefill_schedule(int32_t schedule);
 
 #ifdef __cplusplus
 }

@@ -46,11 +46,12 @@ PA_DEVERR_REFCOUNT = 8
 
 #: every symbol include/pa.h declares
 #: PA_ABI_VERSION this binding is written against (pa_kv_desc layout, entry points)
-ABI_VERSION = 3
+ABI_VERSION = 4
 EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_workspace_size",
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
             "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
-            "pa_mixed_workspace_size", "pa_mixed_attention")
+            "pa_mixed_workspace_size", "pa_mixed_attention", "pa_prefill_workspace_size",
+            "pa_prefill_chunk_balanced", "pa_test_prefill_schedule")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -109,6 +110,10 @@ def load(path: Optional[str] = None):
         lib.pa_decode.restype = ctypes.c_int
         lib.pa_prefill_chunk.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P]
         lib.pa_prefill_chunk.restype = ctypes.c_int
+        lib.pa_prefill_workspace_size.argtypes = [D, I32, I32]
+        lib.pa_prefill_workspace_size.restype = SZ
+        lib.pa_prefill_chunk_balanced.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P, SZ, P]
+        lib.pa_prefill_chunk_balanced.restype = ctypes.c_int
         lib.pa_prefix_attention.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, F, P]
         lib.pa_prefix_attention.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [D, P, P, P, P, I32, P]
@@ -128,6 +133,8 @@ def load(path: Optional[str] = None):
         lib.pa_release_blocks.restype = ctypes.c_int
         lib.pa_test_stall_pipelines.argtypes = [I32, ctypes.c_int64]
         lib.pa_test_stall_pipelines.restype = ctypes.c_int
+        lib.pa_test_prefill_schedule.argtypes = [I32]
+        lib.pa_test_prefill_schedule.restype = ctypes.c_int
         if lib.pa_abi_version() != ABI_VERSION:
             raise RuntimeError(f"{p} has ABI version {lib.pa_abi_version()}, this binding expects {ABI_VERSION}: "
                                "rebuild it")
@@ -311,6 +318,34 @@ def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, 
                                    int(max_context_len), float(scale), _stream(stream)))
 
 
+def pa_prefill_workspace_size(desc: PaKvDesc, num_seqs: int, max_q_len: int) -> int:
+    n = load().pa_prefill_workspace_size(ctypes.byref(desc), int(num_seqs), int(max_q_len))
+    if n == 0:
+        raise PaError(PA_ERR_INVALID_ARG, last_error())
+    return n
+
+
+def prefill_workspace(desc: PaKvDesc, num_seqs: int, max_q_len: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace of pa_prefill_workspace_size bytes."""
+    return torch.zeros(pa_prefill_workspace_size(desc, num_seqs, max_q_len), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_prefill_chunk_balanced(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, block_tables,
+                              context_lens, max_q_len: int, max_context_len: int, scale: float, workspace,
+                              lse=None, stream=None):
+    """pa_prefill_chunk with the KV work spread evenly over the SMs (``workspace``:
+    a uint8 CUDA tensor of pa_prefill_workspace_size bytes, zero-filled once)."""
+    S = int(context_lens.shape[0])
+    _check(load().pa_prefill_chunk_balanced(ctypes.byref(desc), _ptr(out, _F32, "out"),
+                                            _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
+                                            _ptr(query_start_loc, _I32, "query_start_loc"),
+                                            _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                            _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
+                                            _ptr(context_lens, _I32, "context_lens"), S, int(max_q_len),
+                                            int(max_context_len), float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
+                                            workspace.numel(), _stream(stream)))
+
+
 def pa_prefix_attention(desc: PaKvDesc, out, lse, q, query_start_loc, k_cache, v_cache, prefix_tables,
                         prefix_lens, max_q_len: int, max_prefix_len: int, scale: float, num_splits: int = 1,
                         out_slots: int = 0, stream=None):
@@ -373,6 +408,12 @@ def pa_test_stall_pipelines(enable: bool, wait_limit_ns: int = 20_000_000):
     prefill kernels issue no copies and their bounded waits (limited to
     ``wait_limit_ns``) run out; they report PA_DEVERR_WAIT_TIMEOUT and return."""
     _check(load().pa_test_stall_pipelines(1 if enable else 0, int(wait_limit_ns)))
+
+
+def pa_test_prefill_schedule(schedule: int):
+    """Test hook: 0 the library's choice, 1 the balanced kernel wherever it
+    applies, 2 pa_prefill_chunk's grid (for pa_prefill_chunk_balanced)."""
+    _check(load().pa_test_prefill_schedule(int(schedule)))
 
 
 def pa_merge_partials(out, part_o, part_lse, num_parts=None, lse_out=None, stream=None):

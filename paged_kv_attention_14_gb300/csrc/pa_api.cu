@@ -63,6 +63,7 @@ pa_status check_desc(const pa_kv_desc *d) {
 
 std::atomic<int> g_test_stall{0};
 std::atomic<unsigned long long> g_test_wait_ns{0};
+std::atomic<int> g_test_schedule{0};  // pa_test_prefill_schedule
 
 pa_status cuda_fail(cudaError_t e) {
   return fail(PA_ERR_CUDA, "CUDA error: %s", cudaGetErrorString(e));
@@ -79,6 +80,7 @@ TestHooks test_hooks() {
   h.stall = g_test_stall.load(std::memory_order_relaxed);
   const unsigned long long w = g_test_wait_ns.load(std::memory_order_relaxed);
   h.wait_ns = (h.stall && w) ? w : kDefaultWaitNs;
+  h.prefill_schedule = g_test_schedule.load(std::memory_order_relaxed);
   return h;
 }
 
@@ -209,6 +211,47 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
   const cudaError_t e = pa::launch_prefill(*desc, out, lse, q, query_start_loc, k_cache, v_cache,
                                            block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                            max_q_len, scale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+size_t pa_prefill_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len) {
+  if (check_desc(desc) != PA_OK || num_seqs < 0 || max_q_len < 0) return 0;
+  const char *why = "";
+  if (pa::check_prefill(*desc, &why) != PA_OK) {
+    fail(PA_ERR_UNSUPPORTED, "%s", why);
+    return 0;
+  }
+  return pa::prefill_sk_workspace_bytes(*desc, num_seqs, max_q_len);
+}
+
+pa_status pa_prefill_chunk_balanced(const pa_kv_desc *desc, float *out, float *lse, const void *q,
+                                    const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len,
+                                    int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                                    pa_stream_t stream) {
+  const pa_status st = pa::validate_prefill(desc, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                            max_blocks_per_seq, context_lens, num_seqs, max_q_len, max_context_len,
+                                            scale);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0 || max_q_len == 0) return ok();
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
+  if (workspace_bytes < pa::prefill_sk_workspace_bytes(*desc, num_seqs, max_q_len))
+    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_prefill_workspace_size()%s");
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the balanced kernel where it applies and pays (or as the test hook says)
+  const int forced = pa::test_hooks().prefill_schedule;
+  const bool balanced =
+      pa::prefill_sk_applies(*desc, num_seqs, max_q_len) &&
+      pa::prefill_sk_units_fit(*desc, num_seqs, max_q_len, max_blocks_per_seq) &&
+      (forced == 1 || (forced == 0 && pa::prefill_sk_pays(*desc, num_seqs, max_q_len, max_context_len)));
+  const cudaError_t e =
+      balanced
+          ? pa::launch_prefill_tc_sk(*desc, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                                     max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, workspace, s)
+          : pa::launch_prefill(*desc, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,
+                               max_blocks_per_seq, context_lens, num_seqs, max_q_len, scale, s);
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 
@@ -390,6 +433,12 @@ pa_status pa_merge_partials(float *out, float *lse_out, const float *part_o,
                                          num_heads, max_parts, head_dim,
                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+pa_status pa_test_prefill_schedule(int32_t schedule) {
+  if (schedule < 0 || schedule > 2) return fail(PA_ERR_INVALID_ARG, "schedule must be 0, 1 or 2%s");
+  g_test_schedule.store(schedule, std::memory_order_relaxed);
+  return ok();
 }
 
 pa_status pa_test_stall_pipelines(int32_t enable, int64_t wait_limit_ns) {

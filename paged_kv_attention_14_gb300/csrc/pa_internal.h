@@ -88,6 +88,31 @@ cudaError_t launch_prefill_tc(const pa_kv_desc &d, float *out, float *lse, const
                               int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
                               bool prefix_mode, int num_splits, int split_len, int out_slots, bool pair_p);
 
+// The prefill kernel a descriptor selects (a pa_prefill_impl value other
+// than AUTO).
+int prefill_impl_of(const pa_kv_desc &d);
+
+// The balanced tcgen05 prefill (pa_prefill_chunk_balanced): one CTA per SM,
+// the KV iterations of all (query tile, kv head) items dealt out evenly, an
+// item cut between CTAs merged in the launch.  It takes batches of at most
+// kPrefillSkMaxPairs (sequence, query tile) pairs with a tcgen05 prefill
+// kernel selected; others run the plain grid.  Workspace bytes (zero-filled
+// once before the first use) and the launch.
+constexpr long long kPrefillSkMaxPairs = 16384;
+size_t prefill_sk_workspace_bytes(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len);
+bool prefill_sk_applies(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len);
+// ... and whether its unit count (KV iterations of all items) stays below 2^31
+bool prefill_sk_units_fit(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len, int32_t max_blocks_per_seq);
+// Whether the balanced kernel is expected to beat the grid: fewer items than
+// SMs, with contexts long enough that the SMs the grid leaves idle cost more
+// than the pieces' partial outputs and merges.
+bool prefill_sk_pays(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len, int32_t max_context_len);
+cudaError_t launch_prefill_tc_sk(const pa_kv_desc &d, float *out, float *lse, const void *q,
+                                 const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t *context_lens, int32_t num_seqs, int32_t max_q_len, float scale,
+                                 void *workspace, cudaStream_t stream);
+
 // Copy-on-write of whole blocks (all kv heads) of both caches.
 cudaError_t launch_copy_blocks(const pa_kv_desc &d, void *k_cache, void *v_cache, const int32_t *src_blocks,
                                const int32_t *dst_blocks, int32_t num_pairs, cudaStream_t stream);
@@ -111,6 +136,7 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 struct TestHooks {
   int stall;
   unsigned long long wait_ns;
+  int prefill_schedule;  // pa_test_prefill_schedule: 0 the library's choice, 1 balanced, 2 grid
 };
 TestHooks test_hooks();
 

@@ -421,6 +421,14 @@ pa_status check_prefill(const pa_kv_desc &d, const char **why) {
   return PA_OK;
 }
 
+int prefill_impl_of(const pa_kv_desc &d) {
+  const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
+  // automatic choice: the tcgen05 kernel, except 8-bit caches of head_dim 64
+  return d.prefill_impl != PA_PREFILL_AUTO ? d.prefill_impl
+         : (fp8 && d.head_dim != 128)      ? PA_PREFILL_MMA_SYNC
+                                           : PA_PREFILL_TCGEN05;
+}
+
 cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const void *q,
                            const int32_t *query_start_loc, const void *k_cache,
                            const void *v_cache, const int32_t *block_tables,
@@ -428,10 +436,7 @@ cudaError_t launch_prefill(const pa_kv_desc &d, float *out, float *lse, const vo
                            int32_t num_seqs, int32_t max_q_len, float scale, cudaStream_t stream,
                            bool prefix_mode, int num_splits, int split_len, int out_slots) {
   const bool fp8 = d.kv_dtype == PA_KV_FP8_E4M3 || d.kv_dtype == PA_KV_FP8_E5M2;
-  // automatic choice: the tcgen05 kernel, except 8-bit caches of head_dim 64
-  const int impl = d.prefill_impl != PA_PREFILL_AUTO       ? d.prefill_impl
-                   : (fp8 && d.head_dim != 128)             ? PA_PREFILL_MMA_SYNC
-                                                            : PA_PREFILL_TCGEN05;
+  const int impl = prefill_impl_of(d);
   if (impl == PA_PREFILL_TCGEN05 || impl == PA_PREFILL_TCGEN05_PAIR)
     return launch_prefill_tc(d, out, lse, q, query_start_loc, k_cache, v_cache, block_tables, max_blocks_per_seq,
                              context_lens, num_seqs, max_q_len, scale, stream, prefix_mode, num_splits, split_len,

@@ -126,7 +126,91 @@ struct Args {
   int checked;      // range-check block ids and lengths (pa_kv_desc.check_indices)
   int stall;        // test hook: the producer issues nothing, so the waits run out
   int num_blocks;   // blocks of the cache (checked mode)
+  // balanced launch (prefill_sk_kernel): items are (pair p, kv head), pair p
+  // = (sequence p / gx, query tile gx - 1 - p % gx), and their KV iterations
+  // are dealt out evenly over the CTAs.  An item cut between CTAs leaves one
+  // piece per CTA in a slot (two slots per CTA: its first and its last item)
+  int num_seqs;
+  int gx;               // query tiles per sequence
+  float *part_o;        // [2 G][D / 4][MROWS] float4: normalised O of a piece
+  float *part_lse;      // [2 G][MROWS]: its log-sum-exp, log2 units
+  int *part_count;      // [num_seqs * gx * num_kv_heads] pieces finished per item
+  int32_t *ws_err;      // the workspace's error word
 };
+
+// One call of prefill_tile: the item (sequence s, key split, kv head,
+// query tile) and the part of its KV iterations that this call covers.  A
+// piece of an item cut between the CTAs of a balanced launch also carries
+// where the item's other pieces are.
+struct Seg {
+  int s, split, kvh, qtile, gx;
+  int it_lo, it_hi;       // KV iterations [it_lo, it_hi) of the item; it_hi < 0: all
+  int piece;              // 1: the item is cut between CTAs c_lo .. c_hi
+  int slot;               // this piece's slot
+  int item;               // the item's piece counter
+  int c_lo, c_hi, me, G;  // CTAs holding the pieces; this CTA; CTAs sharing the work
+  int item_start;         // the item's first unit
+  int U;                  // units of the launch (below 2^31)
+};
+
+// CTA c of G takes units [c U / G, (c + 1) U / G); cta_of(u) is the CTA
+// holding unit u, and a piece's slot is 0 for the CTA's first item (the item
+// began at or before the CTA's first unit) and 1 for its last.
+__device__ __forceinline__ int sk_first_unit(int c, int U, int G) {
+  return static_cast<int>(static_cast<long long>(c) * U / G);
+}
+__device__ __forceinline__ int sk_cta_of(int u, int U, int G) {
+  return static_cast<int>((static_cast<long long>(u + 1) * G - 1) / U);
+}
+__device__ __forceinline__ int sk_slot(int c, int item_start, int U, int G) {
+  return c * 2 + (item_start <= sk_first_unit(c, U, G) ? 0 : 1);
+}
+
+// The queries and keys of one item.  False if it has no query (or a
+// checked length was bad: its rows are then left unwritten); a checked
+// length out of range is reported if report is set.
+struct ItemRange {
+  int qs, q_len, L, qt0, nq, p_lo, p_hi, base_pos, kv_end, kv_lo, j0, n_tiles;
+};
+__device__ __forceinline__ bool item_range(const Args &a, int s, int split, int qtile, int gx, bool report,
+                                           ItemRange &r) {
+  r.qs = __ldg(a.query_start_loc + s);
+  r.q_len = __ldg(a.query_start_loc + s + 1) - r.qs;
+  r.L = __ldg(a.context_lens + s);
+  if (a.checked) {
+    // lengths within the table's capacity; a chunk no longer than its context
+    // nor than the launch's query tiles; rows start at a row >= 0
+    int32_t *e1 = report ? a.err : nullptr, *e2 = report ? a.ws_err : nullptr;
+    r.L = checked_len(r.L, a.max_blocks_per_seq * 16, e1, e2);
+    r.q_len = checked_len(r.q_len, a.prefix_mode ? gx * a.qt : min(r.L, gx * a.qt), e1, e2);
+    if (r.qs < 0) {
+      if (report && threadIdx.x == 0) report_error(a.err, a.ws_err, kErrBadIndex);
+      return false;
+    }
+  }
+  r.qt0 = qtile * a.qt;
+  if (r.qt0 >= r.q_len) return false;
+  r.nq = min(a.qt, r.q_len - r.qt0);
+  // prefix mode: the split covers prefix keys [p_lo, p_hi), and every query
+  // comes after them all; otherwise query i sits at L - q_len + i
+  r.p_lo = a.prefix_mode ? min(r.L, split * a.split_len) : 0;
+  r.p_hi = a.prefix_mode ? min(r.L, r.p_lo + a.split_len) : 0;
+  r.base_pos = a.prefix_mode ? r.p_hi - 1 : r.L - r.q_len + r.qt0;  // position of query qt0
+  r.kv_end = a.prefix_mode ? r.p_hi : r.base_pos + r.nq;            // keys [kv_lo, kv_end) are needed
+  // local attention: the earliest query sees keys from kv_lo on (the first
+  // key never decreases with the position)
+  r.kv_lo = a.prefix_mode ? r.p_lo : local_first_key(r.base_pos, a.window, a.chunk);
+  r.j0 = r.kv_lo / KT;
+  r.n_tiles = (r.kv_end + KT - 1) / KT;
+  return true;
+}
+
+// KV iterations of pair p's items (chunk mode), 0 if it has no query
+__device__ __forceinline__ int pair_iters(const Args &a, int p) {
+  ItemRange r;
+  if (!item_range(a, p / a.gx, 0, a.gx - 1 - p % a.gx, a.gx, false, r)) return 0;
+  return max(0, r.n_tiles - r.j0);
+}
 
 // Optional timeline counters (compiled only with -DPA_PREFILL_TRACE), per
 // CTA slot (blockIdx linearised, first 4096): softmax warp 0 lane 0 cycles
@@ -203,7 +287,7 @@ struct Cfg {
 // barriers: K_FULL[NSK], K_EMPTY[NSK], V_FULL[NSV], V_EMPTY[NSV],
 // S_FULL[tile], P_FULL[tile], V_READY[NSV] (fp16 P: the V tile is in fp16,
 // rows outside the needed keys zeroed), K_READY[NSK] (8-bit caches: the K
-// tile widened to fp16), Q_FULL (the Q tiles that come by TMA)
+// tile widened to fp16), Q_FULL (the Q tiles that come by TMA), Q_EMPTY
 enum Bar {
   K_FULL = 0,
   K_EMPTY = K_FULL + NSK,
@@ -214,9 +298,10 @@ enum Bar {
   V_READY = P_FULL + NQT,
   K_READY = V_READY + NSV,  // 8-bit caches: the K tile widened to fp16
   Q_FULL = K_READY + NSK,   // the Q tiles copied by TMA have landed
-  NBAR = Q_FULL + 1
+  Q_EMPTY = Q_FULL + 1,     // balanced launch: a segment's last QKs completed (Q may be replaced)
+  NBAR = Q_EMPTY + 1
 };
-static_assert(NBAR * 8 + 16 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
+static_assert(NBAR * 8 + 24 <= 256, "barriers, TMEM slot and flags fit their 256 bytes");
 
 // Shared memory of a CTA: the tile's operands at 1024-byte alignment, then
 // its barriers, the TMEM slot and three flags (see Cfg::OFF_BAR).
@@ -224,15 +309,13 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// One prefill tile: query tile bx of gx (counted from the last, so that the
-// longest key ranges come first), kv head by, sequence (or sequence x key
-// split in prefix mode) bz.  Run by all NTHREADS threads of a CTA with
-// tensor memory already allocated (tmem: all TMEM_COLS columns); every
-// thread takes the same early returns.  On return every copy and product of
-// the tile has completed, so that its barriers can be set up again for the
-// next tile.
+// One prefill tile: the item of sg (its KV iterations [it_lo, it_hi)).  Run
+// by all NTHREADS threads of a CTA with tensor memory already allocated
+// (tmem: all TMEM_COLS columns); every thread takes the same early returns.
+// On return every copy and product of the tile has completed, so that its
+// barriers can be set up again for the next tile.
 template <int D, int KVT, int PVM>
-__device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx, int by, int bz, int gx) {
+__device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const Seg &sg) {
   using C = Cfg<D, KVT, PVM>;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + NBAR);
@@ -240,32 +323,18 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   int *s_last_k = s_abort + 1;  // last KV tile whose K copies the producer issued
   int *s_last_v = s_abort + 2;  // ... and whose V copies
 
-  const int split = a.prefix_mode ? bz % a.num_splits : 0;
-  const int s = a.prefix_mode ? bz / a.num_splits : bz;
-  const int kvh = by;
-  const int qtile = gx - 1 - bx;  // longest key ranges first
-  const int qs = __ldg(a.query_start_loc + s);
-  int q_len = __ldg(a.query_start_loc + s + 1) - qs;
-  int L = __ldg(a.context_lens + s);
-  if (a.checked) {
-    // lengths within the table's capacity; a chunk no longer than its context
-    // nor than the launch's query tiles; rows start at a row >= 0
-    L = checked_len(L, a.max_blocks_per_seq * 16, a.err, nullptr);
-    q_len = checked_len(q_len, a.prefix_mode ? gx * a.qt : min(L, gx * a.qt), a.err, nullptr);
-    if (qs < 0) {
-      if (threadIdx.x == 0) report_error(a.err, nullptr, kErrBadIndex);
-      return;
-    }
-  }
-  const int qt0 = qtile * a.qt;
-  if (qt0 >= q_len) return;
-  const int nq = min(a.qt, q_len - qt0);
-  // prefix mode: this CTA's split covers prefix keys [p_lo, p_hi), and every
-  // query comes after them all; otherwise query i sits at L - q_len + i
-  const int p_lo = a.prefix_mode ? min(L, split * a.split_len) : 0;
-  const int p_hi = a.prefix_mode ? min(L, p_lo + a.split_len) : 0;
-  const int base_pos = a.prefix_mode ? p_hi - 1 : L - q_len + qt0;  // position of query qt0
-  const int kv_end = a.prefix_mode ? p_hi : base_pos + nq;         // keys [kv_lo, kv_end) are needed
+  const int split = sg.split;
+  const int s = sg.s;
+  const int kvh = sg.kvh;
+  ItemRange ir;
+  if (!item_range(a, s, split, sg.qtile, sg.gx, true, ir)) return;
+  const int qs = ir.qs;
+  const int qt0 = ir.qt0;
+  const int nq = ir.nq;
+  const int p_lo = ir.p_lo;
+  const int p_hi = ir.p_hi;
+  const int base_pos = ir.base_pos;
+  const int kv_end = ir.kv_end;
   if (a.prefix_mode && p_hi <= p_lo) {
     // no key in this split (an empty or short shared prefix): out = 0,
     // lse = -inf, before any barrier or tensor memory is set up
@@ -277,13 +346,12 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     return;
   }
-  // local attention: the CTA's earliest query sees keys from kv_lo on (the
-  // first key never decreases with the position).  KV tiles j0 .. n_tiles - 1
-  // are walked; the rings and barriers count iterations jj = j - j0.
-  const int kv_lo = a.prefix_mode ? p_lo : local_first_key(base_pos, a.window, a.chunk);
-  const int j0 = kv_lo / KT;
-  const int n_tiles = (kv_end + KT - 1) / KT;
-  const int n_iter = n_tiles - j0;
+  // KV tiles j0 .. j0 + n_iter - 1 are walked (the item's iterations
+  // [it_lo, it_hi)); the rings and barriers count iterations jj = j - j0
+  const int kv_lo = ir.kv_lo;
+  const int it_hi = sg.it_hi < 0 ? ir.n_tiles - ir.j0 : sg.it_hi;
+  const int j0 = ir.j0 + sg.it_lo;
+  const int n_iter = it_hi - sg.it_lo;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -337,7 +405,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   const bool issuer = lane < BPT * BOXES;
   auto block_id = [&](int lb) {
     const int v = __ldg(table + lb);
-    return a.checked ? checked_block(v, a.num_blocks, a.err, nullptr) : v;
+    return a.checked ? checked_block(v, a.num_blocks, a.err, a.ws_err) : v;
   };
   int phys_next = 0;
   if (qtma_tiles != 0) __syncthreads();  // the barriers are set up
@@ -388,7 +456,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
         cp_async16(dst, src, ok);
       }
     }
-    if (C::KV8 && qmax >= 65536.f && qmax <= FLT_MAX) report_error(a.err, nullptr, kErrFp16Range);
+    if (C::KV8 && qmax >= 65536.f && qmax <= FLT_MAX) report_error(a.err, a.ws_err, kErrFp16Range);
     cp_async_commit();
     cp_async_wait<0>();
     fence_proxy_async_smem();
@@ -412,9 +480,10 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
       const int lb = (j + 1) * BPT + bi;  // prefetch the next tile's block id
       phys_next = (issuer && lb * 16 < kv_end) ? block_id(lb) : 0;
       const int nblk = min(BPT, (kv_end - key0 + 15) / 16);
-      // blocks of the first tile entirely before the CTA's first key are not
-      // read (under local attention their pages may be gone)
-      const int bskip = jj == 0 ? (kv_lo >> 4) - j * BPT : 0;
+      // blocks of the first tile entirely before the item's first key are
+      // not read (under local attention their pages may be gone); a piece
+      // that starts later has none
+      const int bskip = jj == 0 ? max(0, (kv_lo >> 4) - j * BPT) : 0;
       const int row = (phys * a.num_kv_heads + kvh) * 16;
       // K of tile j (its slot frees once the QKs of tile j - NSK completed),
       // then V of tile j (once the PVs of tile j - NSV completed)
@@ -452,7 +521,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     if (!ok && lane == 0) *s_abort = 1;
     PF_TRACE(const int slot = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-             if (lane == 0 && slot < 4096) { g_pf_trace[slot][12] = tp_wait; g_pf_trace[slot][13] = clock64() - tp0; g_pf_trace[slot][14] = n_tiles; })
+             if (lane == 0 && slot < 4096) { g_pf_trace[slot][12] = tp_wait; g_pf_trace[slot][13] = clock64() - tp0; g_pf_trace[slot][14] = n_iter; })
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -672,7 +741,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
     }
     // finite values beyond fp16's range (NaN is skipped by fmaxf; an
     // infinity propagates as it does in exact arithmetic)
-    if (C::CONVERT && vmax >= 65536.f && vmax <= FLT_MAX) report_error(a.err, nullptr, kErrFp16Range);
+    if (C::CONVERT && vmax >= 65536.f && vmax <= FLT_MAX) report_error(a.err, a.ws_err, kErrFp16Range);
     if (!ok && lane == 0) *s_abort = 1;
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------- softmax, two threads per row
@@ -920,7 +989,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   tc_fence_before_sync();
   __syncthreads();
   if (*s_abort) {
-    if (tid == 0) report_error(a.err, nullptr, kErrWaitTimeout);
+    if (tid == 0) report_error(a.err, a.ws_err, kErrWaitTimeout);
     if (warp == kProducerWarp && lane == 0) {
       if (qtma_tiles != 0 && !a.stall) mbar_wait(&bar[Q_FULL], 0, a.wait_ns);
       for (int t = max(0, *s_last_k - NSK + 1); t <= *s_last_k; ++t)
@@ -940,6 +1009,28 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx
   }
   tc_fence_before_sync();
   __syncthreads();
+}
+
+// One tile of a grid: query tile bx of gx (counted from the last, so that
+// the longest key ranges come first), kv head by, sequence (or sequence x
+// key split in prefix mode) bz; all of its KV iterations.
+template <int D, int KVT, int PVM>
+__device__ __forceinline__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx, int by, int bz,
+                                             int gx) {
+  Seg sg;
+  sg.split = a.prefix_mode ? bz % a.num_splits : 0;
+  sg.s = a.prefix_mode ? bz / a.num_splits : bz;
+  sg.kvh = by;
+  sg.qtile = gx - 1 - bx;
+  sg.gx = gx;
+  sg.it_lo = 0;
+  sg.it_hi = -1;
+  sg.piece = 0;
+  sg.slot = sg.item = sg.c_lo = sg.c_hi = sg.me = 0;
+  sg.G = 1;
+  sg.item_start = 0;
+  sg.U = 1;
+  prefill_tile<D, KVT, PVM>(a, smem, tmem, sg);
 }
 
 template <int D, int KVT, int PVM>

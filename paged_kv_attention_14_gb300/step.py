@@ -37,13 +37,17 @@ class MixedStep:
     Buffers that persist across steps (the caches, the decode workspace and
     the outputs) are given once; the per-step inputs are passed to
     ``__call__``.  Either part may be absent (``decode_out`` or
-    ``prefill_out`` None)."""
+    ``prefill_out`` None).  With a ``prefill_workspace``
+    (binding.prefill_workspace) the prefill runs as
+    pa_prefill_chunk_balanced, its KV work spread evenly over the SMs;
+    without one as pa_prefill_chunk."""
 
     MODES = ("fused", "streams", "serial")
 
     def __init__(self, desc: B.PaKvDesc, k_cache, v_cache, scale: float, *, decode_out=None, decode_lse=None,
                  workspace=None, max_context_len_decode: int = 0, prefill_out=None, prefill_lse=None,
-                 max_q_len: int = 0, max_context_len_prefill: int = 0, mode: str = "fused"):
+                 max_q_len: int = 0, max_context_len_prefill: int = 0, mode: str = "fused",
+                 prefill_workspace=None):
         if mode not in self.MODES:
             raise ValueError(f"mode must be one of {self.MODES}")
         self.desc = desc
@@ -53,6 +57,7 @@ class MixedStep:
         self.max_context_len_decode = int(max_context_len_decode)
         self.prefill_out, self.prefill_lse = prefill_out, prefill_lse
         self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
+        self.prefill_workspace = prefill_workspace
         both = decode_out is not None and prefill_out is not None
         fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
                     and desc.decode_impl in (B.PA_DECODE_AUTO, B.PA_DECODE_MMA)
@@ -75,6 +80,12 @@ class MixedStep:
                     self.max_context_len_decode, self.scale, self.workspace, lse=self.decode_lse, stream=stream)
 
     def prefill(self, q, query_start_loc, block_tables, context_lens, stream=None):
+        if self.prefill_workspace is not None:
+            B.pa_prefill_chunk_balanced(self.desc, self.prefill_out, q, query_start_loc, self.k_cache,
+                                        self.v_cache, block_tables, context_lens, self.max_q_len,
+                                        self.max_context_len_prefill, self.scale, self.prefill_workspace,
+                                        lse=self.prefill_lse, stream=stream)
+            return
         B.pa_prefill_chunk(self.desc, self.prefill_out, q, query_start_loc, self.k_cache, self.v_cache,
                            block_tables, context_lens, self.max_q_len, self.max_context_len_prefill, self.scale,
                            lse=self.prefill_lse, stream=stream)

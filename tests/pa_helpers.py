@@ -132,7 +132,9 @@ def oracle_decode(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):
     return oracle_in_parallel(call, pairs, int(cl.shape[0]), b.num_q_heads)
 
 
-def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO, window=0, chunk=0):
+def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_AUTO, window=0, chunk=0,
+                workspace=None):
+    """pa_prefill_chunk, or pa_prefill_chunk_balanced with ``workspace``."""
     kc, vc = caches if caches is not None else gpu_caches(b)
     Tq = b.q_prefill.shape[0]
     out = torch.full((Tq, b.num_q_heads, b.head_dim), float("nan"), device=kc.device)
@@ -140,11 +142,23 @@ def gpu_prefill(b: W.PagedBatch, caches=None, prefill_impl: int = B.PA_PREFILL_A
     qsl = b.query_start_loc
     max_q = int((qsl[1:] - qsl[:-1]).max())
     maxL = int(b.context_lens_prefill.max())
-    B.pa_prefill_chunk(desc_of(b, prefill_impl=prefill_impl, window=window, chunk=chunk), out, b.q_prefill, qsl, kc,
-                       vc, b.block_tables_prefill,
-                       b.context_lens_prefill, max_q, maxL, b.scale, lse=lse)
+    d = desc_of(b, prefill_impl=prefill_impl, window=window, chunk=chunk)
+    if workspace is None:
+        B.pa_prefill_chunk(d, out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill, b.context_lens_prefill, max_q,
+                           maxL, b.scale, lse=lse)
+    else:
+        B.pa_prefill_chunk_balanced(d, out, b.q_prefill, qsl, kc, vc, b.block_tables_prefill, b.context_lens_prefill,
+                                    max_q, maxL, b.scale, workspace, lse=lse)
     torch.cuda.synchronize()
     return out, lse
+
+
+def prefill_workspace(b: W.PagedBatch, prefill_impl: int = B.PA_PREFILL_AUTO):
+    """A zeroed workspace for pa_prefill_chunk_balanced on the batch."""
+    qsl = b.query_start_loc
+    max_q = int((qsl[1:] - qsl[:-1]).max())
+    return B.prefill_workspace(desc_of(b, prefill_impl=prefill_impl), int(b.context_lens_prefill.shape[0]), max_q,
+                               b.q_prefill.device)
 
 
 def oracle_prefill(b: W.PagedBatch, ocaches=None, pairs=None, window=0, chunk=0):

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.pa_abi_version() == B.ABI_VERSION == 3
+    assert lib.pa_abi_version() == B.ABI_VERSION == 4
     m = re.search(r"#define\s+PA_ABI_VERSION\s+(\d+)", open(HEADER).read())
     assert int(m.group(1)) == lib.pa_abi_version()
 

@@ -373,9 +373,9 @@ def test_mixed_step_write_then_decode_and_prefill(impl, fp16):
 def test_mixed_step_as_the_bench_runs_it(mode, fp16):
     """Workload 5 through MixedStep, the step bench.py times: cache write,
     then decode and prefill in one persistent launch (fused), the decode on a
-    second stream beside the prefill (streams) or both in order on one
-    stream (serial); every decode and prefill output against the oracle,
-    the cache bit-exact, and the workspace's counters back at zero."""
+    second stream beside the balanced prefill (streams) or both in order on
+    one stream (serial); every decode and prefill output against the oracle,
+    the cache bit-exact, and the workspaces' counters back at zero."""
     from paged_kv_attention_14_gb300.step import MixedStep
     b = W.workload(5, device=DEV, poison=True, fp16=fp16)
     kv = b.kv_dtype
@@ -389,10 +389,12 @@ def test_mixed_step_as_the_bench_runs_it(mode, fp16):
     pf_out = torch.full((b.q_prefill.shape[0], 32, 128), float("nan"), device=DEV)
     pf_lse = torch.full((b.q_prefill.shape[0], 32), float("nan"), device=DEV)
     qsl = b.query_start_loc
+    pws = B.prefill_workspace(d, int(b.context_lens_prefill.shape[0]), int((qsl[1:] - qsl[:-1]).max()), DEV)
     ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, decode_lse=dec_lse, workspace=ws,
                    max_context_len_decode=maxL, prefill_out=pf_out, prefill_lse=pf_lse,
                    max_q_len=int((qsl[1:] - qsl[:-1]).max()),
-                   max_context_len_prefill=int(b.context_lens_prefill.max()), mode=mode)
+                   max_context_len_prefill=int(b.context_lens_prefill.max()), mode=mode,
+                   prefill_workspace=pws)
     assert ms.mode == mode
     for _ in range(2):  # the second call reuses the workspace the first left behind
         dec_out.fill_(float("nan"))
@@ -403,6 +405,7 @@ def test_mixed_step_as_the_bench_runs_it(mode, fp16):
            (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill))
         torch.cuda.synchronize()
         assert ws[:12].view(torch.int32).tolist() == [0, 0, 0], "error word and work counters"
+        assert int(pws.view(torch.int32)[:64 + 4 * 8 * 8].abs().sum()) == 0, "prefill error word and counters"
     code = oracle.KV_F16 if fp16 else oracle.KV_BF16
     ok, ov = oracle.cache_write(code, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
                                 b.k_pool.cpu(), b.v_pool.cpu())
