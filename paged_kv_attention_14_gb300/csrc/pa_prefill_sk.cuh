@@ -103,77 +103,130 @@ struct SkIter {
   }
 };
 
-// The last piece of a cut item merges all of its pieces, those of CTAs
-// c_lo .. c_hi in that order, every one read back from its slot (so the bits
-// do not depend on which piece finished last):
+// A merge a CTA owes: it finished the last piece of a cut item.  The item's
+// pieces lie in the slots of CTAs c_lo .. c_hi; its rows are those of
+// sequence rows qs + qt0 .. (nq queries) and kv head kvh.
+struct SkMerge {
+  int item_start, c_lo, c_hi, qs, qt0, nq, kvh;
+  float vscale;
+};
+constexpr int kMaxMerges = 2;  // a CTA's first and last items are its only pieces
+static_assert(16 + kMaxMerges * sizeof(SkMerge) <= 128, "merge list fits its 128 bytes");
+
+// The merges a CTA owes, once its pipeline has drained (every copy and
+// product complete, the rings free):
 //   out = sum_c w_c O_c / sum_c w_c,  w_c = 2^(lse_c - M),  M = max_c lse_c,
 //   lse = M + log2(sum_c w_c)  (in natural-log units on output)
-// the log-sum-exp combination of partial softmax results (as pa_merge_partials
-// computes it).  Thread (row r, half h) merges its half of row r's columns in
-// both Q tiles.  A cut item has at least two pieces; the loads of the first
-// two are in flight together, each further piece's loads (its weight's
-// too) together.
-template <int D>
-__device__ __forceinline__ void sk_merge(const Args &a, const Seg &sg, int qs, int qt0, int nq, int kvh, int r,
-                                         int h, float vscale) {
+// over the item's pieces in CTA order (the log-sum-exp combination of
+// partial softmax results, as pa_merge_partials computes it; the bits do not
+// depend on which piece finished last).  Per Q tile, each piece's 64 KB of
+// partial output comes into shared memory by one bulk copy, two buffers
+// deep, and softmax thread (row r, half h) accumulates its half of row r.
+template <int D, int KVT, int PVM>
+__device__ void sk_run_merges(const Args &a, uint8_t *smem, int U, int G, int nmerge) {
+  using C = Cfg<D, KVT, PVM>;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  const SkMerge *ml = reinterpret_cast<const SkMerge *>(smem + C::OFF_M + 16);
+  constexpr int TB = MT * D * 4;  // one Q tile of a piece
+  static_assert(2 * TB < C::OFF_BAR - C::OFF_K, "two tile buffers fit the K and V rings");
+  uint8_t *buf0 = smem + C::OFF_K;
+  // the pieces' log-sum-exp vectors (MROWS floats each) behind the buffers
+  float *lse_s = reinterpret_cast<float *>(smem + C::OFF_K + 2 * TB);
+  constexpr int kLseCap = (C::OFF_BAR - C::OFF_K - 2 * TB) / (MROWS * 4);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const bool mt = warp >= kSoftmaxWarp0;  // the merging threads
+  const int h = (warp - kSoftmaxWarp0) >> 2;
+  const int r = ((warp & 3) << 5) | lane;
   const int g = a.g;
   const int rows_used = a.qt * g;
-  const float4 *po = reinterpret_cast<const float4 *>(a.part_o);
-  const int64_t sl0 = sk_slot(sg.c_lo, sg.item_start, sg.U, sg.G);
-  const int64_t sl1 = sk_slot(sg.c_lo + 1, sg.item_start, sg.U, sg.G);
-#pragma unroll 1
-  for (int t = 0; t < NQT; ++t) {
-    const int R = t * MT + r;
-    const int qi = R / g;
-    if (!(R < rows_used && qi < nq)) continue;
-    auto lse_of = [&](int64_t sl) { return __ldcg(a.part_lse + sl * MROWS + R); };
-    const float x0 = lse_of(sl0), x1 = lse_of(sl1);
-    float M = fmaxf(x0, x1);
-#pragma unroll 4
-    for (int c = sg.c_lo + 2; c <= sg.c_hi; ++c) M = fmaxf(M, lse_of(sk_slot(c, sg.item_start, sg.U, sg.G)));
-    if (M == -INFINITY) M = 0.f;  // no key in any piece: every weight is 0
-    const float w0 = exp2f(x0 - M), w1 = exp2f(x1 - M);
-    float W = w0 + w1;
-#pragma unroll 4
-    for (int c = sg.c_lo + 2; c <= sg.c_hi; ++c) W += exp2f(lse_of(sk_slot(c, sg.item_start, sg.U, sg.G)) - M);
-    const float sc = W > 0.f ? vscale / W : 0.f;
-    const int64_t orow_i = static_cast<int64_t>(qs + qt0 + qi) * a.num_q_heads + kvh * g + (R - qi * g);
-    float *orow = a.out + orow_i * D;
-#pragma unroll 1
-    for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
-      float4 x[2][8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        x[0][k] = __ldcg(po + sl0 * (D / 4) * MROWS + (c0 / 4 + k) * MROWS + R);
-        x[1][k] = __ldcg(po + sl1 * (D / 4) * MROWS + (c0 / 4 + k) * MROWS + R);
-      }
-      float o[32];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        o[4 * k] = __fmaf_rn(w1, x[1][k].x, __fmul_rn(w0, x[0][k].x));
-        o[4 * k + 1] = __fmaf_rn(w1, x[1][k].y, __fmul_rn(w0, x[0][k].y));
-        o[4 * k + 2] = __fmaf_rn(w1, x[1][k].z, __fmul_rn(w0, x[0][k].z));
-        o[4 * k + 3] = __fmaf_rn(w1, x[1][k].w, __fmul_rn(w0, x[0][k].w));
-      }
-      for (int c = sg.c_lo + 2; c <= sg.c_hi; ++c) {
-        const int64_t sl = sk_slot(c, sg.item_start, sg.U, sg.G);
-        float4 y[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = __ldcg(po + sl * (D / 4) * MROWS + (c0 / 4 + k) * MROWS + R);
-        const float w = exp2f(lse_of(sl) - M);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          o[4 * k] = __fmaf_rn(w, y[k].x, o[4 * k]);
-          o[4 * k + 1] = __fmaf_rn(w, y[k].y, o[4 * k + 1]);
-          o[4 * k + 2] = __fmaf_rn(w, y[k].z, o[4 * k + 2]);
-          o[4 * k + 3] = __fmaf_rn(w, y[k].w, o[4 * k + 3]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4 *>(orow + c0 + i) = make_float4(o[i] * sc, o[i + 1] * sc, o[i + 2] * sc, o[i + 3] * sc);
+  if (tid == 0) {
+    mbar_init(&bar[K_FULL], 1);      // tile buffer 0
+    mbar_init(&bar[K_FULL + 1], 1);  // tile buffer 1
+    mbar_init(&bar[V_FULL], 1);      // the log-sum-exp vectors
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  int q = 0;  // tile copies issued so far (buffer q & 1, its barrier's phase (q >> 1) & 1)
+  auto issue = [&](int qq, const SkMerge &m, int c, int t) {
+    const int64_t sl = sk_slot(c, m.item_start, U, G);
+    fence_proxy_async_smem();  // earlier reads of the buffer precede the copy's writes
+    mbar_arrive_expect_tx(&bar[K_FULL + (qq & 1)], TB);
+    bulk_g2s(buf0 + (qq & 1) * TB, a.part_o + (sl * NQT + t) * (D / 4) * MT * 4, TB, &bar[K_FULL + (qq & 1)]);
+  };
+  for (int e = 0; e < nmerge; ++e) {
+    const SkMerge m = ml[e];
+    const int n = m.c_hi - m.c_lo + 1;
+    // the pieces' log-sum-exp vectors: into shared memory by one bulk copy
+    // each (1 KB), or read from global memory where more pieces than fit
+    const bool lse_smem = n <= kLseCap;
+    if (tid == 0 && lse_smem) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bar[V_FULL], n * MROWS * 4);
+      for (int c = m.c_lo; c <= m.c_hi; ++c)
+        bulk_g2s(lse_s + (c - m.c_lo) * MROWS, a.part_lse + static_cast<int64_t>(sk_slot(c, m.item_start, U, G)) * MROWS,
+                 MROWS * 4, &bar[V_FULL]);
     }
-    if (h == 0 && a.lse) a.lse[orow_i] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+    if (lse_smem && !mbar_wait(&bar[V_FULL], e & 1, a.wait_ns)) ok = false;
+    auto lse_of = [&](int c, int R) {
+      return lse_smem ? lse_s[(c - m.c_lo) * MROWS + R]
+                      : __ldcg(a.part_lse + static_cast<int64_t>(sk_slot(c, m.item_start, U, G)) * MROWS + R);
+    };
+    for (int t = 0; t < NQT; ++t) {
+      const int R = t * MT + r;
+      const int qi = R / g;
+      const bool rv = mt && ok && R < rows_used && qi < m.nq;
+      if (tid == 0) issue(q, m, m.c_lo, t);
+      float M = -INFINITY, W = 0.f;
+      if (rv) {
+        for (int c = m.c_lo; c <= m.c_hi; ++c) M = fmaxf(M, lse_of(c, R));
+        if (M == -INFINITY) M = 0.f;  // no key in any piece: every weight is 0
+        for (int c = m.c_lo; c <= m.c_hi; ++c) W += exp2f(lse_of(c, R) - M);
+      }
+      float acc[D / 2];
+#pragma unroll
+      for (int i = 0; i < D / 2; ++i) acc[i] = 0.f;
+      for (int c = m.c_lo; c <= m.c_hi; ++c, ++q) {
+        if (tid == 0 && c < m.c_hi) issue(q + 1, m, c + 1, t);
+        if (mt) {
+          const float w = rv ? exp2f(lse_of(c, R) - M) : 0.f;
+          if (!mbar_wait(&bar[K_FULL + (q & 1)], (q >> 1) & 1, a.wait_ns)) ok = false;
+          if (ok && rv) {
+            const float4 *x = reinterpret_cast<const float4 *>(buf0 + (q & 1) * TB);
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) {
+              const float4 y = x[(h * (D / 8) + k) * MT + r];
+              acc[4 * k] = __fmaf_rn(w, y.x, acc[4 * k]);
+              acc[4 * k + 1] = __fmaf_rn(w, y.y, acc[4 * k + 1]);
+              acc[4 * k + 2] = __fmaf_rn(w, y.z, acc[4 * k + 2]);
+              acc[4 * k + 3] = __fmaf_rn(w, y.w, acc[4 * k + 3]);
+            }
+          }
+        }
+        __syncthreads();  // the buffer is read: the copy after next may replace it
+      }
+      if (rv && ok) {
+        const float sc = W > 0.f ? m.vscale / W : 0.f;
+        const int64_t orow_i = static_cast<int64_t>(m.qs + m.qt0 + qi) * a.num_q_heads + m.kvh * g + (R - qi * g);
+        float *orow = a.out + orow_i * D + h * (D / 2);
+#pragma unroll
+        for (int i = 0; i < D / 2; i += 4)
+          *reinterpret_cast<float4 *>(orow + i) = make_float4(acc[i] * sc, acc[i + 1] * sc, acc[i + 2] * sc, acc[i + 3] * sc);
+        if (h == 0 && a.lse) a.lse[orow_i] = W > 0.f ? (M + log2f(W)) * kLn2 : -INFINITY;
+      }
+    }
+    __syncthreads();  // every read of the log-sum-exp vectors is done before the next merge's copies
+  }
+  // a wait that ran out: the copies still in flight land before the CTA exits
+  if (!__syncthreads_and(ok)) {
+    if (tid == 0) {
+      report_error(a.err, a.ws_err, kErrWaitTimeout);
+      for (int i = max(0, q - 2); i < q; ++i) mbar_wait(&bar[K_FULL + (i & 1)], (i >> 1) & 1, a.wait_ns);
+      mbar_wait(&bar[V_FULL], (nmerge - 1) & 1, a.wait_ns);
+    }
+    __syncthreads();
   }
 }
 
@@ -191,7 +244,6 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
   int *s_abort = reinterpret_cast<int *>(tmem_slot + 1);
   int *s_last_k = s_abort + 1;  // last KV iteration whose K copies the producer issued
   int *s_last_v = s_abort + 2;  // ... and whose V copies
-  int *s_flag = s_abort + 3;    // a piece: this CTA merges the item's pieces
   int *s_last_q = s_abort + 4;  // last segment whose Q tiles the producer copied by TMA
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -220,6 +272,7 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
     *s_last_k = -1;
     *s_last_v = -1;
     *s_last_q = -1;
+    *reinterpret_cast<int *>(smem + C::OFF_M) = 0;  // merges owed
     fence_mbar_init();
   }
   tc_fence_before_sync();
@@ -795,9 +848,9 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
           if (rv && h == 0 && a.lse) a.lse[orow_i] = (m_ref[t] + log2f(lt[t])) * kLn2;
         }
       } else {
-        // a piece: its normalised O ([D / 4][MROWS] float4, a warp's rows
-        // side by side) and its log-sum-exp (log2 units) to its slot
-        float4 *po = reinterpret_cast<float4 *>(a.part_o) + static_cast<int64_t>(sg.slot) * (D / 4) * MROWS;
+        // a piece: its normalised O ([Q tile][D / 4][MT] float4, a warp's
+        // rows side by side) and its log-sum-exp (log2 units) to its slot
+        float4 *po = reinterpret_cast<float4 *>(a.part_o) + static_cast<int64_t>(sg.slot) * NQT * (D / 4) * MT;
         float *pl = a.part_lse + static_cast<int64_t>(sg.slot) * MROWS;
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
@@ -815,7 +868,7 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
             if (rv) {
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                po[(c0 / 4 + k) * MROWS + R] = make_float4(__fmul_rn(o[4 * k], inv), __fmul_rn(o[4 * k + 1], inv),
+                po[(t * (D / 4) + c0 / 4 + k) * MT + r] = make_float4(__fmul_rn(o[4 * k], inv), __fmul_rn(o[4 * k + 1], inv),
                                                            __fmul_rn(o[4 * k + 2], inv), __fmul_rn(o[4 * k + 3], inv));
             }
           }
@@ -827,14 +880,14 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
         if (named_bar_and(9, 256, ok)) {
           if (tid == kSoftmaxWarp0 * 32) {
             const int prev = atom_add_acq_rel_gpu(a.part_count + sg.item, 1);
-            const int last = prev == sg.c_hi - sg.c_lo;
-            if (last) st_relaxed_gpu(a.part_count + sg.item, 0);  // ready for the next launch
-            *s_flag = last;
-          }
-          named_bar_sync(9, 256);
-          if (*s_flag) {
-            __threadfence();
-            sk_merge<D>(a, sg, qs, qt0, nq, kvh, r, h, vscale);
+            if (prev == sg.c_hi - sg.c_lo) {
+              // the item's last piece: this CTA merges them, once its
+              // pipeline has drained (sk_run_merges)
+              st_relaxed_gpu(a.part_count + sg.item, 0);  // ready for the next launch
+              int *nm = reinterpret_cast<int *>(smem + C::OFF_M);
+              SkMerge *ml = reinterpret_cast<SkMerge *>(smem + C::OFF_M + 16);
+              if (*nm < kMaxMerges) ml[(*nm)++] = SkMerge{sg.item_start, sg.c_lo, sg.c_hi, qs, qt0, nq, kvh, vscale};
+            }
           }
         } else {
           ok = false;
@@ -873,6 +926,13 @@ __device__ void prefill_run(const Args &a, uint8_t *smem, uint32_t tmem, const S
   }
   tc_fence_before_sync();
   __syncthreads();
+  // the merges this CTA owes (the pieces of other CTAs were complete when it
+  // counted its own: their stores precede their counts)
+  const int nmerge = *reinterpret_cast<volatile int *>(smem + C::OFF_M);
+  if (nmerge > 0 && !*s_abort) {
+    __threadfence();
+    sk_run_merges<D, KVT, PVM>(a, smem, it0.U, it0.G, nmerge);
+  }
 }
 
 // The balanced launch: one CTA per SM (see the file comment).  Each CTA

@@ -132,7 +132,7 @@ struct Args {
   // piece per CTA in a slot (two slots per CTA: its first and its last item)
   int num_seqs;
   int gx;               // query tiles per sequence
-  float *part_o;        // [2 G][D / 4][MROWS] float4: normalised O of a piece
+  float *part_o;        // [2 G][NQT][D / 4][MT] float4: normalised O of a piece
   float *part_lse;      // [2 G][MROWS]: its log-sum-exp, log2 units
   int *part_count;      // [num_seqs * gx * num_kv_heads] pieces finished per item
   int32_t *ws_err;      // the workspace's error word
@@ -268,7 +268,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NSK * KVB;  // [NSV]
   static constexpr int OFF_BAR = OFF_V + NSV * KVB;
   static constexpr int OFF_X = OFF_BAR + 256;          // softmax exchange: [2][MT] fp32
-  static constexpr int SMEM = OFF_X + 2 * MT * 4 + 1024;  // + 1024-B alignment slack
+  static constexpr int OFF_M = OFF_X + 2 * MT * 4;     // balanced launch: merges this CTA owes (128 B)
+  static constexpr int SMEM = OFF_M + 128 + 1024;      // + 1024-B alignment slack
   // at least half an SM's shared memory, so that two CTAs (each holding
   // all 512 TMEM columns) never share an SM
   static constexpr int SMEM_LAUNCH = SMEM > 120 * 1024 ? SMEM : 120 * 1024;
