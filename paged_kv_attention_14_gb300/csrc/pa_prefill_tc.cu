@@ -1,6 +1,6 @@
 // pa_prefill_tc.cu -- launches of the tcgen05 chunked-prefill kernels
 // (pa_prefill_tc.cuh): for pa_prefill_chunk and pa_prefix_attention one CTA
-// per (query tile, kv head, sequence or sequence x key split); for
+// per (kv head, sequence or sequence x key split, query tile); for
 // pa_prefill_chunk_balanced one CTA per SM sharing all items' KV iterations.
 #include "pa_prefill_sk.cuh"
 
@@ -18,6 +18,7 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
     return cudaErrorInvalidValue;
   const int qtiles = (max_q_len + a.qt - 1) / a.qt;
   if (qtiles == 0 || num_seqs == 0) return cudaSuccess;
+  if (qtiles > 65535 || static_cast<long long>(num_seqs) * a.num_splits > 65535) return cudaErrorInvalidConfiguration;
   auto fn = &prefill_tc_kernel<D, KVT, PVM>;
   if (prepare_kernel(reinterpret_cast<const void *>(fn), NTHREADS, Cfg<D, KVT, PVM>::SMEM_LAUNCH) < 1)
     return cudaErrorInvalidConfiguration;
@@ -25,7 +26,8 @@ cudaError_t launch(const pa_kv_desc &d, float *out, float *lse, const void *q, c
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(qtiles, d.num_kv_heads, num_seqs * a.num_splits);
+  // longest key ranges first across the grid: the query tile is the slowest index
+  cfg.gridDim = dim3(d.num_kv_heads, num_seqs * a.num_splits, qtiles);
   cfg.blockDim = dim3(NTHREADS);
   cfg.dynamicSmemBytes = Cfg<D, KVT, PVM>::SMEM_LAUNCH;
   cfg.stream = stream;

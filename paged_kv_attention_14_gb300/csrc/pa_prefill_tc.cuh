@@ -327,6 +327,17 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
   const int split = sg.split;
   const int s = sg.s;
   const int kvh = sg.kvh;
+  // where the first key is 0 (chunk mode, no local attention, the item's
+  // first tile), the producer loads the first tile's block ids at once,
+  // beside the lengths instead of after them
+  const bool spec_ok = !a.prefix_mode && a.window == 0 && a.chunk == 0 && sg.it_lo == 0;
+  int spec = 0;
+  {
+    constexpr int BOXES = C::KV8 ? 1 : C::HALVES;
+    const int l = threadIdx.x & 31, b = l / BOXES;
+    if (spec_ok && (threadIdx.x >> 5) == kProducerWarp && l < BPT * BOXES && b < a.max_blocks_per_seq)
+      spec = __ldg(a.block_tables + static_cast<int64_t>(s) * a.max_blocks_per_seq + b);
+  }
   ItemRange ir;
   if (!item_range(a, s, split, sg.qtile, sg.gx, true, ir)) return;
   const int qs = ir.qs;
@@ -412,7 +423,9 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
   if (qtma_tiles != 0) __syncthreads();  // the barriers are set up
   if (warp == kProducerWarp) {
     // the first KV tile's block ids load while Q is set up
-    if (issuer && (j0 * BPT + bi) * 16 < kv_end) phys_next = block_id(j0 * BPT + bi);
+    if (issuer && (j0 * BPT + bi) * 16 < kv_end)
+      phys_next = spec_ok ? (a.checked ? checked_block(spec, a.num_blocks, a.err, a.ws_err) : spec)
+                          : block_id(j0 * BPT + bi);
     if (qtma_tiles != 0 && lane == 0 && !a.stall) {
       const uint64_t pol = l2_evict_first_policy();
       mbar_arrive_expect_tx(&bar[Q_FULL], __popc(qtma_tiles) * C::QB);
@@ -1049,7 +1062,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  prefill_tile<D, KVT, PVM>(a, smem, tmem, blockIdx.x, blockIdx.y, blockIdx.z, gridDim.x);
+  // grid (kv heads, sequences x splits, query tiles): the CTAs are issued
+  // with every item's longest key range first across the whole grid
+  prefill_tile<D, KVT, PVM>(a, smem, tmem, blockIdx.z, blockIdx.x, blockIdx.y, gridDim.z);
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kMmaWarp) {
