@@ -65,9 +65,9 @@ NCU_TRAFFIC = {
                "sha256": "9dab5f410c2821164ca2057a06aaf1a2a5cf2ec7d48f8e15b5a73c2a18088b18",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 46,223,104 + dram__bytes_write.sum 1,207,808
-    "prefill": {"workload": 5, "bytes": 47_430_912,
-                "sha256": "8e48aba24bca5f8e03097a8c595c77a3b3435dc6fd23f20c84bcacc028ba2d93",
+    # dram__bytes_read.sum 49,322,752 + dram__bytes_write.sum 1,985,024
+    "prefill": {"workload": 5, "bytes": 51_307_776,
+                "sha256": "ad174e4d76ca2c5ec166b436b641a72d14dccf6f573bb12c812337b591343b77",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
