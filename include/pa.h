@@ -81,7 +81,7 @@ extern "C" {
  *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
  *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention.
  * 4: pa_prefill_workspace_size, pa_prefill_chunk_balanced,
- *    pa_test_prefill_schedule. */
+ *    pa_prefill_balanced_chosen, pa_test_prefill_schedule. */
 #define PA_ABI_VERSION 4
 
 /* Symbols of the shared library; everything else in it stays hidden. */
@@ -317,6 +317,17 @@ PA_API size_t pa_prefill_workspace_size(const pa_kv_desc *desc, int32_t num_seqs
  *   workspace : pa_prefill_workspace_size(desc, num_seqs, max_q_len) bytes,
  *               16-byte aligned, zero-filled before its first use.
  */
+/*
+ * Which kernel pa_prefill_chunk_balanced runs for a batch of num_seqs chunks
+ * of at most max_q_len queries over contexts of at most max_context_len
+ * tokens (tables of max_blocks_per_seq blocks): 1 the balanced kernel, 0
+ * pa_prefill_chunk's grid, -1 for an invalid descriptor or arguments.  A
+ * caller that schedules a step can use it to keep such a prefill out of a
+ * single-launch step (see pa_mixed_attention).  Host only; enqueues nothing.
+ */
+PA_API int32_t pa_prefill_balanced_chosen(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len,
+                                          int32_t max_context_len, int32_t max_blocks_per_seq);
+
 PA_API pa_status pa_prefill_chunk_balanced(const pa_kv_desc *desc, float *out, float *lse, const void *q,
                                            const int32_t *query_start_loc, const void *k_cache,
                                            const void *v_cache, const int32_t *block_tables,

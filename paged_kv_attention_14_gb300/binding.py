@@ -51,7 +51,7 @@ EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_work
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
             "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
             "pa_mixed_workspace_size", "pa_mixed_attention", "pa_prefill_workspace_size",
-            "pa_prefill_chunk_balanced", "pa_test_prefill_schedule")
+            "pa_prefill_chunk_balanced", "pa_test_prefill_schedule", "pa_prefill_balanced_chosen")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -114,6 +114,8 @@ def load(path: Optional[str] = None):
         lib.pa_prefill_workspace_size.restype = SZ
         lib.pa_prefill_chunk_balanced.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P, SZ, P]
         lib.pa_prefill_chunk_balanced.restype = ctypes.c_int
+        lib.pa_prefill_balanced_chosen.argtypes = [D, I32, I32, I32, I32]
+        lib.pa_prefill_balanced_chosen.restype = I32
         lib.pa_prefix_attention.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, F, P]
         lib.pa_prefix_attention.restype = ctypes.c_int
         lib.pa_copy_blocks.argtypes = [D, P, P, P, P, I32, P]
@@ -323,6 +325,16 @@ def pa_prefill_workspace_size(desc: PaKvDesc, num_seqs: int, max_q_len: int) -> 
     if n == 0:
         raise PaError(PA_ERR_INVALID_ARG, last_error())
     return n
+
+
+def pa_prefill_balanced_chosen(desc: PaKvDesc, num_seqs: int, max_q_len: int, max_context_len: int,
+                               max_blocks_per_seq: int) -> bool:
+    """Whether pa_prefill_chunk_balanced runs the balanced kernel for such a batch."""
+    r = load().pa_prefill_balanced_chosen(ctypes.byref(desc), int(num_seqs), int(max_q_len), int(max_context_len),
+                                          int(max_blocks_per_seq))
+    if r < 0:
+        raise PaError(PA_ERR_INVALID_ARG, "invalid descriptor or batch shape")
+    return bool(r)
 
 
 def prefill_workspace(desc: PaKvDesc, num_seqs: int, max_q_len: int, device=None) -> torch.Tensor:

@@ -75,12 +75,19 @@ namespace pa {
 
 void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 
+bool prefill_balanced_chosen(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
+                             int32_t max_blocks_per_seq) {
+  // the balanced kernel where it applies and pays (or as the test hook says)
+  const int forced = g_test_schedule.load(std::memory_order_relaxed);
+  return prefill_sk_applies(d, num_seqs, max_q_len) && prefill_sk_units_fit(d, num_seqs, max_q_len, max_blocks_per_seq) &&
+         (forced == 1 || (forced == 0 && prefill_sk_pays(d, num_seqs, max_q_len, max_context_len)));
+}
+
 TestHooks test_hooks() {
   TestHooks h;
   h.stall = g_test_stall.load(std::memory_order_relaxed);
   const unsigned long long w = g_test_wait_ns.load(std::memory_order_relaxed);
   h.wait_ns = (h.stall && w) ? w : kDefaultWaitNs;
-  h.prefill_schedule = g_test_schedule.load(std::memory_order_relaxed);
   return h;
 }
 
@@ -214,6 +221,17 @@ pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse, const
   return e == cudaSuccess ? ok() : cuda_fail(e);
 }
 
+int32_t pa_prefill_balanced_chosen(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len,
+                                   int32_t max_context_len, int32_t max_blocks_per_seq) {
+  if (check_desc(desc) != PA_OK) return -1;
+  const char *why = "";
+  if (num_seqs < 0 || max_q_len < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 ||
+      pa::check_prefill(*desc, &why) != PA_OK)
+    return -1;
+  if (num_seqs == 0 || max_q_len == 0) return 0;
+  return pa::prefill_balanced_chosen(*desc, num_seqs, max_q_len, max_context_len, max_blocks_per_seq) ? 1 : 0;
+}
+
 size_t pa_prefill_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len) {
   if (check_desc(desc) != PA_OK || num_seqs < 0 || max_q_len < 0) return 0;
   const char *why = "";
@@ -240,12 +258,7 @@ pa_status pa_prefill_chunk_balanced(const pa_kv_desc *desc, float *out, float *l
   if (workspace_bytes < pa::prefill_sk_workspace_bytes(*desc, num_seqs, max_q_len))
     return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_prefill_workspace_size()%s");
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the balanced kernel where it applies and pays (or as the test hook says)
-  const int forced = pa::test_hooks().prefill_schedule;
-  const bool balanced =
-      pa::prefill_sk_applies(*desc, num_seqs, max_q_len) &&
-      pa::prefill_sk_units_fit(*desc, num_seqs, max_q_len, max_blocks_per_seq) &&
-      (forced == 1 || (forced == 0 && pa::prefill_sk_pays(*desc, num_seqs, max_q_len, max_context_len)));
+  const bool balanced = pa::prefill_balanced_chosen(*desc, num_seqs, max_q_len, max_context_len, max_blocks_per_seq);
   const cudaError_t e =
       balanced
           ? pa::launch_prefill_tc_sk(*desc, out, lse, q, query_start_loc, k_cache, v_cache, block_tables,

@@ -107,6 +107,9 @@ bool prefill_sk_units_fit(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_l
 // SMs, with contexts long enough that the SMs the grid leaves idle cost more
 // than the pieces' partial outputs and merges.
 bool prefill_sk_pays(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len, int32_t max_context_len);
+// pa_prefill_chunk_balanced's choice: the balanced kernel (true) or the grid
+bool prefill_balanced_chosen(const pa_kv_desc &d, int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
+                             int32_t max_blocks_per_seq);
 cudaError_t launch_prefill_tc_sk(const pa_kv_desc &d, float *out, float *lse, const void *q,
                                  const int32_t *query_start_loc, const void *k_cache, const void *v_cache,
                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -136,7 +139,6 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 struct TestHooks {
   int stall;
   unsigned long long wait_ns;
-  int prefill_schedule;  // pa_test_prefill_schedule: 0 the library's choice, 1 balanced, 2 grid
 };
 TestHooks test_hooks();
 

@@ -16,7 +16,14 @@ concurrently.  Three ways to issue them (``mode``):
   * "fused"  -- one launch of pa_mixed_attention: one persistent kernel whose
                 CTAs take the prefill tiles and then the decode partitions
                 from one work list (with both parts present and a descriptor
-                it takes; "streams" otherwise);
+                it takes; "streams" otherwise).  A prefill of a few long
+                chunks would leave most SMs idle there: given a prefill
+                workspace, a step whose prefill has at most half as many
+                (query tile, kv head) items as there are SMs, and which
+                pa_prefill_chunk_balanced would run on its balanced kernel
+                (pa_prefill_balanced_chosen), runs the decode and then that
+                prefill instead (with more items the fused launch's decode
+                fills the SMs the prefill leaves);
   * "streams" -- the decode on a second stream that waits for the write,
                 beside the prefill on the caller's stream, so that the
                 decode's CTAs take the SMs the prefill's last wave leaves idle;
@@ -58,6 +65,7 @@ class MixedStep:
         self.prefill_out, self.prefill_lse = prefill_out, prefill_lse
         self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
         self.prefill_workspace = prefill_workspace
+        self._balanced = {}  # (prefill sequences, table width) -> the balanced prefill runs
         both = decode_out is not None and prefill_out is not None
         fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
                     and desc.decode_impl in (B.PA_DECODE_AUTO, B.PA_DECODE_MMA)
@@ -90,8 +98,31 @@ class MixedStep:
                            block_tables, context_lens, self.max_q_len, self.max_context_len_prefill, self.scale,
                            lse=self.prefill_lse, stream=stream)
 
+    def prefill_balanced(self, pf_args) -> bool:
+        """Whether this step's prefill runs pa_prefill_chunk_balanced's balanced
+        kernel (a prefill workspace given and the library's choice)."""
+        if self.prefill_workspace is None or pf_args is None or self.prefill_out is None:
+            return False
+        key = (int(pf_args[3].shape[0]), int(pf_args[2].shape[1]))
+        if key not in self._balanced:
+            # items as the prefill kernels count them: 256 (query, head) rows of one kv head
+            g = self.desc.num_q_heads // self.desc.num_kv_heads
+            qt = 256 // g
+            items = key[0] * ((self.max_q_len + qt - 1) // qt) * self.desc.num_kv_heads
+            sms = torch.cuda.get_device_properties(self.k_cache.device).multi_processor_count
+            self._balanced[key] = (2 * items <= sms and
+                                   B.pa_prefill_balanced_chosen(self.desc, key[0], self.max_q_len,
+                                                                self.max_context_len_prefill, key[1]))
+        return self._balanced[key]
+
     def attend(self, dec_args, pf_args):
         """Decode and prefill after a cache write already issued on the current stream."""
+        if self.mode == "fused" and self.prefill_balanced(pf_args):
+            # a few long prefill chunks: the balanced kernel on every SM, after the decode
+            if dec_args is not None and self.decode_out is not None:
+                self.decode(*dec_args)
+            self.prefill(*pf_args)
+            return
         if self.mode == "fused":
             dec = None
             if dec_args is not None and self.decode_out is not None:

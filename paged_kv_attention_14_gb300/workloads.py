@@ -300,10 +300,20 @@ def workload(n: int, device="cpu", poison: bool = False, fp8_format: str = KV_FP
 
 
 def _mixed_batch(seed, device, poison, kv_dtype=KV_BF16, name=WORKLOAD_NAMES[5]) -> PagedBatch:
+    return mixed_batch(seed, device, poison, kv_dtype, name=name)
+
+
+def mixed_batch(seed, device="cpu", poison: bool = False, kv_dtype=KV_BF16, name="mixed continuous-batch step",
+                n_dec: int = 16, dec_range=(256, 4096), n_pf: int = 4, prefix: int = 2048, chunk: int = 512,
+                shared: int = 1024) -> PagedBatch:
+    """One continuous-batch step: n_dec decode sequences with context
+    lengths U[dec_range], and n_pf prefill chunks of `chunk` new tokens on
+    `prefix`-token prefixes whose first `shared` tokens sit in the same
+    physical blocks for every chunk (a prefix-cache hit); 32 q / 8 kv heads,
+    head_dim 128.  With the defaults this is workload 5."""
     Hq, Hkv, D, B = 32, 8, 128, BLOCK_SIZE
     g_cpu = _gen(seed, "cpu")
-    dec_lens = torch.randint(256, 4096 + 1, (16,), generator=g_cpu).to(torch.int32)
-    n_pf, prefix, chunk, shared = 4, 2048, 512, 1024
+    dec_lens = torch.randint(dec_range[0], dec_range[1] + 1, (n_dec,), generator=g_cpu).to(torch.int32)
     pf_len = prefix + chunk
     shared_blocks = shared // B
     own_blocks = (pf_len - shared) // B
@@ -338,7 +348,7 @@ def _mixed_batch(seed, device, poison, kv_dtype=KV_BF16, name=WORKLOAD_NAMES[5])
                    k_pool=None, v_pool=None)
     g = _gen(seed + 7, device)
     act = act_dtype(kv_dtype)
-    b.q_decode = _randn((16, Hq, D), g, device, act)
+    b.q_decode = _randn((n_dec, Hq, D), g, device, act)
     b.q_prefill = _randn((n_pf * chunk, Hq, D), g, device, act)
     b.k_new = _randn((T, Hkv, D), g, device, act)
     b.v_new = _randn((T, Hkv, D), g, device, act)

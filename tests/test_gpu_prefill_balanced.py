@@ -237,3 +237,43 @@ def test_balanced_prefill_checked_indices(corrupt):
     else:
         assert int(ew[0]) == B.PA_DEVERR_BAD_INDEX
         assert int(ws.view(torch.int32)[0]) == B.PA_DEVERR_BAD_INDEX
+
+
+def test_mixed_step_with_a_long_chunk_runs_the_balanced_prefill():
+    """A continuous-batch step whose prefill is one chunk of 512 new tokens on
+    a 7680-token prefix (64 items, fewer than the SMs) beside 8 decode
+    sequences: MixedStep "fused" with a prefill workspace runs the decode and
+    then the balanced prefill (the library's choice), and both parts match
+    the oracle; the cache write bit for bit."""
+    from paged_kv_attention_14_gb300.step import MixedStep
+    B.pa_test_prefill_schedule(0)
+    b = W.mixed_batch(801, device=DEV, poison=True, n_dec=8, dec_range=(256, 2048), n_pf=1, prefix=7680,
+                      chunk=512, shared=0)
+    d = desc_of(b)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    ws = B.mixed_workspace(d, S, maxL, DEV)
+    pws = B.prefill_workspace(d, 1, 512, DEV)
+    dec_out = torch.full((S, 32, 128), float("nan"), device=DEV)
+    pf_out = torch.full((512, 32, 128), float("nan"), device=DEV)
+    pf_lse = torch.full((512, 32), float("nan"), device=DEV)
+    qsl = b.query_start_loc
+    ms = MixedStep(d, kc, vc, b.scale, decode_out=dec_out, workspace=ws, max_context_len_decode=maxL,
+                   prefill_out=pf_out, prefill_lse=pf_lse, max_q_len=512, max_context_len_prefill=8192,
+                   mode="fused", prefill_workspace=pws)
+    pf_args = (b.q_prefill, qsl, b.block_tables_prefill, b.context_lens_prefill)
+    assert ms.mode == "fused" and ms.prefill_balanced(pf_args)
+    ms(b.k_new, b.v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode), pf_args)
+    torch.cuda.synchronize()
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, 8, 128, b.k_new.cpu(), b.v_new.cpu(), b.slot_mapping.cpu(),
+                                b.k_pool.cpu(), b.v_pool.cpu())
+    assert np.array_equal(kc.view(torch.int16).cpu().numpy().view(np.uint16), ok)
+    oc = (oracle.KV_BF16, ok, ov)
+    from pa_helpers import oracle_decode
+    o_ref, _ = oracle_decode(b, ocaches=oc)
+    assert_close(dec_out, o_ref, TOL[b.kv_dtype], "decode out")
+    o_ref, l_ref = oracle_prefill(b, ocaches=oc)
+    assert_close(pf_out, o_ref, TOL[b.kv_dtype], "prefill out")
+    assert_close(pf_lse, l_ref, LSE_TOL[b.kv_dtype], "prefill lse")
+    assert _counters_clear(pws, b)
