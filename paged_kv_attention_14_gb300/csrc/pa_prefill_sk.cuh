@@ -8,12 +8,13 @@
 // length run in ceil(n / SMs) waves, and the last wave may leave SMs idle.
 //
 // How (GB300 design):
-//  * A unit is one 128-key KV tile of one item.  Items are ordered by pair
-//    (sequence, query tile), then kv head; CTA c of G takes units
+//  * A unit is one 128-key KV tile of one item.  Items are ordered by kv
+//    head, then pair (sequence, query tile); CTA c of G takes units
 //    [c U / G, (c + 1) U / G) (a stream-K decomposition).  An item whose
 //    units fall to several CTAs is computed in pieces.  Each piece leaves its
-//    normalised output and log-sum-exp in a slot of the workspace, and the
-//    piece that finishes last merges them all by log-sum-exp.
+//    normalised output and log-sum-exp in a slot of the workspace; the CTA
+//    that finishes the last piece merges them all by log-sum-exp once its
+//    own pipeline has drained.
 //  * Each CTA runs its items ("segments") as one continuous pipeline.  The
 //    K/V rings and every barrier keep counting across segments.  The
 //    producer loads a segment's first K tiles while the previous one is
@@ -35,19 +36,19 @@ namespace pftc {
 
 // One CTA's segments, in the order it runs them: the range's last item
 // first when it runs on into the next CTA and is not also the range's first
-// (so that its two pieces finish early and its merge does not trail the
-// launch), then the range from its first unit.  Units are ordered by kv
-// head, then pair (sequence, query tile), then iteration, so that
-// neighbouring CTAs read the same sequence's K/V of one kv head at about the
-// same time.  Every thread of the CTA walks its own copy; all copies yield
-// the same segments.
+// (the neighbour starts its own piece of that item at once, so both pieces
+// of the item are in flight together), then the range from its first unit.
+// Units are ordered by kv head, then pair (sequence, query tile), then
+// iteration, so that neighbouring CTAs read the same sequence's K/V of one
+// kv head at about the same time.  Every thread of the CTA walks its own
+// copy; all copies yield the same segments.
 struct SkIter {
   int u, ub;  // walk: next unit, end (the range's end, or zs)
   int u1;     // the range's end
   int base;   // the first unit of item (p, kvh)
   int zs;     // the first unit of the item run first
   int U;      // units of the launch (the host keeps it below 2^31)
-  int T;            // units per kv head (all pairs' iterations)
+  int T;      // units per kv head (all pairs' iterations)
   int p, np, kvh, it;  // walk: pair, its iterations, kv head, iteration
   int pz, nz, kvz;     // the item run first: pair, iterations, kv head
   int z_first;         // it is still to run
