@@ -258,6 +258,29 @@ def test_prefill_argument_errors(lib):
                                 2, 8, 16, 0.1, None) == B.PA_ERR_INVALID_ARG
 
 
+def test_balanced_prefill_argument_errors(lib):
+    d = _desc()
+    args = (0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 4, 0x7000)
+    # nothing to do: no workspace needed
+    assert lib.pa_prefill_chunk_balanced(ctypes.byref(d), *args, 0, 8, 16, 0.1, None, 0, None) == B.PA_OK
+    # the workspace is required, 16-byte aligned, and checked after the other arguments
+    assert lib.pa_prefill_chunk_balanced(ctypes.byref(d), *args, 2, 8, 16, 0.1, None, 1 << 20,
+                                         None) == B.PA_ERR_WORKSPACE
+    assert lib.pa_prefill_chunk_balanced(ctypes.byref(d), *args, 2, 8, 16, 0.1, 0x8008, 1 << 20,
+                                         None) == B.PA_ERR_WORKSPACE
+    assert lib.pa_prefill_chunk_balanced(ctypes.byref(d), *args, 2, 8, 100, 0.1, None, 0,
+                                         None) == B.PA_ERR_INVALID_ARG
+    # the schedule query and the sizes reject invalid descriptors; an empty batch runs nothing
+    bad = _desc(head_dim=96)
+    assert lib.pa_prefill_balanced_chosen(ctypes.byref(bad), 2, 8, 16, 4) == -1
+    assert lib.pa_prefill_workspace_size(ctypes.byref(bad), 2, 8) == 0
+    assert lib.pa_prefill_balanced_chosen(ctypes.byref(d), 0, 8, 16, 4) == 0
+    assert lib.pa_prefill_balanced_chosen(ctypes.byref(d), 2, 8, -1, 4) == -1
+    # the test hook takes 0, 1 or 2
+    assert lib.pa_test_prefill_schedule(3) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_test_prefill_schedule(0) == B.PA_OK
+
+
 def test_merge_argument_errors(lib):
     assert lib.pa_merge_partials(0x1000, None, 0x2000, 0x3000, None, 0, 4, 2, 64, None) == B.PA_OK
     assert lib.pa_merge_partials(0x1000, None, 0x2000, 0x3000, None, 2, 4, 2, 66, None) == B.PA_ERR_UNSUPPORTED
