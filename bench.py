@@ -1,10 +1,11 @@
 """Benchmark of the paged-attention hot path on one GB300 (or N replicas).
 
 A step is one pass of the decode hot path over one batch of synthetic input:
-the slot-mapped cache write of each sequence's new token (pa_cache_write),
-then split-KV decode attention over the block-paged cache (pa_decode: the
-decode kernel and the merge kernel of segments split across CTAs).  The
-workload is the Qwen3-8B-shaped decode step: 32 sequences with context
+the write of each sequence's new token into the paged cache and split-KV
+decode attention over the block-paged cache, in one launch
+(pa_decode_append; segments split across CTAs are merged inside it).  With
+``--separate-write`` the step is the two calls pa_cache_write and pa_decode.
+The workload is the Qwen3-8B-shaped decode step: 32 sequences with context
 lengths ~ U[512, 4096], 32 query / 8 kv heads, head_dim 128, block size 16,
 bf16 KV ~ N(0, 1), random non-contiguous block tables from a pool of 1.25x
 the blocks needed (seed 1002).
@@ -59,10 +60,12 @@ MIN_TIMED_S = 0.5
 # source files hash to what they were when it was captured.
 CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
-    # the decode kernel (split segments are merged inside it):
-    # dram__bytes_read.sum 305,458,176 + dram__bytes_write.sum 3,253,760
-    "decode": {"workload": 2, "bytes": 308_711_936,
-               "sha256": "9dab5f410c2821164ca2057a06aaf1a2a5cf2ec7d48f8e15b5a73c2a18088b18",
+    # the decode kernel as the bench launches it, with the step's cache write
+    # fused in (pa_decode_append; split segments are merged inside it):
+    # dram__bytes_read.sum 305,593,344 + dram__bytes_write.sum 3,265,024
+    # (the timed pa_decode launch writes no appended rows: 131 KB, 0.04%, less)
+    "decode": {"workload": 2, "bytes": 308_858_368,
+               "sha256": "93177ee9f2a4e173fc470a3e8a914b68377597354cb5142e3dc96bb963482ee4",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
     # dram__bytes_read.sum 49,322,752 + dram__bytes_write.sum 1,985,024
@@ -405,10 +408,14 @@ def run_ours(args):
     if mixed and args.prefill_entry == "balanced":
         pf_ws = B.prefill_workspace(desc, int(b.context_lens_prefill.shape[0]), pf_maxq, dev)
     pf_entry = "pa_prefill_chunk_balanced" if pf_ws is not None else "pa_prefill_chunk"
+    # a decode-only step whose new rows are one token per sequence (every
+    # decode workload) appends them in the decode launch (pa_decode_append)
+    # where the library takes it, unless --separate-write
+    append = not mixed and not args.separate_write
     ms = MixedStep(desc, kc, vc, b.scale, decode_out=out, workspace=wsp, max_context_len_decode=maxL,
                    prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
                    max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode,
-                   prefill_workspace=pf_ws)
+                   prefill_workspace=pf_ws, decode_append=append)
     decode, prefill, attend = ms.decode, ms.prefill, ms.attend
     if ms.mode == "fused":
         launches_per_step = 2
@@ -423,6 +430,11 @@ def run_ours(args):
             flush()
         step()
     torch.cuda.synchronize()
+    if ms.decode_append:
+        launches_per_step = 1  # the write and the decode in one launch
+    step_how = ("pa_decode_append (the step's cache write and decode in one launch)" if ms.decode_append else
+                "pa_cache_write, then " + ("pa_mixed_attention" if ms.mode == "fused" and mixed else
+                                          "pa_decode" + (" and the prefill" if mixed else "")))
 
     K = args.steps
     # A repeat times exactly K steps.  The K-step measurement is repeated
@@ -619,6 +631,7 @@ def run_ours(args):
                            "inputs, the cache write and attention, and the copy of the outputs to pinned host memory, "
                            "then a wait; host wall clock"},
             # timed region 2 calls each entry point alone: decode (and prefill)
+            "step_calls": step_how,
             "gpu_launches": launches_per_step * K * R + (2 if mixed else 1) * K2 * R2,
             "timed_repeats": {"steps": R, "kernels_alone": R2,
                               "note": f"each repeat times exactly {K} steps ({K2} calls of each entry point alone); "
@@ -803,6 +816,8 @@ def main():
     ap.add_argument("--prefill-entry", choices=["chunk", "balanced"], default="chunk",
                     help="prefill entry point: pa_prefill_chunk (a CTA per query tile and kv head) or "
                          "pa_prefill_chunk_balanced (the library's choice of that grid or the balanced kernel)")
+    ap.add_argument("--separate-write", action="store_true",
+                    help="decode-only workloads: pa_cache_write then pa_decode instead of pa_decode_append")
     ap.add_argument("--mixed-mode", choices=["fused", "streams", "serial"], default="fused",
                     help="mixed step (workload 5): one persistent launch, two streams, or one after the other")
     ap.add_argument("--per-head-scales", action="store_true",

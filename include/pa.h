@@ -81,7 +81,7 @@ extern "C" {
  *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
  *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention.
  * 4: pa_prefill_workspace_size, pa_prefill_chunk_balanced,
- *    pa_prefill_balanced_chosen, pa_test_prefill_schedule. */
+ *    pa_prefill_balanced_chosen, pa_test_prefill_schedule, pa_decode_append. */
 #define PA_ABI_VERSION 4
 
 /* Symbols of the shared library; everything else in it stays hidden. */
@@ -284,6 +284,36 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
                            int32_t max_blocks_per_seq, const int32_t *context_lens,
                            int32_t num_seqs, int32_t max_q_len, int32_t max_context_len,
                            float scale, pa_stream_t stream);
+
+/*
+ * A decode step's cache write and decode attention in one launch: the decode
+ * half of one pass of the engine loop (the "C++20 Continuous Batching Loop"
+ * figure of "Building and Deploying vllm.cpp ...": the new token's K/V go into
+ * the paged cache, then attention reads the sequence's whole context).
+ * Sequence s appends one token at position context_lens[s] - 1 (context_lens
+ * already count it), whose K and V rows are k_new[s] and v_new[s]: the call writes
+ * them into the caches at that position through block_tables (what
+ * pa_cache_write does for those slots) and computes pa_decode's output over
+ * all context_lens[s] tokens, the appended one included.  The kernel puts
+ * the new rows into the tiles it stages as it reads each sequence's last
+ * block, so the attention does not wait for a separate write.
+ *   k_new, v_new : [num_seqs][num_kv_heads][head_dim] in the cache's type,
+ *                  16-byte aligned; a sequence with context length 0 appends
+ *                  nothing.
+ *   the other arguments are pa_decode's (workspace: pa_decode_workspace_size).
+ * Takes bf16 and fp16 caches on the tensor-core decode kernel
+ * (PA_ERR_UNSUPPORTED otherwise: call pa_cache_write and pa_decode).  Errors
+ * found on the host (pa_decode's, NULL or misaligned k_new / v_new:
+ * PA_ERR_INVALID_ARG; PA_ERR_UNSUPPORTED; PA_ERR_WORKSPACE) return before
+ * anything is enqueued.  With check_indices, an out-of-range block id of a
+ * last block is reported and its row is not written.  Two sequences whose
+ * last tokens share a slot race, as duplicate slots of pa_cache_write do.
+ */
+PA_API pa_status pa_decode_append(const pa_kv_desc *desc, float *out, float *lse, const void *q, const void *k_new,
+                                  const void *v_new, void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                                  pa_stream_t stream);
 
 /*
  * Bytes of scratch that pa_prefill_chunk_balanced needs for num_seqs chunks

@@ -51,7 +51,8 @@ EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_work
             "pa_decode", "pa_prefill_chunk", "pa_merge_partials", "pa_decode_static", "pa_prefix_attention",
             "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
             "pa_mixed_workspace_size", "pa_mixed_attention", "pa_prefill_workspace_size",
-            "pa_prefill_chunk_balanced", "pa_test_prefill_schedule", "pa_prefill_balanced_chosen")
+            "pa_prefill_chunk_balanced", "pa_test_prefill_schedule", "pa_prefill_balanced_chosen",
+            "pa_decode_append")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -108,6 +109,8 @@ def load(path: Optional[str] = None):
         lib.pa_decode_workspace_size.restype = SZ
         lib.pa_decode.argtypes = [D, P, P, P, P, P, P, I32, P, I32, I32, F, P, SZ, P]
         lib.pa_decode.restype = ctypes.c_int
+        lib.pa_decode_append.argtypes = [D, P, P, P, P, P, P, P, P, I32, P, I32, I32, F, P, SZ, P]
+        lib.pa_decode_append.restype = ctypes.c_int
         lib.pa_prefill_chunk.argtypes = [D, P, P, P, P, P, P, P, I32, P, I32, I32, I32, F, P]
         lib.pa_prefill_chunk.restype = ctypes.c_int
         lib.pa_prefill_workspace_size.argtypes = [D, I32, I32]
@@ -254,6 +257,22 @@ def pa_decode(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_le
                             _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
                             float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
                             workspace.numel(), _stream(stream)))
+
+
+def pa_decode_append(desc: PaKvDesc, out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                     max_context_len: int, scale: float, workspace, lse=None, stream=None):
+    """One decode step in one launch: sequence s's new token (k_new[s], v_new[s],
+    ``[S, Hkv, D]``) goes into the caches at position context_lens[s] - 1, and the
+    decode attends over all context_lens[s] tokens."""
+    S = int(context_lens.shape[0])
+    _check(load().pa_decode_append(ctypes.byref(desc), _ptr(out, _F32, "out"),
+                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
+                                   _ptr(k_new, _act(desc), "k_new"), _ptr(v_new, _act(desc), "v_new"),
+                                   _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                   _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
+                                   _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
+                                   float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
+                                   workspace.numel(), _stream(stream)))
 
 
 def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_lens,

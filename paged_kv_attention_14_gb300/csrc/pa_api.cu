@@ -232,6 +232,37 @@ int32_t pa_prefill_balanced_chosen(const pa_kv_desc *desc, int32_t num_seqs, int
   return pa::prefill_balanced_chosen(*desc, num_seqs, max_q_len, max_context_len, max_blocks_per_seq) ? 1 : 0;
 }
 
+pa_status pa_decode_append(const pa_kv_desc *desc, float *out, float *lse, const void *q, const void *k_new,
+                           const void *v_new, void *k_cache, void *v_cache, const int32_t *block_tables,
+                           int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
+                           int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                           pa_stream_t stream) {
+  static const char *kNotTaken =
+      "pa_decode_append takes bf16 and fp16 caches on the tensor-core decode kernel (make the pa_cache_write and "
+      "pa_decode calls instead)%s";
+  // the checks that need no device come first
+  pa_status st = check_desc(desc);
+  if (st != PA_OK) return st;
+  if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+    return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be non-NULL and 16-byte aligned%s");
+  if (num_seqs > 0 && desc->kv_dtype != PA_KV_BF16 && desc->kv_dtype != PA_KV_F16)
+    return fail(PA_ERR_UNSUPPORTED, kNotTaken);
+  pa::DecodePlan plan;
+  st = pa::validate_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                           num_seqs, max_context_len, scale, &plan);
+  if (st != PA_OK) return st;
+  if (num_seqs == 0) return ok();
+  if (plan.impl != PA_DECODE_MMA) return fail(PA_ERR_UNSUPPORTED, kNotTaken);
+  if (!workspace || !aligned16(workspace))
+    return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
+  if (workspace_bytes < plan.workspace_bytes)
+    return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_decode_workspace_size()%s");
+  const cudaError_t e = pa::launch_decode(*desc, plan, out, lse, q, k_cache, v_cache, block_tables,
+                                          max_blocks_per_seq, context_lens, num_seqs, scale, workspace,
+                                          reinterpret_cast<cudaStream_t>(stream), k_new, v_new);
+  return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
 size_t pa_prefill_workspace_size(const pa_kv_desc *desc, int32_t num_seqs, int32_t max_q_len) {
   if (check_desc(desc) != PA_OK || num_seqs < 0 || max_q_len < 0) return 0;
   const char *why = "";

@@ -211,12 +211,18 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
                           const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           const int32_t *context_lens, int32_t num_seqs, float scale,
-                          void *workspace, cudaStream_t stream) {
+                          void *workspace, cudaStream_t stream, const void *k_new, const void *v_new) {
   const KernelInfo k = kernel_for(d, plan.impl);
   dec::DecodeArgs a;
   if (!dec::make_decode_args(d, plan, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                              num_seqs, scale, workspace, &a))
     return cudaErrorInvalidValue;
+  if (k_new != nullptr) {
+    a.k_new = static_cast<const uint8_t *>(k_new);
+    a.v_new = static_cast<const uint8_t *>(v_new);
+    a.k_write = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+    a.v_write = static_cast<uint8_t *>(const_cast<void *>(v_cache));
+  }
   // programmatic dependent launch: the kernel's launch overlaps the tail of
   // the preceding kernel in the stream (typically pa_cache_write); the kernel
   // waits for that kernel's writes before reading anything

@@ -60,6 +60,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kFlagFirst = 1;
 constexpr int kFlagLast = 2;
+constexpr int kFlagEnd = 4;  // the stage holds the sequence's last token
 constexpr int kStageData = 0;
 constexpr int kStageEnd = 1;
 constexpr int kConsumerWarps = 4;
@@ -70,7 +71,7 @@ struct __align__(16) StageHdr {
   int s;
   int grp;     // kv head group (kv heads grp * HG .. grp * HG + HG - 1)
   int ntok;    // tokens of this stage before the sequence's end
-  int flags;   // kFlagFirst / kFlagLast of a piece
+  int flags;   // kFlagFirst / kFlagLast of a piece, kFlagEnd
   int seg_nb;  // blocks of the segment
   int tlo;     // tokens at the stage's start before the first key (local attention)
 };
@@ -107,6 +108,15 @@ struct DecodeArgs {
   int32_t *seg_counter;  // [num_seqs * num_groups] pieces of each split segment finished
   float *slot_lse;       // [grid][2][slot heads], log2 domain
   float *slot_o;         // [grid][2][slot heads][D]
+  // pa_decode_append (MMA kernel, 16-bit caches): sequence s's token at
+  // position context_lens[s] - 1 is k_new[s] / v_new[s] ([S][kv heads][D]);
+  // the consumer of the sequence's last block puts it into its staged tile
+  // and into the cache (k_write / v_write, the caches).  NULL: nothing to
+  // append.
+  const uint8_t *k_new;
+  const uint8_t *v_new;
+  uint8_t *k_write;
+  uint8_t *v_write;
 };
 
 // Optional timeline counters (compiled only with -DPA_DECODE_TRACE): per CTA,
@@ -335,7 +345,8 @@ __device__ void produce(const DecodeArgs &a, uint8_t *stages, StageHdr *hdr, uin
             h.s = s;
             h.grp = grp;
             h.ntok = min(L - lb0 * 16, nblk * 16);
-            h.flags = (first ? kFlagFirst : 0) | (k + BPS >= npb ? kFlagLast : 0);
+            h.flags = (first ? kFlagFirst : 0) | (k + BPS >= npb ? kFlagLast : 0) |
+                      (L - lb0 * 16 <= nblk * 16 ? kFlagEnd : 0);
             h.seg_nb = nb;
             h.tlo = max(0, local_first_key(L - 1, a.window, a.chunk) - lb0 * 16);
             hdr[stage] = h;
@@ -1103,6 +1114,10 @@ __device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me,
   int rb = 0;
   uint32_t rpar = 1;  // the partial-state buffers start out free
   float qsc = a.qscale;  // score scale of this warp's kv head (set per segment)
+  // pa_decode_append: this lane's 16-byte chunk of the segment's appended K
+  // (lanes < ROWB / 16) or V row, and its byte offset in the cache (-1: none)
+  uint4 app = make_uint4(0, 0, 0, 0);
+  int64_t app_off = -1;
   PA_TRACE(const long long tc0 = clock64(); long long tc_full = 0, tc_fin = 0, n_st = 0, n_pc = 0;)
   for (;;) {
     PA_TRACE(const long long tw0 = clock64();)
@@ -1117,6 +1132,28 @@ __device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me,
     const uint8_t *Vs = Ks + C::KVB;
     if (h.flags & kFlagFirst) {
       qsc = head_qscale(a, h.grp * HG + hw);
+      if constexpr (kv16(KVT)) {
+        if (a.k_new != nullptr && lane < 2 * (C::ROWB / 16)) {
+          // the token this step appends to the sequence (position L - 1),
+          // loaded now so that the sequence's last block finds it in
+          // registers: a chunk of its K or V row and where it goes in the cache
+          constexpr int CH = C::ROWB / 16;
+          const int kvh = h.grp * HG + hw;
+          const int ch = lane % CH;
+          const uint8_t *src = lane < CH ? a.k_new : a.v_new;
+          app = __ldg(reinterpret_cast<const uint4 *>(src + (static_cast<int64_t>(h.s) * a.num_kv_heads + kvh) *
+                                                                C::ROWB) + ch);
+          const int L = seq_len(a, h.s);
+          app_off = -1;
+          if (L > 0) {
+            const int phys = __ldg(a.block_tables + static_cast<int64_t>(h.s) * a.max_blocks_per_seq + ((L - 1) >> 4));
+            if (!a.checked || (phys >= 0 && phys < a.num_blocks))
+              app_off = ((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * 16 + ((L - 1) & 15)) * C::ROWB + ch * 16;
+            else
+              report(a, kErrBadIndex);  // no row is written outside the cache
+          }
+        }
+      }
       // Q^T fragments of this kv head's query heads (zero past g)
       const uint16_t *Qs = reinterpret_cast<const uint16_t *>(Ks + C::QOFF) + hw * a.g * D;
 #pragma unroll
@@ -1150,6 +1187,21 @@ __device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me,
     }
     const int vt = h.ntok - 16 * bw;  // valid tokens of this warp's block (<= 0: none)
     if (vt > 0) {
+      if constexpr (kv16(KVT)) {
+        if (a.k_new != nullptr && (h.flags & kFlagEnd) && vt <= 16) {
+          // the sequence's last block: its row vt - 1 is the appended token,
+          // put into the staged tile (over the cache's stale row) before any
+          // fragment of the block is read, and into the cache
+          constexpr int CH = C::ROWB / 16;
+          if (lane < 2 * CH) {
+            uint8_t *tile = const_cast<uint8_t *>(lane < CH ? Ks : Vs) + bw * C::GTILE;
+            *reinterpret_cast<uint4 *>(tile + swz_off<C::ROWB, HG>(trow + vt - 1, lane % CH)) = app;
+            if (app_off >= 0) *reinterpret_cast<uint4 *>((lane < CH ? a.k_write : a.v_write) + app_off) = app;
+          }
+          fence_proxy_async_smem();  // the stage's next copy lands after these writes
+          __syncwarp();
+        }
+      }
       const uint32_t kt = smem_u32(Ks + bw * C::GTILE);
       const uint32_t vtl = smem_u32(Vs + bw * C::GTILE);
       // ---- S^T (16 tokens x 8 heads per n-tile) = K Q^T, two accumulator

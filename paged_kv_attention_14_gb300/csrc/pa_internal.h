@@ -37,11 +37,15 @@ pa_status validate_decode(const pa_kv_desc *desc, const float *out, const float 
                           int32_t max_blocks_per_seq, const int32_t *context_lens, int32_t num_seqs,
                           int32_t max_context_len, float scale, DecodePlan *plan);
 
+// k_new / v_new (pa_decode_append; NULL for pa_decode): sequence s's token
+// at position context_lens[s] - 1, [S][kv heads][D] in the cache's 16-bit
+// type, written into the caches by the kernel as it attends (MMA kernel).
 cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *out, float *lse,
                           const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           const int32_t *context_lens, int32_t num_seqs, float scale,
-                          void *workspace, cudaStream_t stream);
+                          void *workspace, cudaStream_t stream, const void *k_new = nullptr,
+                          const void *v_new = nullptr);
 
 pa_status check_prefill(const pa_kv_desc &d, const char **why);
 

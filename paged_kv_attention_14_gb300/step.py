@@ -47,14 +47,19 @@ class MixedStep:
     ``prefill_out`` None).  With a ``prefill_workspace``
     (binding.prefill_workspace) the prefill runs as
     pa_prefill_chunk_balanced, its KV work spread evenly over the SMs;
-    without one as pa_prefill_chunk."""
+    without one as pa_prefill_chunk.  With ``decode_append`` a step without a
+    prefill part whose new rows are one token per decode sequence, in
+    sequence order (k_new[s] at position context_lens[s] - 1), runs as one
+    pa_decode_append launch instead of pa_cache_write and pa_decode; where
+    the library does not take it (8-bit caches, the CUDA-core decode kernel)
+    the step falls back to the two calls."""
 
     MODES = ("fused", "streams", "serial")
 
     def __init__(self, desc: B.PaKvDesc, k_cache, v_cache, scale: float, *, decode_out=None, decode_lse=None,
                  workspace=None, max_context_len_decode: int = 0, prefill_out=None, prefill_lse=None,
                  max_q_len: int = 0, max_context_len_prefill: int = 0, mode: str = "fused",
-                 prefill_workspace=None):
+                 prefill_workspace=None, decode_append: bool = False):
         if mode not in self.MODES:
             raise ValueError(f"mode must be one of {self.MODES}")
         self.desc = desc
@@ -65,6 +70,7 @@ class MixedStep:
         self.prefill_out, self.prefill_lse = prefill_out, prefill_lse
         self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
         self.prefill_workspace = prefill_workspace
+        self.decode_append = bool(decode_append) and decode_out is not None and prefill_out is None
         self._balanced = {}  # (prefill sequences, table width) -> the balanced prefill runs
         both = decode_out is not None and prefill_out is not None
         fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
@@ -150,6 +156,18 @@ class MixedStep:
     def __call__(self, k_new, v_new, slot_mapping, dec_args=None, pf_args=None):
         """dec_args: (q, block_tables, context_lens); pf_args: (q, query_start_loc,
         block_tables, context_lens)."""
+        if self.decode_append and dec_args is not None and k_new is not None and \
+                k_new.shape[0] == dec_args[2].shape[0]:
+            q, block_tables, context_lens = dec_args
+            try:
+                B.pa_decode_append(self.desc, self.decode_out, q, k_new, v_new, self.k_cache, self.v_cache,
+                                   block_tables, context_lens, self.max_context_len_decode, self.scale,
+                                   self.workspace, lse=self.decode_lse)
+                return
+            except B.PaError as e:
+                if e.status != B.PA_ERR_UNSUPPORTED:
+                    raise
+                self.decode_append = False  # checked before anything was enqueued: the two calls below
         if slot_mapping is not None and slot_mapping.numel() > 0:
             B.pa_cache_write(self.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping)
         self.attend(dec_args, pf_args)

@@ -196,6 +196,34 @@ def test_decode_argument_errors(lib):
                          None) == B.PA_ERR_INVALID_ARG
 
 
+def test_decode_append_argument_errors(lib):
+    # the checks that need no device run before anything is planned or enqueued
+    d = _desc()
+    ptrs = (0x1000, None, 0x2000)          # out, lse, q
+    caches = (0x3000, 0x4000, 0x5000, 4, 0x6000)  # k_cache, v_cache, block_tables, width, context_lens
+    # zero sequences: nothing to do, k_new / v_new not needed
+    assert lib.pa_decode_append(ctypes.byref(d), *ptrs, None, None, *caches, 0, 16, 0.1, None, 0, None) == B.PA_OK
+    # k_new / v_new NULL or misaligned
+    assert lib.pa_decode_append(ctypes.byref(d), *ptrs, None, 0x8000, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
+                                None) == B.PA_ERR_INVALID_ARG
+    assert "k_new" in B.last_error()
+    assert lib.pa_decode_append(ctypes.byref(d), *ptrs, 0x8000, 0x9008, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
+                                None) == B.PA_ERR_INVALID_ARG
+    # 8-bit caches are not taken
+    for kv in (B.PA_KV_FP8_E4M3, B.PA_KV_FP8_E5M2):
+        d8 = _desc(kv_dtype=kv, k_scale=1.0, v_scale=1.0)
+        assert lib.pa_decode_append(ctypes.byref(d8), *ptrs, 0x8000, 0x9000, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
+                                    None) == B.PA_ERR_UNSUPPORTED
+        assert "pa_cache_write and pa_decode" in B.last_error()
+    # pa_decode's own checks: NULL out, a length beyond the table, a bad descriptor
+    assert lib.pa_decode_append(ctypes.byref(d), None, None, 0x2000, 0x8000, 0x9000, *caches, 2, 16, 0.1, 0x7000,
+                                1 << 20, None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_append(ctypes.byref(d), *ptrs, 0x8000, 0x9000, *caches, 2, 65, 0.1, 0x7000, 1 << 20,
+                                None) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_decode_append(ctypes.byref(_desc(head_dim=96)), *ptrs, 0x8000, 0x9000, *caches, 2, 16, 0.1,
+                                0x7000, 1 << 20, None) == B.PA_ERR_UNSUPPORTED
+
+
 def test_error_word_and_check_flag_validation(lib):
     d = _desc()
     d.error_word = 0x1002  # not 4-byte aligned
