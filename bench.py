@@ -558,16 +558,26 @@ def run_ours(args):
     pf_host = torch.empty(pf_out.shape, dtype=pf_out.dtype).pin_memory() if mixed else None
     h2d = total
     d2h = out_host.numel() * out_host.element_size() + (pf_host.numel() * pf_host.element_size() if mixed else 0)
+    # a decode-only step's kernel stores its output straight into the pinned
+    # host buffer (the decode entry points take host-resident out / lse), so
+    # the result reaches the host without a copy after the kernel;
+    # --e2e-out device keeps the output on the device and copies it back
+    out_to_host = not mixed and args.e2e_out == "host"
+    ms_e2e = ms
+    if out_to_host:
+        ms_e2e = MixedStep(desc, kc, vc, b.scale, decode_out=out_host, workspace=wsp, max_context_len_decode=maxL,
+                           mode=args.mixed_mode, decode_append=append)
 
     def e2e_issue():
         dev_buf.copy_(host_buf, non_blocking=True)
-        ms(views["k_new"], views["v_new"], views["slot_mapping"],
-           (views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
-           (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
-            views["context_lens_prefill"]) if mixed else None)
+        ms_e2e(views["k_new"], views["v_new"], views["slot_mapping"],
+               (views["q_decode"], views["block_tables_decode"], views["context_lens_decode"]),
+               (views["q_prefill"], views["query_start_loc"], views["block_tables_prefill"],
+                views["context_lens_prefill"]) if mixed else None)
         if mixed:
             pf_host.copy_(pf_out, non_blocking=True)
-        out_host.copy_(out, non_blocking=True)
+        if not out_to_host:
+            out_host.copy_(out, non_blocking=True)
 
     # the public API's step as a user drives it: one CUDA-graph replay of the
     # copies in, the step and the copies out, then a wait for the result
@@ -592,6 +602,10 @@ def run_ours(args):
     e2e_s = tot / ke
     if ws > 1:
         (e2e_s,) = _max_over_ranks([e2e_s], dev)
+    if out_to_host:
+        # the same step with the same inputs: the result in host memory equals
+        # the device-resident one bit for bit
+        assert torch.equal(out_host, out.cpu()), "the output stored into host memory differs"
 
     if rank == 0:
         peak, tc_peak, peak_kind = _peaks()
@@ -628,8 +642,9 @@ def run_ours(args):
             "e2e": {"value": round(_job_throughput(ws, kv_bytes, e2e_s) / 1e9, 1), "unit": "GB/s", "us_per_step": round(e2e_s * 1e6, 1),
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "how": "step.GraphedStep: one CUDA-graph replay per step of the pinned-host-to-device copy of the "
-                           "inputs, the cache write and attention, and the copy of the outputs to pinned host memory, "
-                           "then a wait; host wall clock"},
+                           "inputs, the cache write and attention, and " +
+                           ("the kernel's stores of the output straight into pinned host memory" if out_to_host else
+                            "the copy of the outputs to pinned host memory") + ", then a wait; host wall clock"},
             # timed region 2 calls each entry point alone: decode (and prefill)
             "step_calls": step_how,
             "gpu_launches": launches_per_step * K * R + (2 if mixed else 1) * K2 * R2,
@@ -816,6 +831,9 @@ def main():
     ap.add_argument("--prefill-entry", choices=["chunk", "balanced"], default="chunk",
                     help="prefill entry point: pa_prefill_chunk (a CTA per query tile and kv head) or "
                          "pa_prefill_chunk_balanced (the library's choice of that grid or the balanced kernel)")
+    ap.add_argument("--e2e-out", choices=("host", "device"), default="host",
+                    help="decode-only workloads' e2e step: the kernel stores the output into pinned host memory "
+                         "(host) or on the device, copied back after the kernel (device)")
     ap.add_argument("--separate-write", action="store_true",
                     help="decode-only workloads: pa_cache_write then pa_decode instead of pa_decode_append")
     ap.add_argument("--mixed-mode", choices=["fused", "streams", "serial"], default="fused",

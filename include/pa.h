@@ -33,7 +33,13 @@
  * Query head h attends kv head h / (num_q_heads / num_kv_heads).
  *
  * Ownership: every pointer is caller-owned device memory unless its comment
- * says "host".  The library allocates no device memory and keeps no state
+ * says "host".  One exception: out and lse of pa_decode, pa_decode_append and
+ * pa_decode_static may also be pinned host memory (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister), which unified addressing maps into the
+ * device's address space at the same address.  The decode kernels write
+ * those arrays with plain stores only, so the step's result goes straight to
+ * the host (over NVLink-C2C on a Grace-Blackwell system).  The result is
+ * there once the stream has completed the call.  The library allocates no device memory and keeps no state
  * between calls apart from the thread-local error string and a per-device
  * cache of launch limits (SM count, occupancy).
  *

@@ -190,7 +190,9 @@ def _check(status: int):
         raise PaError(status, last_error())
 
 
-def _ptr(t: Optional[torch.Tensor], dtypes, name: str, allow_none: bool = False):
+def _ptr(t: Optional[torch.Tensor], dtypes, name: str, allow_none: bool = False, host_ok: bool = False):
+    """The tensor's address.  ``host_ok``: a pinned CPU tensor is taken too
+    (unified addressing maps pinned host memory at the same address)."""
     if t is None:
         if allow_none:
             return None
@@ -199,8 +201,8 @@ def _ptr(t: Optional[torch.Tensor], dtypes, name: str, allow_none: bool = False)
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype not in dtypes:
         raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
-    if not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or a pinned CPU tensor" if host_ok else ""))
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
@@ -248,10 +250,12 @@ def decode_workspace(desc: PaKvDesc, num_seqs: int, max_context_len: int, device
 
 def pa_decode(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, context_lens,
               max_context_len: int, scale: float, workspace, lse=None, stream=None):
-    """Decode attention: q ``[S, Hq, D]`` bf16 -> out ``[S, Hq, D]`` fp32 (lse ``[S, Hq]``)."""
+    """Decode attention: q ``[S, Hq, D]`` bf16 -> out ``[S, Hq, D]`` fp32 (lse ``[S, Hq]``).
+    ``out`` / ``lse`` may be pinned CPU tensors: the kernel stores the result
+    straight into host memory."""
     S = int(context_lens.shape[0])
-    _check(load().pa_decode(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                            _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
+    _check(load().pa_decode(ctypes.byref(desc), _ptr(out, _F32, "out", host_ok=True),
+                            _ptr(lse, _F32, "lse", allow_none=True, host_ok=True), _ptr(q, _act(desc), "q"),
                             _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                             _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
                             _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
@@ -265,8 +269,8 @@ def pa_decode_append(desc: PaKvDesc, out, q, k_new, v_new, k_cache, v_cache, blo
     ``[S, Hkv, D]``) goes into the caches at position context_lens[s] - 1, and the
     decode attends over all context_lens[s] tokens."""
     S = int(context_lens.shape[0])
-    _check(load().pa_decode_append(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
+    _check(load().pa_decode_append(ctypes.byref(desc), _ptr(out, _F32, "out", host_ok=True),
+                                   _ptr(lse, _F32, "lse", allow_none=True, host_ok=True), _ptr(q, _act(desc), "q"),
                                    _ptr(k_new, _act(desc), "k_new"), _ptr(v_new, _act(desc), "v_new"),
                                    _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                                    _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
@@ -280,8 +284,8 @@ def pa_decode_static(desc: PaKvDesc, out, q, k_cache, v_cache, block_tables, con
     """pa_decode on the library's own fixed-size scratch (no workspace argument,
     for callers that cannot allocate device memory where they decode)."""
     S = int(context_lens.shape[0])
-    _check(load().pa_decode_static(ctypes.byref(desc), _ptr(out, _F32, "out"),
-                                   _ptr(lse, _F32, "lse", allow_none=True), _ptr(q, _act(desc), "q"),
+    _check(load().pa_decode_static(ctypes.byref(desc), _ptr(out, _F32, "out", host_ok=True),
+                                   _ptr(lse, _F32, "lse", allow_none=True, host_ok=True), _ptr(q, _act(desc), "q"),
                                    _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
                                    _ptr(block_tables, _I32, "block_tables"), int(block_tables.shape[1]),
                                    _ptr(context_lens, _I32, "context_lens"), S, int(max_context_len),
