@@ -303,15 +303,16 @@ PA_API pa_status pa_prefill_chunk(const pa_kv_desc *desc, float *out, float *lse
  * all context_lens[s] tokens, the appended one included.  The kernel puts
  * the new rows into the tiles it stages as it reads each sequence's last
  * block, so the attention does not wait for a separate write.
- *   k_new, v_new : [num_seqs][num_kv_heads][head_dim] in the cache's type,
- *                  16-byte aligned; a sequence with context length 0 appends
- *                  nothing.
+ *   k_new, v_new : [num_seqs][num_kv_heads][head_dim] bf16 (fp16 for an fp16
+ *                  cache), 16-byte aligned; a sequence with context length 0
+ *                  appends nothing.  An 8-bit cache receives the rows encoded
+ *                  exactly as pa_cache_write encodes them (same bytes).
  *   the other arguments are pa_decode's (workspace: pa_decode_workspace_size).
- * Takes bf16 and fp16 caches on the tensor-core decode kernel
- * (PA_ERR_UNSUPPORTED otherwise: call pa_cache_write and pa_decode).  Errors
- * found on the host (pa_decode's, NULL or misaligned k_new / v_new:
- * PA_ERR_INVALID_ARG; PA_ERR_UNSUPPORTED; PA_ERR_WORKSPACE) return before
- * anything is enqueued.  With check_indices, an out-of-range block id of a
+ * Runs on the tensor-core decode kernel, for every cache type
+ * (PA_ERR_UNSUPPORTED with decode_impl PA_DECODE_SIMT: call pa_cache_write
+ * and pa_decode).  Errors found on the host (pa_decode's, NULL or misaligned
+ * k_new / v_new: PA_ERR_INVALID_ARG; PA_ERR_UNSUPPORTED; PA_ERR_WORKSPACE)
+ * return before anything is enqueued.  With check_indices, an out-of-range block id of a
  * last block is reported and its row is not written.  Two sequences whose
  * last tokens share a slot race, as duplicate slots of pa_cache_write do.
  */

@@ -238,15 +238,13 @@ pa_status pa_decode_append(const pa_kv_desc *desc, float *out, float *lse, const
                            int32_t max_context_len, float scale, void *workspace, size_t workspace_bytes,
                            pa_stream_t stream) {
   static const char *kNotTaken =
-      "pa_decode_append takes bf16 and fp16 caches on the tensor-core decode kernel (make the pa_cache_write and "
-      "pa_decode calls instead)%s";
+      "pa_decode_append runs on the tensor-core decode kernel (with decode_impl PA_DECODE_SIMT make the "
+      "pa_cache_write and pa_decode calls instead)%s";
   // the checks that need no device come first
   pa_status st = check_desc(desc);
   if (st != PA_OK) return st;
   if (num_seqs > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
     return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be non-NULL and 16-byte aligned%s");
-  if (num_seqs > 0 && desc->kv_dtype != PA_KV_BF16 && desc->kv_dtype != PA_KV_F16)
-    return fail(PA_ERR_UNSUPPORTED, kNotTaken);
   pa::DecodePlan plan;
   st = pa::validate_decode(desc, out, lse, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            num_seqs, max_context_len, scale, &plan);

@@ -49,25 +49,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(
     reinterpret_cast<uint4 *>(k_cache)[dst] = __ldg(k + i);
     reinterpret_cast<uint4 *>(v_cache)[dst] = __ldg(v + i);
   } else {
-    // x / scale in correctly rounded fp32 division, then E4M3 / E5M2
-    // round-to-nearest-even with finite saturation, 16 values per store
-    auto enc = [](const uint4 &a, const uint4 &b, float s) {
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      uint32_t r[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint16_t lo = pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j]), s), __fdiv_rn(bf16hi(w[2 * j]), s));
-        const uint16_t hi =
-            pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j + 1]), s), __fdiv_rn(bf16hi(w[2 * j + 1]), s));
-        r[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      }
-      return make_uint4(r[0], r[1], r[2], r[3]);
-    };
-    // per-kv-head scales where given
+    // 16 values per store (encode_fp8x16); per-kv-head scales where given
     const float ks = k_scales ? __ldg(k_scales + head) : k_scale;
     const float vs = v_scales ? __ldg(v_scales + head) : v_scale;
-    reinterpret_cast<uint4 *>(k_cache)[dst] = enc(__ldg(k + 2 * i), __ldg(k + 2 * i + 1), ks);
-    reinterpret_cast<uint4 *>(v_cache)[dst] = enc(__ldg(v + 2 * i), __ldg(v + 2 * i + 1), vs);
+    reinterpret_cast<uint4 *>(k_cache)[dst] = encode_fp8x16<KVT>(__ldg(k + 2 * i), __ldg(k + 2 * i + 1), ks);
+    reinterpret_cast<uint4 *>(v_cache)[dst] = encode_fp8x16<KVT>(__ldg(v + 2 * i), __ldg(v + 2 * i + 1), vs);
   }
 }
 

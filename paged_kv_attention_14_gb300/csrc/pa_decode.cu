@@ -222,6 +222,8 @@ cudaError_t launch_decode(const pa_kv_desc &d, const DecodePlan &plan, float *ou
     a.v_new = static_cast<const uint8_t *>(v_new);
     a.k_write = static_cast<uint8_t *>(const_cast<void *>(k_cache));
     a.v_write = static_cast<uint8_t *>(const_cast<void *>(v_cache));
+    a.k_enc = d.k_scale == 0.f ? 1.f : d.k_scale;  // the cache write's per-tensor scales
+    a.v_enc = d.v_scale == 0.f ? 1.f : d.v_scale;
   }
   // programmatic dependent launch: the kernel's launch overlaps the tail of
   // the preceding kernel in the stream (typically pa_cache_write); the kernel

@@ -108,15 +108,19 @@ struct DecodeArgs {
   int32_t *seg_counter;  // [num_seqs * num_groups] pieces of each split segment finished
   float *slot_lse;       // [grid][2][slot heads], log2 domain
   float *slot_o;         // [grid][2][slot heads][D]
-  // pa_decode_append (MMA kernel, 16-bit caches): sequence s's token at
-  // position context_lens[s] - 1 is k_new[s] / v_new[s] ([S][kv heads][D]);
-  // the consumer of the sequence's last block puts it into its staged tile
-  // and into the cache (k_write / v_write, the caches).  NULL: nothing to
-  // append.
+  // pa_decode_append (MMA kernel): sequence s's token at position
+  // context_lens[s] - 1 is k_new[s] / v_new[s] ([S][kv heads][D], the
+  // activation type); the consumer of the sequence's last block puts it into
+  // its staged tile and into the cache (k_write / v_write, the caches), an
+  // 8-bit cache's row encoded as pa_cache_write encodes it, with the
+  // per-tensor scales k_enc / v_enc or the per-head k_scales / v_scales.
+  // NULL: nothing to append.
   const uint8_t *k_new;
   const uint8_t *v_new;
   uint8_t *k_write;
   uint8_t *v_write;
+  float k_enc;
+  float v_enc;
 };
 
 // Optional timeline counters (compiled only with -DPA_DECODE_TRACE): per CTA,
@@ -1132,17 +1136,27 @@ __device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me,
     const uint8_t *Vs = Ks + C::KVB;
     if (h.flags & kFlagFirst) {
       qsc = head_qscale(a, h.grp * HG + hw);
-      if constexpr (kv16(KVT)) {
+      {
         if (a.k_new != nullptr && lane < 2 * (C::ROWB / 16)) {
           // the token this step appends to the sequence (position L - 1),
           // loaded now so that the sequence's last block finds it in
-          // registers: a chunk of its K or V row and where it goes in the cache
+          // registers: a 16-byte chunk of its cache row (K for lanes < CH,
+          // else V) and where it goes in the cache
           constexpr int CH = C::ROWB / 16;
           const int kvh = h.grp * HG + hw;
           const int ch = lane % CH;
-          const uint8_t *src = lane < CH ? a.k_new : a.v_new;
-          app = __ldg(reinterpret_cast<const uint4 *>(src + (static_cast<int64_t>(h.s) * a.num_kv_heads + kvh) *
-                                                                C::ROWB) + ch);
+          const bool is_k = lane < CH;
+          const uint8_t *src = is_k ? a.k_new : a.v_new;
+          const int64_t row = static_cast<int64_t>(h.s) * a.num_kv_heads + kvh;
+          if constexpr (kv16(KVT)) {
+            app = __ldg(reinterpret_cast<const uint4 *>(src + row * C::ROWB) + ch);
+          } else {
+            // 16 activation values (32 bytes) become 16 cache bytes
+            const uint4 *s2 = reinterpret_cast<const uint4 *>(src + row * (2 * C::ROWB)) + 2 * ch;
+            const float *hs = is_k ? a.k_scales : a.v_scales;
+            const float sc = hs ? __ldg(hs + kvh) : (is_k ? a.k_enc : a.v_enc);
+            app = encode_fp8x16<KVT>(__ldg(s2), __ldg(s2 + 1), sc);
+          }
           const int L = seq_len(a, h.s);
           app_off = -1;
           if (L > 0) {
@@ -1187,7 +1201,7 @@ __device__ void decode_partition(const DecodeArgs &a, uint8_t *smem_raw, int me,
     }
     const int vt = h.ntok - 16 * bw;  // valid tokens of this warp's block (<= 0: none)
     if (vt > 0) {
-      if constexpr (kv16(KVT)) {
+      {
         if (a.k_new != nullptr && (h.flags & kFlagEnd) && vt <= 16) {
           // the sequence's last block: its row vt - 1 is the appended token,
           // put into the staged tile (over the cache's stale row) before any

@@ -362,6 +362,24 @@ __device__ __forceinline__ uint16_t pack_fp8x2_satfinite(float lo, float hi) {
   return pack_e4m3x2_satfinite(lo, hi);
 }
 
+// 16 bf16 values (a: the first 8, b: the next 8) to 16 bytes of an 8-bit
+// cache: x / s in correctly rounded fp32 division, then E4M3 / E5M2 round
+// to nearest even with finite saturation.  Every writer of 8-bit cache rows
+// encodes through this function, so they store the same bytes.
+template <int KVT>
+__device__ __forceinline__ uint4 encode_fp8x16(const uint4 &a, const uint4 &b, float s) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint16_t lo = pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j]), s), __fdiv_rn(bf16hi(w[2 * j]), s));
+    const uint16_t hi =
+        pack_fp8x2_satfinite<KVT>(__fdiv_rn(bf16lo(w[2 * j + 1]), s), __fdiv_rn(bf16hi(w[2 * j + 1]), s));
+    r[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // ------------------------------------------------------------ gpu atomics
 
 // atomicAdd with acquire-release semantics at GPU scope: makes this thread's

@@ -51,7 +51,7 @@ class MixedStep:
     prefill part whose new rows are one token per decode sequence, in
     sequence order (k_new[s] at position context_lens[s] - 1), runs as one
     pa_decode_append launch instead of pa_cache_write and pa_decode; where
-    the library does not take it (8-bit caches, the CUDA-core decode kernel)
+    the library does not take it (the CUDA-core decode kernel)
     the step falls back to the two calls."""
 
     MODES = ("fused", "streams", "serial")

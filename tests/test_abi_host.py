@@ -209,12 +209,10 @@ def test_decode_append_argument_errors(lib):
     assert "k_new" in B.last_error()
     assert lib.pa_decode_append(ctypes.byref(d), *ptrs, 0x8000, 0x9008, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
                                 None) == B.PA_ERR_INVALID_ARG
-    # 8-bit caches are not taken
-    for kv in (B.PA_KV_FP8_E4M3, B.PA_KV_FP8_E5M2):
-        d8 = _desc(kv_dtype=kv, k_scale=1.0, v_scale=1.0)
-        assert lib.pa_decode_append(ctypes.byref(d8), *ptrs, 0x8000, 0x9000, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
-                                    None) == B.PA_ERR_UNSUPPORTED
-        assert "pa_cache_write and pa_decode" in B.last_error()
+    # an 8-bit cache's descriptor is checked as pa_decode checks it (a negative scale)
+    d8 = _desc(kv_dtype=B.PA_KV_FP8_E4M3, k_scale=-1.0, v_scale=1.0)
+    assert lib.pa_decode_append(ctypes.byref(d8), *ptrs, 0x8000, 0x9000, *caches, 2, 16, 0.1, 0x7000, 1 << 20,
+                                None) == B.PA_ERR_INVALID_ARG
     # pa_decode's own checks: NULL out, a length beyond the table, a bad descriptor
     assert lib.pa_decode_append(ctypes.byref(d), None, None, 0x2000, 0x8000, 0x9000, *caches, 2, 16, 0.1, 0x7000,
                                 1 << 20, None) == B.PA_ERR_INVALID_ARG

@@ -15,6 +15,7 @@ import torch
 import oracle
 from paged_kv_attention_14_gb300 import binding as B
 from paged_kv_attention_14_gb300 import workloads as W
+import pa_helpers as H
 from pa_helpers import LSE_TOL, TOL, assert_close, desc_of, oracle_decode
 
 pytestmark = pytest.mark.gpu
@@ -110,21 +111,78 @@ def test_decode_append_with_local_attention(window, chunk):
     _run(b, 31, window=window, chunk=chunk)
 
 
-def test_decode_append_refuses_what_it_does_not_take():
-    """8-bit caches and the CUDA-core kernel: PA_ERR_UNSUPPORTED, nothing
-    enqueued (the caller makes the two calls)."""
+def _run8(b, seed):
+    """The same check for an 8-bit cache: the appended rows are encoded in the
+    kernel exactly as pa_cache_write and the oracle encode them."""
+    g = torch.Generator().manual_seed(seed)
+    k_new = (2 * torch.randn(b.k_new.shape, generator=g)).to(torch.bfloat16).to(DEV)
+    v_new = (2 * torch.randn(b.v_new.shape, generator=g)).to(torch.bfloat16).to(DEV)
+    d = desc_of(b, decode_impl=B.PA_DECODE_MMA)
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    slots = b.slot_mapping
+    live = slots >= 0
+    blk, off = slots[live] // 16, slots[live] % 16
+    kc0, vc0 = H.gpu_caches(b)
+    kc, vc = kc0.clone(), vc0.clone()
+    kc[blk, :, off, :] = 0x7F  # NaN codes until the step writes the rows
+    vc[blk, :, off, :] = 0x7F
+    out = torch.full((S, b.num_q_heads, b.head_dim), float("nan"), device=DEV)
+    lse = torch.full((S, b.num_q_heads), float("nan"), device=DEV)
+    ws = B.decode_workspace(d, S, maxL, DEV)
+    B.pa_decode_append(d, out, b.q_decode, k_new, v_new, kc, vc, b.block_tables_decode, b.context_lens_decode, maxL,
+                       b.scale, ws, lse=lse)
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32)[0]) == 0
+    kc2, vc2 = kc0.clone(), vc0.clone()
+    B.pa_cache_write(d, k_new, v_new, kc2, vc2, slots)
+    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
+    B.pa_decode(d, out2, b.q_decode, kc2, vc2, b.block_tables_decode, b.context_lens_decode, maxL, b.scale,
+                B.decode_workspace(d, S, maxL, DEV), lse=lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    code, okc, ovc = H.oracle_caches(b)
+    ok, ov = oracle.cache_write(code, 16, b.num_kv_heads, b.head_dim, k_new.cpu(), v_new.cpu(), slots.cpu(), okc,
+                                ovc, b.k_scale, b.v_scale, k_scales=H._cpu(b.k_scales), v_scales=H._cpu(b.v_scales))
+    assert np.array_equal(kc.cpu().numpy(), ok) and np.array_equal(vc.cpu().numpy(), ov)
+    o_ref, l_ref = oracle_decode(b, ocaches=(code, ok, ov))
+    assert_close(out, o_ref, TOL[b.kv_dtype], "out")
+    assert_close(lse, l_ref, LSE_TOL[b.kv_dtype], "lse")
+
+
+def test_decode_append_on_the_fp8_decode_step():
+    """Workload 4 in full: 128 sequences, 40 q / 8 kv heads, E4M3 cache."""
+    _run8(W.workload(4, device=DEV, poison=False), 41)
+
+
+@pytest.mark.parametrize("kv", [W.KV_FP8, W.KV_FP8_E5M2])
+@pytest.mark.parametrize("per_head", [False, True])
+@pytest.mark.parametrize("D,Hq,Hkv,lens", [
+    (128, 32, 8, [1, 15, 16, 17, 100, 2049]),
+    (128, 40, 8, [5, 64, 513]),
+    (64, 4, 2, [1, 7, 16, 33]),
+])
+def test_decode_append_8bit_random_shapes(kv, per_head, D, Hq, Hkv, lens):
+    b = W.random_decode(980 + D + Hq + len(lens), lens, Hq, Hkv, D, kv_dtype=kv, device=DEV, poison=False,
+                        per_head_scales=per_head)
+    _run8(b, 51 + len(lens))
+
+
+def test_decode_append_refuses_the_cuda_core_kernel():
+    """decode_impl PA_DECODE_SIMT: PA_ERR_UNSUPPORTED, nothing enqueued (the
+    caller makes the two calls)."""
     b = W.random_decode(960, [40, 17], 8, 2, 128, device=DEV, poison=False)
     S, maxL = 2, 40
     out = torch.empty(S, 8, 128, device=DEV)
-    for d in (desc_of(b, decode_impl=B.PA_DECODE_SIMT),
-              B.make_desc(b.num_blocks, 2, 8, 128, B.PA_KV_FP8_E4M3, 1.0, 1.0)):
-        ws = B.decode_workspace(d, S, maxL, DEV)
-        kc = torch.zeros(tuple(b.k_pool.shape), dtype=torch.uint8 if d.kv_dtype == B.PA_KV_FP8_E4M3 else torch.bfloat16,
-                         device=DEV)
-        with pytest.raises(B.PaError) as e:
-            B.pa_decode_append(d, out, b.q_decode, b.k_new, b.v_new, kc, kc.clone(), b.block_tables_decode,
-                               b.context_lens_decode, maxL, b.scale, ws)
-        assert e.value.status == B.PA_ERR_UNSUPPORTED
+    d = desc_of(b, decode_impl=B.PA_DECODE_SIMT)
+    ws = B.decode_workspace(d, S, maxL, DEV)
+    kc = b.k_pool.clone()
+    with pytest.raises(B.PaError) as e:
+        B.pa_decode_append(d, out, b.q_decode, b.k_new, b.v_new, kc, kc.clone(), b.block_tables_decode,
+                           b.context_lens_decode, maxL, b.scale, ws)
+    assert e.value.status == B.PA_ERR_UNSUPPORTED
+    assert torch.equal(kc.view(torch.int16), b.k_pool.view(torch.int16))
 
 
 def test_decode_append_checked_skips_an_out_of_range_last_block():
