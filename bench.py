@@ -62,15 +62,15 @@ CSRC = os.path.join(ROOT, "paged_kv_attention_14_gb300", "csrc")
 NCU_TRAFFIC = {
     # the decode kernel as the bench launches it, with the step's cache write
     # fused in (pa_decode_append; split segments are merged inside it):
-    # dram__bytes_read.sum 305,593,344 + dram__bytes_write.sum 3,265,024
+    # dram__bytes_read.sum 305,605,120 + dram__bytes_write.sum 3,228,928
     # (the timed pa_decode launch writes no appended rows: 131 KB, 0.04%, less)
-    "decode": {"workload": 2, "bytes": 308_858_368,
-               "sha256": "93177ee9f2a4e173fc470a3e8a914b68377597354cb5142e3dc96bb963482ee4",
+    "decode": {"workload": 2, "bytes": 308_834_048,
+               "sha256": "f60f4519bc7b6121e76327083a7effb5ab28087124dca02a19359265384d06a9",
                "sources": ["pa_device.cuh", "pa_decode_kernels.cuh", "pa_decode_mma_bf16.cu", "pa_decode.cu"]},
     # the tcgen05 prefill kernel launched alone (default variant, fp16 P.V):
-    # dram__bytes_read.sum 49,322,752 + dram__bytes_write.sum 1,985,024
-    "prefill": {"workload": 5, "bytes": 51_307_776,
-                "sha256": "ad174e4d76ca2c5ec166b436b641a72d14dccf6f573bb12c812337b591343b77",
+    # dram__bytes_read.sum 48,927,232 + dram__bytes_write.sum 2,052,864
+    "prefill": {"workload": 5, "bytes": 50_980_096,
+                "sha256": "22efeb676687ddfaf2fcda425b5b7f53d10cd95c71813b859cea8c1a9bad369b",
                 "sources": ["pa_device.cuh", "pa_prefill_tc.cuh", "pa_prefill_tc.cu"]},
 }
 
