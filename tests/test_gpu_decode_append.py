@@ -229,3 +229,28 @@ def test_mixed_step_appends_a_decode_only_step():
         outs.append((out, kc, vc))
     assert torch.equal(outs[0][0], outs[1][0])
     assert _same_bits(outs[0][1], outs[1][1]) and _same_bits(outs[0][2], outs[1][2])
+
+
+def test_mixed_step_appends_an_8bit_decode_step():
+    """MixedStep(decode_append=True) with an E4M3 cache: one launch, the same
+    bytes and outputs as pa_cache_write + pa_decode."""
+    from paged_kv_attention_14_gb300.step import MixedStep
+    b = W.random_decode(990, [100, 2049, 17, 512, 1], 40, 8, 128, kv_dtype=W.KV_FP8, device=DEV, poison=False)
+    d = desc_of(b)
+    S = b.context_lens_decode.shape[0]
+    maxL = b.max_context_len_decode()
+    kc0, vc0 = H.gpu_caches(b)
+    g = torch.Generator().manual_seed(3)
+    k_new = torch.randn(tuple(b.k_new.shape), generator=g).to(torch.bfloat16).to(DEV)
+    v_new = torch.randn(tuple(b.v_new.shape), generator=g).to(torch.bfloat16).to(DEV)
+    outs = []
+    for append in (True, False):
+        kc, vc = kc0.clone(), vc0.clone()
+        out = torch.empty(S, 40, 128, device=DEV)
+        ms = MixedStep(d, kc, vc, b.scale, decode_out=out, workspace=B.decode_workspace(d, S, maxL, DEV),
+                       max_context_len_decode=maxL, decode_append=append)
+        ms(k_new, v_new, b.slot_mapping, (b.q_decode, b.block_tables_decode, b.context_lens_decode))
+        torch.cuda.synchronize()
+        assert ms.decode_append == append
+        outs.append((out, kc, vc))
+    assert all(torch.equal(x, y) for x, y in zip(outs[0], outs[1]))
