@@ -412,10 +412,14 @@ def run_ours(args):
     # decode workload) appends them in the decode launch (pa_decode_append)
     # where the library takes it, unless --separate-write
     append = not mixed and not args.separate_write
+    # a mixed step's fused mode writes the step's rows in its launch too
+    # (pa_mixed_attention_append; the workload's chunks start at block
+    # boundaries), unless --separate-write
     ms = MixedStep(desc, kc, vc, b.scale, decode_out=out, workspace=wsp, max_context_len_decode=maxL,
                    prefill_out=pf_out if mixed else None, max_q_len=pf_maxq if mixed else 0,
                    max_context_len_prefill=pf_maxL if mixed else 0, mode=args.mixed_mode,
-                   prefill_workspace=pf_ws, decode_append=append)
+                   prefill_workspace=pf_ws, decode_append=append,
+                   write_in_step=mixed and not args.separate_write)
     decode, prefill, attend = ms.decode, ms.prefill, ms.attend
     if ms.mode == "fused":
         launches_per_step = 2
@@ -430,11 +434,15 @@ def run_ours(args):
             flush()
         step()
     torch.cuda.synchronize()
-    if ms.decode_append:
-        launches_per_step = 1  # the write and the decode in one launch
+    fused_write = (mixed and ms.write_in_step and ms.mode == "fused" and
+                   not ms.prefill_balanced((b.q_prefill, b.query_start_loc, b.block_tables_prefill,
+                                            b.context_lens_prefill)))
+    if ms.decode_append or fused_write:
+        launches_per_step = 1  # the write and the attention in one launch
     step_how = ("pa_decode_append (the step's cache write and decode in one launch)" if ms.decode_append else
-                "pa_cache_write, then " + ("pa_mixed_attention" if ms.mode == "fused" and mixed else
-                                          "pa_decode" + (" and the prefill" if mixed else "")))
+                "pa_mixed_attention_append (the step's cache write, decode and prefill in one launch)" if fused_write
+                else "pa_cache_write, then " + ("pa_mixed_attention" if ms.mode == "fused" and mixed else
+                                                "pa_decode" + (" and the prefill" if mixed else "")))
 
     K = args.steps
     # A repeat times exactly K steps.  The K-step measurement is repeated
@@ -835,7 +843,8 @@ def main():
                     help="decode-only workloads' e2e step: the kernel stores the output into pinned host memory "
                          "(host) or on the device, copied back after the kernel (device)")
     ap.add_argument("--separate-write", action="store_true",
-                    help="decode-only workloads: pa_cache_write then pa_decode instead of pa_decode_append")
+                    help="pa_cache_write as its own launch: then pa_decode instead of pa_decode_append, or "
+                         "pa_mixed_attention instead of pa_mixed_attention_append")
     ap.add_argument("--mixed-mode", choices=["fused", "streams", "serial"], default="fused",
                     help="mixed step (workload 5): one persistent launch, two streams, or one after the other")
     ap.add_argument("--per-head-scales", action="store_true",

@@ -87,7 +87,8 @@ extern "C" {
  *    PA_PREFILL_TCGEN05_PAIR; pa_test_stall_pipelines, pa_bind_blocks,
  *    pa_release_blocks, pa_mixed_workspace_size, pa_mixed_attention.
  * 4: pa_prefill_workspace_size, pa_prefill_chunk_balanced,
- *    pa_prefill_balanced_chosen, pa_test_prefill_schedule, pa_decode_append. */
+ *    pa_prefill_balanced_chosen, pa_test_prefill_schedule, pa_decode_append,
+ *    pa_mixed_attention_append. */
 #define PA_ABI_VERSION 4
 
 /* Symbols of the shared library; everything else in it stays hidden. */
@@ -407,6 +408,44 @@ PA_API pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, floa
                                     int32_t num_pf_seqs, int32_t max_q_len, int32_t pf_max_context_len,
                                     const void *k_cache, const void *v_cache, float scale, void *workspace,
                                     size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * The whole continuous-batch step in one launch: the step's cache write
+ * (what pa_cache_write does for its new tokens) folded into
+ * pa_mixed_attention, whose results it computes over the caches with the
+ * new tokens in them.  No barrier is needed inside the launch:
+ *   - a decode sequence's new row is written, and used, by the warp that
+ *     owns the sequence's last block (as in pa_decode_append);
+ *   - a prefill chunk's own keys are read from k_new / v_new instead of the
+ *     caches, and each tile writes its own queries' rows into the caches.
+ *   k_new, v_new : [num_new_rows][num_kv_heads][head_dim] in the cache's
+ *                  16-bit type, 16-byte aligned.  Row s < num_dec_seqs is
+ *                  decode sequence s's new token (position
+ *                  dec_context_lens[s] - 1); row num_dec_seqs +
+ *                  query_start_loc[s] + i is prefill sequence s's token i
+ *                  (position pf_context_lens[s] - q_len_s + i).
+ *   num_new_rows : rows of k_new / v_new (num_dec_seqs +
+ *                  query_start_loc[num_pf_seqs]), host value.  With a
+ *                  prefill part it must exceed num_dec_seqs.
+ * Every prefill chunk must start at a multiple of block_size
+ * (pf_context_lens[s] - q_len_s), so that a block holds either cached or new
+ * tokens.  A chunk that does not is reported on the device
+ * (PA_DEVERR_BAD_INDEX) and its outputs are meaningless; for such a step
+ * make the pa_cache_write and pa_mixed_attention calls.  The other
+ * arguments, restrictions and errors are pa_mixed_attention's; k_new /
+ * v_new problems give PA_ERR_INVALID_ARG before anything is enqueued.  Do
+ * not issue pa_cache_write for these rows as well.
+ */
+PA_API pa_status pa_mixed_attention_append(const pa_kv_desc *desc, float *dec_out, float *dec_lse,
+                                           const void *dec_q, const int32_t *dec_block_tables,
+                                           int32_t dec_max_blocks_per_seq, const int32_t *dec_context_lens,
+                                           int32_t num_dec_seqs, int32_t dec_max_context_len, float *pf_out,
+                                           float *pf_lse, const void *pf_q, const int32_t *query_start_loc,
+                                           const int32_t *pf_block_tables, int32_t pf_max_blocks_per_seq,
+                                           const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
+                                           int32_t pf_max_context_len, const void *k_new, const void *v_new,
+                                           int64_t num_new_rows, void *k_cache, void *v_cache, float scale,
+                                           void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
 /*
  * Shared-prefix (cascade) attention.  A prefix-cache hit binds several

@@ -52,7 +52,7 @@ EXPORTED = ("pa_abi_version", "pa_last_error", "pa_cache_write", "pa_decode_work
             "pa_copy_blocks", "pa_test_stall_pipelines", "pa_bind_blocks", "pa_release_blocks",
             "pa_mixed_workspace_size", "pa_mixed_attention", "pa_prefill_workspace_size",
             "pa_prefill_chunk_balanced", "pa_test_prefill_schedule", "pa_prefill_balanced_chosen",
-            "pa_decode_append")
+            "pa_decode_append", "pa_mixed_attention_append")
 
 
 class PaKvDesc(ctypes.Structure):
@@ -132,6 +132,9 @@ def load(path: Optional[str] = None):
         lib.pa_mixed_attention.argtypes = [D, P, P, P, P, I32, P, I32, I32, P, P, P, P, P, I32, P, I32, I32, I32,
                                            P, P, F, P, SZ, P]
         lib.pa_mixed_attention.restype = ctypes.c_int
+        lib.pa_mixed_attention_append.argtypes = [D, P, P, P, P, I32, P, I32, I32, P, P, P, P, P, I32, P, I32, I32,
+                                                  I32, P, P, ctypes.c_int64, P, P, F, P, SZ, P]
+        lib.pa_mixed_attention_append.restype = ctypes.c_int
         lib.pa_bind_blocks.argtypes = [D, P, I32, I32, P, P, P, I32, P, P]
         lib.pa_bind_blocks.restype = ctypes.c_int
         lib.pa_release_blocks.argtypes = [D, P, I32, I32, P, P, I32, P, P, P, P]
@@ -300,12 +303,8 @@ def mixed_workspace(desc: PaKvDesc, num_dec_seqs: int, max_context_len: int, dev
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def pa_mixed_attention(desc: PaKvDesc, k_cache, v_cache, scale: float, workspace, dec=None, pf=None, stream=None):
-    """Decode and prefill attention of one step in one launch.  ``dec``:
-    (out, q, block_tables, context_lens, max_context_len[, lse]) or None;
-    ``pf``: (out, q, query_start_loc, block_tables, context_lens, max_q_len,
-    max_context_len[, lse]) or None.  ``workspace``: mixed_workspace() for
-    the decode part's batch."""
+def _mixed_args(desc: PaKvDesc, dec, pf):
+    """The dec_* and pf_* arguments of the mixed entry points."""
     if dec is not None:
         d_out, d_q, d_bt, d_cl, d_maxL = dec[:5]
         d_lse = dec[5] if len(dec) > 5 else None
@@ -323,10 +322,34 @@ def pa_mixed_attention(desc: PaKvDesc, k_cache, v_cache, scale: float, workspace
                  int(p_cl.shape[0]), int(p_maxq), int(p_maxL))
     else:
         pargs = (None, None, None, None, None, 1, None, 0, 0, 0)
+    return dargs, pargs
+
+
+def pa_mixed_attention(desc: PaKvDesc, k_cache, v_cache, scale: float, workspace, dec=None, pf=None, stream=None):
+    """Decode and prefill attention of one step in one launch.  ``dec``:
+    (out, q, block_tables, context_lens, max_context_len[, lse]) or None;
+    ``pf``: (out, q, query_start_loc, block_tables, context_lens, max_q_len,
+    max_context_len[, lse]) or None.  ``workspace``: mixed_workspace() for
+    the decode part's batch."""
+    dargs, pargs = _mixed_args(desc, dec, pf)
     _check(load().pa_mixed_attention(ctypes.byref(desc), *dargs, *pargs, _ptr(k_cache, _CACHE, "k_cache"),
                                      _ptr(v_cache, _CACHE, "v_cache"), float(scale),
                                      _ptr(workspace, (torch.uint8,), "workspace"), workspace.numel(),
                                      _stream(stream)))
+
+
+def pa_mixed_attention_append(desc: PaKvDesc, k_new, v_new, k_cache, v_cache, scale: float, workspace, dec=None,
+                              pf=None, stream=None):
+    """pa_mixed_attention with the step's cache write in the same launch.
+    ``k_new`` / ``v_new``: ``[T, Hkv, D]``, the decode sequences' new tokens
+    first, then the prefill chunks' tokens in query order; every chunk
+    starts at a block boundary."""
+    dargs, pargs = _mixed_args(desc, dec, pf)
+    _check(load().pa_mixed_attention_append(ctypes.byref(desc), *dargs, *pargs, _ptr(k_new, _act(desc), "k_new"),
+                                            _ptr(v_new, _act(desc), "v_new"), int(k_new.shape[0]),
+                                            _ptr(k_cache, _CACHE, "k_cache"), _ptr(v_cache, _CACHE, "v_cache"),
+                                            float(scale), _ptr(workspace, (torch.uint8,), "workspace"),
+                                            workspace.numel(), _stream(stream)))
 
 
 def pa_prefill_chunk(desc: PaKvDesc, out, q, query_start_loc, k_cache, v_cache, block_tables,

@@ -309,14 +309,18 @@ size_t pa_mixed_workspace_size(const pa_kv_desc *desc, int32_t num_dec_seqs, int
   return pa::mixed_plan(*desc, num_dec_seqs, plan).workspace_bytes;
 }
 
-pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
-                             const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
-                             const int32_t *dec_context_lens, int32_t num_dec_seqs, int32_t dec_max_context_len,
-                             float *pf_out, float *pf_lse, const void *pf_q, const int32_t *query_start_loc,
-                             const int32_t *pf_block_tables, int32_t pf_max_blocks_per_seq,
-                             const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
-                             int32_t pf_max_context_len, const void *k_cache, const void *v_cache, float scale,
-                             void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+namespace {
+
+// pa_mixed_attention and pa_mixed_attention_append: the same checks, and
+// the append's new rows (NULL: none)
+pa_status mixed_call(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
+                     const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq, const int32_t *dec_context_lens,
+                     int32_t num_dec_seqs, int32_t dec_max_context_len, float *pf_out, float *pf_lse, const void *pf_q,
+                     const int32_t *query_start_loc, const int32_t *pf_block_tables, int32_t pf_max_blocks_per_seq,
+                     const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
+                     int32_t pf_max_context_len, const void *k_cache, const void *v_cache, float scale,
+                     void *workspace, size_t workspace_bytes, pa_stream_t stream, bool append, const void *k_new,
+                     const void *v_new, int64_t num_new_rows) {
   // the decode part's checks (and its plan, whose workspace the call uses);
   // with no decode sequence only the descriptor and the plan of an empty batch
   pa::DecodePlan plan;
@@ -335,17 +339,60 @@ pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_
   const char *why = "";
   st = pa::check_mixed(*desc, plan, &why);
   if (st != PA_OK) return fail(st, "%s", why);
+  const bool has_pf = num_pf_seqs > 0 && max_q_len > 0;
+  if (append) {
+    if (num_dec_seqs > 0 || has_pf) {
+      if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))
+        return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be non-NULL and 16-byte aligned%s");
+      if (num_new_rows < num_dec_seqs + (has_pf ? 1 : 0))
+        return fail(PA_ERR_INVALID_ARG,
+                    "num_new_rows must count the decode rows and the prefill chunks' rows of k_new%s");
+    }
+    if (!has_pf) num_new_rows = num_dec_seqs;
+  }
   plan = pa::mixed_plan(*desc, num_dec_seqs, plan);
   if (!workspace || !aligned16(workspace))
     return fail(PA_ERR_WORKSPACE, "workspace must be non-NULL and 16-byte aligned%s");
   if (workspace_bytes < plan.workspace_bytes)
     return fail(PA_ERR_WORKSPACE, "workspace is smaller than pa_mixed_workspace_size()%s");
-  const cudaError_t e = pa::launch_mixed(*desc, plan, dec_out, dec_lse, dec_q, dec_block_tables,
-                                         dec_max_blocks_per_seq, dec_context_lens, num_dec_seqs, pf_out, pf_lse, pf_q,
-                                         query_start_loc, pf_block_tables, pf_max_blocks_per_seq, pf_context_lens,
-                                         num_pf_seqs, max_q_len, k_cache, v_cache, scale, workspace,
-                                         reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e = pa::launch_mixed(
+      *desc, plan, dec_out, dec_lse, dec_q, dec_block_tables, dec_max_blocks_per_seq, dec_context_lens, num_dec_seqs,
+      pf_out, pf_lse, pf_q, query_start_loc, pf_block_tables, pf_max_blocks_per_seq, pf_context_lens, num_pf_seqs,
+      max_q_len, k_cache, v_cache, scale, workspace, reinterpret_cast<cudaStream_t>(stream),
+      append ? k_new : nullptr, append ? v_new : nullptr, append ? num_new_rows : 0);
   return e == cudaSuccess ? ok() : cuda_fail(e);
+}
+
+}  // namespace
+
+pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
+                             const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
+                             const int32_t *dec_context_lens, int32_t num_dec_seqs, int32_t dec_max_context_len,
+                             float *pf_out, float *pf_lse, const void *pf_q, const int32_t *query_start_loc,
+                             const int32_t *pf_block_tables, int32_t pf_max_blocks_per_seq,
+                             const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
+                             int32_t pf_max_context_len, const void *k_cache, const void *v_cache, float scale,
+                             void *workspace, size_t workspace_bytes, pa_stream_t stream) {
+  return mixed_call(desc, dec_out, dec_lse, dec_q, dec_block_tables, dec_max_blocks_per_seq, dec_context_lens,
+                    num_dec_seqs, dec_max_context_len, pf_out, pf_lse, pf_q, query_start_loc, pf_block_tables,
+                    pf_max_blocks_per_seq, pf_context_lens, num_pf_seqs, max_q_len, pf_max_context_len, k_cache,
+                    v_cache, scale, workspace, workspace_bytes, stream, false, nullptr, nullptr, 0);
+}
+
+pa_status pa_mixed_attention_append(const pa_kv_desc *desc, float *dec_out, float *dec_lse, const void *dec_q,
+                                    const int32_t *dec_block_tables, int32_t dec_max_blocks_per_seq,
+                                    const int32_t *dec_context_lens, int32_t num_dec_seqs,
+                                    int32_t dec_max_context_len, float *pf_out, float *pf_lse, const void *pf_q,
+                                    const int32_t *query_start_loc, const int32_t *pf_block_tables,
+                                    int32_t pf_max_blocks_per_seq, const int32_t *pf_context_lens,
+                                    int32_t num_pf_seqs, int32_t max_q_len, int32_t pf_max_context_len,
+                                    const void *k_new, const void *v_new, int64_t num_new_rows, void *k_cache,
+                                    void *v_cache, float scale, void *workspace, size_t workspace_bytes,
+                                    pa_stream_t stream) {
+  return mixed_call(desc, dec_out, dec_lse, dec_q, dec_block_tables, dec_max_blocks_per_seq, dec_context_lens,
+                    num_dec_seqs, dec_max_context_len, pf_out, pf_lse, pf_q, query_start_loc, pf_block_tables,
+                    pf_max_blocks_per_seq, pf_context_lens, num_pf_seqs, max_q_len, pf_max_context_len, k_cache,
+                    v_cache, scale, workspace, workspace_bytes, stream, true, k_new, v_new, num_new_rows);
 }
 
 pa_status pa_prefix_attention(const pa_kv_desc *desc, float *out, float *lse, const void *q,

@@ -70,7 +70,8 @@ cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec
                          const void *pf_q, const int32_t *query_start_loc, const int32_t *pf_block_tables,
                          int32_t pf_max_blocks, const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
                          const void *k_cache, const void *v_cache, float scale, void *workspace,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const void *k_new = nullptr, const void *v_new = nullptr,
+                         int64_t num_new_rows = 0);
 
 // prefix_mode: every query of sequence s comes after all context_lens[s]
 // keys and sees them all (shared-prefix / cascade attention) instead of the

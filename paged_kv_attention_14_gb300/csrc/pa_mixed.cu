@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(pftc::NTHREADS, 1) mixed_kernel(const __grid_c
   constexpr int NCW = mixed_decode_warps<GQ>();
   constexpr int NS = dec::mma_stages<D, KVT, GQ, 1, NCW>();
   // launched as a programmatic dependent of the preceding kernel (the cache
-  // write): nothing is read before its writes are visible
+  // write, unless this launch writes the step's rows itself): nothing is
+  // read before its writes are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = pftc::align1024(smem_raw);
@@ -199,7 +200,7 @@ cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec
                          const void *pf_q, const int32_t *query_start_loc, const int32_t *pf_block_tables,
                          int32_t pf_max_blocks, const int32_t *pf_context_lens, int32_t num_pf_seqs, int32_t max_q_len,
                          const void *k_cache, const void *v_cache, float scale, void *workspace,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const void *k_new, const void *v_new, int64_t num_new_rows) {
   MixedArgs m;
   memset(&m, 0, sizeof m);
   const int g = d.num_q_heads / d.num_kv_heads;
@@ -208,11 +209,36 @@ cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec
                                dec_context_lens, num_dec_seqs, scale, workspace, &m.dec))
       return cudaErrorInvalidValue;
     m.n_dec = plan.num_ctas;
+    if (k_new != nullptr) {
+      // the decode sequences' new tokens are rows 0 .. num_dec_seqs - 1:
+      // each is written and used by the warp that owns its sequence's last
+      // block (see pa_decode_append)
+      m.dec.k_new = static_cast<const uint8_t *>(k_new);
+      m.dec.v_new = static_cast<const uint8_t *>(v_new);
+      m.dec.k_write = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+      m.dec.v_write = static_cast<uint8_t *>(const_cast<void *>(v_cache));
+      m.dec.k_enc = m.dec.v_enc = 1.f;
+    }
   }
   if (num_pf_seqs > 0 && max_q_len > 0) {
     if (!pftc::make_args<128>(&m.pf, d, pf_out, pf_lse, pf_q, query_start_loc, k_cache, v_cache, pf_block_tables,
                               pf_max_blocks, pf_context_lens, scale, false, 1, 0, 1))
       return cudaErrorInvalidValue;
+    if (k_new != nullptr) {
+      // the chunks' new tokens follow the decode rows, in query order
+      const int64_t row_bytes = static_cast<int64_t>(d.num_kv_heads) * d.head_dim * 2;
+      const uint8_t *kp = static_cast<const uint8_t *>(k_new) + num_dec_seqs * row_bytes;
+      const uint8_t *vp = static_cast<const uint8_t *>(v_new) + num_dec_seqs * row_bytes;
+      const int64_t pf_rows = num_new_rows - num_dec_seqs;
+      if (!pftc::make_new_rows_map<128>(&m.pf.knmap, kp, pf_rows, d) ||
+          !pftc::make_new_rows_map<128>(&m.pf.vnmap, vp, pf_rows, d))
+        return cudaErrorInvalidValue;
+      m.pf.new_rows = 1;
+      m.pf.k_new = kp;
+      m.pf.v_new = vp;
+      m.pf.k_write = static_cast<uint8_t *>(const_cast<void *>(k_cache));
+      m.pf.v_write = static_cast<uint8_t *>(const_cast<void *>(v_cache));
+    }
     m.pf_gx = (max_q_len + m.pf.qt - 1) / m.pf.qt;
     m.pf_gy = d.num_kv_heads;
     m.pf_gz = num_pf_seqs;

@@ -136,6 +136,20 @@ struct Args {
   float *part_lse;      // [2 G][MROWS]: its log-sum-exp, log2 units
   int *part_count;      // [num_seqs * gx * num_kv_heads] pieces finished per item
   int32_t *ws_err;      // the workspace's error word
+  // the step's cache write folded into the launch (pa_mixed_attention_append,
+  // 16-bit caches, chunk mode): the new K/V rows of the chunks, row
+  // query_start_loc[s] + i for query i of sequence s, as [rows][kv heads][D]
+  // (box {64, 1, 16}: 16 consecutive tokens of one kv head).  Keys at or past
+  // a chunk's first position come from these rows, not from the caches, and
+  // every tile writes its own queries' rows into the caches (k_write,
+  // v_write).  Each chunk starts at a block boundary (checked).
+  CUtensorMap knmap;
+  CUtensorMap vnmap;
+  int new_rows;         // 1: the above applies
+  const uint8_t *k_new;
+  const uint8_t *v_new;
+  uint8_t *k_write;
+  uint8_t *v_write;
 };
 
 // One call of prefill_tile: the item (sequence s, key split, kv head,
@@ -347,6 +361,13 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
   const int p_hi = ir.p_hi;
   const int base_pos = ir.base_pos;
   const int kv_end = ir.kv_end;
+  // the chunk's new rows are read from the step's new K/V (a fused cache
+  // write).  chunk0 is the position of the chunk's first query (base_pos is
+  // that of this tile's first query, qt0 queries later); it must start a
+  // block, or the block it falls in would hold new rows not yet in the cache
+  const bool new_src = !C::KV8 && a.new_rows && !a.prefix_mode;
+  const int chunk0 = base_pos - qt0;
+  if (new_src && (chunk0 & 15) != 0 && threadIdx.x == 0) report_error(a.err, a.ws_err, kErrBadIndex);
   if (a.prefix_mode && p_hi <= p_lo) {
     // no key in this split (an empty or short shared prefix): out = 0,
     // lse = -inf, before any barrier or tensor memory is set up
@@ -528,7 +549,13 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
         if (issuer && bi < nblk && bi >= bskip) {
           uint8_t *slot = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB;
           uint8_t *dst = C::KV8 ? slot + C::KVHALF + bi * 16 * D : slot + hh * C::KVHALF + bi * 16 * 128;
-          tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
+          const int lpos0 = key0 + bi * 16;  // the block's first position
+          if (!C::KV8 && new_src && lpos0 >= chunk0)
+            // a block of the chunk's own new tokens (query lpos0 - chunk0
+            // onwards): from the step's new rows
+            tma_load_3d(dst, part ? &a.vnmap : &a.knmap, hh * 64, kvh, qs + (lpos0 - chunk0), &bar[full], pol);
+          else
+            tma_load_2d(dst, part ? &a.vmap : &a.kmap, hh * 64, row, &bar[full], pol);
         }
         if (lane == 0) *(part ? s_last_v : s_last_k) = jj;
       }
@@ -789,6 +816,39 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
       first[t] = a.prefix_mode ? kv_lo : local_first_key(pos[t], a.window, a.chunk);  // ... and keys >= first
       m_ref[t] = -INFINITY;
       l[t] = 0.f;
+    }
+    if constexpr (!C::KV8) {
+      if (new_src) {
+        // the fused cache write: this tile's queries' new K and V rows (of
+        // its kv head) into the caches, before the first scores arrive.  In
+        // this launch nothing reads those cache rows: every tile takes the
+        // chunk's keys from the new rows.  Four tasks per query (K or V, half
+        // a row each), 16-byte vectors.
+        constexpr int NV = D / 16;  // vectors per half row
+        const int st0 = tid - kSoftmaxWarp0 * 32;
+        for (int task = st0; task < nq * 4; task += 256) {
+          const int qi = task >> 2, isv = (task >> 1) & 1, half = task & 1;
+          const int pos = base_pos + qi;  // query qt0 + qi of the chunk
+          int phys = __ldg(table + (pos >> 4));
+          if (a.checked && (phys < 0 || phys >= a.num_blocks)) {
+            report_error(a.err, a.ws_err, kErrBadIndex);  // nothing written outside the cache
+            continue;
+          }
+          const uint4 *src = reinterpret_cast<const uint4 *>(
+                                 (isv ? a.v_new : a.k_new) +
+                                 (static_cast<int64_t>(qs + qt0 + qi) * a.num_kv_heads + kvh) * (D * 2)) +
+                             half * NV;
+          uint4 *dst = reinterpret_cast<uint4 *>(
+                           (isv ? a.v_write : a.k_write) +
+                           ((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * 16 + (pos & 15)) * (D * 2)) +
+                       half * NV;
+          uint4 v[NV];
+#pragma unroll
+          for (int i = 0; i < NV; ++i) v[i] = __ldg(src + i);
+#pragma unroll
+          for (int i = 0; i < NV; ++i) dst[i] = v[i];
+        }
+      }
     }
     bool ok = true;
     PF_TRACE(const long long ts0 = clock64(); long long tq[7] = {0, 0, 0, 0, 0, 0, 0}; long long tc, tk;)
@@ -1102,6 +1162,45 @@ inline bool make_map(CUtensorMap *map, const void *base, const pa_kv_desc &d) {
   const cuuint32_t box[2] = {kv8 ? static_cast<cuuint32_t>(D) : 64u, 16};
   const cuuint32_t estr[2] = {1, 1};
   if (enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  cache.put(key, *map);
+  return true;
+}
+
+// A step's new K or V rows as a tensor map: [rows][kv heads][D] of the
+// cache's 16-bit type, box {64 columns, 1 kv head, 16 rows}: 16 consecutive
+// tokens of one kv head land as one 16-row block tile, the layout of a
+// cache block's box.  The row extent is the caller's row count, so a box
+// that runs past the last row reads zeros.
+template <int D>
+inline bool make_new_rows_map(CUtensorMap *map, const void *base, int64_t rows, const pa_kv_desc &d) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || rows <= 0) return false;
+  const CUtensorMapDataType dt =
+      d.kv_dtype == PA_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                     const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                     CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                     CUtensorMapFloatOOBfill);
+  static EncodeTiledFn enc = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  if (!enc) return false;
+  thread_local MapCache<> cache;
+  const MapKey key = map_key(base, rows, d.num_kv_heads, D, d.kv_dtype, -3);
+  if (cache.find(key, map)) return true;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(d.num_kv_heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(d.num_kv_heads) * D * 2};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;

@@ -52,14 +52,19 @@ class MixedStep:
     sequence order (k_new[s] at position context_lens[s] - 1), runs as one
     pa_decode_append launch instead of pa_cache_write and pa_decode; where
     the library does not take it (the CUDA-core decode kernel)
-    the step falls back to the two calls."""
+    the step falls back to the two calls.  With ``write_in_step`` the fused
+    mode runs a step with both parts, cache write included, as one
+    pa_mixed_attention_append launch: the caller's new rows are then the
+    decode sequences' tokens in sequence order followed by the prefill
+    chunks' tokens in query order, and every chunk starts at a block
+    boundary."""
 
     MODES = ("fused", "streams", "serial")
 
     def __init__(self, desc: B.PaKvDesc, k_cache, v_cache, scale: float, *, decode_out=None, decode_lse=None,
                  workspace=None, max_context_len_decode: int = 0, prefill_out=None, prefill_lse=None,
                  max_q_len: int = 0, max_context_len_prefill: int = 0, mode: str = "fused",
-                 prefill_workspace=None, decode_append: bool = False):
+                 prefill_workspace=None, decode_append: bool = False, write_in_step: bool = False):
         if mode not in self.MODES:
             raise ValueError(f"mode must be one of {self.MODES}")
         self.desc = desc
@@ -71,6 +76,7 @@ class MixedStep:
         self.max_q_len, self.max_context_len_prefill = int(max_q_len), int(max_context_len_prefill)
         self.prefill_workspace = prefill_workspace
         self.decode_append = bool(decode_append) and decode_out is not None and prefill_out is None
+        self.write_in_step = bool(write_in_step)
         self._balanced = {}  # (prefill sequences, table width) -> the balanced prefill runs
         both = decode_out is not None and prefill_out is not None
         fused_ok = (desc.kv_dtype in (B.PA_KV_BF16, B.PA_KV_F16) and desc.head_dim == 128
@@ -121,6 +127,16 @@ class MixedStep:
                                                                 self.max_context_len_prefill, key[1]))
         return self._balanced[key]
 
+    def _mixed_parts(self, dec_args, pf_args):
+        """The dec and pf arguments of the mixed entry points."""
+        dec = None
+        if dec_args is not None and self.decode_out is not None:
+            dec = (self.decode_out, *dec_args, self.max_context_len_decode, self.decode_lse)
+        pf = None
+        if pf_args is not None and self.prefill_out is not None:
+            pf = (self.prefill_out, *pf_args, self.max_q_len, self.max_context_len_prefill, self.prefill_lse)
+        return dec, pf
+
     def attend(self, dec_args, pf_args):
         """Decode and prefill after a cache write already issued on the current stream."""
         if self.mode == "fused" and self.prefill_balanced(pf_args):
@@ -130,13 +146,8 @@ class MixedStep:
             self.prefill(*pf_args)
             return
         if self.mode == "fused":
-            dec = None
-            if dec_args is not None and self.decode_out is not None:
-                dec = (self.decode_out, *dec_args, self.max_context_len_decode, self.decode_lse)
-            pf = None
-            if pf_args is not None and self.prefill_out is not None:
-                pf = (self.prefill_out, *pf_args, self.max_q_len, self.max_context_len_prefill, self.prefill_lse)
-            B.pa_mixed_attention(self.desc, self.k_cache, self.v_cache, self.scale, self.workspace, dec=dec, pf=pf)
+            B.pa_mixed_attention(self.desc, self.k_cache, self.v_cache, self.scale, self.workspace,
+                                 *self._mixed_parts(dec_args, pf_args))
             return
         if self.overlap:
             main = torch.cuda.current_stream()
@@ -168,6 +179,12 @@ class MixedStep:
                 if e.status != B.PA_ERR_UNSUPPORTED:
                     raise
                 self.decode_append = False  # checked before anything was enqueued: the two calls below
+        if (self.write_in_step and self.mode == "fused" and k_new is not None and dec_args is not None
+                and pf_args is not None and not self.prefill_balanced(pf_args)):
+            # the whole step in one launch, the cache write included
+            B.pa_mixed_attention_append(self.desc, k_new, v_new, self.k_cache, self.v_cache, self.scale,
+                                        self.workspace, *self._mixed_parts(dec_args, pf_args))
+            return
         if slot_mapping is not None and slot_mapping.numel() > 0:
             B.pa_cache_write(self.desc, k_new, v_new, self.k_cache, self.v_cache, slot_mapping)
         self.attend(dec_args, pf_args)

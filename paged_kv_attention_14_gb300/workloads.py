@@ -316,7 +316,7 @@ def mixed_batch(seed, device="cpu", poison: bool = False, kv_dtype=KV_BF16, name
     dec_lens = torch.randint(dec_range[0], dec_range[1] + 1, (n_dec,), generator=g_cpu).to(torch.int32)
     pf_len = prefix + chunk
     shared_blocks = shared // B
-    own_blocks = (pf_len - shared) // B
+    own_blocks = (pf_len - shared + B - 1) // B  # the last one partly filled unless pf_len is a block multiple
     dec_nblk = [(int(L) + B - 1) // B for L in dec_lens]
     needed = sum(dec_nblk) + shared_blocks + n_pf * own_blocks
     NB = _pool_size(needed)
@@ -324,7 +324,7 @@ def mixed_batch(seed, device="cpu", poison: bool = False, kv_dtype=KV_BF16, name
     dec_tables, used = _tables(dec_lens, perm, B)
     shared_ids = perm[used:used + shared_blocks].to(torch.int32)
     used += shared_blocks
-    pf_tables = torch.full((n_pf, pf_len // B), -1, dtype=torch.int32)
+    pf_tables = torch.full((n_pf, shared_blocks + own_blocks), -1, dtype=torch.int32)
     for s in range(n_pf):
         pf_tables[s, :shared_blocks] = shared_ids
         pf_tables[s, shared_blocks:] = perm[used:used + own_blocks].to(torch.int32)
