@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(pftc::NTHREADS, 1) mixed_kernel(const __grid_c
       // (kv head, sequence) first
       const int yz = m.pf_gy * m.pf_gz;
       const int x = item / yz, y = (item % yz) % m.pf_gy, z = (item % yz) / m.pf_gy;
-      pftc::prefill_tile<D, KVT, pftc::kPvF16>(m.pf, smem, tmem, x, y, z, m.pf_gx);
+      pftc::prefill_tile<D, KVT, pftc::kPvF16, true>(m.pf, smem, tmem, x, y, z, m.pf_gx);
     } else {
       dec::decode_partition<D, KVT, GQ, 1, NS, NCW>(m.dec, smem_raw, item - m.n_pf, m.n_dec);
     }

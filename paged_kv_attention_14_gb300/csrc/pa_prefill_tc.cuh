@@ -328,8 +328,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 // by all NTHREADS threads of a CTA with tensor memory already allocated
 // (tmem: all TMEM_COLS columns); every thread takes the same early returns.
 // On return every copy and product of the tile has completed, so that its
-// barriers can be set up again for the next tile.
-template <int D, int KVT, int PVM>
+// barriers can be set up again for the next tile.  NR: compiled with the
+// fused cache write of a step (Args::new_rows), which only the single-launch
+// step uses; the other kernels are built without it.
+template <int D, int KVT, int PVM, bool NR = false>
 __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const Seg &sg) {
   using C = Cfg<D, KVT, PVM>;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -365,7 +367,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
   // write).  chunk0 is the position of the chunk's first query (base_pos is
   // that of this tile's first query, qt0 queries later); it must start a
   // block, or the block it falls in would hold new rows not yet in the cache
-  const bool new_src = !C::KV8 && a.new_rows && !a.prefix_mode;
+  const bool new_src = NR && !C::KV8 && a.new_rows && !a.prefix_mode;
   const int chunk0 = base_pos - qt0;
   if (new_src && (chunk0 & 15) != 0 && threadIdx.x == 0) report_error(a.err, a.ws_err, kErrBadIndex);
   if (a.prefix_mode && p_hi <= p_lo) {
@@ -550,7 +552,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
           uint8_t *slot = smem + (part ? C::OFF_V : C::OFF_K) + st * C::KVB;
           uint8_t *dst = C::KV8 ? slot + C::KVHALF + bi * 16 * D : slot + hh * C::KVHALF + bi * 16 * 128;
           const int lpos0 = key0 + bi * 16;  // the block's first position
-          if (!C::KV8 && new_src && lpos0 >= chunk0)
+          if (NR && !C::KV8 && new_src && lpos0 >= chunk0)
             // a block of the chunk's own new tokens (query lpos0 - chunk0
             // onwards): from the step's new rows
             tma_load_3d(dst, part ? &a.vnmap : &a.knmap, hh * 64, kvh, qs + (lpos0 - chunk0), &bar[full], pol);
@@ -817,7 +819,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
       m_ref[t] = -INFINITY;
       l[t] = 0.f;
     }
-    if constexpr (!C::KV8) {
+    if constexpr (NR && !C::KV8) {
       if (new_src) {
         // the fused cache write: this tile's queries' new K and V rows (of
         // its kv head) into the caches, before the first scores arrive.  In
@@ -1088,7 +1090,7 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
 // One tile of a grid: query tile bx of gx (counted from the last, so that
 // the longest key ranges come first), kv head by, sequence (or sequence x
 // key split in prefix mode) bz; all of its KV iterations.
-template <int D, int KVT, int PVM>
+template <int D, int KVT, int PVM, bool NR = false>
 __device__ __forceinline__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, int bx, int by, int bz,
                                              int gx) {
   Seg sg;
@@ -1104,7 +1106,7 @@ __device__ __forceinline__ void prefill_tile(const Args &a, uint8_t *smem, uint3
   sg.G = 1;
   sg.item_start = 0;
   sg.U = 1;
-  prefill_tile<D, KVT, PVM>(a, smem, tmem, sg);
+  prefill_tile<D, KVT, PVM, NR>(a, smem, tmem, sg);
 }
 
 template <int D, int KVT, int PVM>
