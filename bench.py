@@ -285,7 +285,8 @@ def _local_config(args) -> dict:
     if args.per_head_scales:
         d["fp8_scales"] = "per kv head"
     if args.workload == 5:
-        d["mixed_step"] = {"fused": "cache write, then decode and prefill in one persistent launch",
+        d["mixed_step"] = {"fused": ("cache write, then decode and prefill in one persistent launch" if args.separate_write
+                                     else "cache write, decode and prefill in one persistent launch"),
                            "streams": "cache write, then the decode on a second stream beside the prefill",
                            "serial": "cache write, decode, prefill in order on one stream"}[args.mixed_mode]
     if args.prefill_impl:
@@ -401,9 +402,10 @@ def run_ours(args):
         # the timed kernels start instead of during them
         flush = _L2Flush(2 * l2_bytes, dev)
 
-    # mixed step: after the cache write, decode and prefill in one persistent
-    # launch (--mixed-mode fused), the decode on a second stream beside the
-    # prefill (streams) or one after the other (serial)
+    # mixed step: decode and prefill in one persistent launch, the cache
+    # write inside it (--mixed-mode fused), the decode on a second stream
+    # beside the prefill (streams) or one after the other (serial), these
+    # two after a cache write of their own
     pf_ws = None
     if mixed and args.prefill_entry == "balanced":
         pf_ws = B.prefill_workspace(desc, int(b.context_lens_prefill.shape[0]), pf_maxq, dev)

@@ -384,7 +384,8 @@ PA_API pa_status pa_prefill_chunk_balanced(const pa_kv_desc *desc, float *out, f
  * in one persistent launch whose CTAs take the prefill's tiles (longest key
  * ranges first) and then the decode's partitions from one work list: the
  * decode fills the SMs the prefill's last wave leaves idle.  Issue the
- * step's pa_cache_write first, on the same stream.
+ * step's pa_cache_write first, on the same stream (or use
+ * pa_mixed_attention_append, which writes the rows in the same launch).
  *   workspace : pa_mixed_workspace_size(desc, num_dec_seqs,
  *               dec_max_context_len) bytes, zero-filled before its first use;
  *               every call that completes without error leaves it ready for

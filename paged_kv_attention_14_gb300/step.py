@@ -39,7 +39,8 @@ from . import binding as B
 
 
 class MixedStep:
-    """Issues one step: cache write, then decode and prefill.
+    """Issues one step: the cache write, decode and prefill (as one launch
+    where the library takes it, else as a cache write and the attention).
 
     Buffers that persist across steps (the caches, the decode workspace and
     the outputs) are given once; the per-step inputs are passed to
