@@ -427,7 +427,8 @@ PA_API pa_status pa_mixed_attention(const pa_kv_desc *desc, float *dec_out, floa
  *                  (position pf_context_lens[s] - q_len_s + i).
  *   num_new_rows : rows of k_new / v_new (num_dec_seqs +
  *                  query_start_loc[num_pf_seqs]), host value.  With a
- *                  prefill part it must exceed num_dec_seqs.
+ *                  prefill part it must exceed num_dec_seqs; a chunk row
+ *                  past it is neither read nor written (PA_DEVERR_BAD_INDEX).
  * Every prefill chunk must start at a multiple of block_size
  * (pf_context_lens[s] - q_len_s), so that a block holds either cached or new
  * tokens.  A chunk that does not is reported on the device

@@ -234,6 +234,7 @@ cudaError_t launch_mixed(const pa_kv_desc &d, const DecodePlan &plan, float *dec
           !pftc::make_new_rows_map<128>(&m.pf.vnmap, vp, pf_rows, d))
         return cudaErrorInvalidValue;
       m.pf.new_rows = 1;
+      m.pf.new_row_count = pf_rows;
       m.pf.k_new = kp;
       m.pf.v_new = vp;
       m.pf.k_write = static_cast<uint8_t *>(const_cast<void *>(k_cache));

@@ -146,6 +146,7 @@ struct Args {
   CUtensorMap knmap;
   CUtensorMap vnmap;
   int new_rows;         // 1: the above applies
+  int64_t new_row_count;  // rows of k_new / v_new (of the prefill part)
   const uint8_t *k_new;
   const uint8_t *v_new;
   uint8_t *k_write;
@@ -832,8 +833,9 @@ __device__ void prefill_tile(const Args &a, uint8_t *smem, uint32_t tmem, const 
           const int qi = task >> 2, isv = (task >> 1) & 1, half = task & 1;
           const int pos = base_pos + qi;  // query qt0 + qi of the chunk
           int phys = __ldg(table + (pos >> 4));
-          if (a.checked && (phys < 0 || phys >= a.num_blocks)) {
-            report_error(a.err, a.ws_err, kErrBadIndex);  // nothing written outside the cache
+          if ((a.checked && (phys < 0 || phys >= a.num_blocks)) || qs + qt0 + qi >= a.new_row_count) {
+            // nothing written outside the cache, nothing read past the new rows
+            report_error(a.err, a.ws_err, kErrBadIndex);
             continue;
           }
           const uint4 *src = reinterpret_cast<const uint4 *>(

@@ -188,3 +188,25 @@ def test_mixed_step_writes_in_the_launch():
     for x, y in zip(res[0][:4], res[1][:4]):
         assert torch.equal(x, y)
     assert _same_bits(res[0][4], res[1][4]) and _same_bits(res[0][5], res[1][5])
+
+
+def test_rows_past_the_declared_count_are_reported():
+    """num_new_rows short of the chunks' rows: the rows past it are neither
+    read nor written, and the step reports PA_DEVERR_BAD_INDEX."""
+    b = W.mixed_batch(1370, device=DEV, poison=False, n_dec=2, dec_range=(10, 100), n_pf=2, prefix=32, chunk=40,
+                      shared=16)
+    ew = torch.zeros(1, dtype=torch.int32, device=DEV)
+    d = B.make_desc(b.num_blocks, b.num_kv_heads, b.num_q_heads, b.head_dim, error_word=ew)
+    dec, pf, S, maxLd = _parts(b)
+    short = 2 + 40 + 8  # the decode rows, the first chunk and 8 rows of the second
+    k_new, v_new = b.k_new[:short].contiguous(), b.v_new[:short].contiguous()
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_mixed_attention_append(d, k_new, v_new, kc, vc, b.scale, B.mixed_workspace(d, S, maxLd, DEV),
+                                dec=dec, pf=pf)
+    torch.cuda.synchronize()
+    assert int(ew[0]) & B.PA_DEVERR_BAD_INDEX
+    # the rows up to the count went where the slots say; the others are untouched
+    kc2, vc2 = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(d, k_new, v_new, kc2, vc2, b.slot_mapping[:short].contiguous())
+    torch.cuda.synchronize()
+    assert _same_bits(kc, kc2) and _same_bits(vc, vc2)
