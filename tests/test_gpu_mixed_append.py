@@ -210,3 +210,31 @@ def test_rows_past_the_declared_count_are_reported():
     B.pa_cache_write(d, k_new, v_new, kc2, vc2, b.slot_mapping[:short].contiguous())
     torch.cuda.synchronize()
     assert _same_bits(kc, kc2) and _same_bits(vc, vc2)
+
+
+@pytest.mark.parametrize("window,chunk", [(96, 0), (0, 64)])
+def test_fused_step_with_local_attention(window, chunk):
+    """Sliding-window and chunked-local attention: pages below every window
+    are skipped, the chunk's own keys still come from the new rows."""
+    b = W.mixed_batch(1380 + window + chunk, device=DEV, poison=True, n_dec=3, dec_range=(50, 600), n_pf=2,
+                      prefix=256, chunk=200, shared=128)
+    d = desc_of(b, window=window, chunk=chunk)
+    dec, pf, S, maxLd = _parts(b)
+    kc, vc = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_mixed_attention_append(d, b.k_new, b.v_new, kc, vc, b.scale, B.mixed_workspace(d, S, maxLd, DEV),
+                                dec=dec, pf=pf)
+    dec2, pf2, _, _ = _parts(b)
+    kc2, vc2 = b.k_pool.clone(), b.v_pool.clone()
+    B.pa_cache_write(d, b.k_new, b.v_new, kc2, vc2, b.slot_mapping)
+    B.pa_mixed_attention(d, kc2, vc2, b.scale, B.mixed_workspace(d, S, maxLd, DEV), dec=dec2, pf=pf2)
+    torch.cuda.synchronize()
+    assert _same_bits(kc, kc2) and _same_bits(vc, vc2)
+    for x, y in ((dec[0], dec2[0]), (dec[5], dec2[5]), (pf[0], pf2[0]), (pf[7], pf2[7])):
+        assert torch.equal(x, y)
+    ok, ov = oracle.cache_write(oracle.KV_BF16, 16, b.num_kv_heads, b.head_dim, b.k_new.cpu(), b.v_new.cpu(),
+                                b.slot_mapping.cpu(), b.k_pool.cpu(), b.v_pool.cpu())
+    o_ref, l_ref = H.oracle_decode(b, ocaches=(oracle.KV_BF16, ok, ov), window=window, chunk=chunk)
+    assert_close(dec[0], o_ref, TOL[b.kv_dtype], "decode out")
+    p_ref, pl_ref = H.oracle_prefill(b, ocaches=(oracle.KV_BF16, ok, ov), window=window, chunk=chunk)
+    assert_close(pf[0], p_ref, TOL[b.kv_dtype], "prefill out")
+    assert_close(pf[7], pl_ref, LSE_TOL[b.kv_dtype], "prefill lse")
